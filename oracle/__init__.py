@@ -1,0 +1,311 @@
+"""The oracle: a plain, slow CPU statement of FPS, kNN and Ball Query.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The product
+path (``point_cloud_neighbor_gb300``) never imports, loads or calls it, and it
+imports nothing from the product path.
+
+The arithmetic lives in ``pc_oracle.c`` (float32, one rounding per operation,
+compiled with ``-ffp-contract=off``), which follows the mps-pointops 0.5.0
+project page, "The operators in equations", and the "Numerical contracts"
+page, "Selection and output".  This module only builds that file with gcc,
+loads it with ctypes and marshals numpy arrays.  Rows of independent queries
+(and clouds for FPS) can be spread over host threads: ctypes releases the GIL
+during each call, and every row is computed by the same plain C loop.
+
+Pins (what ties this oracle to something other than itself) are in
+``tests/test_oracle_pins.py``; the readings of the pages it takes are listed
+in the repository's design notes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pc_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libpc_oracle.so")
+
+# -ffp-contract=off: no a*b+c -> fma contraction (GCC on aarch64 contracts by
+# default).  No -ffast-math, no -ffinite-math-only: IEEE semantics, subnormals
+# kept.  -fno-builtin-sqrtf is not needed: sqrtf is correctly rounded anyway.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+          "-fPIC", "-shared"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pc_oracle.c`` into ``oracle/_build/libpc_oracle.so``."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(lib):
+    P = ctypes.c_void_p
+    I = ctypes.c_int64
+    lib.orc_s32.restype = ctypes.c_float
+    lib.orc_s32.argtypes = [P, P]
+    lib.orc_radius_threshold.restype = ctypes.c_float
+    lib.orc_radius_threshold.argtypes = [ctypes.c_double]
+    lib.orc_fps.restype = ctypes.c_int
+    lib.orc_fps.argtypes = [P, I, I, I, I, P]
+    lib.orc_min_dist_to_set.restype = ctypes.c_int
+    lib.orc_min_dist_to_set.argtypes = [P, I, P, I, P, I, P]
+    lib.orc_knn_rows.restype = ctypes.c_int
+    lib.orc_knn_rows.argtypes = [P, I, I, P, I, I, P, I, P, P]
+    lib.orc_ball_query_rows.restype = ctypes.c_int
+    lib.orc_ball_query_rows.argtypes = [P, I, I, P, I, ctypes.c_double,
+                                        I, P, I, P, P]
+    lib.orc_ball_query_scan_len.restype = ctypes.c_int
+    lib.orc_ball_query_scan_len.argtypes = [P, I, I, P, I,
+                                            ctypes.c_double, I, P, I, P]
+    lib.orc_s32_pairs.restype = None
+    lib.orc_s32_pairs.argtypes = [P, P, I, P]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+        return _lib
+
+
+def compile_variant(source_text: str, out_path: str) -> str:
+    """Compile a modified copy of the oracle source (used by the tests that
+    plant a mistake in the oracle to show that the pins catch it)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(source_text)
+    subprocess.run(["gcc", *CFLAGS, src, "-o", out_path, "-lm"], check=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+class use_library:
+    """Context manager: route this module's calls to another build of the
+    oracle source (a planted-mistake variant) for the duration."""
+
+    def __init__(self, path: str):
+        self.path = path
+        self.saved = None
+
+    def __enter__(self):
+        global _lib
+        _load()
+        with _lock:
+            self.saved = _lib
+            _lib = _bind(ctypes.CDLL(self.path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        with _lock:
+            _lib = self.saved
+        return False
+
+
+def _f32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (code {rc})")
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def _split(n: int, parts: int):
+    parts = max(1, min(parts, n))
+    step = -(-n // parts)
+    return [(i, min(n, i + step)) for i in range(0, n, step)]
+
+
+def s32(a, b) -> np.ndarray:
+    """Squared distances s32(a_i, b_i) of matching rows of two [n,3] arrays."""
+    a = _f32(a).reshape(-1, 3)
+    b = _f32(b).reshape(-1, 3)
+    assert a.shape == b.shape
+    out = np.empty(a.shape[0], dtype=np.float32)
+    _load().orc_s32_pairs(_ptr(a), _ptr(b), a.shape[0], _ptr(out))
+    return out
+
+
+def radius_threshold(radius: float) -> np.float32:
+    """R2 = fl32(fl32(r) * fl32(r))."""
+    return np.float32(_load().orc_radius_threshold(float(radius)))
+
+
+def fps(xyz, npoint: int, start_idx: int = 0, threads: int = 1) -> np.ndarray:
+    """Farthest point sampling of every cloud of ``xyz`` [B,N,3] -> [B,npoint]."""
+    xyz = _f32(xyz)
+    B, N, _ = xyz.shape
+    out = np.empty((B, npoint), dtype=np.int64)
+    lib = _load()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        sub = np.ascontiguousarray(xyz[lo:hi])
+        o = np.empty((hi - lo, npoint), dtype=np.int64)
+        _check(lib.orc_fps(_ptr(sub), hi - lo, N, npoint, start_idx, _ptr(o)),
+               "fps")
+        out[lo:hi] = o
+
+    chunks = _split(B, threads)
+    if len(chunks) <= 1:
+        run(0, B)
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            list(ex.map(lambda c: run(*c), chunks))
+    return out
+
+
+def min_dist_to_set(x, centers, points) -> np.ndarray:
+    """m_j = min_u s32(x_j, x_{centers[u]}) for each j in ``points`` (one cloud)."""
+    x = _f32(x).reshape(-1, 3)
+    centers = np.ascontiguousarray(centers, dtype=np.int64)
+    points = np.ascontiguousarray(points, dtype=np.int64)
+    out = np.empty(points.shape[0], dtype=np.float32)
+    _check(_load().orc_min_dist_to_set(_ptr(x), x.shape[0], _ptr(centers),
+                                       centers.shape[0], _ptr(points),
+                                       points.shape[0], _ptr(out)),
+           "min_dist_to_set")
+    return out
+
+
+def _rows_arg(rows, total):
+    if rows is None:
+        return np.arange(total, dtype=np.int64)
+    return np.ascontiguousarray(rows, dtype=np.int64)
+
+
+def knn(query, ref, k: int, rows=None, threads: int = 1):
+    """kNN of query [B,Q,3] against ref [B,N,3].
+
+    Returns (dist [R,k] float32, idx [R,k] int64) for the flat rows ``rows``
+    (row = b*Q + i; all B*Q rows when ``rows`` is None).
+    """
+    query = _f32(query)
+    ref = _f32(ref)
+    B, Q, _ = query.shape
+    N = ref.shape[1]
+    rows = _rows_arg(rows, B * Q)
+    R = rows.shape[0]
+    dist = np.empty((R, k), dtype=np.float32)
+    idx = np.empty((R, k), dtype=np.int64)
+    lib = _load()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        rr = np.ascontiguousarray(rows[lo:hi])
+        d = np.empty((hi - lo, k), dtype=np.float32)
+        i = np.empty((hi - lo, k), dtype=np.int64)
+        _check(lib.orc_knn_rows(_ptr(query), B, Q, _ptr(ref), N, k, _ptr(rr),
+                                hi - lo, _ptr(d), _ptr(i)), "knn")
+        dist[lo:hi] = d
+        idx[lo:hi] = i
+
+    chunks = _split(R, threads)
+    if len(chunks) <= 1:
+        run(0, R)
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            list(ex.map(lambda c: run(*c), chunks))
+    return dist, idx
+
+
+def ball_query(query, ref, radius: float, K: int, rows=None, threads: int = 1):
+    """First-K Ball Query of query [B,Q,3] against ref [B,N,3].
+
+    Returns (dist2 [R,K] float32, idx [R,K] int64) for the flat rows ``rows``.
+    """
+    query = _f32(query)
+    ref = _f32(ref)
+    B, Q, _ = query.shape
+    N = ref.shape[1]
+    rows = _rows_arg(rows, B * Q)
+    R = rows.shape[0]
+    dist2 = np.empty((R, K), dtype=np.float32)
+    idx = np.empty((R, K), dtype=np.int64)
+    lib = _load()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        rr = np.ascontiguousarray(rows[lo:hi])
+        d = np.empty((hi - lo, K), dtype=np.float32)
+        i = np.empty((hi - lo, K), dtype=np.int64)
+        _check(lib.orc_ball_query_rows(_ptr(query), B, Q, _ptr(ref), N,
+                                       float(radius), K, _ptr(rr), hi - lo,
+                                       _ptr(d), _ptr(i)), "ball_query")
+        dist2[lo:hi] = d
+        idx[lo:hi] = i
+
+    chunks = _split(R, threads)
+    if len(chunks) <= 1:
+        run(0, R)
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            list(ex.map(lambda c: run(*c), chunks))
+    return dist2, idx
+
+
+def ball_query_scan_len(query, ref, radius: float, K: int, rows=None,
+                        threads: int = 1) -> np.ndarray:
+    """Pairs the first-K rule must examine per row (position of K-th hit + 1, or N)."""
+    query = _f32(query)
+    ref = _f32(ref)
+    B, Q, _ = query.shape
+    N = ref.shape[1]
+    rows = _rows_arg(rows, B * Q)
+    R = rows.shape[0]
+    out = np.empty(R, dtype=np.int64)
+    lib = _load()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        rr = np.ascontiguousarray(rows[lo:hi])
+        o = np.empty(hi - lo, dtype=np.int64)
+        _check(lib.orc_ball_query_scan_len(_ptr(query), B, Q, _ptr(ref), N,
+                                           float(radius), K, _ptr(rr),
+                                           hi - lo, _ptr(o)), "scan_len")
+        out[lo:hi] = o
+
+    chunks = _split(R, threads)
+    if len(chunks) <= 1:
+        run(0, R)
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            list(ex.map(lambda c: run(*c), chunks))
+    return out

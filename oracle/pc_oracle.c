@@ -1,0 +1,271 @@
+/*
+ * pc_oracle.c -- the ORACLE for dense point-cloud neighbor search.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header, table or constant with the
+ * CUDA library.
+ *
+ * It is the plain, slow, obviously correct CPU statement of the operator
+ * definitions on the mps-pointops 0.5.0 project page, section "The operators
+ * in equations", and of the mps-pointops "Numerical contracts" page, section
+ * "Selection and output".  Every function below names the passage it follows.
+ *
+ * Arithmetic: IEEE-754 binary32, round to nearest even, each operation rounded
+ * separately.  The file must be compiled with -ffp-contract=off and without
+ * -ffast-math (aarch64 GCC contracts a*b+c into an FMA by default, which would
+ * change the rounding that the selection rules depend on).  Subnormals are
+ * kept.  The squared distance is summed in the order ((dx*dx + dy*dy) + dz*dz),
+ * the order the project page's "How the kernels work" section gives for FPS
+ * and kNN; the "Numerical contracts" page fixes the Ball Query threshold as
+ * fl32(fl32(r) * fl32(r)) with a strict "<".
+ *
+ * Inputs are finite float32 coordinates, row-major [B, N, 3]; indices int64.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+#if defined(__FAST_MATH__)
+#error "the oracle must not be built with fast-math"
+#endif
+
+/* Status codes of the oracle's own entry points. */
+#define ORC_OK 0
+#define ORC_BAD_ARGUMENT 1
+#define ORC_NO_MEMORY 2
+
+/*
+ * Squared distance s = sum_{d=0..2} (a_d - b_d)^2.
+ * Project page, "The operators in equations" (the shared squared distance);
+ * summation order ((dx^2 + dy^2) + dz^2) from "How the kernels work".
+ * Each statement below is one float32 operation.
+ */
+float orc_s32(const float *a, const float *b)
+{
+    float dx = a[0] - b[0];
+    float dy = a[1] - b[1];
+    float dz = a[2] - b[2];
+    float xx = dx * dx;
+    float yy = dy * dy;
+    float zz = dz * dz;
+    float sxy = xx + yy;
+    return sxy + zz;
+}
+
+/*
+ * Ball Query threshold R2 = fl32(fl32(r) * fl32(r)).
+ * Project page, "Ball Query: first K within a radius"; "Numerical contracts",
+ * "Selection and output" (r32 = fl32(r); R2_dense = fl32(r32 * r32)).
+ */
+float orc_radius_threshold(double radius)
+{
+    float r32 = (float)radius;
+    float r2 = r32 * r32;
+    return r2;
+}
+
+/*
+ * Farthest point sampling, one call for all B clouds.
+ * Project page, "Farthest point sampling":
+ *   c_0 = start_idx,
+ *   m_j(t) = min_{0<=u<=t} s(x_j, x_{c_u}),
+ *   c_{t+1} = the smallest j with m_j(t) = max_l m_l(t).
+ * The running minimum is the literal min over the selected centers, started
+ * from the first center (no sentinel).  The scan for the maximum keeps the
+ * first j that reaches it, which is the smallest index on an exact tie.  Once
+ * every m_j is 0 the rule itself yields j = 0, so the slots after exhaustion
+ * repeat index 0 (project page, "Contracts": furthest_point_sample).
+ */
+int orc_fps(const float *xyz, int64_t B, int64_t N, int64_t npoint,
+            int64_t start_idx, int64_t *out_idx)
+{
+    if (B < 0 || N < 1 || npoint < 1 || start_idx < 0 || start_idx >= N)
+        return ORC_BAD_ARGUMENT;
+    float *m = (float *)malloc((size_t)N * sizeof(float));
+    if (!m) return ORC_NO_MEMORY;
+    for (int64_t b = 0; b < B; ++b) {
+        const float *x = xyz + (size_t)b * (size_t)N * 3;
+        int64_t *sel = out_idx + (size_t)b * (size_t)npoint;
+        int64_t c = start_idx;
+        sel[0] = c;
+        for (int64_t j = 0; j < N; ++j)
+            m[j] = orc_s32(x + 3 * j, x + 3 * c);
+        for (int64_t t = 1; t < npoint; ++t) {
+            /* c_t = smallest j attaining max_l m_l */
+            int64_t best = 0;
+            for (int64_t j = 1; j < N; ++j)
+                if (m[j] > m[best]) best = j;
+            c = best;
+            sel[t] = c;
+            /* m_j = min(m_j, s(x_j, x_c)) */
+            for (int64_t j = 0; j < N; ++j) {
+                float s = orc_s32(x + 3 * j, x + 3 * c);
+                if (s < m[j]) m[j] = s;
+            }
+        }
+    }
+    free(m);
+    return ORC_OK;
+}
+
+/*
+ * m_j for a given set of centers: min over the centers u of s(x_j, x_{c_u}).
+ * The FPS running minimum of the project page's "Farthest point sampling"
+ * equation, evaluated for chosen points j only.  Used by the at-scale property
+ * checks (the selected center must attain the maximum of m).
+ */
+int orc_min_dist_to_set(const float *x, int64_t N, const int64_t *centers,
+                        int64_t ncenters, const int64_t *points,
+                        int64_t npoints, float *out)
+{
+    if (N < 1 || ncenters < 1) return ORC_BAD_ARGUMENT;
+    for (int64_t i = 0; i < npoints; ++i) {
+        int64_t j = points[i];
+        if (j < 0 || j >= N) return ORC_BAD_ARGUMENT;
+        float m = 0.0f;
+        for (int64_t u = 0; u < ncenters; ++u) {
+            int64_t c = centers[u];
+            if (c < 0 || c >= N) return ORC_BAD_ARGUMENT;
+            float s = orc_s32(x + 3 * j, x + 3 * c);
+            if (u == 0 || s < m) m = s;
+        }
+        out[i] = m;
+    }
+    return ORC_OK;
+}
+
+/* One (squared distance, index) candidate of the kNN sort. */
+typedef struct {
+    float s;
+    int64_t j;
+} orc_pair;
+
+/* Lexicographic order on (s, j): "sort by squared distance and then input
+ * index" (project page, "k nearest neighbors"). */
+static int orc_pair_cmp(const void *pa, const void *pb)
+{
+    const orc_pair *a = (const orc_pair *)pa;
+    const orc_pair *b = (const orc_pair *)pb;
+    if (a->s < b->s) return -1;
+    if (a->s > b->s) return 1;
+    if (a->j < b->j) return -1;
+    if (a->j > b->j) return 1;
+    return 0;
+}
+
+/*
+ * kNN for a list of query rows.  Row r = b*Q + i names query i of cloud b.
+ * Project page, "k nearest neighbors":
+ *   pi_bi = argsort_j (s_bij, j),  I_bik = pi_bi[k],  D_bik = sqrt(s_bi,I_bik).
+ * "Numerical contracts": the smallest k distances, exact ties to the smaller
+ * reference index, Euclidean distances returned.  The sort is the C library's
+ * qsort over all N candidates; k <= N ("Contracts": knn).  sqrtf is the
+ * correctly rounded IEEE square root.
+ * Outputs: out_dist[nrows*k] float32, out_idx[nrows*k] int64, row-major.
+ */
+int orc_knn_rows(const float *query, int64_t B, int64_t Q, const float *ref,
+                 int64_t N, int64_t k, const int64_t *rows, int64_t nrows,
+                 float *out_dist, int64_t *out_idx)
+{
+    if (B < 0 || Q < 0 || N < 1 || k < 1 || k > N) return ORC_BAD_ARGUMENT;
+    orc_pair *cand = (orc_pair *)malloc((size_t)N * sizeof(orc_pair));
+    if (!cand) return ORC_NO_MEMORY;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t row = rows[r];
+        if (row < 0 || row >= B * Q) {
+            free(cand);
+            return ORC_BAD_ARGUMENT;
+        }
+        int64_t b = row / Q;
+        const float *q = query + (size_t)row * 3;
+        const float *x = ref + (size_t)b * (size_t)N * 3;
+        for (int64_t j = 0; j < N; ++j) {
+            cand[j].s = orc_s32(q, x + 3 * j);
+            cand[j].j = j;
+        }
+        qsort(cand, (size_t)N, sizeof(orc_pair), orc_pair_cmp);
+        for (int64_t t = 0; t < k; ++t) {
+            out_dist[r * k + t] = sqrtf(cand[t].s);
+            out_idx[r * k + t] = cand[t].j;
+        }
+    }
+    free(cand);
+    return ORC_OK;
+}
+
+/*
+ * Ball Query for a list of query rows.  Row r = b*Q + i names query i of
+ * cloud b.  Project page, "Ball Query: first K within a radius":
+ *   R2 = fl32(fl32(r) * fl32(r)),
+ *   J_bi = [ j in 0..N-1 : s_bij < R2 ] in input order,
+ *   (I, S)_bik = (J_bi[k], s_bi,J_bi[k]) for k < min(K, |J_bi|), else (-1, 0).
+ * "Numerical contracts", "Selection and output": accept iff s32 < R2 (strict).
+ * Outputs: out_dist2[nrows*K] float32, out_idx[nrows*K] int64, row-major.
+ * N = 0 is allowed and gives padding only.
+ */
+int orc_ball_query_rows(const float *query, int64_t B, int64_t Q,
+                        const float *ref, int64_t N, double radius, int64_t K,
+                        const int64_t *rows, int64_t nrows, float *out_dist2,
+                        int64_t *out_idx)
+{
+    if (B < 0 || Q < 0 || N < 0 || K < 1) return ORC_BAD_ARGUMENT;
+    float R2 = orc_radius_threshold(radius);
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t row = rows[r];
+        if (row < 0 || row >= B * Q) return ORC_BAD_ARGUMENT;
+        int64_t b = row / Q;
+        const float *q = query + (size_t)row * 3;
+        const float *x = ref + (size_t)b * (size_t)N * 3;
+        int64_t cnt = 0;
+        for (int64_t j = 0; j < N && cnt < K; ++j) {
+            float s = orc_s32(q, x + 3 * j);
+            if (s < R2) {
+                out_idx[r * K + cnt] = j;
+                out_dist2[r * K + cnt] = s;
+                ++cnt;
+            }
+        }
+        for (; cnt < K; ++cnt) {
+            out_idx[r * K + cnt] = -1;
+            out_dist2[r * K + cnt] = 0.0f;
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Number of (query, reference) pairs the first-K Ball Query rule has to
+ * examine for each row: the position of the K-th accepted reference plus one,
+ * or N when fewer than K references are accepted.  Used to count the
+ * algorithmic work of a Ball Query launch; it follows the same definition as
+ * orc_ball_query_rows.
+ */
+int orc_ball_query_scan_len(const float *query, int64_t B, int64_t Q,
+                            const float *ref, int64_t N, double radius,
+                            int64_t K, const int64_t *rows, int64_t nrows,
+                            int64_t *out_len)
+{
+    if (B < 0 || Q < 0 || N < 0 || K < 1) return ORC_BAD_ARGUMENT;
+    float R2 = orc_radius_threshold(radius);
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t row = rows[r];
+        if (row < 0 || row >= B * Q) return ORC_BAD_ARGUMENT;
+        int64_t b = row / Q;
+        const float *q = query + (size_t)row * 3;
+        const float *x = ref + (size_t)b * (size_t)N * 3;
+        int64_t cnt = 0, j = 0;
+        for (; j < N && cnt < K; ++j)
+            if (orc_s32(q, x + 3 * j) < R2) ++cnt;
+        out_len[r] = j;
+    }
+    return ORC_OK;
+}
+
+/* Pairwise squared distances s32(a_i, b_i) for n point pairs (test helper). */
+void orc_s32_pairs(const float *a, const float *b, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_s32(a + 3 * i, b + 3 * i);
+}
