@@ -1,0 +1,187 @@
+/*
+ * pointcloud.h -- C ABI of the GB300 (sm_103a) dense point-cloud neighbor
+ * search library (libpointcloud.so).
+ *
+ * Three operators over dense, batched float32 clouds, with the selection rules
+ * of the mps-pointops 0.5.0 project page ("The operators in equations",
+ * "Contracts") and the mps-pointops "Numerical contracts" page ("Selection and
+ * output"):
+ *
+ *   squared distance  s(i,j) = ((dx*dx + dy*dy) + dz*dz), dx = q_x - x_x, ...
+ *                     every operation a separately rounded float32 operation
+ *                     (round to nearest even, no FMA contraction, subnormals
+ *                     kept).  All three operators select on this value.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout: coordinates are row-major [B, N, 3] float32 (x, y, z of a point
+ *    adjacent; clouds adjacent); outputs are row-major as stated per call.
+ *  - Memory: every pointer argument named *xyz, *query, *ref, *out_* is a
+ *    DEVICE pointer (cudaMalloc / caching-allocator / managed memory) on the
+ *    current CUDA device, owned by the caller.  The library never frees or
+ *    keeps a caller pointer.  Coordinates must be 4-byte aligned, int64
+ *    outputs 8-byte aligned.  Inputs and outputs must not overlap.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Every call only enqueues work on that stream and
+ *    returns; results are ready when the stream reaches that point.  Calls
+ *    on one stream run in order; calls on different streams share nothing
+ *    except the library's device status word (see pc_device_status).
+ *  - Errors: arguments are validated on the host before anything is
+ *    enqueued; a rejected call enqueues nothing and returns a status code.
+ *    There is no silent fallback to another device or to the CPU.
+ *    pc_last_error_message() gives a one-line reason for the last failing
+ *    call on the calling host thread.
+ *  - Inputs must be finite.  Ball Query never accepts a NaN distance; FPS and
+ *    kNN results for non-finite coordinates are unspecified.
+ *  - Sizes: B, N, Q >= 0 with N < 2^31 and every output size < 2^62 elements.
+ */
+#ifndef POINTCLOUD_H
+#define POINTCLOUD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum pc_status {
+    PC_OK = 0,
+    PC_ERR_INVALID_ARGUMENT = 1, /* a size, pointer or parameter is invalid  */
+    PC_ERR_UNSUPPORTED = 2,      /* valid, but beyond what this build runs   */
+    PC_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed     */
+    PC_ERR_DEVICE_TIMEOUT = 4,   /* a bounded device-side wait ran out       */
+    PC_ERR_NO_DEVICE = 5         /* no usable sm_103 device is current       */
+} pc_status;
+
+/* Static, NUL-terminated name of a status code ("PC_OK", ...). */
+const char *pc_status_string(int status);
+
+/* One-line reason for the last non-OK status returned on this host thread
+ * (empty string if none).  The pointer stays valid until the next call that
+ * fails on this thread. */
+const char *pc_last_error_message(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int pc_version(void);
+
+/*
+ * Farthest point sampling.
+ * Project page, "Farthest point sampling": c_0 = start_idx; with
+ * m_j(t) = min_{u<=t} s(x_j, x_{c_u}), the next center is the smallest j
+ * attaining max_l m_l(t).  "Contracts": once every point is taken the
+ * remaining slots repeat index 0.  The same start index is used for every
+ * cloud.
+ *
+ *   xyz        [B, N, 3] float32, device.
+ *   out_idx    [B, npoint] int64, device; written in full.
+ *   npoint     >= 1 (npoint > N is allowed).  0 <= start_idx < N when B > 0.
+ *   workspace  device scratch of at least pc_fps_workspace_bytes(B, N,
+ *              npoint) bytes, 256-byte aligned, or NULL.  When the chosen
+ *              schedule needs scratch and workspace is NULL the library takes
+ *              it from the stream-ordered allocator (cudaMallocAsync) and
+ *              frees it after the launch on the same stream.  A workspace must
+ *              not be shared by calls that may run concurrently.
+ *
+ * Schedules (chosen from B and N): one thread block per cloud, one thread
+ * block cluster per cloud (distributed shared memory), or -- for clouds too
+ * large for one cluster -- a cooperative grid per cloud that exchanges one
+ * 64-bit key per block and step through the workspace.  Only the grid
+ * schedule uses scratch and bounded device-side waits; if a wait runs out the
+ * kernel stops, writes -1 into the remaining out_idx slots of that cloud
+ * and raises the device status word (PC_ERR_DEVICE_TIMEOUT).
+ *
+ * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_UNSUPPORTED (cloud too large
+ * for the on-chip schedules), PC_ERR_CUDA or PC_ERR_NO_DEVICE.
+ */
+int pc_fps(const float *xyz, int64_t B, int64_t N, int64_t npoint,
+           int64_t start_idx, int64_t *out_idx, void *workspace,
+           size_t workspace_bytes, void *stream);
+
+/* Scratch bytes pc_fps needs for these sizes (0 when no scratch is used). */
+size_t pc_fps_workspace_bytes(int64_t B, int64_t N, int64_t npoint);
+
+/* FPS schedule selectors for pc_fps_ex. */
+typedef enum pc_fps_strategy {
+    PC_FPS_AUTO = 0,
+    PC_FPS_BLOCK = 1,   /* one thread block per cloud                        */
+    PC_FPS_CLUSTER = 2, /* one thread block cluster per cloud                */
+    PC_FPS_GRID = 3     /* cooperative grid, workspace exchange (see above)  */
+} pc_fps_strategy;
+
+/* pc_fps with an explicit schedule (results are identical for every
+ * schedule).  `cluster_size` (1..16, 0 = automatic) applies to
+ * PC_FPS_CLUSTER; `blocks_per_cloud` (0 = automatic) to PC_FPS_GRID.  The
+ * workspace size for PC_FPS_GRID is pc_fps_workspace_bytes_ex. */
+int pc_fps_ex(const float *xyz, int64_t B, int64_t N, int64_t npoint,
+              int64_t start_idx, int64_t *out_idx, void *workspace,
+              size_t workspace_bytes, int strategy, int cluster_size,
+              int blocks_per_cloud, void *stream);
+
+size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
+                                 int strategy, int blocks_per_cloud);
+
+/*
+ * k nearest neighbors.
+ * Project page, "k nearest neighbors": for each query, candidates sorted by
+ * (s, j) -- squared distance, then reference index -- and the first k
+ * returned with Euclidean distance D = sqrt(s) (correctly rounded float32
+ * square root).  "Numerical contracts": exact ties go to the smaller index.
+ *
+ *   query     [B, Q, 3] float32, device.   ref [B, N, 3] float32, device.
+ *   out_dist  [B, Q, k] float32, device.   out_idx [B, Q, k] int64, device.
+ *             Row (b, i) lists the k neighbors of query i of cloud b in
+ *             increasing (s, j) order; indices are into cloud b of ref.
+ *   k         1 <= k <= N ("Contracts": k <= N), and k <= 256.
+ *
+ * Returns PC_OK, PC_ERR_INVALID_ARGUMENT (k > N, k < 1, bad pointer ...),
+ * PC_ERR_UNSUPPORTED (k > 256), PC_ERR_CUDA or PC_ERR_NO_DEVICE.
+ */
+int pc_knn(const float *query, int64_t B, int64_t Q, const float *ref,
+           int64_t N, int64_t k, float *out_dist, int64_t *out_idx,
+           void *stream);
+
+/*
+ * Ball Query: the first K references in input order inside the radius.
+ * Project page, "Ball Query: first K within a radius"; "Numerical
+ * contracts", "Selection and output":
+ *   R2 = fl32(fl32(r) * fl32(r)); reference j is accepted iff s < R2
+ *   (strict); the first K accepted j in increasing order are returned with
+ *   their squared distances; unused slots hold (index -1, distance 0).
+ *
+ *   query      [B, Q, 3] float32, device.  ref [B, N, 3] float32, device.
+ *   radius     finite and > 0 (rounded to float32 by the library).
+ *   K          >= 1.  N = 0 is allowed (all slots padded).
+ *   out_dist2  [B, Q, K] float32, device.  out_idx [B, Q, K] int64, device.
+ *
+ * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_CUDA or PC_ERR_NO_DEVICE.
+ */
+int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
+                  int64_t N, double radius, int64_t K, float *out_dist2,
+                  int64_t *out_idx, void *stream);
+
+/*
+ * Device status word.  Kernels that wait on other thread blocks bound every
+ * wait; when a wait runs out they record PC_ERR_DEVICE_TIMEOUT here (the
+ * first error wins) and return instead of hanging.  This call synchronizes
+ * `stream`, copies the word of the current device to *out_status (PC_OK if
+ * nothing was recorded) and, if `reset` is non-zero, clears it.
+ */
+int pc_device_status(void *stream, int reset, int32_t *out_status);
+
+/*
+ * Bound on each device-side wait, in nanoseconds (default 2e9).  Applies to
+ * launches enqueued after the call, on every device.  Values below 1000 are
+ * raised to 1000.  Testing hook: pc_debug_set_fps_grid_stall(1) makes the
+ * next PC_FPS_GRID launches withhold block 0's first exchange, so that every
+ * waiting block runs out its bound; 0 restores normal operation.
+ */
+void pc_set_wait_timeout_ns(uint64_t ns);
+void pc_debug_set_fps_grid_stall(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POINTCLOUD_H */

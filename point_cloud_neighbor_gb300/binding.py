@@ -1,0 +1,231 @@
+"""Thin Python binding of libpointcloud.so (include/pointcloud.h).
+
+Argument marshalling only: the functions check tensor placement, dtype,
+layout and shapes, allocate outputs with torch's caching allocator, pass raw
+device pointers and the current CUDA stream through ctypes, and turn a
+non-OK status into :class:`PointCloudError`.  Every step of FPS, kNN and Ball
+Query runs in the library's CUDA kernels.  There is no CPU path: CPU
+tensors, a missing library or a non-sm_103 device raise.
+
+Names follow the C ABI (``pc_fps``, ``pc_knn``, ``pc_ball_query``); the
+aliases ``furthest_point_sample``, ``knn`` and ``ball_query`` mirror the
+mps-pointops dense API ("Contracts" section of its project page).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpointcloud.so")
+
+PC_OK = 0
+PC_ERR_INVALID_ARGUMENT = 1
+PC_ERR_UNSUPPORTED = 2
+PC_ERR_CUDA = 3
+PC_ERR_DEVICE_TIMEOUT = 4
+PC_ERR_NO_DEVICE = 5
+
+PC_FPS_AUTO, PC_FPS_BLOCK, PC_FPS_CLUSTER, PC_FPS_GRID = 0, 1, 2, 3
+
+# Every symbol include/pointcloud.h declares, with its ctypes signature.
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_SIGNATURES = {
+    "pc_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "pc_last_error_message": (ctypes.c_char_p, []),
+    "pc_version": (ctypes.c_int, []),
+    "pc_fps": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+    "pc_fps_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I]),
+    "pc_fps_ex": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P, ctypes.c_size_t,
+                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
+    "pc_fps_workspace_bytes_ex": (ctypes.c_size_t, [_I, _I, _I, ctypes.c_int,
+                                                    ctypes.c_int]),
+    "pc_knn": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _P, _P, _P]),
+    "pc_ball_query": (ctypes.c_int, [_P, _I, _I, _P, _I, ctypes.c_double, _I,
+                                     _P, _P, _P]),
+    "pc_device_status": (ctypes.c_int, [_P, ctypes.c_int,
+                                        ctypes.POINTER(ctypes.c_int32)]),
+    "pc_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
+    "pc_debug_set_fps_grid_stall": (None, [ctypes.c_int]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PointCloudError(RuntimeError):
+    """A library call returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpointcloud.so (built by ``point_cloud_neighbor_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -m point_cloud_neighbor_gb300.build); there is no "
+                    "CPU fallback")
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+        return _lib
+
+
+def exported_symbols():
+    return list(_SIGNATURES)
+
+
+def _raise_on(status: int, what: str):
+    if status != PC_OK:
+        L = lib()
+        name = L.pc_status_string(status).decode()
+        msg = L.pc_last_error_message().decode()
+        raise PointCloudError(status, f"{what}: {name}: {msg}")
+
+
+def _stream_ptr(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_cloud(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got {t.device}); "
+                         "this library has no CPU path")
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32 (got {t.dtype})")
+    if t.dim() != 3 or t.shape[-1] != 3:
+        raise ValueError(f"{name} must have shape [B, N, 3] (got {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def pc_fps(xyz: torch.Tensor, npoint: int, start_idx: int = 0, *,
+           strategy: int = PC_FPS_AUTO, cluster_size: int = 0,
+           blocks_per_cloud: int = 0, out: torch.Tensor | None = None,
+           workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Farthest point sampling: [B,N,3] float32 -> [B,npoint] int64."""
+    _check_cloud(xyz, "xyz")
+    B, N, _ = xyz.shape
+    L = lib()
+    with torch.cuda.device(xyz.device):
+        if out is None:
+            out = torch.empty((B, npoint), dtype=torch.int64, device=xyz.device)
+        ws_ptr, ws_bytes = None, 0
+        if B > 0 and N > 0:
+            need = L.pc_fps_workspace_bytes_ex(B, N, npoint, strategy,
+                                               blocks_per_cloud)
+            if need:
+                if workspace is None or workspace.numel() < need:
+                    workspace = torch.empty(need, dtype=torch.uint8,
+                                            device=xyz.device)
+                ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+        st = L.pc_fps_ex(xyz.data_ptr(), B, N, npoint, start_idx,
+                         out.data_ptr(), ws_ptr, ws_bytes, strategy,
+                         cluster_size, blocks_per_cloud,
+                         _stream_ptr(xyz.device))
+    _raise_on(st, "pc_fps")
+    return out
+
+
+def pc_knn(query: torch.Tensor, ref: torch.Tensor, k: int, *,
+           out_dist: torch.Tensor | None = None,
+           out_idx: torch.Tensor | None = None):
+    """k nearest neighbors: returns (dist [B,Q,k] float32, idx [B,Q,k] int64)."""
+    _check_cloud(query, "query")
+    _check_cloud(ref, "ref")
+    B, Q, _ = query.shape
+    if ref.shape[0] != B:
+        raise ValueError("query and ref must have the same batch size")
+    if ref.device != query.device:
+        raise ValueError("query and ref must be on the same device")
+    N = ref.shape[1]
+    L = lib()
+    with torch.cuda.device(query.device):
+        if out_dist is None:
+            out_dist = torch.empty((B, Q, k), dtype=torch.float32,
+                                   device=query.device)
+        if out_idx is None:
+            out_idx = torch.empty((B, Q, k), dtype=torch.int64,
+                                  device=query.device)
+        st = L.pc_knn(query.data_ptr(), B, Q, ref.data_ptr(), N, k,
+                      out_dist.data_ptr(), out_idx.data_ptr(),
+                      _stream_ptr(query.device))
+    _raise_on(st, "pc_knn")
+    return out_dist, out_idx
+
+
+def pc_ball_query(query: torch.Tensor, ref: torch.Tensor, radius: float,
+                  K: int, *, out_dist2: torch.Tensor | None = None,
+                  out_idx: torch.Tensor | None = None):
+    """First-K Ball Query: returns (dist2 [B,Q,K] float32, idx [B,Q,K] int64)."""
+    _check_cloud(query, "query")
+    _check_cloud(ref, "ref")
+    B, Q, _ = query.shape
+    if ref.shape[0] != B:
+        raise ValueError("query and ref must have the same batch size")
+    if ref.device != query.device:
+        raise ValueError("query and ref must be on the same device")
+    N = ref.shape[1]
+    L = lib()
+    with torch.cuda.device(query.device):
+        if out_dist2 is None:
+            out_dist2 = torch.empty((B, Q, K), dtype=torch.float32,
+                                    device=query.device)
+        if out_idx is None:
+            out_idx = torch.empty((B, Q, K), dtype=torch.int64,
+                                  device=query.device)
+        st = L.pc_ball_query(query.data_ptr(), B, Q,
+                             ref.data_ptr() if N > 0 else None, N,
+                             float(radius), K, out_dist2.data_ptr(),
+                             out_idx.data_ptr(), _stream_ptr(query.device))
+    _raise_on(st, "pc_ball_query")
+    return out_dist2, out_idx
+
+
+def pc_device_status(reset: bool = True, device=None) -> int:
+    """Synchronize the current stream and return (and clear) the status word."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    out = ctypes.c_int32(0)
+    with torch.cuda.device(device):
+        st = lib().pc_device_status(_stream_ptr(device), int(reset),
+                                    ctypes.byref(out))
+    _raise_on(st, "pc_device_status")
+    return out.value
+
+
+def pc_set_wait_timeout_ns(ns: int):
+    lib().pc_set_wait_timeout_ns(int(ns))
+
+
+def pc_debug_set_fps_grid_stall(enable: bool):
+    lib().pc_debug_set_fps_grid_stall(int(bool(enable)))
+
+
+# mps-pointops-style names
+def furthest_point_sample(xyz, npoint, start_idx=0):
+    return pc_fps(xyz, npoint, start_idx)
+
+
+def knn(query, ref, k):
+    return pc_knn(query, ref, k)
+
+
+def ball_query(query, ref, radius, K):
+    return pc_ball_query(query, ref, radius, K)

@@ -1,0 +1,320 @@
+// pc_api.cu -- the C ABI of libpointcloud.so (declared in
+// include/pointcloud.h): host-side validation, device checks, schedule
+// choice, workspace handling and the device status word.  Every compute step
+// runs in the kernels of pc_fps.cu, pc_knn.cu and pc_ball_query.cu.
+#include "pointcloud.h"
+#include "pc_internal.h"
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+namespace {
+
+// The device status word: the first device-side error (a bounded wait that
+// ran out) is recorded here.  One instance per device (module global).
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr int kVersion = 10000 * 0 + 100 * 1 + 0;  // 0.1.0
+
+thread_local std::string t_error;
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_fps_stall{0};
+std::mutex g_dev_mutex;
+pcn::DeviceInfo g_devices[kMaxDevices];
+bool g_device_ready[kMaxDevices] = {};
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_error = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(PC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+}
+
+// Resolve and cache the current device; checks that it is the architecture
+// this library is built for (compute capability 10.3, 32-wide warps).
+int current_device(const pcn::DeviceInfo **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PC_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
+    }
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(PC_ERR_NO_DEVICE, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_device_ready[dev]) {
+        pcn::DeviceInfo d;
+        d.device = dev;
+        int v = 0;
+        auto attr = [&](cudaDeviceAttr a) {
+            v = 0;
+            cudaDeviceGetAttribute(&v, a, dev);
+            return v;
+        };
+        d.sm_count = attr(cudaDevAttrMultiProcessorCount);
+        d.cc_major = attr(cudaDevAttrComputeCapabilityMajor);
+        d.cc_minor = attr(cudaDevAttrComputeCapabilityMinor);
+        d.warp_size = attr(cudaDevAttrWarpSize);
+        d.smem_per_block_optin = size_t(attr(cudaDevAttrMaxSharedMemoryPerBlockOptin));
+        d.smem_per_sm = size_t(attr(cudaDevAttrMaxSharedMemoryPerMultiprocessor));
+        d.max_threads_per_sm = attr(cudaDevAttrMaxThreadsPerMultiProcessor);
+        d.cooperative = attr(cudaDevAttrCooperativeLaunch);
+        if (d.cc_major != 10 || d.cc_minor != 3)
+            return fail(PC_ERR_NO_DEVICE,
+                        "device %d has compute capability %d.%d; this library "
+                        "is built for sm_103a only", dev, d.cc_major, d.cc_minor);
+        if (d.warp_size != 32)
+            return fail(PC_ERR_NO_DEVICE, "device %d reports warp size %d, need 32",
+                        dev, d.warp_size);
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return cuda_fail(e, "status word address");
+        d.status_word = static_cast<int *>(p);
+        g_devices[dev] = d;
+        g_device_ready[dev] = true;
+    }
+    *out = &g_devices[dev];
+    return PC_OK;
+}
+
+// A caller pointer must be device (or managed) memory of `dev`, aligned.
+int check_ptr(const void *p, int dev, size_t align, const char *name) {
+    if (p == nullptr) return fail(PC_ERR_INVALID_ARGUMENT, "%s is NULL", name);
+    if (reinterpret_cast<uintptr_t>(p) % align != 0)
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s is not %zu-byte aligned", name,
+                    align);
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s is not a CUDA pointer (%s)",
+                    name, cudaGetErrorString(e));
+    }
+    if (at.type == cudaMemoryTypeManaged) return PC_OK;
+    if (at.type != cudaMemoryTypeDevice)
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "%s is not device memory (host pointers are not accepted)",
+                    name);
+    if (at.device != dev)
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "%s lives on device %d but device %d is current", name,
+                    at.device, dev);
+    return PC_OK;
+}
+
+constexpr int64_t kMaxInt = 2147483647;
+constexpr int64_t kMaxElems = int64_t(1) << 62;
+
+bool mul_ok(int64_t a, int64_t b, int64_t c) {
+    if (a == 0 || b == 0 || c == 0) return true;
+    return a <= kMaxElems / b && a * b <= kMaxElems / c;
+}
+
+}  // namespace
+
+namespace pcn {
+uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+int fps_grid_stall() { return g_fps_stall.load(); }
+}  // namespace pcn
+
+extern "C" {
+
+const char *pc_status_string(int status) {
+    switch (status) {
+        case PC_OK: return "PC_OK";
+        case PC_ERR_INVALID_ARGUMENT: return "PC_ERR_INVALID_ARGUMENT";
+        case PC_ERR_UNSUPPORTED: return "PC_ERR_UNSUPPORTED";
+        case PC_ERR_CUDA: return "PC_ERR_CUDA";
+        case PC_ERR_DEVICE_TIMEOUT: return "PC_ERR_DEVICE_TIMEOUT";
+        case PC_ERR_NO_DEVICE: return "PC_ERR_NO_DEVICE";
+        default: return "PC_ERR_UNKNOWN";
+    }
+}
+
+const char *pc_last_error_message(void) { return t_error.c_str(); }
+
+int pc_version(void) { return kVersion; }
+
+void pc_set_wait_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns < 1000 ? 1000 : ns);
+}
+
+void pc_debug_set_fps_grid_stall(int enable) { g_fps_stall.store(enable ? 1 : 0); }
+
+size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
+                                 int strategy, int blocks_per_cloud) {
+    (void)npoint;
+    if (B <= 0 || N <= 0) return 0;
+    const pcn::DeviceInfo *dev = nullptr;
+    if (current_device(&dev) != PC_OK) return 0;
+    pcn::FpsPlan p = pcn::plan_fps(*dev, B, N, strategy, 0, blocks_per_cloud);
+    return p.ok ? p.workspace_bytes : 0;
+}
+
+size_t pc_fps_workspace_bytes(int64_t B, int64_t N, int64_t npoint) {
+    return pc_fps_workspace_bytes_ex(B, N, npoint, PC_FPS_AUTO, 0);
+}
+
+int pc_fps_ex(const float *xyz, int64_t B, int64_t N, int64_t npoint,
+              int64_t start_idx, int64_t *out_idx, void *workspace,
+              size_t workspace_bytes, int strategy, int cluster_size,
+              int blocks_per_cloud, void *stream) {
+    if (B < 0 || N < 0 || npoint < 1)
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "fps: need B >= 0, N >= 0, npoint >= 1 (got %lld, %lld, %lld)",
+                    (long long)B, (long long)N, (long long)npoint);
+    if (strategy < PC_FPS_AUTO || strategy > PC_FPS_GRID)
+        return fail(PC_ERR_INVALID_ARGUMENT, "fps: unknown strategy %d", strategy);
+    if (cluster_size < 0 || cluster_size > 16 || blocks_per_cloud < 0)
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "fps: cluster_size must be 0..16 and blocks_per_cloud >= 0");
+    if (B == 0) return PC_OK;
+    if (N < 1 || start_idx < 0 || start_idx >= N)
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "fps: need 0 <= start_idx < N (got start_idx=%lld, N=%lld)",
+                    (long long)start_idx, (long long)N);
+    if (N > kMaxInt || npoint > kMaxInt || B > kMaxInt || !mul_ok(B, N, 3) ||
+        !mul_ok(B, npoint, 1))
+        return fail(PC_ERR_UNSUPPORTED, "fps: sizes beyond 32-bit indexing");
+    const pcn::DeviceInfo *dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != PC_OK) return rc;
+    if ((rc = check_ptr(xyz, dev->device, 4, "xyz")) != PC_OK) return rc;
+    if ((rc = check_ptr(out_idx, dev->device, 8, "out_idx")) != PC_OK) return rc;
+    pcn::FpsPlan plan =
+        pcn::plan_fps(*dev, B, N, strategy, cluster_size, blocks_per_cloud);
+    if (!plan.ok)
+        return fail(PC_ERR_UNSUPPORTED, "fps: %s (B=%lld, N=%lld)", plan.why,
+                    (long long)B, (long long)N);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void *ws = workspace;
+    bool owned = false;
+    if (plan.workspace_bytes > 0) {
+        if (ws != nullptr) {
+            if (workspace_bytes < plan.workspace_bytes)
+                return fail(PC_ERR_INVALID_ARGUMENT,
+                            "fps: workspace of %zu bytes, need %zu",
+                            workspace_bytes, plan.workspace_bytes);
+            if ((rc = check_ptr(ws, dev->device, 256, "workspace")) != PC_OK)
+                return rc;
+        } else {
+            cudaError_t e = cudaMallocAsync(&ws, plan.workspace_bytes, st);
+            if (e != cudaSuccess) return cuda_fail(e, "fps: workspace allocation");
+            owned = true;
+        }
+    }
+    cudaError_t e = pcn::launch_fps(*dev, plan, xyz, B, N, npoint, start_idx,
+                                    out_idx, ws, st);
+    if (owned) {
+        cudaError_t e2 = cudaFreeAsync(ws, st);
+        if (e == cudaSuccess) e = e2;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "fps: launch");
+    return PC_OK;
+}
+
+int pc_fps(const float *xyz, int64_t B, int64_t N, int64_t npoint,
+           int64_t start_idx, int64_t *out_idx, void *workspace,
+           size_t workspace_bytes, void *stream) {
+    return pc_fps_ex(xyz, B, N, npoint, start_idx, out_idx, workspace,
+                     workspace_bytes, PC_FPS_AUTO, 0, 0, stream);
+}
+
+int pc_knn(const float *query, int64_t B, int64_t Q, const float *ref,
+           int64_t N, int64_t k, float *out_dist, int64_t *out_idx,
+           void *stream) {
+    if (B < 0 || Q < 0 || N < 0)
+        return fail(PC_ERR_INVALID_ARGUMENT, "knn: negative size");
+    if (k < 1 || k > N)
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "knn: need 1 <= k <= N (got k=%lld, N=%lld)", (long long)k,
+                    (long long)N);
+    if (k > 256)
+        return fail(PC_ERR_UNSUPPORTED, "knn: k=%lld above the maximum 256",
+                    (long long)k);
+    if (B > 65535)
+        return fail(PC_ERR_UNSUPPORTED, "knn: B=%lld above 65535", (long long)B);
+    if (Q > kMaxInt || N > kMaxInt || !mul_ok(B, Q, k) || !mul_ok(B, N, 3) ||
+        !mul_ok(B, Q, 3))
+        return fail(PC_ERR_UNSUPPORTED, "knn: sizes beyond 32-bit indexing");
+    if (B == 0 || Q == 0) return PC_OK;
+    const pcn::DeviceInfo *dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != PC_OK) return rc;
+    if ((rc = check_ptr(query, dev->device, 4, "query")) != PC_OK) return rc;
+    if ((rc = check_ptr(ref, dev->device, 4, "ref")) != PC_OK) return rc;
+    if ((rc = check_ptr(out_dist, dev->device, 4, "out_dist")) != PC_OK) return rc;
+    if ((rc = check_ptr(out_idx, dev->device, 8, "out_idx")) != PC_OK) return rc;
+    cudaError_t e = pcn::launch_knn(*dev, query, B, Q, ref, N, int(k), out_dist,
+                                    out_idx, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "knn: launch");
+    return PC_OK;
+}
+
+int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
+                  int64_t N, double radius, int64_t K, float *out_dist2,
+                  int64_t *out_idx, void *stream) {
+    if (B < 0 || Q < 0 || N < 0)
+        return fail(PC_ERR_INVALID_ARGUMENT, "ball_query: negative size");
+    if (!std::isfinite(radius) || !(radius > 0.0))
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "ball_query: radius must be finite and > 0 (got %g)", radius);
+    if (K < 1)
+        return fail(PC_ERR_INVALID_ARGUMENT, "ball_query: need K >= 1 (got %lld)",
+                    (long long)K);
+    if (B > 65535)
+        return fail(PC_ERR_UNSUPPORTED, "ball_query: B=%lld above 65535",
+                    (long long)B);
+    if (Q > kMaxInt || N > kMaxInt || K > kMaxInt || !mul_ok(B, Q, K) ||
+        !mul_ok(B, N, 3) || !mul_ok(B, Q, 3))
+        return fail(PC_ERR_UNSUPPORTED, "ball_query: sizes beyond 32-bit indexing");
+    if (B == 0 || Q == 0) return PC_OK;
+    const pcn::DeviceInfo *dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != PC_OK) return rc;
+    if ((rc = check_ptr(query, dev->device, 4, "query")) != PC_OK) return rc;
+    if (N > 0 && (rc = check_ptr(ref, dev->device, 4, "ref")) != PC_OK) return rc;
+    if ((rc = check_ptr(out_dist2, dev->device, 4, "out_dist2")) != PC_OK) return rc;
+    if ((rc = check_ptr(out_idx, dev->device, 8, "out_idx")) != PC_OK) return rc;
+    const float r32 = static_cast<float>(radius);
+    cudaError_t e = pcn::launch_ball_query(*dev, query, B, Q, ref, N, r32, K,
+                                           out_dist2, out_idx,
+                                           static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "ball_query: launch");
+    return PC_OK;
+}
+
+int pc_device_status(void *stream, int reset, int32_t *out_status) {
+    if (out_status == nullptr)
+        return fail(PC_ERR_INVALID_ARGUMENT, "device_status: out_status is NULL");
+    const pcn::DeviceInfo *dev = nullptr;
+    int rc = current_device(&dev);
+    if (rc != PC_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "device_status: synchronize");
+    int v = 0;
+    e = cudaMemcpy(&v, dev->status_word, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "device_status: read");
+    if (reset && v != 0) {
+        e = cudaMemset(dev->status_word, 0, sizeof(int));
+        if (e != cudaSuccess) return cuda_fail(e, "device_status: reset");
+    }
+    *out_status = v;
+    return PC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,208 @@
+// pc_device.cuh -- device primitives shared by the FPS, kNN and Ball Query
+// kernels: the non-contracted squared distance, warp reductions, and inline
+// PTX for mbarriers, TMA bulk copies, clusters and bounded waits (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pcn {
+
+// ---------------------------------------------------------------------------
+// Squared distance s = ((dx*dx + dy*dy) + dz*dz), each operation rounded to
+// nearest even on its own (no FMA), as the mps-pointops project page's
+// "How the kernels work" section states for FPS and kNN and as the
+// "Numerical contracts" page's s32 requires for all three operators.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float sqdist(float ax, float ay, float az,
+                                        float bx, float by, float bz) {
+    float dx = __fsub_rn(ax, bx);
+    float dy = __fsub_rn(ay, by);
+    float dz = __fsub_rn(az, bz);
+    return __fadd_rn(__fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy)),
+                     __fmul_rn(dz, dz));
+}
+
+// Two references (packed in the .x/.y halves) against one point whose
+// coordinates are given NEGATED: d = x + (-q) is the same float as -(q - x)
+// under round-to-nearest-even, and the square removes the sign, so each half
+// equals sqdist() bit for bit.  One packed f32x2 instruction per operation.
+__device__ __forceinline__ float2 sqdist2(float2 x, float2 y, float2 z,
+                                          float2 nqx, float2 nqy, float2 nqz) {
+    float2 dx = __fadd2_rn(x, nqx);
+    float2 dy = __fadd2_rn(y, nqy);
+    float2 dz = __fadd2_rn(z, nqz);
+    return __fadd2_rn(__fadd2_rn(__fmul2_rn(dx, dx), __fmul2_rn(dy, dy)),
+                      __fmul2_rn(dz, dz));
+}
+
+__device__ __forceinline__ unsigned lane_id() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%laneid;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier (shared::cta) and TMA bulk copies global -> shared.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
+                                                      unsigned bytes) {
+    asm volatile(
+        "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, at most `timeout_ns`.
+// Returns false if the bound ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar,
+                                                  unsigned parity,
+                                                  uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = global_timer_ns();
+    for (;;) {
+        #pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// 1-D bulk copy (TMA) of `bytes` bytes global -> shared, completing on `bar`
+// as transaction bytes.  dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src,
+                                         unsigned bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (for unaligned tile edges).
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+                 "l"(src)
+                 : "memory");
+}
+
+// Make `bar` track completion of this thread's prior cp.async operations
+// (the pending count is raised now and lowered when they land).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Thread block clusters.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ unsigned cluster_nctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared variable in cluster block `rank`.
+__device__ __forceinline__ uint32_t map_shared_rank(const void *p,
+                                                    unsigned rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(r)
+                 : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a,
+                                              uint32_t b, uint32_t c,
+                                              uint32_t d) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Full cluster barrier: every thread of every block of the cluster arrives
+// (release) and waits (acquire).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Global memory accesses with explicit memory-model semantics.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v)
+                 : "memory");
+}
+
+// Record the first device-side error in the library's status word.
+__device__ __forceinline__ void raise_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Warp reductions of (hi, lo) pairs in lexicographic order.
+// ---------------------------------------------------------------------------
+// Returns the largest hi over the warp and, among lanes holding it, the
+// smallest lo.
+__device__ __forceinline__ void warp_argmax_hi_min_lo(unsigned hi, unsigned lo,
+                                                      unsigned &best_hi,
+                                                      unsigned &best_lo) {
+    best_hi = __reduce_max_sync(0xffffffffu, hi);
+    best_lo = __reduce_min_sync(0xffffffffu, hi == best_hi ? lo : 0xffffffffu);
+}
+
+}  // namespace pcn

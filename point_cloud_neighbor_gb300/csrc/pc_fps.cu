@@ -1,0 +1,552 @@
+// pc_fps.cu -- farthest point sampling on sm_103a, all steps in one launch.
+//
+// Operator (mps-pointops project page, "Farthest point sampling" and
+// "Contracts"): c_0 = start_idx; m_j(t) = min_{u<=t} s(x_j, x_{c_u});
+// c_{t+1} = the smallest j attaining max_l m_l(t).
+//
+// Every point's coordinates and running minimum m_j stay in registers of the
+// thread that owns it for the whole launch (PPT points per thread), so a step
+// reads no memory except the new center.  Per step:
+//   1. each thread updates its m_j with the previous center and keeps its own
+//      (max m, smallest j) -- points are visited in increasing j, so a strict
+//      ">" keeps the smallest index on a tie;
+//   2. a warp reduces the key (bits(m) + 1, j) with two redux.sync
+//      instructions (max of the first half, then min j among the lanes that
+//      hold it); warp leaders publish to shared memory;
+//   3. warp 0 reduces the block's candidates and looks the winner's
+//      coordinates up in the block's shared-memory copy of its points;
+//   4. blocks of a cloud exchange their candidates:
+//      - BLOCK schedule (one block per cloud): nothing to exchange;
+//      - CLUSTER schedule (one thread block cluster per cloud): warp 0 writes
+//        the candidate (key, coordinates) into slot [step parity][its rank]
+//        of every block of the cluster through distributed shared memory,
+//        then one barrier.cluster; every warp then reduces the cluster's
+//        slots itself, so no further block barrier is needed.  Slots are
+//        double buffered by step parity, which makes one cluster barrier per
+//        step sufficient;
+//      - GRID schedule (cooperative launch, several blocks per cloud): each
+//        block writes one 64-bit word [bits(m)+1 : 31 | 2^24-1-j : 24 |
+//        step mod 512 : 9] into its slot of the caller's workspace; warp 0
+//        of every block polls the cloud's slots until all carry this step's
+//        tag, reduces them, and reads the winner's coordinates from the
+//        input.  Every wait is bounded (timeout -> status word, -1 outputs).
+// Points are (bits(m) + 1) so that a block without points (key 0) never
+// wins; once every m is 0 the smallest index, 0, wins, which reproduces
+// "remaining slots repeat index 0".
+#include "pc_device.cuh"
+#include "pc_internal.h"
+
+#include <algorithm>
+
+namespace pcn {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int FPS_MAX_THREADS = 1024;
+constexpr int FPS_MAX_PPT = 8;
+constexpr int FPS_MAX_CLUSTER = 16;
+constexpr int FPS_GRID_MAX_N = 1 << 24;  // index field of the exchange word
+
+struct FpsArgs {
+    const float *xyz;
+    int N, npoint, start;
+    int64_t *out;
+    int chunk;     // points per block
+    int nblocks;   // blocks per cloud (cluster size or grid blocks per cloud)
+    uint64_t *slots;
+    int *status;
+    uint64_t timeout_ns;
+    int stall;
+};
+
+struct __align__(16) ClusterSlot {
+    unsigned hi, j;
+    float x, y;
+    float z, pad0, pad1, pad2;
+};
+
+__host__ __device__ constexpr size_t fps_coords_bytes(int chunk) {
+    return (size_t(chunk) * 12 + 15) & ~size_t(15);
+}
+
+// Steps 1-3: update the owned points with center (cx, cy, cz), reduce the
+// block's (key, j) and return it in warp 0's lanes (other warps: undefined).
+template <int PPT>
+__device__ __forceinline__ void fps_local_step(float (&px)[PPT],
+                                               float (&py)[PPT],
+                                               float (&pz)[PPT],
+                                               float (&pm)[PPT], float cx,
+                                               float cy, float cz, int j_first,
+                                               int T, uint2 *wslot,
+                                               unsigned &bhi, unsigned &bj) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float best = -1.0f;
+    int bp = 0;
+#pragma unroll
+    for (int p = 0; p < PPT; ++p) {
+        const float s = sqdist(px[p], py[p], pz[p], cx, cy, cz);
+        pm[p] = fminf(pm[p], s);
+        if (pm[p] > best) {
+            best = pm[p];
+            bp = p;
+        }
+    }
+    const unsigned khi = best >= 0.0f ? __float_as_uint(best) + 1u : 0u;
+    const unsigned kj = khi ? unsigned(j_first + bp * T) : FULL;
+    unsigned whi, wj;
+    warp_argmax_hi_min_lo(khi, kj, whi, wj);
+    if (lane == 0) wslot[warp] = make_uint2(whi, wj);
+    __syncthreads();
+    if (warp == 0) {
+        const uint2 v = lane < (T >> 5) ? wslot[lane] : make_uint2(0u, FULL);
+        warp_argmax_hi_min_lo(v.x, v.y, bhi, bj);
+    }
+}
+
+template <int PPT>
+__device__ __forceinline__ void fps_load_points(const float *x, int lo, int hi,
+                                                int T, float (&px)[PPT],
+                                                float (&py)[PPT],
+                                                float (&pz)[PPT],
+                                                float (&pm)[PPT],
+                                                float *scoord) {
+#pragma unroll
+    for (int p = 0; p < PPT; ++p) {
+        const int j = lo + int(threadIdx.x) + p * T;
+        if (j < hi) {
+            px[p] = x[size_t(j) * 3 + 0];
+            py[p] = x[size_t(j) * 3 + 1];
+            pz[p] = x[size_t(j) * 3 + 2];
+            pm[p] = __int_as_float(0x7f800000);  // +inf: first min() gives s
+            if (scoord) {
+                scoord[(j - lo) * 3 + 0] = px[p];
+                scoord[(j - lo) * 3 + 1] = py[p];
+                scoord[(j - lo) * 3 + 2] = pz[p];
+            }
+        } else {
+            px[p] = py[p] = pz[p] = 0.0f;
+            pm[p] = -1.0f;  // no point: never the maximum
+        }
+    }
+}
+
+// BLOCK (CLUSTER == false, one block per cloud) and CLUSTER schedules.
+template <int PPT, bool CLUSTER>
+__global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
+    fps_cluster_kernel(const FpsArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *scoord = reinterpret_cast<float *>(smem);
+    uint2 *wslot = reinterpret_cast<uint2 *>(smem + fps_coords_bytes(a.chunk));
+    ClusterSlot *cslot = reinterpret_cast<ClusterSlot *>(
+        smem + fps_coords_bytes(a.chunk) + 32 * sizeof(uint2));
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int T = blockDim.x;
+    const unsigned rank = CLUSTER ? cluster_ctarank() : 0u;
+    const int b = blockIdx.x / a.nblocks;
+    const float *x = a.xyz + size_t(b) * size_t(a.N) * 3;
+    const int lo = int(rank) * a.chunk;
+    const int hi = min(a.N, lo + a.chunk);
+
+    float px[PPT], py[PPT], pz[PPT], pm[PPT];
+    fps_load_points<PPT>(x, lo, hi, T, px, py, pz, pm, scoord);
+    float cx = x[size_t(a.start) * 3 + 0];
+    float cy = x[size_t(a.start) * 3 + 1];
+    float cz = x[size_t(a.start) * 3 + 2];
+    int64_t *out = a.out + size_t(b) * a.npoint;
+    if (rank == 0 && threadIdx.x == 0) out[0] = a.start;
+    __syncthreads();
+    if (CLUSTER) cluster_sync_all();  // every block's slots exist before use
+
+    for (int t = 1; t < a.npoint; ++t) {
+        const int par = t & 1;
+        unsigned bhi, bj;
+        fps_local_step<PPT>(px, py, pz, pm, cx, cy, cz, lo + int(threadIdx.x),
+                            T, wslot, bhi, bj);
+        if (warp == 0) {
+            float wx = 0.f, wy = 0.f, wz = 0.f;
+            if (bhi) {
+                const float *c = scoord + (int(bj) - lo) * 3;
+                wx = c[0];
+                wy = c[1];
+                wz = c[2];
+            }
+            ClusterSlot *mine = &cslot[par * FPS_MAX_CLUSTER + rank];
+            if (CLUSTER) {
+                if (lane < a.nblocks) {
+                    const uint32_t ra = map_shared_rank(mine, unsigned(lane));
+                    st_cluster_v4(ra, bhi, bj, __float_as_uint(wx),
+                                  __float_as_uint(wy));
+                    st_cluster_v4(ra + 16, __float_as_uint(wz), 0u, 0u, 0u);
+                }
+            } else if (lane == 0) {
+                mine->hi = bhi;
+                mine->j = bj;
+                mine->x = wx;
+                mine->y = wy;
+                mine->z = wz;
+            }
+        }
+        if (CLUSTER)
+            cluster_sync_all();
+        else
+            __syncthreads();
+        // every warp reduces the cloud's candidates
+        const ClusterSlot *cs = &cslot[par * FPS_MAX_CLUSTER];
+        unsigned vhi = 0u, vj = FULL;
+        float vx = 0.f, vy = 0.f, vz = 0.f;
+        if (lane < a.nblocks) {
+            vhi = cs[lane].hi;
+            vj = cs[lane].j;
+            vx = cs[lane].x;
+            vy = cs[lane].y;
+            vz = cs[lane].z;
+        }
+        unsigned chi, cj;
+        warp_argmax_hi_min_lo(vhi, vj, chi, cj);
+        const int who = __ffs(__ballot_sync(FULL, vhi == chi && vj == cj)) - 1;
+        cx = __shfl_sync(FULL, vx, who);
+        cy = __shfl_sync(FULL, vy, who);
+        cz = __shfl_sync(FULL, vz, who);
+        if (rank == 0 && threadIdx.x == 0) out[t] = int64_t(cj);
+    }
+    if (CLUSTER) cluster_sync_all();  // no block exits while peers may write
+}
+
+// GRID schedule: cooperative launch, a.nblocks blocks per cloud.
+template <int PPT>
+__global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
+    fps_grid_kernel(const FpsArgs a) {
+    __shared__ uint2 wslot[32];
+    __shared__ float4 s_center;
+    __shared__ int s_fail;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int T = blockDim.x;
+    const int b = blockIdx.x / a.nblocks;
+    const int r = blockIdx.x % a.nblocks;
+    const float *x = a.xyz + size_t(b) * size_t(a.N) * 3;
+    const int lo = r * a.chunk;
+    const int hi = min(a.N, lo + a.chunk);
+    uint64_t *slots = a.slots + size_t(b) * 2 * a.nblocks;
+
+    float px[PPT], py[PPT], pz[PPT], pm[PPT];
+    fps_load_points<PPT>(x, lo, hi, T, px, py, pz, pm, nullptr);
+    float cx = x[size_t(a.start) * 3 + 0];
+    float cy = x[size_t(a.start) * 3 + 1];
+    float cz = x[size_t(a.start) * 3 + 2];
+    int64_t *out = a.out + size_t(b) * a.npoint;
+    if (r == 0 && threadIdx.x == 0) out[0] = a.start;
+    if (threadIdx.x == 0) s_fail = 0;
+
+    int t = 1;
+    for (; t < a.npoint; ++t) {
+        const int par = t & 1;
+        const unsigned tag = unsigned(t) & 511u;
+        unsigned bhi, bj;
+        fps_local_step<PPT>(px, py, pz, pm, cx, cy, cz, lo + int(threadIdx.x),
+                            T, wslot, bhi, bj);
+        if (warp == 0) {
+            uint64_t *ps = slots + size_t(par) * a.nblocks;
+            if (lane == 0 && !(a.stall && r == 0 && t == 1)) {
+                const uint64_t key =
+                    (uint64_t(bhi) << 33) |
+                    (uint64_t((FPS_GRID_MAX_N - 1) - (bhi ? bj : 0u)) << 9) |
+                    tag;
+                st_relaxed_gpu_u64(&ps[r], key);
+            }
+            // poll until every block of the cloud published this step
+            uint64_t best = 0;
+            bool ok = false;
+            const uint64_t t0 = global_timer_ns();
+            for (int spin = 0;; ++spin) {
+                bool mine_ok = true;
+                uint64_t m = 0;
+                for (int i = lane; i < a.nblocks; i += 32) {
+                    const uint64_t v = ld_relaxed_gpu_u64(&ps[i]);
+                    if ((v & 511u) != tag)
+                        mine_ok = false;
+                    else
+                        m = v > m ? v : m;
+                }
+                if (__all_sync(FULL, mine_ok)) {
+                    best = m;
+                    ok = true;
+                    break;
+                }
+                if ((spin & 63) == 63 &&
+                    global_timer_ns() - t0 > a.timeout_ns)
+                    break;
+            }
+            if (!ok) {
+                if (lane == 0) {
+                    s_fail = 1;
+                    raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
+                }
+            } else {
+                unsigned mhi, mlo;
+                warp_argmax_hi_min_lo(unsigned(best >> 32), 0u, mhi, mlo);
+                const unsigned lo32 = __reduce_max_sync(
+                    FULL, unsigned(best >> 32) == mhi ? unsigned(best) : 0u);
+                const uint64_t w = (uint64_t(mhi) << 32) | lo32;
+                const unsigned wj =
+                    (FPS_GRID_MAX_N - 1) - unsigned((w >> 9) & 0xffffffu);
+                if (lane == 0) {
+                    s_center = make_float4(x[size_t(wj) * 3 + 0],
+                                           x[size_t(wj) * 3 + 1],
+                                           x[size_t(wj) * 3 + 2],
+                                           __int_as_float(int(wj)));
+                    if (r == 0) out[t] = int64_t(wj);
+                }
+            }
+        }
+        __syncthreads();
+        if (s_fail) break;
+        const float4 c = s_center;
+        cx = c.x;
+        cy = c.y;
+        cz = c.z;
+        __syncthreads();  // s_center is rewritten next step
+    }
+    if (s_fail && r == 0) {
+        for (int i = t + int(threadIdx.x); i < a.npoint; i += T) out[i] = -1;
+    }
+}
+
+template <int PPT>
+const void *cluster_kernel_ptr(bool cluster) {
+    return cluster ? reinterpret_cast<const void *>(&fps_cluster_kernel<PPT, true>)
+                   : reinterpret_cast<const void *>(&fps_cluster_kernel<PPT, false>);
+}
+
+const void *fps_kernel_ptr(int strategy, int ppt) {
+    const bool cl = strategy == 2;
+    if (strategy == 3) {
+        switch (ppt) {
+            case 1: return reinterpret_cast<const void *>(&fps_grid_kernel<1>);
+            case 2: return reinterpret_cast<const void *>(&fps_grid_kernel<2>);
+            case 4: return reinterpret_cast<const void *>(&fps_grid_kernel<4>);
+            case 6: return reinterpret_cast<const void *>(&fps_grid_kernel<6>);
+            default: return reinterpret_cast<const void *>(&fps_grid_kernel<8>);
+        }
+    }
+    switch (ppt) {
+        case 1: return cluster_kernel_ptr<1>(cl);
+        case 2: return cluster_kernel_ptr<2>(cl);
+        case 4: return cluster_kernel_ptr<4>(cl);
+        case 6: return cluster_kernel_ptr<6>(cl);
+        default: return cluster_kernel_ptr<8>(cl);
+    }
+}
+
+int pick_ppt(int chunk) {
+    for (int p : {1, 2, 4, 6, 8})
+        if (chunk <= FPS_MAX_THREADS * p) return p;
+    return 0;
+}
+
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+bool cluster_fits(const DeviceInfo &dev, int cs, int threads, size_t smem,
+                  int ppt) {
+    // cudaOccupancyMaxActiveClusters: can at least one cluster of `cs` blocks
+    // of this kernel be resident at once?
+    const void *fn = fps_kernel_ptr(2, ppt);
+    if (cs > 8 &&
+        cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                             1) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(smem)) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(cs));
+    cfg.blockDim = dim3(unsigned(threads));
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return n >= 1;
+}
+
+size_t cluster_smem(int chunk) {
+    return fps_coords_bytes(chunk) + 32 * sizeof(uint2) +
+           2 * FPS_MAX_CLUSTER * sizeof(ClusterSlot);
+}
+
+}  // namespace
+
+FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
+                 int cluster_size, int blocks_per_cloud) {
+    FpsPlan p;
+    const int64_t cap_block = int64_t(FPS_MAX_THREADS) * FPS_MAX_PPT;
+    const int nsm = std::max(1, dev.sm_count);
+    if (strategy == 0) {  // automatic
+        if (N <= 2048 || (B >= nsm / 2 && N <= cap_block))
+            strategy = 1;
+        else if (N <= cap_block * FPS_MAX_CLUSTER)
+            strategy = 2;
+        else
+            strategy = 3;
+    }
+    p.strategy = strategy;
+    if (strategy == 1 || strategy == 2) {
+        int cs = 1;
+        if (strategy == 2) {
+            if (cluster_size > 0) {
+                cs = cluster_size;
+            } else {
+                cs = 1;
+                while (cs < FPS_MAX_CLUSTER && int64_t(cs) * cap_block < N) cs *= 2;
+                while (cs < FPS_MAX_CLUSTER && B * (cs * 2) <= nsm &&
+                       N / (cs * 2) >= 1024)
+                    cs *= 2;
+            }
+            if (cs < 1 || cs > FPS_MAX_CLUSTER) {
+                p.why = "cluster size must be 1..16";
+                return p;
+            }
+        }
+        p.cluster = cs;
+        p.blocks_per_cloud = cs;
+        p.chunk = int((N + cs - 1) / cs);
+        p.ppt = pick_ppt(p.chunk);
+        if (p.ppt == 0) {
+            p.why = "cloud too large for one block/cluster schedule";
+            return p;
+        }
+        p.threads = std::max(32, round_up((p.chunk + p.ppt - 1) / p.ppt, 32));
+        p.smem_bytes = cluster_smem(p.chunk);
+        if (p.smem_bytes > dev.smem_per_block_optin) {
+            p.why = "block's share of the cloud exceeds shared memory";
+            return p;
+        }
+        if (strategy == 2 && !cluster_fits(dev, cs, p.threads, p.smem_bytes, p.ppt)) {
+            if (cluster_size > 0 || cs <= 8) {
+                p.why = "cluster of this size cannot be resident on this device";
+                return p;
+            }
+            // 16-block clusters unavailable: retry with 8 or the grid schedule
+            if (N <= cap_block * 8)
+                return plan_fps(dev, B, N, 2, 8, 0);
+            return plan_fps(dev, B, N, 3, 0, 0);
+        }
+        p.ok = true;
+        return p;
+    }
+    if (strategy == 3) {
+        if (N >= FPS_GRID_MAX_N) {
+            p.why = "grid schedule supports N < 2^24";
+            return p;
+        }
+        if (!dev.cooperative) {
+            p.why = "device has no cooperative launch";
+            return p;
+        }
+        int bpc = blocks_per_cloud;
+        if (bpc <= 0) bpc = int(std::max<int64_t>(1, nsm / std::max<int64_t>(B, 1)));
+        bpc = int(std::min<int64_t>(bpc, N));
+        if (int64_t(bpc) * B > nsm) {
+            p.why = "grid schedule needs blocks_per_cloud * B <= SM count";
+            return p;
+        }
+        p.blocks_per_cloud = bpc;
+        p.cluster = 1;
+        p.chunk = int((N + bpc - 1) / bpc);
+        p.ppt = pick_ppt(p.chunk);
+        if (p.ppt == 0) {
+            p.why = "cloud too large for the on-chip FPS schedules";
+            return p;
+        }
+        p.threads = std::max(32, round_up((p.chunk + p.ppt - 1) / p.ppt, 32));
+        p.smem_bytes = 0;
+        p.workspace_bytes = (size_t(B) * 2 * bpc * sizeof(uint64_t) + 255) & ~size_t(255);
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm, fps_kernel_ptr(3, p.ppt), p.threads, 0) != cudaSuccess) {
+            cudaGetLastError();
+            p.why = "occupancy query failed";
+            return p;
+        }
+        if (int64_t(per_sm) * nsm < int64_t(bpc) * B) {
+            p.why = "grid schedule blocks cannot all be resident";
+            return p;
+        }
+        p.ok = true;
+        return p;
+    }
+    p.why = "unknown FPS strategy";
+    return p;
+}
+
+cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
+                       const float *xyz, int64_t B, int64_t N, int64_t npoint,
+                       int64_t start_idx, int64_t *out_idx, void *workspace,
+                       cudaStream_t stream) {
+    (void)dev;
+    FpsArgs a{};
+    a.xyz = xyz;
+    a.N = int(N);
+    a.npoint = int(npoint);
+    a.start = int(start_idx);
+    a.out = out_idx;
+    a.chunk = plan.chunk;
+    a.nblocks = plan.blocks_per_cloud;
+    a.slots = static_cast<uint64_t *>(workspace);
+    a.status = dev.status_word;
+    a.timeout_ns = wait_timeout_ns();
+    a.stall = plan.strategy == 3 ? fps_grid_stall() : 0;
+
+    const void *fn = fps_kernel_ptr(plan.strategy, plan.ppt);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(B * plan.blocks_per_cloud));
+    cfg.blockDim = dim3(unsigned(plan.threads));
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    cudaError_t e;
+    if (plan.strategy == 3) {
+        e = cudaMemsetAsync(workspace, 0, plan.workspace_bytes, stream);
+        if (e != cudaSuccess) return e;
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.numAttrs = 1;
+    } else {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(plan.smem_bytes));
+        if (e != cudaSuccess) return e;
+        if (plan.strategy == 2) {
+            if (plan.cluster > 8) {
+                e = cudaFuncSetAttribute(
+                    fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = unsigned(plan.cluster);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.numAttrs = 1;
+        }
+    }
+    void *args[] = {&a};
+    e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace pcn

@@ -1,0 +1,72 @@
+// pc_internal.h -- host-side declarations shared by the launchers and the C
+// ABI (not installed; the public interface is include/pointcloud.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pcn {
+
+// Cached properties of one device, filled once per device.
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+    int warp_size = 0;
+    size_t smem_per_block_optin = 0;
+    size_t smem_per_sm = 0;
+    int max_threads_per_sm = 0;
+    int cooperative = 0;
+    int *status_word = nullptr;  // device address of the status word
+};
+
+// Device-side wait bound, in ns (see pc_set_wait_timeout_ns).
+uint64_t wait_timeout_ns();
+// Testing hook for the FPS grid exchange (see pc_debug_set_fps_grid_stall).
+int fps_grid_stall();
+
+// Launch plans --------------------------------------------------------------
+struct ScanPlan {       // kNN / Ball Query
+    int warps = 8;      // warps per block
+    int q_per_warp = 1; // queries per warp
+    int blocks_per_cloud = 1;
+    int ntiles = 0;     // reference tiles per cloud
+    int tile_stride = 1;
+    size_t smem_bytes = 0;
+};
+
+// Launchers: enqueue on `stream`, return the first CUDA error.
+cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
+                       int64_t Q, const float *ref, int64_t N, int k,
+                       float *out_dist, int64_t *out_idx, cudaStream_t stream);
+
+cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
+                              int64_t B, int64_t Q, const float *ref,
+                              int64_t N, float r32, int64_t K,
+                              float *out_dist2, int64_t *out_idx,
+                              cudaStream_t stream);
+
+struct FpsPlan {
+    int strategy = 0;       // PC_FPS_BLOCK / CLUSTER / GRID
+    int cluster = 1;        // blocks per cluster (BLOCK: 1)
+    int blocks_per_cloud = 1;
+    int threads = 1024;
+    int ppt = 1;            // points per thread
+    int chunk = 0;          // points per block
+    size_t smem_bytes = 0;
+    size_t workspace_bytes = 0;
+    bool ok = false;
+    const char *why = "";
+};
+
+FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
+                 int cluster_size, int blocks_per_cloud);
+
+cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
+                       const float *xyz, int64_t B, int64_t N, int64_t npoint,
+                       int64_t start_idx, int64_t *out_idx, void *workspace,
+                       cudaStream_t stream);
+
+}  // namespace pcn
