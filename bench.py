@@ -1,0 +1,528 @@
+"""Benchmark: one step = FPS + kNN + Ball Query on the 100k-point workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Workload (the single-large-cloud configuration): B=1, N=100,000 points from a
+mixture of 64 isotropic Gaussians (sigma 0.05, means uniform in [0,1)^3),
+random order.  One step runs, on inputs already resident in device memory:
+  * farthest point sampling of 4,096 centers from index 0,
+  * kNN with k=16 of all 100,000 points against all 100,000,
+  * Ball Query r=0.02, K=32 of all 100,000 points against all 100,000.
+Headline ``value``: (kNN queries + Ball Query queries) per second of whole
+steps (FPS time included in the step time); per-operator throughputs
+(queries/s, samples/s) and roofline fractions are in ``ops``.
+
+Timing: W untimed warm-up steps, then K steps, each preceded by an L2 flush
+(a 512 MiB device write outside the timed events) and bracketed by CUDA
+events on the launching stream; a barrier + synchronize brackets the whole
+timed loop; the max over ranks is reported.  With N > 1 (torchrun) every rank
+runs its own replica of the workload on its own GPU (the three operators
+have no cross-GPU exchange step): value = N * units / max time, scaling
+"weak".
+
+``--impl reference`` times the CPU oracle (the plain restatement of the
+operator definitions that the parity tests use) on the host cores, on a
+bounded sample of the same workload per step, and reports the same metric
+extrapolated to the full step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "kNN & Ball Query queries/s, FPS samples/s at 100k pts; % of FP32/HBM roofline"
+UNIT = "queries/s"
+WORKLOAD = dict(name="large", B=1, N=100_000, npoint=4096, start_idx=0,
+                knn_k=16, bq_radius=0.02, bq_K=32, order="random")
+FLOPS_PER_PAIR = 8          # 3 sub + 3 mul + 2 add per (query, reference) pair
+FPS_BYTES_PER_POINT_STEP = 20  # 12 B coordinates + 4 B min read + 4 B write
+L2_FLUSH_BYTES = 512 << 20
+
+
+def workload_config(extra=None):
+    cfg = {
+        "workload": ("single large cloud: B=1, N=100000 fp32 points, mixture of "
+                     "64 Gaussians (sigma 0.05), random order; FPS npoint=4096 "
+                     "start 0; kNN k=16, 100000 queries vs 100000; Ball Query "
+                     "r=0.02 K=32, 100000 queries vs 100000"),
+        "B": 1, "N": 100000, "fps_npoint": 4096, "knn_k": 16, "knn_queries": 100000,
+        "bq_radius": 0.02, "bq_K": 32, "bq_queries": 100000, "seed": 3,
+        "l2": "flushed between timed steps (512 MiB device write outside the events)",
+    }
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (torchrun: one rank per GPU)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of a list of floats over all ranks."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# GPU clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.lines:
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# roofline inputs
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_alu_peak_tflops(sm_count: int, mhz: float) -> float:
+    """FP32 CUDA-core peak counting an FMA as 2 flops: SMs x 128 lanes x 2 x clock."""
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def kernel_source_hash(name: str) -> str:
+    src = os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc", name)
+    h = hashlib.sha256()
+    for f in (src, os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
+                                "pc_device.cuh"),
+              os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
+                           "pc_tiles.cuh")):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(op: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {"knn": "pc_knn.cu", "ball_query": "pc_ball_query.cu",
+           "fps": "pc_fps.cu"}[op]
+    want = kernel_source_hash(src)
+    for line in open(path):
+        kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
+        if kv.get("op") == op and kv.get("src_sha256") == want:
+            try:
+                return float(kv["dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        init_dist(world, "nccl")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+
+    import point_cloud_neighbor_gb300 as pc
+    from point_cloud_neighbor_gb300 import inputs
+
+    W = WORKLOAD
+    x_host = inputs.large(seed=3, morton=False)        # [1, N, 3] float32
+    x = torch.from_numpy(x_host).to(device)
+    B, N = 1, W["N"]
+    npoint, k, r, K = W["npoint"], W["knn_k"], W["bq_radius"], W["bq_K"]
+    stream = torch.cuda.current_stream(device)
+
+    fps_out = torch.empty((B, npoint), dtype=torch.int64, device=device)
+    knn_d = torch.empty((B, N, k), dtype=torch.float32, device=device)
+    knn_i = torch.empty((B, N, k), dtype=torch.int64, device=device)
+    bq_d = torch.empty((B, N, K), dtype=torch.float32, device=device)
+    bq_i = torch.empty((B, N, K), dtype=torch.int64, device=device)
+    ws_bytes = pc.binding.lib().pc_fps_workspace_bytes(B, N, npoint)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        pc.pc_fps(x, npoint, 0, out=fps_out, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+        pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
+        if ev is not None:
+            ev[2].record(stream)
+        pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    assert pc.pc_device_status(reset=True, device=device) == 0
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+              for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    with ClockSampler(device.index if world == 1 else local) as clocks:
+        for s in range(args.steps):
+            flush.zero_()
+            step(events[s])
+        torch.cuda.synchronize(device)
+    wall1 = time.perf_counter()
+    barrier(world)
+    launches = 3 * args.steps
+
+    t_fps = [e[0].elapsed_time(e[1]) for e in events]
+    t_knn = [e[1].elapsed_time(e[2]) for e in events]
+    t_bq = [e[2].elapsed_time(e[3]) for e in events]
+    total_ms = sum(e[0].elapsed_time(e[3]) for e in events)
+    total_ms, fps_ms, knn_ms, bq_ms = max_over_ranks(
+        [total_ms, sum(t_fps), sum(t_knn), sum(t_bq)], world, device)
+    ms_per_step = total_ms / args.steps
+    units = (N + N) * world               # kNN + Ball Query queries, all ranks
+    value = units / (ms_per_step / 1e3)
+
+    # algorithmic work of each launch
+    bq_idx = bq_i.cpu().numpy().reshape(N, K)
+    last = bq_idx[:, K - 1]
+    bq_pairs = float(np.where(last >= 0, last + 1, N).sum())   # first-K scan length
+    knn_pairs = float(N) * float(N)
+    fps_bytes = float(N) * (npoint - 1) * FPS_BYTES_PER_POINT_STEP
+
+    peaks, peak_kind = measured_peaks()
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    clk = clocks.summary()
+    max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = fp32_alu_peak_tflops(sm_count, max_mhz)
+    hbm_peak = float(peaks["hbm_gbs"])
+
+    per = {
+        "fps": fps_ms / args.steps, "knn": knn_ms / args.steps,
+        "ball_query": bq_ms / args.steps,
+    }
+    ops = {
+        "fps": {
+            "samples_per_s": npoint * world / (per["fps"] / 1e3),
+            "ms": per["fps"],
+            "algorithmic_bytes": fps_bytes,
+            "achieved_gbs": fps_bytes / (per["fps"] / 1e3) / 1e9,
+            "hbm_frac": fps_bytes / (per["fps"] / 1e3) / 1e9 / hbm_peak,
+            "us_per_sample": per["fps"] * 1e3 / (npoint - 1),
+        },
+        "knn": {
+            "queries_per_s": N * world / (per["knn"] / 1e3),
+            "ms": per["knn"], "pairs": knn_pairs,
+            "achieved_tflops": knn_pairs * FLOPS_PER_PAIR / (per["knn"] / 1e3) / 1e12,
+        },
+        "ball_query": {
+            "queries_per_s": N * world / (per["ball_query"] / 1e3),
+            "ms": per["ball_query"], "pairs": bq_pairs,
+            "achieved_tflops": bq_pairs * FLOPS_PER_PAIR / (per["ball_query"] / 1e3) / 1e12,
+        },
+    }
+    for op in ("knn", "ball_query"):
+        ops[op]["alu_frac_max_clock"] = ops[op]["achieved_tflops"] / alu_peak
+        if clk["sm_mhz"]:
+            ops[op]["alu_frac_load_clock"] = (
+                ops[op]["achieved_tflops"] / fp32_alu_peak_tflops(sm_count, clk["sm_mhz"]))
+
+    dominant = max(per, key=per.get)
+    if dominant == "fps":
+        roof = {"bound": "hbm", "achieved": ops["fps"]["achieved_gbs"],
+                "peak": hbm_peak, "unit": "GB/s",
+                "frac": ops["fps"]["achieved_gbs"] / hbm_peak}
+        traffic = recorded_traffic("fps")
+    else:
+        roof = {"bound": "alu", "achieved": ops[dominant]["achieved_tflops"],
+                "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": ops[dominant]["achieved_tflops"] / alu_peak}
+        traffic = recorded_traffic(dominant)
+    roof["traffic"] = traffic
+    roof["kernel"] = dominant
+    roof["peak_source"] = (f"FP32 CUDA cores: {sm_count} SMs x 128 x 2 flop x "
+                           f"{max_mhz:.0f} MHz ({peak_kind} max SM clock)"
+                           if roof["bound"] == "alu" else
+                           f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})")
+
+    # end to end through the public API: pinned host in, pinned host out
+    e2e = run_e2e(args, pc, x_host, device, world)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": workload_config({"parallelism": f"replicas x{world}"}),
+        "roofline": roof, "ops": ops, "e2e": e2e, "gpu_launches": launches,
+        "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
+                   "reasons": clk["reasons"], "samples": clk["samples"]},
+        "wall_s_timed_loop": wall1 - wall0,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(x_host, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, pc, x_host, device, world):
+    """Same step through the public API with host buffers: the input is copied
+    from pinned host memory each step and every result is read back into
+    pinned host memory; wall time around each synchronized step."""
+    import torch
+    W = WORKLOAD
+    N, npoint, k, r, K = W["N"], W["npoint"], W["knn_k"], W["bq_radius"], W["bq_K"]
+    x_pin = torch.from_numpy(x_host).pin_memory()
+    outs = {
+        "fps": torch.empty((1, npoint), dtype=torch.int64).pin_memory(),
+        "knn_d": torch.empty((1, N, k), dtype=torch.float32).pin_memory(),
+        "knn_i": torch.empty((1, N, k), dtype=torch.int64).pin_memory(),
+        "bq_d": torch.empty((1, N, K), dtype=torch.float32).pin_memory(),
+        "bq_i": torch.empty((1, N, K), dtype=torch.int64).pin_memory(),
+    }
+    h2d = x_pin.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def one():
+        xd = x_pin.to(device, non_blocking=True)
+        f = pc.pc_fps(xd, npoint, 0)
+        d, i = pc.pc_knn(xd, xd, k)
+        d2, i2 = pc.pc_ball_query(xd, xd, r, K)
+        outs["fps"].copy_(f, non_blocking=True)
+        outs["knn_d"].copy_(d, non_blocking=True)
+        outs["knn_i"].copy_(i, non_blocking=True)
+        outs["bq_d"].copy_(d2, non_blocking=True)
+        outs["bq_i"].copy_(i2, non_blocking=True)
+        torch.cuda.synchronize(device)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    steps = max(3, min(args.steps, 20))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    t1 = time.perf_counter()
+    (elapsed,) = max_over_ranks([t1 - t0], world, device)
+    value = (N + N) * world * steps / elapsed
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": elapsed / steps * 1e3,
+            "note": "pinned host input copied in and all outputs read back every step"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timings (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step_costs(x_host, knn_rows, bq_rows, fps_steps, threads, seed=0):
+    """Seconds per kNN query, per Ball Query query and per FPS sample of the
+    oracle, measured on bounded samples of the workload."""
+    import oracle
+    oracle.build()
+    W = WORKLOAD
+    N = W["N"]
+    rng = np.random.default_rng(seed)
+    rk = np.sort(rng.choice(N, knn_rows, replace=False)).astype(np.int64)
+    rb = np.sort(rng.choice(N, bq_rows, replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.knn(x_host, x_host, W["knn_k"], rows=rk, threads=threads)
+    t1 = time.perf_counter()
+    oracle.ball_query(x_host, x_host, W["bq_radius"], W["bq_K"], rows=rb,
+                      threads=threads)
+    t2 = time.perf_counter()
+    oracle.fps(x_host, fps_steps + 1, 0)
+    t3 = time.perf_counter()
+    return {"knn_s_per_query": (t1 - t0) / knn_rows,
+            "bq_s_per_query": (t2 - t1) / bq_rows,
+            "fps_s_per_sample": (t3 - t2) / fps_steps,
+            "knn_rows": knn_rows, "bq_rows": bq_rows, "fps_steps": fps_steps,
+            "elapsed_s": t3 - t0}
+
+
+def extrapolated_step_s(c):
+    W = WORKLOAD
+    return (c["knn_s_per_query"] * W["N"] + c["bq_s_per_query"] * W["N"] +
+            c["fps_s_per_sample"] * (W["npoint"] - 1))
+
+
+def cpu_baseline(x_host, budget_s=20.0):
+    threads = os.cpu_count() or 1
+    # calibrate sample sizes so the whole leg takes about budget_s
+    probe = oracle_step_costs(x_host, knn_rows=threads, bq_rows=16 * threads,
+                              fps_steps=16, threads=threads)
+    share = budget_s / 3.0
+    knn_rows = int(max(threads, min(4096, share / max(probe["knn_s_per_query"], 1e-9))))
+    bq_rows = int(max(threads, min(100000, share / max(probe["bq_s_per_query"], 1e-9))))
+    fps_steps = int(max(8, min(4095, share / max(probe["fps_s_per_sample"], 1e-9))))
+    c = oracle_step_costs(x_host, knn_rows, bq_rows, fps_steps, threads, seed=1)
+    step_s = extrapolated_step_s(c)
+    return {"value": 2 * WORKLOAD["N"] / step_s, "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": (f"{knn_rows} kNN queries and {bq_rows} Ball Query queries "
+                       f"on {threads} threads, {fps_steps} FPS samples on 1 thread "
+                       f"(FPS is sequential), extrapolated to the full step"),
+            "step_s_extrapolated": step_s, "measured_s": c["elapsed_s"],
+            "per_unit_s": {k: c[k] for k in ("knn_s_per_query", "bq_s_per_query",
+                                             "fps_s_per_sample")}}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return   # the CPU oracle runs once, on rank 0
+    from point_cloud_neighbor_gb300 import inputs
+    x_host = inputs.large(seed=3, morton=False)
+    threads = os.cpu_count() or 1
+    knn_rows, bq_rows, fps_steps = 2 * threads, 64 * threads, 16
+    for _ in range(args.warmup):
+        oracle_step_costs(x_host, knn_rows, bq_rows, fps_steps, threads, seed=99)
+    costs = [oracle_step_costs(x_host, knn_rows, bq_rows, fps_steps, threads,
+                               seed=s) for s in range(args.steps)]
+    agg = {k: statistics.mean(c[k] for c in costs)
+           for k in ("knn_s_per_query", "bq_s_per_query", "fps_s_per_sample")}
+    step_s = extrapolated_step_s(agg)
+    value = 2 * WORKLOAD["N"] / step_s
+    sample = (f"per step {knn_rows} kNN queries and {bq_rows} Ball Query queries "
+              f"on {threads} threads and {fps_steps} FPS samples on 1 thread, "
+              f"extrapolated to the full step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config({"parallelism": "host cores, oracle"}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+        "per_unit_s": agg,
+    }))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle work for the cpu_baseline leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

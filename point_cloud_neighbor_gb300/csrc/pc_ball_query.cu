@@ -47,6 +47,7 @@ struct BqArgs {
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
+    float negzero;  // -0.0f, see sq2_rn
 };
 
 __host__ __device__ constexpr size_t bq_fixed_smem() {
@@ -58,6 +59,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
     const int G = a.q_per_warp;
     const int q_warp0 = (blockIdx.x * BQ_WARPS + warp) * G;
     const int nq = max(0, min(G, a.Q - q_warp0));
@@ -142,7 +144,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             bool any = false;
 #pragma unroll
             for (int p = 0; p < BQ_R / 2; ++p) {
-                const float2 sv = sqdist2(rx[p], ry[p], rz[p], nx, ny, nz);
+                const float2 sv = sqdist2(rx[p], ry[p], rz[p], nx, ny, nz, nz0);
                 s[2 * p] = sv.x;
                 s[2 * p + 1] = sv.y;
                 any |= (sv.x < a.R2) | (sv.y < a.R2);
@@ -211,6 +213,7 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
+    a.negzero = -0.0f;
 
     const int slots = dev.sm_count * 2;
     const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));

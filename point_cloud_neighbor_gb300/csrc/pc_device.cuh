@@ -23,17 +23,52 @@ __device__ __forceinline__ float sqdist(float ax, float ay, float az,
                      __fmul_rn(dz, dz));
 }
 
+// Packed f32x2 arithmetic in PTX.  add2_rn is one round-to-nearest-even
+// addition per half.  Squares are NOT written as mul.rn.f32x2: ptxas fuses a
+// single-use packed multiply into the packed add that consumes it (an FMA,
+// one rounding instead of two) even with an explicit .rn modifier and
+// --fmad=false.  A square is therefore computed as fma.rn.f32x2(d, d, z) with
+// z = (-0, -0) supplied at run time: d*d + (-0) is exactly d*d (also for a
+// zero product, +0 + -0 = +0), so the FMA returns RN(d*d), the same float as
+// a separately rounded multiply; and since the addend is not a compile-time
+// constant the compiler cannot rewrite the FMA into a fusable multiply.
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// RN(a * a) per half; `negzero` must hold (-0.0f, -0.0f) at run time.
+__device__ __forceinline__ float2 sq2_rn(float2 a, float2 negzero) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rz, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rz, {%4, %5};\n\t"
+        "fma.rn.f32x2 rd, ra, ra, rz;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(negzero.x), "f"(negzero.y));
+    return d;
+}
+
 // Two references (packed in the .x/.y halves) against one point whose
 // coordinates are given NEGATED: d = x + (-q) is the same float as -(q - x)
 // under round-to-nearest-even, and the square removes the sign, so each half
-// equals sqdist() bit for bit.  One packed f32x2 instruction per operation.
+// equals sqdist() bit for bit: ((dx*dx + dy*dy) + dz*dz), five roundings.
 __device__ __forceinline__ float2 sqdist2(float2 x, float2 y, float2 z,
-                                          float2 nqx, float2 nqy, float2 nqz) {
-    float2 dx = __fadd2_rn(x, nqx);
-    float2 dy = __fadd2_rn(y, nqy);
-    float2 dz = __fadd2_rn(z, nqz);
-    return __fadd2_rn(__fadd2_rn(__fmul2_rn(dx, dx), __fmul2_rn(dy, dy)),
-                      __fmul2_rn(dz, dz));
+                                          float2 nqx, float2 nqy, float2 nqz,
+                                          float2 negzero) {
+    const float2 dx = add2_rn(x, nqx);
+    const float2 dy = add2_rn(y, nqy);
+    const float2 dz = add2_rn(z, nqz);
+    return add2_rn(add2_rn(sq2_rn(dx, negzero), sq2_rn(dy, negzero)),
+                   sq2_rn(dz, negzero));
 }
 
 __device__ __forceinline__ unsigned lane_id() {

@@ -53,6 +53,7 @@ struct KnnArgs {
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
+    float negzero;  // -0.0f, see sq2_rn
 };
 
 __host__ __device__ constexpr size_t knn_fixed_smem() {
@@ -161,6 +162,7 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
     const int G = a.q_per_warp;
     const int q_warp0 = (blockIdx.x * KNN_WARPS + warp) * G;
     const int nq = max(0, min(G, a.Q - q_warp0));
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
             bool any = false;
 #pragma unroll
             for (int p = 0; p < KNN_R / 2; ++p) {
-                const float2 sv = sqdist2(rx[p], ry[p], rz[p], nx, ny, nz);
+                const float2 sv = sqdist2(rx[p], ry[p], rz[p], nx, ny, nz, nz0);
                 s[2 * p] = sv.x;
                 s[2 * p + 1] = sv.y;
                 any |= (sv.x <= q.w) | (sv.y <= q.w);
@@ -354,6 +356,7 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
+    a.negzero = -0.0f;
     if (k <= 32) return launch_knn_t<1>(dev, a, B, Q, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
     if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);

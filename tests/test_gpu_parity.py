@@ -332,6 +332,18 @@ def test_ball_query_edge_sizes(B, Q, N, r, K):
     check_bq(q, x, r, K, what=f"bq B={B} Q={Q} N={N} r={r} K={K}")
 
 
+@pytest.mark.parametrize("B,Q,N", [(1, 100, 2000), (3, 57, 1333)])
+def test_random_coordinates_bit_exact(B, Q, N):
+    """Non-grid coordinates: every operation rounds, so any difference in the
+    arithmetic (contraction, rounding mode, flushing) shows in the distances."""
+    x = inputs.random_cloud(500 + N, B, N)
+    q = inputs.random_cloud(600 + Q, B, Q)
+    check_knn(q, x, 24, what="knn random coordinates")
+    check_bq(q, x, 0.45, 48, what="bq random coordinates")
+    idx = gpu_fps(x, 200, 1)
+    assert_idx_equal(idx, oracle.fps(x, 200, 1), "fps random coordinates")
+
+
 def test_ball_query_large_radius_early_exit():
     x = inputs.random_cloud(5, 2, 20000)
     q = inputs.random_cloud(6, 2, 500)
