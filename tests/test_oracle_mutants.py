@@ -56,6 +56,7 @@ PIN_FUNCTIONS = [
     (pins.test_knn_duplicate_ties_go_to_smaller_index, {}),
     (pins.test_fps_line_matches_interval_bisection, {"n": 23, "start": 7}),
     (pins.test_fps_matches_brute_force, {"seed": 1, "grid": 1 / 4}),
+    (pins.test_ball_query_scan_length, {}),
 ]
 
 

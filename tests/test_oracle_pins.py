@@ -417,3 +417,19 @@ def test_fps_rejects_bad_start(oracle_mod):
     x = inputs.random_cloud(0, 1, 4)
     with pytest.raises(ValueError):
         oracle_mod.fps(x, 2, 4)
+
+
+def test_ball_query_scan_length(oracle_mod):
+    """Pairs the first-K rule examines: the K-th accepted index + 1, else N
+    (exact s32 and numpy nonzero, independent of the oracle's scan)."""
+    x = inputs.random_cloud(31, 2, 60, grid=1 / 8)
+    q = inputs.random_cloud(32, 2, 9, grid=1 / 8)
+    r, K = 0.7, 5
+    R2 = round_f32(F(np.float32(r)) * F(np.float32(r)))
+    got = oracle_mod.ball_query_scan_len(q, x, r, K)
+    for b in range(2):
+        for i in range(9):
+            s = np.array([s32_exact(q[b, i], x[b, j]) for j in range(60)], np.float32)
+            hits = np.nonzero(s < R2)[0]
+            want = hits[K - 1] + 1 if len(hits) >= K else 60
+            assert got[b * 9 + i] == want
