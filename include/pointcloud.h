@@ -123,6 +123,32 @@ size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
                                  int strategy, int blocks_per_cloud);
 
 /*
+ * pc_fps_grid_static: pc_fps with the PC_FPS_GRID schedule for callers that
+ * cannot allocate device memory at call time (for instance a host program
+ * that has given all device memory to its own pool, so cudaMalloc would fail
+ * or break its accounting, or a real-time loop with a fixed footprint).  The
+ * mps-pointops pages have no counterpart of this entry point.
+ *
+ * The grid schedule's exchange scratch is a fixed array of 4096 64-bit words
+ * (32 KiB) inside the library, present on every device that loads the
+ * library until the process exits; the call allocates nothing.  Limit: the
+ * schedule needs 2 * blocks_per_cloud * B words, so B * blocks_per_cloud
+ * must not exceed 2048 (it is also bounded by the SM count); larger requests
+ * return PC_ERR_INVALID_ARGUMENT.  Arguments and results are those of
+ * pc_fps_ex with strategy PC_FPS_GRID (blocks_per_cloud 0 = automatic).
+ *
+ * The first call on a device (while it is current) looks up the array's
+ * device address with cudaGetSymbolAddress; make that first call before any
+ * stream capture.  Every call on a device uses the same array, and each call
+ * clears the words it needs (stream-ordered) before its kernel.  Calls whose
+ * work may overlap on the GPU (different streams without ordering between
+ * them) race on the array and must not be issued.
+ */
+int pc_fps_grid_static(const float *xyz, int64_t B, int64_t N, int64_t npoint,
+                       int64_t start_idx, int64_t *out_idx,
+                       int blocks_per_cloud, void *stream);
+
+/*
  * k nearest neighbors.
  * Project page, "k nearest neighbors": for each query, candidates sorted by
  * (s, j) -- squared distance, then reference index -- and the first k

@@ -44,6 +44,8 @@ _SIGNATURES = {
                                  ctypes.c_int, ctypes.c_int, ctypes.c_int, _P]),
     "pc_fps_workspace_bytes_ex": (ctypes.c_size_t, [_I, _I, _I, ctypes.c_int,
                                                     ctypes.c_int]),
+    "pc_fps_grid_static": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, ctypes.c_int,
+                                          _P]),
     "pc_knn": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _P, _P, _P]),
     "pc_ball_query": (ctypes.c_int, [_P, _I, _I, _P, _I, ctypes.c_double, _I,
                                      _P, _P, _P]),

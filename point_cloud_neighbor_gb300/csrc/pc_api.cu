@@ -128,6 +128,11 @@ bool mul_ok(int64_t a, int64_t b, int64_t c) {
 namespace pcn {
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 int fps_grid_stall() { return g_fps_stall.load(); }
+int api_current_device(const DeviceInfo **out) { return current_device(out); }
+int api_check_ptr(const void *p, int dev, size_t align, const char *name) {
+    return check_ptr(p, dev, align, name);
+}
+int api_fail(int code, const char *message) { return fail(code, "%s", message); }
 }  // namespace pcn
 
 extern "C" {

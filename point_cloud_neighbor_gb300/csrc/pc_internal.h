@@ -27,6 +27,12 @@ uint64_t wait_timeout_ns();
 // Testing hook for the FPS grid exchange (see pc_debug_set_fps_grid_stall).
 int fps_grid_stall();
 
+// Device resolution, pointer checks and error messages of the C ABI, for
+// entry points defined outside pc_api.cu.
+int api_current_device(const DeviceInfo **out);
+int api_check_ptr(const void *p, int dev, size_t align, const char *name);
+int api_fail(int code, const char *message);
+
 // Launch plans --------------------------------------------------------------
 struct ScanPlan {       // kNN / Ball Query
     int warps = 8;      // warps per block
