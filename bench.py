@@ -371,6 +371,33 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_only(args):
+    """One operator of the step on the workload, W untimed + K timed calls."""
+    import torch
+    import point_cloud_neighbor_gb300 as pc
+    from point_cloud_neighbor_gb300 import inputs
+    W = WORKLOAD
+    device = torch.device("cuda", 0)
+    x = torch.from_numpy(inputs.large(seed=3, morton=False)).to(device)
+    calls = {
+        "fps": lambda: pc.pc_fps(x, W["npoint"], 0),
+        "knn": lambda: pc.pc_knn(x, x, W["knn_k"]),
+        "ball_query": lambda: pc.pc_ball_query(x, x, W["bq_radius"], W["bq_K"]),
+    }
+    fn = calls[args.only]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize(device)
+    print(json.dumps({"op": args.only, "ms": e0.elapsed_time(e1) / args.steps,
+                      "calls": args.steps}))
+
+
 def run_e2e(args, pc, x_host, device, world):
     """Same step through the public API with host buffers: the input is copied
     from pinned host memory each step and every result is read back into
@@ -515,11 +542,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["fps", "knn", "ball_query"],
+                    help="run one operator of the step W + K times and print "
+                         "its mean CUDA-event time (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_gpu(args)
 
