@@ -7,19 +7,28 @@
 // distances, unused slots hold (-1, 0).
 //
 // Design (one launch, no scratch memory):
-//  * A block of BQ_WARPS warps owns BQ_WARPS * G queries of one cloud; a warp
-//    owns G of them, kept in shared memory as float4 (x, y, z, hits so far).
-//  * Reference tiles of BQ_T = 32 * BQ_R points are staged into shared memory
-//    by TMA bulk copies (double buffered) strictly in input order, then held
-//    in registers: lane l holds tile points l + 32 r, so for each r the warp
-//    holds 32 consecutive references in lane order.
+//  * A block has BQ_CWARPS consumer warps and one producer warp.  Consumer
+//    warp w owns G queries of one cloud, kept in shared memory negated and
+//    duplicated for the packed instructions, (-x,-x,-y,-y) and
+//    (-z,-z,hits,query).
+//  * The producer's lane 0 streams reference tiles of BQ_T = 32 * BQ_R points
+//    strictly in input order through a BQ_STAGES ring (TMA bulk copies,
+//    full/empty mbarriers); consumer warps copy a tile into registers (lane l
+//    holds tile points l + 32 r, so for each r the warp holds 32 consecutive
+//    references in lane order), release it and compute.
 //  * Per (query, tile) each lane evaluates BQ_R distances with packed f32x2
-//    instructions and one warp vote asks whether any is inside the radius.
-//    Only then, per r, a ballot gives the hits of those 32 consecutive
-//    references and __popc(ballot & lanemask_lt) gives each hit its rank, so
-//    a hit is written straight to slot (hits so far + rank) -- input order is
-//    kept without any sort.  A query stops at K hits; the block stops reading
-//    tiles when all of its queries are full.
+//    instructions and one vote asks whether any is inside the radius; no
+//    distance stays live past the vote, so the hot loop is only the packed
+//    arithmetic, the compares and the vote.  On a hit (rare) the slow path
+//    recomputes the distances and, per r, a ballot gives the hits among 32
+//    consecutive references and __popc(ballot & lanemask_lt) gives each hit
+//    its rank, so a hit is written straight to slot (hits so far + rank):
+//    input order is kept without any sort.
+//  * A query stops at K hits: it is swapped behind the still-active queries
+//    of its warp, so the hot loop tests nothing per query.  When every query
+//    of a block is full, a stop flag ends the block: the producer stops
+//    issuing tiles (after letting its copies in flight land) and the
+//    consumers leave the tile loop.
 #include "pc_device.cuh"
 #include "pc_internal.h"
 #include "pc_tiles.cuh"
@@ -31,8 +40,9 @@ namespace {
 
 constexpr int BQ_R = 8;
 constexpr int BQ_T = 32 * BQ_R;
-constexpr int BQ_WARPS = 8;
-constexpr int BQ_THREADS = 32 * BQ_WARPS;
+constexpr int BQ_CWARPS = 8;
+constexpr int BQ_THREADS = 32 * (BQ_CWARPS + 1);
+constexpr int BQ_STAGES = 4;
 constexpr unsigned FULL = 0xffffffffu;
 
 struct BqArgs {
@@ -50,8 +60,55 @@ struct BqArgs {
     float negzero;  // -0.0f, see sq2_rn
 };
 
+struct __align__(16) BqSlot {
+    float4 nxy;  // (-x, -x, -y, -y)
+    float4 nzh;  // (-z, -z, hits so far (int bits), query index in warp (int bits))
+};
+
+constexpr unsigned BQ_BUF = tile_buffer_bytes(BQ_T);
+
 __host__ __device__ constexpr size_t bq_fixed_smem() {
-    return 2 * size_t(tile_buffer_bytes(BQ_T)) + 32;
+    // ring, 2 * STAGES mbarriers, flags (error, stop, warps done)
+    return size_t(BQ_STAGES) * BQ_BUF + 2 * BQ_STAGES * 8 + 16;
+}
+
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+
+// Slow path, taken only when a vote found a hit: recompute the tile's
+// distances for this query and record the hits in input order.  Returns the
+// new hit count (<= K).
+__device__ __forceinline__ int bq_record(const float2 (&rx)[BQ_R / 2],
+                                         const float2 (&ry)[BQ_R / 2],
+                                         const float2 (&rz)[BQ_R / 2],
+                                         const BqSlot q, float2 nz0, int hits,
+                                         int j0, int cnt, float R2, int K,
+                                         size_t row, float *out_dist2,
+                                         int64_t *out_idx) {
+    const int lane = static_cast<int>(lane_id());
+    float s[BQ_R];
+#pragma unroll
+    for (int p = 0; p < BQ_R / 2; ++p) {
+        const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy), hi2(q.nxy),
+                                 lo2(q.nzh), nz0);
+        s[2 * p] = v.x;
+        s[2 * p + 1] = v.y;
+    }
+#pragma unroll
+    for (int r = 0; r < BQ_R; ++r) {
+        const bool hit = (r * 32 + lane < cnt) && s[r] < R2;
+        const unsigned bal = __ballot_sync(FULL, hit);
+        if (bal) {
+            const int pos = hits + __popc(bal & lanemask_lt());
+            if (hit && pos < K) {
+                out_idx[row * K + pos] = j0 + r * 32 + lane;
+                out_dist2[row * K + pos] = s[r];
+            }
+            hits += __popc(bal);
+            if (hits >= K) break;
+        }
+    }
+    return min(hits, K);
 }
 
 __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
@@ -59,56 +116,80 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
-    const float2 nz0 = make_float2(a.negzero, a.negzero);
     const int G = a.q_per_warp;
-    const int q_warp0 = (blockIdx.x * BQ_WARPS + warp) * G;
-    const int nq = max(0, min(G, a.Q - q_warp0));
     const int K = a.K;
 
-    constexpr unsigned BUF = tile_buffer_bytes(BQ_T);
-    // tile buffer of stage st: smem + st * BUF
-    auto tbuf = [&](int st) { return reinterpret_cast<float *>(smem + st * BUF); };
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * BUF);
-    int *s_err = reinterpret_cast<int *>(smem + 2 * BUF + 16);
-    float4 *qst = reinterpret_cast<float4 *>(smem + bq_fixed_smem()) + warp * G;
+    TileRing ring;
+    ring.base = smem;
+    ring.bytes = BQ_BUF;
+    ring.full = reinterpret_cast<uint64_t *>(smem + BQ_STAGES * BQ_BUF);
+    ring.empty = ring.full + BQ_STAGES;
+    int *s_err = reinterpret_cast<int *>(ring.empty + BQ_STAGES);
+    int *s_stop = s_err + 1;
+    int *s_ndone = s_err + 2;
+    BqSlot *slots_all = reinterpret_cast<BqSlot *>(smem + bq_fixed_smem());
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
-    const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int s = 0; s < BQ_STAGES; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], BQ_CWARPS);
+        }
         *s_err = 0;
+        *s_stop = 0;
+        *s_ndone = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int g = lane; g < G; g += 32) {
-        float4 v = make_float4(0.f, 0.f, 0.f, __int_as_float(0));
-        if (g < nq) {
-            const float *p = cq + size_t(q_warp0 + g) * 3;
-            v.x = p[0];
-            v.y = p[1];
-            v.z = p[2];
-        }
-        qst[g] = v;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int it = 0; it < 2 && it < a.ntiles; ++it) {
-            const int j0 = it * BQ_T;
-            issue_tile(tbuf(it), cref + size_t(j0) * 3, min(BQ_T, a.N - j0),
-                       &bars[it]);
-        }
+
+    if (warp == BQ_CWARPS) {  // producer warp
+        __syncthreads();
+        if (lane == 0)
+            ring_produce<BQ_STAGES>(
+                ring, cref, a.N, BQ_T, a.ntiles, [](int it) { return it; },
+                s_stop, s_err, a.timeout_ns);
+        return;
     }
 
-    int ndone = 0;  // queries of this warp holding K hits
-    int failed_it = -1, stop_it = a.ntiles;
+    const int q_warp0 = (blockIdx.x * BQ_CWARPS + warp) * G;
+    const int nq = max(0, min(G, a.Q - q_warp0));
+    BqSlot *slots = slots_all + warp * G;
+    const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
+    for (int g = lane; g < G; g += 32) {
+        float x = 0.f, y = 0.f, z = 0.f;
+        if (g < nq) {
+            const float *p = cq + size_t(q_warp0 + g) * 3;
+            x = p[0];
+            y = p[1];
+            z = p[2];
+        }
+        slots[g].nxy = make_float4(-x, -x, -y, -y);
+        slots[g].nzh = make_float4(-z, -z, __int_as_float(0), __int_as_float(g));
+    }
+    __syncthreads();
+
+    // Queries still short of K hits occupy slots [0, active); a query that
+    // fills up is swapped behind them, so the hot loop checks nothing per
+    // query.
+    volatile int *vstop = s_stop;
+    int active = nq;
+    if (active == 0 && lane == 0 && atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS)
+        *vstop = 1;
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
+    bool failed = false;
     for (int it = 0; it < a.ntiles; ++it) {
-        const int st = it & 1;
-        const unsigned par = (it >> 1) & 1;
-        if (!mbar_wait_bounded(&bars[st], par, a.timeout_ns)) *s_err = 1;
+        if (__any_sync(FULL, *vstop != 0)) break;
+        const int st = it % BQ_STAGES;
+        const WaitResult w = mbar_wait_or_stop(
+            &ring.full[st], unsigned((it / BQ_STAGES) & 1), s_stop, a.timeout_ns);
+        if (!__all_sync(FULL, w == WAIT_OK)) {
+            failed = !__all_sync(FULL, w != WAIT_TIMEOUT);
+            break;
+        }
         const int j0 = it * BQ_T;
         const int cnt = min(BQ_T, a.N - j0);
-        const float *buf = tbuf(st) + tile_float_offset(cref + size_t(j0) * 3);
+        const float *buf =
+            ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
         float2 rx[BQ_R / 2], ry[BQ_R / 2], rz[BQ_R / 2];
 #pragma unroll
         for (int p = 0; p < BQ_R / 2; ++p) {
@@ -118,75 +199,68 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             ry[p] = make_float2(p0[1], p1[1]);
             rz[p] = make_float2(p0[2], p1[2]);
         }
-        // buffer `st` fully read; stop when every query of the block is full
-        const bool all_done = __syncthreads_and(ndone == nq);
-        if (*s_err) {
-            failed_it = it;
-            break;
-        }
-        if (all_done) {
-            stop_it = it;
-            break;
-        }
-        if (threadIdx.x == 0 && it + 2 < a.ntiles) {
-            const int j2 = (it + 2) * BQ_T;
-            issue_tile(tbuf(st), cref + size_t(j2) * 3, min(BQ_T, a.N - j2),
-                       &bars[st]);
-        }
-        for (int g = 0; g < nq; ++g) {
-            const float4 q = qst[g];
-            int hits = __float_as_int(q.w);
-            if (hits >= K) continue;
-            const float2 nx = make_float2(-q.x, -q.x);
-            const float2 ny = make_float2(-q.y, -q.y);
-            const float2 nz = make_float2(-q.z, -q.z);
-            float s[BQ_R];
-            bool any = false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[st]);
+        if (active == 0) continue;  // keep the ring moving
+
+        bool any_full = false;
+        BqSlot *sp = slots;
+        BqSlot *const send = slots + active;
+        for (; sp < send; ++sp) {
+            const BqSlot q = *sp;
+            bool t = false;
 #pragma unroll
             for (int p = 0; p < BQ_R / 2; ++p) {
-                const float2 sv = sqdist2(rx[p], ry[p], rz[p], nx, ny, nz, nz0);
-                s[2 * p] = sv.x;
-                s[2 * p + 1] = sv.y;
-                any |= (sv.x < a.R2) | (sv.y < a.R2);
+                const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy),
+                                         hi2(q.nxy), lo2(q.nzh), nz0);
+                t |= (v.x < a.R2) | (v.y < a.R2);
             }
-            if (!__any_sync(FULL, any)) continue;
-            const size_t row = size_t(b) * a.Q + q_warp0 + g;
-#pragma unroll
-            for (int r = 0; r < BQ_R; ++r) {
-                const bool hit = (r * 32 + lane < cnt) && s[r] < a.R2;
-                const unsigned bal = __ballot_sync(FULL, hit);
-                if (bal) {
-                    const int pos = hits + __popc(bal & lanemask_lt());
-                    if (hit && pos < K) {
-                        a.out_idx[row * K + pos] = j0 + r * 32 + lane;
-                        a.out_dist2[row * K + pos] = s[r];
+            if (__any_sync(FULL, t)) {
+                const size_t row =
+                    size_t(b) * a.Q + q_warp0 + __float_as_int(q.nzh.w);
+                const int h = bq_record(rx, ry, rz, q, nz0,
+                                        __float_as_int(q.nzh.z), j0, cnt,
+                                        a.R2, K, row, a.out_dist2, a.out_idx);
+                if (lane == 0) sp->nzh.z = __int_as_float(h);
+                any_full |= h >= K;
+            }
+        }
+        if (any_full) {  // rare: move full queries behind the active ones
+            __syncwarp();
+            if (lane == 0) {
+                int g = 0;
+                while (g < active) {
+                    if (__float_as_int(slots[g].nzh.z) >= K) {
+                        const BqSlot t = slots[g];
+                        slots[g] = slots[active - 1];
+                        slots[active - 1] = t;
+                        --active;
+                    } else {
+                        ++g;
                     }
-                    hits += __popc(bal);
-                    if (hits >= K) break;
                 }
             }
-            hits = min(hits, K);
-            if (lane == 0) qst[g].w = __int_as_float(hits);
-            if (hits >= K) ++ndone;
+            active = __shfl_sync(FULL, active, 0);
+            __syncwarp();
+            if (active == 0 && lane == 0 &&
+                atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS)
+                *vstop = 1;
         }
     }
 
-    if (threadIdx.x == 0) {
-        // let copies still in flight land before the block's shared memory is
-        // released: after a stop at tile `it`, tile it + 1 may be in flight
-        // (tile it + 2 was never issued)
-        const int from = failed_it >= 0 ? failed_it : stop_it;
-        for (int it = from; it < from + 2 && it < a.ntiles; ++it)
-            if (it > from || failed_it >= 0)
-                mbar_wait_bounded(&bars[it & 1], (it >> 1) & 1, a.timeout_ns);
+    if (failed) {
+        if (lane == 0) {
+            *s_err = 1;
+            *vstop = 1;
+        }
+        raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
     }
-    if (failed_it >= 0) raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
-
-    // pad the unused slots with (-1, 0)
+    // pad the unused slots with (-1, 0); after a failure every slot
     __syncwarp();
     for (int g = 0; g < nq; ++g) {
-        const size_t row = size_t(b) * a.Q + q_warp0 + g;
-        const int hits = failed_it >= 0 ? 0 : __float_as_int(qst[g].w);
+        const BqSlot q = slots[g];
+        const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(q.nzh.w);
+        const int hits = failed ? 0 : __float_as_int(q.nzh.z);
         for (int e = hits + lane; e < K; e += 32) {
             a.out_idx[row * K + e] = -1;
             a.out_dist2[row * K + e] = 0.0f;
@@ -217,15 +291,15 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
 
     const int slots = dev.sm_count * 2;
     const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));
-    int64_t G = (Q + BQ_WARPS * bpc_target - 1) / (BQ_WARPS * bpc_target);
+    int64_t G = (Q + BQ_CWARPS * bpc_target - 1) / (BQ_CWARPS * bpc_target);
     const size_t budget =
         std::min<size_t>(dev.smem_per_block_optin, dev.smem_per_sm / 2 - 2048);
     const int64_t gmax = std::max<int64_t>(
-        1, int64_t((budget - bq_fixed_smem()) / (BQ_WARPS * sizeof(float4))));
+        1, int64_t((budget - bq_fixed_smem()) / (BQ_CWARPS * sizeof(BqSlot))));
     G = std::max<int64_t>(1, std::min(G, gmax));
     a.q_per_warp = static_cast<int>(G);
-    const int64_t bpc = (Q + BQ_WARPS * G - 1) / (BQ_WARPS * G);
-    const size_t smem = bq_fixed_smem() + size_t(BQ_WARPS) * G * sizeof(float4);
+    const int64_t bpc = (Q + BQ_CWARPS * G - 1) / (BQ_CWARPS * G);
+    const size_t smem = bq_fixed_smem() + size_t(BQ_CWARPS) * G * sizeof(BqSlot);
     cudaError_t e = cudaFuncSetAttribute(
         bq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));

@@ -123,6 +123,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Wait for phase `parity` of `bar` to complete, at most `timeout_ns`.
 // Returns false if the bound ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar,

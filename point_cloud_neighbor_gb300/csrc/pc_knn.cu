@@ -6,27 +6,32 @@
 // D = sqrt(s).
 //
 // Design (one launch, no scratch memory):
-//  * A block of KNN_WARPS warps owns KNN_WARPS * G queries of one cloud; each
-//    warp owns G of them.  The warp's queries live in shared memory as
-//    float4 (x, y, z, tau) where tau is the query's current k-th squared
-//    distance.
-//  * Reference tiles of KNN_T = 32 * KNN_R points are staged into shared
-//    memory by TMA bulk copies (double buffered, mbarrier completion) and
-//    then held in registers: lane l holds tile points l + 32 r, r < KNN_R,
-//    packed in pairs for the f32x2 distance instructions.
-//  * For each (query, tile) a lane evaluates KNN_R distances (4 packed
-//    instructions per pair of references), compares them with tau and one
-//    warp vote decides whether any lane has a candidate.  Candidates are rare
-//    once a query's list is full.
-//  * Each query's sorted list of 32 * KPL (s, j) entries is spread over the
-//    warp (lane l holds entries l, l + 32, ...).  A candidate is inserted with
-//    one ballot per 32 entries for its rank and a shuffle shift; the order is
-//    the lexicographic (s, j) order, so the result does not depend on the
-//    order in which tiles are visited.
+//  * A block has KNN_CWARPS consumer warps and one producer warp.  Consumer
+//    warp w owns G queries of one cloud.  Per query, shared memory holds the
+//    coordinates negated and duplicated for the packed instructions,
+//    (-x,-x,-y,-y) and (-z,-z,tau,tau), where tau is the query's current k-th
+//    squared distance, and the query's sorted list of k (s, j) entries.
+//  * The producer's lane 0 streams reference tiles of KNN_T = 32 * KNN_R
+//    points through a KNN_STAGES ring in shared memory with TMA bulk copies
+//    (full/empty mbarriers, see TileRing); consumer warps copy a tile into
+//    registers (lane l holds points l + 32 r, packed in pairs), release it
+//    and compute, drifting freely instead of meeting at a block barrier.
+//  * Per (query, tile) a lane evaluates KNN_R distances with packed f32x2
+//    instructions and compares them with the query's tau; one vote decides
+//    whether the warp inserts.  No distance stays live past the vote, so the
+//    hot loop is only the packed arithmetic, the compares and the vote.
+//    Candidates are rare once a list is full.
+//  * Insertion (slow path) recomputes the tile's distances for the query;
+//    each lane builds a bitmask of its candidate slots and parks its
+//    distances in a per-warp scratch row; the warp walks the candidates
+//    and inserts each into the warp-distributed list (lane l holds entries l,
+//    l + 32, ...): one ballot per 32 entries gives the rank, a shuffle shift
+//    makes room.  The order is the lexicographic (s, j) order, so the result
+//    does not depend on the order in which candidates or tiles are visited.
 //  * Tiles are visited in a scrambled order (stride ~0.618 * tiles, coprime
 //    with the tile count) so that spatially sorted inputs do not feed each
 //    query a stream of ever-closer candidates (the project page's kNN kernel
-//    notes reports a 6-8x slowdown from storage order on sorted input).
+//    notes report a 6-8x slowdown from storage order on sorted input).
 #include "pc_device.cuh"
 #include "pc_internal.h"
 #include "pc_tiles.cuh"
@@ -37,10 +42,11 @@
 namespace pcn {
 namespace {
 
-constexpr int KNN_R = 8;               // reference points per lane per tile
-constexpr int KNN_T = 32 * KNN_R;      // reference points per tile
-constexpr int KNN_WARPS = 8;           // warps per block
-constexpr int KNN_THREADS = 32 * KNN_WARPS;
+constexpr int KNN_R = 8;                  // reference points per lane per tile
+constexpr int KNN_T = 32 * KNN_R;         // reference points per tile
+constexpr int KNN_CWARPS = 8;             // consumer warps per block
+constexpr int KNN_THREADS = 32 * (KNN_CWARPS + 1);
+constexpr int KNN_STAGES = 4;
 constexpr unsigned FULL = 0xffffffffu;
 
 struct KnnArgs {
@@ -56,14 +62,32 @@ struct KnnArgs {
     float negzero;  // -0.0f, see sq2_rn
 };
 
+// One query in shared memory: coordinates negated and duplicated so that the
+// halves are packed operands, plus the filter threshold tau (twice).
+struct __align__(16) QuerySlot {
+    float4 nxy;  // (-x, -x, -y, -y)
+    float4 nzt;  // (-z, -z, tau, tau)
+};
+
+constexpr unsigned KNN_BUF = tile_buffer_bytes(KNN_T);
+
 __host__ __device__ constexpr size_t knn_fixed_smem() {
-    return 2 * size_t(tile_buffer_bytes(KNN_T)) + 32;
+    // ring, 2 * STAGES mbarriers, error flag, per-warp candidate scratch
+    return size_t(KNN_STAGES) * KNN_BUF + 2 * KNN_STAGES * 8 + 16 +
+           size_t(KNN_CWARPS) * 32 * KNN_R * sizeof(float);
+}
+
+__host__ __device__ constexpr size_t knn_per_query_smem(int k) {
+    return sizeof(QuerySlot) + size_t(k) * (sizeof(float) + sizeof(int));
 }
 
 __device__ __forceinline__ int knn_tile_at(const KnnArgs &a, int it) {
     return static_cast<int>((static_cast<long long>(it) * a.tile_stride) %
                             a.ntiles);
 }
+
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
 
 // Entry k-1 of the warp-distributed list: (s, j) broadcast to every lane.
 template <int KPL>
@@ -83,35 +107,59 @@ __device__ __forceinline__ void list_kth(const float (&ls)[KPL],
     tj = __shfl_sync(FULL, vj, kl);
 }
 
-// Insert every candidate of this tile into the query's list.  s[r] is this
-// lane's squared distance to tile point r*32 + lane; j0 the tile's first
-// index; cnt the number of valid points in the tile.  Warp-uniform.
+// Insert this tile's candidates for one query (warp-uniform).  The tile's
+// points are in rx/ry/rz (lane l: points l + 32 r); j0 is the tile's first
+// index and cnt its number of valid points.
 template <int KPL>
-__device__ __forceinline__ void knn_insert(const float (&s)[KNN_R], int j0,
-                                        int cnt, int k, float *ls_sm,
-                                        int *lj_sm, float *tau_sm) {
+__device__ __forceinline__ void knn_insert(const float2 (&rx)[KNN_R / 2],
+                                           const float2 (&ry)[KNN_R / 2],
+                                           const float2 (&rz)[KNN_R / 2],
+                                           float2 nz0, int j0, int cnt, int k,
+                                           QuerySlot *qs, float *ls_sm,
+                                           int *lj_sm, float *scratch) {
     const int lane = static_cast<int>(lane_id());
+    const QuerySlot q = *qs;
+    const float tau0 = q.nzt.z;
+    // the fast path keeps no distance live past its vote: recompute them
+    float s[KNN_R];
+#pragma unroll
+    for (int p = 0; p < KNN_R / 2; ++p) {
+        const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy), hi2(q.nxy),
+                                 lo2(q.nzt), nz0);
+        s[2 * p] = v.x;
+        s[2 * p + 1] = v.y;
+    }
+    unsigned m = 0;
+#pragma unroll
+    for (int r = 0; r < KNN_R; ++r)
+        if (r * 32 + lane < cnt && s[r] <= tau0) m |= 1u << r;
+    if (m) {
+        float4 *row = reinterpret_cast<float4 *>(scratch + lane * KNN_R);
+        row[0] = make_float4(s[0], s[1], s[2], s[3]);
+        row[1] = make_float4(s[4], s[5], s[6], s[7]);
+    }
     float ls[KPL];
     int lj[KPL];
 #pragma unroll
     for (int c = 0; c < KPL; ++c) {
-        ls[c] = ls_sm[c * 32 + lane];
-        lj[c] = lj_sm[c * 32 + lane];
+        const int e = c * 32 + lane;
+        ls[c] = e < k ? ls_sm[e] : __int_as_float(0x7f800000);
+        lj[c] = e < k ? lj_sm[e] : INT_MAX;
     }
+    __syncwarp();
     float ts;
     int tj;
     list_kth<KPL>(ls, lj, k, ts, tj);
     bool changed = false;
-#pragma unroll
-    for (int r = 0; r < KNN_R; ++r) {
-        const int jr = j0 + r * 32 + lane;
-        const bool valid = r * 32 + lane < cnt;
-        const bool pass = valid && (s[r] < ts || (s[r] == ts && jr < tj));
-        unsigned bal = __ballot_sync(FULL, pass);
-        while (bal) {
-            const int src = __ffs(bal) - 1;
-            bal &= bal - 1;
-            const float cs = __shfl_sync(FULL, s[r], src);
+    unsigned bal = __ballot_sync(FULL, m != 0);
+    while (bal) {
+        const int src = __ffs(bal) - 1;
+        bal &= bal - 1;
+        unsigned mm = __shfl_sync(FULL, m, src);
+        while (mm) {
+            const int r = __ffs(mm) - 1;
+            mm &= mm - 1;
+            const float cs = scratch[src * KNN_R + r];
             const int cj = j0 + r * 32 + src;
             if (cs < ts || (cs == ts && cj < tj)) {
                 int pos = 0;
@@ -148,81 +196,103 @@ __device__ __forceinline__ void knn_insert(const float (&s)[KNN_R], int j0,
     if (changed) {
 #pragma unroll
         for (int c = 0; c < KPL; ++c) {
-            ls_sm[c * 32 + lane] = ls[c];
-            lj_sm[c * 32 + lane] = lj[c];
+            const int e = c * 32 + lane;
+            if (e < k) {
+                ls_sm[e] = ls[c];
+                lj_sm[e] = lj[c];
+            }
         }
-        if (lane == 0) *tau_sm = ts;
+        if (lane == 0) {
+            qs->nzt.z = ts;
+            qs->nzt.w = ts;
+        }
     }
+    __syncwarp();  // the scratch row is reused by the next insertion
 }
 
 template <int KPL>
 __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
-    constexpr int L = 32 * KPL;
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
-    const float2 nz0 = make_float2(a.negzero, a.negzero);
     const int G = a.q_per_warp;
-    const int q_warp0 = (blockIdx.x * KNN_WARPS + warp) * G;
-    const int nq = max(0, min(G, a.Q - q_warp0));
+    const int k = a.k;
 
-    constexpr unsigned BUF = tile_buffer_bytes(KNN_T);
-    // tile buffer of stage st: smem + st * BUF
-    auto tbuf = [&](int st) { return reinterpret_cast<float *>(smem + st * BUF); };
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * BUF);
-    int *s_err = reinterpret_cast<int *>(smem + 2 * BUF + 16);
-    float4 *q_all = reinterpret_cast<float4 *>(smem + knn_fixed_smem());
-    float *s_all = reinterpret_cast<float *>(q_all + KNN_WARPS * G);
-    int *j_all = reinterpret_cast<int *>(s_all + size_t(KNN_WARPS) * G * L);
-    float4 *qst = q_all + warp * G;
-    float *lst_s = s_all + size_t(warp) * G * L;
-    int *lst_j = j_all + size_t(warp) * G * L;
+    TileRing ring;
+    ring.base = smem;
+    ring.bytes = KNN_BUF;
+    ring.full = reinterpret_cast<uint64_t *>(smem + KNN_STAGES * KNN_BUF);
+    ring.empty = ring.full + KNN_STAGES;
+    int *s_err = reinterpret_cast<int *>(ring.empty + KNN_STAGES);
+    float *scratch_all = reinterpret_cast<float *>(
+        smem + KNN_STAGES * KNN_BUF + 2 * KNN_STAGES * 8 + 16);
+    QuerySlot *slots_all =
+        reinterpret_cast<QuerySlot *>(smem + knn_fixed_smem());
+    float *ls_all = reinterpret_cast<float *>(slots_all + KNN_CWARPS * G);
+    int *lj_all = reinterpret_cast<int *>(ls_all + size_t(KNN_CWARPS) * G * k);
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
-    const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int s = 0; s < KNN_STAGES; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], KNN_CWARPS);
+        }
         *s_err = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int g = 0; g < G; ++g) {
-        if (lane == 0) {
-            float4 v = make_float4(0.f, 0.f, 0.f, __int_as_float(0x7f800000));
-            if (g < nq) {
-                const float *p = cq + size_t(q_warp0 + g) * 3;
-                v.x = p[0];
-                v.y = p[1];
-                v.z = p[2];
-            }
-            qst[g] = v;
-        }
-        for (int e = lane; e < L; e += 32) {
-            lst_s[g * L + e] = __int_as_float(0x7f800000);
-            lst_j[g * L + e] = INT_MAX;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        for (int it = 0; it < 2 && it < a.ntiles; ++it) {
-            const int t = knn_tile_at(a, it);
-            const int j0 = t * KNN_T;
-            issue_tile(tbuf(it), cref + size_t(j0) * 3, min(KNN_T, a.N - j0),
-                       &bars[it]);
-        }
+
+    if (warp == KNN_CWARPS) {  // producer warp
+        __syncthreads();
+        if (lane == 0)
+            ring_produce<KNN_STAGES>(
+                ring, cref, a.N, KNN_T, a.ntiles,
+                [&](int it) { return knn_tile_at(a, it); }, s_err, s_err,
+                a.timeout_ns);
+        return;
     }
 
-    int failed_it = -1;
+    // consumer warp: set up this warp's queries and lists
+    const int q_warp0 = (blockIdx.x * KNN_CWARPS + warp) * G;
+    const int nq = max(0, min(G, a.Q - q_warp0));
+    QuerySlot *slots = slots_all + warp * G;
+    float *ls_w = ls_all + size_t(warp) * G * k;
+    int *lj_w = lj_all + size_t(warp) * G * k;
+    float *scratch = scratch_all + warp * 32 * KNN_R;
+    const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
+    const float inf = __int_as_float(0x7f800000);
+    for (int g = lane; g < G; g += 32) {
+        float x = 0.f, y = 0.f, z = 0.f;
+        if (g < nq) {
+            const float *p = cq + size_t(q_warp0 + g) * 3;
+            x = p[0];
+            y = p[1];
+            z = p[2];
+        }
+        slots[g].nxy = make_float4(-x, -x, -y, -y);
+        slots[g].nzt = make_float4(-z, -z, inf, inf);
+    }
+    for (int e = lane; e < G * k; e += 32) {
+        ls_w[e] = inf;
+        lj_w[e] = INT_MAX;
+    }
+    __syncthreads();
+
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
+    bool failed = false;
     for (int it = 0; it < a.ntiles; ++it) {
-        const int st = it & 1;
-        const unsigned par = (it >> 1) & 1;
-        if (!mbar_wait_bounded(&bars[st], par, a.timeout_ns)) *s_err = 1;
-        const int t = knn_tile_at(a, it);
-        const int j0 = t * KNN_T;
+        const int st = it % KNN_STAGES;
+        const WaitResult w = mbar_wait_or_stop(
+            &ring.full[st], unsigned((it / KNN_STAGES) & 1), s_err, a.timeout_ns);
+        if (!__all_sync(FULL, w == WAIT_OK)) {
+            failed = true;
+            break;
+        }
+        const int j0 = knn_tile_at(a, it) * KNN_T;
         const int cnt = min(KNN_T, a.N - j0);
-        const float *buf = tbuf(st) + tile_float_offset(cref + size_t(j0) * 3);
+        const float *buf =
+            ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
         float2 rx[KNN_R / 2], ry[KNN_R / 2], rz[KNN_R / 2];
 #pragma unroll
         for (int p = 0; p < KNN_R / 2; ++p) {
@@ -232,63 +302,41 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
             ry[p] = make_float2(p0[1], p1[1]);
             rz[p] = make_float2(p0[2], p1[2]);
         }
-        __syncthreads();  // buffer `st` fully read by every warp
-        if (*s_err) {
-            failed_it = it;
-            break;
-        }
-        if (threadIdx.x == 0 && it + 2 < a.ntiles) {
-            const int t2 = knn_tile_at(a, it + 2);
-            const int j2 = t2 * KNN_T;
-            issue_tile(tbuf(st), cref + size_t(j2) * 3, min(KNN_T, a.N - j2),
-                       &bars[st]);
-        }
-        float4 qn = nq > 0 ? qst[0] : make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int g = 0; g < nq; ++g) {
-            const float4 q = qn;
-            if (g + 1 < nq) qn = qst[g + 1];
-            const float2 nx = make_float2(-q.x, -q.x);
-            const float2 ny = make_float2(-q.y, -q.y);
-            const float2 nz = make_float2(-q.z, -q.z);
-            float s[KNN_R];
-            bool any = false;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[st]);
+
+        QuerySlot *sp = slots;
+        float *lsp = ls_w;
+        int *ljp = lj_w;
+        for (int g = 0; g < nq; ++g, ++sp, lsp += k, ljp += k) {
+            const QuerySlot q = *sp;
+            bool t = false;
 #pragma unroll
             for (int p = 0; p < KNN_R / 2; ++p) {
-                const float2 sv = sqdist2(rx[p], ry[p], rz[p], nx, ny, nz, nz0);
-                s[2 * p] = sv.x;
-                s[2 * p + 1] = sv.y;
-                any |= (sv.x <= q.w) | (sv.y <= q.w);
+                const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy),
+                                         hi2(q.nxy), lo2(q.nzt), nz0);
+                t |= (v.x <= q.nzt.z) | (v.y <= q.nzt.z);
             }
-            if (__any_sync(FULL, any))
-                knn_insert<KPL>(s, j0, cnt, a.k, lst_s + g * L, lst_j + g * L,
-                                &qst[g].w);
+            if (__any_sync(FULL, t))
+                knn_insert<KPL>(rx, ry, rz, nz0, j0, cnt, k, sp, lsp, ljp,
+                                scratch);
         }
     }
 
-    if (failed_it >= 0) {
+    if (failed) {
+        if (lane == 0) *s_err = 1;
         raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
-        if (threadIdx.x == 0) {
-            // let the copies still in flight (tiles failed_it, failed_it + 1)
-            // land before the block's shared memory is released
-            for (int it = failed_it; it < failed_it + 2 && it < a.ntiles; ++it)
-                mbar_wait_bounded(&bars[it & 1], (it >> 1) & 1, a.timeout_ns);
-        }
         for (int g = 0; g < nq; ++g) {
             const size_t row = size_t(b) * a.Q + q_warp0 + g;
-            for (int e = lane; e < a.k; e += 32) a.out_idx[row * a.k + e] = -1;
+            for (int e = lane; e < k; e += 32) a.out_idx[row * k + e] = -1;
         }
         return;
     }
-
     for (int g = 0; g < nq; ++g) {
         const size_t row = size_t(b) * a.Q + q_warp0 + g;
-#pragma unroll
-        for (int c = 0; c < KPL; ++c) {
-            const int e = c * 32 + lane;
-            if (e < a.k) {
-                a.out_idx[row * a.k + e] = lst_j[g * L + e];
-                a.out_dist[row * a.k + e] = __fsqrt_rn(lst_s[g * L + e]);
-            }
+        for (int e = lane; e < k; e += 32) {
+            a.out_idx[row * k + e] = lj_w[g * k + e];
+            a.out_dist[row * k + e] = __fsqrt_rn(ls_w[g * k + e]);
         }
     }
 }
@@ -315,20 +363,19 @@ template <int KPL>
 cudaError_t launch_knn_t(const DeviceInfo &dev, const KnnArgs &a0, int64_t B,
                          int64_t Q, cudaStream_t stream) {
     KnnArgs a = a0;
-    constexpr int L = 32 * KPL;
-    const size_t per_q = sizeof(float4) + size_t(L) * 8;
+    const size_t per_q = knn_per_query_smem(a.k);
     const int slots = dev.sm_count * 2;
     // queries per warp: spread B*Q over about one wave of 2 blocks per SM
     const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));
-    int64_t G = (Q + KNN_WARPS * bpc_target - 1) / (KNN_WARPS * bpc_target);
+    int64_t G = (Q + KNN_CWARPS * bpc_target - 1) / (KNN_CWARPS * bpc_target);
     const size_t budget =
         std::min<size_t>(dev.smem_per_block_optin, dev.smem_per_sm / 2 - 2048);
     const int64_t gmax = std::max<int64_t>(
-        1, int64_t((budget - knn_fixed_smem()) / (KNN_WARPS * per_q)));
+        1, int64_t((budget - knn_fixed_smem()) / (KNN_CWARPS * per_q)));
     G = std::max<int64_t>(1, std::min(G, gmax));
     a.q_per_warp = static_cast<int>(G);
-    const int64_t bpc = (Q + KNN_WARPS * G - 1) / (KNN_WARPS * G);
-    const size_t smem = knn_fixed_smem() + size_t(KNN_WARPS) * G * per_q;
+    const int64_t bpc = (Q + KNN_CWARPS * G - 1) / (KNN_CWARPS * G);
+    const size_t smem = knn_fixed_smem() + size_t(KNN_CWARPS) * G * per_q;
     cudaError_t e = cudaFuncSetAttribute(
         knn_kernel<KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));

@@ -53,4 +53,79 @@ __device__ __forceinline__ void issue_tile(float *buf, const float *gsrc,
         bulk_g2s(b + (a0 - base), reinterpret_cast<const void *>(a0), bulk, bar);
 }
 
+// ---------------------------------------------------------------------------
+// Ring of STAGES tile buffers shared by the consumer warps of a block and
+// filled by one producer thread.  full[s] (count 1 + transaction bytes)
+// completes when tile data has landed; empty[s] (count = consumer warps)
+// completes when every consumer warp has copied the tile into registers.
+// Consumers therefore drift freely by up to STAGES - 1 tiles instead of
+// meeting at a block barrier every tile.
+// ---------------------------------------------------------------------------
+struct TileRing {
+    unsigned char *base;  // STAGES buffers of `bytes` bytes, 16-byte aligned
+    unsigned bytes;
+    uint64_t *full;
+    uint64_t *empty;
+    __device__ __forceinline__ float *buf(int s) const {
+        return reinterpret_cast<float *>(base + size_t(s) * bytes);
+    }
+};
+
+// Status of a bounded wait that may also be told to stop.
+enum WaitResult { WAIT_OK = 0, WAIT_TIMEOUT = 1, WAIT_STOPPED = 2 };
+
+// Wait for phase `parity` of `bar`; give up when `*stop` becomes non-zero
+// (checked every 64 polls) or after timeout_ns.
+__device__ __forceinline__ WaitResult mbar_wait_or_stop(uint64_t *bar,
+                                                        unsigned parity,
+                                                        const volatile int *stop,
+                                                        uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return WAIT_OK;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return WAIT_OK;
+        if (stop && *stop) return WAIT_STOPPED;
+        if (global_timer_ns() - t0 > timeout_ns) return WAIT_TIMEOUT;
+    }
+}
+
+// Producer loop, run by ONE thread.  Tile `it` (it = 0..ntiles-1) covers
+// points [tile_at(it) * T, ...) of the cloud starting at `cref`.  Stops early
+// when `*stop` becomes non-zero; on a timeout it raises *err.  Before
+// returning it waits (bounded) until every copy it issued has landed, so no
+// copy is in flight when the block exits.
+template <int STAGES, class TileAt>
+__device__ __forceinline__ void ring_produce(const TileRing &ring,
+                                             const float *cref, int N, int T,
+                                             int ntiles, TileAt tile_at,
+                                             volatile int *stop,
+                                             volatile int *err,
+                                             uint64_t timeout_ns) {
+    int issued = 0;
+    for (int it = 0; it < ntiles; ++it) {
+        const int st = it % STAGES;
+        if (it >= STAGES) {
+            const WaitResult w = mbar_wait_or_stop(
+                &ring.empty[st], unsigned((it / STAGES - 1) & 1), stop,
+                timeout_ns);
+            if (w == WAIT_TIMEOUT) *err = 1;
+            if (w != WAIT_OK) break;
+        }
+        if (*stop || *err) break;
+        const int j0 = tile_at(it) * T;
+        issue_tile(ring.buf(st), cref + size_t(j0) * 3, min(T, N - j0),
+                   &ring.full[st]);
+        issued = it + 1;
+    }
+    for (int st = 0; st < STAGES; ++st) {
+        // last tile issued into stage st
+        const int last = issued - 1 - ((issued - 1 - st) % STAGES + STAGES) % STAGES;
+        if (issued > 0 && last >= 0 && last % STAGES == st)
+            mbar_wait_bounded(&ring.full[st], unsigned((last / STAGES) & 1),
+                              timeout_ns);
+    }
+}
+
 }  // namespace pcn
