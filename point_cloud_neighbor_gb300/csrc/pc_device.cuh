@@ -205,6 +205,56 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a,
                  : "memory");
 }
 
+// Asynchronous stores into another block's shared memory (distributed shared
+// memory) that signal completion as transaction bytes on an mbarrier in that
+// block.  Both addresses are shared::cluster addresses (map_shared_rank).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a,
+                                            uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 "
+        "[%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v,
+                                             uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 "
+        "[%0], %1, [%2];" ::"r"(addr),
+        "r"(v), "r"(bar)
+        : "memory");
+}
+
+// try_wait with cluster-scope acquire: data that other blocks of the cluster
+// delivered with st.async is visible once the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar,
+                                                      unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar,
+                                                          unsigned parity,
+                                                          uint64_t timeout_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
 // Full cluster barrier: every thread of every block of the cluster arrives
 // (release) and waits (acquire).
 __device__ __forceinline__ void cluster_sync_all() {

@@ -5,8 +5,10 @@
 // c_{t+1} = the smallest j attaining max_l m_l(t).
 //
 // Every point's coordinates and running minimum m_j stay in registers of the
-// thread that owns it for the whole launch (PPT points per thread), so a step
-// reads no memory except the new center.  Per step:
+// thread that owns it for the whole launch (PPT points per thread, packed in
+// pairs for the f32x2 instructions), so a step reads no memory except the new
+// center.  Few fat threads (about eight warps per block) keep the per-step
+// reductions and barriers short.  Per step:
 //   1. each thread updates its m_j with the previous center and keeps its own
 //      (max m, smallest j) -- points are visited in increasing j, so a strict
 //      ">" keeps the smallest index on a tie;
@@ -17,13 +19,15 @@
 //      coordinates up in the block's shared-memory copy of its points;
 //   4. blocks of a cloud exchange their candidates:
 //      - BLOCK schedule (one block per cloud): nothing to exchange;
-//      - CLUSTER schedule (one thread block cluster per cloud): warp 0 writes
+//      - CLUSTER schedule (one thread block cluster per cloud): warp 0 sends
 //        the candidate (key, coordinates) into slot [step parity][its rank]
-//        of every block of the cluster through distributed shared memory,
-//        then one barrier.cluster; every warp then reduces the cluster's
-//        slots itself, so no further block barrier is needed.  Slots are
-//        double buffered by step parity, which makes one cluster barrier per
-//        step sufficient;
+//        of every block of the cluster with st.async, which completes as
+//        transaction bytes on that block's own mbarrier for this step
+//        parity; each block waits only on its local mbarrier (one-way
+//        latency, no cluster-wide barrier) and every warp reduces the
+//        cluster's slots itself.  Slots and mbarriers are double buffered by
+//        step parity: a block can only send step t+2 after every block sent
+//        step t+1, which each does after reading step t;
 //      - GRID schedule (cooperative launch, several blocks per cloud): each
 //        block writes one 64-bit word [bits(m)+1 : 31 | 2^24-1-j : 24 |
 //        step mod 512 : 9] into its slot of the caller's workspace; warp 0
@@ -37,15 +41,21 @@
 #include "pc_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace pcn {
 namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr int FPS_MAX_THREADS = 1024;
-constexpr int FPS_MAX_PPT = 8;
 constexpr int FPS_MAX_CLUSTER = 16;
 constexpr int FPS_GRID_MAX_N = 1 << 24;  // index field of the exchange word
+constexpr int FPS_CAND_BYTES = 20;       // key, index, x, y, z sent per block
+
+// Threads per block a kernel with PPT points per thread may use: the points'
+// registers (4 per point) must fit next to the working set.
+__host__ __device__ constexpr int fps_max_threads(int ppt) {
+    return ppt <= 8 ? 1024 : ppt <= 16 ? 512 : ppt <= 24 ? 384 : 256;
+}
 
 struct FpsArgs {
     const float *xyz;
@@ -57,6 +67,7 @@ struct FpsArgs {
     int *status;
     uint64_t timeout_ns;
     int stall;
+    float negzero;  // -0.0f, see sq2_rn
 };
 
 struct __align__(16) ClusterSlot {
@@ -69,26 +80,73 @@ __host__ __device__ constexpr size_t fps_coords_bytes(int chunk) {
     return (size_t(chunk) * 12 + 15) & ~size_t(15);
 }
 
+// The points of one thread: point p of the thread is j_first + p * T, packed
+// in pairs (p = 2i, 2i+1) for the f32x2 instructions.
+template <int PPT>
+struct ThreadPoints {
+    float2 x[PPT / 2], y[PPT / 2], z[PPT / 2];
+    float m[PPT];
+};
+
+template <int PPT>
+__device__ __forceinline__ void fps_load_points(const float *x, int lo, int hi,
+                                                int T, ThreadPoints<PPT> &pt,
+                                                float *scoord) {
+#pragma unroll
+    for (int p = 0; p < PPT; ++p) {
+        const int j = lo + int(threadIdx.x) + p * T;
+        float vx = 0.f, vy = 0.f, vz = 0.f;
+        if (j < hi) {
+            vx = x[size_t(j) * 3 + 0];
+            vy = x[size_t(j) * 3 + 1];
+            vz = x[size_t(j) * 3 + 2];
+            pt.m[p] = __int_as_float(0x7f800000);  // +inf: first min() gives s
+            if (scoord) {
+                scoord[(j - lo) * 3 + 0] = vx;
+                scoord[(j - lo) * 3 + 1] = vy;
+                scoord[(j - lo) * 3 + 2] = vz;
+            }
+        } else {
+            pt.m[p] = -1.0f;  // no point: never the maximum
+        }
+        if (p & 1) {
+            pt.x[p / 2].y = vx;
+            pt.y[p / 2].y = vy;
+            pt.z[p / 2].y = vz;
+        } else {
+            pt.x[p / 2].x = vx;
+            pt.y[p / 2].x = vy;
+            pt.z[p / 2].x = vz;
+        }
+    }
+}
+
 // Steps 1-3: update the owned points with center (cx, cy, cz), reduce the
 // block's (key, j) and return it in warp 0's lanes (other warps: undefined).
 template <int PPT>
-__device__ __forceinline__ void fps_local_step(float (&px)[PPT],
-                                               float (&py)[PPT],
-                                               float (&pz)[PPT],
-                                               float (&pm)[PPT], float cx,
-                                               float cy, float cz, int j_first,
-                                               int T, uint2 *wslot,
-                                               unsigned &bhi, unsigned &bj) {
+__device__ __forceinline__ void fps_local_step(ThreadPoints<PPT> &pt, float cx,
+                                               float cy, float cz, float2 nz0,
+                                               int j_first, int T,
+                                               uint2 *wslot, unsigned &bhi,
+                                               unsigned &bj) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float2 ncx = make_float2(-cx, -cx);
+    const float2 ncy = make_float2(-cy, -cy);
+    const float2 ncz = make_float2(-cz, -cz);
     float best = -1.0f;
     int bp = 0;
 #pragma unroll
-    for (int p = 0; p < PPT; ++p) {
-        const float s = sqdist(px[p], py[p], pz[p], cx, cy, cz);
-        pm[p] = fminf(pm[p], s);
-        if (pm[p] > best) {
-            best = pm[p];
-            bp = p;
+    for (int i = 0; i < PPT / 2; ++i) {
+        const float2 s = sqdist2(pt.x[i], pt.y[i], pt.z[i], ncx, ncy, ncz, nz0);
+        pt.m[2 * i] = fminf(pt.m[2 * i], s.x);
+        pt.m[2 * i + 1] = fminf(pt.m[2 * i + 1], s.y);
+        if (pt.m[2 * i] > best) {
+            best = pt.m[2 * i];
+            bp = 2 * i;
+        }
+        if (pt.m[2 * i + 1] > best) {
+            best = pt.m[2 * i + 1];
+            bp = 2 * i + 1;
         }
     }
     const unsigned khi = best >= 0.0f ? __float_as_uint(best) + 1u : 0u;
@@ -103,42 +161,17 @@ __device__ __forceinline__ void fps_local_step(float (&px)[PPT],
     }
 }
 
-template <int PPT>
-__device__ __forceinline__ void fps_load_points(const float *x, int lo, int hi,
-                                                int T, float (&px)[PPT],
-                                                float (&py)[PPT],
-                                                float (&pz)[PPT],
-                                                float (&pm)[PPT],
-                                                float *scoord) {
-#pragma unroll
-    for (int p = 0; p < PPT; ++p) {
-        const int j = lo + int(threadIdx.x) + p * T;
-        if (j < hi) {
-            px[p] = x[size_t(j) * 3 + 0];
-            py[p] = x[size_t(j) * 3 + 1];
-            pz[p] = x[size_t(j) * 3 + 2];
-            pm[p] = __int_as_float(0x7f800000);  // +inf: first min() gives s
-            if (scoord) {
-                scoord[(j - lo) * 3 + 0] = px[p];
-                scoord[(j - lo) * 3 + 1] = py[p];
-                scoord[(j - lo) * 3 + 2] = pz[p];
-            }
-        } else {
-            px[p] = py[p] = pz[p] = 0.0f;
-            pm[p] = -1.0f;  // no point: never the maximum
-        }
-    }
-}
-
 // BLOCK (CLUSTER == false, one block per cloud) and CLUSTER schedules.
 template <int PPT, bool CLUSTER>
-__global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
+__global__ void __launch_bounds__(fps_max_threads(PPT), 1)
     fps_cluster_kernel(const FpsArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     float *scoord = reinterpret_cast<float *>(smem);
     uint2 *wslot = reinterpret_cast<uint2 *>(smem + fps_coords_bytes(a.chunk));
     ClusterSlot *cslot = reinterpret_cast<ClusterSlot *>(
         smem + fps_coords_bytes(a.chunk) + 32 * sizeof(uint2));
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(cslot + 2 * FPS_MAX_CLUSTER);
+    int *s_fail = reinterpret_cast<int *>(xbar + 2);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T = blockDim.x;
@@ -147,22 +180,33 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
     const float *x = a.xyz + size_t(b) * size_t(a.N) * 3;
     const int lo = int(rank) * a.chunk;
     const int hi = min(a.N, lo + a.chunk);
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
+    const unsigned xbytes = unsigned(FPS_CAND_BYTES * a.nblocks);
 
-    float px[PPT], py[PPT], pz[PPT], pm[PPT];
-    fps_load_points<PPT>(x, lo, hi, T, px, py, pz, pm, scoord);
+    ThreadPoints<PPT> pt;
+    fps_load_points<PPT>(x, lo, hi, T, pt, scoord);
     float cx = x[size_t(a.start) * 3 + 0];
     float cy = x[size_t(a.start) * 3 + 1];
     float cz = x[size_t(a.start) * 3 + 2];
     int64_t *out = a.out + size_t(b) * a.npoint;
     if (rank == 0 && threadIdx.x == 0) out[0] = a.start;
+    if (CLUSTER && threadIdx.x == 0) {
+        // one exchange mbarrier per step parity, armed for its first step
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        *s_fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(&xbar[0], xbytes);
+        mbar_arrive_expect_tx(&xbar[1], xbytes);
+    }
     __syncthreads();
-    if (CLUSTER) cluster_sync_all();  // every block's slots exist before use
+    if (CLUSTER) cluster_sync_all();  // every block's barriers exist before use
 
     for (int t = 1; t < a.npoint; ++t) {
         const int par = t & 1;
         unsigned bhi, bj;
-        fps_local_step<PPT>(px, py, pz, pm, cx, cy, cz, lo + int(threadIdx.x),
-                            T, wslot, bhi, bj);
+        fps_local_step<PPT>(pt, cx, cy, cz, nz0, lo + int(threadIdx.x), T,
+                            wslot, bhi, bj);
         if (warp == 0) {
             float wx = 0.f, wy = 0.f, wz = 0.f;
             if (bhi) {
@@ -175,9 +219,10 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
             if (CLUSTER) {
                 if (lane < a.nblocks) {
                     const uint32_t ra = map_shared_rank(mine, unsigned(lane));
-                    st_cluster_v4(ra, bhi, bj, __float_as_uint(wx),
-                                  __float_as_uint(wy));
-                    st_cluster_v4(ra + 16, __float_as_uint(wz), 0u, 0u, 0u);
+                    const uint32_t rb = map_shared_rank(&xbar[par], unsigned(lane));
+                    st_async_v4(ra, bhi, bj, __float_as_uint(wx),
+                                __float_as_uint(wy), rb);
+                    st_async_b32(ra + 16, __float_as_uint(wz), rb);
                 }
             } else if (lane == 0) {
                 mine->hi = bhi;
@@ -187,10 +232,23 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
                 mine->z = wz;
             }
         }
-        if (CLUSTER)
-            cluster_sync_all();
-        else
+        if (CLUSTER) {
+            const unsigned ph = unsigned((t - 1) >> 1) & 1u;
+            if (!mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns))
+                *s_fail = 1;
+            // re-arm this parity's barrier for step t + 2 (its next phase
+            // cannot complete before every block has passed this point)
+            if (threadIdx.x == 0) mbar_arrive_expect_tx(&xbar[par], xbytes);
+            if (__syncthreads_or(*s_fail)) {
+                raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
+                if (rank == 0)
+                    for (int i = t + int(threadIdx.x); i < a.npoint; i += T)
+                        out[i] = -1;
+                break;
+            }
+        } else {
             __syncthreads();
+        }
         // every warp reduces the cloud's candidates
         const ClusterSlot *cs = &cslot[par * FPS_MAX_CLUSTER];
         unsigned vhi = 0u, vj = FULL;
@@ -215,7 +273,7 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
 
 // GRID schedule: cooperative launch, a.nblocks blocks per cloud.
 template <int PPT>
-__global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
+__global__ void __launch_bounds__(fps_max_threads(PPT), 1)
     fps_grid_kernel(const FpsArgs a) {
     __shared__ uint2 wslot[32];
     __shared__ float4 s_center;
@@ -229,9 +287,10 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
     const int lo = r * a.chunk;
     const int hi = min(a.N, lo + a.chunk);
     uint64_t *slots = a.slots + size_t(b) * 2 * a.nblocks;
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
 
-    float px[PPT], py[PPT], pz[PPT], pm[PPT];
-    fps_load_points<PPT>(x, lo, hi, T, px, py, pz, pm, nullptr);
+    ThreadPoints<PPT> pt;
+    fps_load_points<PPT>(x, lo, hi, T, pt, nullptr);
     float cx = x[size_t(a.start) * 3 + 0];
     float cy = x[size_t(a.start) * 3 + 1];
     float cz = x[size_t(a.start) * 3 + 2];
@@ -244,8 +303,8 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
         const int par = t & 1;
         const unsigned tag = unsigned(t) & 511u;
         unsigned bhi, bj;
-        fps_local_step<PPT>(px, py, pz, pm, cx, cy, cz, lo + int(threadIdx.x),
-                            T, wslot, bhi, bj);
+        fps_local_step<PPT>(pt, cx, cy, cz, nz0, lo + int(threadIdx.x), T,
+                            wslot, bhi, bj);
         if (warp == 0) {
             uint64_t *ps = slots + size_t(par) * a.nblocks;
             if (lane == 0 && !(a.stall && r == 0 && t == 1)) {
@@ -284,8 +343,7 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
                     raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
                 }
             } else {
-                unsigned mhi, mlo;
-                warp_argmax_hi_min_lo(unsigned(best >> 32), 0u, mhi, mlo);
+                const unsigned mhi = __reduce_max_sync(FULL, unsigned(best >> 32));
                 const unsigned lo32 = __reduce_max_sync(
                     FULL, unsigned(best >> 32) == mhi ? unsigned(best) : 0u);
                 const uint64_t w = (uint64_t(mhi) << 32) | lo32;
@@ -306,7 +364,6 @@ __global__ void __launch_bounds__(FPS_MAX_THREADS, 1)
         cx = c.x;
         cy = c.y;
         cz = c.z;
-        __syncthreads();  // s_center is rewritten next step
     }
     if (s_fail && r == 0) {
         for (int i = t + int(threadIdx.x); i < a.npoint; i += T) out[i] = -1;
@@ -319,33 +376,67 @@ const void *cluster_kernel_ptr(bool cluster) {
                    : reinterpret_cast<const void *>(&fps_cluster_kernel<PPT, false>);
 }
 
+constexpr int kPptChoices[] = {2, 4, 8, 16, 24, 32};
+
 const void *fps_kernel_ptr(int strategy, int ppt) {
     const bool cl = strategy == 2;
     if (strategy == 3) {
         switch (ppt) {
-            case 1: return reinterpret_cast<const void *>(&fps_grid_kernel<1>);
             case 2: return reinterpret_cast<const void *>(&fps_grid_kernel<2>);
             case 4: return reinterpret_cast<const void *>(&fps_grid_kernel<4>);
-            case 6: return reinterpret_cast<const void *>(&fps_grid_kernel<6>);
-            default: return reinterpret_cast<const void *>(&fps_grid_kernel<8>);
+            case 8: return reinterpret_cast<const void *>(&fps_grid_kernel<8>);
+            case 16: return reinterpret_cast<const void *>(&fps_grid_kernel<16>);
+            case 24: return reinterpret_cast<const void *>(&fps_grid_kernel<24>);
+            default: return reinterpret_cast<const void *>(&fps_grid_kernel<32>);
         }
     }
     switch (ppt) {
-        case 1: return cluster_kernel_ptr<1>(cl);
         case 2: return cluster_kernel_ptr<2>(cl);
         case 4: return cluster_kernel_ptr<4>(cl);
-        case 6: return cluster_kernel_ptr<6>(cl);
-        default: return cluster_kernel_ptr<8>(cl);
+        case 8: return cluster_kernel_ptr<8>(cl);
+        case 16: return cluster_kernel_ptr<16>(cl);
+        case 24: return cluster_kernel_ptr<24>(cl);
+        default: return cluster_kernel_ptr<32>(cl);
     }
 }
 
-int pick_ppt(int chunk) {
-    for (int p : {1, 2, 4, 6, 8})
-        if (chunk <= FPS_MAX_THREADS * p) return p;
-    return 0;
+int round_up(int v, int m) { return (v + m - 1) / m * m; }
+
+// Points per thread and threads for a block holding `chunk` points: the
+// fewest points per thread that keep the block at or below `target` threads
+// (about eight warps keep the per-step reductions short); if no choice gets
+// there, the most threads the largest choice allows.  Returns false when the
+// chunk does not fit at all.
+bool pick_shape(int chunk, int target, int &ppt, int &threads) {
+    for (int p : kPptChoices) {
+        const int t = std::max(32, round_up((chunk + p - 1) / p, 32));
+        if (t <= target && t <= fps_max_threads(p)) {
+            ppt = p;
+            threads = t;
+            return true;
+        }
+    }
+    for (int p : kPptChoices) {
+        const int t = std::max(32, round_up((chunk + p - 1) / p, 32));
+        if (t <= fps_max_threads(p)) {
+            ppt = p;
+            threads = t;
+            return true;
+        }
+    }
+    return false;
 }
 
-int round_up(int v, int m) { return (v + m - 1) / m * m; }
+int64_t block_capacity() {
+    int64_t c = 0;
+    for (int p : kPptChoices) c = std::max<int64_t>(c, int64_t(p) * fps_max_threads(p));
+    return c;
+}
+
+int target_threads() {
+    const char *e = std::getenv("PCN_FPS_THREADS");
+    return e ? std::max(32, std::atoi(e)) : 256;
+}
 
 bool cluster_fits(const DeviceInfo &dev, int cs, int threads, size_t smem,
                   int ppt) {
@@ -384,7 +475,7 @@ bool cluster_fits(const DeviceInfo &dev, int cs, int threads, size_t smem,
 
 size_t cluster_smem(int chunk) {
     return fps_coords_bytes(chunk) + 32 * sizeof(uint2) +
-           2 * FPS_MAX_CLUSTER * sizeof(ClusterSlot);
+           2 * FPS_MAX_CLUSTER * sizeof(ClusterSlot) + 2 * sizeof(uint64_t) + 16;
 }
 
 }  // namespace
@@ -392,7 +483,7 @@ size_t cluster_smem(int chunk) {
 FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
                  int cluster_size, int blocks_per_cloud) {
     FpsPlan p;
-    const int64_t cap_block = int64_t(FPS_MAX_THREADS) * FPS_MAX_PPT;
+    const int64_t cap_block = block_capacity();
     const int nsm = std::max(1, dev.sm_count);
     if (strategy == 0) {  // automatic
         if (N <= 2048 || (B >= nsm / 2 && N <= cap_block))
@@ -423,12 +514,10 @@ FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
         p.cluster = cs;
         p.blocks_per_cloud = cs;
         p.chunk = int((N + cs - 1) / cs);
-        p.ppt = pick_ppt(p.chunk);
-        if (p.ppt == 0) {
+        if (!pick_shape(p.chunk, target_threads(), p.ppt, p.threads)) {
             p.why = "cloud too large for one block/cluster schedule";
             return p;
         }
-        p.threads = std::max(32, round_up((p.chunk + p.ppt - 1) / p.ppt, 32));
         p.smem_bytes = cluster_smem(p.chunk);
         if (p.smem_bytes > dev.smem_per_block_optin) {
             p.why = "block's share of the cloud exceeds shared memory";
@@ -466,12 +555,10 @@ FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
         p.blocks_per_cloud = bpc;
         p.cluster = 1;
         p.chunk = int((N + bpc - 1) / bpc);
-        p.ppt = pick_ppt(p.chunk);
-        if (p.ppt == 0) {
+        if (!pick_shape(p.chunk, target_threads(), p.ppt, p.threads)) {
             p.why = "cloud too large for the on-chip FPS schedules";
             return p;
         }
-        p.threads = std::max(32, round_up((p.chunk + p.ppt - 1) / p.ppt, 32));
         p.smem_bytes = 0;
         p.workspace_bytes = (size_t(B) * 2 * bpc * sizeof(uint64_t) + 255) & ~size_t(255);
         int per_sm = 0;
@@ -509,6 +596,7 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
     a.stall = plan.strategy == 3 ? fps_grid_stall() : 0;
+    a.negzero = -0.0f;
 
     const void *fn = fps_kernel_ptr(plan.strategy, plan.ppt);
     cudaLaunchConfig_t cfg = {};
