@@ -188,6 +188,41 @@ int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
                   int64_t *out_idx, void *stream);
 
 /*
+ * Exact grid-accelerated kNN and Ball Query.
+ * mps-pointops project page, "Roadmap" (Phase 4: spatial acceleration
+ * structures, a uniform grid or BVH, for large clouds): the same operators
+ * as pc_knn and pc_ball_query -- same squared-distance arithmetic, same
+ * (s, j) order, same strict radius test, same padding -- computed from a
+ * uniform grid over each reference cloud, so that a query examines only the
+ * cells that can hold its answer.  Results are identical to pc_knn and
+ * pc_ball_query for finite inputs.
+ *
+ * A grid is caller-owned device memory of pc_grid_bytes(B, N) bytes,
+ * 256-byte aligned.  pc_grid_build fills it from ref [B, N, 3] (enqueued on
+ * `stream`; the points are copied into the grid, so ref may change
+ * afterwards); the query calls read it and may run any number of times, on
+ * any stream ordered after the build.  A grid must not be rebuilt while a
+ * query that reads it may still run.
+ *
+ *   pc_knn_grid:         1 <= k <= N, k <= 256; outputs as pc_knn.
+ *   pc_ball_query_grid:  radius finite and > 0, 1 <= K <= 256; outputs as
+ *                        pc_ball_query.  N = 0 gives padding only.
+ * B, N must be the values the grid was built with.
+ */
+size_t pc_grid_bytes(int64_t B, int64_t N);
+
+int pc_grid_build(const float *ref, int64_t B, int64_t N, void *grid,
+                  size_t grid_bytes, void *stream);
+
+int pc_knn_grid(const float *query, int64_t B, int64_t Q, const void *grid,
+                int64_t N, int64_t k, float *out_dist, int64_t *out_idx,
+                void *stream);
+
+int pc_ball_query_grid(const float *query, int64_t B, int64_t Q,
+                       const void *grid, int64_t N, double radius, int64_t K,
+                       float *out_dist2, int64_t *out_idx, void *stream);
+
+/*
  * Device status word.  Kernels that wait on other thread blocks bound every
  * wait; when a wait runs out they record PC_ERR_DEVICE_TIMEOUT here (the
  * first error wins) and return instead of hanging.  This call synchronizes

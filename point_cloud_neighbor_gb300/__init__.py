@@ -5,13 +5,16 @@ ABI of include/pointcloud.h); this package holds its ctypes binding, the
 build script and the seeded workload generators.
 """
 from .binding import (PC_FPS_AUTO, PC_FPS_BLOCK, PC_FPS_CLUSTER, PC_FPS_GRID,
-                      PointCloudError, ball_query, furthest_point_sample, knn,
-                      pc_ball_query, pc_debug_set_fps_grid_stall,
-                      pc_device_status, pc_fps, pc_knn, pc_set_wait_timeout_ns)
+                      PointCloudError, PointGrid, ball_query,
+                      furthest_point_sample, knn, pc_ball_query,
+                      pc_ball_query_grid, pc_debug_set_fps_grid_stall,
+                      pc_device_status, pc_fps, pc_grid_build, pc_knn,
+                      pc_knn_grid, pc_set_wait_timeout_ns)
 
 __all__ = [
     "PC_FPS_AUTO", "PC_FPS_BLOCK", "PC_FPS_CLUSTER", "PC_FPS_GRID",
     "PointCloudError", "ball_query", "furthest_point_sample", "knn",
     "pc_ball_query", "pc_debug_set_fps_grid_stall", "pc_device_status",
-    "pc_fps", "pc_knn", "pc_set_wait_timeout_ns",
+    "pc_fps", "pc_knn", "pc_set_wait_timeout_ns", "PointGrid",
+    "pc_grid_build", "pc_knn_grid", "pc_ball_query_grid",
 ]

@@ -47,6 +47,11 @@ _SIGNATURES = {
     "pc_fps_grid_static": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, ctypes.c_int,
                                           _P]),
     "pc_knn": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _P, _P, _P]),
+    "pc_grid_bytes": (ctypes.c_size_t, [_I, _I]),
+    "pc_grid_build": (ctypes.c_int, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
+    "pc_knn_grid": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _P, _P, _P]),
+    "pc_ball_query_grid": (ctypes.c_int, [_P, _I, _I, _P, _I, ctypes.c_double,
+                                          _I, _P, _P, _P]),
     "pc_ball_query": (ctypes.c_int, [_P, _I, _I, _P, _I, ctypes.c_double, _I,
                                      _P, _P, _P]),
     "pc_device_status": (ctypes.c_int, [_P, ctypes.c_int,
@@ -197,6 +202,72 @@ def pc_ball_query(query: torch.Tensor, ref: torch.Tensor, radius: float,
                              float(radius), K, out_dist2.data_ptr(),
                              out_idx.data_ptr(), _stream_ptr(query.device))
     _raise_on(st, "pc_ball_query")
+    return out_dist2, out_idx
+
+
+class PointGrid:
+    """A uniform grid over a reference cloud [B, N, 3] on the GPU (device
+    memory owned by a torch tensor), for pc_knn_grid / pc_ball_query_grid."""
+
+    def __init__(self, ref: torch.Tensor):
+        _check_cloud(ref, "ref")
+        self.B, self.N, _ = ref.shape
+        self.device = ref.device
+        L = lib()
+        nbytes = L.pc_grid_bytes(self.B, self.N)
+        self.buffer = torch.empty(max(nbytes, 256), dtype=torch.uint8,
+                                  device=ref.device)
+        with torch.cuda.device(ref.device):
+            st = L.pc_grid_build(ref.data_ptr() if self.N > 0 else None,
+                                 self.B, self.N, self.buffer.data_ptr(),
+                                 self.buffer.numel(), _stream_ptr(ref.device))
+        _raise_on(st, "pc_grid_build")
+
+
+def pc_grid_build(ref: torch.Tensor) -> PointGrid:
+    """Build the grid of reference cloud(s) ref [B, N, 3] float32 (CUDA)."""
+    return PointGrid(ref)
+
+
+def pc_knn_grid(query: torch.Tensor, grid: PointGrid, k: int, *,
+                out_dist: torch.Tensor | None = None,
+                out_idx: torch.Tensor | None = None):
+    """kNN from a grid; same results as pc_knn(query, ref, k)."""
+    _check_cloud(query, "query")
+    B, Q, _ = query.shape
+    if B != grid.B or query.device != grid.device:
+        raise ValueError("query and grid must share batch size and device")
+    L = lib()
+    with torch.cuda.device(query.device):
+        if out_dist is None:
+            out_dist = torch.empty((B, Q, k), dtype=torch.float32, device=query.device)
+        if out_idx is None:
+            out_idx = torch.empty((B, Q, k), dtype=torch.int64, device=query.device)
+        st = L.pc_knn_grid(query.data_ptr(), B, Q, grid.buffer.data_ptr(),
+                           grid.N, k, out_dist.data_ptr(), out_idx.data_ptr(),
+                           _stream_ptr(query.device))
+    _raise_on(st, "pc_knn_grid")
+    return out_dist, out_idx
+
+
+def pc_ball_query_grid(query: torch.Tensor, grid: PointGrid, radius: float,
+                       K: int, *, out_dist2: torch.Tensor | None = None,
+                       out_idx: torch.Tensor | None = None):
+    """Ball Query from a grid; same results as pc_ball_query(query, ref, r, K)."""
+    _check_cloud(query, "query")
+    B, Q, _ = query.shape
+    if B != grid.B or query.device != grid.device:
+        raise ValueError("query and grid must share batch size and device")
+    L = lib()
+    with torch.cuda.device(query.device):
+        if out_dist2 is None:
+            out_dist2 = torch.empty((B, Q, K), dtype=torch.float32, device=query.device)
+        if out_idx is None:
+            out_idx = torch.empty((B, Q, K), dtype=torch.int64, device=query.device)
+        st = L.pc_ball_query_grid(query.data_ptr(), B, Q, grid.buffer.data_ptr(),
+                                  grid.N, float(radius), K, out_dist2.data_ptr(),
+                                  out_idx.data_ptr(), _stream_ptr(query.device))
+    _raise_on(st, "pc_ball_query_grid")
     return out_dist2, out_idx
 
 
