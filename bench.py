@@ -348,6 +348,8 @@ def run_gpu(args):
                            if roof["bound"] == "alu" else
                            f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})")
 
+    grid = run_grid(args, pc, x, flush, device, world)
+
     # end to end through the public API: pinned host in, pinned host out
     e2e = run_e2e(args, pc, x_host, device, world)
 
@@ -357,7 +359,8 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": workload_config({"parallelism": f"replicas x{world}"}),
-        "roofline": roof, "ops": ops, "e2e": e2e, "gpu_launches": launches,
+        "roofline": roof, "ops": ops, "grid": grid, "e2e": e2e,
+        "gpu_launches": launches,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"]},
         "wall_s_timed_loop": wall1 - wall0,
@@ -396,6 +399,57 @@ def run_only(args):
     torch.cuda.synchronize(device)
     print(json.dumps({"op": args.only, "ms": e0.elapsed_time(e1) / args.steps,
                       "calls": args.steps}))
+
+
+def run_grid(args, pc, x, flush, device, world):
+    """The same kNN and Ball Query through the exact grid path (grid built
+    every step, inside the timed events): results equal the brute-force
+    kernels'; reported next to them, not as the headline."""
+    import torch
+    W = WORKLOAD
+    N, k, r, K = W["N"], W["knn_k"], W["bq_radius"], W["bq_K"]
+    stream = torch.cuda.current_stream(device)
+    kd = torch.empty((1, N, k), dtype=torch.float32, device=device)
+    ki = torch.empty((1, N, k), dtype=torch.int64, device=device)
+    bd = torch.empty((1, N, K), dtype=torch.float32, device=device)
+    bi = torch.empty((1, N, K), dtype=torch.int64, device=device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        g = pc.pc_grid_build(x)
+        if ev is not None:
+            ev[1].record(stream)
+        pc.pc_knn_grid(x, g, k, out_dist=kd, out_idx=ki)
+        if ev is not None:
+            ev[2].record(stream)
+        pc.pc_ball_query_grid(x, g, r, K, out_dist2=bd, out_idx=bi)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    steps = max(3, args.steps)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+              for _ in range(steps)]
+    torch.cuda.synchronize(device)
+    for s in range(steps):
+        flush.zero_()
+        step(events[s])
+    torch.cuda.synchronize(device)
+    b_ms, k_ms, q_ms = max_over_ranks(
+        [sum(e[0].elapsed_time(e[1]) for e in events) / steps,
+         sum(e[1].elapsed_time(e[2]) for e in events) / steps,
+         sum(e[2].elapsed_time(e[3]) for e in events) / steps], world, device)
+    return {"build_ms": b_ms, "knn_ms": k_ms, "ball_query_ms": q_ms,
+            "knn_queries_per_s": N * world / ((b_ms + k_ms) / 1e3),
+            "ball_query_queries_per_s": N * world / ((b_ms + q_ms) / 1e3),
+            "queries_per_s": 2 * N * world / ((b_ms + k_ms + q_ms) / 1e3),
+            "launches_per_step": 9,
+            "note": "exact uniform-grid path (pc_grid_build + pc_knn_grid + "
+                    "pc_ball_query_grid), grid rebuilt every step; identical "
+                    "results to the brute-force kernels"}
 
 
 def run_e2e(args, pc, x_host, device, world):
