@@ -18,18 +18,20 @@
 //      contiguous range.
 // Query (one warp per query): kNN searches cubes of cells of growing
 // half-width R around the query's cell, a shell at a time, and stops once the
-// distance from the query to everything outside the cube, lowered by a
-// rounding margin, proves that no unexamined point can have s <= tau (the
-// current k-th squared distance).  Ball Query examines the cells whose range
-// covers the radius plus the same margin and keeps the K smallest indices
-// among the hits.  Candidates are inserted into warp-distributed sorted lists
-// (lane l holds entries l, l + 32, ...).
+// cube holds every cell that can contain a point with s <= tau (tau: the
+// current k-th squared distance).  Ball Query examines the cells that can
+// hold a point with s < fl(r^2) and keeps the K smallest indices among the
+// hits.  Candidates are inserted into warp-distributed sorted lists (lane l
+// holds entries l, l + 32, ...).
 //
-// Rounding margin: a point assigned to cell i satisfies
-// fl(fl(x - lo) * inv_h) >= i (or < i + 1), so its true coordinate is within
-// 3u * (|lo| + D / inv_h) of the nominal face lo + i / inv_h; the bounds use
-// faces moved by 1e-6 * (|lo| + D / inv_h), and s32 >= s (1 - 6u) is covered by
-// requiring d^2 (1 - 1e-6) > tau.
+// Exactness: the cell of a coordinate, floor(fl(fl(x - lo) * inv_h)) clamped,
+// is monotone in x.  A point with s32 <= rho^2 has |x - q| <= rho (1 + 3u) +
+// 6.5e-23 on every axis (u = 2^-24; the absolute term covers squares that
+// round below the normal range), so it lies between the cells of the floats
+// q - reach and q + reach once reach exceeds that bound by the rounding of
+// q -+ reach: reach = rho (1 + 1e-5) + 1e-5 (|qx| + |qy| + |qz|) + 1e-22.
+// The same cell function and header serve the build and the queries, so no
+// face of a cell is ever computed.
 #include "pointcloud.h"
 #include "pc_device.cuh"
 #include "pc_internal.h"
@@ -111,6 +113,26 @@ __device__ __forceinline__ float key_to_float(unsigned k) {
 __device__ __forceinline__ int cell_axis(float x, float lo, float inv_h, int D) {
     const float t = __fmul_rn(__fsub_rn(x, lo), inv_h);
     return min(max(__float2int_rd(t), 0), D - 1);
+}
+
+// Slack added to a real radius r before it is turned into a range of cells
+// around a query q: 1e-5 r + 1e-5 (|qx| + |qy| + |qz|) + 1e-22.  It covers
+// (a) s32 >= s (1 - 5u) - 5 * 2^-150 (three roundings of squares and two of
+// sums, absolute error below the normal range), i.e. |dx| <= sqrt(s32)
+// (1 + 3u) + 6.5e-23 for every point with s32 <= r^2, and (b) the rounding of
+// q -+ reach and of the slack itself (u = 2^-24 each).
+__device__ __forceinline__ float query_slack(float qx, float qy, float qz) {
+    return 1e-5f * (fabsf(qx) + fabsf(qy) + fabsf(qz)) + 1e-22f;
+}
+
+// Cells [c0, c1] along one axis that hold every reference point x with
+// |x - q| <= reach_needed: cell_axis is monotone in x, so the cells of the
+// floats q - reach and q + reach (each rounded outwards of the needed range
+// by the slack) bound the cells of all such points.
+__device__ __forceinline__ void cell_span(float q, float reach, float lo,
+                                          float inv_h, int D, int &c0, int &c1) {
+    c0 = cell_axis(__fsub_rn(q, reach), lo, inv_h, D);
+    c1 = cell_axis(__fadd_rn(q, reach), lo, inv_h, D);
 }
 
 // ---------------------------------------------------------------------------
@@ -340,7 +362,6 @@ __global__ void __launch_bounds__(256) knn_grid_kernel(const QueryArgs a) {
     const int cq[3] = {cell_axis(qx, h.lo[0], h.inv_h[0], D),
                        cell_axis(qy, h.lo[1], h.inv_h[1], D),
                        cell_axis(qz, h.lo[2], h.inv_h[2], D)};
-    const double qd[3] = {qx, qy, qz};
     const int *st = a.start + size_t(b) * (a.C + 1);
     const float4 *pts = a.pts + size_t(b) * a.N;
     const int k = a.k;
@@ -387,10 +408,8 @@ __global__ void __launch_bounds__(256) knn_grid_kernel(const QueryArgs a) {
         scan_range(st[c0], st[c0 + (x1 - x0) + 1]);
     };
 
-    const double margin0 = 1e-6 * (fabs(double(h.lo[0])) + D / double(h.inv_h[0]));
-    const double margin1 = 1e-6 * (fabs(double(h.lo[1])) + D / double(h.inv_h[1]));
-    const double margin2 = 1e-6 * (fabs(double(h.lo[2])) + D / double(h.inv_h[2]));
-    const double margin = fmax(margin0, fmax(margin1, margin2));
+    const float slack = query_slack(qx, qy, qz);
+    const float qf[3] = {qx, qy, qz};
 
     for (int R = 0; R <= D; ++R) {
         // the shell of half-width R: rows with |dz| == R or |dy| == R in
@@ -409,26 +428,19 @@ __global__ void __launch_bounds__(256) knn_grid_kernel(const QueryArgs a) {
                 }
             }
         }
-        // everything outside the cube is at least `d` away
-        double d = INFINITY;
-        bool all = true;
+        // done once the cube holds every cell that can contain a point with
+        // s32 <= tau (the current k-th squared distance), or all cells
+        bool covered = true;
+        const float reach =
+            tj == INT_MAX ? __int_as_float(0x7f800000)
+                          : __fsqrt_rn(ts) * (1.0f + 1e-5f) + slack;
 #pragma unroll
         for (int ax = 0; ax < 3; ++ax) {
-            const double hh = 1.0 / double(h.inv_h[ax]);
-            if (cq[ax] - R > 0) {
-                all = false;
-                d = fmin(d, qd[ax] - (double(h.lo[ax]) + (cq[ax] - R) * hh));
-            }
-            if (cq[ax] + R < D - 1) {
-                all = false;
-                d = fmin(d, (double(h.lo[ax]) + (cq[ax] + R + 1) * hh) - qd[ax]);
-            }
+            int c0, c1;
+            cell_span(qf[ax], reach, h.lo[ax], h.inv_h[ax], D, c0, c1);
+            covered = covered && c0 >= cq[ax] - R && c1 <= cq[ax] + R;
         }
-        if (all) break;
-        if (tj != INT_MAX) {
-            const double dm = d - margin;
-            if (dm > 0.0 && dm * dm * (1.0 - 1e-6) - 1e-40 > double(ts)) break;
-        }
+        if (covered) break;
     }
 
     const size_t row = size_t(b) * a.Q + qi;
@@ -443,8 +455,8 @@ __global__ void __launch_bounds__(256) knn_grid_kernel(const QueryArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Ball Query from the grid: one warp per query; cells covering the radius
-// plus the margin; the K smallest indices among the hits.
+// Ball Query from the grid: one warp per query; the cells that can hold a
+// hit; the K smallest indices among the hits.
 // ---------------------------------------------------------------------------
 template <int KPL>
 __global__ void __launch_bounds__(256) bq_grid_kernel(const QueryArgs a,
@@ -468,20 +480,15 @@ __global__ void __launch_bounds__(256) bq_grid_kernel(const QueryArgs a,
         const int D = a.D;
         const float *qp = a.query + row * 3;
         const float qx = qp[0], qy = qp[1], qz = qp[2];
-        const double qd[3] = {qx, qy, qz};
+        const float qf[3] = {qx, qy, qz};
         const int *st = a.start + size_t(b) * (a.C + 1);
         const float4 *pts = a.pts + size_t(b) * a.N;
+        // every point with s32 < fl(r^2) lies in these cells
+        const float reach = r32 * (1.0f + 1e-5f) + query_slack(qx, qy, qz);
         int lo_c[3], hi_c[3];
-        const double reach = double(r32) * (1.0 + 1e-5);
 #pragma unroll
-        for (int ax = 0; ax < 3; ++ax) {
-            const double inv = double(h.inv_h[ax]);
-            const double mg = 1e-6 * (fabs(double(h.lo[ax])) + D / inv);
-            const double t0 = (qd[ax] - double(h.lo[ax]) - reach - mg) * inv;
-            const double t1 = (qd[ax] - double(h.lo[ax]) + reach + mg) * inv;
-            lo_c[ax] = int(fmax(0.0, fmin(double(D - 1), floor(t0))));
-            hi_c[ax] = int(fmax(0.0, fmin(double(D - 1), floor(t1))));
-        }
+        for (int ax = 0; ax < 3; ++ax)
+            cell_span(qf[ax], reach, h.lo[ax], h.inv_h[ax], D, lo_c[ax], hi_c[ax]);
         int tj = INT_MAX;  // K-th smallest index among the hits so far
         for (int z = lo_c[2]; z <= hi_c[2]; ++z) {
             for (int y = lo_c[1]; y <= hi_c[1]; ++y) {
