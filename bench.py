@@ -382,10 +382,15 @@ def run_only(args):
     W = WORKLOAD
     device = torch.device("cuda", 0)
     x = torch.from_numpy(inputs.large(seed=3, morton=False)).to(device)
+    g = pc.pc_grid_build(x) if args.only.startswith("grid") else None
     calls = {
         "fps": lambda: pc.pc_fps(x, W["npoint"], 0),
         "knn": lambda: pc.pc_knn(x, x, W["knn_k"]),
         "ball_query": lambda: pc.pc_ball_query(x, x, W["bq_radius"], W["bq_K"]),
+        "grid_build": lambda: pc.pc_grid_build(x),
+        "grid_knn": lambda: pc.pc_knn_grid(x, g, W["knn_k"]),
+        "grid_ball_query": lambda: pc.pc_ball_query_grid(x, g, W["bq_radius"],
+                                                         W["bq_K"]),
     }
     fn = calls[args.only]
     for _ in range(args.warmup):
@@ -596,7 +601,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["fps", "knn", "ball_query"],
+    ap.add_argument("--only", choices=["fps", "knn", "ball_query", "grid_build",
+                                       "grid_knn", "grid_ball_query"],
                     help="run one operator of the step W + K times and print "
                          "its mean CUDA-event time (for profiler captures)")
     args = ap.parse_args()
