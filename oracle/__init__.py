@@ -76,6 +76,18 @@ def _bind(lib):
                                             ctypes.c_double, I, P, I, P]
     lib.orc_s32_pairs.restype = None
     lib.orc_s32_pairs.argtypes = [P, P, I, P]
+    lib.orc_knn_masked_rows.restype = ctypes.c_int
+    lib.orc_knn_masked_rows.argtypes = [P, I, I, P, I, I, P, P, ctypes.c_int,
+                                        P, I, P, P]
+    lib.orc_ball_query_masked_rows.restype = ctypes.c_int
+    lib.orc_ball_query_masked_rows.argtypes = [P, I, I, P, I, P, P,
+                                               ctypes.c_double, I, P, I, P, P]
+    lib.orc_gather_points.restype = ctypes.c_int
+    lib.orc_gather_points.argtypes = [P, I, I, P, I, I, P]
+    lib.orc_three_interpolate.restype = ctypes.c_int
+    lib.orc_three_interpolate.argtypes = [P, I, I, I, P, P, I, P]
+    lib.orc_three_interpolate_backward.restype = ctypes.c_int
+    lib.orc_three_interpolate_backward.argtypes = [P, I, I, I, P, P, I, P]
     return lib
 
 
@@ -309,3 +321,183 @@ def ball_query_scan_len(query, ref, radius: float, K: int, rows=None,
         with ThreadPoolExecutor(len(chunks)) as ex:
             list(ex.map(lambda c: run(*c), chunks))
     return out
+
+
+# ---------------------------------------------------------------------------
+# Lengths-masked kNN / Ball Query, gather, three_interpolate, Chamfer.
+# ---------------------------------------------------------------------------
+def _lens(lengths, B):
+    if lengths is None:
+        return None
+    a = np.ascontiguousarray(lengths, dtype=np.int64)
+    if a.shape != (B,):
+        raise ValueError(f"lengths must have shape [{B}]")
+    return a
+
+
+def _opt_ptr(a):
+    return None if a is None else _ptr(a)
+
+
+def knn_masked(query, ref, k: int, query_lengths=None, ref_lengths=None,
+               squared: bool = False, rows=None, threads: int = 1):
+    """kNN over the valid prefix of every cloud (``orc_knn_masked_rows``).
+
+    Returns (dist [R,k], idx [R,k]); dist is s when ``squared`` else sqrt(s);
+    rows past the query length and slots past the references are (0, -1).
+    """
+    query = _f32(query)
+    ref = _f32(ref)
+    B, Q, _ = query.shape
+    N = ref.shape[1]
+    ql, rl = _lens(query_lengths, B), _lens(ref_lengths, B)
+    rows = _rows_arg(rows, B * Q)
+    R = rows.shape[0]
+    dist = np.empty((R, k), dtype=np.float32)
+    idx = np.empty((R, k), dtype=np.int64)
+    lib = _load()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        rr = np.ascontiguousarray(rows[lo:hi])
+        d = np.empty((hi - lo, k), dtype=np.float32)
+        i = np.empty((hi - lo, k), dtype=np.int64)
+        _check(lib.orc_knn_masked_rows(_ptr(query), B, Q, _ptr(ref), N, k,
+                                       _opt_ptr(ql), _opt_ptr(rl), int(squared),
+                                       _ptr(rr), hi - lo, _ptr(d), _ptr(i)),
+               "knn_masked")
+        dist[lo:hi] = d
+        idx[lo:hi] = i
+
+    chunks = _split(R, threads)
+    if len(chunks) <= 1:
+        run(0, R)
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            list(ex.map(lambda c: run(*c), chunks))
+    return dist, idx
+
+
+def ball_query_masked(query, ref, radius: float, K: int, query_lengths=None,
+                      ref_lengths=None, rows=None):
+    """First-K Ball Query over the valid prefix of every cloud."""
+    query = _f32(query)
+    ref = _f32(ref)
+    B, Q, _ = query.shape
+    N = ref.shape[1]
+    ql, rl = _lens(query_lengths, B), _lens(ref_lengths, B)
+    rows = _rows_arg(rows, B * Q)
+    R = rows.shape[0]
+    d = np.empty((R, K), dtype=np.float32)
+    i = np.empty((R, K), dtype=np.int64)
+    _check(_load().orc_ball_query_masked_rows(
+        _ptr(query), B, Q, _ptr(ref), N, _opt_ptr(ql), _opt_ptr(rl),
+        float(radius), K, _ptr(rows), R, _ptr(d), _ptr(i)), "ball_query_masked")
+    return d, i
+
+
+def gather_points(x, idx) -> np.ndarray:
+    """out[b,i,t,:] = x[b, idx[b,i,t], :], zeros where idx = -1."""
+    x = _f32(x)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    B, N, _ = x.shape
+    _, Q, K = idx.shape
+    out = np.empty((B, Q, K, 3), dtype=np.float32)
+    _check(_load().orc_gather_points(_ptr(x), B, N, _ptr(idx), Q, K, _ptr(out)),
+           "gather_points")
+    return out
+
+
+def three_interpolate(features, idx, weight) -> np.ndarray:
+    """features [B,C,M], idx [B,n,3] int64, weight [B,n,3] -> [B,C,n]."""
+    f = np.ascontiguousarray(features, dtype=np.float32)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    w = np.ascontiguousarray(weight, dtype=np.float32)
+    B, C, M = f.shape
+    n = idx.shape[1]
+    out = np.empty((B, C, n), dtype=np.float32)
+    _check(_load().orc_three_interpolate(_ptr(f), B, C, M, _ptr(idx), _ptr(w),
+                                         n, _ptr(out)), "three_interpolate")
+    return out
+
+
+def three_interpolate_backward(grad_out, idx, weight, M: int) -> np.ndarray:
+    """grad_out [B,C,n] -> grad_features [B,C,M] (sequential float32 sums)."""
+    g = np.ascontiguousarray(grad_out, dtype=np.float32)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    w = np.ascontiguousarray(weight, dtype=np.float32)
+    B, C, n = g.shape
+    out = np.empty((B, C, M), dtype=np.float32)
+    _check(_load().orc_three_interpolate_backward(_ptr(g), B, C, n, _ptr(idx),
+                                                  _ptr(w), M, _ptr(out)),
+           "three_interpolate_backward")
+    return out
+
+
+REDUCTIONS = ("none", "sum", "mean")
+
+
+def chamfer(x, y, x_lengths=None, y_lengths=None, weights=None,
+            point_reduction: str = "mean", batch_reduction: str = "mean",
+            single_directional: bool = False, threads: int = 1):
+    """Bidirectional squared-L2 Chamfer distance (project page, "Roadmap",
+    Phase 4):  L = sum_i |q_i - x_a(i)|^2 + sum_j |x_j - q_b(j)|^2, with a(i)
+    the nearest point of y to x_i and b(j) the nearest point of x to y_j
+    (kNN with k = 1: smallest (s, index)).
+
+    Readings taken (the pages name lengths, weights, point and batch
+    reductions without giving their divisors): points past a cloud's length
+    are excluded as queries and as references; a point with no valid
+    reference contributes 0 and gets index -1; "mean" over points divides a
+    cloud's sum by max(length, 1); weights [B] scale each cloud's loss;
+    "mean" over the batch divides by B.  Sums are exact (math.fsum over the
+    float32 terms), the divisions and products are in float64, and the
+    result is rounded once to float32.
+
+    Returns (loss, (dist_x [B,P1], idx_x [B,P1]), (dist_y, idx_y) or None):
+    loss is a float32 scalar, or [B] float32 for batch_reduction "none".
+    """
+    import math
+    x = _f32(x)
+    y = _f32(y)
+    B, P1, _ = x.shape
+    P2 = y.shape[1]
+    xl, yl = _lens(x_lengths, B), _lens(y_lengths, B)
+    dx, ix = knn_masked(x, y, 1, xl, yl, squared=True, threads=threads)
+    dx, ix = dx.reshape(B, P1), ix.reshape(B, P1)
+    if single_directional:
+        dy = iy = None
+    else:
+        dy, iy = knn_masked(y, x, 1, yl, xl, squared=True, threads=threads)
+        dy, iy = dy.reshape(B, P2), iy.reshape(B, P2)
+    if point_reduction not in ("sum", "mean") or batch_reduction not in REDUCTIONS:
+        raise ValueError("point_reduction: sum|mean; batch_reduction: none|sum|mean")
+
+    def clamp(lens, b, full):
+        if lens is None:
+            return full
+        return min(max(int(lens[b]), 0), full)
+
+    per = []
+    for b in range(B):
+        nx = clamp(xl, b, P1)
+        t = math.fsum(float(v) for v in dx[b, :nx])
+        if point_reduction == "mean":
+            t = t / max(nx, 1)
+        if not single_directional:
+            ny = clamp(yl, b, P2)
+            u = math.fsum(float(v) for v in dy[b, :ny])
+            if point_reduction == "mean":
+                u = u / max(ny, 1)
+            t = t + u
+        if weights is not None:
+            t = t * float(np.float32(weights[b]))
+        per.append(t)
+    if batch_reduction == "none":
+        loss = np.array(per, dtype=np.float64).astype(np.float32)
+    elif batch_reduction == "sum":
+        loss = np.float32(math.fsum(per))
+    else:
+        loss = np.float32(math.fsum(per) / B) if B > 0 else np.float32(0.0)
+    return loss, (dx, ix), (None if single_directional else (dy, iy))

@@ -269,3 +269,212 @@ void orc_s32_pairs(const float *a, const float *b, int64_t n, float *out)
     for (int64_t i = 0; i < n; ++i)
         out[i] = orc_s32(a + 3 * i, b + 3 * i);
 }
+
+/* ------------------------------------------------------------------------
+ * Per-cloud valid lengths.  The project page's Chamfer contract ("Roadmap",
+ * Phase 4: "lengths mask padding in forward and backward") and its
+ * PyTorch3D-style Ball Query ("lengths1, lengths2") restrict cloud b to its
+ * first qlen[b] queries and first rlen[b] references.  Reading taken: a
+ * length outside [0, Q] (or [0, N]) is clamped to that range; rows past the
+ * query length and slots past the available references hold (-1, 0), the
+ * padding convention of "Ball Query: first K within a radius".
+ * ---------------------------------------------------------------------- */
+static int64_t orc_clamp_len(const int64_t *len, int64_t b, int64_t full)
+{
+    if (!len) return full;
+    if (len[b] < 0) return 0;
+    return len[b] > full ? full : len[b];
+}
+
+/*
+ * kNN with lengths, optionally returning the squared distance.  Project
+ * page, "k nearest neighbors": pi = argsort_j (s_bij, j) over the valid
+ * references j < rlen[b]; D = sqrt(s), or s itself when `squared` is set
+ * (the Chamfer operator's squared-L2 nearest distance, "Roadmap" Phase 4).
+ * The first min(k, rlen[b]) entries are real; the rest are (-1, 0).
+ */
+int orc_knn_masked_rows(const float *query, int64_t B, int64_t Q,
+                        const float *ref, int64_t N, int64_t k,
+                        const int64_t *qlen, const int64_t *rlen, int squared,
+                        const int64_t *rows, int64_t nrows, float *out_dist,
+                        int64_t *out_idx)
+{
+    if (B < 0 || Q < 0 || N < 0 || k < 1) return ORC_BAD_ARGUMENT;
+    orc_pair *cand = (orc_pair *)malloc((size_t)(N > 0 ? N : 1) * sizeof(orc_pair));
+    if (!cand) return ORC_NO_MEMORY;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t row = rows[r];
+        if (row < 0 || row >= B * Q) {
+            free(cand);
+            return ORC_BAD_ARGUMENT;
+        }
+        int64_t b = row / Q, i = row % Q;
+        int64_t nq = orc_clamp_len(qlen, b, Q);
+        int64_t nr = orc_clamp_len(rlen, b, N);
+        int64_t real = 0;
+        if (i < nq) {
+            const float *q = query + (size_t)row * 3;
+            const float *x = ref + (size_t)b * (size_t)N * 3;
+            for (int64_t j = 0; j < nr; ++j) {
+                cand[j].s = orc_s32(q, x + 3 * j);
+                cand[j].j = j;
+            }
+            qsort(cand, (size_t)nr, sizeof(orc_pair), orc_pair_cmp);
+            real = k < nr ? k : nr;
+        }
+        for (int64_t t = 0; t < k; ++t) {
+            if (t < real) {
+                out_dist[r * k + t] = squared ? cand[t].s : sqrtf(cand[t].s);
+                out_idx[r * k + t] = cand[t].j;
+            } else {
+                out_dist[r * k + t] = 0.0f;
+                out_idx[r * k + t] = -1;
+            }
+        }
+    }
+    free(cand);
+    return ORC_OK;
+}
+
+/*
+ * Ball Query with lengths.  Project page, "Ball Query: first K within a
+ * radius", over the valid references j < rlen[b]; query rows i >= qlen[b]
+ * are padding in full ("PyTorch3D-style Ball Query": lengths1, lengths2).
+ */
+int orc_ball_query_masked_rows(const float *query, int64_t B, int64_t Q,
+                               const float *ref, int64_t N,
+                               const int64_t *qlen, const int64_t *rlen,
+                               double radius, int64_t K, const int64_t *rows,
+                               int64_t nrows, float *out_dist2,
+                               int64_t *out_idx)
+{
+    if (B < 0 || Q < 0 || N < 0 || K < 1) return ORC_BAD_ARGUMENT;
+    float R2 = orc_radius_threshold(radius);
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t row = rows[r];
+        if (row < 0 || row >= B * Q) return ORC_BAD_ARGUMENT;
+        int64_t b = row / Q, i = row % Q;
+        int64_t nq = orc_clamp_len(qlen, b, Q);
+        int64_t nr = orc_clamp_len(rlen, b, N);
+        int64_t cnt = 0;
+        if (i < nq) {
+            const float *q = query + (size_t)row * 3;
+            const float *x = ref + (size_t)b * (size_t)N * 3;
+            for (int64_t j = 0; j < nr && cnt < K; ++j) {
+                float s = orc_s32(q, x + 3 * j);
+                int accept = s < R2;
+                if (accept) {
+                    out_idx[r * K + cnt] = j;
+                    out_dist2[r * K + cnt] = s;
+                    ++cnt;
+                }
+            }
+        }
+        for (; cnt < K; ++cnt) {
+            out_dist2[r * K + cnt] = 0.0f;
+            out_idx[r * K + cnt] = (int64_t)-1;
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Gather of neighbor coordinates: out[b,i,t,:] = x[b, idx[b,i,t], :], and
+ * (0, 0, 0) where idx = -1.  Project page, "PyTorch3D-style Ball Query":
+ * return_nn gives the neighbor coordinates, "with zero coordinates in knn
+ * where idx = -1".  Any other index outside [0, N) is an error.
+ */
+int orc_gather_points(const float *x, int64_t B, int64_t N,
+                      const int64_t *idx, int64_t Q, int64_t K, float *out)
+{
+    if (B < 0 || N < 0 || Q < 0 || K < 0) return ORC_BAD_ARGUMENT;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t e = 0; e < Q * K; ++e) {
+            int64_t j = idx[b * Q * K + e];
+            float *o = out + (size_t)(b * Q * K + e) * 3;
+            if (j == -1) {
+                o[0] = o[1] = o[2] = 0.0f;
+            } else if (j < 0 || j >= N) {
+                return ORC_BAD_ARGUMENT;
+            } else {
+                const float *p = x + (size_t)(b * N + j) * 3;
+                o[0] = p[0];
+                o[1] = p[1];
+                o[2] = p[2];
+            }
+        }
+    return ORC_OK;
+}
+
+/*
+ * three_interpolate forward (project page, Quick start and "Roadmap" Phase 2:
+ * PointNet++ feature propagation with externally computed weights):
+ *   out[b,c,i] = sum_{t=0..2} w[b,i,t] * f[b,c,idx[b,i,t]]
+ * features f [B,C,M], idx [B,n,3] int64, w [B,n,3], out [B,C,n].
+ * Reading taken: float32, each product and sum rounded separately, summed
+ * in the order ((w0 f0 + w1 f1) + w2 f2); idx = -1 (padding) reads the
+ * feature as 0; any other index outside [0, M) is an error.
+ */
+int orc_three_interpolate(const float *f, int64_t B, int64_t C, int64_t M,
+                          const int64_t *idx, const float *w, int64_t n,
+                          float *out)
+{
+    if (B < 0 || C < 0 || M < 0 || n < 0) return ORC_BAD_ARGUMENT;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t i = 0; i < n; ++i)
+            for (int t = 0; t < 3; ++t) {
+                int64_t m = idx[(b * n + i) * 3 + t];
+                if (m != -1 && (m < 0 || m >= M)) return ORC_BAD_ARGUMENT;
+            }
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t c = 0; c < C; ++c) {
+            const float *fr = f + (size_t)(b * C + c) * (size_t)M;
+            for (int64_t i = 0; i < n; ++i) {
+                const int64_t *id = idx + (b * n + i) * 3;
+                const float *wi = w + (b * n + i) * 3;
+                float term[3];
+                for (int t = 0; t < 3; ++t) {
+                    float v = id[t] == -1 ? 0.0f : fr[id[t]];
+                    term[t] = wi[t] * v;
+                }
+                float s01 = term[0] + term[1];
+                out[(b * C + c) * n + i] = s01 + term[2];
+            }
+        }
+    return ORC_OK;
+}
+
+/*
+ * three_interpolate backward ("Roadmap" Phase 2: "accumulates backward
+ * gradients into input features"): with upstream gradient g [B,C,n],
+ *   grad_f[b,c,m] = sum over (i, t) with idx[b,i,t] = m of w[b,i,t] g[b,c,i].
+ * The sum is accumulated in float32 from 0 in increasing (i, t) order, each
+ * product and addition rounded; the pages allow any summation order (the
+ * GPU accumulates atomically), so parity is to a bound on the order.
+ */
+int orc_three_interpolate_backward(const float *g, int64_t B, int64_t C,
+                                   int64_t n, const int64_t *idx,
+                                   const float *w, int64_t M, float *grad_f)
+{
+    if (B < 0 || C < 0 || M < 0 || n < 0) return ORC_BAD_ARGUMENT;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t i = 0; i < n; ++i)
+            for (int t = 0; t < 3; ++t) {
+                int64_t m = idx[(b * n + i) * 3 + t];
+                if (m != -1 && (m < 0 || m >= M)) return ORC_BAD_ARGUMENT;
+            }
+    memset(grad_f, 0, (size_t)(B * C * M) * sizeof(float));
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t c = 0; c < C; ++c) {
+            float *gr = grad_f + (size_t)(b * C + c) * (size_t)M;
+            const float *gi = g + (size_t)(b * C + c) * (size_t)n;
+            for (int64_t i = 0; i < n; ++i)
+                for (int t = 0; t < 3; ++t) {
+                    int64_t m = idx[(b * n + i) * 3 + t];
+                    if (m == -1) continue;
+                    float p = w[(b * n + i) * 3 + t] * gi[i];
+                    gr[m] = gr[m] + p;
+                }
+        }
+    return ORC_OK;
+}

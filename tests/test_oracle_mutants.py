@@ -12,6 +12,7 @@ import os
 
 import pytest
 
+import test_oracle_ext_pins as ext
 import test_oracle_pins as pins
 
 # (name, text to replace in pc_oracle.c, replacement)
@@ -40,6 +41,23 @@ MUTANTS = [
      "out_idx[r * K + cnt] = 0;"),
     ("bq_keeps_last_k", "for (int64_t j = 0; j < N && cnt < K; ++j) {\n            float s = orc_s32(q, x + 3 * j);\n            if (s < R2) {",
      "for (int64_t j = N - 1; j >= 0 && cnt < K; --j) {\n            float s = orc_s32(q, x + 3 * j);\n            if (s < R2) {"),
+    ("bq_masked_non_strict", "int accept = s < R2;", "int accept = s <= R2;"),
+    ("bq_masked_padding_zero_index", "out_idx[r * K + cnt] = (int64_t)-1;",
+     "out_idx[r * K + cnt] = 0;"),
+    ("lengths_ignored", "return len[b] > full ? full : len[b];", "return full;"),
+    ("knn_masked_squared_flag_inverted",
+     "squared ? cand[t].s : sqrtf(cand[t].s)", "squared ? sqrtf(cand[t].s) : cand[t].s"),
+    ("bq_masked_rows_past_length_searched",
+     "if (i < nq) {\n            const float *q = query + (size_t)row * 3;\n            const float *x = ref + (size_t)b * (size_t)N * 3;\n            for (int64_t j = 0; j < nr && cnt < K; ++j) {",
+     "if (1) {\n            const float *q = query + (size_t)row * 3;\n            const float *x = ref + (size_t)b * (size_t)N * 3;\n            for (int64_t j = 0; j < nr && cnt < K; ++j) {"),
+    ("gather_padding_not_zero", "o[0] = o[1] = o[2] = 0.0f;",
+     "o[0] = x[b * N * 3]; o[1] = x[b * N * 3 + 1]; o[2] = x[b * N * 3 + 2];"),
+    ("interp_wrong_weight_slot", "term[t] = wi[t] * v;", "term[t] = wi[0] * v;"),
+    ("interp_padding_reads_feature_0", "float v = id[t] == -1 ? 0.0f : fr[id[t]];",
+     "float v = id[t] == -1 ? fr[0] : fr[id[t]];"),
+    ("interp_backward_drops_weight", "float p = w[(b * n + i) * 3 + t] * gi[i];",
+     "float p = gi[i];"),
+    ("interp_backward_overwrites", "gr[m] = gr[m] + p;", "gr[m] = p;"),
 ]
 
 PIN_FUNCTIONS = [
@@ -57,6 +75,19 @@ PIN_FUNCTIONS = [
     (pins.test_fps_line_matches_interval_bisection, {"n": 23, "start": 7}),
     (pins.test_fps_matches_brute_force, {"seed": 1, "grid": 1 / 4}),
     (pins.test_ball_query_scan_length, {}),
+    (ext.test_quickstart_three_nn, {}),
+    (ext.test_quickstart_three_interpolate, {}),
+    (ext.test_quickstart_chamfer, {}),
+    (ext.test_knn_masked_equals_knn_on_sliced_clouds, {}),
+    (ext.test_knn_masked_squared_is_s32_of_the_pair, {}),
+    (ext.test_ball_query_masked_equals_sliced, {}),
+    (ext.test_gather_points_matches_fancy_indexing, {}),
+    (ext.test_three_interpolate_one_hot_is_a_gather, {}),
+    (ext.test_three_interpolate_exact_on_small_integers, {}),
+    (ext.test_three_interpolate_padding_reads_zero, {}),
+    (ext.test_three_interpolate_backward_exact_on_small_integers, {}),
+    (ext.test_chamfer_brute_force_and_reductions, {}),
+    (ext.test_chamfer_lengths_equal_sliced_clouds, {}),
 ]
 
 
