@@ -169,6 +169,31 @@ int pc_knn(const float *query, int64_t B, int64_t Q, const float *ref,
            void *stream);
 
 /*
+ * kNN with per-cloud valid lengths and a choice of returned distance.
+ * Same selection as pc_knn (project page, "k nearest neighbors"), restricted
+ * per cloud b to queries i < query_lengths[b] and references
+ * j < ref_lengths[b] (the lengths masks of the project page's Chamfer and
+ * PyTorch3D-style contracts, "Roadmap" Phase 4 and "PyTorch3D-style Ball
+ * Query").
+ *
+ *   query_lengths, ref_lengths  [B] int64, device, or NULL (= Q, = N).
+ *              Values are clamped to [0, Q] and [0, N].
+ *   k          1 <= k <= 256; k > N is allowed here.
+ *   flags      0, or PC_KNN_SQUARED to return the squared distance s
+ *              instead of sqrt(s).
+ *   Rows i >= query_lengths[b], and slots past the cloud's valid reference
+ *   count, hold (index -1, distance 0).  Other outputs as pc_knn.
+ *
+ * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_UNSUPPORTED, PC_ERR_CUDA or
+ * PC_ERR_NO_DEVICE.
+ */
+#define PC_KNN_SQUARED 1
+int pc_knn_ex(const float *query, int64_t B, int64_t Q, const float *ref,
+              int64_t N, int64_t k, const int64_t *query_lengths,
+              const int64_t *ref_lengths, int flags, float *out_dist,
+              int64_t *out_idx, void *stream);
+
+/*
  * Ball Query: the first K references in input order inside the radius.
  * Project page, "Ball Query: first K within a radius"; "Numerical
  * contracts", "Selection and output":
@@ -186,6 +211,21 @@ int pc_knn(const float *query, int64_t B, int64_t Q, const float *ref,
 int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
                   int64_t N, double radius, int64_t K, float *out_dist2,
                   int64_t *out_idx, void *stream);
+
+/*
+ * Ball Query with per-cloud valid lengths: pc_ball_query restricted per cloud
+ * b to queries i < query_lengths[b] and references j < ref_lengths[b]
+ * (project page, "PyTorch3D-style Ball Query": lengths1, lengths2).
+ *
+ *   query_lengths, ref_lengths  [B] int64, device, or NULL (= Q, = N).
+ *              Values are clamped to [0, Q] and [0, N].
+ *   Rows i >= query_lengths[b] hold (index -1, distance 0) in every slot.
+ *   Other arguments and outputs as pc_ball_query.
+ */
+int pc_ball_query_ex(const float *query, int64_t B, int64_t Q,
+                     const float *ref, int64_t N, const int64_t *query_lengths,
+                     const int64_t *ref_lengths, double radius, int64_t K,
+                     float *out_dist2, int64_t *out_idx, void *stream);
 
 /*
  * Exact grid-accelerated kNN and Ball Query.
@@ -221,6 +261,95 @@ int pc_knn_grid(const float *query, int64_t B, int64_t Q, const void *grid,
 int pc_ball_query_grid(const float *query, int64_t B, int64_t Q,
                        const void *grid, int64_t N, double radius, int64_t K,
                        float *out_dist2, int64_t *out_idx, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Chamfer distance, PointNet++ feature propagation, neighbor gather.
+ * ---------------------------------------------------------------------- */
+
+typedef enum pc_reduction {
+    PC_REDUCTION_NONE = 0,
+    PC_REDUCTION_SUM = 1,
+    PC_REDUCTION_MEAN = 2
+} pc_reduction;
+
+/*
+ * Bidirectional squared-L2 Chamfer distance, forward.  Project page, "Quick
+ * start" (chamfer_distance) and "Roadmap", Phase 4:
+ *   L = sum_i |x_i - y_a(i)|^2 + sum_j |y_j - x_b(j)|^2,
+ * a(i) the nearest valid point of y to x_i and b(j) the nearest valid point
+ * of x to y_j, found exactly as pc_knn_ex with k = 1 (smallest s, ties to the
+ * smaller index).
+ *
+ *   x [B, P1, 3], y [B, P2, 3]  float32, device.
+ *   x_lengths, y_lengths  [B] int64, device, or NULL; clamped to [0, P].
+ *              Points past a cloud's length are neither queries nor
+ *              references.
+ *   weights    [B] float32, device, or NULL: each cloud's loss is scaled.
+ *   point_reduction  PC_REDUCTION_SUM or PC_REDUCTION_MEAN (a cloud's sum
+ *              divided by max(length, 1)).
+ *   batch_reduction  PC_REDUCTION_NONE (out_loss [B]), SUM or MEAN (out_loss
+ *              [1]; MEAN divides by B).
+ *   single_directional  nonzero: only the x -> y term (out_*_y unused).
+ *   out_dist_x [B, P1] float32, out_idx_x [B, P1] int64: squared distance and
+ *              index of each x point's nearest y point ((0, -1) for masked
+ *              points and for clouds without valid y points).
+ *   out_dist_y, out_idx_y  [B, P2], the other direction.
+ *   out_loss   float32, device, or NULL (no reduction).  Sums are formed in
+ *              float64 in a fixed order and rounded once to float32.
+ * Launches: two kNN kernels and one reduction kernel.
+ *
+ * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_UNSUPPORTED, PC_ERR_CUDA or
+ * PC_ERR_NO_DEVICE.
+ */
+int pc_chamfer(const float *x, int64_t B, int64_t P1, const float *y,
+               int64_t P2, const int64_t *x_lengths, const int64_t *y_lengths,
+               const float *weights, int point_reduction, int batch_reduction,
+               int single_directional, float *out_dist_x, int64_t *out_idx_x,
+               float *out_dist_y, int64_t *out_idx_y, float *out_loss,
+               void *stream);
+
+/*
+ * three_interpolate, forward.  Project page, "Quick start" and "Roadmap",
+ * Phase 2 (PointNet++ feature propagation with externally computed weights):
+ *   out[b,c,i] = (w0 f[b,c,m0] + w1 f[b,c,m1]) + w2 f[b,c,m2],
+ *   (m_t, w_t) = (idx[b,i,t], weight[b,i,t]); float32, each product and sum
+ *   rounded separately in that order.
+ *
+ *   features [B, C, M] float32, idx [B, n, 3] int64, weight [B, n, 3]
+ *   float32, out [B, C, n] float32; all device.
+ *   idx = -1 reads the feature as 0 (padding).  Any other index outside
+ *   [0, M) is also read as 0 and sets PC_ERR_INVALID_ARGUMENT in the device
+ *   status word (pc_device_status).
+ */
+int pc_three_interpolate(const float *features, int64_t B, int64_t C,
+                         int64_t M, const int64_t *idx, const float *weight,
+                         int64_t n, float *out, void *stream);
+
+/*
+ * three_interpolate, backward ("Roadmap", Phase 2: gradients accumulated into
+ * the input features):
+ *   grad_features[b,c,m] = sum over (i, t) with idx[b,i,t] = m of
+ *                          weight[b,i,t] * grad_out[b,c,i].
+ * grad_features [B, C, M] is overwritten (zeroed, then accumulated with
+ * float32 atomic adds: the summation order is not fixed).  Index rules as
+ * pc_three_interpolate.
+ */
+int pc_three_interpolate_backward(const float *grad_out, int64_t B, int64_t C,
+                                  int64_t n, const int64_t *idx,
+                                  const float *weight, int64_t M,
+                                  float *grad_features, void *stream);
+
+/*
+ * Neighbor coordinates for a [B, Q, K] index tensor (project page,
+ * "PyTorch3D-style Ball Query": return_nn, zero coordinates where idx = -1):
+ *   out[b,q,t,:] = xyz[b, idx[b,q,t], :], or (0, 0, 0) for idx = -1.
+ *   xyz [B, N, 3] float32, idx [B, Q, K] int64, out [B, Q, K, 3] float32;
+ *   device.  Other out-of-range indices give zeros and set
+ *   PC_ERR_INVALID_ARGUMENT in the device status word.
+ */
+int pc_gather_points(const float *xyz, int64_t B, int64_t N,
+                     const int64_t *idx, int64_t Q, int64_t K, float *out,
+                     void *stream);
 
 /*
  * Device status word.  Kernels that wait on other thread blocks bound every

@@ -238,54 +238,83 @@ int pc_fps(const float *xyz, int64_t B, int64_t N, int64_t npoint,
                      workspace_bytes, PC_FPS_AUTO, 0, 0, stream);
 }
 
-int pc_knn(const float *query, int64_t B, int64_t Q, const float *ref,
-           int64_t N, int64_t k, float *out_dist, int64_t *out_idx,
-           void *stream) {
+// Shared validation and launch of kNN; `strict` enforces the plain
+// operator's k <= N rule (the ex form pads instead).
+static int knn_common(const char *name, const float *query, int64_t B,
+                      int64_t Q, const float *ref, int64_t N, int64_t k,
+                      const int64_t *q_len, const int64_t *r_len, int flags,
+                      bool strict, float *out_dist, int64_t *out_idx,
+                      void *stream) {
     if (B < 0 || Q < 0 || N < 0)
-        return fail(PC_ERR_INVALID_ARGUMENT, "knn: negative size");
-    if (k < 1 || k > N)
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s: negative size", name);
+    if (k < 1 || (strict && k > N))
         return fail(PC_ERR_INVALID_ARGUMENT,
-                    "knn: need 1 <= k <= N (got k=%lld, N=%lld)", (long long)k,
-                    (long long)N);
+                    "%s: need 1 <= k <= N (got k=%lld, N=%lld)", name,
+                    (long long)k, (long long)N);
+    if ((flags & ~PC_KNN_SQUARED) != 0)
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s: unknown flags 0x%x", name, flags);
     if (k > 256)
-        return fail(PC_ERR_UNSUPPORTED, "knn: k=%lld above the maximum 256",
+        return fail(PC_ERR_UNSUPPORTED, "%s: k=%lld above the maximum 256", name,
                     (long long)k);
     if (B > 65535)
-        return fail(PC_ERR_UNSUPPORTED, "knn: B=%lld above 65535", (long long)B);
+        return fail(PC_ERR_UNSUPPORTED, "%s: B=%lld above 65535", name, (long long)B);
     if (Q > kMaxInt || N > kMaxInt || !mul_ok(B, Q, k) || !mul_ok(B, N, 3) ||
         !mul_ok(B, Q, 3))
-        return fail(PC_ERR_UNSUPPORTED, "knn: sizes beyond 32-bit indexing");
+        return fail(PC_ERR_UNSUPPORTED, "%s: sizes beyond 32-bit indexing", name);
     if (B == 0 || Q == 0) return PC_OK;
     const pcn::DeviceInfo *dev = nullptr;
     int rc = current_device(&dev);
     if (rc != PC_OK) return rc;
     if ((rc = check_ptr(query, dev->device, 4, "query")) != PC_OK) return rc;
-    if ((rc = check_ptr(ref, dev->device, 4, "ref")) != PC_OK) return rc;
+    if (N > 0 && (rc = check_ptr(ref, dev->device, 4, "ref")) != PC_OK) return rc;
     if ((rc = check_ptr(out_dist, dev->device, 4, "out_dist")) != PC_OK) return rc;
     if ((rc = check_ptr(out_idx, dev->device, 8, "out_idx")) != PC_OK) return rc;
-    cudaError_t e = pcn::launch_knn(*dev, query, B, Q, ref, N, int(k), out_dist,
-                                    out_idx, static_cast<cudaStream_t>(stream));
+    if (q_len && (rc = check_ptr(q_len, dev->device, 8, "query_lengths")) != PC_OK)
+        return rc;
+    if (r_len && (rc = check_ptr(r_len, dev->device, 8, "ref_lengths")) != PC_OK)
+        return rc;
+    cudaError_t e = pcn::launch_knn(*dev, query, B, Q, ref, N, int(k), q_len,
+                                    r_len, (flags & PC_KNN_SQUARED) != 0,
+                                    out_dist, out_idx,
+                                    static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "knn: launch");
     return PC_OK;
 }
 
-int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
-                  int64_t N, double radius, int64_t K, float *out_dist2,
-                  int64_t *out_idx, void *stream) {
+int pc_knn(const float *query, int64_t B, int64_t Q, const float *ref,
+           int64_t N, int64_t k, float *out_dist, int64_t *out_idx,
+           void *stream) {
+    return knn_common("knn", query, B, Q, ref, N, k, nullptr, nullptr, 0, true,
+                      out_dist, out_idx, stream);
+}
+
+int pc_knn_ex(const float *query, int64_t B, int64_t Q, const float *ref,
+              int64_t N, int64_t k, const int64_t *query_lengths,
+              const int64_t *ref_lengths, int flags, float *out_dist,
+              int64_t *out_idx, void *stream) {
+    return knn_common("knn_ex", query, B, Q, ref, N, k, query_lengths,
+                      ref_lengths, flags, false, out_dist, out_idx, stream);
+}
+
+static int bq_common(const char *name, const float *query, int64_t B,
+                     int64_t Q, const float *ref, int64_t N,
+                     const int64_t *q_len, const int64_t *r_len, double radius,
+                     int64_t K, float *out_dist2, int64_t *out_idx,
+                     void *stream) {
     if (B < 0 || Q < 0 || N < 0)
-        return fail(PC_ERR_INVALID_ARGUMENT, "ball_query: negative size");
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s: negative size", name);
     if (!std::isfinite(radius) || !(radius > 0.0))
         return fail(PC_ERR_INVALID_ARGUMENT,
-                    "ball_query: radius must be finite and > 0 (got %g)", radius);
+                    "%s: radius must be finite and > 0 (got %g)", name, radius);
     if (K < 1)
-        return fail(PC_ERR_INVALID_ARGUMENT, "ball_query: need K >= 1 (got %lld)",
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s: need K >= 1 (got %lld)", name,
                     (long long)K);
     if (B > 65535)
-        return fail(PC_ERR_UNSUPPORTED, "ball_query: B=%lld above 65535",
+        return fail(PC_ERR_UNSUPPORTED, "%s: B=%lld above 65535", name,
                     (long long)B);
     if (Q > kMaxInt || N > kMaxInt || K > kMaxInt || !mul_ok(B, Q, K) ||
         !mul_ok(B, N, 3) || !mul_ok(B, Q, 3))
-        return fail(PC_ERR_UNSUPPORTED, "ball_query: sizes beyond 32-bit indexing");
+        return fail(PC_ERR_UNSUPPORTED, "%s: sizes beyond 32-bit indexing", name);
     if (B == 0 || Q == 0) return PC_OK;
     const pcn::DeviceInfo *dev = nullptr;
     int rc = current_device(&dev);
@@ -294,12 +323,31 @@ int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
     if (N > 0 && (rc = check_ptr(ref, dev->device, 4, "ref")) != PC_OK) return rc;
     if ((rc = check_ptr(out_dist2, dev->device, 4, "out_dist2")) != PC_OK) return rc;
     if ((rc = check_ptr(out_idx, dev->device, 8, "out_idx")) != PC_OK) return rc;
+    if (q_len && (rc = check_ptr(q_len, dev->device, 8, "query_lengths")) != PC_OK)
+        return rc;
+    if (r_len && (rc = check_ptr(r_len, dev->device, 8, "ref_lengths")) != PC_OK)
+        return rc;
     const float r32 = static_cast<float>(radius);
-    cudaError_t e = pcn::launch_ball_query(*dev, query, B, Q, ref, N, r32, K,
-                                           out_dist2, out_idx,
+    cudaError_t e = pcn::launch_ball_query(*dev, query, B, Q, ref, N, q_len,
+                                           r_len, r32, K, out_dist2, out_idx,
                                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "ball_query: launch");
     return PC_OK;
+}
+
+int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
+                  int64_t N, double radius, int64_t K, float *out_dist2,
+                  int64_t *out_idx, void *stream) {
+    return bq_common("ball_query", query, B, Q, ref, N, nullptr, nullptr,
+                     radius, K, out_dist2, out_idx, stream);
+}
+
+int pc_ball_query_ex(const float *query, int64_t B, int64_t Q,
+                     const float *ref, int64_t N, const int64_t *query_lengths,
+                     const int64_t *ref_lengths, double radius, int64_t K,
+                     float *out_dist2, int64_t *out_idx, void *stream) {
+    return bq_common("ball_query_ex", query, B, Q, ref, N, query_lengths,
+                     ref_lengths, radius, K, out_dist2, out_idx, stream);
 }
 
 int pc_device_status(void *stream, int reset, int32_t *out_status) {

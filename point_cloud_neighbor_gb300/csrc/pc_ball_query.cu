@@ -48,11 +48,12 @@ constexpr unsigned FULL = 0xffffffffu;
 struct BqArgs {
     const float *query;
     const float *ref;
+    const int64_t *q_len;  // valid queries per cloud (NULL: Q)
+    const int64_t *r_len;  // valid references per cloud (NULL: N)
     int Q, N;
     float R2;
     int K;
     int q_per_warp;
-    int ntiles;
     float *out_dist2;
     int64_t *out_idx;
     int *status;
@@ -74,6 +75,13 @@ __host__ __device__ constexpr size_t bq_fixed_smem() {
 
 __device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
 __device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+
+// Valid length of cloud b: lens[b] clamped to [0, full], or full.
+__device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
+    if (lens == nullptr) return full;
+    const int64_t v = lens[b];
+    return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
+}
 
 // Slow path, taken only when a vote found a hit: recompute the tile's
 // distances for this query and record the hits in input order.  Returns the
@@ -130,6 +138,22 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     BqSlot *slots_all = reinterpret_cast<BqSlot *>(smem + bq_fixed_smem());
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
+    const int Nb = valid_len(a.r_len, b, a.N);
+    const int Qb = valid_len(a.q_len, b, a.Q);
+    const int ntiles = (Nb + BQ_T - 1) / BQ_T;
+
+    if (blockIdx.x * BQ_CWARPS * G >= Qb) {
+        // every query of this block is past the cloud's valid length
+        const int r0 = blockIdx.x * BQ_CWARPS * G;
+        const int r1 = min(a.Q, r0 + BQ_CWARPS * G);
+        const size_t e0 = (size_t(b) * a.Q + r0) * K;
+        const size_t e1 = (size_t(b) * a.Q + r1) * K;
+        for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+            a.out_idx[e] = -1;
+            a.out_dist2[e] = 0.0f;
+        }
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < BQ_STAGES; ++s) {
@@ -146,13 +170,13 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
         __syncthreads();
         if (lane == 0)
             ring_produce<BQ_STAGES>(
-                ring, cref, a.N, BQ_T, a.ntiles, [](int it) { return it; },
+                ring, cref, Nb, BQ_T, ntiles, [](int it) { return it; },
                 s_stop, s_err, a.timeout_ns);
         return;
     }
 
     const int q_warp0 = (blockIdx.x * BQ_CWARPS + warp) * G;
-    const int nq = max(0, min(G, a.Q - q_warp0));
+    const int nq = max(0, min(G, Qb - q_warp0));
     BqSlot *slots = slots_all + warp * G;
     const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
     for (int g = lane; g < G; g += 32) {
@@ -177,7 +201,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
         *vstop = 1;
     const float2 nz0 = make_float2(a.negzero, a.negzero);
     bool failed = false;
-    for (int it = 0; it < a.ntiles; ++it) {
+    for (int it = 0; it < ntiles; ++it) {
         if (__any_sync(FULL, *vstop != 0)) break;
         const int st = it % BQ_STAGES;
         const WaitResult w = mbar_wait_or_stop(
@@ -187,7 +211,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             break;
         }
         const int j0 = it * BQ_T;
-        const int cnt = min(BQ_T, a.N - j0);
+        const int cnt = min(BQ_T, Nb - j0);
         const float *buf =
             ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
         float2 rx[BQ_R / 2], ry[BQ_R / 2], rz[BQ_R / 2];
@@ -255,8 +279,17 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
         }
         raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
     }
-    // pad the unused slots with (-1, 0); after a failure every slot
+    // pad the unused slots with (-1, 0); after a failure every slot; rows
+    // past the valid length in full
     __syncwarp();
+    const int nrows = max(0, min(G, a.Q - q_warp0));
+    for (int g = nq; g < nrows; ++g) {
+        const size_t row = size_t(b) * a.Q + q_warp0 + g;
+        for (int e = lane; e < K; e += 32) {
+            a.out_idx[row * K + e] = -1;
+            a.out_dist2[row * K + e] = 0.0f;
+        }
+    }
     for (int g = 0; g < nq; ++g) {
         const BqSlot q = slots[g];
         const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(q.nzh.w);
@@ -272,17 +305,19 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
 
 cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
                               int64_t B, int64_t Q, const float *ref,
-                              int64_t N, float r32, int64_t K,
+                              int64_t N, const int64_t *q_len,
+                              const int64_t *r_len, float r32, int64_t K,
                               float *out_dist2, int64_t *out_idx,
                               cudaStream_t stream) {
     BqArgs a{};
     a.query = query;
     a.ref = ref;
+    a.q_len = q_len;
+    a.r_len = r_len;
     a.Q = static_cast<int>(Q);
     a.N = static_cast<int>(N);
     a.R2 = r32 * r32;  // fl32(fl32(r) * fl32(r)): a single float multiply
     a.K = static_cast<int>(K);
-    a.ntiles = static_cast<int>((N + BQ_T - 1) / BQ_T);
     a.out_dist2 = out_dist2;
     a.out_idx = out_idx;
     a.status = dev.status_word;

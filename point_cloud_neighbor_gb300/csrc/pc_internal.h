@@ -44,13 +44,17 @@ struct ScanPlan {       // kNN / Ball Query
 };
 
 // Launchers: enqueue on `stream`, return the first CUDA error.
+// q_len / r_len: valid queries / references per cloud (device, NULL = all);
+// rows past q_len and slots past r_len are padded with (-1, 0).
 cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
                        int64_t Q, const float *ref, int64_t N, int k,
+                       const int64_t *q_len, const int64_t *r_len, bool squared,
                        float *out_dist, int64_t *out_idx, cudaStream_t stream);
 
 cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
                               int64_t B, int64_t Q, const float *ref,
-                              int64_t N, float r32, int64_t K,
+                              int64_t N, const int64_t *q_len,
+                              const int64_t *r_len, float r32, int64_t K,
                               float *out_dist2, int64_t *out_idx,
                               cudaStream_t stream);
 

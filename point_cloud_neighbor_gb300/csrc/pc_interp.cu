@@ -1,0 +1,243 @@
+// pc_interp.cu -- PointNet++ feature propagation (three_interpolate forward
+// and backward) and the neighbor-coordinate gather on sm_103a.
+//
+// three_interpolate (mps-pointops project page, "Quick start"; "Roadmap",
+// Phase 2: externally computed weights, gradients accumulated into the input
+// features):
+//   out[b,c,i] = sum_{t<3} w[b,i,t] f[b,c,idx[b,i,t]]     f [B,C,M], out [B,C,n]
+//   grad_f[b,c,m] += w[b,i,t] g[b,c,i]  for every idx[b,i,t] = m.
+// Forward: float32, products and sums rounded separately in the order
+// ((w0 f0 + w1 f1) + w2 f2), so the result is bit-identical to the oracle's.
+// Backward: float32 atomic adds (reduction order unspecified, as the pages
+// allow for accumulated gradients).  idx = -1 is padding (reads 0, adds
+// nothing); any other index outside [0, M) sets PC_ERR_INVALID_ARGUMENT in
+// the device status word and is treated as padding.
+//
+// Both kernels stream the [.., n] axis with one thread per point i (loads of
+// out / grad_out coalesced along i) and loop over a chunk of channels, so the
+// three indices and weights of a point are read once per chunk; the gathers
+// from f hit L2 (a [C, M] feature block is re-read across the chunk's points).
+//
+// gather_points (project page, "PyTorch3D-style Ball Query": return_nn gives
+// the neighbor coordinates, zeros where idx = -1):
+//   out[b,q,t,:] = x[b, idx[b,q,t], :].
+#include "pointcloud.h"
+#include "pc_device.cuh"
+#include "pc_internal.h"
+
+#include <algorithm>
+#include <cstdio>
+
+namespace pcn {
+namespace {
+
+constexpr int INTERP_THREADS = 128;
+constexpr int INTERP_CCHUNK = 16;  // channels per block
+
+// Load the three (index, weight) pairs of point i; bad indices become padding
+// and raise the status word.
+__device__ __forceinline__ void load_triplet(const int64_t *idx,
+                                             const float *w, size_t base,
+                                             int M, int (&m)[3], float (&wt)[3],
+                                             int *status) {
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+        const int64_t v = idx[base + t];
+        wt[t] = w[base + t];
+        if (v == -1) {
+            m[t] = -1;
+        } else if (v < 0 || v >= M) {
+            m[t] = -1;
+            raise_status(status, PC_ERR_INVALID_ARGUMENT);
+        } else {
+            m[t] = static_cast<int>(v);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(INTERP_THREADS)
+three_interpolate_kernel(const float *__restrict__ f,
+                         const int64_t *__restrict__ idx,
+                         const float *__restrict__ w, int C, int M, int n,
+                         float *__restrict__ out, int *status) {
+    const int i = blockIdx.x * INTERP_THREADS + threadIdx.x;
+    if (i >= n) return;
+    const int b = blockIdx.z;
+    const int c0 = blockIdx.y * INTERP_CCHUNK;
+    const int c1 = min(C, c0 + INTERP_CCHUNK);
+    int m[3];
+    float wt[3];
+    load_triplet(idx, w, (size_t(b) * n + i) * 3, M, m, wt, status);
+#pragma unroll 4
+    for (int c = c0; c < c1; ++c) {
+        const float *fr = f + (size_t(b) * C + c) * size_t(M);
+        const float v0 = m[0] >= 0 ? __ldg(fr + m[0]) : 0.0f;
+        const float v1 = m[1] >= 0 ? __ldg(fr + m[1]) : 0.0f;
+        const float v2 = m[2] >= 0 ? __ldg(fr + m[2]) : 0.0f;
+        const float s01 = __fadd_rn(__fmul_rn(wt[0], v0), __fmul_rn(wt[1], v1));
+        out[(size_t(b) * C + c) * size_t(n) + i] = __fadd_rn(s01, __fmul_rn(wt[2], v2));
+    }
+}
+
+__global__ void __launch_bounds__(INTERP_THREADS)
+three_interpolate_backward_kernel(const float *__restrict__ g,
+                                  const int64_t *__restrict__ idx,
+                                  const float *__restrict__ w, int C, int M,
+                                  int n, float *grad_f, int *status) {
+    const int i = blockIdx.x * INTERP_THREADS + threadIdx.x;
+    if (i >= n) return;
+    const int b = blockIdx.z;
+    const int c0 = blockIdx.y * INTERP_CCHUNK;
+    const int c1 = min(C, c0 + INTERP_CCHUNK);
+    int m[3];
+    float wt[3];
+    load_triplet(idx, w, (size_t(b) * n + i) * 3, M, m, wt, status);
+#pragma unroll 4
+    for (int c = c0; c < c1; ++c) {
+        const float gv = __ldg(g + (size_t(b) * C + c) * size_t(n) + i);
+        float *gr = grad_f + (size_t(b) * C + c) * size_t(M);
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+            if (m[t] >= 0) atomicAdd(gr + m[t], __fmul_rn(wt[t], gv));
+    }
+}
+
+__global__ void gather_points_kernel(const float *__restrict__ x, int N,
+                                     const int64_t *__restrict__ idx,
+                                     int64_t QK, int64_t total,
+                                     float *__restrict__ out, int *status) {
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t b = e / QK;
+        const int64_t j = idx[e];
+        float px = 0.f, py = 0.f, pz = 0.f;
+        if (j >= 0 && j < N) {
+            const float *p = x + (size_t(b) * N + size_t(j)) * 3;
+            px = p[0];
+            py = p[1];
+            pz = p[2];
+        } else if (j != -1) {
+            raise_status(status, PC_ERR_INVALID_ARGUMENT);
+        }
+        out[e * 3 + 0] = px;
+        out[e * 3 + 1] = py;
+        out[e * 3 + 2] = pz;
+    }
+}
+
+}  // namespace
+}  // namespace pcn
+
+namespace {
+
+constexpr int64_t kMaxInt = 2147483647;
+
+int cuda_err(cudaError_t e, const char *what) {
+    char m[200];
+    std::snprintf(m, sizeof(m), "%s: %s", what, cudaGetErrorString(e));
+    return pcn::api_fail(PC_ERR_CUDA, m);
+}
+
+// Sizes of a [B, C, n] / [B, C, M] problem: non-negative, within 32-bit
+// point indexing and 2^40 elements per tensor.
+int interp_sizes(const char *what, int64_t B, int64_t C, int64_t M, int64_t n) {
+    char m[200];
+    if (B < 0 || C < 0 || M < 0 || n < 0) {
+        std::snprintf(m, sizeof(m), "%s: negative size", what);
+        return pcn::api_fail(PC_ERR_INVALID_ARGUMENT, m);
+    }
+    const int64_t lim = int64_t(1) << 40;
+    const int64_t longest = std::max<int64_t>(std::max<int64_t>(M, n), 1);
+    if (B > 65535 || C > int64_t(65535) * 16 || M > kMaxInt || n > kMaxInt ||
+        B * C > lim / longest) {
+        std::snprintf(m, sizeof(m), "%s: sizes beyond the supported range", what);
+        return pcn::api_fail(PC_ERR_UNSUPPORTED, m);
+    }
+    return PC_OK;
+}
+
+}  // namespace
+
+extern "C" int pc_three_interpolate(const float *features, int64_t B,
+                                    int64_t C, int64_t M, const int64_t *idx,
+                                    const float *weight, int64_t n, float *out,
+                                    void *stream) {
+    int rc = interp_sizes("three_interpolate", B, C, M, n);
+    if (rc != PC_OK) return rc;
+    if (B == 0 || C == 0 || n == 0) return PC_OK;
+    const pcn::DeviceInfo *dev = nullptr;
+    if ((rc = pcn::api_current_device(&dev)) != PC_OK) return rc;
+    const int d = dev->device;
+    if (M > 0 && (rc = pcn::api_check_ptr(features, d, 4, "features")) != PC_OK) return rc;
+    if ((rc = pcn::api_check_ptr(idx, d, 8, "idx")) != PC_OK) return rc;
+    if ((rc = pcn::api_check_ptr(weight, d, 4, "weight")) != PC_OK) return rc;
+    if ((rc = pcn::api_check_ptr(out, d, 4, "out")) != PC_OK) return rc;
+    const dim3 grid(unsigned((n + pcn::INTERP_THREADS - 1) / pcn::INTERP_THREADS),
+                    unsigned((C + pcn::INTERP_CCHUNK - 1) / pcn::INTERP_CCHUNK),
+                    unsigned(B));
+    pcn::three_interpolate_kernel<<<grid, pcn::INTERP_THREADS, 0,
+                                    static_cast<cudaStream_t>(stream)>>>(
+        features, idx, weight, int(C), int(M), int(n), out, dev->status_word);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PC_OK : cuda_err(e, "three_interpolate: launch");
+}
+
+extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
+                                             int64_t C, int64_t n,
+                                             const int64_t *idx,
+                                             const float *weight, int64_t M,
+                                             float *grad_features,
+                                             void *stream) {
+    int rc = interp_sizes("three_interpolate_backward", B, C, M, n);
+    if (rc != PC_OK) return rc;
+    if (B == 0 || C == 0 || M == 0) return PC_OK;
+    const pcn::DeviceInfo *dev = nullptr;
+    if ((rc = pcn::api_current_device(&dev)) != PC_OK) return rc;
+    const int d = dev->device;
+    if ((rc = pcn::api_check_ptr(grad_features, d, 4, "grad_features")) != PC_OK)
+        return rc;
+    if (n > 0) {
+        if ((rc = pcn::api_check_ptr(grad_out, d, 4, "grad_out")) != PC_OK) return rc;
+        if ((rc = pcn::api_check_ptr(idx, d, 8, "idx")) != PC_OK) return rc;
+        if ((rc = pcn::api_check_ptr(weight, d, 4, "weight")) != PC_OK) return rc;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(grad_features, 0,
+                                    size_t(B) * size_t(C) * size_t(M) * sizeof(float), st);
+    if (e == cudaSuccess && n > 0) {
+        const dim3 grid(unsigned((n + pcn::INTERP_THREADS - 1) / pcn::INTERP_THREADS),
+                        unsigned((C + pcn::INTERP_CCHUNK - 1) / pcn::INTERP_CCHUNK),
+                        unsigned(B));
+        pcn::three_interpolate_backward_kernel<<<grid, pcn::INTERP_THREADS, 0, st>>>(
+            grad_out, idx, weight, int(C), int(M), int(n), grad_features,
+            dev->status_word);
+        e = cudaGetLastError();
+    }
+    return e == cudaSuccess ? PC_OK : cuda_err(e, "three_interpolate_backward");
+}
+
+extern "C" int pc_gather_points(const float *xyz, int64_t B, int64_t N,
+                                const int64_t *idx, int64_t Q, int64_t K,
+                                float *out, void *stream) {
+    if (B < 0 || N < 0 || Q < 0 || K < 0)
+        return pcn::api_fail(PC_ERR_INVALID_ARGUMENT, "gather_points: negative size");
+    if (N > kMaxInt || B > 65535 || (Q > 0 && K > (int64_t(1) << 40) / Q) ||
+        (Q * K > 0 && B > (int64_t(1) << 40) / (Q * K)))
+        return pcn::api_fail(PC_ERR_UNSUPPORTED, "gather_points: sizes beyond the supported range");
+    const int64_t total = B * Q * K;
+    if (total == 0) return PC_OK;
+    const pcn::DeviceInfo *dev = nullptr;
+    int rc = pcn::api_current_device(&dev);
+    if (rc != PC_OK) return rc;
+    const int d = dev->device;
+    if (N > 0 && (rc = pcn::api_check_ptr(xyz, d, 4, "xyz")) != PC_OK) return rc;
+    if ((rc = pcn::api_check_ptr(idx, d, 8, "idx")) != PC_OK) return rc;
+    if ((rc = pcn::api_check_ptr(out, d, 4, "out")) != PC_OK) return rc;
+    const int64_t blocks = (total + 255) / 256;
+    const unsigned grid = unsigned(blocks < int64_t(dev->sm_count) * 16 ? blocks
+                                                                       : int64_t(dev->sm_count) * 16);
+    pcn::gather_points_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        xyz, int(N), idx, Q * K, total, out, dev->status_word);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PC_OK : cuda_err(e, "gather_points: launch");
+}

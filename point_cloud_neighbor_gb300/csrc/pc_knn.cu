@@ -52,9 +52,11 @@ constexpr unsigned FULL = 0xffffffffu;
 struct KnnArgs {
     const float *query;
     const float *ref;
+    const int64_t *q_len;  // valid queries per cloud (NULL: Q)
+    const int64_t *r_len;  // valid references per cloud (NULL: N)
     int Q, N, k;
+    int squared;           // return s instead of sqrt(s)
     int q_per_warp;
-    int ntiles, tile_stride;
     float *out_dist;
     int64_t *out_idx;
     int *status;
@@ -81,9 +83,33 @@ __host__ __device__ constexpr size_t knn_per_query_smem(int k) {
     return sizeof(QuerySlot) + size_t(k) * (sizeof(float) + sizeof(int));
 }
 
-__device__ __forceinline__ int knn_tile_at(const KnnArgs &a, int it) {
-    return static_cast<int>((static_cast<long long>(it) * a.tile_stride) %
-                            a.ntiles);
+__device__ __forceinline__ int gcd_int(int a, int b) {
+    while (b) {
+        const int t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+// A stride near 0.618 * n that is coprime with n, so that it*stride mod n
+// visits every tile once (the project page's scrambled chunk order).
+__device__ __forceinline__ int scramble_stride(int n) {
+    if (n <= 2) return 1;
+    int s = max(1, static_cast<int>(0.6180339887 * n));
+    while (gcd_int(s, n) != 1) ++s;
+    return s % n == 0 ? 1 : s;
+}
+
+__device__ __forceinline__ int knn_tile_at(int it, int stride, int ntiles) {
+    return static_cast<int>((static_cast<long long>(it) * stride) % ntiles);
+}
+
+// Valid length of cloud b: lens[b] clamped to [0, full], or full.
+__device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
+    if (lens == nullptr) return full;
+    const int64_t v = lens[b];
+    return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
 }
 
 __device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
@@ -233,6 +259,23 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
     int *lj_all = reinterpret_cast<int *>(ls_all + size_t(KNN_CWARPS) * G * k);
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
+    const int Nb = valid_len(a.r_len, b, a.N);
+    const int Qb = valid_len(a.q_len, b, a.Q);
+    const int ntiles = (Nb + KNN_T - 1) / KNN_T;
+    const int tstride = scramble_stride(ntiles);
+
+    if (blockIdx.x * KNN_CWARPS * G >= Qb) {
+        // every query of this block is past the cloud's valid length
+        const int r0 = blockIdx.x * KNN_CWARPS * G;
+        const int r1 = min(a.Q, r0 + KNN_CWARPS * G);
+        const size_t e0 = (size_t(b) * a.Q + r0) * k;
+        const size_t e1 = (size_t(b) * a.Q + r1) * k;
+        for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+            a.out_idx[e] = -1;
+            a.out_dist[e] = 0.0f;
+        }
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < KNN_STAGES; ++s) {
@@ -247,15 +290,16 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         __syncthreads();
         if (lane == 0)
             ring_produce<KNN_STAGES>(
-                ring, cref, a.N, KNN_T, a.ntiles,
-                [&](int it) { return knn_tile_at(a, it); }, s_err, s_err,
+                ring, cref, Nb, KNN_T, ntiles,
+                [&](int it) { return knn_tile_at(it, tstride, ntiles); }, s_err,
+                s_err,
                 a.timeout_ns);
         return;
     }
 
     // consumer warp: set up this warp's queries and lists
     const int q_warp0 = (blockIdx.x * KNN_CWARPS + warp) * G;
-    const int nq = max(0, min(G, a.Q - q_warp0));
+    const int nq = max(0, min(G, Qb - q_warp0));
     QuerySlot *slots = slots_all + warp * G;
     float *ls_w = ls_all + size_t(warp) * G * k;
     int *lj_w = lj_all + size_t(warp) * G * k;
@@ -281,7 +325,7 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 
     const float2 nz0 = make_float2(a.negzero, a.negzero);
     bool failed = false;
-    for (int it = 0; it < a.ntiles; ++it) {
+    for (int it = 0; it < ntiles; ++it) {
         const int st = it % KNN_STAGES;
         const WaitResult w = mbar_wait_or_stop(
             &ring.full[st], unsigned((it / KNN_STAGES) & 1), s_err, a.timeout_ns);
@@ -289,8 +333,8 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
             failed = true;
             break;
         }
-        const int j0 = knn_tile_at(a, it) * KNN_T;
-        const int cnt = min(KNN_T, a.N - j0);
+        const int j0 = knn_tile_at(it, tstride, ntiles) * KNN_T;
+        const int cnt = min(KNN_T, Nb - j0);
         const float *buf =
             ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
         float2 rx[KNN_R / 2], ry[KNN_R / 2], rz[KNN_R / 2];
@@ -323,6 +367,15 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         }
     }
 
+    // rows of this warp past the valid length: padding
+    const int nrows = max(0, min(G, a.Q - q_warp0));
+    for (int g = nq; g < nrows; ++g) {
+        const size_t row = size_t(b) * a.Q + q_warp0 + g;
+        for (int e = lane; e < k; e += 32) {
+            a.out_idx[row * k + e] = -1;
+            a.out_dist[row * k + e] = 0.0f;
+        }
+    }
     if (failed) {
         if (lane == 0) *s_err = 1;
         raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
@@ -332,31 +385,17 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         }
         return;
     }
+    // slots past the number of valid references (k > Nb): padding
+    const int kv = min(k, Nb);
     for (int g = 0; g < nq; ++g) {
         const size_t row = size_t(b) * a.Q + q_warp0 + g;
         for (int e = lane; e < k; e += 32) {
-            a.out_idx[row * k + e] = lj_w[g * k + e];
-            a.out_dist[row * k + e] = __fsqrt_rn(ls_w[g * k + e]);
+            const float sv = ls_w[g * k + e];
+            a.out_idx[row * k + e] = e < kv ? int64_t(lj_w[g * k + e]) : int64_t(-1);
+            a.out_dist[row * k + e] =
+                e < kv ? (a.squared ? sv : __fsqrt_rn(sv)) : 0.0f;
         }
     }
-}
-
-int gcd_int(int a, int b) {
-    while (b) {
-        const int t = a % b;
-        a = b;
-        b = t;
-    }
-    return a;
-}
-
-// A stride near 0.618 * n that is coprime with n, so that it*stride mod n
-// visits every tile once.
-int scramble_stride(int n) {
-    if (n <= 2) return 1;
-    int s = std::max(1, static_cast<int>(0.6180339887 * n));
-    while (gcd_int(s, n) != 1) ++s;
-    return s % n == 0 ? 1 : s;
 }
 
 template <int KPL>
@@ -389,16 +428,18 @@ cudaError_t launch_knn_t(const DeviceInfo &dev, const KnnArgs &a0, int64_t B,
 
 cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
                        int64_t Q, const float *ref, int64_t N, int k,
+                       const int64_t *q_len, const int64_t *r_len, bool squared,
                        float *out_dist, int64_t *out_idx,
                        cudaStream_t stream) {
     KnnArgs a{};
     a.query = query;
     a.ref = ref;
+    a.q_len = q_len;
+    a.r_len = r_len;
     a.Q = static_cast<int>(Q);
     a.N = static_cast<int>(N);
     a.k = k;
-    a.ntiles = static_cast<int>((N + KNN_T - 1) / KNN_T);
-    a.tile_stride = scramble_stride(a.ntiles);
+    a.squared = squared ? 1 : 0;
     a.out_dist = out_dist;
     a.out_idx = out_idx;
     a.status = dev.status_word;
