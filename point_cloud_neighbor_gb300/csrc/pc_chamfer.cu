@@ -178,6 +178,7 @@ extern "C" int pc_chamfer(const float *x, int64_t B, int64_t P1,
         a.P2 = int(P2);
         a.point_mean = point_reduction == PC_REDUCTION_MEAN;
         a.batch_mode = batch_reduction;
+        a.out_loss = out_loss;
         pcn::chamfer_reduce_kernel<<<1, pcn::RED_THREADS, 0, st>>>(a);
         e = cudaGetLastError();
     }
