@@ -156,6 +156,8 @@ def default_threads() -> int:
 
 
 def _split(n: int, parts: int):
+    if n <= 0:
+        return []
     parts = max(1, min(parts, n))
     step = -(-n // parts)
     return [(i, min(n, i + step)) for i in range(0, n, step)]
