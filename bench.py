@@ -349,6 +349,9 @@ def run_gpu(args):
                            f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})")
 
     grid = run_grid(args, pc, x, flush, device, world)
+    next_rows = run_next_rows(args, pc, flush, device, world,
+                              with_oracle=(rank == 0 and world == 1
+                                           and not args.no_cpu_baseline))
 
     # end to end through the public API: pinned host in, pinned host out
     e2e = run_e2e(args, pc, x_host, device, world)
@@ -359,8 +362,11 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": workload_config({"parallelism": f"replicas x{world}"}),
-        "roofline": roof, "ops": ops, "grid": grid, "e2e": e2e,
+        "roofline": roof, "ops": ops, "grid": grid, "next_rows": next_rows,
+        "e2e": e2e,
         "gpu_launches": launches,
+        "gpu_launches_note": "the timed FPS + kNN + Ball Query step; the grid and "
+                             "next_rows sections are timed separately",
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"]},
         "wall_s_timed_loop": wall1 - wall0,
@@ -392,6 +398,20 @@ def run_only(args):
         "grid_ball_query": lambda: pc.pc_ball_query_grid(x, g, W["bq_radius"],
                                                          W["bq_K"]),
     }
+    if args.only in ("chamfer", "three_interpolate", "three_interpolate_backward"):
+        cx = torch.from_numpy(inputs.random_cloud(5, 4, 16384)).to(device)
+        cy = torch.from_numpy(inputs.random_cloud(6, 4, 16384)).to(device)
+        px = torch.from_numpy(inputs.pointnet2()).to(device)
+        centers = px[:, :1024].contiguous()
+        d, idx = pc.three_nn(px, centers)
+        w = (1.0 / (d + 1e-8))
+        w = (w / w.sum(-1, keepdim=True)).contiguous()
+        feats = torch.randn((16, 256, 1024), device=device)
+        gup = torch.randn((16, 256, 4096), device=device)
+        calls["chamfer"] = lambda: pc.pc_chamfer(cx, cy)
+        calls["three_interpolate"] = lambda: pc.pc_three_interpolate(feats, idx, w)
+        calls["three_interpolate_backward"] = lambda: pc.pc_three_interpolate_backward(
+            gup, idx, w, 1024)
     fn = calls[args.only]
     for _ in range(args.warmup):
         fn()
@@ -455,6 +475,128 @@ def run_grid(args, pc, x, flush, device, world):
             "note": "exact uniform-grid path (pc_grid_build + pc_knn_grid + "
                     "pc_ball_query_grid), grid rebuilt every step; identical "
                     "results to the brute-force kernels"}
+
+
+def _timed(fn, steps, warmup, flush, stream):
+    """Mean CUDA-event time (ms) of fn() over `steps` calls, L2 flushed
+    before each call."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        flush.zero_()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def run_next_rows(args, pc, flush, device, world, with_oracle):
+    """The operators built on the hot path, each on the workload the pages
+    time it on: Chamfer forward (batch 4, 16,384 points per cloud), the
+    PointNet++ feature-propagation three_interpolate (16 clouds, 1024 centers
+    -> 4096 points, 256 channels) and the PyTorch3D-style Ball Query (16
+    clouds, 1024 centers vs 4096 points, r = 0.2, K = 64, return_nn)."""
+    import torch
+    from point_cloud_neighbor_gb300 import inputs
+    from point_cloud_neighbor_gb300.pytorch3d import ball_query as p3d_ball_query
+    stream = torch.cuda.current_stream(device)
+    steps, warm = max(3, args.steps), max(3, args.warmup)
+    peaks, _ = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    alu = fp32_alu_peak_tflops(sm_count, float(peaks.get("sm_max_mhz", 2070.0)))
+    out = {}
+
+    # Chamfer forward
+    CB, CP = 4, 16384
+    cx_h = inputs.random_cloud(5, CB, CP)
+    cy_h = inputs.random_cloud(6, CB, CP)
+    cx, cy = torch.from_numpy(cx_h).to(device), torch.from_numpy(cy_h).to(device)
+    ms = _timed(lambda: pc.pc_chamfer(cx, cy), steps, warm, flush, stream)
+    pairs = 2.0 * CB * CP * CP
+    tfl = pairs * FLOPS_PER_PAIR / (ms / 1e3) / 1e12
+    out["chamfer"] = {
+        "workload": f"B={CB}, P1=P2={CP} uniform in [0,1)^3, bidirectional, point+batch mean",
+        "ms": ms, "clouds_per_s": CB * world / (ms / 1e3),
+        "pairs": pairs, "achieved_tflops": tfl,
+        "roofline": {"bound": "alu", "achieved": tfl, "peak": alu, "unit": "TFLOP/s",
+                     "frac": tfl / alu}, "launches": 3}
+
+    # three_interpolate forward / backward at the PointNet++ FP shape
+    TB, TM, TN, TC = 16, 1024, 4096, 256
+    px_h = inputs.pointnet2()                       # [16, 4096, 3]
+    px = torch.from_numpy(px_h).to(device)
+    centers = torch.from_numpy(np.ascontiguousarray(px_h[:, :TM])).to(device)
+    d, idx = pc.three_nn(px, centers)
+    w = 1.0 / (d + 1e-8)
+    w = (w / w.sum(-1, keepdim=True)).contiguous()
+    feats = torch.randn((TB, TC, TM), generator=torch.Generator(device="cpu").manual_seed(7)).to(device)
+    g = torch.randn((TB, TC, TN), generator=torch.Generator(device="cpu").manual_seed(8)).to(device)
+    fout = torch.empty((TB, TC, TN), dtype=torch.float32, device=device)
+    gout = torch.empty((TB, TC, TM), dtype=torch.float32, device=device)
+    fwd = _timed(lambda: pc.pc_three_interpolate(feats, idx, w, out=fout), steps, warm,
+                 flush, stream)
+    bwd = _timed(lambda: pc.pc_three_interpolate_backward(g, idx, w, TM, out=gout),
+                 steps, warm, flush, stream)
+    trip = TB * TN * 3 * (8 + 4)
+    fwd_bytes = 4.0 * TB * TC * TN + 4.0 * TB * TC * TM + trip
+    bwd_bytes = 4.0 * TB * TC * TN + 4.0 * TB * TC * TM + trip
+    out["three_interpolate"] = {
+        "workload": f"B={TB}, M={TM} centers -> n={TN} points, C={TC} channels, "
+                    "indices from three_nn, inverse-distance weights",
+        "forward_ms": fwd, "backward_ms": bwd,
+        "forward_algorithmic_bytes": fwd_bytes, "backward_algorithmic_bytes": bwd_bytes,
+        "forward_roofline": {"bound": "hbm", "achieved": fwd_bytes / (fwd / 1e3) / 1e9,
+                             "peak": hbm, "unit": "GB/s",
+                             "frac": fwd_bytes / (fwd / 1e3) / 1e9 / hbm},
+        "backward_roofline": {"bound": "hbm", "achieved": bwd_bytes / (bwd / 1e3) / 1e9,
+                              "peak": hbm, "unit": "GB/s",
+                              "frac": bwd_bytes / (bwd / 1e3) / 1e9 / hbm},
+        "launches": {"forward": 1, "backward": "1 + memset"}}
+
+    # PyTorch3D-style Ball Query with return_nn
+    bq_ms = _timed(lambda: p3d_ball_query(centers, px, K=64, radius=0.2), steps, warm,
+                   flush, stream)
+    out["pytorch3d_ball_query"] = {
+        "workload": f"B={TB}, {TM} centers vs {TN} points, r=0.2, K=64, return_nn",
+        "ms": bq_ms, "queries_per_s": TB * TM * world / (bq_ms / 1e3), "launches": 2}
+
+    if with_oracle:
+        import oracle
+        threads = os.cpu_count() or 1
+        rows = np.arange(0, CB * CP, CB * CP // (64 * threads), dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.knn_masked(cx_h, cy_h, 1, squared=True, rows=rows, threads=threads)
+        t1 = time.perf_counter()
+        per_row = (t1 - t0) / len(rows)
+        out["chamfer"]["oracle"] = {
+            "ms_extrapolated": per_row * 2 * CB * CP * 1e3, "cores": threads,
+            "sample": f"{len(rows)} nearest-neighbour rows of one direction, "
+                      "extrapolated to both directions"}
+        fi, ii, wi = feats.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.three_interpolate(fi, ii, wi)
+        t1 = time.perf_counter()
+        oracle.three_interpolate_backward(g.cpu().numpy(), ii, wi, TM)
+        t2 = time.perf_counter()
+        out["three_interpolate"]["oracle"] = {
+            "forward_ms": (t1 - t0) * 1e3, "backward_ms": (t2 - t1) * 1e3, "cores": 1,
+            "sample": "full workload, single thread"}
+        qrows = np.arange(0, TB * TM, 16, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.ball_query_masked(np.ascontiguousarray(px_h[:, :TM]), px_h, 0.2, 64,
+                                 rows=qrows)
+        t1 = time.perf_counter()
+        out["pytorch3d_ball_query"]["oracle"] = {
+            "ms_extrapolated": (t1 - t0) / len(qrows) * TB * TM * 1e3, "cores": 1,
+            "sample": f"{len(qrows)} query rows (gather not included), extrapolated"}
+    return out
 
 
 def run_e2e(args, pc, x_host, device, world):
@@ -602,7 +744,9 @@ def main():
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=["fps", "knn", "ball_query", "grid_build",
-                                       "grid_knn", "grid_ball_query"],
+                                       "grid_knn", "grid_ball_query", "chamfer",
+                                       "three_interpolate",
+                                       "three_interpolate_backward"],
                     help="run one operator of the step W + K times and print "
                          "its mean CUDA-event time (for profiler captures)")
     args = ap.parse_args()
