@@ -186,7 +186,9 @@ def kernel_source_hash(name: str) -> str:
     for f in (src, os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
                                 "pc_device.cuh"),
               os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
-                           "pc_tiles.cuh")):
+                           "pc_tiles.cuh"),
+              os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
+                           "pc_filter.cuh")):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -8,28 +8,31 @@
 //
 // Design (one launch, no scratch memory):
 //  * A block has BQ_CWARPS consumer warps and one producer warp.  Consumer
-//    warp w owns G queries of one cloud, kept in shared memory negated and
-//    duplicated for the packed instructions, (-x,-x,-y,-y) and
-//    (-z,-z,hits,query).
+//    warp w owns G queries of one cloud, kept in shared memory as the filter
+//    constants of pc_filter.cuh duplicated for the packed instructions,
+//    (-2x', -2x', -2y', -2y') and (-2z', -2z', thr, query index), plus the
+//    raw coordinates and the hit count.
 //  * The producer's lane 0 streams reference tiles of BQ_T = 32 * BQ_R points
 //    strictly in input order through a BQ_STAGES ring (TMA bulk copies,
-//    full/empty mbarriers); consumer warps copy a tile into registers (lane l
-//    holds tile points l + 32 r, so for each r the warp holds 32 consecutive
-//    references in lane order), release it and compute.
-//  * Per (query, tile) each lane evaluates BQ_R distances with packed f32x2
-//    instructions and one vote asks whether any is inside the radius; no
-//    distance stays live past the vote, so the hot loop is only the packed
-//    arithmetic, the compares and the vote.  On a hit (rare) the slow path
-//    recomputes the distances and, per r, a ballot gives the hits among 32
-//    consecutive references and __popc(ballot & lanemask_lt) gives each hit
-//    its rank, so a hit is written straight to slot (hits so far + rank):
-//    input order is kept without any sort.
+//    full/empty mbarriers); consumer warps derive the centred coordinates
+//    and w' of their points into registers (lane l holds tile points
+//    l + 32 r, so for each r the warp holds 32 consecutive references in
+//    lane order) and release the raw tile once their queries are done.
+//  * Per (query, tile) each lane evaluates the conservative filter for its
+//    BQ_R points (three packed FMAs per pair) and one vote asks whether any
+//    may be inside the radius; the hot loop is only the FMAs, the compares
+//    and the vote.  On a vote (rare) the slow path computes the exact s32
+//    from the raw tile in shared memory and, per r, a ballot gives the hits
+//    among 32 consecutive references and __popc(ballot & lanemask_lt) gives
+//    each hit its rank, so a hit is written straight to slot (hits so far +
+//    rank): input order is kept without any sort.
 //  * A query stops at K hits: it is swapped behind the still-active queries
 //    of its warp, so the hot loop tests nothing per query.  When every query
 //    of a block is full, a stop flag ends the block: the producer stops
 //    issuing tiles (after letting its copies in flight land) and the
 //    consumers leave the tile loop.
 #include "pc_device.cuh"
+#include "pc_filter.cuh"
 #include "pc_internal.h"
 #include "pc_tiles.cuh"
 
@@ -58,12 +61,12 @@ struct BqArgs {
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
-    float negzero;  // -0.0f, see sq2_rn
 };
 
 struct __align__(16) BqSlot {
-    float4 nxy;  // (-x, -x, -y, -y)
-    float4 nzh;  // (-z, -z, hits so far (int bits), query index in warp (int bits))
+    float4 axy;  // (-2x', -2x', -2y', -2y')   centred coordinates
+    float4 azt;  // (-2z', -2z', thr, query index in warp (int bits))
+    float4 raw;  // (x, y, z, hits so far (int bits))
 };
 
 constexpr unsigned BQ_BUF = tile_buffer_bytes(BQ_T);
@@ -73,8 +76,6 @@ __host__ __device__ constexpr size_t bq_fixed_smem() {
     return size_t(BQ_STAGES) * BQ_BUF + 2 * BQ_STAGES * 8 + 16;
 }
 
-__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
-__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
 
 // Valid length of cloud b: lens[b] clamped to [0, full], or full.
 __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
@@ -83,34 +84,25 @@ __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
     return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
 }
 
-// Slow path, taken only when a vote found a hit: recompute the tile's
-// distances for this query and record the hits in input order.  Returns the
-// new hit count (<= K).
-__device__ __forceinline__ int bq_record(const float2 (&rx)[BQ_R / 2],
-                                         const float2 (&ry)[BQ_R / 2],
-                                         const float2 (&rz)[BQ_R / 2],
-                                         const BqSlot q, float2 nz0, int hits,
-                                         int j0, int cnt, float R2, int K,
-                                         size_t row, float *out_dist2,
+// Slow path, taken only when a vote let a pair through: the exact s32 of the
+// tile's points for this query from the raw tile in shared memory, hits
+// recorded in input order.  Returns the new hit count (<= K).
+__device__ __forceinline__ int bq_record(const float *tile, const float4 q,
+                                         int hits, int j0, int cnt, float R2,
+                                         int K, size_t row, float *out_dist2,
                                          int64_t *out_idx) {
     const int lane = static_cast<int>(lane_id());
-    float s[BQ_R];
-#pragma unroll
-    for (int p = 0; p < BQ_R / 2; ++p) {
-        const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy), hi2(q.nxy),
-                                 lo2(q.nzh), nz0);
-        s[2 * p] = v.x;
-        s[2 * p + 1] = v.y;
-    }
 #pragma unroll
     for (int r = 0; r < BQ_R; ++r) {
-        const bool hit = (r * 32 + lane < cnt) && s[r] < R2;
+        const float *p = tile + 3 * (lane + 32 * r);
+        const float s = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
+        const bool hit = (r * 32 + lane < cnt) && s < R2;
         const unsigned bal = __ballot_sync(FULL, hit);
         if (bal) {
             const int pos = hits + __popc(bal & lanemask_lt());
             if (hit && pos < K) {
                 out_idx[row * K + pos] = j0 + r * 32 + lane;
-                out_dist2[row * K + pos] = s[r];
+                out_dist2[row * K + pos] = s;
             }
             hits += __popc(bal);
             if (hits >= K) break;
@@ -179,6 +171,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     const int nq = max(0, min(G, Qb - q_warp0));
     BqSlot *slots = slots_all + warp * G;
     const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
+    const FilterFrame fr = filter_frame(cref, min(BQ_T, Nb));
     for (int g = lane; g < G; g += 32) {
         float x = 0.f, y = 0.f, z = 0.f;
         if (g < nq) {
@@ -187,8 +180,13 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             y = p[1];
             z = p[2];
         }
-        slots[g].nxy = make_float4(-x, -x, -y, -y);
-        slots[g].nzh = make_float4(-z, -z, __int_as_float(0), __int_as_float(g));
+        const float xp = __fsub_rn(x, fr.cx), yp = __fsub_rn(y, fr.cy),
+                    zp = __fsub_rn(z, fr.cz);
+        const float ax = -2.0f * xp, ay = -2.0f * yp, az = -2.0f * zp;
+        const float thr = filter_threshold(a.R2, filter_norm2(xp, yp, zp));
+        slots[g].axy = make_float4(ax, ax, ay, ay);
+        slots[g].azt = make_float4(az, az, thr, __int_as_float(g));
+        slots[g].raw = make_float4(x, y, z, __int_as_float(0));
     }
     __syncthreads();
 
@@ -199,7 +197,6 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     int active = nq;
     if (active == 0 && lane == 0 && atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS)
         *vstop = 1;
-    const float2 nz0 = make_float2(a.negzero, a.negzero);
     bool failed = false;
     for (int it = 0; it < ntiles; ++it) {
         if (__any_sync(FULL, *vstop != 0)) break;
@@ -214,62 +211,73 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
         const int cnt = min(BQ_T, Nb - j0);
         const float *buf =
             ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
-        float2 rx[BQ_R / 2], ry[BQ_R / 2], rz[BQ_R / 2];
-#pragma unroll
-        for (int p = 0; p < BQ_R / 2; ++p) {
-            const float *p0 = buf + 3 * (lane + 32 * (2 * p));
-            const float *p1 = buf + 3 * (lane + 32 * (2 * p + 1));
-            rx[p] = make_float2(p0[0], p1[0]);
-            ry[p] = make_float2(p0[1], p1[1]);
-            rz[p] = make_float2(p0[2], p1[2]);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[st]);
-        if (active == 0) continue;  // keep the ring moving
-
-        bool any_full = false;
-        BqSlot *sp = slots;
-        BqSlot *const send = slots + active;
-        for (; sp < send; ++sp) {
-            const BqSlot q = *sp;
-            bool t = false;
+        if (active > 0) {
+            // centred coordinates and w' of this lane's points (points past
+            // cnt hold stale values: they may pass and are masked exactly)
+            float2 rx[BQ_R / 2], ry[BQ_R / 2], rz[BQ_R / 2], rw[BQ_R / 2];
 #pragma unroll
             for (int p = 0; p < BQ_R / 2; ++p) {
-                const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy),
-                                         hi2(q.nxy), lo2(q.nzh), nz0);
-                t |= (v.x < a.R2) | (v.y < a.R2);
+                const float *p0 = buf + 3 * (lane + 32 * (2 * p));
+                const float *p1 = buf + 3 * (lane + 32 * (2 * p + 1));
+                const float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
+                            z0 = __fsub_rn(p0[2], fr.cz);
+                const float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
+                            z1 = __fsub_rn(p1[2], fr.cz);
+                rx[p] = make_float2(x0, x1);
+                ry[p] = make_float2(y0, y1);
+                rz[p] = make_float2(z0, z1);
+                rw[p] = make_float2(filter_ref_w(x0, y0, z0),
+                                    filter_ref_w(x1, y1, z1));
             }
-            if (__any_sync(FULL, t)) {
-                const size_t row =
-                    size_t(b) * a.Q + q_warp0 + __float_as_int(q.nzh.w);
-                const int h = bq_record(rx, ry, rz, q, nz0,
-                                        __float_as_int(q.nzh.z), j0, cnt,
-                                        a.R2, K, row, a.out_dist2, a.out_idx);
-                if (lane == 0) sp->nzh.z = __int_as_float(h);
-                any_full |= h >= K;
-            }
-        }
-        if (any_full) {  // rare: move full queries behind the active ones
-            __syncwarp();
-            if (lane == 0) {
-                int g = 0;
-                while (g < active) {
-                    if (__float_as_int(slots[g].nzh.z) >= K) {
-                        const BqSlot t = slots[g];
-                        slots[g] = slots[active - 1];
-                        slots[active - 1] = t;
-                        --active;
-                    } else {
-                        ++g;
-                    }
+
+            bool any_full = false;
+            BqSlot *sp = slots;
+            BqSlot *const send = slots + active;
+            for (; sp < send; ++sp) {
+                const float4 axy = sp->axy;
+                const float4 azt = sp->azt;
+                bool t = false;
+#pragma unroll
+                for (int p = 0; p < BQ_R / 2; ++p) {
+                    float2 v = fma2_rn(rx[p], make_float2(axy.x, axy.y), rw[p]);
+                    v = fma2_rn(ry[p], make_float2(axy.z, axy.w), v);
+                    v = fma2_rn(rz[p], make_float2(azt.x, azt.y), v);
+                    t |= !(v.x > azt.z) | !(v.y > azt.z);
+                }
+                if (__any_sync(FULL, t)) {
+                    const float4 q = sp->raw;
+                    const size_t row =
+                        size_t(b) * a.Q + q_warp0 + __float_as_int(azt.w);
+                    const int h = bq_record(buf, q, __float_as_int(q.w), j0, cnt,
+                                            a.R2, K, row, a.out_dist2, a.out_idx);
+                    if (lane == 0) sp->raw.w = __int_as_float(h);
+                    any_full |= h >= K;
                 }
             }
-            active = __shfl_sync(FULL, active, 0);
-            __syncwarp();
-            if (active == 0 && lane == 0 &&
-                atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS)
-                *vstop = 1;
+            if (any_full) {  // rare: move full queries behind the active ones
+                __syncwarp();
+                if (lane == 0) {
+                    int g = 0;
+                    while (g < active) {
+                        if (__float_as_int(slots[g].raw.w) >= K) {
+                            const BqSlot t = slots[g];
+                            slots[g] = slots[active - 1];
+                            slots[active - 1] = t;
+                            --active;
+                        } else {
+                            ++g;
+                        }
+                    }
+                }
+                active = __shfl_sync(FULL, active, 0);
+                __syncwarp();
+                if (active == 0 && lane == 0 &&
+                    atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS)
+                    *vstop = 1;
+            }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[st]);  // raw tile no longer read
     }
 
     if (failed) {
@@ -292,8 +300,8 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     }
     for (int g = 0; g < nq; ++g) {
         const BqSlot q = slots[g];
-        const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(q.nzh.w);
-        const int hits = failed ? 0 : __float_as_int(q.nzh.z);
+        const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(q.azt.w);
+        const int hits = failed ? 0 : __float_as_int(q.raw.w);
         for (int e = hits + lane; e < K; e += 32) {
             a.out_idx[row * K + e] = -1;
             a.out_dist2[row * K + e] = 0.0f;
@@ -322,7 +330,6 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
-    a.negzero = -0.0f;
 
     const int slots = dev.sm_count * 2;
     const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));

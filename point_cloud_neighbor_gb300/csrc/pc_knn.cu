@@ -8,31 +8,34 @@
 // Design (one launch, no scratch memory):
 //  * A block has KNN_CWARPS consumer warps and one producer warp.  Consumer
 //    warp w owns G queries of one cloud.  Per query, shared memory holds the
-//    coordinates negated and duplicated for the packed instructions,
-//    (-x,-x,-y,-y) and (-z,-z,tau,tau), where tau is the query's current k-th
-//    squared distance, and the query's sorted list of k (s, j) entries.
+//    filter constants (-2q', -2q', thr, thr; pc_filter.cuh), the raw
+//    coordinates and |q'|^2, and the query's sorted list of k (s, j) entries.
 //  * The producer's lane 0 streams reference tiles of KNN_T = 32 * KNN_R
 //    points through a KNN_STAGES ring in shared memory with TMA bulk copies
-//    (full/empty mbarriers, see TileRing); consumer warps copy a tile into
-//    registers (lane l holds points l + 32 r, packed in pairs), release it
-//    and compute, drifting freely instead of meeting at a block barrier.
-//  * Per (query, tile) a lane evaluates KNN_R distances with packed f32x2
-//    instructions and compares them with the query's tau; one vote decides
-//    whether the warp inserts.  No distance stays live past the vote, so the
-//    hot loop is only the packed arithmetic, the compares and the vote.
-//    Candidates are rare once a list is full.
-//  * Insertion (slow path) recomputes the tile's distances for the query;
-//    each lane builds a bitmask of its candidate slots and parks its
-//    distances in a per-warp scratch row; the warp walks the candidates
-//    and inserts each into the warp-distributed list (lane l holds entries l,
-//    l + 32, ...): one ballot per 32 entries gives the rank, a shuffle shift
-//    makes room.  The order is the lexicographic (s, j) order, so the result
-//    does not depend on the order in which candidates or tiles are visited.
+//    (full/empty mbarriers, see TileRing); consumer warps derive the centred
+//    coordinates and w' of their KNN_R points per lane (lane l holds points
+//    l + 32 r, packed in pairs) into registers and keep the raw tile in the
+//    ring until their queries are done, drifting freely instead of meeting
+//    at a block barrier.
+//  * Per (query, tile) a lane evaluates the conservative filter of
+//    pc_filter.cuh for its KNN_R points (three packed FMAs per pair of
+//    points) against the query's threshold; one vote decides whether the
+//    warp looks closer.  The hot loop is only those FMAs, the compares and
+//    the vote.  Candidates are rare once a list is full.
+//  * The slow path computes the exact s32 of the tile's points from the raw
+//    coordinates in shared memory; each lane builds a bitmask of its slots
+//    that beat the list's k-th (s, j) entry and parks its distances in a
+//    per-warp scratch row; the warp walks the candidates and inserts each
+//    into the warp-distributed list (lane l holds entries l, l + 32, ...):
+//    one ballot per 32 entries gives the rank, a shuffle shift makes room.
+//    The order is the lexicographic (s, j) order, so the result does not
+//    depend on the order in which candidates or tiles are visited.
 //  * Tiles are visited in a scrambled order (stride ~0.618 * tiles, coprime
 //    with the tile count) so that spatially sorted inputs do not feed each
 //    query a stream of ever-closer candidates (the project page's kNN kernel
 //    notes report a 6-8x slowdown from storage order on sorted input).
 #include "pc_device.cuh"
+#include "pc_filter.cuh"
 #include "pc_internal.h"
 #include "pc_tiles.cuh"
 
@@ -61,14 +64,14 @@ struct KnnArgs {
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
-    float negzero;  // -0.0f, see sq2_rn
 };
 
-// One query in shared memory: coordinates negated and duplicated so that the
-// halves are packed operands, plus the filter threshold tau (twice).
+// One query in shared memory: the filter constants duplicated so that the
+// halves are packed operands, and the raw coordinates for the exact path.
 struct __align__(16) QuerySlot {
-    float4 nxy;  // (-x, -x, -y, -y)
-    float4 nzt;  // (-z, -z, tau, tau)
+    float4 axy;  // (-2x', -2x', -2y', -2y')   centred coordinates
+    float4 azt;  // (-2z', -2z', thr, thr)     filter threshold
+    float4 raw;  // (x, y, z, |q'|^2)
 };
 
 constexpr unsigned KNN_BUF = tile_buffer_bytes(KNN_T);
@@ -112,8 +115,6 @@ __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
     return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
 }
 
-__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
-__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
 
 // Entry k-1 of the warp-distributed list: (s, j) broadcast to every lane.
 template <int KPL>
@@ -133,37 +134,15 @@ __device__ __forceinline__ void list_kth(const float (&ls)[KPL],
     tj = __shfl_sync(FULL, vj, kl);
 }
 
-// Insert this tile's candidates for one query (warp-uniform).  The tile's
-// points are in rx/ry/rz (lane l: points l + 32 r); j0 is the tile's first
-// index and cnt its number of valid points.
+// Insert this tile's candidates for one query (warp-uniform).  `tile` is
+// the raw tile in shared memory (lane l: points l + 32 r), j0 the tile's
+// first index and cnt its number of valid points.
 template <int KPL>
-__device__ __forceinline__ void knn_insert(const float2 (&rx)[KNN_R / 2],
-                                           const float2 (&ry)[KNN_R / 2],
-                                           const float2 (&rz)[KNN_R / 2],
-                                           float2 nz0, int j0, int cnt, int k,
-                                           QuerySlot *qs, float *ls_sm,
+__device__ __forceinline__ void knn_insert(const float *tile, int j0, int cnt,
+                                           int k, QuerySlot *qs, float *ls_sm,
                                            int *lj_sm, float *scratch) {
     const int lane = static_cast<int>(lane_id());
-    const QuerySlot q = *qs;
-    const float tau0 = q.nzt.z;
-    // the fast path keeps no distance live past its vote: recompute them
-    float s[KNN_R];
-#pragma unroll
-    for (int p = 0; p < KNN_R / 2; ++p) {
-        const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy), hi2(q.nxy),
-                                 lo2(q.nzt), nz0);
-        s[2 * p] = v.x;
-        s[2 * p + 1] = v.y;
-    }
-    unsigned m = 0;
-#pragma unroll
-    for (int r = 0; r < KNN_R; ++r)
-        if (r * 32 + lane < cnt && s[r] <= tau0) m |= 1u << r;
-    if (m) {
-        float4 *row = reinterpret_cast<float4 *>(scratch + lane * KNN_R);
-        row[0] = make_float4(s[0], s[1], s[2], s[3]);
-        row[1] = make_float4(s[4], s[5], s[6], s[7]);
-    }
+    const float4 q = qs->raw;
     float ls[KPL];
     int lj[KPL];
 #pragma unroll
@@ -172,10 +151,26 @@ __device__ __forceinline__ void knn_insert(const float2 (&rx)[KNN_R / 2],
         ls[c] = e < k ? ls_sm[e] : __int_as_float(0x7f800000);
         lj[c] = e < k ? lj_sm[e] : INT_MAX;
     }
-    __syncwarp();
     float ts;
     int tj;
     list_kth<KPL>(ls, lj, k, ts, tj);
+    // exact s32 of this lane's points; candidates beat (ts, tj)
+    float s[KNN_R];
+    unsigned m = 0;
+#pragma unroll
+    for (int r = 0; r < KNN_R; ++r) {
+        const float *p = tile + 3 * (lane + 32 * r);
+        s[r] = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
+        const int j = j0 + r * 32 + lane;
+        if (r * 32 + lane < cnt && (s[r] < ts || (s[r] == ts && j < tj)))
+            m |= 1u << r;
+    }
+    if (m) {
+        float4 *row = reinterpret_cast<float4 *>(scratch + lane * KNN_R);
+        row[0] = make_float4(s[0], s[1], s[2], s[3]);
+        row[1] = make_float4(s[4], s[5], s[6], s[7]);
+    }
+    __syncwarp();
     bool changed = false;
     unsigned bal = __ballot_sync(FULL, m != 0);
     while (bal) {
@@ -229,8 +224,10 @@ __device__ __forceinline__ void knn_insert(const float2 (&rx)[KNN_R / 2],
             }
         }
         if (lane == 0) {
-            qs->nzt.z = ts;
-            qs->nzt.w = ts;
+            const float thr = tj == INT_MAX ? __int_as_float(0x7f800000)
+                                            : filter_threshold(ts, q.w);
+            qs->azt.z = thr;
+            qs->azt.w = thr;
         }
     }
     __syncwarp();  // the scratch row is reused by the next insertion
@@ -306,6 +303,7 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
     float *scratch = scratch_all + warp * 32 * KNN_R;
     const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
     const float inf = __int_as_float(0x7f800000);
+    const FilterFrame fr = filter_frame(cref, min(KNN_T, Nb));
     for (int g = lane; g < G; g += 32) {
         float x = 0.f, y = 0.f, z = 0.f;
         if (g < nq) {
@@ -314,8 +312,12 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
             y = p[1];
             z = p[2];
         }
-        slots[g].nxy = make_float4(-x, -x, -y, -y);
-        slots[g].nzt = make_float4(-z, -z, inf, inf);
+        const float xp = __fsub_rn(x, fr.cx), yp = __fsub_rn(y, fr.cy),
+                    zp = __fsub_rn(z, fr.cz);
+        const float ax = -2.0f * xp, ay = -2.0f * yp, az = -2.0f * zp;
+        slots[g].axy = make_float4(ax, ax, ay, ay);
+        slots[g].azt = make_float4(az, az, inf, inf);
+        slots[g].raw = make_float4(x, y, z, filter_norm2(xp, yp, zp));
     }
     for (int e = lane; e < G * k; e += 32) {
         ls_w[e] = inf;
@@ -323,7 +325,6 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
     }
     __syncthreads();
 
-    const float2 nz0 = make_float2(a.negzero, a.negzero);
     bool failed = false;
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % KNN_STAGES;
@@ -337,34 +338,42 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         const int cnt = min(KNN_T, Nb - j0);
         const float *buf =
             ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
-        float2 rx[KNN_R / 2], ry[KNN_R / 2], rz[KNN_R / 2];
+        // centred coordinates and w' of this lane's points (points past cnt
+        // hold stale values: they may pass the filter and are masked exactly)
+        float2 rx[KNN_R / 2], ry[KNN_R / 2], rz[KNN_R / 2], rw[KNN_R / 2];
 #pragma unroll
         for (int p = 0; p < KNN_R / 2; ++p) {
             const float *p0 = buf + 3 * (lane + 32 * (2 * p));
             const float *p1 = buf + 3 * (lane + 32 * (2 * p + 1));
-            rx[p] = make_float2(p0[0], p1[0]);
-            ry[p] = make_float2(p0[1], p1[1]);
-            rz[p] = make_float2(p0[2], p1[2]);
+            const float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
+                        z0 = __fsub_rn(p0[2], fr.cz);
+            const float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
+                        z1 = __fsub_rn(p1[2], fr.cz);
+            rx[p] = make_float2(x0, x1);
+            ry[p] = make_float2(y0, y1);
+            rz[p] = make_float2(z0, z1);
+            rw[p] = make_float2(filter_ref_w(x0, y0, z0), filter_ref_w(x1, y1, z1));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[st]);
 
         QuerySlot *sp = slots;
         float *lsp = ls_w;
         int *ljp = lj_w;
         for (int g = 0; g < nq; ++g, ++sp, lsp += k, ljp += k) {
-            const QuerySlot q = *sp;
+            const float4 axy = sp->axy;
+            const float4 azt = sp->azt;
             bool t = false;
 #pragma unroll
             for (int p = 0; p < KNN_R / 2; ++p) {
-                const float2 v = sqdist2(rx[p], ry[p], rz[p], lo2(q.nxy),
-                                         hi2(q.nxy), lo2(q.nzt), nz0);
-                t |= (v.x <= q.nzt.z) | (v.y <= q.nzt.z);
+                float2 v = fma2_rn(rx[p], make_float2(axy.x, axy.y), rw[p]);
+                v = fma2_rn(ry[p], make_float2(axy.z, axy.w), v);
+                v = fma2_rn(rz[p], make_float2(azt.x, azt.y), v);
+                t |= !(v.x > azt.z) | !(v.y > azt.z);
             }
             if (__any_sync(FULL, t))
-                knn_insert<KPL>(rx, ry, rz, nz0, j0, cnt, k, sp, lsp, ljp,
-                                scratch);
+                knn_insert<KPL>(buf, j0, cnt, k, sp, lsp, ljp, scratch);
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[st]);  // raw tile no longer read
     }
 
     // rows of this warp past the valid length: padding
@@ -444,7 +453,6 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
-    a.negzero = -0.0f;
     if (k <= 32) return launch_knn_t<1>(dev, a, B, Q, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
     if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
