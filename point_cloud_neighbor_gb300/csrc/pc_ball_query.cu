@@ -84,19 +84,30 @@ __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
     return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
 }
 
-// Slow path, taken only when a vote let a pair through: the exact s32 of the
-// tile's points for this query from the raw tile in shared memory, hits
-// recorded in input order.  Returns the new hit count (<= K).
-__device__ __forceinline__ int bq_record(const float *tile, const float4 q,
+// Slow path, taken only when a vote let a pair through: the lane's filter
+// mask is recomputed from its registers, points that pass get their exact
+// s32 from the raw tile in shared memory (lane l: points l + 32 r), and hits
+// are recorded in input order.  Returns the new hit count (<= K).
+__device__ __forceinline__ int bq_record(const float *tile,
+                                         const float2 (&rx)[BQ_R / 2],
+                                         const float2 (&ry)[BQ_R / 2],
+                                         const float2 (&rz)[BQ_R / 2],
+                                         const float2 (&rw)[BQ_R / 2],
+                                         float4 axy, float4 azt, const float4 q,
                                          int hits, int j0, int cnt, float R2,
                                          int K, size_t row, float *out_dist2,
                                          int64_t *out_idx) {
     const int lane = static_cast<int>(lane_id());
+    const unsigned pm = filter_mask8(rx, ry, rz, rw, axy, azt);
 #pragma unroll
     for (int r = 0; r < BQ_R; ++r) {
-        const float *p = tile + 3 * (lane + 32 * r);
-        const float s = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
-        const bool hit = (r * 32 + lane < cnt) && s < R2;
+        float s = 0.f;
+        bool hit = false;
+        if (((pm >> r) & 1u) && r * 32 + lane < cnt) {
+            const float *p = tile + 3 * (lane + 32 * r);
+            s = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
+            hit = s < R2;
+        }
         const unsigned bal = __ballot_sync(FULL, hit);
         if (bal) {
             const int pos = hits + __popc(bal & lanemask_lt());
@@ -236,20 +247,13 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             for (; sp < send; ++sp) {
                 const float4 axy = sp->axy;
                 const float4 azt = sp->azt;
-                bool t = false;
-#pragma unroll
-                for (int p = 0; p < BQ_R / 2; ++p) {
-                    float2 v = fma2_rn(rx[p], make_float2(axy.x, axy.y), rw[p]);
-                    v = fma2_rn(ry[p], make_float2(axy.z, axy.w), v);
-                    v = fma2_rn(rz[p], make_float2(azt.x, azt.y), v);
-                    t |= !(v.x > azt.z) | !(v.y > azt.z);
-                }
-                if (__any_sync(FULL, t)) {
+                if (__any_sync(FULL, filter_any8(rx, ry, rz, rw, axy, azt))) {
                     const float4 q = sp->raw;
                     const size_t row =
                         size_t(b) * a.Q + q_warp0 + __float_as_int(azt.w);
-                    const int h = bq_record(buf, q, __float_as_int(q.w), j0, cnt,
-                                            a.R2, K, row, a.out_dist2, a.out_idx);
+                    const int h = bq_record(buf, rx, ry, rz, rw, axy, azt, q,
+                                            __float_as_int(q.w), j0, cnt, a.R2,
+                                            K, row, a.out_dist2, a.out_idx);
                     if (lane == 0) sp->raw.w = __int_as_float(h);
                     any_full |= h >= K;
                 }

@@ -45,16 +45,43 @@ namespace pcn {
 
 // Packed fused multiply-add, one rounding per half: a * b + c.
 __device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-        "mov.b64 ra, {%2, %3};\n\t"
-        "mov.b64 rb, {%4, %5};\n\t"
-        "mov.b64 rc, {%6, %7};\n\t"
-        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-        "mov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
+    return __ffma2_rn(a, b, c);
+}
+
+// The filter of one query against a lane's 8 points (4 packed pairs):
+// bit r of the result is set when point r may satisfy the selection bound.
+__device__ __forceinline__ unsigned filter_mask8(const float2 (&x)[4],
+                                                 const float2 (&y)[4],
+                                                 const float2 (&z)[4],
+                                                 const float2 (&w)[4],
+                                                 float4 axy, float4 azt) {
+    unsigned m = 0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float2 v = fma2_rn(x[p], make_float2(axy.x, axy.y), w[p]);
+        v = fma2_rn(y[p], make_float2(axy.z, axy.w), v);
+        v = fma2_rn(z[p], make_float2(azt.x, azt.y), v);
+        m |= (!(v.x > azt.z) ? 1u : 0u) << (2 * p);
+        m |= (!(v.y > azt.z) ? 1u : 0u) << (2 * p + 1);
+    }
+    return m;
+}
+
+// Any point of the lane's 8 passing the filter (the hot-loop form).
+__device__ __forceinline__ bool filter_any8(const float2 (&x)[4],
+                                            const float2 (&y)[4],
+                                            const float2 (&z)[4],
+                                            const float2 (&w)[4], float4 axy,
+                                            float4 azt) {
+    bool t = false;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float2 v = fma2_rn(x[p], make_float2(axy.x, axy.y), w[p]);
+        v = fma2_rn(y[p], make_float2(axy.z, axy.w), v);
+        v = fma2_rn(z[p], make_float2(azt.x, azt.y), v);
+        t |= !(v.x > azt.z) | !(v.y > azt.z);
+    }
+    return t;
 }
 
 struct FilterFrame {

@@ -72,6 +72,7 @@ struct __align__(16) QuerySlot {
     float4 axy;  // (-2x', -2x', -2y', -2y')   centred coordinates
     float4 azt;  // (-2z', -2z', thr, thr)     filter threshold
     float4 raw;  // (x, y, z, |q'|^2)
+    float4 kth;  // (s, j (int bits), -, -) of the list's k-th entry
 };
 
 constexpr unsigned KNN_BUF = tile_buffer_bytes(KNN_T);
@@ -134,15 +135,44 @@ __device__ __forceinline__ void list_kth(const float (&ls)[KPL],
     tj = __shfl_sync(FULL, vj, kl);
 }
 
-// Insert this tile's candidates for one query (warp-uniform).  `tile` is
-// the raw tile in shared memory (lane l: points l + 32 r), j0 the tile's
-// first index and cnt its number of valid points.
+// Insert this tile's candidates for one query (warp-uniform), called when
+// the filter let at least one pair through.  The lane's filter mask is
+// recomputed from its registers; only points that pass get their exact s32
+// (from the raw tile in shared memory, lane l: points l + 32 r), and only
+// those that beat the list's k-th (s, j) entry are inserted.  The list is
+// not touched when every pass was a false positive.
 template <int KPL>
-__device__ __forceinline__ void knn_insert(const float *tile, int j0, int cnt,
-                                           int k, QuerySlot *qs, float *ls_sm,
-                                           int *lj_sm, float *scratch) {
+__device__ __forceinline__ void knn_insert(const float *tile,
+                                           const float2 (&rx)[KNN_R / 2],
+                                           const float2 (&ry)[KNN_R / 2],
+                                           const float2 (&rz)[KNN_R / 2],
+                                           const float2 (&rw)[KNN_R / 2],
+                                           float4 axy, float4 azt, int j0,
+                                           int cnt, int k, QuerySlot *qs,
+                                           float *ls_sm, int *lj_sm,
+                                           float *scratch) {
     const int lane = static_cast<int>(lane_id());
+    unsigned pm = filter_mask8(rx, ry, rz, rw, axy, azt);
+    const int left = cnt - lane;  // points r with r * 32 < left are valid
+    pm &= left >= KNN_T ? 0xffu : (left > 0 ? (1u << ((left + 31) >> 5)) - 1u : 0u);
     const float4 q = qs->raw;
+    const float4 kth = qs->kth;
+    float ts = kth.x;
+    int tj = __float_as_int(kth.y);
+    unsigned m = 0;
+    while (pm) {
+        const int r = __ffs(pm) - 1;
+        pm &= pm - 1;
+        const float *p = tile + 3 * (lane + 32 * r);
+        const float sv = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
+        const int j = j0 + r * 32 + lane;
+        if (sv < ts || (sv == ts && j < tj)) {
+            m |= 1u << r;
+            scratch[lane * KNN_R + r] = sv;
+        }
+    }
+    unsigned bal = __ballot_sync(FULL, m != 0);
+    if (bal == 0) return;
     float ls[KPL];
     int lj[KPL];
 #pragma unroll
@@ -151,28 +181,7 @@ __device__ __forceinline__ void knn_insert(const float *tile, int j0, int cnt,
         ls[c] = e < k ? ls_sm[e] : __int_as_float(0x7f800000);
         lj[c] = e < k ? lj_sm[e] : INT_MAX;
     }
-    float ts;
-    int tj;
-    list_kth<KPL>(ls, lj, k, ts, tj);
-    // exact s32 of this lane's points; candidates beat (ts, tj)
-    float s[KNN_R];
-    unsigned m = 0;
-#pragma unroll
-    for (int r = 0; r < KNN_R; ++r) {
-        const float *p = tile + 3 * (lane + 32 * r);
-        s[r] = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
-        const int j = j0 + r * 32 + lane;
-        if (r * 32 + lane < cnt && (s[r] < ts || (s[r] == ts && j < tj)))
-            m |= 1u << r;
-    }
-    if (m) {
-        float4 *row = reinterpret_cast<float4 *>(scratch + lane * KNN_R);
-        row[0] = make_float4(s[0], s[1], s[2], s[3]);
-        row[1] = make_float4(s[4], s[5], s[6], s[7]);
-    }
     __syncwarp();
-    bool changed = false;
-    unsigned bal = __ballot_sync(FULL, m != 0);
     while (bal) {
         const int src = __ffs(bal) - 1;
         bal &= bal - 1;
@@ -210,25 +219,23 @@ __device__ __forceinline__ void knn_insert(const float *tile, int j0, int cnt,
                     }
                 }
                 list_kth<KPL>(ls, lj, k, ts, tj);
-                changed = true;
             }
         }
     }
-    if (changed) {
 #pragma unroll
-        for (int c = 0; c < KPL; ++c) {
-            const int e = c * 32 + lane;
-            if (e < k) {
-                ls_sm[e] = ls[c];
-                lj_sm[e] = lj[c];
-            }
+    for (int c = 0; c < KPL; ++c) {
+        const int e = c * 32 + lane;
+        if (e < k) {
+            ls_sm[e] = ls[c];
+            lj_sm[e] = lj[c];
         }
-        if (lane == 0) {
-            const float thr = tj == INT_MAX ? __int_as_float(0x7f800000)
-                                            : filter_threshold(ts, q.w);
-            qs->azt.z = thr;
-            qs->azt.w = thr;
-        }
+    }
+    if (lane == 0) {
+        const float thr = tj == INT_MAX ? __int_as_float(0x7f800000)
+                                        : filter_threshold(ts, q.w);
+        qs->azt.z = thr;
+        qs->azt.w = thr;
+        qs->kth = make_float4(ts, __int_as_float(tj), 0.f, 0.f);
     }
     __syncwarp();  // the scratch row is reused by the next insertion
 }
@@ -318,6 +325,7 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         slots[g].axy = make_float4(ax, ax, ay, ay);
         slots[g].azt = make_float4(az, az, inf, inf);
         slots[g].raw = make_float4(x, y, z, filter_norm2(xp, yp, zp));
+        slots[g].kth = make_float4(inf, __int_as_float(INT_MAX), 0.f, 0.f);
     }
     for (int e = lane; e < G * k; e += 32) {
         ls_w[e] = inf;
@@ -361,16 +369,9 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         for (int g = 0; g < nq; ++g, ++sp, lsp += k, ljp += k) {
             const float4 axy = sp->axy;
             const float4 azt = sp->azt;
-            bool t = false;
-#pragma unroll
-            for (int p = 0; p < KNN_R / 2; ++p) {
-                float2 v = fma2_rn(rx[p], make_float2(axy.x, axy.y), rw[p]);
-                v = fma2_rn(ry[p], make_float2(axy.z, axy.w), v);
-                v = fma2_rn(rz[p], make_float2(azt.x, azt.y), v);
-                t |= !(v.x > azt.z) | !(v.y > azt.z);
-            }
-            if (__any_sync(FULL, t))
-                knn_insert<KPL>(buf, j0, cnt, k, sp, lsp, ljp, scratch);
+            if (__any_sync(FULL, filter_any8(rx, ry, rz, rw, axy, azt)))
+                knn_insert<KPL>(buf, rx, ry, rz, rw, axy, azt, j0, cnt, k, sp,
+                                lsp, ljp, scratch);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ring.empty[st]);  // raw tile no longer read
