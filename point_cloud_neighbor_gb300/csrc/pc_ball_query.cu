@@ -242,21 +242,32 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             }
 
             bool any_full = false;
-            BqSlot *sp = slots;
-            BqSlot *const send = slots + active;
-            for (; sp < send; ++sp) {
-                const float4 axy = sp->axy;
-                const float4 azt = sp->azt;
-                if (__any_sync(FULL, filter_any8(rx, ry, rz, rw, axy, azt))) {
-                    const float4 q = sp->raw;
-                    const size_t row =
-                        size_t(b) * a.Q + q_warp0 + __float_as_int(azt.w);
-                    const int h = bq_record(buf, rx, ry, rz, rw, axy, azt, q,
-                                            __float_as_int(q.w), j0, cnt, a.R2,
-                                            K, row, a.out_dist2, a.out_idx);
-                    if (lane == 0) sp->raw.w = __int_as_float(h);
-                    any_full |= h >= K;
-                }
+            auto record = [&](BqSlot *sp, float4 axy, float4 azt) {
+                const float4 q = sp->raw;
+                const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(azt.w);
+                const int h = bq_record(buf, rx, ry, rz, rw, axy, azt, q,
+                                        __float_as_int(q.w), j0, cnt, a.R2, K, row,
+                                        a.out_dist2, a.out_idx);
+                if (lane == 0) sp->raw.w = __int_as_float(h);
+                any_full |= h >= K;
+            };
+            // two queries per step: independent filter chains for the scheduler
+            int g = 0;
+            for (; g + 1 < active; g += 2) {
+                BqSlot *s0 = slots + g;
+                const float4 axy0 = s0[0].axy, azt0 = s0[0].azt;
+                const float4 axy1 = s0[1].axy, azt1 = s0[1].azt;
+                const bool t0 = filter_any8(rx, ry, rz, rw, axy0, azt0);
+                const bool t1 = filter_any8(rx, ry, rz, rw, axy1, azt1);
+                const bool v0 = __any_sync(FULL, t0), v1 = __any_sync(FULL, t1);
+                if (v0) record(s0, axy0, azt0);
+                if (v1) record(s0 + 1, axy1, azt1);
+            }
+            if (g < active) {
+                BqSlot *s0 = slots + g;
+                const float4 axy = s0->axy, azt = s0->azt;
+                if (__any_sync(FULL, filter_any8(rx, ry, rz, rw, axy, azt)))
+                    record(s0, axy, azt);
             }
             if (any_full) {  // rare: move full queries behind the active ones
                 __syncwarp();

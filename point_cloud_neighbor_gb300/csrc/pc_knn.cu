@@ -363,15 +363,29 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
             rw[p] = make_float2(filter_ref_w(x0, y0, z0), filter_ref_w(x1, y1, z1));
         }
 
-        QuerySlot *sp = slots;
-        float *lsp = ls_w;
-        int *ljp = lj_w;
-        for (int g = 0; g < nq; ++g, ++sp, lsp += k, ljp += k) {
-            const float4 axy = sp->axy;
-            const float4 azt = sp->azt;
+        // two queries per step: independent filter chains for the scheduler
+        int g = 0;
+        for (; g + 1 < nq; g += 2) {
+            QuerySlot *s0 = slots + g;
+            const float4 axy0 = s0[0].axy, azt0 = s0[0].azt;
+            const float4 axy1 = s0[1].axy, azt1 = s0[1].azt;
+            const bool t0 = filter_any8(rx, ry, rz, rw, axy0, azt0);
+            const bool t1 = filter_any8(rx, ry, rz, rw, axy1, azt1);
+            const bool v0 = __any_sync(FULL, t0), v1 = __any_sync(FULL, t1);
+            if (v0)
+                knn_insert<KPL>(buf, rx, ry, rz, rw, axy0, azt0, j0, cnt, k, s0,
+                                ls_w + size_t(g) * k, lj_w + size_t(g) * k, scratch);
+            if (v1)
+                knn_insert<KPL>(buf, rx, ry, rz, rw, axy1, azt1, j0, cnt, k, s0 + 1,
+                                ls_w + size_t(g + 1) * k, lj_w + size_t(g + 1) * k,
+                                scratch);
+        }
+        if (g < nq) {
+            QuerySlot *s0 = slots + g;
+            const float4 axy = s0->axy, azt = s0->azt;
             if (__any_sync(FULL, filter_any8(rx, ry, rz, rw, axy, azt)))
-                knn_insert<KPL>(buf, rx, ry, rz, rw, axy, azt, j0, cnt, k, sp,
-                                lsp, ljp, scratch);
+                knn_insert<KPL>(buf, rx, ry, rz, rw, axy, azt, j0, cnt, k, s0,
+                                ls_w + size_t(g) * k, lj_w + size_t(g) * k, scratch);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ring.empty[st]);  // raw tile no longer read
