@@ -188,7 +188,9 @@ def kernel_source_hash(name: str) -> str:
               os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
                            "pc_tiles.cuh"),
               os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
-                           "pc_filter.cuh")):
+                           "pc_filter.cuh"),
+              os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
+                           "pc_stream.cuh")):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -27,7 +27,8 @@ LIB = os.path.join(BUILD, "libpointcloud.so")
 
 SOURCES = ["pc_api.cu", "pc_fps.cu", "pc_knn.cu", "pc_ball_query.cu",
            "pc_fps_static.cu", "pc_grid.cu", "pc_chamfer.cu", "pc_interp.cu"]
-HEADERS = ["pc_device.cuh", "pc_tiles.cuh", "pc_filter.cuh", "pc_internal.h"]
+HEADERS = ["pc_device.cuh", "pc_tiles.cuh", "pc_filter.cuh", "pc_stream.cuh",
+           "pc_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = [
     *ARCH, "-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-ftz=false",

@@ -37,6 +37,7 @@
 #include "pc_device.cuh"
 #include "pc_filter.cuh"
 #include "pc_internal.h"
+#include "pc_stream.cuh"
 #include "pc_tiles.cuh"
 
 #include <algorithm>
@@ -422,6 +423,205 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// k <= 32: one query per lane (the kernel used for every k up to 32).
+//
+// The producer warp streams the tiles in the scrambled order and prepares
+// them (pc_stream.cuh).  A lane keeps its query's current k best (s, j) as a
+// max-heap in shared memory (entry e of lane l at [e * 32 + l], lexicographic
+// (s, j) order, root = the k-th best) and the root in registers; its filter
+// threshold follows the root.  Per step the lane filters 8 points (three
+// packed FMAs per two points, broadcast shared-memory operands); on a pass it
+// recomputes which points passed, takes their exact s32 from the raw tile
+// and replaces the root by every point that beats it (sift-down).  At the end
+// each lane heap-sorts its k entries into ascending (s, j) order.
+// ---------------------------------------------------------------------------
+constexpr int KL_CWARPS = 8;
+constexpr int KL_THREADS = 32 * (KL_CWARPS + 1);
+
+__host__ __device__ constexpr size_t knn_lane_smem(int k) {
+    return stream_smem_bytes() + size_t(KL_CWARPS) * 32 * size_t(k) * 8;
+}
+
+// Lexicographic (s, j) "a after b".
+__device__ __forceinline__ bool sj_after(float as, int aj, float bs, int bj) {
+    return as > bs || (as == bs && aj > bj);
+}
+
+// Sift (s, j) down from `pos` in the max-heap hs/hj of n entries (stride 32).
+__device__ __forceinline__ void heap_sift(float *hs, int *hj, int n, int pos,
+                                          float s, int j) {
+    for (;;) {
+        int c = 2 * pos + 1;
+        if (c >= n) break;
+        float cs = hs[c * 32];
+        int cj = hj[c * 32];
+        if (c + 1 < n) {
+            const float ds = hs[(c + 1) * 32];
+            const int dj = hj[(c + 1) * 32];
+            if (sj_after(ds, dj, cs, cj)) {
+                ++c;
+                cs = ds;
+                cj = dj;
+            }
+        }
+        if (!sj_after(cs, cj, s, j)) break;
+        hs[pos * 32] = cs;
+        hj[pos * 32] = cj;
+        pos = c;
+    }
+    hs[pos * 32] = s;
+    hj[pos * 32] = j;
+}
+
+__global__ void __launch_bounds__(KL_THREADS, 3) knn_lane_kernel(const KnnArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.y;
+    const int k = a.k;
+    const float inf = __int_as_float(0x7f800000);
+
+    StreamRing ring;
+    int *flags = stream_carve(smem, ring);
+    int *s_err = flags;
+    float *hs_all = reinterpret_cast<float *>(smem + stream_smem_bytes());
+    int *hj_all = reinterpret_cast<int *>(hs_all + size_t(KL_CWARPS) * 32 * k);
+
+    const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
+    const int Nb = valid_len(a.r_len, b, a.N);
+    const int Qb = valid_len(a.q_len, b, a.Q);
+    const int ntiles = (Nb + ST_T - 1) / ST_T;
+    const int tstride = scramble_stride(ntiles);
+    const int q0 = blockIdx.x * KL_CWARPS * 32;
+
+    if (q0 >= Qb) {
+        // every query of this block is past the cloud's valid length
+        const int r1 = min(a.Q, q0 + KL_CWARPS * 32);
+        const size_t e0 = (size_t(b) * a.Q + q0) * k;
+        const size_t e1 = (size_t(b) * a.Q + r1) * k;
+        for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+            a.out_idx[e] = -1;
+            a.out_dist[e] = 0.0f;
+        }
+        return;
+    }
+    if (threadIdx.x == 0) {
+        stream_init(ring, KL_CWARPS);
+        *s_err = 0;
+    }
+    const FilterFrame fr = filter_frame(cref, min(ST_T, Nb));
+    __syncthreads();
+
+    if (warp == KL_CWARPS) {  // producer warp
+        stream_produce(ring, cref, Nb, ntiles,
+                       [&](int it) { return knn_tile_at(it, tstride, ntiles); }, fr,
+                       s_err, s_err, a.timeout_ns);
+        return;
+    }
+
+    const int qi = q0 + warp * 32 + lane;
+    const bool valid = qi < Qb;
+    float qx = 0.f, qy = 0.f, qz = 0.f;
+    if (valid) {
+        const float *p = a.query + (size_t(b) * a.Q + qi) * 3;
+        qx = p[0];
+        qy = p[1];
+        qz = p[2];
+    }
+    const float xp = __fsub_rn(qx, fr.cx), yp = __fsub_rn(qy, fr.cy),
+                zp = __fsub_rn(qz, fr.cz);
+    const float2 ax = make_float2(-2.0f * xp, -2.0f * xp);
+    const float2 ay = make_float2(-2.0f * yp, -2.0f * yp);
+    const float2 az = make_float2(-2.0f * zp, -2.0f * zp);
+    const float qq = filter_norm2(xp, yp, zp);
+    float *hs = hs_all + size_t(warp) * 32 * k + lane;
+    int *hj = hj_all + size_t(warp) * 32 * k + lane;
+    for (int e = 0; e < k; ++e) {
+        hs[e * 32] = inf;
+        hj[e * 32] = INT_MAX;
+    }
+    float ts = inf;      // root: the k-th best so far
+    int tj = INT_MAX;
+    float thr = valid ? inf : -inf;
+
+    bool failed = false;
+    for (int it = 0; it < ntiles; ++it) {
+        const int st = it % ST_STAGES;
+        const WaitResult w = warp_wait(&ring.ready[st], unsigned((it / ST_STAGES) & 1),
+                                       s_err, a.timeout_ns);
+        if (w != WAIT_OK) {
+            failed = true;
+            break;
+        }
+        const float4 *ck = ring.cooked_tile(st);
+        const int j0 = knn_tile_at(it, tstride, ntiles) * ST_T;
+        const int cnt = min(ST_T, Nb - j0);
+        const float *raw = ring.raw_tile(st) + tile_float_offset(cref + size_t(j0) * 3);
+        const int npairs = (cnt + 1) >> 1;
+        for (int p = 0; p < npairs; p += 4) {
+            if (!stream_any<4>(ck, p, ax, ay, az, thr)) continue;
+            unsigned m = stream_mask<4>(ck, p, ax, ay, az, thr);
+            while (m) {
+                const int i = 2 * p + __ffs(m) - 1;
+                m &= m - 1;
+                if (i >= cnt || !valid) continue;
+                const float sv = sqdist(qx, qy, qz, raw[3 * i], raw[3 * i + 1],
+                                        raw[3 * i + 2]);
+                const int j = j0 + i;
+                if (sj_after(ts, tj, sv, j)) {
+                    heap_sift(hs, hj, k, 0, sv, j);
+                    ts = hs[0];
+                    tj = hj[0];
+                    thr = tj == INT_MAX ? inf : filter_threshold(ts, qq);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.empty[st]);  // tile no longer read
+    }
+
+    const size_t row = size_t(b) * a.Q + qi;
+    if (failed) {
+        if (lane == 0) *s_err = 1;
+        raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
+        if (qi < a.Q)
+            for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
+        return;
+    }
+    // heap sort: the largest entry moves to the end, k - 1 times
+    for (int n = k - 1; n > 0; --n) {
+        const float s = hs[n * 32];
+        const int j = hj[n * 32];
+        hs[n * 32] = hs[0];
+        hj[n * 32] = hj[0];
+        heap_sift(hs, hj, n, 0, s, j);
+    }
+    if (qi < a.Q) {
+        const int kv = valid ? min(k, Nb) : 0;
+        for (int e = 0; e < k; ++e) {
+            const float sv = hs[e * 32];
+            a.out_idx[row * k + e] = e < kv ? int64_t(hj[e * 32]) : int64_t(-1);
+            a.out_dist[row * k + e] = e < kv ? (a.squared ? sv : __fsqrt_rn(sv)) : 0.0f;
+        }
+    }
+}
+
+cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a, int64_t B,
+                            int64_t Q, cudaStream_t stream) {
+    (void)dev;
+    const size_t smem = knn_lane_smem(a.k);
+    cudaError_t e = cudaFuncSetAttribute(
+        knn_lane_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int64_t per_block = int64_t(KL_CWARPS) * 32;
+    dim3 grid(static_cast<unsigned>((Q + per_block - 1) / per_block),
+              static_cast<unsigned>(B));
+    knn_lane_kernel<<<grid, KL_THREADS, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
 template <int KPL>
 cudaError_t launch_knn_t(const DeviceInfo &dev, const KnnArgs &a0, int64_t B,
                          int64_t Q, cudaStream_t stream) {
@@ -468,7 +668,7 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
-    if (k <= 32) return launch_knn_t<1>(dev, a, B, Q, stream);
+    if (k <= 32) return launch_knn_lane(dev, a, B, Q, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
     if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
     return launch_knn_t<8>(dev, a, B, Q, stream);

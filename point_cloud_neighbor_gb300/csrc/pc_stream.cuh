@@ -1,0 +1,206 @@
+// pc_stream.cuh -- reference-tile streaming with producer-side preparation,
+// for the lane-per-query kNN and Ball Query kernels.
+//
+// A block has CW consumer warps and one producer warp.  The producer warp
+// streams reference tiles of ST_T points through an ST_STAGES ring:
+//   1. its lane 0 copies the raw tile (x, y, z float32) into the raw buffer of
+//      a stage with TMA (issue_tile of pc_tiles.cuh), up to ST_STAGES tiles
+//      ahead of the consumers;
+//   2. once a raw tile has landed, the whole warp "cooks" it: the centred
+//      coordinates and w' of the filter of pc_filter.cuh, packed for the
+//      paired instructions, two points per 32 bytes:
+//          cooked[2p]     = (x'_2p, x'_2p+1, y'_2p, y'_2p+1)
+//          cooked[2p + 1] = (z'_2p, z'_2p+1, w'_2p, w'_2p+1)
+//      points past the tile's end get (0, 0, 0, +inf): they pass the filter
+//      only against an infinite threshold and are masked exactly;
+//   3. all 32 producer lanes arrive on the stage's `ready` barrier.
+// Consumers wait on `ready`, read the cooked tile (every lane reads the same
+// 16 bytes: shared-memory broadcasts) and, on their rare slow paths, the raw
+// tile; then each consumer warp arrives on `empty`, which the producer waits
+// on before it reuses the stage (raw and cooked).  Every wait is bounded.
+#pragma once
+
+#include "pc_device.cuh"
+#include "pc_filter.cuh"
+#include "pc_tiles.cuh"
+
+namespace pcn {
+
+constexpr int ST_T = 256;  // points per tile
+constexpr int ST_STAGES = 4;
+constexpr unsigned ST_RAW = tile_buffer_bytes(ST_T);
+constexpr unsigned ST_COOKED = (ST_T / 2) * 32;
+
+static_assert(ST_RAW % 16 == 0, "raw tile buffers stay 16-byte aligned");
+
+struct StreamRing {
+    float4 *cooked;        // STAGES x ST_T / 2 x 2 float4
+    unsigned char *raw;    // STAGES x ST_RAW bytes
+    uint64_t *raw_full;    // count 1 + transaction bytes
+    uint64_t *ready;       // count 32 (the producer warp)
+    uint64_t *empty;       // count = consumer warps
+    __device__ __forceinline__ const float4 *cooked_tile(int s) const {
+        return cooked + size_t(s) * (ST_T / 2) * 2;
+    }
+    __device__ __forceinline__ float *raw_tile(int s) const {
+        return reinterpret_cast<float *>(raw + size_t(s) * ST_RAW);
+    }
+};
+
+// Shared memory of the ring plus 16 bytes of flags (error, stop, warps done).
+__host__ __device__ constexpr size_t stream_smem_bytes() {
+    return size_t(ST_STAGES) * (ST_COOKED + ST_RAW) + 3 * ST_STAGES * 8 + 16;
+}
+
+// Carve the ring out of `smem` (16-byte aligned); returns the flag words.
+__device__ __forceinline__ int *stream_carve(unsigned char *smem, StreamRing &r) {
+    r.cooked = reinterpret_cast<float4 *>(smem);
+    r.raw = smem + size_t(ST_STAGES) * ST_COOKED;
+    r.raw_full = reinterpret_cast<uint64_t *>(r.raw + size_t(ST_STAGES) * ST_RAW);
+    r.ready = r.raw_full + ST_STAGES;
+    r.empty = r.ready + ST_STAGES;
+    return reinterpret_cast<int *>(r.empty + ST_STAGES);
+}
+
+// Called by thread 0 before the block's first __syncthreads.
+__device__ __forceinline__ void stream_init(const StreamRing &r, int consumer_warps) {
+    for (int s = 0; s < ST_STAGES; ++s) {
+        mbar_init(&r.raw_full[s], 1);
+        mbar_init(&r.ready[s], 32);
+        mbar_init(&r.empty[s], consumer_warps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Warp-uniform bounded wait (every lane polls; the result is agreed on).
+__device__ __forceinline__ WaitResult warp_wait(uint64_t *bar, unsigned parity,
+                                                const volatile int *stop,
+                                                uint64_t timeout_ns) {
+    const WaitResult w = mbar_wait_or_stop(bar, parity, stop, timeout_ns);
+    if (__all_sync(0xffffffffu, w == WAIT_OK)) return WAIT_OK;
+    return __any_sync(0xffffffffu, w == WAIT_TIMEOUT) ? WAIT_TIMEOUT : WAIT_STOPPED;
+}
+
+// The producer warp.  Tile `it` covers points [tile_at(it) * ST_T, ...) of
+// the cloud at `cref` (N valid points).  Stops when *stop becomes non-zero;
+// a timeout raises *err.  Before returning it waits (bounded) for every raw
+// copy it issued, so none is in flight when the block exits.
+template <class TileAt>
+__device__ __forceinline__ void stream_produce(const StreamRing &ring,
+                                               const float *cref, int N,
+                                               int ntiles, TileAt tile_at,
+                                               FilterFrame fr,
+                                               volatile int *stop,
+                                               volatile int *err,
+                                               uint64_t timeout_ns) {
+    const int lane = static_cast<int>(lane_id());
+    const float inf = __int_as_float(0x7f800000);
+    int issued = 0, cooked = 0;
+    bool ok = true;
+    for (int it = 0; it < ntiles && ok; ++it) {
+        while (issued < ntiles && issued < it + ST_STAGES) {
+            const int st = issued % ST_STAGES;
+            if (issued >= ST_STAGES) {
+                const WaitResult w = warp_wait(
+                    &ring.empty[st], unsigned((issued / ST_STAGES - 1) & 1), stop,
+                    timeout_ns);
+                if (w == WAIT_TIMEOUT && lane == 0) *err = 1;
+                if (w != WAIT_OK) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (__any_sync(0xffffffffu, *stop != 0 || *err != 0)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                const int j0 = tile_at(issued) * ST_T;
+                issue_tile(ring.raw_tile(st), cref + size_t(j0) * 3,
+                           min(ST_T, N - j0), &ring.raw_full[st]);
+            }
+            ++issued;
+        }
+        if (!ok) break;
+        const int st = it % ST_STAGES;
+        const WaitResult w = warp_wait(&ring.raw_full[st],
+                                       unsigned((it / ST_STAGES) & 1), nullptr,
+                                       timeout_ns);
+        if (w != WAIT_OK) {
+            if (lane == 0) *err = 1;
+            break;
+        }
+        cooked = it + 1;
+        const int j0 = tile_at(it) * ST_T;
+        const int cnt = min(ST_T, N - j0);
+        const float *src = ring.raw_tile(st) + tile_float_offset(cref + size_t(j0) * 3);
+        float4 *dst = ring.cooked + size_t(st) * (ST_T / 2) * 2;
+#pragma unroll
+        for (int u = 0; u < ST_T / 64; ++u) {
+            const int p = lane + 32 * u;
+            float c[2][4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = 2 * p + h;
+                if (i < cnt) {
+                    const float xp = __fsub_rn(src[3 * i], fr.cx);
+                    const float yp = __fsub_rn(src[3 * i + 1], fr.cy);
+                    const float zp = __fsub_rn(src[3 * i + 2], fr.cz);
+                    c[h][0] = xp;
+                    c[h][1] = yp;
+                    c[h][2] = zp;
+                    c[h][3] = filter_ref_w(xp, yp, zp);
+                } else {
+                    c[h][0] = c[h][1] = c[h][2] = 0.f;
+                    c[h][3] = inf;
+                }
+            }
+            dst[2 * p] = make_float4(c[0][0], c[1][0], c[0][1], c[1][1]);
+            dst[2 * p + 1] = make_float4(c[0][2], c[1][2], c[0][3], c[1][3]);
+        }
+        mbar_arrive(&ring.ready[st]);
+    }
+    // raw copies issued but never waited for must land before the block exits
+    for (int t = cooked; t < issued; ++t)
+        mbar_wait_bounded(&ring.raw_full[t % ST_STAGES], unsigned((t / ST_STAGES) & 1),
+                          timeout_ns);
+}
+
+// The filter of one query (broadcast operands a = (-2q', -2q') per axis)
+// against points 2p .. 2p + 2v - 1 of a cooked tile: bit h of the result
+// (h < 2v) is set when point 2p + h may satisfy the selection bound.
+template <int V>
+__device__ __forceinline__ unsigned stream_mask(const float4 *ck, int p, float2 ax,
+                                                float2 ay, float2 az, float thr) {
+    unsigned m = 0;
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const float4 A = ck[2 * (p + u)];
+        const float4 Z = ck[2 * (p + u) + 1];
+        float2 v = __ffma2_rn(make_float2(A.x, A.y), ax, make_float2(Z.z, Z.w));
+        v = __ffma2_rn(make_float2(A.z, A.w), ay, v);
+        v = __ffma2_rn(make_float2(Z.x, Z.y), az, v);
+        m |= (!(v.x > thr) ? 1u : 0u) << (2 * u);
+        m |= (!(v.y > thr) ? 1u : 0u) << (2 * u + 1);
+    }
+    return m;
+}
+
+// The hot-loop form: does any of the 2V points pass?
+template <int V>
+__device__ __forceinline__ bool stream_any(const float4 *ck, int p, float2 ax,
+                                           float2 ay, float2 az, float thr) {
+    bool t = false;
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+        const float4 A = ck[2 * (p + u)];
+        const float4 Z = ck[2 * (p + u) + 1];
+        float2 v = __ffma2_rn(make_float2(A.x, A.y), ax, make_float2(Z.z, Z.w));
+        v = __ffma2_rn(make_float2(A.z, A.w), ay, v);
+        v = __ffma2_rn(make_float2(Z.x, Z.y), az, v);
+        t |= !(v.x > thr) | !(v.y > thr);
+    }
+    return t;
+}
+
+}  // namespace pcn
