@@ -7,26 +7,33 @@
 // distances, unused slots hold (-1, 0).
 //
 // Design (one launch, no scratch memory):
-//  * A block has BQ_CWARPS consumer warps and one producer warp; each lane of
-//    a consumer warp owns one query (its filter constants -2q' in packed
-//    registers, its threshold, its hit count).  The producer streams the
-//    cloud's reference tiles strictly in input order and prepares them
-//    (pc_stream.cuh): centred coordinates and w' packed two points per 32
-//    bytes.
-//  * The hot loop: per step, a lane evaluates the conservative filter of
-//    pc_filter.cuh for 8 points (three packed FMAs per two points, operands
-//    read as shared-memory broadcasts) against its threshold.  No vote and no
-//    per-query shared state: 8 independent FMA chains per step per lane.
-//  * On a pass (rare) the lane recomputes which of the 8 points passed,
-//    computes their exact s32 from the raw tile and appends the hits in
-//    input order straight to its output row; at K hits its threshold becomes
-//    -inf.  When every query of a block is full a stop flag ends the block:
-//    the producer stops issuing tiles (after letting its copies in flight
-//    land) and the consumers leave the tile loop.
+//  * A block has BQ_CWARPS consumer warps and one producer warp.  Consumer
+//    warp w owns G queries of one cloud, kept in shared memory as the filter
+//    constants of pc_filter.cuh duplicated for the packed instructions,
+//    (-2x', -2x', -2y', -2y') and (-2z', -2z', thr, query index), plus the
+//    raw coordinates and the hit count.
+//  * The producer's lane 0 streams reference tiles of BQ_T = 32 * BQ_R points
+//    strictly in input order through a BQ_STAGES ring (TMA bulk copies,
+//    full/empty mbarriers); consumer warps derive the centred coordinates
+//    and w' of their points into registers (lane l holds tile points
+//    l + 32 r, so for each r the warp holds 32 consecutive references in
+//    lane order) and release the raw tile once their queries are done.
+//  * Per (query, tile) each lane evaluates the conservative filter for its
+//    BQ_R points (three packed FMAs per pair) and one vote asks whether any
+//    may be inside the radius; the hot loop is only the FMAs, the compares
+//    and the vote.  On a vote (rare) the slow path computes the exact s32
+//    from the raw tile in shared memory and, per r, a ballot gives the hits
+//    among 32 consecutive references and __popc(ballot & lanemask_lt) gives
+//    each hit its rank, so a hit is written straight to slot (hits so far +
+//    rank): input order is kept without any sort.
+//  * A query stops at K hits: it is swapped behind the still-active queries
+//    of its warp, so the hot loop tests nothing per query.  When every query
+//    of a block is full, a stop flag ends the block: the producer stops
+//    issuing tiles (after letting its copies in flight land) and the
+//    consumers leave the tile loop.
 #include "pc_device.cuh"
 #include "pc_filter.cuh"
 #include "pc_internal.h"
-#include "pc_stream.cuh"
 #include "pc_tiles.cuh"
 
 #include <algorithm>
@@ -34,8 +41,11 @@
 namespace pcn {
 namespace {
 
+constexpr int BQ_R = 8;
+constexpr int BQ_T = 32 * BQ_R;
 constexpr int BQ_CWARPS = 8;
 constexpr int BQ_THREADS = 32 * (BQ_CWARPS + 1);
+constexpr int BQ_STAGES = 4;
 constexpr unsigned FULL = 0xffffffffu;
 
 struct BqArgs {
@@ -46,11 +56,26 @@ struct BqArgs {
     int Q, N;
     float R2;
     int K;
+    int q_per_warp;
     float *out_dist2;
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
 };
+
+struct __align__(16) BqSlot {
+    float4 axy;  // (-2x', -2x', -2y', -2y')   centred coordinates
+    float4 azt;  // (-2z', -2z', thr, query index in warp (int bits))
+    float4 raw;  // (x, y, z, hits so far (int bits))
+};
+
+constexpr unsigned BQ_BUF = tile_buffer_bytes(BQ_T);
+
+__host__ __device__ constexpr size_t bq_fixed_smem() {
+    // ring, 2 * STAGES mbarriers, flags (error, stop, warps done)
+    return size_t(BQ_STAGES) * BQ_BUF + 2 * BQ_STAGES * 8 + 16;
+}
+
 
 // Valid length of cloud b: lens[b] clamped to [0, full], or full.
 __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
@@ -59,28 +84,72 @@ __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
     return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
 }
 
-__global__ void __launch_bounds__(BQ_THREADS, 3) bq_kernel(const BqArgs a) {
+// Slow path, taken only when a vote let a pair through: the lane's filter
+// mask is recomputed from its registers, points that pass get their exact
+// s32 from the raw tile in shared memory (lane l: points l + 32 r), and hits
+// are recorded in input order.  Returns the new hit count (<= K).
+__device__ __forceinline__ int bq_record(const float *tile,
+                                         const float2 (&rx)[BQ_R / 2],
+                                         const float2 (&ry)[BQ_R / 2],
+                                         const float2 (&rz)[BQ_R / 2],
+                                         const float2 (&rw)[BQ_R / 2],
+                                         float4 axy, float4 azt, const float4 q,
+                                         int hits, int j0, int cnt, float R2,
+                                         int K, size_t row, float *out_dist2,
+                                         int64_t *out_idx) {
+    const int lane = static_cast<int>(lane_id());
+    const unsigned pm = filter_mask8(rx, ry, rz, rw, axy, azt);
+#pragma unroll
+    for (int r = 0; r < BQ_R; ++r) {
+        float s = 0.f;
+        bool hit = false;
+        if (((pm >> r) & 1u) && r * 32 + lane < cnt) {
+            const float *p = tile + 3 * (lane + 32 * r);
+            s = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
+            hit = s < R2;
+        }
+        const unsigned bal = __ballot_sync(FULL, hit);
+        if (bal) {
+            const int pos = hits + __popc(bal & lanemask_lt());
+            if (hit && pos < K) {
+                out_idx[row * K + pos] = j0 + r * 32 + lane;
+                out_dist2[row * K + pos] = s;
+            }
+            hits += __popc(bal);
+            if (hits >= K) break;
+        }
+    }
+    return min(hits, K);
+}
+
+__global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.y;
+    const int G = a.q_per_warp;
     const int K = a.K;
-    const float inf = __int_as_float(0x7f800000);
 
-    StreamRing ring;
-    int *flags = stream_carve(smem, ring);
-    int *s_err = flags, *s_stop = flags + 1, *s_ndone = flags + 2;
+    TileRing ring;
+    ring.base = smem;
+    ring.bytes = BQ_BUF;
+    ring.full = reinterpret_cast<uint64_t *>(smem + BQ_STAGES * BQ_BUF);
+    ring.empty = ring.full + BQ_STAGES;
+    int *s_err = reinterpret_cast<int *>(ring.empty + BQ_STAGES);
+    int *s_stop = s_err + 1;
+    int *s_ndone = s_err + 2;
+    BqSlot *slots_all = reinterpret_cast<BqSlot *>(smem + bq_fixed_smem());
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
     const int Nb = valid_len(a.r_len, b, a.N);
     const int Qb = valid_len(a.q_len, b, a.Q);
-    const int ntiles = (Nb + ST_T - 1) / ST_T;
-    const int q0 = blockIdx.x * BQ_CWARPS * 32;
+    const int ntiles = (Nb + BQ_T - 1) / BQ_T;
 
-    if (q0 >= Qb) {
+    if (blockIdx.x * BQ_CWARPS * G >= Qb) {
         // every query of this block is past the cloud's valid length
-        const int r1 = min(a.Q, q0 + BQ_CWARPS * 32);
-        const size_t e0 = (size_t(b) * a.Q + q0) * K;
+        const int r0 = blockIdx.x * BQ_CWARPS * G;
+        const int r1 = min(a.Q, r0 + BQ_CWARPS * G);
+        const size_t e0 = (size_t(b) * a.Q + r0) * K;
         const size_t e1 = (size_t(b) * a.Q + r1) * K;
         for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
             a.out_idx[e] = -1;
@@ -88,89 +157,142 @@ __global__ void __launch_bounds__(BQ_THREADS, 3) bq_kernel(const BqArgs a) {
         }
         return;
     }
+
     if (threadIdx.x == 0) {
-        stream_init(ring, BQ_CWARPS);
+        for (int s = 0; s < BQ_STAGES; ++s) {
+            mbar_init(&ring.full[s], 1);
+            mbar_init(&ring.empty[s], BQ_CWARPS);
+        }
         *s_err = 0;
         *s_stop = 0;
         *s_ndone = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    const FilterFrame fr = filter_frame(cref, min(ST_T, Nb));
-    __syncthreads();
 
     if (warp == BQ_CWARPS) {  // producer warp
-        stream_produce(ring, cref, Nb, ntiles, [](int it) { return it; }, fr,
-                       s_stop, s_err, a.timeout_ns);
+        __syncthreads();
+        if (lane == 0)
+            ring_produce<BQ_STAGES>(
+                ring, cref, Nb, BQ_T, ntiles, [](int it) { return it; },
+                s_stop, s_err, a.timeout_ns);
         return;
     }
 
-    const int qi = q0 + warp * 32 + lane;
-    const bool valid = qi < Qb;
-    float qx = 0.f, qy = 0.f, qz = 0.f;
-    if (valid) {
-        const float *p = a.query + (size_t(b) * a.Q + qi) * 3;
-        qx = p[0];
-        qy = p[1];
-        qz = p[2];
+    const int q_warp0 = (blockIdx.x * BQ_CWARPS + warp) * G;
+    const int nq = max(0, min(G, Qb - q_warp0));
+    BqSlot *slots = slots_all + warp * G;
+    const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
+    const FilterFrame fr = filter_frame(cref, min(BQ_T, Nb));
+    for (int g = lane; g < G; g += 32) {
+        float x = 0.f, y = 0.f, z = 0.f;
+        if (g < nq) {
+            const float *p = cq + size_t(q_warp0 + g) * 3;
+            x = p[0];
+            y = p[1];
+            z = p[2];
+        }
+        const float xp = __fsub_rn(x, fr.cx), yp = __fsub_rn(y, fr.cy),
+                    zp = __fsub_rn(z, fr.cz);
+        const float ax = -2.0f * xp, ay = -2.0f * yp, az = -2.0f * zp;
+        const float thr = filter_threshold(a.R2, filter_norm2(xp, yp, zp));
+        slots[g].axy = make_float4(ax, ax, ay, ay);
+        slots[g].azt = make_float4(az, az, thr, __int_as_float(g));
+        slots[g].raw = make_float4(x, y, z, __int_as_float(0));
     }
-    const float xp = __fsub_rn(qx, fr.cx), yp = __fsub_rn(qy, fr.cy),
-                zp = __fsub_rn(qz, fr.cz);
-    const float2 ax = make_float2(-2.0f * xp, -2.0f * xp);
-    const float2 ay = make_float2(-2.0f * yp, -2.0f * yp);
-    const float2 az = make_float2(-2.0f * zp, -2.0f * zp);
-    float thr = valid ? filter_threshold(a.R2, filter_norm2(xp, yp, zp)) : -inf;
-    const size_t row = size_t(b) * a.Q + qi;
-    int hits = 0;
-    bool done = !valid;
-    bool reported = false;
-    volatile int *vstop = s_stop;
-    if (__all_sync(FULL, done)) {
-        reported = true;
-        if (lane == 0 && atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS) *vstop = 1;
-    }
+    __syncthreads();
 
+    // Queries still short of K hits occupy slots [0, active); a query that
+    // fills up is swapped behind them, so the hot loop checks nothing per
+    // query.
+    volatile int *vstop = s_stop;
+    int active = nq;
+    if (active == 0 && lane == 0 && atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS)
+        *vstop = 1;
     bool failed = false;
     for (int it = 0; it < ntiles; ++it) {
         if (__any_sync(FULL, *vstop != 0)) break;
-        const int st = it % ST_STAGES;
-        const WaitResult w = warp_wait(&ring.ready[st], unsigned((it / ST_STAGES) & 1),
-                                       s_stop, a.timeout_ns);
-        if (w != WAIT_OK) {
-            failed = w == WAIT_TIMEOUT;
+        const int st = it % BQ_STAGES;
+        const WaitResult w = mbar_wait_or_stop(
+            &ring.full[st], unsigned((it / BQ_STAGES) & 1), s_stop, a.timeout_ns);
+        if (!__all_sync(FULL, w == WAIT_OK)) {
+            failed = !__all_sync(FULL, w != WAIT_TIMEOUT);
             break;
         }
-        if (!__all_sync(FULL, done)) {
-            const float4 *ck = ring.cooked_tile(st);
-            const int j0 = it * ST_T;
-            const int cnt = min(ST_T, Nb - j0);
-            const float *raw =
-                ring.raw_tile(st) + tile_float_offset(cref + size_t(j0) * 3);
-            const int npairs = (cnt + 1) >> 1;
-            for (int p = 0; p < npairs; p += 4) {
-                if (!stream_any<4>(ck, p, ax, ay, az, thr)) continue;
-                unsigned m = stream_mask<4>(ck, p, ax, ay, az, thr);
-                while (m) {  // points in increasing index order
-                    const int i = 2 * p + __ffs(m) - 1;
-                    m &= m - 1;
-                    if (i >= cnt || hits >= K) continue;
-                    const float sv = sqdist(qx, qy, qz, raw[3 * i], raw[3 * i + 1],
-                                            raw[3 * i + 2]);
-                    if (sv < a.R2) {
-                        a.out_idx[row * K + hits] = j0 + i;
-                        a.out_dist2[row * K + hits] = sv;
-                        if (++hits == K) {
-                            done = true;
-                            thr = -inf;
+        const int j0 = it * BQ_T;
+        const int cnt = min(BQ_T, Nb - j0);
+        const float *buf =
+            ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
+        if (active > 0) {
+            // centred coordinates and w' of this lane's points (points past
+            // cnt hold stale values: they may pass and are masked exactly)
+            float2 rx[BQ_R / 2], ry[BQ_R / 2], rz[BQ_R / 2], rw[BQ_R / 2];
+#pragma unroll
+            for (int p = 0; p < BQ_R / 2; ++p) {
+                const float *p0 = buf + 3 * (lane + 32 * (2 * p));
+                const float *p1 = buf + 3 * (lane + 32 * (2 * p + 1));
+                const float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
+                            z0 = __fsub_rn(p0[2], fr.cz);
+                const float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
+                            z1 = __fsub_rn(p1[2], fr.cz);
+                rx[p] = make_float2(x0, x1);
+                ry[p] = make_float2(y0, y1);
+                rz[p] = make_float2(z0, z1);
+                rw[p] = make_float2(filter_ref_w(x0, y0, z0),
+                                    filter_ref_w(x1, y1, z1));
+            }
+
+            bool any_full = false;
+            auto record = [&](BqSlot *sp, float4 axy, float4 azt) {
+                const float4 q = sp->raw;
+                const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(azt.w);
+                const int h = bq_record(buf, rx, ry, rz, rw, axy, azt, q,
+                                        __float_as_int(q.w), j0, cnt, a.R2, K, row,
+                                        a.out_dist2, a.out_idx);
+                if (lane == 0) sp->raw.w = __int_as_float(h);
+                any_full |= h >= K;
+            };
+            // two queries per step: independent filter chains for the scheduler
+            int g = 0;
+            for (; g + 1 < active; g += 2) {
+                BqSlot *s0 = slots + g;
+                const float4 axy0 = s0[0].axy, azt0 = s0[0].azt;
+                const float4 axy1 = s0[1].axy, azt1 = s0[1].azt;
+                const bool t0 = filter_any8(rx, ry, rz, rw, axy0, azt0);
+                const bool t1 = filter_any8(rx, ry, rz, rw, axy1, azt1);
+                const bool v0 = __any_sync(FULL, t0), v1 = __any_sync(FULL, t1);
+                if (v0) record(s0, axy0, azt0);
+                if (v1) record(s0 + 1, axy1, azt1);
+            }
+            if (g < active) {
+                BqSlot *s0 = slots + g;
+                const float4 axy = s0->axy, azt = s0->azt;
+                if (__any_sync(FULL, filter_any8(rx, ry, rz, rw, axy, azt)))
+                    record(s0, axy, azt);
+            }
+            if (any_full) {  // rare: move full queries behind the active ones
+                __syncwarp();
+                if (lane == 0) {
+                    int g = 0;
+                    while (g < active) {
+                        if (__float_as_int(slots[g].raw.w) >= K) {
+                            const BqSlot t = slots[g];
+                            slots[g] = slots[active - 1];
+                            slots[active - 1] = t;
+                            --active;
+                        } else {
+                            ++g;
                         }
                     }
                 }
+                active = __shfl_sync(FULL, active, 0);
+                __syncwarp();
+                if (active == 0 && lane == 0 &&
+                    atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS)
+                    *vstop = 1;
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[st]);  // tile no longer read
-        if (!reported && __all_sync(FULL, done)) {
-            reported = true;
-            if (lane == 0 && atomicAdd(s_ndone, 1) + 1 == BQ_CWARPS) *vstop = 1;
-        }
+        if (lane == 0) mbar_arrive(&ring.empty[st]);  // raw tile no longer read
     }
 
     if (failed) {
@@ -179,12 +301,23 @@ __global__ void __launch_bounds__(BQ_THREADS, 3) bq_kernel(const BqArgs a) {
             *vstop = 1;
         }
         raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
-        hits = 0;
     }
-    (void)inf;
-    // pad the unused slots with (-1, 0); rows past the valid length in full
-    if (qi < a.Q) {
-        for (int e = valid ? hits : 0; e < K; ++e) {
+    // pad the unused slots with (-1, 0); after a failure every slot; rows
+    // past the valid length in full
+    __syncwarp();
+    const int nrows = max(0, min(G, a.Q - q_warp0));
+    for (int g = nq; g < nrows; ++g) {
+        const size_t row = size_t(b) * a.Q + q_warp0 + g;
+        for (int e = lane; e < K; e += 32) {
+            a.out_idx[row * K + e] = -1;
+            a.out_dist2[row * K + e] = 0.0f;
+        }
+    }
+    for (int g = 0; g < nq; ++g) {
+        const BqSlot q = slots[g];
+        const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(q.azt.w);
+        const int hits = failed ? 0 : __float_as_int(q.raw.w);
+        for (int e = hits + lane; e < K; e += 32) {
             a.out_idx[row * K + e] = -1;
             a.out_dist2[row * K + e] = 0.0f;
         }
@@ -212,15 +345,23 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
-    (void)dev.smem_per_sm;
-    const size_t smem = stream_smem_bytes();
+
+    const int slots = dev.sm_count * 2;
+    const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));
+    int64_t G = (Q + BQ_CWARPS * bpc_target - 1) / (BQ_CWARPS * bpc_target);
+    const size_t budget =
+        std::min<size_t>(dev.smem_per_block_optin, dev.smem_per_sm / 2 - 2048);
+    const int64_t gmax = std::max<int64_t>(
+        1, int64_t((budget - bq_fixed_smem()) / (BQ_CWARPS * sizeof(BqSlot))));
+    G = std::max<int64_t>(1, std::min(G, gmax));
+    a.q_per_warp = static_cast<int>(G);
+    const int64_t bpc = (Q + BQ_CWARPS * G - 1) / (BQ_CWARPS * G);
+    const size_t smem = bq_fixed_smem() + size_t(BQ_CWARPS) * G * sizeof(BqSlot);
     cudaError_t e = cudaFuncSetAttribute(
         bq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t per_block = int64_t(BQ_CWARPS) * 32;
-    dim3 grid(static_cast<unsigned>((Q + per_block - 1) / per_block),
-              static_cast<unsigned>(B));
+    dim3 grid(static_cast<unsigned>(bpc), static_cast<unsigned>(B));
     bq_kernel<<<grid, BQ_THREADS, smem, stream>>>(a);
     return cudaGetLastError();
 }

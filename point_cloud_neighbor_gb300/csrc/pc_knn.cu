@@ -436,11 +436,14 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // and replaces the root by every point that beats it (sift-down).  At the end
 // each lane heap-sorts its k entries into ascending (s, j) order.
 // ---------------------------------------------------------------------------
-constexpr int KL_CWARPS = 8;
+constexpr int KL_QL = 1;                        // queries per lane (1: measured best)
+constexpr int KL_CWARPS = 8 / KL_QL;            // consumer warps per block
+constexpr int KL_QPB = KL_CWARPS * 32 * KL_QL;  // queries per block
 constexpr int KL_THREADS = 32 * (KL_CWARPS + 1);
+constexpr int KL_MINB = KL_QL == 1 ? 2 : (KL_QL == 2 ? 3 : 5);  // blocks per SM
 
 __host__ __device__ constexpr size_t knn_lane_smem(int k) {
-    return stream_smem_bytes() + size_t(KL_CWARPS) * 32 * size_t(k) * 8;
+    return stream_smem_bytes() + size_t(KL_QPB) * size_t(k) * 8;
 }
 
 // Lexicographic (s, j) "a after b".
@@ -474,7 +477,7 @@ __device__ __forceinline__ void heap_sift(float *hs, int *hj, int n, int pos,
     hj[pos * 32] = j;
 }
 
-__global__ void __launch_bounds__(KL_THREADS, 3) knn_lane_kernel(const KnnArgs a) {
+__global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const KnnArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -486,18 +489,18 @@ __global__ void __launch_bounds__(KL_THREADS, 3) knn_lane_kernel(const KnnArgs a
     int *flags = stream_carve(smem, ring);
     int *s_err = flags;
     float *hs_all = reinterpret_cast<float *>(smem + stream_smem_bytes());
-    int *hj_all = reinterpret_cast<int *>(hs_all + size_t(KL_CWARPS) * 32 * k);
+    int *hj_all = reinterpret_cast<int *>(hs_all + size_t(KL_QPB) * k);
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
     const int Nb = valid_len(a.r_len, b, a.N);
     const int Qb = valid_len(a.q_len, b, a.Q);
     const int ntiles = (Nb + ST_T - 1) / ST_T;
     const int tstride = scramble_stride(ntiles);
-    const int q0 = blockIdx.x * KL_CWARPS * 32;
+    const int q0 = blockIdx.x * KL_QPB;
 
     if (q0 >= Qb) {
         // every query of this block is past the cloud's valid length
-        const int r1 = min(a.Q, q0 + KL_CWARPS * 32);
+        const int r1 = min(a.Q, q0 + KL_QPB);
         const size_t e0 = (size_t(b) * a.Q + q0) * k;
         const size_t e1 = (size_t(b) * a.Q + r1) * k;
         for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
@@ -520,30 +523,40 @@ __global__ void __launch_bounds__(KL_THREADS, 3) knn_lane_kernel(const KnnArgs a
         return;
     }
 
-    const int qi = q0 + warp * 32 + lane;
-    const bool valid = qi < Qb;
-    float qx = 0.f, qy = 0.f, qz = 0.f;
-    if (valid) {
-        const float *p = a.query + (size_t(b) * a.Q + qi) * 3;
-        qx = p[0];
-        qy = p[1];
-        qz = p[2];
+    // query q of this lane: q0 + (warp * KL_QL + q) * 32 + lane; its heap is
+    // at slot (warp * KL_QL + q) * 32 + lane, entries 32 apart
+    int qi[KL_QL];
+    bool valid[KL_QL];
+    float qx[KL_QL], qy[KL_QL], qz[KL_QL], qq[KL_QL], thr[KL_QL], ts[KL_QL];
+    int tj[KL_QL];
+    float2 ax[KL_QL], ay[KL_QL], az[KL_QL];
+#pragma unroll
+    for (int q = 0; q < KL_QL; ++q) {
+        qi[q] = q0 + (warp * KL_QL + q) * 32 + lane;
+        valid[q] = qi[q] < Qb;
+        qx[q] = qy[q] = qz[q] = 0.f;
+        if (valid[q]) {
+            const float *p = a.query + (size_t(b) * a.Q + qi[q]) * 3;
+            qx[q] = p[0];
+            qy[q] = p[1];
+            qz[q] = p[2];
+        }
+        const float xp = __fsub_rn(qx[q], fr.cx), yp = __fsub_rn(qy[q], fr.cy),
+                    zp = __fsub_rn(qz[q], fr.cz);
+        ax[q] = make_float2(-2.0f * xp, -2.0f * xp);
+        ay[q] = make_float2(-2.0f * yp, -2.0f * yp);
+        az[q] = make_float2(-2.0f * zp, -2.0f * zp);
+        qq[q] = filter_norm2(xp, yp, zp);
+        ts[q] = inf;      // heap root: the k-th best so far
+        tj[q] = INT_MAX;
+        thr[q] = valid[q] ? inf : -inf;
+        float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+        int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+        for (int e = 0; e < k; ++e) {
+            hs[e * 32] = inf;
+            hj[e * 32] = INT_MAX;
+        }
     }
-    const float xp = __fsub_rn(qx, fr.cx), yp = __fsub_rn(qy, fr.cy),
-                zp = __fsub_rn(qz, fr.cz);
-    const float2 ax = make_float2(-2.0f * xp, -2.0f * xp);
-    const float2 ay = make_float2(-2.0f * yp, -2.0f * yp);
-    const float2 az = make_float2(-2.0f * zp, -2.0f * zp);
-    const float qq = filter_norm2(xp, yp, zp);
-    float *hs = hs_all + size_t(warp) * 32 * k + lane;
-    int *hj = hj_all + size_t(warp) * 32 * k + lane;
-    for (int e = 0; e < k; ++e) {
-        hs[e * 32] = inf;
-        hj[e * 32] = INT_MAX;
-    }
-    float ts = inf;      // root: the k-th best so far
-    int tj = INT_MAX;
-    float thr = valid ? inf : -inf;
 
     bool failed = false;
     for (int it = 0; it < ntiles; ++it) {
@@ -560,20 +573,40 @@ __global__ void __launch_bounds__(KL_THREADS, 3) knn_lane_kernel(const KnnArgs a
         const float *raw = ring.raw_tile(st) + tile_float_offset(cref + size_t(j0) * 3);
         const int npairs = (cnt + 1) >> 1;
         for (int p = 0; p < npairs; p += 4) {
-            if (!stream_any<4>(ck, p, ax, ay, az, thr)) continue;
-            unsigned m = stream_mask<4>(ck, p, ax, ay, az, thr);
-            while (m) {
-                const int i = 2 * p + __ffs(m) - 1;
-                m &= m - 1;
-                if (i >= cnt || !valid) continue;
-                const float sv = sqdist(qx, qy, qz, raw[3 * i], raw[3 * i + 1],
-                                        raw[3 * i + 2]);
-                const int j = j0 + i;
-                if (sj_after(ts, tj, sv, j)) {
-                    heap_sift(hs, hj, k, 0, sv, j);
-                    ts = hs[0];
-                    tj = hj[0];
-                    thr = tj == INT_MAX ? inf : filter_threshold(ts, qq);
+            bool pass = false;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 A = ck[2 * (p + u)];
+                const float4 Z = ck[2 * (p + u) + 1];
+#pragma unroll
+                for (int q = 0; q < KL_QL; ++q) {
+                    float2 v = __ffma2_rn(make_float2(A.x, A.y), ax[q],
+                                          make_float2(Z.z, Z.w));
+                    v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
+                    v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
+                    pass |= !(v.x > thr[q]) | !(v.y > thr[q]);
+                }
+            }
+            if (!pass) continue;
+#pragma unroll
+            for (int q = 0; q < KL_QL; ++q) {
+                unsigned m = stream_mask<4>(ck, p, ax[q], ay[q], az[q], thr[q]);
+                if (!valid[q]) m = 0;
+                float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+                int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+                while (m) {
+                    const int i = 2 * p + __ffs(m) - 1;
+                    m &= m - 1;
+                    if (i >= cnt) continue;
+                    const float sv = sqdist(qx[q], qy[q], qz[q], raw[3 * i],
+                                            raw[3 * i + 1], raw[3 * i + 2]);
+                    const int j = j0 + i;
+                    if (sj_after(ts[q], tj[q], sv, j)) {
+                        heap_sift(hs, hj, k, 0, sv, j);
+                        ts[q] = hs[0];
+                        tj[q] = hj[0];
+                        thr[q] = tj[q] == INT_MAX ? inf : filter_threshold(ts[q], qq[q]);
+                    }
                 }
             }
         }
@@ -581,24 +614,29 @@ __global__ void __launch_bounds__(KL_THREADS, 3) knn_lane_kernel(const KnnArgs a
         if (lane == 0) mbar_arrive(&ring.empty[st]);  // tile no longer read
     }
 
-    const size_t row = size_t(b) * a.Q + qi;
     if (failed) {
         if (lane == 0) *s_err = 1;
         raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
-        if (qi < a.Q)
+    }
+#pragma unroll
+    for (int q = 0; q < KL_QL; ++q) {
+        if (qi[q] >= a.Q) continue;
+        const size_t row = size_t(b) * a.Q + qi[q];
+        if (failed) {
             for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
-        return;
-    }
-    // heap sort: the largest entry moves to the end, k - 1 times
-    for (int n = k - 1; n > 0; --n) {
-        const float s = hs[n * 32];
-        const int j = hj[n * 32];
-        hs[n * 32] = hs[0];
-        hj[n * 32] = hj[0];
-        heap_sift(hs, hj, n, 0, s, j);
-    }
-    if (qi < a.Q) {
-        const int kv = valid ? min(k, Nb) : 0;
+            continue;
+        }
+        float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+        int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+        // heap sort: the largest entry moves to the end, k - 1 times
+        for (int n = k - 1; n > 0; --n) {
+            const float s = hs[n * 32];
+            const int j = hj[n * 32];
+            hs[n * 32] = hs[0];
+            hj[n * 32] = hj[0];
+            heap_sift(hs, hj, n, 0, s, j);
+        }
+        const int kv = valid[q] ? min(k, Nb) : 0;
         for (int e = 0; e < k; ++e) {
             const float sv = hs[e * 32];
             a.out_idx[row * k + e] = e < kv ? int64_t(hj[e * 32]) : int64_t(-1);
@@ -615,7 +653,7 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a, int64_t B,
         knn_lane_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t per_block = int64_t(KL_CWARPS) * 32;
+    const int64_t per_block = KL_QPB;
     dim3 grid(static_cast<unsigned>((Q + per_block - 1) / per_block),
               static_cast<unsigned>(B));
     knn_lane_kernel<<<grid, KL_THREADS, smem, stream>>>(a);
