@@ -247,18 +247,32 @@ def run_gpu(args):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
+    # FPS runs one thread-block cluster per cloud (16 SMs here) for thousands
+    # of dependent steps; kNN and Ball Query are independent of it and fill
+    # the other SMs, so the step issues FPS on a side stream concurrently
+    # with kNN + Ball Query on the main stream (--serial: one stream).
+    side = torch.cuda.Stream(device) if not args.serial else stream
+    fork = torch.cuda.Event()
+
     def step(ev=None):
+        # ev: [start, fps_end (side), knn_end, bq_end, step_end]
         if ev is not None:
             ev[0].record(stream)
-        pc.pc_fps(x, npoint, 0, out=fps_out, workspace=ws)
-        if ev is not None:
-            ev[1].record(stream)
+        fork.record(stream)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            pc.pc_fps(x, npoint, 0, out=fps_out, workspace=ws)
+            if ev is not None:
+                ev[1].record(side)
         pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
         if ev is not None:
             ev[2].record(stream)
         pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
         if ev is not None:
             ev[3].record(stream)
+        stream.wait_stream(side)
+        if ev is not None:
+            ev[4].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -266,7 +280,7 @@ def run_gpu(args):
     torch.cuda.synchronize(device)
     assert pc.pc_device_status(reset=True, device=device) == 0
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
               for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(device)
@@ -280,10 +294,12 @@ def run_gpu(args):
     barrier(world)
     launches = 3 * args.steps
 
+    # each operator timed on the stream it runs on (FPS: side stream from the
+    # fork; kNN from the fork when concurrent, after FPS when serial)
     t_fps = [e[0].elapsed_time(e[1]) for e in events]
-    t_knn = [e[1].elapsed_time(e[2]) for e in events]
+    t_knn = [(e[1] if args.serial else e[0]).elapsed_time(e[2]) for e in events]
     t_bq = [e[2].elapsed_time(e[3]) for e in events]
-    total_ms = sum(e[0].elapsed_time(e[3]) for e in events)
+    total_ms = sum(e[0].elapsed_time(e[4]) for e in events)
     total_ms, fps_ms, knn_ms, bq_ms = max_over_ranks(
         [total_ms, sum(t_fps), sum(t_knn), sum(t_bq)], world, device)
     ms_per_step = total_ms / args.steps
@@ -365,7 +381,9 @@ def run_gpu(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": workload_config({"parallelism": f"replicas x{world}"}),
+        "config": workload_config({"parallelism": f"replicas x{world}",
+                                   "streams": ("1 (serial)" if args.serial else
+                                               "2: FPS concurrent with kNN + Ball Query")}),
         "roofline": roof, "ops": ops, "grid": grid, "next_rows": next_rows,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -621,11 +639,18 @@ def run_e2e(args, pc, x_host, device, world):
     h2d = x_pin.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
 
+    main = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device) if not args.serial else main
+
     def one():
         xd = x_pin.to(device, non_blocking=True)
-        f = pc.pc_fps(xd, npoint, 0)
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            f = pc.pc_fps(xd, npoint, 0)
         d, i = pc.pc_knn(xd, xd, k)
         d2, i2 = pc.pc_ball_query(xd, xd, r, K)
+        main.wait_stream(side)
+        f.record_stream(main)
         outs["fps"].copy_(f, non_blocking=True)
         outs["knn_d"].copy_(d, non_blocking=True)
         outs["knn_i"].copy_(i, non_blocking=True)
@@ -747,6 +772,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial", action="store_true",
+                    help="run FPS, kNN and Ball Query one after another on one "
+                         "stream instead of FPS concurrently on a side stream")
     ap.add_argument("--only", choices=["fps", "knn", "ball_query", "grid_build",
                                        "grid_knn", "grid_ball_query", "chamfer",
                                        "three_interpolate",
