@@ -522,6 +522,11 @@ FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
             p.why = "block's share of the cloud exceeds shared memory";
             return p;
         }
+        // When the schedule fits in one wave, each block claims its SM's whole
+        // shared memory: blocks of kernels running concurrently on other
+        // streams then cannot share an FPS SM and slow its per-step latency.
+        if (B * cs <= nsm)
+            p.smem_bytes = std::max(p.smem_bytes, dev.smem_per_block_optin);
         if (strategy == 2 && !cluster_fits(dev, cs, p.threads, p.smem_bytes, p.ppt)) {
             if (cluster_size > 0 || cs <= 8) {
                 p.why = "cluster of this size cannot be resident on this device";
