@@ -249,30 +249,34 @@ def run_gpu(args):
 
     # FPS runs one thread-block cluster per cloud (16 SMs here) for thousands
     # of dependent steps; kNN and Ball Query are independent of it and fill
-    # the other SMs, so the step issues FPS on a side stream concurrently
-    # with kNN + Ball Query on the main stream (--serial: one stream).
+    # the other SMs.  FPS is issued first, on the main stream, so that its
+    # cluster is resident before the kNN and Ball Query blocks (issued on a
+    # side stream after the same start point) occupy the rest of the GPU
+    # (--serial: everything on one stream).
     side = torch.cuda.Stream(device) if not args.serial else stream
     fork = torch.cuda.Event()
 
     def step(ev=None):
-        # ev: [start, fps_end (side), knn_end, bq_end, step_end]
+        # ev: [start, fps_end, knn_start (side), knn_end, bq_end, step_end]
         if ev is not None:
             ev[0].record(stream)
         fork.record(stream)
+        pc.pc_fps(x, npoint, 0, out=fps_out, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
         side.wait_event(fork)
         with torch.cuda.stream(side):
-            pc.pc_fps(x, npoint, 0, out=fps_out, workspace=ws)
             if ev is not None:
-                ev[1].record(side)
-        pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
-        if ev is not None:
-            ev[2].record(stream)
-        pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
-        if ev is not None:
-            ev[3].record(stream)
+                ev[2].record(side)
+            pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
+            if ev is not None:
+                ev[3].record(side)
+            pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
+            if ev is not None:
+                ev[4].record(side)
         stream.wait_stream(side)
         if ev is not None:
-            ev[4].record(stream)
+            ev[5].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -280,7 +284,7 @@ def run_gpu(args):
     torch.cuda.synchronize(device)
     assert pc.pc_device_status(reset=True, device=device) == 0
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
               for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(device)
@@ -294,12 +298,11 @@ def run_gpu(args):
     barrier(world)
     launches = 3 * args.steps
 
-    # each operator timed on the stream it runs on (FPS: side stream from the
-    # fork; kNN from the fork when concurrent, after FPS when serial)
+    # each operator timed on the stream it runs on
     t_fps = [e[0].elapsed_time(e[1]) for e in events]
-    t_knn = [(e[1] if args.serial else e[0]).elapsed_time(e[2]) for e in events]
-    t_bq = [e[2].elapsed_time(e[3]) for e in events]
-    total_ms = sum(e[0].elapsed_time(e[4]) for e in events)
+    t_knn = [e[2].elapsed_time(e[3]) for e in events]
+    t_bq = [e[3].elapsed_time(e[4]) for e in events]
+    total_ms = sum(e[0].elapsed_time(e[5]) for e in events)
     total_ms, fps_ms, knn_ms, bq_ms = max_over_ranks(
         [total_ms, sum(t_fps), sum(t_knn), sum(t_bq)], world, device)
     ms_per_step = total_ms / args.steps
@@ -645,12 +648,13 @@ def run_e2e(args, pc, x_host, device, world):
     def one():
         xd = x_pin.to(device, non_blocking=True)
         side.wait_stream(main)
+        f = pc.pc_fps(xd, npoint, 0)
         with torch.cuda.stream(side):
-            f = pc.pc_fps(xd, npoint, 0)
-        d, i = pc.pc_knn(xd, xd, k)
-        d2, i2 = pc.pc_ball_query(xd, xd, r, K)
+            d, i = pc.pc_knn(xd, xd, k)
+            d2, i2 = pc.pc_ball_query(xd, xd, r, K)
         main.wait_stream(side)
-        f.record_stream(main)
+        for t in (d, i, d2, i2):
+            t.record_stream(main)
         outs["fps"].copy_(f, non_blocking=True)
         outs["knn_d"].copy_(d, non_blocking=True)
         outs["knn_i"].copy_(i, non_blocking=True)
