@@ -13,10 +13,18 @@
 // nothing); any other index outside [0, M) sets PC_ERR_INVALID_ARGUMENT in
 // the device status word and is treated as padding.
 //
-// Both kernels stream the [.., n] axis with one thread per point i (loads of
-// out / grad_out coalesced along i) and loop over a chunk of channels, so the
-// three indices and weights of a point are read once per chunk; the gathers
-// from f hit L2 (a [C, M] feature block is re-read across the chunk's points).
+// Staged kernels (used when a chunk of channels of one cloud fits in shared
+// memory, M <= 16384): a block owns (cloud b, channels c0 .. c0 + CC):
+//   forward  -- copies f[b, c0.., :] into shared memory (coalesced), then for
+//               a range of points i reads the three (index, weight) pairs once
+//               and writes out[b, c, i] for its CC channels (coalesced along
+//               i), gathering from shared memory;
+//   backward -- accumulates grad_f[b, c0.., :] in shared memory over all n
+//               points (shared-memory atomic adds of w * grad_out, grad_out
+//               read coalesced along i), then writes the block out once: no
+//               memset and no global atomics.
+// Otherwise the direct kernels gather from global memory (L2) with one thread
+// per point and global atomic adds for the backward.
 //
 // gather_points (project page, "PyTorch3D-style Ball Query": return_nn gives
 // the neighbor coordinates, zeros where idx = -1):
@@ -102,6 +110,69 @@ three_interpolate_backward_kernel(const float *__restrict__ g,
     }
 }
 
+// --- staged (shared-memory) kernels -------------------------------------------
+constexpr int STG_THREADS = 256;
+constexpr int STG_SMEM_FLOATS = 16384;   // 64 KB of features per block
+constexpr int STG_POINTS = 1024;         // points per forward block
+
+__global__ void __launch_bounds__(STG_THREADS)
+three_interpolate_staged_kernel(const float *__restrict__ f,
+                                const int64_t *__restrict__ idx,
+                                const float *__restrict__ w, int C, int M, int n,
+                                int CC, float *__restrict__ out, int *status) {
+    extern __shared__ float tile[];  // [CC][M]
+    const int b = blockIdx.z;
+    const int c0 = blockIdx.y * CC;
+    const int cc = min(CC, C - c0);
+    const float *fb = f + (size_t(b) * C + c0) * size_t(M);
+    for (int e = threadIdx.x; e < cc * M; e += STG_THREADS) tile[e] = __ldg(fb + e);
+    __syncthreads();
+    const int i1 = min(n, (blockIdx.x + 1) * STG_POINTS);
+    for (int i = blockIdx.x * STG_POINTS + threadIdx.x; i < i1; i += STG_THREADS) {
+        int m[3];
+        float wt[3];
+        load_triplet(idx, w, (size_t(b) * n + i) * 3, M, m, wt, status);
+        for (int c = 0; c < cc; ++c) {
+            const float *tr = tile + c * M;
+            const float v0 = m[0] >= 0 ? tr[m[0]] : 0.0f;
+            const float v1 = m[1] >= 0 ? tr[m[1]] : 0.0f;
+            const float v2 = m[2] >= 0 ? tr[m[2]] : 0.0f;
+            const float s01 = __fadd_rn(__fmul_rn(wt[0], v0), __fmul_rn(wt[1], v1));
+            out[(size_t(b) * C + c0 + c) * size_t(n) + i] =
+                __fadd_rn(s01, __fmul_rn(wt[2], v2));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(STG_THREADS)
+three_interpolate_backward_staged_kernel(const float *__restrict__ g,
+                                         const int64_t *__restrict__ idx,
+                                         const float *__restrict__ w, int C,
+                                         int M, int n, int CC,
+                                         float *__restrict__ grad_f, int *status) {
+    extern __shared__ float tile[];  // [CC][M]
+    const int b = blockIdx.y;
+    const int c0 = blockIdx.x * CC;
+    const int cc = min(CC, C - c0);
+    for (int e = threadIdx.x; e < cc * M; e += STG_THREADS) tile[e] = 0.0f;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += STG_THREADS) {
+        int m[3];
+        float wt[3];
+        load_triplet(idx, w, (size_t(b) * n + i) * 3, M, m, wt, status);
+        for (int c = 0; c < cc; ++c) {
+            const float gv = __ldg(g + (size_t(b) * C + c0 + c) * size_t(n) + i);
+            float *tr = tile + c * M;
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+                if (m[t] >= 0) atomicAdd(tr + m[t], __fmul_rn(wt[t], gv));
+        }
+    }
+    __syncthreads();
+    float *gb = grad_f + (size_t(b) * C + c0) * size_t(M);
+    for (int e = threadIdx.x; e < cc * M; e += STG_THREADS) gb[e] = tile[e];
+}
+
 __global__ void gather_points_kernel(const float *__restrict__ x, int N,
                                      const int64_t *__restrict__ idx,
                                      int64_t QK, int64_t total,
@@ -172,13 +243,30 @@ extern "C" int pc_three_interpolate(const float *features, int64_t B,
     if ((rc = pcn::api_check_ptr(idx, d, 8, "idx")) != PC_OK) return rc;
     if ((rc = pcn::api_check_ptr(weight, d, 4, "weight")) != PC_OK) return rc;
     if ((rc = pcn::api_check_ptr(out, d, 4, "out")) != PC_OK) return rc;
-    const dim3 grid(unsigned((n + pcn::INTERP_THREADS - 1) / pcn::INTERP_THREADS),
-                    unsigned((C + pcn::INTERP_CCHUNK - 1) / pcn::INTERP_CCHUNK),
-                    unsigned(B));
-    pcn::three_interpolate_kernel<<<grid, pcn::INTERP_THREADS, 0,
-                                    static_cast<cudaStream_t>(stream)>>>(
-        features, idx, weight, int(C), int(M), int(n), out, dev->status_word);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (M > 0 && M <= pcn::STG_SMEM_FLOATS) {
+        const int CC = int(std::min<int64_t>(C, pcn::STG_SMEM_FLOATS / M));
+        const size_t smem = size_t(CC) * size_t(M) * sizeof(float);
+        e = cudaFuncSetAttribute(pcn::three_interpolate_staged_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e == cudaSuccess) {
+            const dim3 grid(unsigned((n + pcn::STG_POINTS - 1) / pcn::STG_POINTS),
+                            unsigned((C + CC - 1) / CC), unsigned(B));
+            pcn::three_interpolate_staged_kernel<<<grid, pcn::STG_THREADS, smem,
+                                                   static_cast<cudaStream_t>(stream)>>>(
+                features, idx, weight, int(C), int(M), int(n), CC, out,
+                dev->status_word);
+            e = cudaGetLastError();
+        }
+    } else {
+        const dim3 grid(unsigned((n + pcn::INTERP_THREADS - 1) / pcn::INTERP_THREADS),
+                        unsigned((C + pcn::INTERP_CCHUNK - 1) / pcn::INTERP_CCHUNK),
+                        unsigned(B));
+        pcn::three_interpolate_kernel<<<grid, pcn::INTERP_THREADS, 0,
+                                        static_cast<cudaStream_t>(stream)>>>(
+            features, idx, weight, int(C), int(M), int(n), out, dev->status_word);
+        e = cudaGetLastError();
+    }
     return e == cudaSuccess ? PC_OK : cuda_err(e, "three_interpolate: launch");
 }
 
@@ -202,6 +290,26 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         if ((rc = pcn::api_check_ptr(weight, d, 4, "weight")) != PC_OK) return rc;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (M <= pcn::STG_SMEM_FLOATS) {
+        // channels per block: a shared-memory tile of at most 64 KB, and about
+        // two blocks per SM when the problem allows it
+        const int64_t want = std::max<int64_t>(1, (B * C) / (2 * int64_t(dev->sm_count)));
+        const int CC = int(std::max<int64_t>(
+            1, std::min<int64_t>({C, pcn::STG_SMEM_FLOATS / M, want})));
+        const size_t smem = size_t(CC) * size_t(M) * sizeof(float);
+        cudaError_t e = cudaFuncSetAttribute(
+            pcn::three_interpolate_backward_staged_kernel,
+            cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e == cudaSuccess) {
+            const dim3 grid(unsigned((C + CC - 1) / CC), unsigned(B));
+            pcn::three_interpolate_backward_staged_kernel<<<grid, pcn::STG_THREADS,
+                                                            smem, st>>>(
+                grad_out, idx, weight, int(C), int(M), int(n), CC, grad_features,
+                dev->status_word);
+            e = cudaGetLastError();
+        }
+        return e == cudaSuccess ? PC_OK : cuda_err(e, "three_interpolate_backward");
+    }
     cudaError_t e = cudaMemsetAsync(grad_features, 0,
                                     size_t(B) * size_t(C) * size_t(M) * sizeof(float), st);
     if (e == cudaSuccess && n > 0) {

@@ -182,6 +182,8 @@ def test_three_interpolate_quickstart():
 @pytest.mark.parametrize("B,C,M,n,pad", [
     (1, 1, 3, 1, False), (2, 5, 11, 17, True), (3, 33, 100, 130, False),
     (16, 64, 1024, 4096, False), (2, 16, 7, 1000, True),
+    (1, 3, 20000, 500, True),   # M above the shared-memory tile: direct kernel
+    (2, 40, 16384, 300, False),  # largest staged tile, one channel per block
 ])
 def test_three_interpolate_forward_bit_exact(B, C, M, n, pad):
     f, idx, w = interp_case(40 + n, B, C, M, n, pad)
@@ -193,6 +195,8 @@ def test_three_interpolate_forward_bit_exact(B, C, M, n, pad):
 @pytest.mark.parametrize("B,C,M,n,pad", [
     (2, 5, 11, 17, True), (3, 33, 100, 130, False), (16, 32, 1024, 4096, False),
     (1, 3, 2, 2000, False),   # heavy collisions: 3000 terms per element
+    (1, 3, 20000, 500, True),  # M above the shared-memory tile: direct kernel
+    (2, 5, 300, 0, False),     # no points: the gradient is zero
 ])
 def test_three_interpolate_backward_within_bound(B, C, M, n, pad):
     f, idx, w = interp_case(50 + n, B, C, M, n, pad)
