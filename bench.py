@@ -371,13 +371,15 @@ def run_gpu(args):
                            if roof["bound"] == "alu" else
                            f"hbm_gbs of MEASURED_PEAKS.json ({peak_kind})")
 
-    grid = run_grid(args, pc, x, flush, device, world)
-    next_rows = run_next_rows(args, pc, flush, device, world,
-                              with_oracle=(rank == 0 and world == 1
-                                           and not args.no_cpu_baseline))
+    grid = next_rows = None
+    if not args.step_only:
+        grid = run_grid(args, pc, x, flush, device, world)
+        next_rows = run_next_rows(args, pc, flush, device, world,
+                                  with_oracle=(rank == 0 and world == 1
+                                               and not args.no_cpu_baseline))
 
     # end to end through the public API: pinned host in, pinned host out
-    e2e = run_e2e(args, pc, x_host, device, world)
+    e2e = None if args.step_only else run_e2e(args, pc, x_host, device, world)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -776,6 +778,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0,
                     help="seconds of oracle work for the cpu_baseline leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time only the FPS + kNN + Ball Query step (no grid, "
+                         "next-row or end-to-end sections; for profiler captures)")
     ap.add_argument("--serial", action="store_true",
                     help="run FPS, kNN and Ball Query one after another on one "
                          "stream instead of FPS concurrently on a side stream")
