@@ -130,3 +130,66 @@ def test_wait_timeout_setter_accepts_any_value(L):
     L.pc_set_wait_timeout_ns(0)
     L.pc_set_wait_timeout_ns(2_000_000_000)
     L.pc_debug_set_fps_grid_stall(0)
+
+
+def test_knn_ex_validation(L):
+    # k > N is allowed in the ex form (padded); k above 256 is unsupported
+    assert L.pc_knn_ex(None, 0, 4, None, 8, 300, None, None, 0, None, None, None) == 2
+    assert L.pc_knn_ex(FAKE, 1, 4, FAKE, 8, 0, None, None, 0, FAKE, FAKE, None) == 1
+    assert L.pc_knn_ex(FAKE, 1, 4, FAKE, 8, 2, None, None, 4, FAKE, FAKE, None) == 1
+    assert "unknown flags" in _msg(L)
+    assert L.pc_knn_ex(None, 0, 4, None, 3, 5, None, None, 1, None, None, None) == 0
+
+
+def test_ball_query_ex_validation(L):
+    assert L.pc_ball_query_ex(FAKE, 1, 1, FAKE, 4, None, None, -1.0, 2, FAKE, FAKE,
+                              None) == 1
+    assert L.pc_ball_query_ex(FAKE, 1, 1, FAKE, 4, None, None, 0.5, 0, FAKE, FAKE,
+                              None) == 1
+    assert L.pc_ball_query_ex(None, 2, 0, None, 4, None, None, 0.5, 3, None, None,
+                              None) == 0
+
+
+def test_chamfer_validation(L):
+    args = (FAKE, 1, 4, FAKE, 4, None, None, None)
+    outs = (FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert L.pc_chamfer(FAKE, -1, 4, FAKE, 4, None, None, None, 2, 2, 0, *outs) == 1
+    assert L.pc_chamfer(*args, 0, 2, 0, *outs) == 1     # point reduction NONE
+    assert "point_reduction" in _msg(L)
+    assert L.pc_chamfer(*args, 2, 7, 0, *outs) == 1     # unknown batch reduction
+    assert L.pc_chamfer(FAKE, 70000, 4, FAKE, 4, None, None, None, 2, 2, 0,
+                        *outs) == 2
+    # B = 0 without a reduced loss: nothing to do
+    assert L.pc_chamfer(None, 0, 4, None, 4, None, None, None, 2, 0, 0,
+                        None, None, None, None, None, None) == 0
+
+
+def test_interp_and_gather_validation(L):
+    assert L.pc_three_interpolate(FAKE, -1, 2, 3, FAKE, FAKE, 4, FAKE, None) == 1
+    assert L.pc_three_interpolate(FAKE, 70000, 2, 3, FAKE, FAKE, 4, FAKE, None) == 2
+    assert L.pc_three_interpolate(None, 0, 2, 3, None, None, 4, None, None) == 0
+    assert L.pc_three_interpolate_backward(FAKE, 1, 2, -4, FAKE, FAKE, 3, FAKE,
+                                           None) == 1
+    assert L.pc_three_interpolate_backward(None, 2, 0, 4, None, None, 3, None,
+                                           None) == 0
+    assert L.pc_gather_points(FAKE, 1, -1, FAKE, 2, 2, FAKE, None) == 1
+    assert L.pc_gather_points(None, 1, 5, None, 0, 3, None, None) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_new_entry_points_report_no_device(L):
+    assert L.pc_knn_ex(FAKE, 1, 4, FAKE, 8, 2, None, None, 0, FAKE, FAKE,
+                       None) == binding.PC_ERR_NO_DEVICE
+    assert L.pc_chamfer(FAKE, 1, 4, FAKE, 4, None, None, None, 2, 2, 0,
+                        FAKE, FAKE, FAKE, FAKE, FAKE, None) == binding.PC_ERR_NO_DEVICE
+    assert L.pc_three_interpolate(FAKE, 1, 2, 3, FAKE, FAKE, 4, FAKE,
+                                  None) == binding.PC_ERR_NO_DEVICE
+    assert L.pc_gather_points(FAKE, 1, 5, FAKE, 2, 2, FAKE,
+                              None) == binding.PC_ERR_NO_DEVICE
+
+
+def test_pytorch3d_adapter_rejects_cpu_tensors(L):
+    from point_cloud_neighbor_gb300.pytorch3d import ball_query
+    x = torch.zeros(1, 8, 3)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        ball_query(x, x, K=4, radius=0.5)
