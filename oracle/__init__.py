@@ -76,6 +76,10 @@ def _bind(lib):
                                             ctypes.c_double, I, P, I, P]
     lib.orc_s32_pairs.restype = None
     lib.orc_s32_pairs.argtypes = [P, P, I, P]
+    lib.orc_sd.restype = ctypes.c_float
+    lib.orc_sd.argtypes = [P, P, I]
+    lib.orc_knn_d_rows.restype = ctypes.c_int
+    lib.orc_knn_d_rows.argtypes = [P, I, I, P, I, I, I, ctypes.c_int, P, I, P, P]
     lib.orc_knn_masked_rows.restype = ctypes.c_int
     lib.orc_knn_masked_rows.argtypes = [P, I, I, P, I, I, P, P, ctypes.c_int,
                                         P, I, P, P]
@@ -503,3 +507,46 @@ def chamfer(x, y, x_lengths=None, y_lengths=None, weights=None,
     else:
         loss = np.float32(math.fsum(per) / B) if B > 0 else np.float32(0.0)
     return loss, (dx, ix), (None if single_directional else (dy, iy))
+
+
+def sd(a, b) -> np.float32:
+    """Dimension-by-dimension squared distance of two float32 vectors."""
+    a = np.ascontiguousarray(a, dtype=np.float32).reshape(-1)
+    b = np.ascontiguousarray(b, dtype=np.float32).reshape(-1)
+    return np.float32(_load().orc_sd(_ptr(a), _ptr(b), a.shape[0]))
+
+
+def knn_d(query, ref, k: int, squared: bool = False, rows=None, threads: int = 1):
+    """kNN of query [B,Q,D] against ref [B,N,D] with the dimension-by-dimension
+    distance (``orc_knn_d_rows``); returns (dist [R,k], idx [R,k])."""
+    query = np.ascontiguousarray(query, dtype=np.float32)
+    ref = np.ascontiguousarray(ref, dtype=np.float32)
+    B, Q, D = query.shape
+    N = ref.shape[1]
+    if ref.shape[2] != D:
+        raise ValueError("query and ref dimensions differ")
+    rows = _rows_arg(rows, B * Q)
+    R = rows.shape[0]
+    dist = np.empty((R, k), dtype=np.float32)
+    idx = np.empty((R, k), dtype=np.int64)
+    lib = _load()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        rr = np.ascontiguousarray(rows[lo:hi])
+        d = np.empty((hi - lo, k), dtype=np.float32)
+        i = np.empty((hi - lo, k), dtype=np.int64)
+        _check(lib.orc_knn_d_rows(_ptr(query), B, Q, _ptr(ref), N, D, k,
+                                  int(squared), _ptr(rr), hi - lo, _ptr(d),
+                                  _ptr(i)), "knn_d")
+        dist[lo:hi] = d
+        idx[lo:hi] = i
+
+    chunks = _split(R, threads)
+    if len(chunks) <= 1:
+        run(0, R)
+    else:
+        with ThreadPoolExecutor(len(chunks)) as ex:
+            list(ex.map(lambda c: run(*c), chunks))
+    return dist, idx

@@ -478,3 +478,56 @@ int orc_three_interpolate_backward(const float *g, int64_t B, int64_t C,
         }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------
+ * kNN in D dimensions (project page, "Roadmap", Phase 2: kNN in arbitrary
+ * dimension for feature-space neighbour search, with "direct
+ * dimension-by-dimension distance accumulation as the numerical baseline"):
+ *   s = fl(... fl(fl(t_0 + t_1) + t_2) ... + t_{D-1}),  t_d = fl(fl(q_d - x_d)^2),
+ * accumulated in increasing d, each operation a separately rounded float32
+ * operation (for D = 3 this is exactly s32).  Selection as "k nearest
+ * neighbors": the first k of the lexicographic (s, j) order; D = sqrt(s)
+ * or s itself when `squared` is set.  query [B, Q, D], ref [B, N, D].
+ * ---------------------------------------------------------------------- */
+float orc_sd(const float *a, const float *b, int64_t D)
+{
+    float s = 0.0f;
+    for (int64_t d = 0; d < D; ++d) {
+        float t = a[d] - b[d];
+        float t2 = t * t;
+        s = s + t2;
+    }
+    return s;
+}
+
+int orc_knn_d_rows(const float *query, int64_t B, int64_t Q, const float *ref,
+                   int64_t N, int64_t D, int64_t k, int squared,
+                   const int64_t *rows, int64_t nrows, float *out_dist,
+                   int64_t *out_idx)
+{
+    if (B < 0 || Q < 0 || N < 1 || D < 1 || k < 1 || k > N) return ORC_BAD_ARGUMENT;
+    orc_pair *cand = (orc_pair *)malloc((size_t)N * sizeof(orc_pair));
+    if (!cand) return ORC_NO_MEMORY;
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t row = rows[r];
+        if (row < 0 || row >= B * Q) {
+            free(cand);
+            return ORC_BAD_ARGUMENT;
+        }
+        int64_t b = row / Q;
+        const float *q = query + (size_t)row * (size_t)D;
+        const float *x = ref + (size_t)b * (size_t)N * (size_t)D;
+        for (int64_t j = 0; j < N; ++j) {
+            cand[j].s = orc_sd(q, x + (size_t)j * (size_t)D, D);
+            cand[j].j = j;
+        }
+        qsort(cand, (size_t)N, sizeof(orc_pair), orc_pair_cmp);
+        for (int64_t t = 0; t < k; ++t) {
+            float sd = cand[t].s;
+            out_dist[r * k + t] = squared ? sd : sqrtf(sd);
+            out_idx[r * k + t] = cand[t].j;
+        }
+    }
+    free(cand);
+    return ORC_OK;
+}

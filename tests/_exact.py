@@ -61,3 +61,14 @@ def s32_fma_variant(q, x) -> np.float32:
 def s_real(q, x) -> Fraction:
     """The real squared distance of the float32 inputs, exactly."""
     return sum((F(q[i]) - F(x[i])) ** 2 for i in range(3))
+
+
+def sd_exact(q, x) -> np.float32:
+    """Dimension-by-dimension sum of squared differences, accumulated in
+    increasing dimension, one binary32 rounding per operation."""
+    s = np.float32(0.0)
+    for i in range(len(q)):
+        t = round_f32(F(q[i]) - F(x[i]))
+        t2 = round_f32(F(t) * F(t))
+        s = round_f32(F(s) + F(t2))
+    return s

@@ -13,6 +13,7 @@ import os
 import pytest
 
 import test_oracle_ext_pins as ext
+import test_oracle_knn_d_pins as kd
 import test_oracle_pins as pins
 
 # (name, text to replace in pc_oracle.c, replacement)
@@ -58,6 +59,13 @@ MUTANTS = [
     ("interp_backward_drops_weight", "float p = w[(b * n + i) * 3 + t] * gi[i];",
      "float p = gi[i];"),
     ("interp_backward_overwrites", "gr[m] = gr[m] + p;", "gr[m] = p;"),
+    ("knn_d_reversed_dimensions", "for (int64_t d = 0; d < D; ++d) {\n        float t = a[d] - b[d];",
+     "for (int64_t d = D - 1; d >= 0; --d) {\n        float t = a[d] - b[d];"),
+    ("knn_d_fma", "float t2 = t * t;\n        s = s + t2;", "s = fmaf(t, t, s);"),
+    ("knn_d_drops_last_dimension", "for (int64_t d = 0; d < D; ++d) {\n        float t = a[d] - b[d];",
+     "for (int64_t d = 0; d + 1 < D; ++d) {\n        float t = a[d] - b[d];"),
+    ("knn_d_squared_ignored", "out_dist[r * k + t] = squared ? sd : sqrtf(sd);",
+     "out_dist[r * k + t] = sqrtf(sd);"),
 ]
 
 PIN_FUNCTIONS = [
@@ -88,6 +96,10 @@ PIN_FUNCTIONS = [
     (ext.test_three_interpolate_backward_exact_on_small_integers, {}),
     (ext.test_chamfer_brute_force_and_reductions, {}),
     (ext.test_chamfer_lengths_equal_sliced_clouds, {}),
+    (kd.test_distance_matches_exact_rounding_per_operation, {}),
+    (kd.test_order_of_accumulation_is_increasing_dimension, {}),
+    (kd.test_three_dimensions_equal_the_point_operator, {}),
+    (kd.test_selection_on_a_lattice_is_the_exact_lexsort, {}),
 ]
 
 
