@@ -425,6 +425,9 @@ def run_only(args):
         "grid_ball_query": lambda: pc.pc_ball_query_grid(x, g, W["bq_radius"],
                                                          W["bq_K"]),
     }
+    if args.only == "knn_d":
+        fx = torch.randn((32, 1024, 64), device=device)
+        calls["knn_d"] = lambda: pc.pc_knn_d(fx, fx, 20)
     if args.only in ("chamfer", "three_interpolate", "three_interpolate_backward"):
         cx = torch.from_numpy(inputs.random_cloud(5, 4, 16384)).to(device)
         cy = torch.from_numpy(inputs.random_cloud(6, 4, 16384)).to(device)
@@ -594,9 +597,33 @@ def run_next_rows(args, pc, flush, device, world, with_oracle):
         "workload": f"B={TB}, {TM} centers vs {TN} points, r=0.2, K=64, return_nn",
         "ms": bq_ms, "queries_per_s": TB * TM * world / (bq_ms / 1e3), "launches": 2}
 
+    # kNN in D dimensions at the DGCNN EdgeConv feature shape
+    DB, DN, DD, Dk = 32, 1024, 64, 20
+    fx_h = np.random.default_rng(9).standard_normal((DB, DN, DD)).astype(np.float32)
+    fx = torch.from_numpy(fx_h).to(device)
+    kd_ms = _timed(lambda: pc.pc_knn_d(fx, fx, Dk), steps, warm, flush, stream)
+    kd_flops = 3.0 * DD * DB * DN * DN
+    kd_tfl = kd_flops / (kd_ms / 1e3) / 1e12
+    out["knn_d"] = {
+        "workload": f"B={DB} clouds of {DN} points with {DD}-d features, k={Dk}, "
+                    "every point a query (DGCNN EdgeConv shape)",
+        "ms": kd_ms, "queries_per_s": DB * DN * world / (kd_ms / 1e3),
+        "algorithmic_flops": kd_flops,
+        "roofline": {"bound": "alu", "achieved": kd_tfl, "peak": alu,
+                     "unit": "TFLOP/s", "frac": kd_tfl / alu,
+                     "note": "3 flops (sub, mul, add) per dimension and pair"},
+        "launches": 1}
+
     if with_oracle:
         import oracle
         threads = os.cpu_count() or 1
+        krows = np.arange(0, DB * DN, DB * DN // (16 * threads), dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.knn_d(fx_h, fx_h, Dk, rows=krows, threads=threads)
+        t1 = time.perf_counter()
+        out["knn_d"]["oracle"] = {
+            "ms_extrapolated": (t1 - t0) / len(krows) * DB * DN * 1e3,
+            "cores": threads, "sample": f"{len(krows)} query rows, extrapolated"}
         rows = np.arange(0, CB * CP, CB * CP // (64 * threads), dtype=np.int64)
         t0 = time.perf_counter()
         oracle.knn_masked(cx_h, cy_h, 1, squared=True, rows=rows, threads=threads)
@@ -787,7 +814,7 @@ def main():
     ap.add_argument("--only", choices=["fps", "knn", "ball_query", "grid_build",
                                        "grid_knn", "grid_ball_query", "chamfer",
                                        "three_interpolate",
-                                       "three_interpolate_backward"],
+                                       "three_interpolate_backward", "knn_d"],
                     help="run one operator of the step W + K times and print "
                          "its mean CUDA-event time (for profiler captures)")
     args = ap.parse_args()

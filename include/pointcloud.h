@@ -262,6 +262,23 @@ int pc_ball_query_grid(const float *query, int64_t B, int64_t Q,
                        const void *grid, int64_t N, double radius, int64_t K,
                        float *out_dist2, int64_t *out_idx, void *stream);
 
+/*
+ * kNN in D dimensions (feature-space neighbour search).  Project page,
+ * "Roadmap", Phase 2: "direct dimension-by-dimension distance accumulation":
+ *   s = fl(... fl(fl(t_0 + t_1) + t_2) ... + t_{D-1}),  t_d = fl(fl(q_d - x_d)^2),
+ * accumulated in increasing d, every operation a separately rounded float32
+ * operation (D = 3 gives the s32 of pc_knn).  Selection as pc_knn: the first
+ * k of the (s, j) lexicographic order; distance sqrt(s), or s with
+ * PC_KNN_SQUARED.
+ *
+ *   query [B, Q, D], ref [B, N, D] float32, device.  1 <= k <= N, k <= 32,
+ *   1 <= D <= 256 (PC_ERR_UNSUPPORTED above).
+ *   out_dist [B, Q, k] float32, out_idx [B, Q, k] int64, device.
+ */
+int pc_knn_d(const float *query, int64_t B, int64_t Q, const float *ref,
+             int64_t N, int64_t D, int64_t k, int flags, float *out_dist,
+             int64_t *out_idx, void *stream);
+
 /* ------------------------------------------------------------------------
  * Chamfer distance, PointNet++ feature propagation, neighbor gather.
  * ---------------------------------------------------------------------- */

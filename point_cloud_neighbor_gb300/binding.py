@@ -67,6 +67,8 @@ _SIGNATURES = {
     "pc_three_interpolate_backward": (ctypes.c_int, [_P, _I, _I, _I, _P, _P, _I,
                                                      _P, _P]),
     "pc_gather_points": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _P, _P]),
+    "pc_knn_d": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _I, ctypes.c_int, _P, _P,
+                                _P]),
     "pc_device_status": (ctypes.c_int, [_P, ctypes.c_int,
                                         ctypes.POINTER(ctypes.c_int32)]),
     "pc_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
@@ -328,6 +330,32 @@ def pc_ball_query_grid(query: torch.Tensor, grid: PointGrid, radius: float,
                                   out_idx.data_ptr(), _stream_ptr(query.device))
     _raise_on(st, "pc_ball_query_grid")
     return out_dist2, out_idx
+
+
+def pc_knn_d(query: torch.Tensor, ref: torch.Tensor, k: int, *,
+             squared: bool = False, out_dist: torch.Tensor | None = None,
+             out_idx: torch.Tensor | None = None):
+    """kNN in D dimensions: query [B,Q,D], ref [B,N,D] float32 (CUDA) ->
+    (dist [B,Q,k], idx [B,Q,k]); dimension-by-dimension accumulation."""
+    for t, name in ((query, "query"), (ref, "ref")):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor; this library has no CPU path")
+        if t.dtype != torch.float32 or t.dim() != 3 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 tensor [B, n, D]")
+    B, Q, D = query.shape
+    if ref.shape[0] != B or ref.shape[2] != D or ref.device != query.device:
+        raise ValueError("query and ref must share batch size, dimension and device")
+    N = ref.shape[1]
+    with torch.cuda.device(query.device):
+        if out_dist is None:
+            out_dist = torch.empty((B, Q, k), dtype=torch.float32, device=query.device)
+        if out_idx is None:
+            out_idx = torch.empty((B, Q, k), dtype=torch.int64, device=query.device)
+        st = lib().pc_knn_d(query.data_ptr(), B, Q, ref.data_ptr(), N, D, k,
+                            PC_KNN_SQUARED if squared else 0, out_dist.data_ptr(),
+                            out_idx.data_ptr(), _stream_ptr(query.device))
+    _raise_on(st, "pc_knn_d")
+    return out_dist, out_idx
 
 
 _REDUCTIONS = {"none": PC_REDUCTION_NONE, None: PC_REDUCTION_NONE,

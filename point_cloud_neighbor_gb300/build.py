@@ -26,7 +26,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpointcloud.so")
 
 SOURCES = ["pc_api.cu", "pc_fps.cu", "pc_knn.cu", "pc_ball_query.cu",
-           "pc_fps_static.cu", "pc_grid.cu", "pc_chamfer.cu", "pc_interp.cu"]
+           "pc_fps_static.cu", "pc_grid.cu", "pc_chamfer.cu", "pc_interp.cu",
+           "pc_knn_d.cu"]
 HEADERS = ["pc_device.cuh", "pc_tiles.cuh", "pc_filter.cuh", "pc_stream.cuh",
            "pc_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
