@@ -572,8 +572,15 @@ __global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const Knn
         const int cnt = min(ST_T, Nb - j0);
         const float *raw = ring.raw_tile(st) + tile_float_offset(cref + size_t(j0) * 3);
         const int npairs = (cnt + 1) >> 1;
-        for (int p = 0; p < npairs; p += 4) {
-            bool pass = false;
+        // pass 1: filter the whole tile, remembering which 8-point steps let
+        // something through for which query (32 steps per tile)
+        unsigned pend[KL_QL];
+#pragma unroll
+        for (int q = 0; q < KL_QL; ++q) pend[q] = 0;
+        for (int p = 0, step = 0; p < npairs; p += 4, ++step) {
+            bool pass[KL_QL];
+#pragma unroll
+            for (int q = 0; q < KL_QL; ++q) pass[q] = false;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float4 A = ck[2 * (p + u)];
@@ -584,16 +591,25 @@ __global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const Knn
                                           make_float2(Z.z, Z.w));
                     v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
                     v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
-                    pass |= !(v.x > thr[q]) | !(v.y > thr[q]);
+                    pass[q] |= !(v.x > thr[q]) | !(v.y > thr[q]);
                 }
             }
-            if (!pass) continue;
 #pragma unroll
-            for (int q = 0; q < KL_QL; ++q) {
+            for (int q = 0; q < KL_QL; ++q) pend[q] |= (pass[q] ? 1u : 0u) << step;
+        }
+        // pass 2: the lanes with pending steps process them together (one
+        // step per lane per round), exact s32 and heap insertion; thresholds
+        // only tighten, so re-filtering with the current one is still safe
+#pragma unroll
+        for (int q = 0; q < KL_QL; ++q) {
+            if (!valid[q]) pend[q] = 0;
+            float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+            int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+            while (__any_sync(FULL, pend[q] != 0)) {
+                if (pend[q] == 0) continue;
+                const int p = 4 * (__ffs(pend[q]) - 1);
+                pend[q] &= pend[q] - 1;
                 unsigned m = stream_mask<4>(ck, p, ax[q], ay[q], az[q], thr[q]);
-                if (!valid[q]) m = 0;
-                float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
-                int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
                 while (m) {
                     const int i = 2 * p + __ffs(m) - 1;
                     m &= m - 1;
