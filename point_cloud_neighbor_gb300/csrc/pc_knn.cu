@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // and replaces the root by every point that beats it (sift-down).  At the end
 // each lane heap-sorts its k entries into ascending (s, j) order.
 // ---------------------------------------------------------------------------
-constexpr int KL_QL = 1;                        // queries per lane (1: measured best)
+constexpr int KL_QL = 2;                        // queries per lane (2: measured best)
 constexpr int KL_CWARPS = 8 / KL_QL;            // consumer warps per block
 constexpr int KL_QPB = KL_CWARPS * 32 * KL_QL;  // queries per block
 constexpr int KL_THREADS = 32 * (KL_CWARPS + 1);
