@@ -48,16 +48,17 @@ __device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
     return __ffma2_rn(a, b, c);
 }
 
-// The filter of one query against a lane's 8 points (4 packed pairs):
+// The filter of one query against a lane's 2P points (P packed pairs):
 // bit r of the result is set when point r may satisfy the selection bound.
-__device__ __forceinline__ unsigned filter_mask8(const float2 (&x)[4],
-                                                 const float2 (&y)[4],
-                                                 const float2 (&z)[4],
-                                                 const float2 (&w)[4],
-                                                 float4 axy, float4 azt) {
+template <int P>
+__device__ __forceinline__ unsigned filter_mask(const float2 (&x)[P],
+                                                const float2 (&y)[P],
+                                                const float2 (&z)[P],
+                                                const float2 (&w)[P],
+                                                float4 axy, float4 azt) {
     unsigned m = 0;
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < P; ++p) {
         float2 v = fma2_rn(x[p], make_float2(axy.x, axy.y), w[p]);
         v = fma2_rn(y[p], make_float2(axy.z, axy.w), v);
         v = fma2_rn(z[p], make_float2(azt.x, azt.y), v);
@@ -67,21 +68,38 @@ __device__ __forceinline__ unsigned filter_mask8(const float2 (&x)[4],
     return m;
 }
 
-// Any point of the lane's 8 passing the filter (the hot-loop form).
-__device__ __forceinline__ bool filter_any8(const float2 (&x)[4],
-                                            const float2 (&y)[4],
-                                            const float2 (&z)[4],
-                                            const float2 (&w)[4], float4 axy,
-                                            float4 azt) {
+// Any of the lane's 2P points passing the filter (the hot-loop form).
+template <int P>
+__device__ __forceinline__ bool filter_any(const float2 (&x)[P],
+                                           const float2 (&y)[P],
+                                           const float2 (&z)[P],
+                                           const float2 (&w)[P], float4 axy,
+                                           float4 azt) {
     bool t = false;
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < P; ++p) {
         float2 v = fma2_rn(x[p], make_float2(axy.x, axy.y), w[p]);
         v = fma2_rn(y[p], make_float2(axy.z, axy.w), v);
         v = fma2_rn(z[p], make_float2(azt.x, azt.y), v);
         t |= !(v.x > azt.z) | !(v.y > azt.z);
     }
     return t;
+}
+
+__device__ __forceinline__ unsigned filter_mask8(const float2 (&x)[4],
+                                                 const float2 (&y)[4],
+                                                 const float2 (&z)[4],
+                                                 const float2 (&w)[4],
+                                                 float4 axy, float4 azt) {
+    return filter_mask<4>(x, y, z, w, axy, azt);
+}
+
+__device__ __forceinline__ bool filter_any8(const float2 (&x)[4],
+                                            const float2 (&y)[4],
+                                            const float2 (&z)[4],
+                                            const float2 (&w)[4], float4 axy,
+                                            float4 azt) {
+    return filter_any<4>(x, y, z, w, axy, azt);
 }
 
 struct FilterFrame {
