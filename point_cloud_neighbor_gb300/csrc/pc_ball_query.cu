@@ -41,10 +41,9 @@
 namespace pcn {
 namespace {
 
-constexpr int BQ_R = 16;  // points per lane per tile (one vote per query covers 512)
+constexpr int BQ_R = 8;
 constexpr int BQ_T = 32 * BQ_R;
-constexpr int BQ_CWARPS = 4;
-constexpr int BQ_MINB = 3;  // blocks per SM
+constexpr int BQ_CWARPS = 8;
 constexpr int BQ_THREADS = 32 * (BQ_CWARPS + 1);
 constexpr int BQ_STAGES = 4;
 constexpr unsigned FULL = 0xffffffffu;
@@ -99,7 +98,7 @@ __device__ __forceinline__ int bq_record(const float *tile,
                                          int K, size_t row, float *out_dist2,
                                          int64_t *out_idx) {
     const int lane = static_cast<int>(lane_id());
-    const unsigned pm = filter_mask<BQ_R / 2>(rx, ry, rz, rw, axy, azt);
+    const unsigned pm = filter_mask8(rx, ry, rz, rw, axy, azt);
 #pragma unroll
     for (int r = 0; r < BQ_R; ++r) {
         float s = 0.f;
@@ -123,7 +122,7 @@ __device__ __forceinline__ int bq_record(const float *tile,
     return min(hits, K);
 }
 
-__global__ void __launch_bounds__(BQ_THREADS, BQ_MINB) bq_kernel(const BqArgs a) {
+__global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -258,8 +257,8 @@ __global__ void __launch_bounds__(BQ_THREADS, BQ_MINB) bq_kernel(const BqArgs a)
                 BqSlot *s0 = slots + g;
                 const float4 axy0 = s0[0].axy, azt0 = s0[0].azt;
                 const float4 axy1 = s0[1].axy, azt1 = s0[1].azt;
-                const bool t0 = filter_any<BQ_R / 2>(rx, ry, rz, rw, axy0, azt0);
-                const bool t1 = filter_any<BQ_R / 2>(rx, ry, rz, rw, axy1, azt1);
+                const bool t0 = filter_any8(rx, ry, rz, rw, axy0, azt0);
+                const bool t1 = filter_any8(rx, ry, rz, rw, axy1, azt1);
                 const bool v0 = __any_sync(FULL, t0), v1 = __any_sync(FULL, t1);
                 if (v0) record(s0, axy0, azt0);
                 if (v1) record(s0 + 1, axy1, azt1);
@@ -267,7 +266,7 @@ __global__ void __launch_bounds__(BQ_THREADS, BQ_MINB) bq_kernel(const BqArgs a)
             if (g < active) {
                 BqSlot *s0 = slots + g;
                 const float4 axy = s0->axy, azt = s0->azt;
-                if (__any_sync(FULL, filter_any<BQ_R / 2>(rx, ry, rz, rw, axy, azt)))
+                if (__any_sync(FULL, filter_any8(rx, ry, rz, rw, axy, azt)))
                     record(s0, axy, azt);
             }
             if (any_full) {  // rare: move full queries behind the active ones
@@ -347,11 +346,11 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
 
-    const int slots = dev.sm_count * BQ_MINB;
+    const int slots = dev.sm_count * 2;
     const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));
     int64_t G = (Q + BQ_CWARPS * bpc_target - 1) / (BQ_CWARPS * bpc_target);
     const size_t budget =
-        std::min<size_t>(dev.smem_per_block_optin, dev.smem_per_sm / BQ_MINB - 2048);
+        std::min<size_t>(dev.smem_per_block_optin, dev.smem_per_sm / 2 - 2048);
     const int64_t gmax = std::max<int64_t>(
         1, int64_t((budget - bq_fixed_smem()) / (BQ_CWARPS * sizeof(BqSlot))));
     G = std::max<int64_t>(1, std::min(G, gmax));
