@@ -193,8 +193,8 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
         }
         const float xp = __fsub_rn(x, fr.cx), yp = __fsub_rn(y, fr.cy),
                     zp = __fsub_rn(z, fr.cz);
-        const float ax = -2.0f * xp, ay = -2.0f * yp, az = -2.0f * zp;
-        const float thr = filter_threshold(a.R2, filter_norm2(xp, yp, zp));
+        float ax, ay, az;
+        const float thr = filter_threshold(a.R2, filter_query(xp, yp, zp, ax, ay, az));
         slots[g].axy = make_float4(ax, ax, ay, ay);
         slots[g].azt = make_float4(az, az, thr, __int_as_float(g));
         slots[g].raw = make_float4(x, y, z, __int_as_float(0));
@@ -230,15 +230,15 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             for (int p = 0; p < BQ_R / 2; ++p) {
                 const float *p0 = buf + 3 * (lane + 32 * (2 * p));
                 const float *p1 = buf + 3 * (lane + 32 * (2 * p + 1));
-                const float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
-                            z0 = __fsub_rn(p0[2], fr.cz);
-                const float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
-                            z1 = __fsub_rn(p1[2], fr.cz);
+                float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
+                      z0 = __fsub_rn(p0[2], fr.cz);
+                float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
+                      z1 = __fsub_rn(p1[2], fr.cz);
+                const float w0 = filter_ref(x0, y0, z0), w1 = filter_ref(x1, y1, z1);
                 rx[p] = make_float2(x0, x1);
                 ry[p] = make_float2(y0, y1);
                 rz[p] = make_float2(z0, z1);
-                rw[p] = make_float2(filter_ref_w(x0, y0, z0),
-                                    filter_ref_w(x1, y1, z1));
+                rw[p] = make_float2(w0, w1);
             }
 
             bool any_full = false;

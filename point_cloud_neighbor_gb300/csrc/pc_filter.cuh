@@ -9,7 +9,7 @@
 //     t' = fma(az, z', fma(ay, y', fma(ax, x', w')))        3 FMAs
 // with coordinates centred on a point c of the cloud, x' = fl(x - c),
 // q' = fl(q - c), a = -2 q' (exact), w' = fl(|x'|^2 (1 - 2^-17)) per
-// reference, and let a pair through when NOT (t' > thr), where
+// reference, and let a pair through when t' <= thr, where
 //     thr = fl(fl(tau (1 + 2^-20)) - fl(qq (1 - 2^-19))) + 2^-120,
 //     qq = |q'|^2 (float FMA chain).
 // Every pair that passes is re-evaluated with the exact s32 from the raw
@@ -30,10 +30,13 @@
 //  * The float evaluation of thr is at least tau (1 + 13.9u)
 //    - qq (1 - 29.9u) before the 2^-120 term, which covers the absolute
 //    terms; so t' <= thr whenever s32 <= tau.
-//  * Overflow: a reference with w > 1e30 gets w' = -inf and a query with
-//    qq > 1e30 (or tau = inf) gets thr = +inf, so both always pass; below
-//    those bounds |x'|, |q'| <= 1e15 and no FMA overflows.  A NaN t' passes
-//    as well (the test is NOT(t' > thr)).
+//  * Overflow and NaN: a reference with w > 1e30 gets x' = y' = z' = 0 and
+//    w' = -inf (t' = -inf, always passes); a query with qq > 1e30 gets a = 0
+//    and thr = +inf (t' = w' <= +inf, always passes); below those bounds
+//    |x'|, |q'| <= 1e15 and no product or sum overflows, so t' is never NaN
+//    for finite coordinates and the ordered compare t' <= thr (or a running
+//    minimum compared once) is exact.  A NaN coordinate gives a NaN exact
+//    s32, which no selection rule accepts.
 // The centre only affects how tight the filter is (the slack grows with
 // |x'|^2 + |q'|^2): each consumer warp uses the centre of the bounding box
 // of the cloud's first (up to) 256 points.
@@ -62,28 +65,29 @@ __device__ __forceinline__ unsigned filter_mask(const float2 (&x)[P],
         float2 v = fma2_rn(x[p], make_float2(axy.x, axy.y), w[p]);
         v = fma2_rn(y[p], make_float2(axy.z, axy.w), v);
         v = fma2_rn(z[p], make_float2(azt.x, azt.y), v);
-        m |= (!(v.x > azt.z) ? 1u : 0u) << (2 * p);
-        m |= (!(v.y > azt.z) ? 1u : 0u) << (2 * p + 1);
+        m |= (v.x <= azt.z ? 1u : 0u) << (2 * p);
+        m |= (v.y <= azt.z ? 1u : 0u) << (2 * p + 1);
     }
     return m;
 }
 
-// Any of the lane's 2P points passing the filter (the hot-loop form).
+// Any of the lane's 2P points passing the filter (the hot-loop form: a
+// running minimum, compared once).
 template <int P>
 __device__ __forceinline__ bool filter_any(const float2 (&x)[P],
                                            const float2 (&y)[P],
                                            const float2 (&z)[P],
                                            const float2 (&w)[P], float4 axy,
                                            float4 azt) {
-    bool t = false;
+    float m = __int_as_float(0x7f800000);
 #pragma unroll
     for (int p = 0; p < P; ++p) {
         float2 v = fma2_rn(x[p], make_float2(axy.x, axy.y), w[p]);
         v = fma2_rn(y[p], make_float2(axy.z, axy.w), v);
         v = fma2_rn(z[p], make_float2(azt.x, azt.y), v);
-        t |= !(v.x > azt.z) | !(v.y > azt.z);
+        m = fminf(m, fminf(v.x, v.y));
     }
-    return t;
+    return m <= azt.z;
 }
 
 __device__ __forceinline__ unsigned filter_mask8(const float2 (&x)[4],
@@ -149,10 +153,25 @@ __device__ __forceinline__ float filter_norm2(float x, float y, float z) {
     return __fmaf_rn(z, z, __fmaf_rn(y, y, __fmul_rn(x, x)));
 }
 
-// w' of a centred reference: |x'|^2 (1 - 2^-17), or -inf beyond 1e30.
-__device__ __forceinline__ float filter_ref_w(float xp, float yp, float zp) {
+// A centred reference for the filter: w' = |x'|^2 (1 - 2^-17); beyond 1e30
+// the coordinates become 0 and w' = -inf (the point always passes).
+__device__ __forceinline__ float filter_ref(float &xp, float &yp, float &zp) {
     const float w = filter_norm2(xp, yp, zp);
-    return w <= 1e30f ? __fmul_rn(w, 1.0f - 0x1p-17f) : -__int_as_float(0x7f800000);
+    if (w <= 1e30f) return __fmul_rn(w, 1.0f - 0x1p-17f);
+    xp = yp = zp = 0.0f;
+    return -__int_as_float(0x7f800000);
+}
+
+// The query side: a = -2 q' per axis (0 when |q'|^2 > 1e30, where the
+// threshold is +inf) and qq = |q'|^2.
+__device__ __forceinline__ float filter_query(float xp, float yp, float zp,
+                                              float &ax, float &ay, float &az) {
+    const float qq = filter_norm2(xp, yp, zp);
+    const bool big = !(qq <= 1e30f);
+    ax = big ? 0.0f : -2.0f * xp;
+    ay = big ? 0.0f : -2.0f * yp;
+    az = big ? 0.0f : -2.0f * zp;
+    return qq;
 }
 
 // The pass threshold for a query with qq = |q'|^2 and selection bound tau.

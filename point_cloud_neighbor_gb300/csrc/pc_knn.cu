@@ -322,10 +322,11 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         }
         const float xp = __fsub_rn(x, fr.cx), yp = __fsub_rn(y, fr.cy),
                     zp = __fsub_rn(z, fr.cz);
-        const float ax = -2.0f * xp, ay = -2.0f * yp, az = -2.0f * zp;
+        float ax, ay, az;
+        const float qq = filter_query(xp, yp, zp, ax, ay, az);
         slots[g].axy = make_float4(ax, ax, ay, ay);
         slots[g].azt = make_float4(az, az, inf, inf);
-        slots[g].raw = make_float4(x, y, z, filter_norm2(xp, yp, zp));
+        slots[g].raw = make_float4(x, y, z, qq);
         slots[g].kth = make_float4(inf, __int_as_float(INT_MAX), 0.f, 0.f);
     }
     for (int e = lane; e < G * k; e += 32) {
@@ -354,14 +355,15 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
         for (int p = 0; p < KNN_R / 2; ++p) {
             const float *p0 = buf + 3 * (lane + 32 * (2 * p));
             const float *p1 = buf + 3 * (lane + 32 * (2 * p + 1));
-            const float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
-                        z0 = __fsub_rn(p0[2], fr.cz);
-            const float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
-                        z1 = __fsub_rn(p1[2], fr.cz);
+            float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
+                  z0 = __fsub_rn(p0[2], fr.cz);
+            float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
+                  z1 = __fsub_rn(p1[2], fr.cz);
+            const float w0 = filter_ref(x0, y0, z0), w1 = filter_ref(x1, y1, z1);
             rx[p] = make_float2(x0, x1);
             ry[p] = make_float2(y0, y1);
             rz[p] = make_float2(z0, z1);
-            rw[p] = make_float2(filter_ref_w(x0, y0, z0), filter_ref_w(x1, y1, z1));
+            rw[p] = make_float2(w0, w1);
         }
 
         // two queries per step: independent filter chains for the scheduler
@@ -543,10 +545,11 @@ __global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const Knn
         }
         const float xp = __fsub_rn(qx[q], fr.cx), yp = __fsub_rn(qy[q], fr.cy),
                     zp = __fsub_rn(qz[q], fr.cz);
-        ax[q] = make_float2(-2.0f * xp, -2.0f * xp);
-        ay[q] = make_float2(-2.0f * yp, -2.0f * yp);
-        az[q] = make_float2(-2.0f * zp, -2.0f * zp);
-        qq[q] = filter_norm2(xp, yp, zp);
+        float axs, ays, azs;
+        qq[q] = filter_query(xp, yp, zp, axs, ays, azs);
+        ax[q] = make_float2(axs, axs);
+        ay[q] = make_float2(ays, ays);
+        az[q] = make_float2(azs, azs);
         ts[q] = inf;      // heap root: the k-th best so far
         tj[q] = INT_MAX;
         thr[q] = valid[q] ? inf : -inf;
@@ -578,9 +581,9 @@ __global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const Knn
 #pragma unroll
         for (int q = 0; q < KL_QL; ++q) pend[q] = 0;
         for (int p = 0, step = 0; p < npairs; p += 4, ++step) {
-            bool pass[KL_QL];
+            float mn[KL_QL];  // running minimum of t' per query
 #pragma unroll
-            for (int q = 0; q < KL_QL; ++q) pass[q] = false;
+            for (int q = 0; q < KL_QL; ++q) mn[q] = inf;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float4 A = ck[2 * (p + u)];
@@ -591,11 +594,11 @@ __global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const Knn
                                           make_float2(Z.z, Z.w));
                     v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
                     v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
-                    pass[q] |= !(v.x > thr[q]) | !(v.y > thr[q]);
+                    mn[q] = fminf(mn[q], fminf(v.x, v.y));
                 }
             }
 #pragma unroll
-            for (int q = 0; q < KL_QL; ++q) pend[q] |= (pass[q] ? 1u : 0u) << step;
+            for (int q = 0; q < KL_QL; ++q) pend[q] |= (mn[q] <= thr[q] ? 1u : 0u) << step;
         }
         // pass 2: the lanes with pending steps process them together (one
         // step per lane per round), exact s32 and heap insertion; thresholds

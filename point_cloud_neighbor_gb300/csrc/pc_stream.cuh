@@ -12,7 +12,8 @@
 //          cooked[2p]     = (x'_2p, x'_2p+1, y'_2p, y'_2p+1)
 //          cooked[2p + 1] = (z'_2p, z'_2p+1, w'_2p, w'_2p+1)
 //      points past the tile's end get (0, 0, 0, +inf): they pass the filter
-//      only against an infinite threshold and are masked exactly;
+//      only against an infinite threshold and are masked exactly (t' = +inf
+//      there; every other t' is finite or -inf, see pc_filter.cuh);
 //   3. all 32 producer lanes arrive on the stage's `ready` barrier.
 // Consumers wait on `ready`, read the cooked tile (every lane reads the same
 // 16 bytes: shared-memory broadcasts) and, on their rare slow paths, the raw
@@ -143,13 +144,13 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
             for (int h = 0; h < 2; ++h) {
                 const int i = 2 * p + h;
                 if (i < cnt) {
-                    const float xp = __fsub_rn(src[3 * i], fr.cx);
-                    const float yp = __fsub_rn(src[3 * i + 1], fr.cy);
-                    const float zp = __fsub_rn(src[3 * i + 2], fr.cz);
+                    float xp = __fsub_rn(src[3 * i], fr.cx);
+                    float yp = __fsub_rn(src[3 * i + 1], fr.cy);
+                    float zp = __fsub_rn(src[3 * i + 2], fr.cz);
+                    c[h][3] = filter_ref(xp, yp, zp);
                     c[h][0] = xp;
                     c[h][1] = yp;
                     c[h][2] = zp;
-                    c[h][3] = filter_ref_w(xp, yp, zp);
                 } else {
                     c[h][0] = c[h][1] = c[h][2] = 0.f;
                     c[h][3] = inf;
@@ -180,8 +181,8 @@ __device__ __forceinline__ unsigned stream_mask(const float4 *ck, int p, float2 
         float2 v = __ffma2_rn(make_float2(A.x, A.y), ax, make_float2(Z.z, Z.w));
         v = __ffma2_rn(make_float2(A.z, A.w), ay, v);
         v = __ffma2_rn(make_float2(Z.x, Z.y), az, v);
-        m |= (!(v.x > thr) ? 1u : 0u) << (2 * u);
-        m |= (!(v.y > thr) ? 1u : 0u) << (2 * u + 1);
+        m |= (v.x <= thr ? 1u : 0u) << (2 * u);
+        m |= (v.y <= thr ? 1u : 0u) << (2 * u + 1);
     }
     return m;
 }
@@ -190,7 +191,7 @@ __device__ __forceinline__ unsigned stream_mask(const float4 *ck, int p, float2 
 template <int V>
 __device__ __forceinline__ bool stream_any(const float4 *ck, int p, float2 ax,
                                            float2 ay, float2 az, float thr) {
-    bool t = false;
+    float m = __int_as_float(0x7f800000);
 #pragma unroll
     for (int u = 0; u < V; ++u) {
         const float4 A = ck[2 * (p + u)];
@@ -198,9 +199,9 @@ __device__ __forceinline__ bool stream_any(const float4 *ck, int p, float2 ax,
         float2 v = __ffma2_rn(make_float2(A.x, A.y), ax, make_float2(Z.z, Z.w));
         v = __ffma2_rn(make_float2(A.z, A.w), ay, v);
         v = __ffma2_rn(make_float2(Z.x, Z.y), az, v);
-        t |= !(v.x > thr) | !(v.y > thr);
+        m = fminf(m, fminf(v.x, v.y));
     }
-    return t;
+    return m <= thr;
 }
 
 }  // namespace pcn
