@@ -597,6 +597,28 @@ def run_next_rows(args, pc, flush, device, world, with_oracle):
         "workload": f"B={TB}, {TM} centers vs {TN} points, r=0.2, K=64, return_nn",
         "ms": bq_ms, "queries_per_s": TB * TM * world / (bq_ms / 1e3), "launches": 2}
 
+    # FPS at 1M points (workload 5: 16384 samples), the cooperative-grid
+    # schedule (too large for one cluster)
+    vx_h = inputs.very_large()
+    vx = torch.from_numpy(vx_h).to(device)
+    fps_out_v = torch.empty((1, 16384), dtype=torch.int64, device=device)
+    ws_v = torch.empty(max(pc.binding.lib().pc_fps_workspace_bytes(1, vx_h.shape[1], 16384),
+                           256), dtype=torch.uint8, device=device)
+    fv_ms = _timed(lambda: pc.pc_fps(vx, 16384, 0, out=fps_out_v, workspace=ws_v),
+                   max(3, min(steps, 5)), 3, flush, stream)
+    fv_bytes = float(vx_h.shape[1]) * 16383 * FPS_BYTES_PER_POINT_STEP
+    out["fps_1m"] = {
+        "workload": "N=1,000,000 uniform in [0,1)^3 with 1% duplicates, 16384 samples",
+        "ms": fv_ms, "us_per_sample": fv_ms * 1e3 / 16383,
+        "samples_per_s": 16384 * world / (fv_ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": fv_bytes / (fv_ms / 1e3) / 1e9,
+                     "peak": hbm, "unit": "GB/s",
+                     "frac": fv_bytes / (fv_ms / 1e3) / 1e9 / hbm,
+                     "note": "20 B per point-step if streamed; the kernel keeps "
+                             "points and minima on chip"},
+        "launches": 1}
+    del vx, ws_v
+
     # kNN in D dimensions at the DGCNN EdgeConv feature shape
     DB, DN, DD, Dk = 32, 1024, 64, 20
     fx_h = np.random.default_rng(9).standard_normal((DB, DN, DD)).astype(np.float32)
