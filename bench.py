@@ -180,18 +180,25 @@ def fp32_alu_peak_tflops(sm_count: int, mhz: float) -> float:
     return sm_count * 128 * 2 * mhz * 1e6 / 1e12
 
 
-def kernel_source_hash(name: str) -> str:
-    src = os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc", name)
+# The sources each operator's kernel is compiled from (its .cu file and the
+# headers it includes); a recorded DRAM figure is used only while they are
+# unchanged.
+KERNEL_SOURCES = {
+    "knn": ["pc_knn.cu", "pc_device.cuh", "pc_filter.cuh", "pc_stream.cuh",
+            "pc_tiles.cuh"],
+    "ball_query": ["pc_ball_query.cu", "pc_device.cuh", "pc_filter.cuh",
+                   "pc_tiles.cuh"],
+    "fps": ["pc_fps.cu", "pc_device.cuh"],
+    "grid_knn": ["pc_grid.cu", "pc_device.cuh"],
+    "grid_ball_query": ["pc_grid.cu", "pc_device.cuh"],
+}
+
+
+def kernel_source_hash(op: str) -> str:
     h = hashlib.sha256()
-    for f in (src, os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
-                                "pc_device.cuh"),
-              os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
-                           "pc_tiles.cuh"),
-              os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
-                           "pc_filter.cuh"),
-              os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc",
-                           "pc_stream.cuh")):
-        with open(f, "rb") as fh:
+    for name in KERNEL_SOURCES[op]:
+        with open(os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc", name),
+                  "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -202,9 +209,7 @@ def recorded_traffic(op: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {"knn": "pc_knn.cu", "ball_query": "pc_ball_query.cu",
-           "fps": "pc_fps.cu"}[op]
-    want = kernel_source_hash(src)
+    want = kernel_source_hash(op)
     for line in open(path):
         kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
         if kv.get("op") == op and kv.get("src_sha256") == want:
