@@ -485,3 +485,24 @@ def test_fps_grid_wait_timeout_is_reported():
     # the context is still usable and the next call is correct
     idx = gpu_fps(x, 20, 0, strategy=pc.PC_FPS_GRID, blocks_per_cloud=4)
     assert_idx_equal(idx, oracle.fps(x, 20, 0), "fps after timeout")
+
+
+def test_concurrent_streams_equal_serial():
+    """FPS, kNN and Ball Query issued on three streams at once (the benchmark
+    step) give exactly the results of the same calls one after another."""
+    x = to_dev(inputs.large())
+    serial = (pc.pc_fps(x, 256, 0), *pc.pc_knn(x, x, 16), *pc.pc_ball_query(x, x, 0.02, 32))
+    torch.cuda.synchronize()
+    main = torch.cuda.current_stream()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(main)
+    s2.wait_stream(main)
+    f = pc.pc_fps(x, 256, 0)
+    with torch.cuda.stream(s1):
+        kd, ki = pc.pc_knn(x, x, 16)
+    with torch.cuda.stream(s2):
+        bd, bi = pc.pc_ball_query(x, x, 0.02, 32)
+    torch.cuda.synchronize()
+    for a, b in zip(serial, (f, kd, ki, bd, bi)):
+        assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                           b.view(torch.int32) if b.dtype == torch.float32 else b)
