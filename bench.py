@@ -259,13 +259,10 @@ def run_gpu(args):
     # side stream after the same start point) occupy the rest of the GPU
     # (--serial: everything on one stream).
     side = torch.cuda.Stream(device) if not args.serial else stream
-    side2 = torch.cuda.Stream(device) if not args.serial else stream
     fork = torch.cuda.Event()
 
     def step(ev=None):
-        # ev: [start, fps_end, knn_start, knn_end, bq_start, bq_end, step_end]
-        # FPS on the main stream, kNN and Ball Query on two side streams (Ball
-        # Query blocks fill the SMs that kNN's last blocks leave idle)
+        # ev: [start, fps_end, knn_start (side), knn_end, bq_end, step_end]
         if ev is not None:
             ev[0].record(stream)
         fork.record(stream)
@@ -279,17 +276,12 @@ def run_gpu(args):
             pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
             if ev is not None:
                 ev[3].record(side)
-        side2.wait_event(fork)
-        with torch.cuda.stream(side2):
-            if ev is not None:
-                ev[4].record(side2)
             pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
             if ev is not None:
-                ev[5].record(side2)
+                ev[4].record(side)
         stream.wait_stream(side)
-        stream.wait_stream(side2)
         if ev is not None:
-            ev[6].record(stream)
+            ev[5].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -297,7 +289,7 @@ def run_gpu(args):
     torch.cuda.synchronize(device)
     assert pc.pc_device_status(reset=True, device=device) == 0
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)]
               for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize(device)
@@ -314,8 +306,8 @@ def run_gpu(args):
     # each operator timed on the stream it runs on
     t_fps = [e[0].elapsed_time(e[1]) for e in events]
     t_knn = [e[2].elapsed_time(e[3]) for e in events]
-    t_bq = [e[4].elapsed_time(e[5]) for e in events]
-    total_ms = sum(e[0].elapsed_time(e[6]) for e in events)
+    t_bq = [e[3].elapsed_time(e[4]) for e in events]
+    total_ms = sum(e[0].elapsed_time(e[5]) for e in events)
     total_ms, fps_ms, knn_ms, bq_ms = max_over_ranks(
         [total_ms, sum(t_fps), sum(t_knn), sum(t_bq)], world, device)
     ms_per_step = total_ms / args.steps
@@ -401,7 +393,7 @@ def run_gpu(args):
         "dtype": "f32", "data": "synthetic",
         "config": workload_config({"parallelism": f"replicas x{world}",
                                    "streams": ("1 (serial)" if args.serial else
-                                               "3: FPS, kNN and Ball Query concurrent")}),
+                                               "2: FPS concurrent with kNN then Ball Query")}),
         "roofline": roof, "ops": ops, "grid": grid, "next_rows": next_rows,
         "e2e": e2e,
         "gpu_launches": launches,
