@@ -8,10 +8,15 @@
 //   grad_f[b,c,m] += w[b,i,t] g[b,c,i]  for every idx[b,i,t] = m.
 // Forward: float32, products and sums rounded separately in the order
 // ((w0 f0 + w1 f1) + w2 f2), so the result is bit-identical to the oracle's.
-// Backward: float32 atomic adds (reduction order unspecified, as the pages
-// allow for accumulated gradients).  idx = -1 is padding (reads 0, adds
-// nothing); any other index outside [0, M) sets PC_ERR_INVALID_ARGUMENT in
-// the device status word and is treated as padding.
+// Backward (M <= 16384): deterministic and bit-exact with the oracle -- each
+// grad_f[b, c, m] is summed from 0 in increasing (i, t) order, each product
+// and addition rounded.  Per cloud a CSR of the entries (i, t) of every m,
+// in increasing entry order, is built once (count, scan, stable fill), then
+// one thread per (b, c, m) sums its list.  Larger M: float32 atomic adds
+// (order unspecified, as the pages allow for accumulated gradients).
+// idx = -1 is padding (reads 0, adds nothing); any other index outside
+// [0, M) sets PC_ERR_INVALID_ARGUMENT in the device status word and is
+// treated as padding.
 //
 // Staged kernels (used when a chunk of channels of one cloud fits in shared
 // memory, M <= 16384): a block owns (cloud b, channels c0 .. c0 + CC):
@@ -19,12 +24,8 @@
 //               a range of points i reads the three (index, weight) pairs once
 //               and writes out[b, c, i] for its CC channels (coalesced along
 //               i), gathering from shared memory;
-//   backward -- accumulates grad_f[b, c0.., :] in shared memory over all n
-//               points (shared-memory atomic adds of w * grad_out, grad_out
-//               read coalesced along i), then writes the block out once: no
-//               memset and no global atomics.
-// Otherwise the direct kernels gather from global memory (L2) with one thread
-// per point and global atomic adds for the backward.
+// Otherwise the direct kernel gathers from global memory (L2) with one thread
+// per point.
 //
 // gather_points (project page, "PyTorch3D-style Ball Query": return_nn gives
 // the neighbor coordinates, zeros where idx = -1):
@@ -144,33 +145,109 @@ three_interpolate_staged_kernel(const float *__restrict__ f,
     }
 }
 
-__global__ void __launch_bounds__(STG_THREADS)
-three_interpolate_backward_staged_kernel(const float *__restrict__ g,
-                                         const int64_t *__restrict__ idx,
-                                         const float *__restrict__ w, int C,
-                                         int M, int n, int CC,
-                                         float *__restrict__ grad_f, int *status) {
-    extern __shared__ float tile[];  // [CC][M]
-    const int b = blockIdx.y;
-    const int c0 = blockIdx.x * CC;
-    const int cc = min(CC, C - c0);
-    for (int e = threadIdx.x; e < cc * M; e += STG_THREADS) tile[e] = 0.0f;
+// --- deterministic backward: per-cloud CSR, then ordered sums ---------------
+constexpr int CSR_THREADS = 1024;
+
+// One block per cloud: counts of every m (shared memory), exclusive scan into
+// start[b][0..M], then warp 0 places the entries e = 3 i + t in increasing
+// order into their m's segment of list[b] (ranks within a group of 32 from
+// __match_any_sync, cursors in shared memory; one warp, so the order holds).
+__global__ void __launch_bounds__(CSR_THREADS)
+interp_csr_kernel(const int64_t *__restrict__ idx, int n, int M,
+                  int *__restrict__ start, int *__restrict__ list, int *status) {
+    extern __shared__ int cnt[];  // [M] counts, then cursors; [32] warp sums
+    int *wsum = cnt + M;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int E = 3 * n;
+    const int64_t *ib = idx + size_t(b) * E;
+    for (int m = tid; m < M; m += CSR_THREADS) cnt[m] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += STG_THREADS) {
-        int m[3];
-        float wt[3];
-        load_triplet(idx, w, (size_t(b) * n + i) * 3, M, m, wt, status);
-        for (int c = 0; c < cc; ++c) {
-            const float gv = __ldg(g + (size_t(b) * C + c0 + c) * size_t(n) + i);
-            float *tr = tile + c * M;
-#pragma unroll
-            for (int t = 0; t < 3; ++t)
-                if (m[t] >= 0) atomicAdd(tr + m[t], __fmul_rn(wt[t], gv));
-        }
+    for (int e = tid; e < E; e += CSR_THREADS) {
+        const int64_t v = ib[e];
+        if (v >= 0 && v < M)
+            atomicAdd(&cnt[v], 1);
+        else if (v != -1)
+            raise_status(status, PC_ERR_INVALID_ARGUMENT);
     }
     __syncthreads();
-    float *gb = grad_f + (size_t(b) * C + c0) * size_t(M);
-    for (int e = threadIdx.x; e < cc * M; e += STG_THREADS) gb[e] = tile[e];
+    // exclusive scan: thread tid owns [tid * ch, (tid + 1) * ch)
+    const int ch = (M + CSR_THREADS - 1) / CSR_THREADS;
+    const int m0 = min(M, tid * ch), m1 = min(M, m0 + ch);
+    int local = 0;
+    for (int m = m0; m < m1; ++m) local += cnt[m];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += t;
+        }
+        wsum[lane] = w;
+    }
+    __syncthreads();
+    int run = (warp > 0 ? wsum[warp - 1] : 0) + incl - local;
+    int *sb = start + size_t(b) * (M + 1);
+    for (int m = m0; m < m1; ++m) {
+        const int c = cnt[m];
+        cnt[m] = run;  // becomes the cursor of m
+        sb[m] = run;
+        run += c;
+    }
+    if (tid == CSR_THREADS - 1) sb[M] = wsum[31];
+    __syncthreads();
+    if (warp != 0) return;
+    int *lb = list + size_t(b) * E;
+    for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int m = -1;
+        if (e < E) {
+            const int64_t v = ib[e];
+            if (v >= 0 && v < M) m = static_cast<int>(v);
+        }
+        const unsigned group = __match_any_sync(0xffffffffu, m);
+        const int leader = __ffs(group) - 1;
+        int p = 0;
+        if (m >= 0 && lane == leader) {
+            p = cnt[m];
+            cnt[m] = p + __popc(group);
+        }
+        p = __shfl_sync(0xffffffffu, p, leader);
+        if (m >= 0) lb[p + __popc(group & lanemask_lt())] = e;
+        __syncwarp();
+    }
+}
+
+// grad_f[b, c, m] = sum over the entries e of m, in increasing order, of
+// w[b, e] * g[b, c, e / 3] (each product and sum rounded).
+__global__ void __launch_bounds__(256)
+interp_gather_kernel(const float *__restrict__ g, const float *__restrict__ w,
+                     const int *__restrict__ start, const int *__restrict__ list,
+                     int C, int M, int n, float *__restrict__ grad_f) {
+    const int m = blockIdx.x * 256 + threadIdx.x;
+    const int b = blockIdx.z;
+    if (m >= M) return;
+    const int *sb = start + size_t(b) * (M + 1);
+    const int p0 = sb[m], p1 = sb[m + 1];
+    const int *lb = list + size_t(b) * 3 * n;
+    const float *wb = w + size_t(b) * 3 * n;
+    for (int c = blockIdx.y; c < C; c += gridDim.y) {
+        const float *gr = g + (size_t(b) * C + c) * size_t(n);
+        float acc = 0.0f;
+        for (int p = p0; p < p1; ++p) {
+            const int e = lb[p];
+            acc = __fadd_rn(acc, __fmul_rn(wb[e], __ldg(gr + e / 3)));
+        }
+        grad_f[(size_t(b) * C + c) * size_t(M) + m] = acc;
+    }
 }
 
 __global__ void gather_points_kernel(const float *__restrict__ x, int N,
@@ -290,24 +367,33 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         if ((rc = pcn::api_check_ptr(weight, d, 4, "weight")) != PC_OK) return rc;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M <= pcn::STG_SMEM_FLOATS) {
-        // channels per block: a shared-memory tile of at most 64 KB, and about
-        // two blocks per SM when the problem allows it
-        const int64_t want = std::max<int64_t>(1, (B * C) / (2 * int64_t(dev->sm_count)));
-        const int CC = int(std::max<int64_t>(
-            1, std::min<int64_t>({C, pcn::STG_SMEM_FLOATS / M, want})));
-        const size_t smem = size_t(CC) * size_t(M) * sizeof(float);
-        cudaError_t e = cudaFuncSetAttribute(
-            pcn::three_interpolate_backward_staged_kernel,
-            cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (M <= pcn::STG_SMEM_FLOATS && 3 * n <= kMaxInt) {
+        // deterministic path: stream-ordered scratch for the per-cloud CSR
+        const size_t E = size_t(3) * size_t(n);
+        const size_t bytes = size_t(B) * (size_t(M) + 1 + E) * sizeof(int);
+        void *scratch = nullptr;
+        cudaError_t e = cudaMallocAsync(&scratch, bytes, st);
+        if (e != cudaSuccess) return cuda_err(e, "three_interpolate_backward: scratch");
+        int *start = static_cast<int *>(scratch);
+        int *list = start + size_t(B) * (size_t(M) + 1);
+        const size_t csr_smem = (size_t(M) + 32) * sizeof(int);
+        e = cudaFuncSetAttribute(pcn::interp_csr_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(csr_smem));
         if (e == cudaSuccess) {
-            const dim3 grid(unsigned((C + CC - 1) / CC), unsigned(B));
-            pcn::three_interpolate_backward_staged_kernel<<<grid, pcn::STG_THREADS,
-                                                            smem, st>>>(
-                grad_out, idx, weight, int(C), int(M), int(n), CC, grad_features,
-                dev->status_word);
+            pcn::interp_csr_kernel<<<unsigned(B), pcn::CSR_THREADS, csr_smem, st>>>(
+                idx, int(n), int(M), start, list, dev->status_word);
             e = cudaGetLastError();
         }
+        if (e == cudaSuccess) {
+            const dim3 grid(unsigned((M + 255) / 256),
+                            unsigned(std::min<int64_t>(C, 65535)), unsigned(B));
+            pcn::interp_gather_kernel<<<grid, 256, 0, st>>>(
+                grad_out, weight, start, list, int(C), int(M), int(n), grad_features);
+            e = cudaGetLastError();
+        }
+        const cudaError_t ef = cudaFreeAsync(scratch, st);
+        if (e == cudaSuccess) e = ef;
         return e == cudaSuccess ? PC_OK : cuda_err(e, "three_interpolate_backward");
     }
     cudaError_t e = cudaMemsetAsync(grad_features, 0,
