@@ -8,11 +8,12 @@
 //   grad_f[b,c,m] += w[b,i,t] g[b,c,i]  for every idx[b,i,t] = m.
 // Forward: float32, products and sums rounded separately in the order
 // ((w0 f0 + w1 f1) + w2 f2), so the result is bit-identical to the oracle's.
-// Backward (M <= 16384): deterministic and bit-exact with the oracle -- each
+// Backward (M, n <= 16384): deterministic and bit-exact with the oracle -- each
 // grad_f[b, c, m] is summed from 0 in increasing (i, t) order, each product
 // and addition rounded.  Per cloud a CSR of the entries (i, t) of every m,
 // in increasing entry order, is built once (count, scan, stable fill), then
-// one thread per (b, c, m) sums its list.  Larger M: float32 atomic adds
+// one thread per (b, m) sums its list for a chunk of channels whose
+// grad_out rows are staged in shared memory.  Larger sizes: float32 atomic adds
 // (order unspecified, as the pages allow for accumulated gradients).
 // idx = -1 is padding (reads 0, adds nothing); any other index outside
 // [0, M) sets PC_ERR_INVALID_ARGUMENT in the device status word and is
@@ -147,16 +148,20 @@ three_interpolate_staged_kernel(const float *__restrict__ f,
 
 // --- deterministic backward: per-cloud CSR, then ordered sums ---------------
 constexpr int CSR_THREADS = 1024;
+constexpr int CSR_CHUNK = 8192;  // entries staged in shared memory at a time
 
 // One block per cloud: counts of every m (shared memory), exclusive scan into
-// start[b][0..M], then warp 0 places the entries e = 3 i + t in increasing
-// order into their m's segment of list[b] (ranks within a group of 32 from
-// __match_any_sync, cursors in shared memory; one warp, so the order holds).
+// start[b][0..M], then the entries e = 3 i + t are placed in increasing order
+// into their m's segment of list[b]: chunks of entries are staged in shared
+// memory by the block, and warp 0 walks each chunk in order (ranks within a
+// group of 32 from __match_any_sync, cursors in shared memory; one warp, so
+// the order holds).
 __global__ void __launch_bounds__(CSR_THREADS)
 interp_csr_kernel(const int64_t *__restrict__ idx, int n, int M,
                   int *__restrict__ start, int *__restrict__ list, int *status) {
-    extern __shared__ int cnt[];  // [M] counts, then cursors; [32] warp sums
-    int *wsum = cnt + M;
+    extern __shared__ int cnt[];  // [M] counts then cursors, [32] warp sums,
+    int *wsum = cnt + M;          // [CSR_CHUNK] staged entries
+    int *stage = wsum + 32;
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = 3 * n;
@@ -203,50 +208,72 @@ interp_csr_kernel(const int64_t *__restrict__ idx, int n, int M,
         run += c;
     }
     if (tid == CSR_THREADS - 1) sb[M] = wsum[31];
-    __syncthreads();
-    if (warp != 0) return;
     int *lb = list + size_t(b) * E;
-    for (int base = 0; base < E; base += 32) {
-        const int e = base + lane;
-        int m = -1;
-        if (e < E) {
-            const int64_t v = ib[e];
-            if (v >= 0 && v < M) m = static_cast<int>(v);
+    for (int c0 = 0; c0 < E; c0 += CSR_CHUNK) {
+        const int cn = min(CSR_CHUNK, E - c0);
+        __syncthreads();  // cursors written / previous chunk consumed
+        for (int e = tid; e < cn; e += CSR_THREADS) {
+            const int64_t v = ib[c0 + e];
+            stage[e] = (v >= 0 && v < M) ? static_cast<int>(v) : -1;
         }
-        const unsigned group = __match_any_sync(0xffffffffu, m);
-        const int leader = __ffs(group) - 1;
-        int p = 0;
-        if (m >= 0 && lane == leader) {
-            p = cnt[m];
-            cnt[m] = p + __popc(group);
+        __syncthreads();
+        if (warp != 0) continue;
+        for (int base = 0; base < cn; base += 32) {
+            const int e = base + lane;
+            const int m = e < cn ? stage[e] : -1;
+            const unsigned group = __match_any_sync(0xffffffffu, m);
+            const int leader = __ffs(group) - 1;
+            int p = 0;
+            if (m >= 0 && lane == leader) {
+                p = cnt[m];
+                cnt[m] = p + __popc(group);
+            }
+            p = __shfl_sync(0xffffffffu, p, leader);
+            if (m >= 0) lb[p + __popc(group & lanemask_lt())] = c0 + e;
+            __syncwarp();
         }
-        p = __shfl_sync(0xffffffffu, p, leader);
-        if (m >= 0) lb[p + __popc(group & lanemask_lt())] = e;
-        __syncwarp();
     }
 }
 
-// grad_f[b, c, m] = sum over the entries e of m, in increasing order, of
-// w[b, e] * g[b, c, e / 3] (each product and sum rounded).
-__global__ void __launch_bounds__(256)
+// A block owns (cloud b, channels c0 .. c0 + CC): it stages grad_out[b, c, :]
+// for its channels in shared memory, then each thread, for its m, walks the
+// entries of m in increasing order and accumulates w * g for every channel:
+//   grad_f[b, c, m] = sum over e of w[b, e] * g[b, c, e / 3]
+// (each product and sum rounded, from 0).
+constexpr int GATH_THREADS = 256;
+constexpr int GATH_SMEM_FLOATS = 16384;  // 64 KB of grad_out per block
+constexpr int GATH_MAXCC = 8;
+
+__global__ void __launch_bounds__(GATH_THREADS)
 interp_gather_kernel(const float *__restrict__ g, const float *__restrict__ w,
                      const int *__restrict__ start, const int *__restrict__ list,
-                     int C, int M, int n, float *__restrict__ grad_f) {
-    const int m = blockIdx.x * 256 + threadIdx.x;
-    const int b = blockIdx.z;
-    if (m >= M) return;
+                     int C, int M, int n, int CC, float *__restrict__ grad_f) {
+    extern __shared__ float gt[];  // [CC][n]
+    const int b = blockIdx.y;
+    const int c0 = blockIdx.x * CC;
+    const int cc = min(CC, C - c0);
+    const float *gb = g + (size_t(b) * C + c0) * size_t(n);
+    for (int e = threadIdx.x; e < cc * n; e += GATH_THREADS) gt[e] = __ldg(gb + e);
+    __syncthreads();
     const int *sb = start + size_t(b) * (M + 1);
-    const int p0 = sb[m], p1 = sb[m + 1];
     const int *lb = list + size_t(b) * 3 * n;
     const float *wb = w + size_t(b) * 3 * n;
-    for (int c = blockIdx.y; c < C; c += gridDim.y) {
-        const float *gr = g + (size_t(b) * C + c) * size_t(n);
-        float acc = 0.0f;
+    for (int m = threadIdx.x; m < M; m += GATH_THREADS) {
+        const int p0 = sb[m], p1 = sb[m + 1];
+        float acc[GATH_MAXCC];
+#pragma unroll
+        for (int c = 0; c < GATH_MAXCC; ++c) acc[c] = 0.0f;
         for (int p = p0; p < p1; ++p) {
             const int e = lb[p];
-            acc = __fadd_rn(acc, __fmul_rn(wb[e], __ldg(gr + e / 3)));
+            const float wv = wb[e];
+            const int i = e / 3;
+#pragma unroll
+            for (int c = 0; c < GATH_MAXCC; ++c)
+                if (c < cc) acc[c] = __fadd_rn(acc[c], __fmul_rn(wv, gt[c * n + i]));
         }
-        grad_f[(size_t(b) * C + c) * size_t(M) + m] = acc;
+#pragma unroll
+        for (int c = 0; c < GATH_MAXCC; ++c)
+            if (c < cc) grad_f[(size_t(b) * C + c0 + c) * size_t(M) + m] = acc[c];
     }
 }
 
@@ -367,7 +394,7 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         if ((rc = pcn::api_check_ptr(weight, d, 4, "weight")) != PC_OK) return rc;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M <= pcn::STG_SMEM_FLOATS && 3 * n <= kMaxInt) {
+    if (M <= pcn::STG_SMEM_FLOATS && n <= pcn::GATH_SMEM_FLOATS) {
         // deterministic path: stream-ordered scratch for the per-cloud CSR
         const size_t E = size_t(3) * size_t(n);
         const size_t bytes = size_t(B) * (size_t(M) + 1 + E) * sizeof(int);
@@ -376,7 +403,7 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         if (e != cudaSuccess) return cuda_err(e, "three_interpolate_backward: scratch");
         int *start = static_cast<int *>(scratch);
         int *list = start + size_t(B) * (size_t(M) + 1);
-        const size_t csr_smem = (size_t(M) + 32) * sizeof(int);
+        const size_t csr_smem = (size_t(M) + 32 + pcn::CSR_CHUNK) * sizeof(int);
         e = cudaFuncSetAttribute(pcn::interp_csr_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(csr_smem));
@@ -385,11 +412,18 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
                 idx, int(n), int(M), start, list, dev->status_word);
             e = cudaGetLastError();
         }
+        const int CC = int(std::max<int64_t>(1, std::min<int64_t>(
+            {C, pcn::GATH_MAXCC, pcn::GATH_SMEM_FLOATS / std::max<int64_t>(n, 1)})));
+        const size_t g_smem = size_t(CC) * size_t(std::max<int64_t>(n, 1)) * sizeof(float);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(pcn::interp_gather_kernel,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(g_smem));
         if (e == cudaSuccess) {
-            const dim3 grid(unsigned((M + 255) / 256),
-                            unsigned(std::min<int64_t>(C, 65535)), unsigned(B));
-            pcn::interp_gather_kernel<<<grid, 256, 0, st>>>(
-                grad_out, weight, start, list, int(C), int(M), int(n), grad_features);
+            const dim3 grid(unsigned((C + CC - 1) / CC), unsigned(B));
+            pcn::interp_gather_kernel<<<grid, pcn::GATH_THREADS, g_smem, st>>>(
+                grad_out, weight, start, list, int(C), int(M), int(n), CC,
+                grad_features);
             e = cudaGetLastError();
         }
         const cudaError_t ef = cudaFreeAsync(scratch, st);
