@@ -11,7 +11,8 @@
 // Backward (M, n <= 16384): deterministic and bit-exact with the oracle -- each
 // grad_f[b, c, m] is summed from 0 in increasing (i, t) order, each product
 // and addition rounded.  Per cloud a CSR of the entries (i, t) of every m,
-// in increasing entry order, is built once (count, scan, stable fill), then
+// in increasing entry order, is built once (count, scan, fill, then a sort of
+// each short segment by entry), then
 // one thread per (b, m) sums its list for a chunk of channels whose
 // grad_out rows are staged in shared memory.  Larger sizes: float32 atomic adds
 // (order unspecified, as the pages allow for accumulated gradients).
@@ -148,20 +149,18 @@ three_interpolate_staged_kernel(const float *__restrict__ f,
 
 // --- deterministic backward: per-cloud CSR, then ordered sums ---------------
 constexpr int CSR_THREADS = 1024;
-constexpr int CSR_CHUNK = 8192;  // entries staged in shared memory at a time
 
-// One block per cloud: counts of every m (shared memory), exclusive scan into
-// start[b][0..M], then the entries e = 3 i + t are placed in increasing order
-// into their m's segment of list[b]: chunks of entries are staged in shared
-// memory by the block, and warp 0 walks each chunk in order (ranks within a
-// group of 32 from __match_any_sync, cursors in shared memory; one warp, so
-// the order holds).
+// One block per cloud: counts of every m (shared-memory atomics), exclusive
+// scan into start[b][0..M], then every entry e = 3 i + t is placed in its m's
+// segment at a cursor taken with a shared-memory atomic, as the pair
+// (e, weight) -- the order inside a segment is fixed afterwards by
+// interp_sort_kernel.
 __global__ void __launch_bounds__(CSR_THREADS)
-interp_csr_kernel(const int64_t *__restrict__ idx, int n, int M,
-                  int *__restrict__ start, int *__restrict__ list, int *status) {
-    extern __shared__ int cnt[];  // [M] counts then cursors, [32] warp sums,
-    int *wsum = cnt + M;          // [CSR_CHUNK] staged entries
-    int *stage = wsum + 32;
+interp_csr_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w,
+                  int n, int M, int *__restrict__ start, int2 *__restrict__ list,
+                  int *status) {
+    extern __shared__ int cnt[];  // [M] counts then cursors, [32] warp sums
+    int *wsum = cnt + M;
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int E = 3 * n;
@@ -190,13 +189,13 @@ interp_csr_kernel(const int64_t *__restrict__ idx, int n, int M,
     if (lane == 31) wsum[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int w = wsum[lane];
+        int x = wsum[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += t;
+            const int t = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += t;
         }
-        wsum[lane] = w;
+        wsum[lane] = x;
     }
     __syncthreads();
     int run = (warp > 0 ? wsum[warp - 1] : 0) + incl - local;
@@ -208,36 +207,42 @@ interp_csr_kernel(const int64_t *__restrict__ idx, int n, int M,
         run += c;
     }
     if (tid == CSR_THREADS - 1) sb[M] = wsum[31];
-    int *lb = list + size_t(b) * E;
-    for (int c0 = 0; c0 < E; c0 += CSR_CHUNK) {
-        const int cn = min(CSR_CHUNK, E - c0);
-        __syncthreads();  // cursors written / previous chunk consumed
-        for (int e = tid; e < cn; e += CSR_THREADS) {
-            const int64_t v = ib[c0 + e];
-            stage[e] = (v >= 0 && v < M) ? static_cast<int>(v) : -1;
+    __syncthreads();
+    int2 *lb = list + size_t(b) * E;
+    const float *wb = w + size_t(b) * E;
+    for (int e = tid; e < E; e += CSR_THREADS) {
+        const int64_t v = ib[e];
+        if (v >= 0 && v < M) {
+            const int p = atomicAdd(&cnt[v], 1);
+            lb[p] = make_int2(e, __float_as_int(wb[e]));
         }
-        __syncthreads();
-        if (warp != 0) continue;
-        for (int base = 0; base < cn; base += 32) {
-            const int e = base + lane;
-            const int m = e < cn ? stage[e] : -1;
-            const unsigned group = __match_any_sync(0xffffffffu, m);
-            const int leader = __ffs(group) - 1;
-            int p = 0;
-            if (m >= 0 && lane == leader) {
-                p = cnt[m];
-                cnt[m] = p + __popc(group);
-            }
-            p = __shfl_sync(0xffffffffu, p, leader);
-            if (m >= 0) lb[p + __popc(group & lanemask_lt())] = c0 + e;
-            __syncwarp();
+    }
+}
+
+// One thread per (b, m): insertion sort of m's segment by entry e (segments
+// hold ~3n/M entries), so the sums run in increasing (i, t) order.
+__global__ void interp_sort_kernel(const int *__restrict__ start,
+                                   int2 *__restrict__ list, int B, int M, int n) {
+    const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= int64_t(B) * M) return;
+    const int b = int(t / M), m = int(t % M);
+    const int *sb = start + size_t(b) * (M + 1);
+    int2 *lb = list + size_t(b) * 3 * n;
+    const int p0 = sb[m], p1 = sb[m + 1];
+    for (int p = p0 + 1; p < p1; ++p) {
+        const int2 v = lb[p];
+        int q = p - 1;
+        while (q >= p0 && lb[q].x > v.x) {
+            lb[q + 1] = lb[q];
+            --q;
         }
+        lb[q + 1] = v;
     }
 }
 
 // A block owns (cloud b, channels c0 .. c0 + CC): it stages grad_out[b, c, :]
 // for its channels in shared memory, then each thread, for its m, walks the
-// entries of m in increasing order and accumulates w * g for every channel:
+// sorted entries of m and accumulates w * g for every channel:
 //   grad_f[b, c, m] = sum over e of w[b, e] * g[b, c, e / 3]
 // (each product and sum rounded, from 0).
 constexpr int GATH_THREADS = 256;
@@ -245,9 +250,9 @@ constexpr int GATH_SMEM_FLOATS = 16384;  // 64 KB of grad_out per block
 constexpr int GATH_MAXCC = 8;
 
 __global__ void __launch_bounds__(GATH_THREADS)
-interp_gather_kernel(const float *__restrict__ g, const float *__restrict__ w,
-                     const int *__restrict__ start, const int *__restrict__ list,
-                     int C, int M, int n, int CC, float *__restrict__ grad_f) {
+interp_gather_kernel(const float *__restrict__ g, const int *__restrict__ start,
+                     const int2 *__restrict__ list, int C, int M, int n, int CC,
+                     float *__restrict__ grad_f) {
     extern __shared__ float gt[];  // [CC][n]
     const int b = blockIdx.y;
     const int c0 = blockIdx.x * CC;
@@ -256,17 +261,16 @@ interp_gather_kernel(const float *__restrict__ g, const float *__restrict__ w,
     for (int e = threadIdx.x; e < cc * n; e += GATH_THREADS) gt[e] = __ldg(gb + e);
     __syncthreads();
     const int *sb = start + size_t(b) * (M + 1);
-    const int *lb = list + size_t(b) * 3 * n;
-    const float *wb = w + size_t(b) * 3 * n;
+    const int2 *lb = list + size_t(b) * 3 * n;
     for (int m = threadIdx.x; m < M; m += GATH_THREADS) {
         const int p0 = sb[m], p1 = sb[m + 1];
         float acc[GATH_MAXCC];
 #pragma unroll
         for (int c = 0; c < GATH_MAXCC; ++c) acc[c] = 0.0f;
         for (int p = p0; p < p1; ++p) {
-            const int e = lb[p];
-            const float wv = wb[e];
-            const int i = e / 3;
+            const int2 v = __ldg(lb + p);
+            const float wv = __int_as_float(v.y);
+            const int i = v.x / 3;
 #pragma unroll
             for (int c = 0; c < GATH_MAXCC; ++c)
                 if (c < cc) acc[c] = __fadd_rn(acc[c], __fmul_rn(wv, gt[c * n + i]));
@@ -397,19 +401,26 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
     if (M <= pcn::STG_SMEM_FLOATS && n <= pcn::GATH_SMEM_FLOATS) {
         // deterministic path: stream-ordered scratch for the per-cloud CSR
         const size_t E = size_t(3) * size_t(n);
-        const size_t bytes = size_t(B) * (size_t(M) + 1 + E) * sizeof(int);
+        const size_t start_bytes = (size_t(B) * (size_t(M) + 1) * sizeof(int) + 15) & ~size_t(15);
+        const size_t bytes = start_bytes + size_t(B) * E * sizeof(int2);
         void *scratch = nullptr;
         cudaError_t e = cudaMallocAsync(&scratch, bytes, st);
         if (e != cudaSuccess) return cuda_err(e, "three_interpolate_backward: scratch");
         int *start = static_cast<int *>(scratch);
-        int *list = start + size_t(B) * (size_t(M) + 1);
-        const size_t csr_smem = (size_t(M) + 32 + pcn::CSR_CHUNK) * sizeof(int);
+        int2 *list = reinterpret_cast<int2 *>(static_cast<char *>(scratch) + start_bytes);
+        const size_t csr_smem = (size_t(M) + 32) * sizeof(int);
         e = cudaFuncSetAttribute(pcn::interp_csr_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(csr_smem));
         if (e == cudaSuccess) {
             pcn::interp_csr_kernel<<<unsigned(B), pcn::CSR_THREADS, csr_smem, st>>>(
-                idx, int(n), int(M), start, list, dev->status_word);
+                idx, weight, int(n), int(M), start, list, dev->status_word);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            const int64_t segs = B * M;
+            pcn::interp_sort_kernel<<<unsigned((segs + 255) / 256), 256, 0, st>>>(
+                start, list, int(B), int(M), int(n));
             e = cudaGetLastError();
         }
         const int CC = int(std::max<int64_t>(1, std::min<int64_t>(
@@ -422,8 +433,7 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         if (e == cudaSuccess) {
             const dim3 grid(unsigned((C + CC - 1) / CC), unsigned(B));
             pcn::interp_gather_kernel<<<grid, pcn::GATH_THREADS, g_smem, st>>>(
-                grad_out, weight, start, list, int(C), int(M), int(n), CC,
-                grad_features);
+                grad_out, start, list, int(C), int(M), int(n), CC, grad_features);
             e = cudaGetLastError();
         }
         const cudaError_t ef = cudaFreeAsync(scratch, st);
