@@ -258,7 +258,16 @@ interp_gather_kernel(const float *__restrict__ g, const int *__restrict__ start,
     const int c0 = blockIdx.x * CC;
     const int cc = min(CC, C - c0);
     const float *gb = g + (size_t(b) * C + c0) * size_t(n);
-    for (int e = threadIdx.x; e < cc * n; e += GATH_THREADS) gt[e] = __ldg(gb + e);
+    const int tot = cc * n;
+    if ((reinterpret_cast<uintptr_t>(gb) & 15) == 0 && (tot & 3) == 0) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(gb);
+        float4 *s4 = reinterpret_cast<float4 *>(gt);
+#pragma unroll 4
+        for (int e = threadIdx.x; e < tot / 4; e += GATH_THREADS) s4[e] = __ldg(g4 + e);
+    } else {
+#pragma unroll 8
+        for (int e = threadIdx.x; e < tot; e += GATH_THREADS) gt[e] = __ldg(gb + e);
+    }
     __syncthreads();
     const int *sb = start + size_t(b) * (M + 1);
     const int2 *lb = list + size_t(b) * 3 * n;
@@ -267,13 +276,20 @@ interp_gather_kernel(const float *__restrict__ g, const int *__restrict__ start,
         float acc[GATH_MAXCC];
 #pragma unroll
         for (int c = 0; c < GATH_MAXCC; ++c) acc[c] = 0.0f;
-        for (int p = p0; p < p1; ++p) {
-            const int2 v = __ldg(lb + p);
-            const float wv = __int_as_float(v.y);
-            const int i = v.x / 3;
+        for (int pc = p0; pc < p1; pc += 16) {
+            int2 v[16];  // the next 16 entries, loaded before any is used
 #pragma unroll
-            for (int c = 0; c < GATH_MAXCC; ++c)
-                if (c < cc) acc[c] = __fadd_rn(acc[c], __fmul_rn(wv, gt[c * n + i]));
+            for (int u = 0; u < 16; ++u)
+                v[u] = pc + u < p1 ? __ldg(lb + pc + u) : make_int2(0, 0);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                if (pc + u >= p1) break;
+                const float wv = __int_as_float(v[u].y);
+                const int i = v[u].x / 3;
+#pragma unroll
+                for (int c = 0; c < GATH_MAXCC; ++c)
+                    if (c < cc) acc[c] = __fadd_rn(acc[c], __fmul_rn(wv, gt[c * n + i]));
+            }
         }
 #pragma unroll
         for (int c = 0; c < GATH_MAXCC; ++c)
