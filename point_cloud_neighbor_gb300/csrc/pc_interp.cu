@@ -240,42 +240,37 @@ __global__ void interp_sort_kernel(const int *__restrict__ start,
     }
 }
 
-// A block owns (cloud b, channels c0 .. c0 + CC): it stages grad_out[b, c, :]
-// for its channels in shared memory, then each thread, for its m, walks the
-// sorted entries of m and accumulates w * g for every channel:
+// A block owns (cloud b, channels c0 .. c0 + 4): it stages grad_out[b, c, :]
+// for its channels in shared memory point-major (the 4 channels of a point
+// are one 16-byte word), then each thread, for its m, walks the sorted
+// entries of m and accumulates w * g for the 4 channels:
 //   grad_f[b, c, m] = sum over e of w[b, e] * g[b, c, e / 3]
 // (each product and sum rounded, from 0).
 constexpr int GATH_THREADS = 256;
-constexpr int GATH_SMEM_FLOATS = 16384;  // 64 KB of grad_out per block
-constexpr int GATH_MAXCC = 8;
+constexpr int GATH_SMEM_FLOATS = 32768;  // 128 KB of grad_out per block (n <= 8192)
+constexpr int GATH_CC = 4;
 
 __global__ void __launch_bounds__(GATH_THREADS)
 interp_gather_kernel(const float *__restrict__ g, const int *__restrict__ start,
-                     const int2 *__restrict__ list, int C, int M, int n, int CC,
+                     const int2 *__restrict__ list, int C, int M, int n,
                      float *__restrict__ grad_f) {
-    extern __shared__ float gt[];  // [CC][n]
+    extern __shared__ float4 gt4[];  // [n]: channels c0 .. c0 + 3 of point i
     const int b = blockIdx.y;
-    const int c0 = blockIdx.x * CC;
-    const int cc = min(CC, C - c0);
+    const int c0 = blockIdx.x * GATH_CC;
+    const int cc = min(GATH_CC, C - c0);
     const float *gb = g + (size_t(b) * C + c0) * size_t(n);
-    const int tot = cc * n;
-    if ((reinterpret_cast<uintptr_t>(gb) & 15) == 0 && (tot & 3) == 0) {
-        const float4 *g4 = reinterpret_cast<const float4 *>(gb);
-        float4 *s4 = reinterpret_cast<float4 *>(gt);
+    float *gts = reinterpret_cast<float *>(gt4);
 #pragma unroll 4
-        for (int e = threadIdx.x; e < tot / 4; e += GATH_THREADS) s4[e] = __ldg(g4 + e);
-    } else {
-#pragma unroll 8
-        for (int e = threadIdx.x; e < tot; e += GATH_THREADS) gt[e] = __ldg(gb + e);
+    for (int e = threadIdx.x; e < GATH_CC * n; e += GATH_THREADS) {
+        const int c = e / n, i = e - c * n;
+        gts[i * GATH_CC + c] = c < cc ? __ldg(gb + e) : 0.0f;
     }
     __syncthreads();
     const int *sb = start + size_t(b) * (M + 1);
     const int2 *lb = list + size_t(b) * 3 * n;
     for (int m = threadIdx.x; m < M; m += GATH_THREADS) {
         const int p0 = sb[m], p1 = sb[m + 1];
-        float acc[GATH_MAXCC];
-#pragma unroll
-        for (int c = 0; c < GATH_MAXCC; ++c) acc[c] = 0.0f;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
         for (int pc = p0; pc < p1; pc += 16) {
             int2 v[16];  // the next 16 entries, loaded before any is used
 #pragma unroll
@@ -285,15 +280,18 @@ interp_gather_kernel(const float *__restrict__ g, const int *__restrict__ start,
             for (int u = 0; u < 16; ++u) {
                 if (pc + u >= p1) break;
                 const float wv = __int_as_float(v[u].y);
-                const int i = v[u].x / 3;
-#pragma unroll
-                for (int c = 0; c < GATH_MAXCC; ++c)
-                    if (c < cc) acc[c] = __fadd_rn(acc[c], __fmul_rn(wv, gt[c * n + i]));
+                const float4 gv = gt4[v[u].x / 3];
+                a0 = __fadd_rn(a0, __fmul_rn(wv, gv.x));
+                a1 = __fadd_rn(a1, __fmul_rn(wv, gv.y));
+                a2 = __fadd_rn(a2, __fmul_rn(wv, gv.z));
+                a3 = __fadd_rn(a3, __fmul_rn(wv, gv.w));
             }
         }
-#pragma unroll
-        for (int c = 0; c < GATH_MAXCC; ++c)
-            if (c < cc) grad_f[(size_t(b) * C + c0 + c) * size_t(M) + m] = acc[c];
+        float *out = grad_f + (size_t(b) * C + c0) * size_t(M) + m;
+        out[0] = a0;
+        if (cc > 1) out[size_t(M)] = a1;
+        if (cc > 2) out[2 * size_t(M)] = a2;
+        if (cc > 3) out[3 * size_t(M)] = a3;
     }
 }
 
@@ -414,7 +412,7 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         if ((rc = pcn::api_check_ptr(weight, d, 4, "weight")) != PC_OK) return rc;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (M <= pcn::STG_SMEM_FLOATS && n <= pcn::GATH_SMEM_FLOATS) {
+    if (M <= pcn::STG_SMEM_FLOATS && n <= pcn::GATH_SMEM_FLOATS / pcn::GATH_CC) {
         // deterministic path: stream-ordered scratch for the per-cloud CSR
         const size_t E = size_t(3) * size_t(n);
         const size_t start_bytes = (size_t(B) * (size_t(M) + 1) * sizeof(int) + 15) & ~size_t(15);
@@ -439,17 +437,16 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
                 start, list, int(B), int(M), int(n));
             e = cudaGetLastError();
         }
-        const int CC = int(std::max<int64_t>(1, std::min<int64_t>(
-            {C, pcn::GATH_MAXCC, pcn::GATH_SMEM_FLOATS / std::max<int64_t>(n, 1)})));
-        const size_t g_smem = size_t(CC) * size_t(std::max<int64_t>(n, 1)) * sizeof(float);
+        const size_t g_smem = size_t(pcn::GATH_CC) * size_t(std::max<int64_t>(n, 1)) *
+                              sizeof(float);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(pcn::interp_gather_kernel,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      int(g_smem));
         if (e == cudaSuccess) {
-            const dim3 grid(unsigned((C + CC - 1) / CC), unsigned(B));
+            const dim3 grid(unsigned((C + pcn::GATH_CC - 1) / pcn::GATH_CC), unsigned(B));
             pcn::interp_gather_kernel<<<grid, pcn::GATH_THREADS, g_smem, st>>>(
-                grad_out, start, list, int(C), int(M), int(n), CC, grad_features);
+                grad_out, start, list, int(C), int(M), int(n), grad_features);
             e = cudaGetLastError();
         }
         const cudaError_t ef = cudaFreeAsync(scratch, st);
