@@ -1,0 +1,98 @@
+"""Seeded randomized parity sweep: many small configurations of every
+operator against the oracle, element by element.
+
+Sizes, k/K, radii, lengths, duplicate points and lattice coordinates (exact
+ties, points on the radius boundary) are drawn from a fixed seed, so every
+run checks the same cases; the sizes straddle the kernels' tile and block
+boundaries (256-point tiles, 32-lane warps, 64/256-query blocks).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import point_cloud_neighbor_gb300 as pc
+from test_gpu_parity import THREADS, assert_dist_equal, assert_idx_equal, to_dev
+
+pytestmark = pytest.mark.gpu
+
+CASES = 40
+
+
+@pytest.fixture(autouse=True)
+def clean_status():
+    yield
+    assert pc.pc_device_status(reset=True) == 0
+
+
+def cloud(rng, B, N):
+    kind = rng.integers(0, 3)
+    if kind == 0:      # lattice: exact ties and boundary hits
+        x = rng.integers(0, 16, (B, N, 3)) / 16.0
+    elif kind == 1:    # clustered
+        x = rng.random((B, 1, 3)) + 0.02 * rng.standard_normal((B, N, 3))
+    else:
+        x = rng.random((B, N, 3)) * 4.0 - 2.0
+    x = x.astype(np.float32)
+    if N > 4 and rng.random() < 0.5:  # duplicates
+        src = rng.integers(0, N, N // 8)
+        dst = rng.integers(0, N, N // 8)
+        x[:, dst] = x[:, src]
+    return np.ascontiguousarray(x)
+
+
+def sizes(rng):
+    B = int(rng.integers(1, 4))
+    N = int(rng.choice([1, 2, 31, 32, 33, 255, 256, 257, 511, 700, 1500]))
+    Q = int(rng.choice([1, 7, 31, 32, 33, 64, 255, 256, 257, 300]))
+    return B, Q, N
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_knn(case):
+    rng = np.random.default_rng(5000 + case)
+    B, Q, N = sizes(rng)
+    k = int(min(N, rng.choice([1, 2, 3, 16, 32, 33, 64, 100])))
+    q, x = cloud(rng, B, Q), cloud(rng, B, N)
+    d, i = pc.pc_knn(to_dev(q), to_dev(x), k)
+    wd, wi = oracle.knn(q, x, k, threads=THREADS)
+    what = f"fuzz knn B={B} Q={Q} N={N} k={k}"
+    assert_idx_equal(i.cpu().numpy().reshape(-1, k), wi, what)
+    assert_dist_equal(d.cpu().numpy().reshape(-1, k), wd, what)
+
+
+@pytest.mark.parametrize("case", range(CASES))
+def test_fuzz_ball_query_with_lengths(case):
+    rng = np.random.default_rng(6000 + case)
+    B, Q, N = sizes(rng)
+    K = int(rng.choice([1, 5, 32, 33, 100, 300]))
+    r = float(rng.choice([0.0625, 0.125, 0.25, 0.5, 1.0, 3.0]))
+    q, x = cloud(rng, B, Q), cloud(rng, B, N)
+    ql = rng.integers(-1, Q + 2, B) if rng.random() < 0.5 else None
+    rl = rng.integers(-1, N + 2, B) if rng.random() < 0.5 else None
+    lens = lambda v: None if v is None else torch.tensor(v, dtype=torch.int64,
+                                                        device="cuda")
+    d, i = pc.pc_ball_query(to_dev(q), to_dev(x), r, K, query_lengths=lens(ql),
+                            ref_lengths=lens(rl))
+    wd, wi = oracle.ball_query_masked(q, x, r, K, ql, rl)
+    what = f"fuzz bq B={B} Q={Q} N={N} r={r} K={K} ql={ql} rl={rl}"
+    assert_idx_equal(i.cpu().numpy().reshape(-1, K), wi, what)
+    assert_dist_equal(d.cpu().numpy().reshape(-1, K), wd, what)
+
+
+@pytest.mark.parametrize("case", range(CASES // 2))
+def test_fuzz_fps_and_grid(case):
+    rng = np.random.default_rng(7000 + case)
+    B, _, N = sizes(rng)
+    x = cloud(rng, B, N)
+    npoint = int(rng.choice([1, 2, 17, 64, 300]))
+    start = int(rng.integers(0, N))
+    idx = pc.pc_fps(to_dev(x), npoint, start)
+    assert_idx_equal(idx.cpu().numpy(), oracle.fps(x, npoint, start),
+                     f"fuzz fps N={N} npoint={npoint} start={start}")
+    k = int(min(N, rng.choice([1, 4, 16])))
+    g = pc.pc_grid_build(to_dev(x))
+    gd, gi = pc.pc_knn_grid(to_dev(x), g, k)
+    wd, wi = oracle.knn(x, x, k, threads=THREADS)
+    assert_idx_equal(gi.cpu().numpy().reshape(-1, k), wi, f"fuzz grid knn N={N}")
+    assert_dist_equal(gd.cpu().numpy().reshape(-1, k), wd, f"fuzz grid knn N={N}")
