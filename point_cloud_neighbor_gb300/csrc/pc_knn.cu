@@ -438,11 +438,14 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // and replaces the root by every point that beats it (sift-down).  At the end
 // each lane heap-sorts its k entries into ascending (s, j) order.
 // ---------------------------------------------------------------------------
-constexpr int KL_QL = 2;                        // queries per lane (2: measured best)
-constexpr int KL_CWARPS = 8 / KL_QL;            // consumer warps per block
-constexpr int KL_QPB = KL_CWARPS * 32 * KL_QL;  // queries per block
-constexpr int KL_THREADS = 32 * (KL_CWARPS + 1);
-constexpr int KL_MINB = KL_QL == 1 ? 2 : (KL_QL == 2 ? 3 : 5);  // blocks per SM
+// QL queries per lane: 2 for k <= 16, 1 above (measured: k = 16 3.23 vs
+// 3.43 ms, k = 32 5.30 vs 6.24 ms, where the heaps limit the blocks per SM)
+constexpr int KL_QPB = 256;  // queries per block
+template <int QL> struct LaneShape {
+    static constexpr int CWARPS = 8 / QL;  // consumer warps per block
+    static constexpr int THREADS = 32 * (CWARPS + 1);
+    static constexpr int MINB = QL == 1 ? 2 : 3;  // blocks per SM (registers)
+};
 
 __host__ __device__ constexpr size_t knn_lane_smem(int k) {
     return stream_smem_bytes() + size_t(KL_QPB) * size_t(k) * 8;
@@ -479,7 +482,10 @@ __device__ __forceinline__ void heap_sift(float *hs, int *hj, int n, int pos,
     hj[pos * 32] = j;
 }
 
-__global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const KnnArgs a) {
+template <int KL_QL>
+__global__ void __launch_bounds__(LaneShape<KL_QL>::THREADS, LaneShape<KL_QL>::MINB)
+knn_lane_kernel(const KnnArgs a) {
+    constexpr int KL_CWARPS = LaneShape<KL_QL>::CWARPS;
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -664,18 +670,19 @@ __global__ void __launch_bounds__(KL_THREADS, KL_MINB) knn_lane_kernel(const Knn
     }
 }
 
+template <int QL>
 cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a, int64_t B,
                             int64_t Q, cudaStream_t stream) {
     (void)dev;
     const size_t smem = knn_lane_smem(a.k);
     cudaError_t e = cudaFuncSetAttribute(
-        knn_lane_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        knn_lane_kernel<QL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t per_block = KL_QPB;
     dim3 grid(static_cast<unsigned>((Q + per_block - 1) / per_block),
               static_cast<unsigned>(B));
-    knn_lane_kernel<<<grid, KL_THREADS, smem, stream>>>(a);
+    knn_lane_kernel<QL><<<grid, LaneShape<QL>::THREADS, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -725,7 +732,8 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
-    if (k <= 32) return launch_knn_lane(dev, a, B, Q, stream);
+    if (k <= 16) return launch_knn_lane<2>(dev, a, B, Q, stream);
+    if (k <= 32) return launch_knn_lane<1>(dev, a, B, Q, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
     if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
     return launch_knn_t<8>(dev, a, B, Q, stream);
