@@ -99,8 +99,11 @@ __device__ __forceinline__ int bq_record(const float *tile,
                                          int64_t *out_idx) {
     const int lane = static_cast<int>(lane_id());
     const unsigned pm = filter_mask8(rx, ry, rz, rw, axy, azt);
-#pragma unroll
-    for (int r = 0; r < BQ_R; ++r) {
+    // rows r where some lane may hold a hit, in increasing r (input order)
+    unsigned rows = __reduce_or_sync(FULL, pm);
+    while (rows) {
+        const int r = __ffs(rows) - 1;
+        rows &= rows - 1;
         float s = 0.f;
         bool hit = false;
         if (((pm >> r) & 1u) && r * 32 + lane < cnt) {
