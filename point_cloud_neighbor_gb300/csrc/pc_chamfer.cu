@@ -8,7 +8,8 @@
 // batch reductions.  Here:
 //   * each direction is the brute-force kNN kernel (pc_knn.cu) with k = 1,
 //     the clouds' valid lengths and the squared distance returned: nearest
-//     index and s32 with exact ties to the smaller index;
+//     index and s32 with exact ties to the smaller index; the two directions
+//     share one launch;
 //   * one block of 1024 threads reduces the per-point distances in float64
 //     in a fixed order (strided per thread, then a fixed shuffle tree), so
 //     the loss is deterministic from run to run and within a few float64
@@ -160,12 +161,19 @@ extern "C" int pc_chamfer(const float *x, int64_t B, int64_t P1,
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;
-    if (B > 0 && P1 > 0)
-        e = pcn::launch_knn(*dev, x, B, P1, y, P2, 1, x_lengths, y_lengths, true,
-                            out_dist_x, out_idx_x, st);
-    if (e == cudaSuccess && both && B > 0 && P2 > 0)
-        e = pcn::launch_knn(*dev, y, B, P2, x, P1, 1, y_lengths, x_lengths, true,
-                            out_dist_y, out_idx_y, st);
+    if (both && B > 0 && P1 > 0 && P2 > 0) {
+        // both directions in one launch: twice the blocks of either alone
+        e = pcn::launch_knn_pair(*dev, B, 1, true, x, P1, y, P2, x_lengths,
+                                 y_lengths, out_dist_x, out_idx_x, y, P2, x, P1,
+                                 y_lengths, x_lengths, out_dist_y, out_idx_y, st);
+    } else {
+        if (B > 0 && P1 > 0)
+            e = pcn::launch_knn(*dev, x, B, P1, y, P2, 1, x_lengths, y_lengths, true,
+                                out_dist_x, out_idx_x, st);
+        if (e == cudaSuccess && both && B > 0 && P2 > 0)
+            e = pcn::launch_knn(*dev, y, B, P2, x, P1, 1, y_lengths, x_lengths, true,
+                                out_dist_y, out_idx_y, st);
+    }
     if (e == cudaSuccess && out_loss != nullptr) {
         pcn::ChamferReduceArgs a{};
         a.dist_x = P1 > 0 ? out_dist_x : nullptr;

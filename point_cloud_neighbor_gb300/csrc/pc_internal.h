@@ -51,6 +51,16 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
                        const int64_t *q_len, const int64_t *r_len, bool squared,
                        float *out_dist, int64_t *out_idx, cudaStream_t stream);
 
+// Two kNN problems with the same B and k in one launch when k <= 32 (the
+// Chamfer distance's two directions); two launches otherwise.
+cudaError_t launch_knn_pair(const DeviceInfo &dev, int64_t B, int k, bool squared,
+                            const float *q0, int64_t Q0, const float *r0, int64_t N0,
+                            const int64_t *ql0, const int64_t *rl0, float *d0,
+                            int64_t *i0, const float *q1, int64_t Q1,
+                            const float *r1, int64_t N1, const int64_t *ql1,
+                            const int64_t *rl1, float *d1, int64_t *i1,
+                            cudaStream_t stream);
+
 cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
                               int64_t B, int64_t Q, const float *ref,
                               int64_t N, const int64_t *q_len,

@@ -482,14 +482,19 @@ __device__ __forceinline__ void heap_sift(float *hs, int *hj, int n, int pos,
     hj[pos * 32] = j;
 }
 
+// Two problems with the same k can share one launch: block rows
+// blockIdx.y < B0 run a0 (cloud blockIdx.y), the rest a1 (cloud
+// blockIdx.y - B0) -- used for the two directions of the Chamfer distance.
 template <int KL_QL>
 __global__ void __launch_bounds__(LaneShape<KL_QL>::THREADS, LaneShape<KL_QL>::MINB)
-knn_lane_kernel(const KnnArgs a) {
+knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     constexpr int KL_CWARPS = LaneShape<KL_QL>::CWARPS;
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.y;
+    const bool second = int(blockIdx.y) >= B0;
+    const KnnArgs a = second ? a1 : a0;
+    const int b = second ? int(blockIdx.y) - B0 : int(blockIdx.y);
     const int k = a.k;
     const float inf = __int_as_float(0x7f800000);
 
@@ -579,7 +584,7 @@ knn_lane_kernel(const KnnArgs a) {
         const float4 *ck = ring.cooked_tile(st);
         const int j0 = knn_tile_at(it, tstride, ntiles) * ST_T;
         const int cnt = min(ST_T, Nb - j0);
-        const float *raw = ring.raw_tile(st) + tile_float_offset(cref + size_t(j0) * 3);
+        const float *raw = ring.raw_copy(st);
         const int npairs = (cnt + 1) >> 1;
         // pass 1: filter the whole tile, remembering which 8-point steps let
         // something through for which query (32 steps per tile)
@@ -671,18 +676,19 @@ knn_lane_kernel(const KnnArgs a) {
 }
 
 template <int QL>
-cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a, int64_t B,
-                            int64_t Q, cudaStream_t stream) {
-    (void)dev;
-    const size_t smem = knn_lane_smem(a.k);
+cudaError_t launch_knn_lane(const KnnArgs &a0, int64_t B0, const KnnArgs &a1,
+                            int64_t B1, cudaStream_t stream) {
+    const size_t smem = knn_lane_smem(a0.k);
     cudaError_t e = cudaFuncSetAttribute(
         knn_lane_kernel<QL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t per_block = KL_QPB;
+    const int64_t Q = std::max<int64_t>(a0.Q, B1 > 0 ? a1.Q : 0);
     dim3 grid(static_cast<unsigned>((Q + per_block - 1) / per_block),
-              static_cast<unsigned>(B));
-    knn_lane_kernel<QL><<<grid, LaneShape<QL>::THREADS, smem, stream>>>(a);
+              static_cast<unsigned>(B0 + B1));
+    knn_lane_kernel<QL><<<grid, LaneShape<QL>::THREADS, smem, stream>>>(a0, a1,
+                                                                          int(B0));
     return cudaGetLastError();
 }
 
@@ -714,11 +720,12 @@ cudaError_t launch_knn_t(const DeviceInfo &dev, const KnnArgs &a0, int64_t B,
 
 }  // namespace
 
-cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
-                       int64_t Q, const float *ref, int64_t N, int k,
-                       const int64_t *q_len, const int64_t *r_len, bool squared,
-                       float *out_dist, int64_t *out_idx,
-                       cudaStream_t stream) {
+namespace {
+
+KnnArgs make_knn_args(const DeviceInfo &dev, const float *query, int64_t Q,
+                      const float *ref, int64_t N, int k, const int64_t *q_len,
+                      const int64_t *r_len, bool squared, float *out_dist,
+                      int64_t *out_idx) {
     KnnArgs a{};
     a.query = query;
     a.ref = ref;
@@ -732,8 +739,40 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
-    if (k <= 16) return launch_knn_lane<2>(dev, a, B, Q, stream);
-    if (k <= 32) return launch_knn_lane<1>(dev, a, B, Q, stream);
+    return a;
+}
+
+}  // namespace
+
+cudaError_t launch_knn_pair(const DeviceInfo &dev, int64_t B, int k, bool squared,
+                            const float *q0, int64_t Q0, const float *r0, int64_t N0,
+                            const int64_t *ql0, const int64_t *rl0, float *d0,
+                            int64_t *i0, const float *q1, int64_t Q1,
+                            const float *r1, int64_t N1, const int64_t *ql1,
+                            const int64_t *rl1, float *d1, int64_t *i1,
+                            cudaStream_t stream) {
+    if (k > 32 || B * 2 > 65535) {
+        cudaError_t e = launch_knn(dev, q0, B, Q0, r0, N0, k, ql0, rl0, squared, d0,
+                                   i0, stream);
+        if (e != cudaSuccess) return e;
+        return launch_knn(dev, q1, B, Q1, r1, N1, k, ql1, rl1, squared, d1, i1,
+                          stream);
+    }
+    const KnnArgs a0 = make_knn_args(dev, q0, Q0, r0, N0, k, ql0, rl0, squared, d0, i0);
+    const KnnArgs a1 = make_knn_args(dev, q1, Q1, r1, N1, k, ql1, rl1, squared, d1, i1);
+    if (k <= 16) return launch_knn_lane<2>(a0, B, a1, B, stream);
+    return launch_knn_lane<1>(a0, B, a1, B, stream);
+}
+
+cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
+                       int64_t Q, const float *ref, int64_t N, int k,
+                       const int64_t *q_len, const int64_t *r_len, bool squared,
+                       float *out_dist, int64_t *out_idx,
+                       cudaStream_t stream) {
+    const KnnArgs a = make_knn_args(dev, query, Q, ref, N, k, q_len, r_len, squared,
+                                    out_dist, out_idx);
+    if (k <= 16) return launch_knn_lane<2>(a, B, a, 0, stream);
+    if (k <= 32) return launch_knn_lane<1>(a, B, a, 0, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
     if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
     return launch_knn_t<8>(dev, a, B, Q, stream);

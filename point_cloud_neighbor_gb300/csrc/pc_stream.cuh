@@ -2,23 +2,28 @@
 // for the lane-per-query kNN and Ball Query kernels.
 //
 // A block has CW consumer warps and one producer warp.  The producer warp
-// streams reference tiles of ST_T points through an ST_STAGES ring:
-//   1. its lane 0 copies the raw tile (x, y, z float32) into the raw buffer of
-//      a stage with TMA (issue_tile of pc_tiles.cuh), up to ST_STAGES tiles
-//      ahead of the consumers;
-//   2. once a raw tile has landed, the whole warp "cooks" it: the centred
-//      coordinates and w' of the filter of pc_filter.cuh, packed for the
-//      paired instructions, two points per 32 bytes:
+// streams reference tiles of ST_T points:
+//   1. its lane 0 copies raw tiles (x, y, z float32) with TMA (issue_tile of
+//      pc_tiles.cuh) into a private ring of ST_RAW_STAGES buffers, up to
+//      ST_RAW_STAGES tiles ahead of its own preparation;
+//   2. once a raw tile has landed and the stage it goes to has been released
+//      by every consumer warp, the whole warp "cooks" it into the stage: the
+//      centred coordinates and w' of the filter of pc_filter.cuh, packed for
+//      the paired instructions, two points per 32 bytes,
 //          cooked[2p]     = (x'_2p, x'_2p+1, y'_2p, y'_2p+1)
-//          cooked[2p + 1] = (z'_2p, z'_2p+1, w'_2p, w'_2p+1)
-//      points past the tile's end get (0, 0, 0, +inf): they pass the filter
-//      only against an infinite threshold and are masked exactly (t' = +inf
-//      there; every other t' is finite or -inf, see pc_filter.cuh);
-//   3. all 32 producer lanes arrive on the stage's `ready` barrier.
-// Consumers wait on `ready`, read the cooked tile (every lane reads the same
-// 16 bytes: shared-memory broadcasts) and, on their rare slow paths, the raw
-// tile; then each consumer warp arrives on `empty`, which the producer waits
-// on before it reuses the stage (raw and cooked).  Every wait is bounded.
+//          cooked[2p + 1] = (z'_2p, z'_2p+1, w'_2p, w'_2p+1),
+//      and a dense copy of the raw coordinates for the exact path; points
+//      past the tile's end get (0, 0, 0, +inf): they pass the filter only
+//      against an infinite threshold and are masked exactly (t' = +inf there;
+//      every other t' is finite or -inf, see pc_filter.cuh);
+//   3. all 32 producer lanes arrive on the stage's `ready` barrier, and the
+//      raw buffer is refilled with the tile ST_RAW_STAGES further on.
+// The raw ring never waits on the consumers, so the producer can run up to
+// ST_STAGES cooked tiles ahead of the slowest consumer warp.  Consumers wait
+// on `ready`, read the cooked tile (every lane reads the same 16 bytes:
+// shared-memory broadcasts) and, on their rare slow paths, the raw copy;
+// then each consumer warp arrives on `empty`, which the producer waits on
+// before it reuses the stage.  Every wait is bounded.
 #pragma once
 
 #include "pc_device.cuh"
@@ -28,45 +33,53 @@
 namespace pcn {
 
 constexpr int ST_T = 256;  // points per tile
-constexpr int ST_STAGES = 4;
+constexpr int ST_STAGES = 4;      // cooked stages (shared with the consumers)
+constexpr int ST_RAW_STAGES = 3;  // TMA landing buffers (producer only)
 constexpr unsigned ST_RAW = tile_buffer_bytes(ST_T);
 constexpr unsigned ST_COOKED = (ST_T / 2) * 32;
+constexpr unsigned ST_COPY = ST_T * 12;  // raw coordinates, dense
+constexpr unsigned ST_STAGE = ST_COOKED + ST_COPY;
 
-static_assert(ST_RAW % 16 == 0, "raw tile buffers stay 16-byte aligned");
+static_assert(ST_RAW % 16 == 0 && ST_STAGE % 16 == 0, "buffers stay 16-byte aligned");
 
 struct StreamRing {
-    float4 *cooked;        // STAGES x ST_T / 2 x 2 float4
-    unsigned char *raw;    // STAGES x ST_RAW bytes
-    uint64_t *raw_full;    // count 1 + transaction bytes
-    uint64_t *ready;       // count 32 (the producer warp)
-    uint64_t *empty;       // count = consumer warps
+    unsigned char *stage;  // ST_STAGES x (cooked, raw copy)
+    unsigned char *raw;    // ST_RAW_STAGES x ST_RAW bytes
+    uint64_t *raw_full;    // [ST_RAW_STAGES] count 1 + transaction bytes
+    uint64_t *ready;       // [ST_STAGES] count 32 (the producer warp)
+    uint64_t *empty;       // [ST_STAGES] count = consumer warps
     __device__ __forceinline__ const float4 *cooked_tile(int s) const {
-        return cooked + size_t(s) * (ST_T / 2) * 2;
+        return reinterpret_cast<const float4 *>(stage + size_t(s) * ST_STAGE);
     }
-    __device__ __forceinline__ float *raw_tile(int s) const {
-        return reinterpret_cast<float *>(raw + size_t(s) * ST_RAW);
+    // x, y, z of point i of the tile at [3 i]
+    __device__ __forceinline__ const float *raw_copy(int s) const {
+        return reinterpret_cast<const float *>(stage + size_t(s) * ST_STAGE + ST_COOKED);
+    }
+    __device__ __forceinline__ float *raw_tile(int r) const {
+        return reinterpret_cast<float *>(raw + size_t(r) * ST_RAW);
     }
 };
 
-// Shared memory of the ring plus 16 bytes of flags (error, stop, warps done).
+// Shared memory of the rings plus 16 bytes of flags (error, stop, warps done).
 __host__ __device__ constexpr size_t stream_smem_bytes() {
-    return size_t(ST_STAGES) * (ST_COOKED + ST_RAW) + 3 * ST_STAGES * 8 + 16;
+    return size_t(ST_STAGES) * ST_STAGE + size_t(ST_RAW_STAGES) * ST_RAW +
+           (ST_RAW_STAGES + 2 * ST_STAGES) * 8 + 16;
 }
 
-// Carve the ring out of `smem` (16-byte aligned); returns the flag words.
+// Carve the rings out of `smem` (16-byte aligned); returns the flag words.
 __device__ __forceinline__ int *stream_carve(unsigned char *smem, StreamRing &r) {
-    r.cooked = reinterpret_cast<float4 *>(smem);
-    r.raw = smem + size_t(ST_STAGES) * ST_COOKED;
-    r.raw_full = reinterpret_cast<uint64_t *>(r.raw + size_t(ST_STAGES) * ST_RAW);
-    r.ready = r.raw_full + ST_STAGES;
+    r.stage = smem;
+    r.raw = smem + size_t(ST_STAGES) * ST_STAGE;
+    r.raw_full = reinterpret_cast<uint64_t *>(r.raw + size_t(ST_RAW_STAGES) * ST_RAW);
+    r.ready = r.raw_full + ST_RAW_STAGES;
     r.empty = r.ready + ST_STAGES;
     return reinterpret_cast<int *>(r.empty + ST_STAGES);
 }
 
 // Called by thread 0 before the block's first __syncthreads.
 __device__ __forceinline__ void stream_init(const StreamRing &r, int consumer_warps) {
+    for (int s = 0; s < ST_RAW_STAGES; ++s) mbar_init(&r.raw_full[s], 1);
     for (int s = 0; s < ST_STAGES; ++s) {
-        mbar_init(&r.raw_full[s], 1);
         mbar_init(&r.ready[s], 32);
         mbar_init(&r.empty[s], consumer_warps);
     }
@@ -96,75 +109,81 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
                                                uint64_t timeout_ns) {
     const int lane = static_cast<int>(lane_id());
     const float inf = __int_as_float(0x7f800000);
-    int issued = 0, cooked = 0;
-    bool ok = true;
-    for (int it = 0; it < ntiles && ok; ++it) {
-        while (issued < ntiles && issued < it + ST_STAGES) {
-            const int st = issued % ST_STAGES;
-            if (issued >= ST_STAGES) {
-                const WaitResult w = warp_wait(
-                    &ring.empty[st], unsigned((issued / ST_STAGES - 1) & 1), stop,
-                    timeout_ns);
-                if (w == WAIT_TIMEOUT && lane == 0) *err = 1;
-                if (w != WAIT_OK) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (__any_sync(0xffffffffu, *stop != 0 || *err != 0)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) {
-                const int j0 = tile_at(issued) * ST_T;
-                issue_tile(ring.raw_tile(st), cref + size_t(j0) * 3,
-                           min(ST_T, N - j0), &ring.raw_full[st]);
-            }
-            ++issued;
+    int issued = 0, landed = 0;
+    if (lane == 0)
+        for (; issued < ntiles && issued < ST_RAW_STAGES; ++issued) {
+            const int j0 = tile_at(issued) * ST_T;
+            issue_tile(ring.raw_tile(issued), cref + size_t(j0) * 3,
+                       min(ST_T, N - j0), &ring.raw_full[issued]);
         }
-        if (!ok) break;
-        const int st = it % ST_STAGES;
-        const WaitResult w = warp_wait(&ring.raw_full[st],
-                                       unsigned((it / ST_STAGES) & 1), nullptr,
-                                       timeout_ns);
-        if (w != WAIT_OK) {
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    for (int it = 0; it < ntiles; ++it) {
+        const int st = it % ST_STAGES, rs = it % ST_RAW_STAGES;
+        const WaitResult wr = warp_wait(&ring.raw_full[rs],
+                                        unsigned((it / ST_RAW_STAGES) & 1), nullptr,
+                                        timeout_ns);
+        if (wr != WAIT_OK) {
             if (lane == 0) *err = 1;
             break;
         }
-        cooked = it + 1;
+        landed = it + 1;
+        if (it >= ST_STAGES) {
+            const WaitResult w = warp_wait(&ring.empty[st],
+                                           unsigned((it / ST_STAGES - 1) & 1), stop,
+                                           timeout_ns);
+            if (w == WAIT_TIMEOUT && lane == 0) *err = 1;
+            if (w != WAIT_OK) break;
+        }
+        if (__any_sync(0xffffffffu, *stop != 0 || *err != 0)) break;
         const int j0 = tile_at(it) * ST_T;
         const int cnt = min(ST_T, N - j0);
-        const float *src = ring.raw_tile(st) + tile_float_offset(cref + size_t(j0) * 3);
-        float4 *dst = ring.cooked + size_t(st) * (ST_T / 2) * 2;
+        const float *src = ring.raw_tile(rs) + tile_float_offset(cref + size_t(j0) * 3);
+        float4 *dst = reinterpret_cast<float4 *>(ring.stage + size_t(st) * ST_STAGE);
+        float2 *copy = reinterpret_cast<float2 *>(ring.stage + size_t(st) * ST_STAGE +
+                                                  ST_COOKED);
 #pragma unroll
         for (int u = 0; u < ST_T / 64; ++u) {
             const int p = lane + 32 * u;
-            float c[2][4];
+            float c[2][4], r[2][3];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int i = 2 * p + h;
                 if (i < cnt) {
-                    float xp = __fsub_rn(src[3 * i], fr.cx);
-                    float yp = __fsub_rn(src[3 * i + 1], fr.cy);
-                    float zp = __fsub_rn(src[3 * i + 2], fr.cz);
+                    r[h][0] = src[3 * i];
+                    r[h][1] = src[3 * i + 1];
+                    r[h][2] = src[3 * i + 2];
+                    float xp = __fsub_rn(r[h][0], fr.cx);
+                    float yp = __fsub_rn(r[h][1], fr.cy);
+                    float zp = __fsub_rn(r[h][2], fr.cz);
                     c[h][3] = filter_ref(xp, yp, zp);
                     c[h][0] = xp;
                     c[h][1] = yp;
                     c[h][2] = zp;
                 } else {
+                    r[h][0] = r[h][1] = r[h][2] = 0.f;
                     c[h][0] = c[h][1] = c[h][2] = 0.f;
                     c[h][3] = inf;
                 }
             }
             dst[2 * p] = make_float4(c[0][0], c[1][0], c[0][1], c[1][1]);
             dst[2 * p + 1] = make_float4(c[0][2], c[1][2], c[0][3], c[1][3]);
+            copy[3 * p] = make_float2(r[0][0], r[0][1]);
+            copy[3 * p + 1] = make_float2(r[0][2], r[1][0]);
+            copy[3 * p + 2] = make_float2(r[1][1], r[1][2]);
         }
+        __syncwarp();  // every lane has read raw buffer rs
+        if (lane == 0 && issued < ntiles) {
+            const int j1 = tile_at(issued) * ST_T;
+            issue_tile(ring.raw_tile(rs), cref + size_t(j1) * 3, min(ST_T, N - j1),
+                       &ring.raw_full[rs]);
+        }
+        if (issued < ntiles) ++issued;
         mbar_arrive(&ring.ready[st]);
     }
     // raw copies issued but never waited for must land before the block exits
-    for (int t = cooked; t < issued; ++t)
-        mbar_wait_bounded(&ring.raw_full[t % ST_STAGES], unsigned((t / ST_STAGES) & 1),
-                          timeout_ns);
+    for (int t = landed; t < issued; ++t)
+        mbar_wait_bounded(&ring.raw_full[t % ST_RAW_STAGES],
+                          unsigned((t / ST_RAW_STAGES) & 1), timeout_ns);
 }
 
 // The filter of one query (broadcast operands a = (-2q', -2q') per axis)
