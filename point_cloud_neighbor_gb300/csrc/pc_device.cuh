@@ -83,6 +83,12 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return r;
 }
 
+// Barrier `id` (1..15) over the first `nthreads` threads that reach it (a
+// multiple of 32: whole warps).
+__device__ __forceinline__ void named_barrier_sync(unsigned id, unsigned nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -438,57 +438,73 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // and replaces the root by every point that beats it (sift-down).  At the end
 // each lane heap-sorts its k entries into ascending (s, j) order.
 // ---------------------------------------------------------------------------
-// QL queries per lane: 2 for k <= 16, 1 above (measured: k = 16 3.23 vs
-// 3.43 ms, k = 32 5.30 vs 6.24 ms, where the heaps limit the blocks per SM)
-constexpr int KL_QPB = 256;  // queries per block
-template <int QL> struct LaneShape {
-    static constexpr int CWARPS = 8 / QL;  // consumer warps per block
-    static constexpr int THREADS = 32 * (CWARPS + 1);
-    static constexpr int MINB = QL == 1 ? 2 : 3;  // blocks per SM (registers)
-};
+// QL queries per lane: 2 for k <= 16, 1 above.  A warp owns a group of
+// 32 * QL consecutive queries.
+//
+// Work layout: one block per SM and wave, with W consumer warps chosen so
+// that every SM gets about the same number of query groups (W = ceil(groups
+// / (SMs x waves))); warp w of block x owns group w * gridDim.x + x of its
+// cloud, so a block's groups are spread over the cloud and the blocks of a
+// launch differ by at most one group.  (Blocks of a fixed 256 queries left
+// 100k queries at 2.57 blocks per SM against 3 slots: the SMs with three
+// blocks set the time.)  One producer serves all W consumer warps.
+constexpr int KL_WMAX = 15;  // consumer warps per block at most (registers)
 
-__host__ __device__ constexpr size_t knn_lane_smem(int k) {
-    return stream_smem_bytes() + size_t(KL_QPB) * size_t(k) * 8;
+__host__ __device__ constexpr size_t knn_lane_smem(int k, int QL, int W) {
+    return stream_smem_bytes() + size_t(W) * 32 * QL * size_t(k) * 8;
 }
 
-// Lexicographic (s, j) "a after b".
-__device__ __forceinline__ bool sj_after(float as, int aj, float bs, int bj) {
-    return as > bs || (as == bs && aj > bj);
+// A heap entry (s, j) as one 64-bit key: the bits of s (a squared distance:
+// +0 .. +inf, never NaN in a heap) above j (0 .. INT_MAX).  For such s the
+// float order is the order of the bit patterns, so the unsigned order of the
+// keys is the lexicographic (s, j) order.  The empty entry is (+inf, INT_MAX).
+__device__ __forceinline__ unsigned long long sj_key(float s, int j) {
+    return (static_cast<unsigned long long>(__float_as_uint(s)) << 32) |
+           static_cast<unsigned>(j);
 }
+__device__ __forceinline__ float key_s(unsigned long long key) {
+    return __uint_as_float(static_cast<unsigned>(key >> 32));
+}
+__device__ __forceinline__ int key_j(unsigned long long key) {
+    return static_cast<int>(static_cast<unsigned>(key));
+}
+constexpr unsigned long long KEY_EMPTY = 0x7f8000007fffffffull;
 
-// Sift (s, j) down from `pos` in the max-heap hs/hj of n entries (stride 32).
-__device__ __forceinline__ void heap_sift(float *hs, int *hj, int n, int pos,
-                                          float s, int j) {
+// Sift `key` down from `pos` in the max-heap h of n keys (stride 32);
+// returns the key then at `pos`.
+__device__ __forceinline__ unsigned long long heap_sift(unsigned long long *h, int n,
+                                                        int pos,
+                                                        unsigned long long key) {
+    unsigned long long top = key;
+    bool first = true;
     for (;;) {
         int c = 2 * pos + 1;
         if (c >= n) break;
-        float cs = hs[c * 32];
-        int cj = hj[c * 32];
+        unsigned long long ck = h[c * 32];
         if (c + 1 < n) {
-            const float ds = hs[(c + 1) * 32];
-            const int dj = hj[(c + 1) * 32];
-            if (sj_after(ds, dj, cs, cj)) {
+            const unsigned long long dk = h[(c + 1) * 32];
+            if (dk > ck) {
                 ++c;
-                cs = ds;
-                cj = dj;
+                ck = dk;
             }
         }
-        if (!sj_after(cs, cj, s, j)) break;
-        hs[pos * 32] = cs;
-        hj[pos * 32] = cj;
+        if (ck <= key) break;
+        h[pos * 32] = ck;
+        if (first) top = ck;
+        first = false;
         pos = c;
     }
-    hs[pos * 32] = s;
-    hj[pos * 32] = j;
+    h[pos * 32] = key;
+    return top;
 }
 
 // Two problems with the same k can share one launch: block rows
 // blockIdx.y < B0 run a0 (cloud blockIdx.y), the rest a1 (cloud
 // blockIdx.y - B0) -- used for the two directions of the Chamfer distance.
 template <int KL_QL>
-__global__ void __launch_bounds__(LaneShape<KL_QL>::THREADS, LaneShape<KL_QL>::MINB)
+__global__ void __launch_bounds__(32 * (KL_WMAX + 1), 1)
 knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
-    constexpr int KL_CWARPS = LaneShape<KL_QL>::CWARPS;
+    constexpr int GQ = 32 * KL_QL;  // queries per group (warp)
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -501,51 +517,60 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     StreamRing ring;
     int *flags = stream_carve(smem, ring);
     int *s_err = flags;
-    float *hs_all = reinterpret_cast<float *>(smem + stream_smem_bytes());
-    int *hj_all = reinterpret_cast<int *>(hs_all + size_t(KL_QPB) * k);
+    unsigned long long *hk_all =
+        reinterpret_cast<unsigned long long *>(smem + stream_smem_bytes());
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
     const int Nb = valid_len(a.r_len, b, a.N);
     const int Qb = valid_len(a.q_len, b, a.Q);
     const int ntiles = (Nb + ST_T - 1) / ST_T;
     const int tstride = scramble_stride(ntiles);
-    const int q0 = blockIdx.x * KL_QPB;
-
-    if (q0 >= Qb) {
-        // every query of this block is past the cloud's valid length
-        const int r1 = min(a.Q, q0 + KL_QPB);
-        const size_t e0 = (size_t(b) * a.Q + q0) * k;
+    const int nwarps = static_cast<int>(blockDim.x >> 5) - 1;  // consumers
+    const int nbx = static_cast<int>(gridDim.x);
+    // this warp's group; the warps whose group holds a valid query (a prefix
+    // of the block's warps) consume the stream
+    const int g = warp * nbx + static_cast<int>(blockIdx.x);
+    const int gvalid = (Qb + GQ - 1) / GQ;
+    const int nact = static_cast<int>(blockIdx.x) < gvalid
+                         ? min(nwarps, (gvalid - static_cast<int>(blockIdx.x) + nbx - 1) / nbx)
+                         : 0;
+    if (warp < nwarps && warp >= nact) {
+        // a group past the cloud's valid length: padding rows only
+        const int r0 = min(a.Q, g * GQ), r1 = min(a.Q, r0 + GQ);
+        const size_t e0 = (size_t(b) * a.Q + r0) * k;
         const size_t e1 = (size_t(b) * a.Q + r1) * k;
-        for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+        for (size_t e = e0 + lane; e < e1; e += 32) {
             a.out_idx[e] = -1;
             a.out_dist[e] = 0.0f;
         }
         return;
     }
+    if (nact == 0) return;  // the producer of a block without consumers
     if (threadIdx.x == 0) {
-        stream_init(ring, KL_CWARPS);
+        stream_init(ring, nact);
         *s_err = 0;
     }
     const FilterFrame fr = filter_frame(cref, min(ST_T, Nb));
-    __syncthreads();
+    // consumers and the producer only (the other warps have left)
+    named_barrier_sync(1, unsigned(32 * (nact + 1)));
 
-    if (warp == KL_CWARPS) {  // producer warp
+    if (warp == nwarps) {  // producer warp
         stream_produce(ring, cref, Nb, ntiles,
                        [&](int it) { return knn_tile_at(it, tstride, ntiles); }, fr,
                        s_err, s_err, a.timeout_ns);
         return;
     }
 
-    // query q of this lane: q0 + (warp * KL_QL + q) * 32 + lane; its heap is
-    // at slot (warp * KL_QL + q) * 32 + lane, entries 32 apart
+    // query q of this lane: g * GQ + q * 32 + lane; its heap is at slot
+    // (warp * KL_QL + q) * 32 + lane, entries 32 apart
     int qi[KL_QL];
     bool valid[KL_QL];
-    float qx[KL_QL], qy[KL_QL], qz[KL_QL], qq[KL_QL], thr[KL_QL], ts[KL_QL];
-    int tj[KL_QL];
+    float qx[KL_QL], qy[KL_QL], qz[KL_QL], qq[KL_QL], thr[KL_QL];
+    unsigned long long tk[KL_QL];  // heap root: the k-th best so far
     float2 ax[KL_QL], ay[KL_QL], az[KL_QL];
 #pragma unroll
     for (int q = 0; q < KL_QL; ++q) {
-        qi[q] = q0 + (warp * KL_QL + q) * 32 + lane;
+        qi[q] = g * GQ + q * 32 + lane;
         valid[q] = qi[q] < Qb;
         qx[q] = qy[q] = qz[q] = 0.f;
         if (valid[q]) {
@@ -561,15 +586,10 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         ax[q] = make_float2(axs, axs);
         ay[q] = make_float2(ays, ays);
         az[q] = make_float2(azs, azs);
-        ts[q] = inf;      // heap root: the k-th best so far
-        tj[q] = INT_MAX;
+        tk[q] = KEY_EMPTY;
         thr[q] = valid[q] ? inf : -inf;
-        float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
-        int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
-        for (int e = 0; e < k; ++e) {
-            hs[e * 32] = inf;
-            hj[e * 32] = INT_MAX;
-        }
+        unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+        for (int e = 0; e < k; ++e) hk[e * 32] = KEY_EMPTY;
     }
 
     bool failed = false;
@@ -591,10 +611,9 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         unsigned pend[KL_QL];
 #pragma unroll
         for (int q = 0; q < KL_QL; ++q) pend[q] = 0;
+#pragma unroll 2
         for (int p = 0, step = 0; p < npairs; p += 4, ++step) {
-            float mn[KL_QL];  // running minimum of t' per query
-#pragma unroll
-            for (int q = 0; q < KL_QL; ++q) mn[q] = inf;
+            float mu[KL_QL][4];  // min of t' over each pair of points
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float4 A = ck[2 * (p + u)];
@@ -605,11 +624,14 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
                                           make_float2(Z.z, Z.w));
                     v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
                     v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
-                    mn[q] = fminf(mn[q], fminf(v.x, v.y));
+                    mu[q][u] = fminf(v.x, v.y);
                 }
             }
 #pragma unroll
-            for (int q = 0; q < KL_QL; ++q) pend[q] |= (mn[q] <= thr[q] ? 1u : 0u) << step;
+            for (int q = 0; q < KL_QL; ++q) {
+                const float mn = fminf(fminf(mu[q][0], mu[q][1]), fminf(mu[q][2], mu[q][3]));
+                pend[q] |= (mn <= thr[q] ? 1u : 0u) << step;
+            }
         }
         // pass 2: the lanes with pending steps process them together (one
         // step per lane per round), exact s32 and heap insertion; thresholds
@@ -617,8 +639,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
 #pragma unroll
         for (int q = 0; q < KL_QL; ++q) {
             if (!valid[q]) pend[q] = 0;
-            float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
-            int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+            unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
             while (__any_sync(FULL, pend[q] != 0)) {
                 if (pend[q] == 0) continue;
                 const int p = 4 * (__ffs(pend[q]) - 1);
@@ -630,12 +651,14 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
                     if (i >= cnt) continue;
                     const float sv = sqdist(qx[q], qy[q], qz[q], raw[3 * i],
                                             raw[3 * i + 1], raw[3 * i + 2]);
-                    const int j = j0 + i;
-                    if (sj_after(ts[q], tj[q], sv, j)) {
-                        heap_sift(hs, hj, k, 0, sv, j);
-                        ts[q] = hs[0];
-                        tj[q] = hj[0];
-                        thr[q] = tj[q] == INT_MAX ? inf : filter_threshold(ts[q], qq[q]);
+                    // s32 >= +0; a NaN s32 has a key above KEY_EMPTY and is
+                    // never accepted
+                    const unsigned long long key = sj_key(sv, j0 + i);
+                    if (key < tk[q]) {
+                        tk[q] = heap_sift(hk, k, 0, key);
+                        thr[q] = key_j(tk[q]) == INT_MAX
+                                     ? inf
+                                     : filter_threshold(key_s(tk[q]), qq[q]);
                     }
                 }
             }
@@ -656,39 +679,50 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
             for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
             continue;
         }
-        float *hs = hs_all + size_t(warp * KL_QL + q) * 32 * k + lane;
-        int *hj = hj_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+        unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
         // heap sort: the largest entry moves to the end, k - 1 times
         for (int n = k - 1; n > 0; --n) {
-            const float s = hs[n * 32];
-            const int j = hj[n * 32];
-            hs[n * 32] = hs[0];
-            hj[n * 32] = hj[0];
-            heap_sift(hs, hj, n, 0, s, j);
+            const unsigned long long key = hk[n * 32];
+            hk[n * 32] = hk[0];
+            heap_sift(hk, n, 0, key);
         }
         const int kv = valid[q] ? min(k, Nb) : 0;
         for (int e = 0; e < k; ++e) {
-            const float sv = hs[e * 32];
-            a.out_idx[row * k + e] = e < kv ? int64_t(hj[e * 32]) : int64_t(-1);
+            const unsigned long long key = hk[e * 32];
+            const float sv = key_s(key);
+            a.out_idx[row * k + e] = e < kv ? int64_t(key_j(key)) : int64_t(-1);
             a.out_dist[row * k + e] = e < kv ? (a.squared ? sv : __fsqrt_rn(sv)) : 0.0f;
         }
     }
 }
 
 template <int QL>
-cudaError_t launch_knn_lane(const KnnArgs &a0, int64_t B0, const KnnArgs &a1,
-                            int64_t B1, cudaStream_t stream) {
-    const size_t smem = knn_lane_smem(a0.k);
+cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0,
+                            const KnnArgs &a1, int64_t B1, cudaStream_t stream) {
+    const int64_t GQ = 32 * QL;
+    const int64_t Q = std::max<int64_t>(a0.Q, B1 > 0 ? a1.Q : 0);
+    const int64_t G = (Q + GQ - 1) / GQ;  // groups per cloud
+    const int64_t total = G * (B0 + B1);
+    if (total == 0) return cudaSuccess;
+    const int64_t nsm = std::max(1, dev.sm_count);
+    // consumer warps per block: shared memory bounds it too (k * 8 bytes per
+    // query); a block per SM and wave
+    const int64_t per_warp = GQ * int64_t(a0.k) * 8;
+    const int64_t wmax = std::max<int64_t>(
+        1, std::min<int64_t>(KL_WMAX, (int64_t(dev.smem_per_block_optin) -
+                                       int64_t(stream_smem_bytes())) / per_warp));
+    const int64_t waves = (total + nsm * wmax - 1) / (nsm * wmax);
+    const int64_t W =
+        std::min(std::min(wmax, G), (total + nsm * waves - 1) / (nsm * waves));
+    const int64_t nbx = (G + W - 1) / W;
+    const size_t smem = knn_lane_smem(a0.k, QL, int(W));
     cudaError_t e = cudaFuncSetAttribute(
         knn_lane_kernel<QL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t per_block = KL_QPB;
-    const int64_t Q = std::max<int64_t>(a0.Q, B1 > 0 ? a1.Q : 0);
-    dim3 grid(static_cast<unsigned>((Q + per_block - 1) / per_block),
-              static_cast<unsigned>(B0 + B1));
-    knn_lane_kernel<QL><<<grid, LaneShape<QL>::THREADS, smem, stream>>>(a0, a1,
-                                                                          int(B0));
+    dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(B0 + B1));
+    knn_lane_kernel<QL><<<grid, unsigned(32 * (W + 1)), smem, stream>>>(a0, a1,
+                                                                        int(B0));
     return cudaGetLastError();
 }
 
@@ -760,8 +794,8 @@ cudaError_t launch_knn_pair(const DeviceInfo &dev, int64_t B, int k, bool square
     }
     const KnnArgs a0 = make_knn_args(dev, q0, Q0, r0, N0, k, ql0, rl0, squared, d0, i0);
     const KnnArgs a1 = make_knn_args(dev, q1, Q1, r1, N1, k, ql1, rl1, squared, d1, i1);
-    if (k <= 16) return launch_knn_lane<2>(a0, B, a1, B, stream);
-    return launch_knn_lane<1>(a0, B, a1, B, stream);
+    if (k <= 16) return launch_knn_lane<2>(dev, a0, B, a1, B, stream);
+    return launch_knn_lane<1>(dev, a0, B, a1, B, stream);
 }
 
 cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
@@ -771,8 +805,8 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
                        cudaStream_t stream) {
     const KnnArgs a = make_knn_args(dev, query, Q, ref, N, k, q_len, r_len, squared,
                                     out_dist, out_idx);
-    if (k <= 16) return launch_knn_lane<2>(a, B, a, 0, stream);
-    if (k <= 32) return launch_knn_lane<1>(a, B, a, 0, stream);
+    if (k <= 16) return launch_knn_lane<2>(dev, a, B, a, 0, stream);
+    if (k <= 32) return launch_knn_lane<1>(dev, a, B, a, 0, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
     if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
     return launch_knn_t<8>(dev, a, B, Q, stream);

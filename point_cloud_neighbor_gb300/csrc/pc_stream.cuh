@@ -33,7 +33,7 @@
 namespace pcn {
 
 constexpr int ST_T = 256;  // points per tile
-constexpr int ST_STAGES = 4;      // cooked stages (shared with the consumers)
+constexpr int ST_STAGES = 8;      // cooked stages (shared with the consumers)
 constexpr int ST_RAW_STAGES = 3;  // TMA landing buffers (producer only)
 constexpr unsigned ST_RAW = tile_buffer_bytes(ST_T);
 constexpr unsigned ST_COOKED = (ST_T / 2) * 32;
