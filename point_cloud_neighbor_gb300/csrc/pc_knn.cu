@@ -448,7 +448,8 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // launch differ by at most one group.  (Blocks of a fixed 256 queries left
 // 100k queries at 2.57 blocks per SM against 3 slots: the SMs with three
 // blocks set the time.)  One producer serves all W consumer warps.
-constexpr int KL_WMAX = 15;  // consumer warps per block at most (registers)
+// consumer warps per block at most (one block per SM: registers)
+__host__ __device__ constexpr int kl_wmax(int QL) { return QL == 1 ? 15 : 12; }
 
 __host__ __device__ constexpr size_t knn_lane_smem(int k, int QL, int W) {
     return stream_smem_bytes() + size_t(W) * 32 * QL * size_t(k) * 8;
@@ -502,9 +503,13 @@ __device__ __forceinline__ unsigned long long heap_sift(unsigned long long *h, i
 // blockIdx.y < B0 run a0 (cloud blockIdx.y), the rest a1 (cloud
 // blockIdx.y - B0) -- used for the two directions of the Chamfer distance.
 template <int KL_QL>
-__global__ void __launch_bounds__(32 * (KL_WMAX + 1), 1)
+__global__ void __launch_bounds__(32 * (kl_wmax(KL_QL) + 1), 1)
 knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     constexpr int GQ = 32 * KL_QL;  // queries per group (warp)
+    // cooked-tile swizzle bits and steps per hot-loop iteration: 3 and 8 for
+    // one query per lane, 2 and 4 for two (registers)
+    constexpr int KL_SB = KL_QL == 1 ? 3 : 2;
+    constexpr int KL_ROW = 1 << KL_SB;
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -555,7 +560,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     named_barrier_sync(1, unsigned(32 * (nact + 1)));
 
     if (warp == nwarps) {  // producer warp
-        stream_produce(ring, cref, Nb, ntiles,
+        stream_produce<KL_SB>(ring, cref, Nb, ntiles,
                        [&](int it) { return knn_tile_at(it, tstride, ntiles); }, fr,
                        s_err, s_err, a.timeout_ns);
         return;
@@ -604,33 +609,42 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         const float4 *ck = ring.cooked_tile(st);
         const int j0 = knn_tile_at(it, tstride, ntiles) * ST_T;
         const int cnt = min(ST_T, Nb - j0);
-        const float *raw = ring.raw_copy(st);
-        const int npairs = (cnt + 1) >> 1;
+        const float4 *raw = ring.raw_copy(st);
+        // whole rows of 8 steps (64 points); the cooked tile is padded to
+        // ST_T points with points that pass only an infinite threshold
+        const int nsteps = ((cnt + 63) >> 6) << 3;
+        static_assert(8 % KL_ROW == 0, "rows of steps divide 8");
         // pass 1: filter the whole tile, remembering which 8-point steps let
         // something through for which query (32 steps per tile)
         unsigned pend[KL_QL];
 #pragma unroll
         for (int q = 0; q < KL_QL; ++q) pend[q] = 0;
-#pragma unroll 2
-        for (int p = 0, step = 0; p < npairs; p += 4, ++step) {
-            float mu[KL_QL][4];  // min of t' over each pair of points
+        for (int s0 = 0; s0 < nsteps; s0 += KL_ROW) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float4 A = ck[2 * (p + u)];
-                const float4 Z = ck[2 * (p + u) + 1];
+            for (int ss = 0; ss < KL_ROW; ++ss) {
+                const int step = s0 + ss;
+                const float4 *row = ck + 8 * step;
+                const int x = ss << (3 - KL_SB);  // the row's slot swizzle
+                float mu[KL_QL][4];  // min of t' over each pair of points
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 A = row[(2 * u) ^ x];
+                    const float4 Z = row[(2 * u + 1) ^ x];
+#pragma unroll
+                    for (int q = 0; q < KL_QL; ++q) {
+                        float2 v = __ffma2_rn(make_float2(A.x, A.y), ax[q],
+                                              make_float2(Z.z, Z.w));
+                        v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
+                        v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
+                        mu[q][u] = fminf(v.x, v.y);
+                    }
+                }
 #pragma unroll
                 for (int q = 0; q < KL_QL; ++q) {
-                    float2 v = __ffma2_rn(make_float2(A.x, A.y), ax[q],
-                                          make_float2(Z.z, Z.w));
-                    v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
-                    v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
-                    mu[q][u] = fminf(v.x, v.y);
+                    const float mn =
+                        fminf(fminf(mu[q][0], mu[q][1]), fminf(mu[q][2], mu[q][3]));
+                    pend[q] |= (mn <= thr[q] ? 1u : 0u) << step;
                 }
-            }
-#pragma unroll
-            for (int q = 0; q < KL_QL; ++q) {
-                const float mn = fminf(fminf(mu[q][0], mu[q][1]), fminf(mu[q][2], mu[q][3]));
-                pend[q] |= (mn <= thr[q] ? 1u : 0u) << step;
             }
         }
         // pass 2: the lanes with pending steps process them together (one
@@ -644,13 +658,13 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
                 if (pend[q] == 0) continue;
                 const int p = 4 * (__ffs(pend[q]) - 1);
                 pend[q] &= pend[q] - 1;
-                unsigned m = stream_mask<4>(ck, p, ax[q], ay[q], az[q], thr[q]);
+                unsigned m = stream_mask<KL_SB, 4>(ck, p, ax[q], ay[q], az[q], thr[q]);
                 while (m) {
                     const int i = 2 * p + __ffs(m) - 1;
                     m &= m - 1;
                     if (i >= cnt) continue;
-                    const float sv = sqdist(qx[q], qy[q], qz[q], raw[3 * i],
-                                            raw[3 * i + 1], raw[3 * i + 2]);
+                    const float4 P = raw[raw_slot(i)];
+                    const float sv = sqdist(qx[q], qy[q], qz[q], P.x, P.y, P.z);
                     // s32 >= +0; a NaN s32 has a key above KEY_EMPTY and is
                     // never accepted
                     const unsigned long long key = sj_key(sv, j0 + i);
@@ -709,7 +723,7 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
     // query); a block per SM and wave
     const int64_t per_warp = GQ * int64_t(a0.k) * 8;
     const int64_t wmax = std::max<int64_t>(
-        1, std::min<int64_t>(KL_WMAX, (int64_t(dev.smem_per_block_optin) -
+        1, std::min<int64_t>(kl_wmax(QL), (int64_t(dev.smem_per_block_optin) -
                                        int64_t(stream_smem_bytes())) / per_warp));
     const int64_t waves = (total + nsm * wmax - 1) / (nsm * wmax);
     const int64_t W =

@@ -9,17 +9,27 @@
 //   2. once a raw tile has landed and the stage it goes to has been released
 //      by every consumer warp, the whole warp "cooks" it into the stage: the
 //      centred coordinates and w' of the filter of pc_filter.cuh, packed for
-//      the paired instructions, two points per 32 bytes,
-//          cooked[2p]     = (x'_2p, x'_2p+1, y'_2p, y'_2p+1)
-//          cooked[2p + 1] = (z'_2p, z'_2p+1, w'_2p, w'_2p+1),
-//      and a dense copy of the raw coordinates for the exact path; points
-//      past the tile's end get (0, 0, 0, +inf): they pass the filter only
-//      against an infinite threshold and are masked exactly (t' = +inf there;
-//      every other t' is finite or -inf, see pc_filter.cuh);
+//      the paired instructions, two points (a "pair" p) per 32 bytes,
+//          A(p) = (x'_2p, x'_2p+1, y'_2p, y'_2p+1)
+//          Z(p) = (z'_2p, z'_2p+1, w'_2p, w'_2p+1),
+//      and a copy of the raw coordinates (x, y, z, 0) per point for the
+//      exact path; points past the tile's end get (0, 0, 0, +inf): they pass
+//      the filter only against an infinite threshold and are masked exactly
+//      (t' = +inf there; every other t' is finite or -inf, see pc_filter.cuh);
 //   3. all 32 producer lanes arrive on the stage's `ready` barrier, and the
 //      raw buffer is refilled with the tile ST_RAW_STAGES further on.
 // The raw ring never waits on the consumers, so the producer can run up to
-// ST_STAGES cooked tiles ahead of the slowest consumer warp.  Consumers wait
+// ST_STAGES cooked tiles ahead of the slowest consumer warp.
+//
+// Layout of a stage: 16-byte slots in rows of 8 (128 bytes, one pass over
+// the 32 banks).  Step s = the 8 points 8s .. 8s + 7 = pairs 4s .. 4s + 3;
+// its cooked row holds A and Z of pair 4s + u at slots 2u and 2u + 1, XORed
+// with the low SB bits of s (shifted to the top of the 3-bit slot index), and
+// its raw row point 8s + r at slot r XOR (s & 7).  A warp whose lanes all
+// read step s gets broadcasts either way; lanes reading the same slot of
+// different steps (the per-lane slow paths) land on 2^SB different bank
+// groups instead of one.  The consumers' hot loop walks 2^SB steps per
+// iteration so that its slot offsets are compile-time constants.  Consumers wait
 // on `ready`, read the cooked tile (every lane reads the same 16 bytes:
 // shared-memory broadcasts) and, on their rare slow paths, the raw copy;
 // then each consumer warp arrives on `empty`, which the producer waits on
@@ -37,7 +47,7 @@ constexpr int ST_STAGES = 8;      // cooked stages (shared with the consumers)
 constexpr int ST_RAW_STAGES = 3;  // TMA landing buffers (producer only)
 constexpr unsigned ST_RAW = tile_buffer_bytes(ST_T);
 constexpr unsigned ST_COOKED = (ST_T / 2) * 32;
-constexpr unsigned ST_COPY = ST_T * 12;  // raw coordinates, dense
+constexpr unsigned ST_COPY = ST_T * 16;  // raw coordinates, 16 bytes a point
 constexpr unsigned ST_STAGE = ST_COOKED + ST_COPY;
 
 static_assert(ST_RAW % 16 == 0 && ST_STAGE % 16 == 0, "buffers stay 16-byte aligned");
@@ -51,9 +61,9 @@ struct StreamRing {
     __device__ __forceinline__ const float4 *cooked_tile(int s) const {
         return reinterpret_cast<const float4 *>(stage + size_t(s) * ST_STAGE);
     }
-    // x, y, z of point i of the tile at [3 i]
-    __device__ __forceinline__ const float *raw_copy(int s) const {
-        return reinterpret_cast<const float *>(stage + size_t(s) * ST_STAGE + ST_COOKED);
+    // (x, y, z, 0) of point i of the tile at [raw_slot(i)]
+    __device__ __forceinline__ const float4 *raw_copy(int s) const {
+        return reinterpret_cast<const float4 *>(stage + size_t(s) * ST_STAGE + ST_COOKED);
     }
     __device__ __forceinline__ float *raw_tile(int r) const {
         return reinterpret_cast<float *>(raw + size_t(r) * ST_RAW);
@@ -74,6 +84,18 @@ __device__ __forceinline__ int *stream_carve(unsigned char *smem, StreamRing &r)
     r.ready = r.raw_full + ST_RAW_STAGES;
     r.empty = r.ready + ST_STAGES;
     return reinterpret_cast<int *>(r.empty + ST_STAGES);
+}
+
+// Slot of A (h = 0) or Z (h = 1) of pair p in a cooked tile (SB = 2 or 3
+// swizzle bits), and of point i in a raw copy.
+template <int SB>
+__host__ __device__ __forceinline__ int cooked_slot(int p, int h) {
+    static_assert(SB >= 1 && SB <= 3, "1 to 3 swizzle bits");
+    return ((p >> 2) << 3) |
+           ((((p & 3) << 1) | h) ^ (((p >> 2) & ((1 << SB) - 1)) << (3 - SB)));
+}
+__host__ __device__ __forceinline__ int raw_slot(int i) {
+    return (i & ~7) | ((i & 7) ^ ((i >> 3) & 7));
 }
 
 // Called by thread 0 before the block's first __syncthreads.
@@ -99,7 +121,7 @@ __device__ __forceinline__ WaitResult warp_wait(uint64_t *bar, unsigned parity,
 // the cloud at `cref` (N valid points).  Stops when *stop becomes non-zero;
 // a timeout raises *err.  Before returning it waits (bounded) for every raw
 // copy it issued, so none is in flight when the block exits.
-template <class TileAt>
+template <int SB, class TileAt>
 __device__ __forceinline__ void stream_produce(const StreamRing &ring,
                                                const float *cref, int N,
                                                int ntiles, TileAt tile_at,
@@ -139,7 +161,7 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
         const int cnt = min(ST_T, N - j0);
         const float *src = ring.raw_tile(rs) + tile_float_offset(cref + size_t(j0) * 3);
         float4 *dst = reinterpret_cast<float4 *>(ring.stage + size_t(st) * ST_STAGE);
-        float2 *copy = reinterpret_cast<float2 *>(ring.stage + size_t(st) * ST_STAGE +
+        float4 *copy = reinterpret_cast<float4 *>(ring.stage + size_t(st) * ST_STAGE +
                                                   ST_COOKED);
 #pragma unroll
         for (int u = 0; u < ST_T / 64; ++u) {
@@ -165,11 +187,10 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
                     c[h][3] = inf;
                 }
             }
-            dst[2 * p] = make_float4(c[0][0], c[1][0], c[0][1], c[1][1]);
-            dst[2 * p + 1] = make_float4(c[0][2], c[1][2], c[0][3], c[1][3]);
-            copy[3 * p] = make_float2(r[0][0], r[0][1]);
-            copy[3 * p + 1] = make_float2(r[0][2], r[1][0]);
-            copy[3 * p + 2] = make_float2(r[1][1], r[1][2]);
+            dst[cooked_slot<SB>(p, 0)] = make_float4(c[0][0], c[1][0], c[0][1], c[1][1]);
+            dst[cooked_slot<SB>(p, 1)] = make_float4(c[0][2], c[1][2], c[0][3], c[1][3]);
+            copy[raw_slot(2 * p)] = make_float4(r[0][0], r[0][1], r[0][2], 0.f);
+            copy[raw_slot(2 * p + 1)] = make_float4(r[1][0], r[1][1], r[1][2], 0.f);
         }
         __syncwarp();  // every lane has read raw buffer rs
         if (lane == 0 && issued < ntiles) {
@@ -189,14 +210,14 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
 // The filter of one query (broadcast operands a = (-2q', -2q') per axis)
 // against points 2p .. 2p + 2v - 1 of a cooked tile: bit h of the result
 // (h < 2v) is set when point 2p + h may satisfy the selection bound.
-template <int V>
+template <int SB, int V>
 __device__ __forceinline__ unsigned stream_mask(const float4 *ck, int p, float2 ax,
                                                 float2 ay, float2 az, float thr) {
     unsigned m = 0;
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-        const float4 A = ck[2 * (p + u)];
-        const float4 Z = ck[2 * (p + u) + 1];
+        const float4 A = ck[cooked_slot<SB>(p + u, 0)];
+        const float4 Z = ck[cooked_slot<SB>(p + u, 1)];
         float2 v = __ffma2_rn(make_float2(A.x, A.y), ax, make_float2(Z.z, Z.w));
         v = __ffma2_rn(make_float2(A.z, A.w), ay, v);
         v = __ffma2_rn(make_float2(Z.x, Z.y), az, v);
@@ -204,23 +225,6 @@ __device__ __forceinline__ unsigned stream_mask(const float4 *ck, int p, float2 
         m |= (v.y <= thr ? 1u : 0u) << (2 * u + 1);
     }
     return m;
-}
-
-// The hot-loop form: does any of the 2V points pass?
-template <int V>
-__device__ __forceinline__ bool stream_any(const float4 *ck, int p, float2 ax,
-                                           float2 ay, float2 az, float thr) {
-    float m = __int_as_float(0x7f800000);
-#pragma unroll
-    for (int u = 0; u < V; ++u) {
-        const float4 A = ck[2 * (p + u)];
-        const float4 Z = ck[2 * (p + u) + 1];
-        float2 v = __ffma2_rn(make_float2(A.x, A.y), ax, make_float2(Z.z, Z.w));
-        v = __ffma2_rn(make_float2(A.z, A.w), ay, v);
-        v = __ffma2_rn(make_float2(Z.x, Z.y), az, v);
-        m = fminf(m, fminf(v.x, v.y));
-    }
-    return m <= thr;
 }
 
 }  // namespace pcn
