@@ -110,9 +110,11 @@ struct FilterFrame {
     float cx, cy, cz;
 };
 
-// Centre of the bounding box of points [0, n) of `cloud` (n <= 256 is read),
-// computed by one full warp; (0, 0, 0) for an empty cloud.
-__device__ __forceinline__ FilterFrame filter_frame(const float *cloud, int n) {
+// Centre of the bounding box of points [0, n) of `cloud` (n <= 256 is read;
+// point i at cloud[stride * i]), computed by one full warp; (0, 0, 0) for an
+// empty cloud.
+__device__ __forceinline__ FilterFrame filter_frame(const float *cloud, int n,
+                                                    int stride = 3) {
     const unsigned full = 0xffffffffu;
     const int lane = static_cast<int>(lane_id());
     const float inf = __int_as_float(0x7f800000);
@@ -121,7 +123,7 @@ __device__ __forceinline__ FilterFrame filter_frame(const float *cloud, int n) {
     for (int i = lane; i < m; i += 32) {
 #pragma unroll
         for (int a = 0; a < 3; ++a) {
-            const float v = cloud[size_t(i) * 3 + a];
+            const float v = cloud[size_t(i) * stride + a];
             lo[a] = fminf(lo[a], v);
             hi[a] = fmaxf(hi[a], v);
         }

@@ -65,7 +65,38 @@ struct KnnArgs {
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
+    // spatial order (lane kernel, ORDERED): per cloud the valid references
+    // and queries as 16-byte points (x, y, z, original index bits) sorted by
+    // cell code, the starts of the reference cells and the cell frame
+    const float *sref;    // [B][N] x 4
+    const float *squery;  // [B][Q] x 4 (== sref for a query set equal to ref)
+    const int *cstart;    // [B][MC_CELLS + 1]
+    const float *cframe;  // [B][8]: lo x, y, z, scale x, y, z
 };
+
+// Cell codes of the spatial order: MC_BITS bits per axis, interleaved
+// (Morton order), so that a run of consecutive cells is a compact block.
+constexpr int MC_BITS = 5;
+constexpr int MC_CELLS = 1 << (3 * MC_BITS);
+
+__device__ __forceinline__ unsigned mc_spread(unsigned v) {  // 5 bits -> every 3rd
+    unsigned r = 0;
+#pragma unroll
+    for (int i = 0; i < MC_BITS; ++i) r |= ((v >> i) & 1u) << (3 * i);
+    return r;
+}
+
+// Code of (x, y, z) in the frame f (lo, scale); coordinates outside the
+// frame or NaN go to the nearest edge cell (any cell is correct: the code
+// only orders the points).
+__device__ __forceinline__ unsigned mc_code(const float *f, float x, float y, float z) {
+    const int hi = (1 << MC_BITS) - 1;
+    const int cx = min(hi, max(0, __float2int_rz(__fmul_rn(__fsub_rn(x, f[0]), f[3]))));
+    const int cy = min(hi, max(0, __float2int_rz(__fmul_rn(__fsub_rn(y, f[1]), f[4]))));
+    const int cz = min(hi, max(0, __float2int_rz(__fmul_rn(__fsub_rn(z, f[2]), f[5]))));
+    return mc_spread(unsigned(cx)) | (mc_spread(unsigned(cy)) << 1) |
+           (mc_spread(unsigned(cz)) << 2);
+}
 
 // One query in shared memory: the filter constants duplicated so that the
 // halves are packed operands, and the raw coordinates for the exact path.
@@ -502,7 +533,15 @@ __device__ __forceinline__ unsigned long long heap_sift(unsigned long long *h, i
 // Two problems with the same k can share one launch: block rows
 // blockIdx.y < B0 run a0 (cloud blockIdx.y), the rest a1 (cloud
 // blockIdx.y - B0) -- used for the two directions of the Chamfer distance.
-template <int KL_QL>
+//
+// ORDERED: the clouds come in the spatial order of the cell codes (sref,
+// squery); a block owns consecutive query groups (a compact region) and
+// visits the reference tiles outwards from the tile where its region's
+// middle query would sit (home, home + 1, home - 1, ...), so the k best
+// (s, j) are found in the first few tiles and the later tiles rarely let a
+// pair through.  Keys carry the original indices, so the result is that of
+// the input order.
+template <int KL_QL, bool ORDERED>
 __global__ void __launch_bounds__(32 * (kl_wmax(KL_QL) + 1), 1)
 knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     constexpr int GQ = 32 * KL_QL;  // queries per group (warp)
@@ -525,21 +564,32 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     unsigned long long *hk_all =
         reinterpret_cast<unsigned long long *>(smem + stream_smem_bytes());
 
-    const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
+    const float *cref = ORDERED ? a.sref + size_t(b) * size_t(a.N) * 4
+                                : a.ref + size_t(b) * size_t(a.N) * 3;
     const int Nb = valid_len(a.r_len, b, a.N);
     const int Qb = valid_len(a.q_len, b, a.Q);
     const int ntiles = (Nb + ST_T - 1) / ST_T;
     const int tstride = scramble_stride(ntiles);
     const int nwarps = static_cast<int>(blockDim.x >> 5) - 1;  // consumers
     const int nbx = static_cast<int>(gridDim.x);
-    // this warp's group; the warps whose group holds a valid query (a prefix
-    // of the block's warps) consume the stream
-    const int g = warp * nbx + static_cast<int>(blockIdx.x);
+    const int bx = static_cast<int>(blockIdx.x);
+    // this warp's group (ORDERED: consecutive groups per block, else strided
+    // over the cloud); the warps whose group holds a valid query (a prefix of
+    // the block's warps) consume the stream
+    const int g = ORDERED ? bx * nwarps + warp : warp * nbx + bx;
     const int gvalid = (Qb + GQ - 1) / GQ;
-    const int nact = static_cast<int>(blockIdx.x) < gvalid
-                         ? min(nwarps, (gvalid - static_cast<int>(blockIdx.x) + nbx - 1) / nbx)
-                         : 0;
-    if (warp < nwarps && warp >= nact) {
+    const int nact = ORDERED ? max(0, min(nwarps, gvalid - bx * nwarps))
+                             : (bx < gvalid ? min(nwarps, (gvalid - bx + nbx - 1) / nbx) : 0);
+    if (ORDERED) {
+        // rows past the cloud's valid length: padding, spread over the blocks
+        if (warp == 0)
+            for (int r = Qb + bx; r < a.Q; r += nbx)
+                for (int e = lane; e < k; e += 32) {
+                    a.out_idx[(size_t(b) * a.Q + r) * k + e] = -1;
+                    a.out_dist[(size_t(b) * a.Q + r) * k + e] = 0.0f;
+                }
+        if (warp < nwarps && warp >= nact) return;
+    } else if (warp < nwarps && warp >= nact) {
         // a group past the cloud's valid length: padding rows only
         const int r0 = min(a.Q, g * GQ), r1 = min(a.Q, r0 + GQ);
         const size_t e0 = (size_t(b) * a.Q + r0) * k;
@@ -555,34 +605,67 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         stream_init(ring, nact);
         *s_err = 0;
     }
-    const FilterFrame fr = filter_frame(cref, min(ST_T, Nb));
+    // the filter's centre from up to 256 points spread over the cloud in
+    // input order (the first points of a spatially sorted cloud would all
+    // sit in one corner)
+    const int fstep = max(1, Nb / ST_T);
+    const FilterFrame fr = filter_frame(a.ref + size_t(b) * size_t(a.N) * 3,
+                                        min(ST_T, Nb), 3 * fstep);
+    // ORDERED: the home tile, where the middle query of the block's region
+    // would sit among the references
+    int home = 0;
+    if (ORDERED && ntiles > 0) {
+        const int pm = min(Qb - 1, bx * nwarps * GQ + (nact * GQ) / 2);
+        const float *qm = a.squery + (size_t(b) * a.Q + pm) * 4;
+        const unsigned code = mc_code(a.cframe + size_t(b) * 8, qm[0], qm[1], qm[2]);
+        home = min(ntiles - 1, a.cstart[size_t(b) * (MC_CELLS + 1) + code] / ST_T);
+    }
     // consumers and the producer only (the other warps have left)
     named_barrier_sync(1, unsigned(32 * (nact + 1)));
+    // tile visited at step `it`: ORDERED outwards from home, else scrambled
+    auto tile_at = [&](int it) {
+        if (ORDERED) {
+            const int off = (it & 1) ? (it + 1) >> 1 : -(it >> 1);
+            int t = (home + off) % ntiles;
+            return t < 0 ? t + ntiles : t;
+        }
+        return knn_tile_at(it, tstride, ntiles);
+    };
 
     if (warp == nwarps) {  // producer warp
-        stream_produce<KL_SB>(ring, cref, Nb, ntiles,
-                       [&](int it) { return knn_tile_at(it, tstride, ntiles); }, fr,
-                       s_err, s_err, a.timeout_ns);
+        stream_produce<KL_SB, ORDERED>(ring, cref, Nb, ntiles, tile_at, fr, s_err, s_err,
+                                       a.timeout_ns);
         return;
     }
 
     // query q of this lane: g * GQ + q * 32 + lane; its heap is at slot
     // (warp * KL_QL + q) * 32 + lane, entries 32 apart
-    int qi[KL_QL];
+    int qi[KL_QL], orow[KL_QL];  // position in the query set, output row
     bool valid[KL_QL];
     float qx[KL_QL], qy[KL_QL], qz[KL_QL], qq[KL_QL], thr[KL_QL];
+    float thr0[KL_QL];  // threshold of the seed bound (below)
     unsigned long long tk[KL_QL];  // heap root: the k-th best so far
     float2 ax[KL_QL], ay[KL_QL], az[KL_QL];
 #pragma unroll
     for (int q = 0; q < KL_QL; ++q) {
         qi[q] = g * GQ + q * 32 + lane;
         valid[q] = qi[q] < Qb;
+        orow[q] = qi[q];
         qx[q] = qy[q] = qz[q] = 0.f;
         if (valid[q]) {
-            const float *p = a.query + (size_t(b) * a.Q + qi[q]) * 3;
-            qx[q] = p[0];
-            qy[q] = p[1];
-            qz[q] = p[2];
+            if (ORDERED) {
+                const float4 p = reinterpret_cast<const float4 *>(
+                    a.squery)[size_t(b) * a.Q + qi[q]];
+                qx[q] = p.x;
+                qy[q] = p.y;
+                qz[q] = p.z;
+                orow[q] = __float_as_int(p.w);
+            } else {
+                const float *p = a.query + (size_t(b) * a.Q + qi[q]) * 3;
+                qx[q] = p[0];
+                qy[q] = p[1];
+                qz[q] = p[2];
+            }
         }
         const float xp = __fsub_rn(qx[q], fr.cx), yp = __fsub_rn(qy[q], fr.cy),
                     zp = __fsub_rn(qz[q], fr.cz);
@@ -592,7 +675,39 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         ay[q] = make_float2(ays, ays);
         az[q] = make_float2(azs, azs);
         tk[q] = KEY_EMPTY;
-        thr[q] = valid[q] ? inf : -inf;
+        // ORDERED: a seed bound tau0 >= the k-th smallest s32 of the query,
+        // from the 32 references around its place in the spatial order:
+        // split into k groups, the largest of the groups' smallest s32 is
+        // the s32 of one of k distinct references, so at least k references
+        // have s32 <= tau0.  Until the heap is full the filter threshold is
+        // that of tau0 instead of +inf (the heap then fills with near
+        // references only); afterwards the smaller of the two.
+        float tau0 = inf;
+        if (ORDERED && valid[q] && Nb >= 32) {
+            const int pos = (a.squery == a.sref && a.Q == a.N && a.q_len == a.r_len)
+                                ? qi[q]
+                                : a.cstart[size_t(b) * (MC_CELLS + 1) +
+                                           mc_code(a.cframe + size_t(b) * 8, qx[q],
+                                                   qy[q], qz[q])];
+            const int p0 = min(max(pos - 16, 0), Nb - 32);
+            const float4 *w4 = reinterpret_cast<const float4 *>(cref) + p0;
+            const int gs = 32 / k;  // group size (k groups)
+            float worst = 0.0f, gm = inf;
+            bool bad = false;
+#pragma unroll 8
+            for (int t = 0; t < 32; ++t) {
+                const float4 r = w4[t];
+                gm = fminf(gm, sqdist(qx[q], qy[q], qz[q], r.x, r.y, r.z));
+                if (t % gs == gs - 1 && t / gs < k) {
+                    bad = bad || !(gm <= inf);  // a group of NaN s32 only
+                    worst = fmaxf(worst, gm);
+                    gm = inf;
+                }
+            }
+            tau0 = bad ? inf : worst;
+        }
+        thr0[q] = valid[q] ? filter_threshold(tau0, qq[q]) : -inf;
+        thr[q] = thr0[q];
         unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
         for (int e = 0; e < k; ++e) hk[e * 32] = KEY_EMPTY;
     }
@@ -607,7 +722,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
             break;
         }
         const float4 *ck = ring.cooked_tile(st);
-        const int j0 = knn_tile_at(it, tstride, ntiles) * ST_T;
+        const int j0 = tile_at(it) * ST_T;
         const int cnt = min(ST_T, Nb - j0);
         const float4 *raw = ring.raw_copy(st);
         // whole rows of 8 steps (64 points); the cooked tile is padded to
@@ -667,12 +782,13 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
                     const float sv = sqdist(qx[q], qy[q], qz[q], P.x, P.y, P.z);
                     // s32 >= +0; a NaN s32 has a key above KEY_EMPTY and is
                     // never accepted
-                    const unsigned long long key = sj_key(sv, j0 + i);
+                    const unsigned long long key =
+                        sj_key(sv, ORDERED ? __float_as_int(P.w) : j0 + i);
                     if (key < tk[q]) {
                         tk[q] = heap_sift(hk, k, 0, key);
-                        thr[q] = key_j(tk[q]) == INT_MAX
-                                     ? inf
-                                     : filter_threshold(key_s(tk[q]), qq[q]);
+                        if (key_j(tk[q]) != INT_MAX)
+                            thr[q] = fminf(thr0[q],
+                                           filter_threshold(key_s(tk[q]), qq[q]));
                     }
                 }
             }
@@ -687,8 +803,8 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     }
 #pragma unroll
     for (int q = 0; q < KL_QL; ++q) {
-        if (qi[q] >= a.Q) continue;
-        const size_t row = size_t(b) * a.Q + qi[q];
+        if (qi[q] >= a.Q || (ORDERED && !valid[q])) continue;
+        const size_t row = size_t(b) * a.Q + orow[q];
         if (failed) {
             for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
             continue;
@@ -710,7 +826,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     }
 }
 
-template <int QL>
+template <int QL, bool ORDERED = false>
 cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0,
                             const KnnArgs &a1, int64_t B1, cudaStream_t stream) {
     const int64_t GQ = 32 * QL;
@@ -731,13 +847,194 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
     const int64_t nbx = (G + W - 1) / W;
     const size_t smem = knn_lane_smem(a0.k, QL, int(W));
     cudaError_t e = cudaFuncSetAttribute(
-        knn_lane_kernel<QL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        knn_lane_kernel<QL, ORDERED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(B0 + B1));
-    knn_lane_kernel<QL><<<grid, unsigned(32 * (W + 1)), smem, stream>>>(a0, a1,
-                                                                        int(B0));
+    knn_lane_kernel<QL, ORDERED>
+        <<<grid, unsigned(32 * (W + 1)), smem, stream>>>(a0, a1, int(B0));
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// The spatial order of the ORDERED lane kernel, per cloud:
+//   1. frame: bounding box of (up to) 4096 valid references spread evenly
+//      over the cloud (whatever its storage order), and 2^MC_BITS cells per
+//      axis over it;
+//   2. count the valid references per cell code; exclusive scan;
+//   3. scatter them as (x, y, z, original index) in code order (the order
+//      within a cell is whatever the atomics give: the kNN result does not
+//      depend on it); the same for the valid queries, with the references'
+//      frame, unless the query set is the reference set.
+// ---------------------------------------------------------------------------
+constexpr int MC_SAMPLE = 4096;
+
+__global__ void __launch_bounds__(256) mc_frame_kernel(const float *pts,
+                                                       const int64_t *lens, int n,
+                                                       float *frame) {
+    __shared__ float red[6][8];
+    const int b = blockIdx.x;
+    const int nv = valid_len(lens, b, n);
+    const int step = max(1, nv / MC_SAMPLE);
+    const int nb = min(nv, MC_SAMPLE);
+    const float *c = pts + size_t(b) * n * 3;
+    const float inf = __int_as_float(0x7f800000);
+    float lo[3] = {inf, inf, inf}, hi[3] = {-inf, -inf, -inf};
+    for (int i = threadIdx.x; i < nb; i += 256)
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            const float v = c[size_t(i) * step * 3 + d];
+            lo[d] = fminf(lo[d], v);
+            hi[d] = fmaxf(hi[d], v);
+        }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            lo[d] = fminf(lo[d], __shfl_xor_sync(FULL, lo[d], o));
+            hi[d] = fmaxf(hi[d], __shfl_xor_sync(FULL, hi[d], o));
+        }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0)
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            red[d][w] = lo[d];
+            red[3 + d][w] = hi[d];
+        }
+    __syncthreads();
+    if (threadIdx.x < 3) {
+        const int d = threadIdx.x;
+        float l = inf, h = -inf;
+        for (int i = 0; i < 8; ++i) {
+            l = fminf(l, red[d][i]);
+            h = fmaxf(h, red[3 + d][i]);
+        }
+        const float ext = h - l;
+        const bool ok = ext > 0.0f && ext < 3e38f && l > -3e38f;
+        frame[size_t(b) * 8 + d] = ok ? l : 0.0f;
+        frame[size_t(b) * 8 + 3 + d] = ok ? float(1 << MC_BITS) / ext : 0.0f;
+    }
+}
+
+__global__ void __launch_bounds__(256) mc_count_kernel(const float *pts,
+                                                       const int64_t *lens, int n,
+                                                       const float *frame, int *hist) {
+    const int b = blockIdx.y;
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    if (i >= valid_len(lens, b, n)) return;
+    const float *p = pts + (size_t(b) * n + i) * 3;
+    const unsigned code = mc_code(frame + size_t(b) * 8, p[0], p[1], p[2]);
+    atomicAdd(&hist[size_t(b) * (MC_CELLS + 1) + code], 1);
+}
+
+// Exclusive scan of each cloud's MC_CELLS counts into start[0 .. MC_CELLS]
+// (start[MC_CELLS] = total) and cursor (a copy of the starts): rows of 1024
+// counts, each scanned by the block (coalesced), with a running carry.
+__global__ void __launch_bounds__(1024) mc_scan_kernel(const int *hist, int *start,
+                                                       int *cursor) {
+    __shared__ int wsum[32];
+    const int b = blockIdx.x;
+    const int *h = hist + size_t(b) * (MC_CELLS + 1);
+    int *st = start + size_t(b) * (MC_CELLS + 1);
+    int *cu = cursor + size_t(b) * (MC_CELLS + 1);
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    int carry = 0;
+    for (int r = 0; r < MC_CELLS; r += 1024) {
+        const int v = h[r + t];
+        int x = v;  // inclusive scan within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int z = wsum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(FULL, z, o);
+                if (lane >= o) z += y;
+            }
+            wsum[lane] = z;
+        }
+        __syncthreads();
+        const int excl = carry + x - v + (w > 0 ? wsum[w - 1] : 0);
+        st[r + t] = excl;
+        cu[r + t] = excl;
+        carry += wsum[31];
+        __syncthreads();  // wsum is rewritten by the next row
+    }
+    if (t == 0) st[MC_CELLS] = carry;
+}
+
+__global__ void __launch_bounds__(256) mc_scatter_kernel(const float *pts,
+                                                         const int64_t *lens, int n,
+                                                         const float *frame, int *cursor,
+                                                         float4 *out) {
+    const int b = blockIdx.y;
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    if (i >= valid_len(lens, b, n)) return;
+    const float *p = pts + (size_t(b) * n + i) * 3;
+    const float x = p[0], y = p[1], z = p[2];
+    const unsigned code = mc_code(frame + size_t(b) * 8, x, y, z);
+    const int pos = atomicAdd(&cursor[size_t(b) * (MC_CELLS + 1) + code], 1);
+    out[size_t(b) * n + pos] = make_float4(x, y, z, __int_as_float(i));
+}
+
+// The ORDERED lane kNN: order the clouds, then one lane-kernel launch.  The
+// scratch memory is stream-ordered (allocated and freed on `stream`).
+template <int QL>
+cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
+                               cudaStream_t stream) {
+    const bool self = a.query == a.ref && a.Q == a.N && a.q_len == a.r_len;
+    const size_t cells = size_t(B) * (MC_CELLS + 1) * sizeof(int);
+    const size_t off_frame = 0;
+    // hist_r then hist_q (zeroed together)
+    const size_t off_hist = (size_t(B) * 8 * sizeof(float) + 255) & ~size_t(255);
+    const size_t off_start = off_hist + 2 * cells;
+    const size_t off_cur = off_start + cells;
+    const size_t off_curq = off_cur + cells;
+    const size_t off_sref = (off_curq + cells + 255) & ~size_t(255);
+    const size_t off_sq = off_sref + ((size_t(B) * a.N * 16 + 255) & ~size_t(255));
+    const size_t total = off_sq + (self ? 0 : size_t(B) * a.Q * 16);
+    char *base = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&base), total, stream);
+    if (e != cudaSuccess) return e;
+    float *frame = reinterpret_cast<float *>(base + off_frame);
+    int *hist = reinterpret_cast<int *>(base + off_hist);
+    int *start = reinterpret_cast<int *>(base + off_start);
+    int *cur = reinterpret_cast<int *>(base + off_cur);
+    int *curq = reinterpret_cast<int *>(base + off_curq);
+    float4 *sref = reinterpret_cast<float4 *>(base + off_sref);
+    float4 *sq = self ? sref : reinterpret_cast<float4 *>(base + off_sq);
+    int *histq = hist + size_t(B) * (MC_CELLS + 1);
+    e = cudaMemsetAsync(hist, 0, 2 * cells, stream);
+    const dim3 gr(unsigned((a.N + 255) / 256), unsigned(B));
+    const dim3 gq(unsigned((a.Q + 255) / 256), unsigned(B));
+    if (e == cudaSuccess) {
+        mc_frame_kernel<<<unsigned(B), 256, 0, stream>>>(a.ref, a.r_len, a.N, frame);
+        mc_count_kernel<<<gr, 256, 0, stream>>>(a.ref, a.r_len, a.N, frame, hist);
+        mc_scan_kernel<<<unsigned(B), 1024, 0, stream>>>(hist, start, cur);
+        mc_scatter_kernel<<<gr, 256, 0, stream>>>(a.ref, a.r_len, a.N, frame, cur, sref);
+        if (!self) {
+            // the query starts are only cursors: scan into curq twice over
+            mc_count_kernel<<<gq, 256, 0, stream>>>(a.query, a.q_len, a.Q, frame, histq);
+            mc_scan_kernel<<<unsigned(B), 1024, 0, stream>>>(histq, curq, curq);
+            mc_scatter_kernel<<<gq, 256, 0, stream>>>(a.query, a.q_len, a.Q, frame, curq,
+                                                      sq);
+        }
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+        a.sref = reinterpret_cast<const float *>(sref);
+        a.squery = reinterpret_cast<const float *>(sq);
+        a.cstart = start;
+        a.cframe = frame;
+        e = launch_knn_lane<QL, true>(dev, a, B, a, 0, stream);
+    }
+    const cudaError_t f = cudaFreeAsync(base, stream);
+    return e != cudaSuccess ? e : f;
 }
 
 template <int KPL>
@@ -819,6 +1116,11 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
                        cudaStream_t stream) {
     const KnnArgs a = make_knn_args(dev, query, Q, ref, N, k, q_len, r_len, squared,
                                     out_dist, out_idx);
+    // large clouds with k >= 2: the spatial order (a few extra launches)
+    // pays for itself many times over in candidate insertions
+    const bool ordered = k >= 2 && k <= 32 && N >= 16384 && Q >= 4096 && B <= 64;
+    if (ordered && k <= 16) return launch_knn_ordered<2>(dev, a, B, stream);
+    if (ordered) return launch_knn_ordered<1>(dev, a, B, stream);
     if (k <= 16) return launch_knn_lane<2>(dev, a, B, a, 0, stream);
     if (k <= 32) return launch_knn_lane<1>(dev, a, B, a, 0, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);

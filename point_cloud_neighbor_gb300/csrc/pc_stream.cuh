@@ -45,7 +45,10 @@ namespace pcn {
 constexpr int ST_T = 256;  // points per tile
 constexpr int ST_STAGES = 8;      // cooked stages (shared with the consumers)
 constexpr int ST_RAW_STAGES = 3;  // TMA landing buffers (producer only)
-constexpr unsigned ST_RAW = tile_buffer_bytes(ST_T);
+// a raw tile: ST_T points of 12 bytes (plus alignment), or of 16 bytes
+// (x, y, z, original index) for clouds in a spatial order
+constexpr unsigned ST_RAW = tile_buffer_bytes(ST_T) > ST_T * 16u ? tile_buffer_bytes(ST_T)
+                                                                  : ST_T * 16u;
 constexpr unsigned ST_COOKED = (ST_T / 2) * 32;
 constexpr unsigned ST_COPY = ST_T * 16;  // raw coordinates, 16 bytes a point
 constexpr unsigned ST_STAGE = ST_COOKED + ST_COPY;
@@ -118,10 +121,13 @@ __device__ __forceinline__ WaitResult warp_wait(uint64_t *bar, unsigned parity,
 }
 
 // The producer warp.  Tile `it` covers points [tile_at(it) * ST_T, ...) of
-// the cloud at `cref` (N valid points).  Stops when *stop becomes non-zero;
-// a timeout raises *err.  Before returning it waits (bounded) for every raw
-// copy it issued, so none is in flight when the block exits.
-template <int SB, class TileAt>
+// the cloud at `cref` (N valid points): (x, y, z) float triples, or with F4
+// 16-byte points (x, y, z, original index bits) starting 16-byte aligned,
+// whose index goes to the fourth component of the raw copy (0 otherwise).
+// Stops when *stop becomes non-zero; a timeout raises *err.  Before
+// returning it waits (bounded) for every raw copy it issued, so none is in
+// flight when the block exits.
+template <int SB, bool F4, class TileAt>
 __device__ __forceinline__ void stream_produce(const StreamRing &ring,
                                                const float *cref, int N,
                                                int ntiles, TileAt tile_at,
@@ -132,12 +138,18 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
     const int lane = static_cast<int>(lane_id());
     const float inf = __int_as_float(0x7f800000);
     int issued = 0, landed = 0;
+    constexpr int PS = F4 ? 4 : 3;  // floats per point
+    auto issue = [&](int t, int slot) {
+        const int j0 = tile_at(t) * ST_T;
+        if (F4)
+            issue_tile16(ring.raw_tile(slot), cref + size_t(j0) * 4, min(ST_T, N - j0),
+                         &ring.raw_full[slot]);
+        else
+            issue_tile(ring.raw_tile(slot), cref + size_t(j0) * 3, min(ST_T, N - j0),
+                       &ring.raw_full[slot]);
+    };
     if (lane == 0)
-        for (; issued < ntiles && issued < ST_RAW_STAGES; ++issued) {
-            const int j0 = tile_at(issued) * ST_T;
-            issue_tile(ring.raw_tile(issued), cref + size_t(j0) * 3,
-                       min(ST_T, N - j0), &ring.raw_full[issued]);
-        }
+        for (; issued < ntiles && issued < ST_RAW_STAGES; ++issued) issue(issued, issued);
     issued = __shfl_sync(0xffffffffu, issued, 0);
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % ST_STAGES, rs = it % ST_RAW_STAGES;
@@ -159,21 +171,24 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
         if (__any_sync(0xffffffffu, *stop != 0 || *err != 0)) break;
         const int j0 = tile_at(it) * ST_T;
         const int cnt = min(ST_T, N - j0);
-        const float *src = ring.raw_tile(rs) + tile_float_offset(cref + size_t(j0) * 3);
+        const float *src =
+            ring.raw_tile(rs) + (F4 ? 0u : tile_float_offset(cref + size_t(j0) * 3));
         float4 *dst = reinterpret_cast<float4 *>(ring.stage + size_t(st) * ST_STAGE);
         float4 *copy = reinterpret_cast<float4 *>(ring.stage + size_t(st) * ST_STAGE +
                                                   ST_COOKED);
 #pragma unroll
         for (int u = 0; u < ST_T / 64; ++u) {
             const int p = lane + 32 * u;
-            float c[2][4], r[2][3];
+            float c[2][4], r[2][4];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int i = 2 * p + h;
+                r[h][3] = 0.f;
                 if (i < cnt) {
-                    r[h][0] = src[3 * i];
-                    r[h][1] = src[3 * i + 1];
-                    r[h][2] = src[3 * i + 2];
+                    r[h][0] = src[PS * i];
+                    r[h][1] = src[PS * i + 1];
+                    r[h][2] = src[PS * i + 2];
+                    if (F4) r[h][3] = src[PS * i + 3];
                     float xp = __fsub_rn(r[h][0], fr.cx);
                     float yp = __fsub_rn(r[h][1], fr.cy);
                     float zp = __fsub_rn(r[h][2], fr.cz);
@@ -189,15 +204,11 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
             }
             dst[cooked_slot<SB>(p, 0)] = make_float4(c[0][0], c[1][0], c[0][1], c[1][1]);
             dst[cooked_slot<SB>(p, 1)] = make_float4(c[0][2], c[1][2], c[0][3], c[1][3]);
-            copy[raw_slot(2 * p)] = make_float4(r[0][0], r[0][1], r[0][2], 0.f);
-            copy[raw_slot(2 * p + 1)] = make_float4(r[1][0], r[1][1], r[1][2], 0.f);
+            copy[raw_slot(2 * p)] = make_float4(r[0][0], r[0][1], r[0][2], r[0][3]);
+            copy[raw_slot(2 * p + 1)] = make_float4(r[1][0], r[1][1], r[1][2], r[1][3]);
         }
         __syncwarp();  // every lane has read raw buffer rs
-        if (lane == 0 && issued < ntiles) {
-            const int j1 = tile_at(issued) * ST_T;
-            issue_tile(ring.raw_tile(rs), cref + size_t(j1) * 3, min(ST_T, N - j1),
-                       &ring.raw_full[rs]);
-        }
+        if (lane == 0 && issued < ntiles) issue(issued, rs);
         if (issued < ntiles) ++issued;
         mbar_arrive(&ring.ready[st]);
     }

@@ -53,6 +53,17 @@ __device__ __forceinline__ void issue_tile(float *buf, const float *gsrc,
         bulk_g2s(b + (a0 - base), reinterpret_cast<const void *>(a0), bulk, bar);
 }
 
+// Called by ONE thread.  Copies cnt >= 1 points of 16 bytes from the
+// 16-byte-aligned `gsrc` into `buf` with one bulk copy; completion is
+// signalled on `bar` (arrival count 1).
+__device__ __forceinline__ void issue_tile16(float *buf, const float *gsrc, int cnt,
+                                             uint64_t *bar) {
+    const unsigned bytes = 16u * static_cast<unsigned>(cnt);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(buf, gsrc, bytes, bar);
+}
+
 // ---------------------------------------------------------------------------
 // Ring of STAGES tile buffers shared by the consumer warps of a block and
 // filled by one producer thread.  full[s] (count 1 + transaction bytes)

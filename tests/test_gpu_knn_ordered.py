@@ -1,0 +1,91 @@
+"""Parity of the spatially ordered brute-force kNN with the oracle.
+
+Clouds of at least 16384 references with 4096 or more queries and
+2 <= k <= 32 are put in cell-code order before the lane kernel runs (the
+keys keep the original indices).  These cases cover that path: the query
+set equal to the reference set and distinct from it, several clouds, valid
+lengths (rows past a query length, fewer valid references than k), exact
+ties from coordinates on a coarse grid and duplicated points, and points far
+outside the frame the cell codes are taken over.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import point_cloud_neighbor_gb300 as pc
+
+pytestmark = pytest.mark.gpu
+
+THREADS = oracle.default_threads()
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def to_dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+def grid_cloud(rng, B, n, step=1.0 / 64):
+    """Uniform points on a grid of spacing `step`, 2% of them duplicated."""
+    x = (rng.integers(0, int(1 / step), size=(B, n, 3)) * step).astype(np.float32)
+    dup = rng.choice(n, size=n // 50, replace=False)
+    x[:, dup] = x[:, rng.choice(n, size=n // 50)]
+    return x
+
+
+def compare(got_d, got_i, want_d, want_i, what):
+    got_i = got_i.reshape(want_i.shape)
+    got_d = got_d.reshape(want_d.shape)
+    bad = int((got_i != want_i).sum())
+    assert bad == 0, f"{what}: {bad} of {want_i.size} indices differ"
+    badd = int((got_d.view(np.uint32) != want_d.view(np.uint32)).sum())
+    assert badd == 0, f"{what}: {badd} of {want_d.size} distances differ"
+
+
+@pytest.fixture(autouse=True)
+def clean_status():
+    yield
+    assert pc.pc_device_status(reset=True) == 0
+
+
+@pytest.mark.parametrize("k", [2, 16, 17, 32])
+def test_ordered_self_knn_with_ties(k):
+    rng = np.random.default_rng(100 + k)
+    x = grid_cloud(rng, 2, 16384)
+    d, i = pc.pc_knn(to_dev(x), to_dev(x), k)
+    rows = np.unique(np.concatenate([rng.choice(2 * 16384, 3000, replace=False),
+                                     [0, 16383, 16384, 2 * 16384 - 1]]))
+    wd, wi = oracle.knn(x, x, k, rows=rows, threads=THREADS)
+    compare(d.cpu().numpy().reshape(-1, k)[rows], i.cpu().numpy().reshape(-1, k)[rows],
+            wd, wi, f"ordered self kNN k={k}")
+
+
+def test_ordered_distinct_queries_with_lengths_and_outliers():
+    rng = np.random.default_rng(7)
+    B, Q, N, k = 3, 5000, 20000, 8
+    x = grid_cloud(rng, B, N, step=1.0 / 128)
+    q = rng.random((B, Q, 3), dtype=np.float32)
+    q[0, :50] *= 40.0          # queries far outside the references' frame
+    x[1, 5:9] = [-1e6, 3e5, 7.0]  # references far outside too
+    ql = np.array([Q, 4321, 4096], dtype=np.int64)
+    rl = np.array([N, 17000, 6], dtype=np.int64)   # cloud 2: fewer than k
+    d, i = pc.pc_knn(to_dev(q), to_dev(x), k, query_lengths=to_dev(ql),
+                     ref_lengths=to_dev(rl))
+    wd, wi = oracle.knn_masked(q, x, k, ql, rl, threads=THREADS)
+    compare(d.cpu().numpy(), i.cpu().numpy(), wd, wi, "ordered masked kNN")
+
+
+def test_ordered_squared_and_sqrt_agree():
+    rng = np.random.default_rng(9)
+    x = rng.random((1, 20000, 3), dtype=np.float32)
+    q = rng.random((1, 4096, 3), dtype=np.float32)
+    d, i = pc.pc_knn(to_dev(q), to_dev(x), 5)
+    s, j = pc.pc_knn(to_dev(q), to_dev(x), 5, squared=True)
+    assert torch.equal(i, j)
+    assert torch.equal(d, torch.sqrt(s))
+    wd, wi = oracle.knn(q, x, 5, rows=np.arange(0, 4096, 7), threads=THREADS)
+    compare(d.cpu().numpy().reshape(-1, 5)[::7], i.cpu().numpy().reshape(-1, 5)[::7],
+            wd, wi, "ordered kNN distinct queries")
