@@ -72,6 +72,9 @@ struct KnnArgs {
     const float *squery;  // [B][Q] x 4 (== sref for a query set equal to ref)
     const int *cstart;    // [B][MC_CELLS + 1]
     const float *cframe;  // [B][8]: lo x, y, z, scale x, y, z
+    // ORDERED with the references split into gridDim.z parts: each part's
+    // sorted k keys per valid query row, [part][B][Q][k] (merged afterwards)
+    unsigned long long *part_keys;
 };
 
 // Cell codes of the spatial order: MC_BITS bits per axis, interleaved
@@ -570,6 +573,13 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     const int Qb = valid_len(a.q_len, b, a.Q);
     const int ntiles = (Nb + ST_T - 1) / ST_T;
     const int tstride = scramble_stride(ntiles);
+    // ORDERED: part blockIdx.z of gridDim.z visits steps [it0, it1) of the
+    // cloud's visiting order
+    const int part = ORDERED ? static_cast<int>(blockIdx.z) : 0;
+    const int nparts = ORDERED ? static_cast<int>(gridDim.z) : 1;
+    const int it0 = static_cast<int>((static_cast<long long>(ntiles) * part) / nparts);
+    const int nsteps_part =
+        static_cast<int>((static_cast<long long>(ntiles) * (part + 1)) / nparts) - it0;
     const int nwarps = static_cast<int>(blockDim.x >> 5) - 1;  // consumers
     const int nbx = static_cast<int>(gridDim.x);
     const int bx = static_cast<int>(blockIdx.x);
@@ -582,7 +592,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
                              : (bx < gvalid ? min(nwarps, (gvalid - bx + nbx - 1) / nbx) : 0);
     if (ORDERED) {
         // rows past the cloud's valid length: padding, spread over the blocks
-        if (warp == 0)
+        if (warp == 0 && part == 0)
             for (int r = Qb + bx; r < a.Q; r += nbx)
                 for (int e = lane; e < k; e += 32) {
                     a.out_idx[(size_t(b) * a.Q + r) * k + e] = -1;
@@ -623,7 +633,8 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     // consumers and the producer only (the other warps have left)
     named_barrier_sync(1, unsigned(32 * (nact + 1)));
     // tile visited at step `it`: ORDERED outwards from home, else scrambled
-    auto tile_at = [&](int it) {
+    auto tile_at = [&](int itp) {
+        const int it = it0 + itp;
         if (ORDERED) {
             const int off = (it & 1) ? (it + 1) >> 1 : -(it >> 1);
             int t = (home + off) % ntiles;
@@ -633,8 +644,8 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     };
 
     if (warp == nwarps) {  // producer warp
-        stream_produce<KL_SB, ORDERED>(ring, cref, Nb, ntiles, tile_at, fr, s_err, s_err,
-                                       a.timeout_ns);
+        stream_produce<KL_SB, ORDERED>(ring, cref, Nb, nsteps_part, tile_at, fr, s_err,
+                                       s_err, a.timeout_ns);
         return;
     }
 
@@ -713,7 +724,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     }
 
     bool failed = false;
-    for (int it = 0; it < ntiles; ++it) {
+    for (int it = 0; it < nsteps_part; ++it) {
         const int st = it % ST_STAGES;
         const WaitResult w = warp_wait(&ring.ready[st], unsigned((it / ST_STAGES) & 1),
                                        s_err, a.timeout_ns);
@@ -806,7 +817,13 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         if (qi[q] >= a.Q || (ORDERED && !valid[q])) continue;
         const size_t row = size_t(b) * a.Q + orow[q];
         if (failed) {
-            for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
+            if (ORDERED && nparts > 1) {
+                unsigned long long *pk =
+                    a.part_keys + ((size_t(part) * gridDim.y + b) * a.Q + orow[q]) * k;
+                for (int e = 0; e < k; ++e) pk[e] = KEY_EMPTY;
+            } else {
+                for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
+            }
             continue;
         }
         unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
@@ -815,6 +832,12 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
             const unsigned long long key = hk[n * 32];
             hk[n * 32] = hk[0];
             heap_sift(hk, n, 0, key);
+        }
+        if (ORDERED && nparts > 1) {  // this part's sorted keys, merged later
+            unsigned long long *pk =
+                a.part_keys + ((size_t(part) * gridDim.y + b) * a.Q + orow[q]) * k;
+            for (int e = 0; e < k; ++e) pk[e] = hk[e * 32];
+            continue;
         }
         const int kv = valid[q] ? min(k, Nb) : 0;
         for (int e = 0; e < k; ++e) {
@@ -826,13 +849,46 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     }
 }
 
+// The k smallest keys of a valid query row over the parts' sorted lists
+// (ORDERED with the references split): one thread per row.
+__global__ void __launch_bounds__(256) knn_merge_parts_kernel(const KnnArgs a, int B,
+                                                              int nparts) {
+    const int b = blockIdx.y;
+    const int r = blockIdx.x * 256 + threadIdx.x;
+    if (r >= valid_len(a.q_len, b, a.Q)) return;
+    const int k = a.k;
+    const int kv = min(k, valid_len(a.r_len, b, a.N));
+    const size_t stride = size_t(B) * a.Q * k;  // between parts
+    const unsigned long long *pk = a.part_keys + (size_t(b) * a.Q + r) * k;
+    int ptr[8];
+    for (int p = 0; p < nparts; ++p) ptr[p] = 0;
+    const size_t row = size_t(b) * a.Q + r;
+    for (int e = 0; e < k; ++e) {
+        unsigned long long best = KEY_EMPTY;
+        int bp = -1;
+        for (int p = 0; p < nparts; ++p)
+            if (ptr[p] < k) {
+                const unsigned long long key = pk[p * stride + ptr[p]];
+                if (key < best) {
+                    best = key;
+                    bp = p;
+                }
+            }
+        if (bp >= 0) ++ptr[bp];
+        const float sv = key_s(best);
+        a.out_idx[row * k + e] = e < kv ? int64_t(key_j(best)) : int64_t(-1);
+        a.out_dist[row * k + e] = e < kv ? (a.squared ? sv : __fsqrt_rn(sv)) : 0.0f;
+    }
+}
+
 template <int QL, bool ORDERED = false>
 cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0,
-                            const KnnArgs &a1, int64_t B1, cudaStream_t stream) {
+                            const KnnArgs &a1, int64_t B1, cudaStream_t stream,
+                            int nparts = 1) {
     const int64_t GQ = 32 * QL;
     const int64_t Q = std::max<int64_t>(a0.Q, B1 > 0 ? a1.Q : 0);
     const int64_t G = (Q + GQ - 1) / GQ;  // groups per cloud
-    const int64_t total = G * (B0 + B1);
+    const int64_t total = G * (B0 + B1) * nparts;
     if (total == 0) return cudaSuccess;
     const int64_t nsm = std::max(1, dev.sm_count);
     // consumer warps per block: shared memory bounds it too (k * 8 bytes per
@@ -850,7 +906,8 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
         knn_lane_kernel<QL, ORDERED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(B0 + B1));
+    dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(B0 + B1),
+              static_cast<unsigned>(nparts));
     knn_lane_kernel<QL, ORDERED>
         <<<grid, unsigned(32 * (W + 1)), smem, stream>>>(a0, a1, int(B0));
     return cudaGetLastError();
@@ -997,7 +1054,15 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
     const size_t off_curq = off_cur + cells;
     const size_t off_sref = (off_curq + cells + 255) & ~size_t(255);
     const size_t off_sq = off_sref + ((size_t(B) * a.N * 16 + 255) & ~size_t(255));
-    const size_t total = off_sq + (self ? 0 : size_t(B) * a.Q * 16);
+    // few queries against many references: split the references into parts
+    // (blocks of the same queries, other tiles), about 10 warps per SM
+    const int64_t groups = B * ((int64_t(a.Q) + 32 * QL - 1) / (32 * QL));
+    const int64_t ntiles = (int64_t(a.N) + ST_T - 1) / ST_T;
+    const int64_t want = (int64_t(std::max(1, dev.sm_count)) * 10 + groups - 1) / groups;
+    const int nparts = int(std::max<int64_t>(1, std::min<int64_t>({8, want, ntiles / 8})));
+    const size_t off_pk = off_sq + ((self ? 0 : size_t(B) * a.Q * 16 + 255) & ~size_t(255));
+    const size_t total =
+        off_pk + (nparts > 1 ? size_t(nparts) * B * a.Q * size_t(a.k) * 8 : 0);
     char *base = nullptr;
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&base), total, stream);
     if (e != cudaSuccess) return e;
@@ -1031,7 +1096,14 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
         a.squery = reinterpret_cast<const float *>(sq);
         a.cstart = start;
         a.cframe = frame;
-        e = launch_knn_lane<QL, true>(dev, a, B, a, 0, stream);
+        a.part_keys =
+            nparts > 1 ? reinterpret_cast<unsigned long long *>(base + off_pk) : nullptr;
+        e = launch_knn_lane<QL, true>(dev, a, B, a, 0, stream, nparts);
+        if (e == cudaSuccess && nparts > 1) {
+            const dim3 gm(unsigned((a.Q + 255) / 256), unsigned(B));
+            knn_merge_parts_kernel<<<gm, 256, 0, stream>>>(a, int(B), nparts);
+            e = cudaGetLastError();
+        }
     }
     const cudaError_t f = cudaFreeAsync(base, stream);
     return e != cudaSuccess ? e : f;
