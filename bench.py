@@ -260,6 +260,9 @@ def run_gpu(args):
     # (--serial: everything on one stream).
     side = torch.cuda.Stream(device) if not args.serial else stream
     fork = torch.cuda.Event()
+    # the kNN and Ball Query grids (one wave) are planned around the SMs
+    # FPS holds while it runs
+    reserve = 0 if args.serial else pc.pc_fps_sm_count(B, N, npoint)
 
     def step(ev=None):
         # ev: [start, fps_end, knn_start (side), knn_end, bq_end, step_end]
@@ -273,10 +276,12 @@ def run_gpu(args):
         with torch.cuda.stream(side):
             if ev is not None:
                 ev[2].record(side)
+            pc.pc_set_sm_reserve(reserve)
             pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
             if ev is not None:
                 ev[3].record(side)
             pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
+            pc.pc_set_sm_reserve(0)
             if ev is not None:
                 ev[4].record(side)
         stream.wait_stream(side)
@@ -712,14 +717,17 @@ def run_e2e(args, pc, x_host, device, world):
 
     main = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device) if not args.serial else main
+    reserve = 0 if args.serial else pc.pc_fps_sm_count(1, N, npoint)
 
     def one():
         xd = x_pin.to(device, non_blocking=True)
         side.wait_stream(main)
         f = pc.pc_fps(xd, npoint, 0)
         with torch.cuda.stream(side):
+            pc.pc_set_sm_reserve(reserve)
             d, i = pc.pc_knn(xd, xd, k)
             d2, i2 = pc.pc_ball_query(xd, xd, r, K)
+            pc.pc_set_sm_reserve(0)
         main.wait_stream(side)
         for t in (d, i, d2, i2):
             t.record_stream(main)

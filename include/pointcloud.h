@@ -387,6 +387,22 @@ int pc_device_status(void *stream, int reset, int32_t *out_status);
 void pc_set_wait_timeout_ns(uint64_t ns);
 void pc_debug_set_fps_grid_stall(int enable);
 
+/*
+ * Concurrency hint: the number of SMs that work running at the same time on
+ * another stream occupies (default 0).  The brute-force kNN (one block per
+ * SM) and Ball Query (two blocks per SM) size their grids for one wave; with
+ * a reserve of n they plan for (SM count - n) SMs (at least 1), so that none
+ * of their blocks waits for the other work to finish.
+ * Results do not depend on it.  Applies to launches enqueued after the call,
+ * on every device; negative values count as 0.
+ */
+void pc_set_sm_reserve(int sms);
+
+/* The number of SMs an FPS launch of these sizes occupies while it runs (its
+ * resident thread blocks, at most the SM count), or 0 when the sizes have no
+ * schedule or there is no device.  npoint does not change it. */
+int pc_fps_sm_count(int64_t B, int64_t N, int64_t npoint);
+
 #ifdef __cplusplus
 }
 #endif

@@ -14,7 +14,8 @@ from .binding import (PC_FPS_AUTO, PC_FPS_BLOCK, PC_FPS_CLUSTER, PC_FPS_GRID,
                       pc_debug_set_fps_grid_stall, pc_device_status, pc_fps,
                       pc_gather_points, pc_grid_build, pc_knn, pc_knn_d,
                       pc_knn_grid,
-                      pc_set_wait_timeout_ns, pc_three_interpolate,
+                      pc_set_wait_timeout_ns, pc_set_sm_reserve,
+                      pc_fps_sm_count, pc_three_interpolate,
                       pc_three_interpolate_backward, three_interpolate,
                       three_nn)
 
@@ -26,4 +27,5 @@ __all__ = [
     "pc_grid_build", "pc_knn_grid", "pc_ball_query_grid", "pc_chamfer",
     "chamfer_distance", "pc_three_interpolate", "pc_three_interpolate_backward",
     "three_interpolate", "three_nn", "pc_gather_points", "pc_knn_d",
+    "pc_set_sm_reserve", "pc_fps_sm_count",
 ]

@@ -73,6 +73,8 @@ _SIGNATURES = {
                                         ctypes.POINTER(ctypes.c_int32)]),
     "pc_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "pc_debug_set_fps_grid_stall": (None, [ctypes.c_int]),
+    "pc_set_sm_reserve": (None, [ctypes.c_int]),
+    "pc_fps_sm_count": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
 }
 
 _lib = None
@@ -551,6 +553,17 @@ def pc_set_wait_timeout_ns(ns: int):
 
 def pc_debug_set_fps_grid_stall(enable: bool):
     lib().pc_debug_set_fps_grid_stall(int(bool(enable)))
+
+
+def pc_set_sm_reserve(sms: int):
+    """SMs that concurrent work on another stream occupies (a planning hint
+    for the brute-force kNN grid; results do not depend on it)."""
+    lib().pc_set_sm_reserve(int(sms))
+
+
+def pc_fps_sm_count(B: int, N: int, npoint: int) -> int:
+    """SMs an FPS launch of these sizes occupies on the current device."""
+    return int(lib().pc_fps_sm_count(int(B), int(N), int(npoint)))
 
 
 # mps-pointops-style names

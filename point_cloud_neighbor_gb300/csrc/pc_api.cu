@@ -23,6 +23,7 @@ constexpr int kVersion = 10000 * 0 + 100 * 1 + 0;  // 0.1.0
 
 thread_local std::string t_error;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<int> g_sm_reserve{0};
 std::atomic<int> g_fps_stall{0};
 std::mutex g_dev_mutex;
 pcn::DeviceInfo g_devices[kMaxDevices];
@@ -127,6 +128,7 @@ bool mul_ok(int64_t a, int64_t b, int64_t c) {
 
 namespace pcn {
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
+int sm_reserve() { return g_sm_reserve.load(); }
 int fps_grid_stall() { return g_fps_stall.load(); }
 int api_current_device(const DeviceInfo **out) { return current_device(out); }
 int api_check_ptr(const void *p, int dev, size_t align, const char *name) {
@@ -158,6 +160,18 @@ void pc_set_wait_timeout_ns(uint64_t ns) {
 }
 
 void pc_debug_set_fps_grid_stall(int enable) { g_fps_stall.store(enable ? 1 : 0); }
+
+void pc_set_sm_reserve(int sms) { g_sm_reserve.store(sms < 0 ? 0 : sms); }
+
+int pc_fps_sm_count(int64_t B, int64_t N, int64_t npoint) {
+    (void)npoint;
+    if (B <= 0 || N <= 0) return 0;
+    const pcn::DeviceInfo *dev = nullptr;
+    if (current_device(&dev) != PC_OK) return 0;
+    const pcn::FpsPlan p = pcn::plan_fps(*dev, B, N, PC_FPS_AUTO, 0, 0);
+    if (!p.ok) return 0;
+    return int(std::min<int64_t>(dev->sm_count, B * int64_t(p.blocks_per_cloud)));
+}
 
 size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
                                  int strategy, int blocks_per_cloud) {

@@ -349,7 +349,8 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
 
-    const int slots = dev.sm_count * 2;
+    // one wave of two blocks per SM, less the SMs other work holds
+    const int slots = std::max(1, dev.sm_count - sm_reserve()) * 2;
     const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));
     int64_t G = (Q + BQ_CWARPS * bpc_target - 1) / (BQ_CWARPS * bpc_target);
     const size_t budget =

@@ -24,6 +24,8 @@ struct DeviceInfo {
 
 // Device-side wait bound, in ns (see pc_set_wait_timeout_ns).
 uint64_t wait_timeout_ns();
+// SMs taken by concurrent work (see pc_set_sm_reserve).
+int sm_reserve();
 // Testing hook for the FPS grid exchange (see pc_debug_set_fps_grid_stall).
 int fps_grid_stall();
 

@@ -890,7 +890,7 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
     const int64_t G = (Q + GQ - 1) / GQ;  // groups per cloud
     const int64_t total = G * (B0 + B1) * nparts;
     if (total == 0) return cudaSuccess;
-    const int64_t nsm = std::max(1, dev.sm_count);
+    const int64_t nsm = std::max(1, dev.sm_count - sm_reserve());
     // consumer warps per block: shared memory bounds it too (k * 8 bytes per
     // query); a block per SM and wave
     const int64_t per_warp = GQ * int64_t(a0.k) * 8;
@@ -1058,7 +1058,8 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
     // (blocks of the same queries, other tiles), about 10 warps per SM
     const int64_t groups = B * ((int64_t(a.Q) + 32 * QL - 1) / (32 * QL));
     const int64_t ntiles = (int64_t(a.N) + ST_T - 1) / ST_T;
-    const int64_t want = (int64_t(std::max(1, dev.sm_count)) * 10 + groups - 1) / groups;
+    const int64_t want =
+        (int64_t(std::max(1, dev.sm_count - sm_reserve())) * 10 + groups - 1) / groups;
     const int nparts = int(std::max<int64_t>(1, std::min<int64_t>({8, want, ntiles / 8})));
     const size_t off_pk = off_sq + ((self ? 0 : size_t(B) * a.Q * 16 + 255) & ~size_t(255));
     const size_t total =

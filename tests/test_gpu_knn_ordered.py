@@ -89,3 +89,18 @@ def test_ordered_squared_and_sqrt_agree():
     wd, wi = oracle.knn(q, x, 5, rows=np.arange(0, 4096, 7), threads=THREADS)
     compare(d.cpu().numpy().reshape(-1, 5)[::7], i.cpu().numpy().reshape(-1, 5)[::7],
             wd, wi, "ordered kNN distinct queries")
+
+
+def test_sm_reserve_only_changes_the_plan():
+    rng = np.random.default_rng(11)
+    x = to_dev(rng.random((1, 30000, 3), dtype=np.float32))
+    n = pc.pc_fps_sm_count(1, 30000, 4096)
+    assert 1 <= n <= torch.cuda.get_device_properties(0).multi_processor_count
+    d0, i0 = pc.pc_knn(x, x, 12)
+    try:
+        for reserve in (n, 100, 10_000):
+            pc.pc_set_sm_reserve(reserve)
+            d1, i1 = pc.pc_knn(x, x, 12)
+            assert torch.equal(i0, i1) and torch.equal(d0, d1), reserve
+    finally:
+        pc.pc_set_sm_reserve(0)
