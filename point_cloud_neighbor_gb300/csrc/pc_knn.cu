@@ -484,6 +484,9 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // blocks set the time.)  One producer serves all W consumer warps.
 // consumer warps per block at most (one block per SM: registers)
 __host__ __device__ constexpr int kl_wmax(int QL) { return QL == 1 ? 15 : 12; }
+// references around a query's place in the spatial order that give its seed
+// bound (k groups of KL_SEED / k)
+constexpr int KL_SEED = 32;
 
 __host__ __device__ constexpr size_t knn_lane_smem(int k, int QL, int W) {
     return stream_smem_bytes() + size_t(W) * 32 * QL * size_t(k) * 8;
@@ -687,26 +690,26 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         az[q] = make_float2(azs, azs);
         tk[q] = KEY_EMPTY;
         // ORDERED: a seed bound tau0 >= the k-th smallest s32 of the query,
-        // from the 32 references around its place in the spatial order:
+        // from the KL_SEED references around its place in the spatial order:
         // split into k groups, the largest of the groups' smallest s32 is
         // the s32 of one of k distinct references, so at least k references
         // have s32 <= tau0.  Until the heap is full the filter threshold is
         // that of tau0 instead of +inf (the heap then fills with near
         // references only); afterwards the smaller of the two.
         float tau0 = inf;
-        if (ORDERED && valid[q] && Nb >= 32) {
+        if (ORDERED && valid[q] && Nb >= KL_SEED) {
             const int pos = (a.squery == a.sref && a.Q == a.N && a.q_len == a.r_len)
                                 ? qi[q]
                                 : a.cstart[size_t(b) * (MC_CELLS + 1) +
                                            mc_code(a.cframe + size_t(b) * 8, qx[q],
                                                    qy[q], qz[q])];
-            const int p0 = min(max(pos - 16, 0), Nb - 32);
+            const int p0 = min(max(pos - KL_SEED / 2, 0), Nb - KL_SEED);
             const float4 *w4 = reinterpret_cast<const float4 *>(cref) + p0;
-            const int gs = 32 / k;  // group size (k groups)
+            const int gs = KL_SEED / k;  // group size (k groups)
             float worst = 0.0f, gm = inf;
             bool bad = false;
 #pragma unroll 8
-            for (int t = 0; t < 32; ++t) {
+            for (int t = 0; t < KL_SEED; ++t) {
                 const float4 r = w4[t];
                 gm = fminf(gm, sqdist(qx[q], qy[q], qz[q], r.x, r.y, r.z));
                 if (t % gs == gs - 1 && t / gs < k) {
