@@ -998,9 +998,15 @@ __global__ void __launch_bounds__(1024) mc_scan_kernel(const int *hist, int *sta
     int *st = start + size_t(b) * (MC_CELLS + 1);
     int *cu = cursor + size_t(b) * (MC_CELLS + 1);
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    constexpr int ROWS = MC_CELLS / 1024;
+    int vr[ROWS];  // every row's count of this thread, loaded up front
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) vr[r] = h[r * 1024 + t];
     int carry = 0;
-    for (int r = 0; r < MC_CELLS; r += 1024) {
-        const int v = h[r + t];
+#pragma unroll
+    for (int rr = 0; rr < ROWS; ++rr) {
+        const int r = rr * 1024;
+        const int v = vr[rr];
         int x = v;  // inclusive scan within the warp
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
