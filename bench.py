@@ -717,23 +717,30 @@ def run_e2e(args, pc, x_host, device, world):
 
     main = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device) if not args.serial else main
+    # the kNN results are read back while Ball Query runs, the FPS result
+    # once FPS ends; only the Ball Query read-back follows the last kernel
+    copy = torch.cuda.Stream(device) if not args.serial else main
     reserve = 0 if args.serial else pc.pc_fps_sm_count(1, N, npoint)
 
     def one():
         xd = x_pin.to(device, non_blocking=True)
         side.wait_stream(main)
         f = pc.pc_fps(xd, npoint, 0)
+        outs["fps"].copy_(f, non_blocking=True)
         with torch.cuda.stream(side):
             pc.pc_set_sm_reserve(reserve)
             d, i = pc.pc_knn(xd, xd, k)
+            copy.wait_stream(side)
             d2, i2 = pc.pc_ball_query(xd, xd, r, K)
             pc.pc_set_sm_reserve(0)
+        with torch.cuda.stream(copy):
+            for t in (d, i):
+                t.record_stream(copy)
+            outs["knn_d"].copy_(d, non_blocking=True)
+            outs["knn_i"].copy_(i, non_blocking=True)
         main.wait_stream(side)
-        for t in (d, i, d2, i2):
+        for t in (d2, i2):
             t.record_stream(main)
-        outs["fps"].copy_(f, non_blocking=True)
-        outs["knn_d"].copy_(d, non_blocking=True)
-        outs["knn_i"].copy_(i, non_blocking=True)
         outs["bq_d"].copy_(d2, non_blocking=True)
         outs["bq_i"].copy_(i2, non_blocking=True)
         torch.cuda.synchronize(device)

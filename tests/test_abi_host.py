@@ -132,6 +132,17 @@ def test_wait_timeout_setter_accepts_any_value(L):
     L.pc_debug_set_fps_grid_stall(0)
 
 
+def test_sm_reserve_and_fps_sm_count_without_device(L):
+    # the reserve is a host-side hint: any value is taken (negative as 0)
+    L.pc_set_sm_reserve(-5)
+    L.pc_set_sm_reserve(16)
+    L.pc_set_sm_reserve(0)
+    # no device here: the FPS footprint is unknown (0), as for empty sizes
+    assert L.pc_fps_sm_count(1, 100000, 4096) == 0
+    assert L.pc_fps_sm_count(0, 100000, 4096) == 0
+    assert L.pc_fps_sm_count(1, 0, 4096) == 0
+
+
 def test_knn_ex_validation(L):
     # k > N is allowed in the ex form (padded); k above 256 is unsupported
     assert L.pc_knn_ex(None, 0, 4, None, 8, 300, None, None, 0, None, None, None) == 2
