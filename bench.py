@@ -187,7 +187,7 @@ KERNEL_SOURCES = {
     "knn": ["pc_knn.cu", "pc_device.cuh", "pc_filter.cuh", "pc_stream.cuh",
             "pc_tiles.cuh"],
     "ball_query": ["pc_ball_query.cu", "pc_device.cuh", "pc_filter.cuh",
-                   "pc_tiles.cuh"],
+                   "pc_stream.cuh", "pc_tiles.cuh"],
     "fps": ["pc_fps.cu", "pc_device.cuh"],
     "grid_knn": ["pc_grid.cu", "pc_device.cuh"],
     "grid_ball_query": ["pc_grid.cu", "pc_device.cuh"],

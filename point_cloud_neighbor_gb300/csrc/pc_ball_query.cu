@@ -34,6 +34,7 @@
 #include "pc_device.cuh"
 #include "pc_filter.cuh"
 #include "pc_internal.h"
+#include "pc_stream.cuh"
 #include "pc_tiles.cuh"
 
 #include <algorithm>
@@ -41,12 +42,11 @@
 namespace pcn {
 namespace {
 
-constexpr int BQ_R = 8;
-constexpr int BQ_T = 32 * BQ_R;
+constexpr int BQ_R = 8;  // reference points per lane per tile
 constexpr int BQ_CWARPS = 8;
 constexpr int BQ_THREADS = 32 * (BQ_CWARPS + 1);
-constexpr int BQ_STAGES = 4;
 constexpr unsigned FULL = 0xffffffffu;
+static_assert(32 * BQ_R == ST_T, "a lane holds 8 of a stream tile's points");
 
 struct BqArgs {
     const float *query;
@@ -69,13 +69,14 @@ struct __align__(16) BqSlot {
     float4 raw;  // (x, y, z, hits so far (int bits))
 };
 
-constexpr unsigned BQ_BUF = tile_buffer_bytes(BQ_T);
+// Swizzle bits of the prepared stages: lanes read pairs l + 32 r, i.e. four
+// consecutive pairs of each of eight steps, and with 3 bits two consecutive
+// steps use complementary halves of the bank groups.
+constexpr int BQ_SB = 3;
 
-__host__ __device__ constexpr size_t bq_fixed_smem() {
-    // ring, 2 * STAGES mbarriers, flags (error, stop, warps done)
-    return size_t(BQ_STAGES) * BQ_BUF + 2 * BQ_STAGES * 8 + 16;
-}
-
+__host__ __device__ constexpr size_t bq_fixed_smem() { return stream_smem_bytes(); }
+// the query slots that follow hold float4s
+static_assert(bq_fixed_smem() % alignof(BqSlot) == 0, "query slots 16-byte aligned");
 
 // Valid length of cloud b: lens[b] clamped to [0, full], or full.
 __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
@@ -84,11 +85,14 @@ __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
     return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
 }
 
-// Slow path, taken only when a vote let a pair through: the lane's filter
-// mask is recomputed from its registers, points that pass get their exact
-// s32 from the raw tile in shared memory (lane l: points l + 32 r), and hits
-// are recorded in input order.  Returns the new hit count (<= K).
-__device__ __forceinline__ int bq_record(const float *tile,
+// Slow path, taken only when a vote let a pair through.  Lane l holds the
+// pairs l + 32 r (points 2 (l + 32 r) + h, bit 2r + h of its filter mask),
+// so for each r the warp holds the 64 consecutive references
+// [64 r, 64 r + 64) in (lane, h) order.  The mask is recomputed, points that
+// pass get their exact s32 from the stage's raw copy, and hits are recorded
+// in input order: two ballots (h = 0, 1) rank every hit of the row.
+// Returns the new hit count (<= K).
+__device__ __forceinline__ int bq_record(const float4 *raw,
                                          const float2 (&rx)[BQ_R / 2],
                                          const float2 (&ry)[BQ_R / 2],
                                          const float2 (&rz)[BQ_R / 2],
@@ -100,25 +104,36 @@ __device__ __forceinline__ int bq_record(const float *tile,
     const int lane = static_cast<int>(lane_id());
     const unsigned pm = filter_mask8(rx, ry, rz, rw, axy, azt);
     // rows r where some lane may hold a hit, in increasing r (input order)
-    unsigned rows = __reduce_or_sync(FULL, pm);
+    const unsigned any = __reduce_or_sync(FULL, pm);
+    unsigned rows = (any | (any >> 1)) & 0x55u;
+    const unsigned lt = lanemask_lt();
     while (rows) {
-        const int r = __ffs(rows) - 1;
+        const int r = (__ffs(rows) - 1) >> 1;
         rows &= rows - 1;
-        float s = 0.f;
-        bool hit = false;
-        if (((pm >> r) & 1u) && r * 32 + lane < cnt) {
-            const float *p = tile + 3 * (lane + 32 * r);
-            s = sqdist(q.x, q.y, q.z, p[0], p[1], p[2]);
-            hit = s < R2;
-        }
-        const unsigned bal = __ballot_sync(FULL, hit);
-        if (bal) {
-            const int pos = hits + __popc(bal & lanemask_lt());
-            if (hit && pos < K) {
-                out_idx[row * K + pos] = j0 + r * 32 + lane;
-                out_dist2[row * K + pos] = s;
+        float s[2] = {0.f, 0.f};
+        bool hit[2] = {false, false};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = 2 * (lane + 32 * r) + h;  // point in the tile
+            if (((pm >> (2 * r + h)) & 1u) && i < cnt) {
+                const float4 p = raw[raw_slot(i)];
+                s[h] = sqdist(q.x, q.y, q.z, p.x, p.y, p.z);
+                hit[h] = s[h] < R2;
             }
-            hits += __popc(bal);
+        }
+        const unsigned b0 = __ballot_sync(FULL, hit[0]);
+        const unsigned b1 = __ballot_sync(FULL, hit[1]);
+        if (b0 | b1) {
+            const int before = hits + __popc(b0 & lt) + __popc(b1 & lt);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int pos = before + (h == 1 && hit[0] ? 1 : 0);
+                if (hit[h] && pos < K) {
+                    out_idx[row * K + pos] = j0 + 2 * (lane + 32 * r) + h;
+                    out_dist2[row * K + pos] = s[h];
+                }
+            }
+            hits += __popc(b0) + __popc(b1);
             if (hits >= K) break;
         }
     }
@@ -133,20 +148,17 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     const int G = a.q_per_warp;
     const int K = a.K;
 
-    TileRing ring;
-    ring.base = smem;
-    ring.bytes = BQ_BUF;
-    ring.full = reinterpret_cast<uint64_t *>(smem + BQ_STAGES * BQ_BUF);
-    ring.empty = ring.full + BQ_STAGES;
-    int *s_err = reinterpret_cast<int *>(ring.empty + BQ_STAGES);
-    int *s_stop = s_err + 1;
-    int *s_ndone = s_err + 2;
+    StreamRing ring;
+    int *flags = stream_carve(smem, ring);
+    int *s_err = flags;
+    int *s_stop = flags + 1;
+    int *s_ndone = flags + 2;
     BqSlot *slots_all = reinterpret_cast<BqSlot *>(smem + bq_fixed_smem());
 
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
     const int Nb = valid_len(a.r_len, b, a.N);
     const int Qb = valid_len(a.q_len, b, a.Q);
-    const int ntiles = (Nb + BQ_T - 1) / BQ_T;
+    const int ntiles = (Nb + ST_T - 1) / ST_T;
 
     if (blockIdx.x * BQ_CWARPS * G >= Qb) {
         // every query of this block is past the cloud's valid length
@@ -162,22 +174,17 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     }
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < BQ_STAGES; ++s) {
-            mbar_init(&ring.full[s], 1);
-            mbar_init(&ring.empty[s], BQ_CWARPS);
-        }
+        stream_init(ring, BQ_CWARPS);
         *s_err = 0;
         *s_stop = 0;
         *s_ndone = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    const FilterFrame fr = filter_frame(cref, min(ST_T, Nb));
+    __syncthreads();
 
-    if (warp == BQ_CWARPS) {  // producer warp
-        __syncthreads();
-        if (lane == 0)
-            ring_produce<BQ_STAGES>(
-                ring, cref, Nb, BQ_T, ntiles, [](int it) { return it; },
-                s_stop, s_err, a.timeout_ns);
+    if (warp == BQ_CWARPS) {  // producer warp: tiles strictly in input order
+        stream_produce<BQ_SB, false>(ring, cref, Nb, ntiles, [](int it) { return it; },
+                                     fr, s_stop, s_err, a.timeout_ns);
         return;
     }
 
@@ -185,7 +192,6 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     const int nq = max(0, min(G, Qb - q_warp0));
     BqSlot *slots = slots_all + warp * G;
     const float *cq = a.query + size_t(b) * size_t(a.Q) * 3;
-    const FilterFrame fr = filter_frame(cref, min(BQ_T, Nb));
     for (int g = lane; g < G; g += 32) {
         float x = 0.f, y = 0.f, z = 0.f;
         if (g < nq) {
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
         slots[g].azt = make_float4(az, az, thr, __int_as_float(g));
         slots[g].raw = make_float4(x, y, z, __int_as_float(0));
     }
-    __syncthreads();
+    __syncwarp();
 
     // Queries still short of K hits occupy slots [0, active); a query that
     // fills up is swapped behind them, so the hot loop checks nothing per
@@ -214,41 +220,37 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     bool failed = false;
     for (int it = 0; it < ntiles; ++it) {
         if (__any_sync(FULL, *vstop != 0)) break;
-        const int st = it % BQ_STAGES;
-        const WaitResult w = mbar_wait_or_stop(
-            &ring.full[st], unsigned((it / BQ_STAGES) & 1), s_stop, a.timeout_ns);
-        if (!__all_sync(FULL, w == WAIT_OK)) {
-            failed = !__all_sync(FULL, w != WAIT_TIMEOUT);
+        const int st = it % ST_STAGES;
+        const WaitResult w = warp_wait(&ring.ready[st], unsigned((it / ST_STAGES) & 1),
+                                       s_stop, a.timeout_ns);
+        if (w != WAIT_OK) {
+            failed = w == WAIT_TIMEOUT;
             break;
         }
-        const int j0 = it * BQ_T;
-        const int cnt = min(BQ_T, Nb - j0);
-        const float *buf =
-            ring.buf(st) + tile_float_offset(cref + size_t(j0) * 3);
+        const int j0 = it * ST_T;
+        const int cnt = min(ST_T, Nb - j0);
+        const float4 *ck = ring.cooked_tile(st);
+        const float4 *raw = ring.raw_copy(st);
         if (active > 0) {
-            // centred coordinates and w' of this lane's points (points past
-            // cnt hold stale values: they may pass and are masked exactly)
+            // the prepared points of this lane: pairs l + 32 p (points past
+            // cnt are (0, 0, 0, +inf): they pass only an infinite threshold
+            // and are masked exactly)
             float2 rx[BQ_R / 2], ry[BQ_R / 2], rz[BQ_R / 2], rw[BQ_R / 2];
 #pragma unroll
             for (int p = 0; p < BQ_R / 2; ++p) {
-                const float *p0 = buf + 3 * (lane + 32 * (2 * p));
-                const float *p1 = buf + 3 * (lane + 32 * (2 * p + 1));
-                float x0 = __fsub_rn(p0[0], fr.cx), y0 = __fsub_rn(p0[1], fr.cy),
-                      z0 = __fsub_rn(p0[2], fr.cz);
-                float x1 = __fsub_rn(p1[0], fr.cx), y1 = __fsub_rn(p1[1], fr.cy),
-                      z1 = __fsub_rn(p1[2], fr.cz);
-                const float w0 = filter_ref(x0, y0, z0), w1 = filter_ref(x1, y1, z1);
-                rx[p] = make_float2(x0, x1);
-                ry[p] = make_float2(y0, y1);
-                rz[p] = make_float2(z0, z1);
-                rw[p] = make_float2(w0, w1);
+                const float4 A = ck[cooked_slot<BQ_SB>(lane + 32 * p, 0)];
+                const float4 Z = ck[cooked_slot<BQ_SB>(lane + 32 * p, 1)];
+                rx[p] = make_float2(A.x, A.y);
+                ry[p] = make_float2(A.z, A.w);
+                rz[p] = make_float2(Z.x, Z.y);
+                rw[p] = make_float2(Z.z, Z.w);
             }
 
             bool any_full = false;
             auto record = [&](BqSlot *sp, float4 axy, float4 azt) {
                 const float4 q = sp->raw;
                 const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(azt.w);
-                const int h = bq_record(buf, rx, ry, rz, rw, axy, azt, q,
+                const int h = bq_record(raw, rx, ry, rz, rw, axy, azt, q,
                                         __float_as_int(q.w), j0, cnt, a.R2, K, row,
                                         a.out_dist2, a.out_idx);
                 if (lane == 0) sp->raw.w = __int_as_float(h);
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[st]);  // raw tile no longer read
+        if (lane == 0) mbar_arrive(&ring.empty[st]);  // stage no longer read
     }
 
     if (failed) {

@@ -73,11 +73,14 @@ struct StreamRing {
     }
 };
 
-// Shared memory of the rings plus 16 bytes of flags (error, stop, warps done).
+// Shared memory of the rings plus 16 bytes of flags (error, stop, warps
+// done), rounded up to 16 bytes so that whatever follows may hold 16-byte
+// vectors.
 __host__ __device__ constexpr size_t stream_smem_bytes() {
-    return size_t(ST_STAGES) * ST_STAGE + size_t(ST_RAW_STAGES) * ST_RAW +
-           (ST_RAW_STAGES + 2 * ST_STAGES) * 8 + 16;
+    return (size_t(ST_STAGES) * ST_STAGE + size_t(ST_RAW_STAGES) * ST_RAW +
+            (ST_RAW_STAGES + 2 * ST_STAGES) * 8 + 16 + 15) & ~size_t(15);
 }
+static_assert(stream_smem_bytes() % 16 == 0, "16-byte aligned end");
 
 // Carve the rings out of `smem` (16-byte aligned); returns the flag words.
 __device__ __forceinline__ int *stream_carve(unsigned char *smem, StreamRing &r) {
