@@ -313,7 +313,9 @@ typedef enum pc_reduction {
  *   out_dist_y, out_idx_y  [B, P2], the other direction.
  *   out_loss   float32, device, or NULL (no reduction).  Sums are formed in
  *              float64 in a fixed order and rounded once to float32.
- * Launches: one kNN kernel (both directions) and one reduction kernel.
+ * Launches: one kNN kernel (both directions), then with out_loss one
+ * reduction block per cloud and, for a batch SUM or MEAN, one more block
+ * (the clouds' losses in stream-ordered scratch of B doubles).
  *
  * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_UNSUPPORTED, PC_ERR_CUDA or
  * PC_ERR_NO_DEVICE.

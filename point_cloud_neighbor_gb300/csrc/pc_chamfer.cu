@@ -10,10 +10,12 @@
 //     the clouds' valid lengths and the squared distance returned: nearest
 //     index and s32 with exact ties to the smaller index; the two directions
 //     share one launch;
-//   * one block of 1024 threads reduces the per-point distances in float64
-//     in a fixed order (strided per thread, then a fixed shuffle tree), so
-//     the loss is deterministic from run to run and within a few float64
-//     roundings of the exact sum before its single rounding to float32.
+//   * one block of 1024 threads per cloud reduces its per-point distances in
+//     float64 in a fixed order (four strided partial sums per thread, then a
+//     fixed shuffle tree), and one more block sums the clouds' losses in the
+//     same way, so the loss is deterministic from run to run and within a few
+//     float64 roundings of the exact sum before its single rounding to
+//     float32.
 // Readings: a point with no valid reference contributes 0 (index -1);
 // "mean" over points divides a cloud's sum by max(length, 1); weights scale
 // each cloud's loss; "mean" over the batch divides by B (0 for B = 0).
@@ -37,6 +39,7 @@ struct ChamferReduceArgs {
     int point_mean;          // 1: mean over points, 0: sum
     int batch_mode;          // PC_REDUCTION_NONE / SUM / MEAN
     float *out_loss;
+    double *cloud_loss;      // [B] scratch (SUM / MEAN)
 };
 
 __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
@@ -45,11 +48,21 @@ __device__ __forceinline__ int valid_len(const int64_t *lens, int b, int full) {
     return v < 0 ? 0 : (v > full ? full : static_cast<int>(v));
 }
 
-// Sum of v[0..n) in float64 over the whole block, in a fixed order; the
+// Sum of v[0..n) in float64 over the whole block, in a fixed order (four
+// strided partial sums per thread, so that four loads are in flight); the
 // result is returned to every thread.
-__device__ double block_sum(const float *v, int n, double *part) {
-    double acc = 0.0;
-    for (int i = threadIdx.x; i < n; i += RED_THREADS) acc += double(v[i]);
+template <class T>
+__device__ double block_sum(const T *v, int n, double *part) {
+    double a0 = 0.0, a1 = 0.0, a2 = 0.0, a3 = 0.0;
+    int i = threadIdx.x;
+    for (; i + 3 * RED_THREADS < n; i += 4 * RED_THREADS) {
+        a0 += double(v[i]);
+        a1 += double(v[i + RED_THREADS]);
+        a2 += double(v[i + 2 * RED_THREADS]);
+        a3 += double(v[i + 3 * RED_THREADS]);
+    }
+    for (; i < n; i += RED_THREADS) a0 += double(v[i]);
+    double acc = (a0 + a1) + (a2 + a3);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_down_sync(FULL, acc, o);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -67,32 +80,38 @@ __device__ double block_sum(const float *v, int n, double *part) {
     return r;
 }
 
+// One block per cloud: its loss, into out_loss[b] (NONE) or cloud_loss[b].
 __global__ void __launch_bounds__(RED_THREADS)
 chamfer_reduce_kernel(const ChamferReduceArgs a) {
     __shared__ double part[33];
-    double total = 0.0;
-    for (int b = 0; b < a.B; ++b) {
-        const int nx = valid_len(a.x_len, b, a.P1);
-        double t = block_sum(a.dist_x + size_t(b) * a.P1, nx, part);
-        if (a.point_mean) t = t / double(max(nx, 1));
-        if (a.dist_y != nullptr) {
-            const int ny = valid_len(a.y_len, b, a.P2);
-            double u = block_sum(a.dist_y + size_t(b) * a.P2, ny, part);
-            if (a.point_mean) u = u / double(max(ny, 1));
-            t = t + u;
-        }
-        if (a.weights != nullptr) t = t * double(a.weights[b]);
-        if (threadIdx.x == 0) {
-            if (a.batch_mode == PC_REDUCTION_NONE) a.out_loss[b] = float(t);
-            total += t;
-        }
+    const int b = blockIdx.x;
+    const int nx = valid_len(a.x_len, b, a.P1);
+    double t = block_sum(a.dist_x + size_t(b) * a.P1, nx, part);
+    if (a.point_mean) t = t / double(max(nx, 1));
+    if (a.dist_y != nullptr) {
+        const int ny = valid_len(a.y_len, b, a.P2);
+        double u = block_sum(a.dist_y + size_t(b) * a.P2, ny, part);
+        if (a.point_mean) u = u / double(max(ny, 1));
+        t = t + u;
     }
+    if (a.weights != nullptr) t = t * double(a.weights[b]);
     if (threadIdx.x == 0) {
-        if (a.batch_mode == PC_REDUCTION_SUM)
-            a.out_loss[0] = float(total);
-        else if (a.batch_mode == PC_REDUCTION_MEAN)
-            a.out_loss[0] = a.B > 0 ? float(total / double(a.B)) : 0.0f;
+        if (a.batch_mode == PC_REDUCTION_NONE)
+            a.out_loss[b] = float(t);
+        else
+            a.cloud_loss[b] = t;
     }
+}
+
+// The batch reduction (SUM / MEAN) over the clouds' losses, one block.
+__global__ void __launch_bounds__(RED_THREADS)
+chamfer_batch_kernel(const ChamferReduceArgs a) {
+    __shared__ double part[33];
+    const double total = block_sum(a.cloud_loss, a.B, part);
+    if (threadIdx.x == 0)
+        a.out_loss[0] = a.batch_mode == PC_REDUCTION_SUM
+                            ? float(total)
+                            : (a.B > 0 ? float(total / double(a.B)) : 0.0f);
 }
 
 }  // namespace
@@ -187,8 +206,24 @@ extern "C" int pc_chamfer(const float *x, int64_t B, int64_t P1,
         a.point_mean = point_reduction == PC_REDUCTION_MEAN;
         a.batch_mode = batch_reduction;
         a.out_loss = out_loss;
-        pcn::chamfer_reduce_kernel<<<1, pcn::RED_THREADS, 0, st>>>(a);
-        e = cudaGetLastError();
+        if (batch_reduction == PC_REDUCTION_NONE) {
+            if (B > 0) pcn::chamfer_reduce_kernel<<<unsigned(B), pcn::RED_THREADS, 0, st>>>(a);
+            e = cudaGetLastError();
+        } else {
+            // the clouds' losses in stream-ordered scratch, then their sum
+            double *cl = nullptr;
+            e = cudaMallocAsync(reinterpret_cast<void **>(&cl),
+                                size_t(B > 0 ? B : 1) * sizeof(double), st);
+            if (e == cudaSuccess) {
+                a.cloud_loss = cl;
+                if (B > 0)
+                    pcn::chamfer_reduce_kernel<<<unsigned(B), pcn::RED_THREADS, 0, st>>>(a);
+                pcn::chamfer_batch_kernel<<<1, pcn::RED_THREADS, 0, st>>>(a);
+                e = cudaGetLastError();
+                const cudaError_t f = cudaFreeAsync(cl, st);
+                if (e == cudaSuccess) e = f;
+            }
+        }
     }
     if (e != cudaSuccess) {
         char m[200];
