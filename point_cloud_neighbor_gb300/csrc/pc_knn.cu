@@ -988,50 +988,60 @@ __global__ void __launch_bounds__(256) mc_count_kernel(const float *pts,
 }
 
 // Exclusive scan of each cloud's MC_CELLS counts into start[0 .. MC_CELLS]
-// (start[MC_CELLS] = total) and cursor (a copy of the starts): rows of 1024
-// counts, each scanned by the block (coalesced), with a running carry.
-__global__ void __launch_bounds__(1024) mc_scan_kernel(const int *hist, int *start,
-                                                       int *cursor) {
-    __shared__ int wsum[32];
-    const int b = blockIdx.x;
-    const int *h = hist + size_t(b) * (MC_CELLS + 1);
-    int *st = start + size_t(b) * (MC_CELLS + 1);
-    int *cu = cursor + size_t(b) * (MC_CELLS + 1);
-    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    constexpr int ROWS = MC_CELLS / 1024;
-    int vr[ROWS];  // every row's count of this thread, loaded up front
+// (start[MC_CELLS] = total) and cursor (a copy of the starts), in chunks of
+// 1024 counts, one block each: mc_chunk_sum_kernel totals every chunk,
+// mc_scan_kernel scans a chunk and adds the totals of the chunks before it.
+constexpr int MC_CHUNKS = MC_CELLS / 1024;
+
+// Inclusive scan of v over the 1024 threads of the block (wsum: 32 ints of
+// shared memory); returns the block total in *total.
+__device__ __forceinline__ int block_scan_1024(int v, int *wsum, int *total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
 #pragma unroll
-    for (int r = 0; r < ROWS; ++r) vr[r] = h[r * 1024 + t];
-    int carry = 0;
-#pragma unroll
-    for (int rr = 0; rr < ROWS; ++rr) {
-        const int r = rr * 1024;
-        const int v = vr[rr];
-        int x = v;  // inclusive scan within the warp
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int z = wsum[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(FULL, x, o);
-            if (lane >= o) x += y;
+            const int y = __shfl_up_sync(FULL, z, o);
+            if (lane >= o) z += y;
         }
-        if (lane == 31) wsum[w] = x;
-        __syncthreads();
-        if (w == 0) {
-            int z = wsum[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(FULL, z, o);
-                if (lane >= o) z += y;
-            }
-            wsum[lane] = z;
-        }
-        __syncthreads();
-        const int excl = carry + x - v + (w > 0 ? wsum[w - 1] : 0);
-        st[r + t] = excl;
-        cu[r + t] = excl;
-        carry += wsum[31];
-        __syncthreads();  // wsum is rewritten by the next row
+        wsum[lane] = z;
     }
-    if (t == 0) st[MC_CELLS] = carry;
+    __syncthreads();
+    *total = wsum[31];
+    return x + (w > 0 ? wsum[w - 1] : 0);
+}
+
+__global__ void __launch_bounds__(1024) mc_chunk_sum_kernel(const int *hist, int *chunk) {
+    __shared__ int wsum[32];
+    const int b = blockIdx.y, c = blockIdx.x;
+    const int v = hist[size_t(b) * (MC_CELLS + 1) + c * 1024 + threadIdx.x];
+    int total;
+    block_scan_1024(v, wsum, &total);
+    if (threadIdx.x == 0) chunk[b * MC_CHUNKS + c] = total;
+}
+
+__global__ void __launch_bounds__(1024) mc_scan_kernel(const int *hist, const int *chunk,
+                                                       int *start, int *cursor) {
+    __shared__ int wsum[32];
+    const int b = blockIdx.y, c = blockIdx.x;
+    int before = 0;  // the chunks before this one, in order
+    for (int i = 0; i < c; ++i) before += chunk[b * MC_CHUNKS + i];
+    const size_t e = size_t(b) * (MC_CELLS + 1) + c * 1024 + threadIdx.x;
+    const int v = hist[e];
+    int total;
+    const int incl = block_scan_1024(v, wsum, &total);
+    start[e] = before + incl - v;
+    cursor[e] = before + incl - v;
+    if (c == MC_CHUNKS - 1 && threadIdx.x == 1023)
+        start[size_t(b) * (MC_CELLS + 1) + MC_CELLS] = before + total;
 }
 
 __global__ void __launch_bounds__(256) mc_scatter_kernel(const float *pts,
@@ -1061,7 +1071,9 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
     const size_t off_start = off_hist + 2 * cells;
     const size_t off_cur = off_start + cells;
     const size_t off_curq = off_cur + cells;
-    const size_t off_sref = (off_curq + cells + 255) & ~size_t(255);
+    const size_t off_chunk = (off_curq + cells + 255) & ~size_t(255);
+    const size_t off_sref =
+        (off_chunk + 2 * size_t(B) * MC_CHUNKS * sizeof(int) + 255) & ~size_t(255);
     const size_t off_sq = off_sref + ((size_t(B) * a.N * 16 + 255) & ~size_t(255));
     // few queries against many references: split the references into parts
     // (blocks of the same queries, other tiles), about 10 warps per SM
@@ -1081,6 +1093,8 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
     int *start = reinterpret_cast<int *>(base + off_start);
     int *cur = reinterpret_cast<int *>(base + off_cur);
     int *curq = reinterpret_cast<int *>(base + off_curq);
+    int *chunk = reinterpret_cast<int *>(base + off_chunk);
+    int *chunkq = chunk + B * MC_CHUNKS;
     float4 *sref = reinterpret_cast<float4 *>(base + off_sref);
     float4 *sq = self ? sref : reinterpret_cast<float4 *>(base + off_sq);
     int *histq = hist + size_t(B) * (MC_CELLS + 1);
@@ -1090,12 +1104,15 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
     if (e == cudaSuccess) {
         mc_frame_kernel<<<unsigned(B), 256, 0, stream>>>(a.ref, a.r_len, a.N, frame);
         mc_count_kernel<<<gr, 256, 0, stream>>>(a.ref, a.r_len, a.N, frame, hist);
-        mc_scan_kernel<<<unsigned(B), 1024, 0, stream>>>(hist, start, cur);
+        const dim3 gc(MC_CHUNKS, unsigned(B));
+        mc_chunk_sum_kernel<<<gc, 1024, 0, stream>>>(hist, chunk);
+        mc_scan_kernel<<<gc, 1024, 0, stream>>>(hist, chunk, start, cur);
         mc_scatter_kernel<<<gr, 256, 0, stream>>>(a.ref, a.r_len, a.N, frame, cur, sref);
         if (!self) {
             // the query starts are only cursors: scan into curq twice over
             mc_count_kernel<<<gq, 256, 0, stream>>>(a.query, a.q_len, a.Q, frame, histq);
-            mc_scan_kernel<<<unsigned(B), 1024, 0, stream>>>(histq, curq, curq);
+            mc_chunk_sum_kernel<<<gc, 1024, 0, stream>>>(histq, chunkq);
+            mc_scan_kernel<<<gc, 1024, 0, stream>>>(histq, chunkq, curq, curq);
             mc_scatter_kernel<<<gq, 256, 0, stream>>>(a.query, a.q_len, a.Q, frame, curq,
                                                       sq);
         }
