@@ -195,11 +195,17 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(op: str) -> str:
+    """Hash of the code of an operator's sources: line comments, trailing
+    blanks and blank lines do not count, so that editing a comment keeps a
+    capture valid while any change of code does not."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[op]:
         with open(os.path.join(ROOT, "point_cloud_neighbor_gb300", "csrc", name),
-                  "rb") as fh:
-            h.update(fh.read())
+                  encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -5,7 +5,12 @@
 // that come first in (s, j) order -- squared distance, then index -- with
 // D = sqrt(s).
 //
-// Design (one launch, no scratch memory):
+// Two kernels.  k <= 32: knn_lane_kernel (below), one or two queries per
+// lane with per-lane heaps, fed by a producer warp that prepares the tiles
+// (pc_stream.cuh); large clouds are first put in a spatial order (a few
+// small kernels and stream-ordered scratch) that the kernel visits outwards
+// from each block's region.  k > 32: knn_kernel, described here (one launch,
+// no scratch memory):
 //  * A block has KNN_CWARPS consumer warps and one producer warp.  Consumer
 //    warp w owns G queries of one cloud.  Per query, shared memory holds the
 //    filter constants (-2q', -2q', thr, thr; pc_filter.cuh), the raw
@@ -460,17 +465,21 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// k <= 32: one query per lane (the kernel used for every k up to 32).
+// k <= 32: a lane owns one or two queries (the kernel used for every k up to
+// 32).
 //
-// The producer warp streams the tiles in the scrambled order and prepares
-// them (pc_stream.cuh).  A lane keeps its query's current k best (s, j) as a
-// max-heap in shared memory (entry e of lane l at [e * 32 + l], lexicographic
-// (s, j) order, root = the k-th best) and the root in registers; its filter
-// threshold follows the root.  Per step the lane filters 8 points (three
-// packed FMAs per two points, broadcast shared-memory operands); on a pass it
-// recomputes which points passed, takes their exact s32 from the raw tile
-// and replaces the root by every point that beats it (sift-down).  At the end
-// each lane heap-sorts its k entries into ascending (s, j) order.
+// The producer warp streams the tiles (scrambled order, or outwards from the
+// block's home tile in the spatial order) and prepares them
+// (pc_stream.cuh).  A lane keeps each query's current k best (s, j) as a
+// max-heap of 64-bit keys in shared memory (entry e of lane l at
+// [e * 32 + l], root = the k-th best) and the query's filter threshold in a
+// register, following the root.  Pass 1, per tile: each 8-point step is
+// filtered (three packed FMAs per two points, broadcast shared-memory
+// operands) and sets one bit of a pending mask when anything passes.  Pass
+// 2: while any lane has a pending step, each such lane re-filters one,
+// takes the exact s32 of the points that pass from the stage's raw copy and
+// replaces the root by every point that beats it (sift-down).  At the end
+// each lane heap-sorts its k keys into ascending (s, j) order.
 // ---------------------------------------------------------------------------
 // QL queries per lane: 2 for k <= 16, 1 above.  A warp owns a group of
 // 32 * QL consecutive queries.
