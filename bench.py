@@ -312,7 +312,10 @@ def run_gpu(args):
         torch.cuda.synchronize(device)
     wall1 = time.perf_counter()
     barrier(world)
-    launches = 3 * args.steps
+    # kernels of one step: FPS 1; kNN on this cloud (spatially ordered: the
+    # query set is the reference set) frame, count, chunk sums, scan, scatter
+    # and the lane kernel = 6 (plus a memset of the cell counts); Ball Query 1
+    launches = (1 + 6 + 1) * args.steps
 
     # each operator timed on the stream it runs on
     t_fps = [e[0].elapsed_time(e[1]) for e in events]
@@ -329,6 +332,8 @@ def run_gpu(args):
     bq_idx = bq_i.cpu().numpy().reshape(N, K)
     last = bq_idx[:, K - 1]
     bq_pairs = float(np.where(last >= 0, last + 1, N).sum())   # first-K scan length
+    # the same scan rounded up to whole blocks of 32 references
+    bq_pairs_32 = float(np.minimum(N, 32 * ((np.where(last >= 0, last + 1, N) + 31) // 32)).sum())
     knn_pairs = float(N) * float(N)
     fps_bytes = float(N) * (npoint - 1) * FPS_BYTES_PER_POINT_STEP
 
@@ -359,10 +364,28 @@ def run_gpu(args):
         },
         "ball_query": {
             "queries_per_s": N * world / (per["ball_query"] / 1e3),
-            "ms": per["ball_query"], "pairs": bq_pairs,
+            "ms": per["ball_query"], "pairs": bq_pairs, "pairs_blocks_of_32": bq_pairs_32,
             "achieved_tflops": bq_pairs * FLOPS_PER_PAIR / (per["ball_query"] / 1e3) / 1e12,
         },
     }
+    # FPS against its two other bounds: ~10 instructions per point-step on the
+    # SMs its schedule uses, and the per-step exchange floor measured with the
+    # same cluster schedule on 1024 points per block
+    fps_sms = pc.pc_fps_sm_count(B, N, npoint)
+    ops["fps"]["alu_bound_ms"] = (float(N) * (npoint - 1) * 10 /
+                                  (max(fps_sms, 1) * 128 * max_mhz * 1e6) * 1e3)
+    if fps_sms > 1:
+        fx = torch.from_numpy(inputs.random_cloud(7, 1, 1024 * fps_sms)).to(device)
+        try:
+            floor_ms = _timed(lambda: pc.pc_fps(fx, npoint, 0, strategy=pc.PC_FPS_CLUSTER,
+                                                cluster_size=fps_sms),
+                              3, 3, flush, stream)
+            ops["fps"]["sync_floor_ms"] = floor_ms
+            ops["fps"]["sync_floor_note"] = (
+                f"the same cluster of {fps_sms} on 1024 points per block, npoint={npoint}")
+        except pc.PointCloudError as err:
+            ops["fps"]["sync_floor_ms"] = None
+            ops["fps"]["sync_floor_note"] = f"not measured: {err}"
     for op in ("knn", "ball_query"):
         ops[op]["alu_frac_max_clock"] = ops[op]["achieved_tflops"] / alu_peak
         if clk["sm_mhz"]:
