@@ -97,10 +97,13 @@ def test_sm_reserve_only_changes_the_plan():
     n = pc.pc_fps_sm_count(1, 30000, 4096)
     assert 1 <= n <= torch.cuda.get_device_properties(0).multi_processor_count
     d0, i0 = pc.pc_knn(x, x, 12)
+    b0, j0 = pc.pc_ball_query(x, x, 0.05, 24)
     try:
         for reserve in (n, 100, 10_000):
             pc.pc_set_sm_reserve(reserve)
             d1, i1 = pc.pc_knn(x, x, 12)
             assert torch.equal(i0, i1) and torch.equal(d0, d1), reserve
+            b1, j1 = pc.pc_ball_query(x, x, 0.05, 24)
+            assert torch.equal(j0, j1) and torch.equal(b0, b1), reserve
     finally:
         pc.pc_set_sm_reserve(0)
