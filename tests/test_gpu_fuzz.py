@@ -96,3 +96,34 @@ def test_fuzz_fps_and_grid(case):
     wd, wi = oracle.knn(x, x, k, threads=THREADS)
     assert_idx_equal(gi.cpu().numpy().reshape(-1, k), wi, f"fuzz grid knn N={N}")
     assert_dist_equal(gd.cpu().numpy().reshape(-1, k), wd, f"fuzz grid knn N={N}")
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_fuzz_knn_spatially_ordered(case):
+    # clouds large enough for the spatially ordered kNN (>= 16384 references,
+    # >= 4096 queries, 2 <= k <= 32), with lengths on half of the cases and
+    # the query set equal to the reference set on the other half; sampled
+    # rows against the oracle
+    rng = np.random.default_rng(7000 + case)
+    B = int(rng.integers(1, 3))
+    N = int(rng.choice([16384, 17000, 20001, 33333]))
+    k = int(rng.choice([2, 5, 8, 16, 17, 24, 32]))
+    x = cloud(rng, B, N)
+    same = case % 2 == 0
+    q = x if same else cloud(rng, B, int(rng.choice([4096, 5000, 9000])))
+    Q = q.shape[1]
+    ql = rl = None
+    if case % 4 == 1:
+        ql = rng.integers(Q // 2, Q + 1, B).astype(np.int64)
+        rl = rng.integers(N // 2, N + 1, B).astype(np.int64)
+    rows = np.unique(rng.integers(0, B * Q, 600))
+    if ql is None:
+        d, i = pc.pc_knn(to_dev(q), to_dev(x), k)
+        wd, wi = oracle.knn(q, x, k, rows=rows, threads=THREADS)
+    else:
+        d, i = pc.pc_knn(to_dev(q), to_dev(x), k, query_lengths=to_dev(ql),
+                         ref_lengths=to_dev(rl))
+        wd, wi = oracle.knn_masked(q, x, k, ql, rl, rows=rows, threads=THREADS)
+    what = f"fuzz ordered knn B={B} Q={Q} N={N} k={k} same={same} lengths={ql is not None}"
+    assert_idx_equal(i.cpu().numpy().reshape(-1, k)[rows], wi, what)
+    assert_dist_equal(d.cpu().numpy().reshape(-1, k)[rows], wd, what)
