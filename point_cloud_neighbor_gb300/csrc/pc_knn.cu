@@ -80,6 +80,9 @@ struct KnnArgs {
     // ORDERED with the references split into gridDim.z parts: each part's
     // sorted k keys per valid query row, [part][B][Q][k] (merged afterwards)
     unsigned long long *part_keys;
+    // ORDERED: per query (in the query order) the exact k best keys over its
+    // seeded tiles, as a max-heap [B][Q][k] (knn_seed_kernel)
+    const unsigned long long *seed;
 };
 
 // Cell codes of the spatial order: MC_BITS bits per axis, interleaved
@@ -493,9 +496,6 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // blocks set the time.)  One producer serves all W consumer warps.
 // consumer warps per block at most (one block per SM: registers)
 __host__ __device__ constexpr int kl_wmax(int QL) { return QL == 1 ? 15 : 12; }
-// references around a query's place in the spatial order that give its seed
-// bound (k groups of KL_SEED / k)
-constexpr int KL_SEED = 32;
 
 __host__ __device__ constexpr size_t knn_lane_smem(int k, int QL, int W) {
     return stream_smem_bytes() + size_t(W) * 32 * QL * size_t(k) * 8;
@@ -543,6 +543,72 @@ __device__ __forceinline__ unsigned long long heap_sift(unsigned long long *h, i
     }
     h[pos * 32] = key;
     return top;
+}
+
+// ORDERED: the reference tile seeded for the query at position qpos of the
+// query order: the tile of its place among the references (qpos itself when
+// the query set is the reference set, else the start of its cell); [lo, hi],
+// empty (hi < lo) without references.  (Seeding the two tiles next to it as
+// well measured slower at 100k points, k = 16: 2.21 vs 2.11 ms.)
+__device__ __forceinline__ void seed_tiles(const KnnArgs &a, int b, int qpos, float qx,
+                                           float qy, float qz, int ntiles, int &lo,
+                                           int &hi) {
+    const bool self = a.squery == a.sref && a.Q == a.N && a.q_len == a.r_len;
+    const int pos = self ? qpos
+                         : a.cstart[size_t(b) * (MC_CELLS + 1) +
+                                    mc_code(a.cframe + size_t(b) * 8, qx, qy, qz)];
+    const int h = min(pos / ST_T, ntiles - 1);
+    lo = max(h, 0);
+    hi = h;
+}
+
+// ORDERED: one thread per valid query: the exact k best (s, j) over its
+// seeded tile (up to ST_T references), kept as a max-heap of keys in
+// shared memory (entry e of a warp's lane l at [e * 32 + l]) and written out
+// as it stands.  Lanes of a warp hold neighbouring queries, so they read the
+// same references (broadcast loads).
+constexpr int SEED_THREADS = 256;
+
+__global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
+                                                                unsigned long long *seed) {
+    extern __shared__ __align__(16) unsigned long long seed_heaps[];
+    const int b = blockIdx.y;
+    const int i = blockIdx.x * SEED_THREADS + threadIdx.x;
+    const int Qb = valid_len(a.q_len, b, a.Q);
+    if (i >= Qb) return;
+    const int k = a.k;
+    const int Nb = valid_len(a.r_len, b, a.N);
+    const int ntiles = (Nb + ST_T - 1) / ST_T;
+    unsigned long long *h = seed_heaps + size_t(threadIdx.x >> 5) * 32 * k + (threadIdx.x & 31);
+    for (int e = 0; e < k; ++e) h[e * 32] = KEY_EMPTY;
+    const float4 qv = reinterpret_cast<const float4 *>(a.squery)[size_t(b) * a.Q + i];
+    int lo, hi;
+    seed_tiles(a, b, i, qv.x, qv.y, qv.z, ntiles, lo, hi);
+    const float4 *rp = reinterpret_cast<const float4 *>(a.sref) + size_t(b) * a.N;
+    unsigned long long root = KEY_EMPTY;
+    const int j1 = min(Nb, (hi + 1) * ST_T);
+    int j = lo * ST_T;
+    // four references at a time: their loads and distances are independent
+    for (; j + 4 <= j1; j += 4) {
+        unsigned long long key[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 r = rp[j + u];
+            // s32 >= +0; a NaN s32 has a key above KEY_EMPTY: never taken
+            key[u] = sj_key(sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z), __float_as_int(r.w));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (key[u] < root) root = heap_sift(h, k, 0, key[u]);
+    }
+    for (; j < j1; ++j) {
+        const float4 r = rp[j];
+        const unsigned long long key =
+            sj_key(sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z), __float_as_int(r.w));
+        if (key < root) root = heap_sift(h, k, 0, key);
+    }
+    unsigned long long *out = seed + (size_t(b) * a.Q + i) * k;
+    for (int e = 0; e < k; ++e) out[e] = h[e * 32];
 }
 
 // Two problems with the same k can share one launch: block rows
@@ -667,6 +733,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     bool valid[KL_QL];
     float qx[KL_QL], qy[KL_QL], qz[KL_QL], qq[KL_QL], thr[KL_QL];
     float thr0[KL_QL];  // threshold of the seed bound (below)
+    int seed_lo[KL_QL], seed_hi[KL_QL];  // ORDERED: seeded tiles, skipped here
     unsigned long long tk[KL_QL];  // heap root: the k-th best so far
     float2 ax[KL_QL], ay[KL_QL], az[KL_QL];
 #pragma unroll
@@ -698,41 +765,29 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         ay[q] = make_float2(ays, ays);
         az[q] = make_float2(azs, azs);
         tk[q] = KEY_EMPTY;
-        // ORDERED: a seed bound tau0 >= the k-th smallest s32 of the query,
-        // from the KL_SEED references around its place in the spatial order:
-        // split into k groups, the largest of the groups' smallest s32 is
-        // the s32 of one of k distinct references, so at least k references
-        // have s32 <= tau0.  Until the heap is full the filter threshold is
-        // that of tau0 instead of +inf (the heap then fills with near
-        // references only); afterwards the smaller of the two.
+        unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+        for (int e = 0; e < k; ++e) hk[e * 32] = KEY_EMPTY;
+        // ORDERED: the query's seeded tiles were searched exactly by
+        // knn_seed_kernel; part 0 starts from that heap, and every part skips
+        // those tiles.  The seed heap's root bounds the k-th smallest s32
+        // (the s32 of the k-th of k distinct references), so until a part's
+        // own heap is full its filter threshold is that bound instead of
+        // +inf; afterwards the smaller of the two.
         float tau0 = inf;
-        if (ORDERED && valid[q] && Nb >= KL_SEED) {
-            const int pos = (a.squery == a.sref && a.Q == a.N && a.q_len == a.r_len)
-                                ? qi[q]
-                                : a.cstart[size_t(b) * (MC_CELLS + 1) +
-                                           mc_code(a.cframe + size_t(b) * 8, qx[q],
-                                                   qy[q], qz[q])];
-            const int p0 = min(max(pos - KL_SEED / 2, 0), Nb - KL_SEED);
-            const float4 *w4 = reinterpret_cast<const float4 *>(cref) + p0;
-            const int gs = KL_SEED / k;  // group size (k groups)
-            float worst = 0.0f, gm = inf;
-            bool bad = false;
-#pragma unroll 8
-            for (int t = 0; t < KL_SEED; ++t) {
-                const float4 r = w4[t];
-                gm = fminf(gm, sqdist(qx[q], qy[q], qz[q], r.x, r.y, r.z));
-                if (t % gs == gs - 1 && t / gs < k) {
-                    bad = bad || !(gm <= inf);  // a group of NaN s32 only
-                    worst = fmaxf(worst, gm);
-                    gm = inf;
-                }
+        seed_lo[q] = 0;
+        seed_hi[q] = -1;
+        if (ORDERED && valid[q]) {
+            seed_tiles(a, b, qi[q], qx[q], qy[q], qz[q], ntiles, seed_lo[q], seed_hi[q]);
+            const unsigned long long *sk = a.seed + (size_t(b) * a.Q + qi[q]) * k;
+            const unsigned long long root = sk[0];
+            if (key_j(root) != INT_MAX) tau0 = key_s(root);
+            if (part == 0) {
+                for (int e = 0; e < k; ++e) hk[e * 32] = sk[e];
+                tk[q] = root;
             }
-            tau0 = bad ? inf : worst;
         }
         thr0[q] = valid[q] ? filter_threshold(tau0, qq[q]) : -inf;
         thr[q] = thr0[q];
-        unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
-        for (int e = 0; e < k; ++e) hk[e * 32] = KEY_EMPTY;
     }
 
     bool failed = false;
@@ -784,6 +839,13 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
                     pend[q] |= (mn <= thr[q] ? 1u : 0u) << step;
                 }
             }
+        }
+        // ORDERED: a query's seeded tiles are already in its heap (part 0)
+        if (ORDERED) {
+            const int tcur = j0 / ST_T;
+#pragma unroll
+            for (int q = 0; q < KL_QL; ++q)
+                if (tcur >= seed_lo[q] && tcur <= seed_hi[q]) pend[q] = 0;
         }
         // pass 2: the lanes with pending steps process them together (one
         // step per lane per round), exact s32 and heap insertion; thresholds
@@ -1092,8 +1154,10 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
         (int64_t(std::max(1, dev.sm_count - sm_reserve())) * 10 + groups - 1) / groups;
     const int nparts = int(std::max<int64_t>(1, std::min<int64_t>({8, want, ntiles / 8})));
     const size_t off_pk = off_sq + ((self ? 0 : size_t(B) * a.Q * 16 + 255) & ~size_t(255));
-    const size_t total =
-        off_pk + (nparts > 1 ? size_t(nparts) * B * a.Q * size_t(a.k) * 8 : 0);
+    const size_t off_seed =
+        off_pk + ((nparts > 1 ? size_t(nparts) * B * a.Q * size_t(a.k) * 8 : 0) + 255 &
+                  ~size_t(255));
+    const size_t total = off_seed + size_t(B) * a.Q * size_t(a.k) * 8;
     char *base = nullptr;
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&base), total, stream);
     if (e != cudaSuccess) return e;
@@ -1134,7 +1198,18 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
         a.cframe = frame;
         a.part_keys =
             nparts > 1 ? reinterpret_cast<unsigned long long *>(base + off_pk) : nullptr;
-        e = launch_knn_lane<QL, true>(dev, a, B, a, 0, stream, nparts);
+        unsigned long long *seed = reinterpret_cast<unsigned long long *>(base + off_seed);
+        a.seed = seed;
+        const size_t seed_smem = size_t(SEED_THREADS) * size_t(a.k) * 8;
+        e = cudaFuncSetAttribute(knn_seed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(seed_smem));
+        if (e == cudaSuccess) {
+            knn_seed_kernel<<<dim3(unsigned((a.Q + SEED_THREADS - 1) / SEED_THREADS),
+                                   unsigned(B)),
+                              SEED_THREADS, seed_smem, stream>>>(a, seed);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) e = launch_knn_lane<QL, true>(dev, a, B, a, 0, stream, nparts);
         if (e == cudaSuccess && nparts > 1) {
             const dim3 gm(unsigned((a.Q + 255) / 256), unsigned(B));
             knn_merge_parts_kernel<<<gm, 256, 0, stream>>>(a, int(B), nparts);
