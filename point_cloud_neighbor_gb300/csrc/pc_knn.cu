@@ -568,6 +568,7 @@ __device__ __forceinline__ void seed_tiles(const KnnArgs &a, int b, int qpos, fl
 // as it stands.  Lanes of a warp hold neighbouring queries, so they read the
 // same references (broadcast loads).
 constexpr int SEED_THREADS = 256;
+constexpr int SEED_UNROLL = 4;
 
 __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
                                                                 unsigned long long *seed) {
@@ -588,17 +589,18 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
     unsigned long long root = KEY_EMPTY;
     const int j1 = min(Nb, (hi + 1) * ST_T);
     int j = lo * ST_T;
-    // four references at a time: their loads and distances are independent
-    for (; j + 4 <= j1; j += 4) {
-        unsigned long long key[4];
+    // SEED_UNROLL references at a time: their loads and distances are
+    // independent
+    for (; j + SEED_UNROLL <= j1; j += SEED_UNROLL) {
+        unsigned long long key[SEED_UNROLL];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < SEED_UNROLL; ++u) {
             const float4 r = rp[j + u];
             // s32 >= +0; a NaN s32 has a key above KEY_EMPTY: never taken
             key[u] = sj_key(sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z), __float_as_int(r.w));
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < SEED_UNROLL; ++u)
             if (key[u] < root) root = heap_sift(h, k, 0, key[u]);
     }
     for (; j < j1; ++j) {
