@@ -313,9 +313,10 @@ def run_gpu(args):
     wall1 = time.perf_counter()
     barrier(world)
     # kernels of one step: FPS 1; kNN on this cloud (spatially ordered: the
-    # query set is the reference set) frame, count, chunk sums, scan, scatter
-    # and the lane kernel = 6 (plus a memset of the cell counts); Ball Query 1
-    launches = (1 + 6 + 1) * args.steps
+    # query set is the reference set) frame, count, chunk sums, scan,
+    # scatter, seed and the lane kernel = 7 (plus a memset of the cell
+    # counts); Ball Query 1
+    launches = (1 + 7 + 1) * args.steps
 
     # each operator timed on the stream it runs on
     t_fps = [e[0].elapsed_time(e[1]) for e in events]
