@@ -50,6 +50,12 @@ WORKLOAD = dict(name="large", B=1, N=100_000, npoint=4096, start_idx=0,
 FLOPS_PER_PAIR = 8          # 3 sub + 3 mul + 2 add per (query, reference) pair
 FPS_BYTES_PER_POINT_STEP = 20  # 12 B coordinates + 4 B min read + 4 B write
 L2_FLUSH_BYTES = 512 << 20
+# Thread-block cluster FPS runs on in the step.  FPS alone plans 16 blocks;
+# next to kNN and Ball Query a 13-block cluster balances the step better:
+# FPS still ends first, and the three SMs it gives back go to the Ball Query
+# grid (GB300: step 4.27 ms with 13 or 12 blocks, 4.31 with 14, 4.34 with 16;
+# FPS alone 3.34 ms with 13 blocks, 3.72 with 16, same samples).
+STEP_FPS_CLUSTER = 13
 
 
 def workload_config(extra=None):
@@ -258,8 +264,8 @@ def run_gpu(args):
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
-    # FPS runs one thread-block cluster per cloud (16 SMs here) for thousands
-    # of dependent steps; kNN and Ball Query are independent of it and fill
+    # FPS runs one thread-block cluster per cloud (STEP_FPS_CLUSTER SMs) for
+    # thousands of dependent steps; kNN and Ball Query are independent of it and fill
     # the other SMs.  FPS is issued first, on the main stream, so that its
     # cluster is resident before the kNN and Ball Query blocks (issued on a
     # side stream after the same start point) occupy the rest of the GPU
@@ -268,14 +274,15 @@ def run_gpu(args):
     fork = torch.cuda.Event()
     # the kNN and Ball Query grids (one wave) are planned around the SMs
     # FPS holds while it runs
-    reserve = 0 if args.serial else pc.pc_fps_sm_count(B, N, npoint)
+    reserve = 0 if args.serial else B * STEP_FPS_CLUSTER
 
     def step(ev=None):
         # ev: [start, fps_end, knn_start (side), knn_end, bq_end, step_end]
         if ev is not None:
             ev[0].record(stream)
         fork.record(stream)
-        pc.pc_fps(x, npoint, 0, out=fps_out, workspace=ws)
+        pc.pc_fps(x, npoint, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=STEP_FPS_CLUSTER,
+                  out=fps_out, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
         side.wait_event(fork)
@@ -372,7 +379,8 @@ def run_gpu(args):
     # FPS against its two other bounds: ~10 instructions per point-step on the
     # SMs its schedule uses, and the per-step exchange floor measured with the
     # same cluster schedule on 1024 points per block
-    fps_sms = pc.pc_fps_sm_count(B, N, npoint)
+    fps_sms = B * STEP_FPS_CLUSTER
+    ops["fps"]["cluster"] = STEP_FPS_CLUSTER
     ops["fps"]["alu_bound_ms"] = (float(N) * (npoint - 1) * 10 /
                                   (max(fps_sms, 1) * 128 * max_mhz * 1e6) * 1e3)
     if fps_sms > 1:
@@ -439,7 +447,8 @@ def run_gpu(args):
         "dtype": "f32", "data": "synthetic",
         "config": workload_config({"parallelism": f"replicas x{world}",
                                    "streams": ("1 (serial)" if args.serial else
-                                               "2: FPS concurrent with kNN then Ball Query")}),
+                                               "2: FPS concurrent with kNN then Ball Query"),
+                                   "fps_cluster": STEP_FPS_CLUSTER}),
         "roofline": roof, "roofline_per_kernel": roof_all, "ops": ops,
         "grid": grid, "next_rows": next_rows,
         "e2e": e2e,
@@ -750,12 +759,13 @@ def run_e2e(args, pc, x_host, device, world):
     # the kNN results are read back while Ball Query runs, the FPS result
     # once FPS ends; only the Ball Query read-back follows the last kernel
     copy = torch.cuda.Stream(device) if not args.serial else main
-    reserve = 0 if args.serial else pc.pc_fps_sm_count(1, N, npoint)
+    reserve = 0 if args.serial else STEP_FPS_CLUSTER
 
     def one():
         xd = x_pin.to(device, non_blocking=True)
         side.wait_stream(main)
-        f = pc.pc_fps(xd, npoint, 0)
+        f = pc.pc_fps(xd, npoint, 0, strategy=pc.PC_FPS_CLUSTER,
+                      cluster_size=STEP_FPS_CLUSTER)
         outs["fps"].copy_(f, non_blocking=True)
         with torch.cuda.stream(side):
             pc.pc_set_sm_reserve(reserve)

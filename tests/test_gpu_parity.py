@@ -403,10 +403,11 @@ def test_fps_schedules_agree_with_oracle(strategy, cs, bpc):
     assert_idx_equal(idx, oracle.fps(x, 300, 17), f"fps schedule {strategy}/{cs}/{bpc}")
 
 
-def test_fps_cluster_16_on_100k():
+@pytest.mark.parametrize("cs", [16, 13])
+def test_fps_cluster_on_100k(cs):
     x = inputs.large()
-    idx = gpu_fps(x, 600, 3, strategy=pc.PC_FPS_CLUSTER, cluster_size=16)
-    assert_idx_equal(idx, oracle.fps(x, 600, 3), "fps cluster 16")
+    idx = gpu_fps(x, 600, 3, strategy=pc.PC_FPS_CLUSTER, cluster_size=cs)
+    assert_idx_equal(idx, oracle.fps(x, 600, 3), f"fps cluster {cs}")
 
 
 def test_fps_grid_on_100k():
