@@ -46,6 +46,7 @@
 #include "pc_tiles.cuh"
 
 #include <algorithm>
+#include <type_traits>
 #include <climits>
 
 namespace pcn {
@@ -81,7 +82,7 @@ struct KnnArgs {
     // sorted k keys per valid query row, [part][B][Q][k] (merged afterwards)
     unsigned long long *part_keys;
     // ORDERED: per query (in the query order) the exact k best keys over its
-    // seeded tiles, as a max-heap [B][Q][k] (knn_seed_kernel)
+    // seeded tile, as a max-heap [B][Q][k] (knn_seed_kernel)
     const unsigned long long *seed;
 };
 
@@ -493,7 +494,11 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 // cloud, so a block's groups are spread over the cloud and the blocks of a
 // launch differ by at most one group.  (Blocks of a fixed 256 queries left
 // 100k queries at 2.57 blocks per SM against 3 slots: the SMs with three
-// blocks set the time.)  One producer serves all W consumer warps.
+// blocks set the time.)  ORDERED, a block takes upb consecutive units of 32
+// queries instead (upb = ceil(units / (SMs x waves))), so that with two
+// slots per lane the SMs differ by half a warp, not a warp: 100k queries on
+// 152 SMs are 149 blocks of 10.5 warps' work where 143 blocks of 11 were
+// (GB300, k = 16: 2.06 -> 2.01 ms).  One producer serves all W consumer warps.
 // consumer warps per block at most (one block per SM: registers)
 __host__ __device__ constexpr int kl_wmax(int QL) { return QL == 1 ? 15 : 12; }
 
@@ -547,19 +552,16 @@ __device__ __forceinline__ unsigned long long heap_sift(unsigned long long *h, i
 
 // ORDERED: the reference tile seeded for the query at position qpos of the
 // query order: the tile of its place among the references (qpos itself when
-// the query set is the reference set, else the start of its cell); [lo, hi],
-// empty (hi < lo) without references.  (Seeding the two tiles next to it as
-// well measured slower at 100k points, k = 16: 2.21 vs 2.11 ms.)
-__device__ __forceinline__ void seed_tiles(const KnnArgs &a, int b, int qpos, float qx,
-                                           float qy, float qz, int ntiles, int &lo,
-                                           int &hi) {
+// the query set is the reference set, else the start of its cell); -1
+// without references.  (Seeding the two tiles next to it as well measured
+// slower at 100k points, k = 16: 2.21 vs 2.11 ms.)
+__device__ __forceinline__ int seed_tile(const KnnArgs &a, int b, int qpos, float qx,
+                                         float qy, float qz, int ntiles) {
     const bool self = a.squery == a.sref && a.Q == a.N && a.q_len == a.r_len;
     const int pos = self ? qpos
                          : a.cstart[size_t(b) * (MC_CELLS + 1) +
                                     mc_code(a.cframe + size_t(b) * 8, qx, qy, qz)];
-    const int h = min(pos / ST_T, ntiles - 1);
-    lo = max(h, 0);
-    hi = h;
+    return min(pos / ST_T, ntiles - 1);
 }
 
 // ORDERED: one thread per valid query: the exact k best (s, j) over its
@@ -583,12 +585,11 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
     unsigned long long *h = seed_heaps + size_t(threadIdx.x >> 5) * 32 * k + (threadIdx.x & 31);
     for (int e = 0; e < k; ++e) h[e * 32] = KEY_EMPTY;
     const float4 qv = reinterpret_cast<const float4 *>(a.squery)[size_t(b) * a.Q + i];
-    int lo, hi;
-    seed_tiles(a, b, i, qv.x, qv.y, qv.z, ntiles, lo, hi);
+    const int t = seed_tile(a, b, i, qv.x, qv.y, qv.z, ntiles);
     const float4 *rp = reinterpret_cast<const float4 *>(a.sref) + size_t(b) * a.N;
     unsigned long long root = KEY_EMPTY;
-    const int j1 = min(Nb, (hi + 1) * ST_T);
-    int j = lo * ST_T;
+    const int j1 = min(Nb, (t + 1) * ST_T);
+    int j = max(t, 0) * ST_T;
     // SEED_UNROLL references at a time: their loads and distances are
     // independent
     for (; j + SEED_UNROLL <= j1; j += SEED_UNROLL) {
@@ -613,25 +614,69 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
     for (int e = 0; e < k; ++e) out[e] = h[e * 32];
 }
 
+// Pass 1 over one prepared tile for the first NQ query slots of a lane: per
+// 8-point step and query, the filter of the step's points (three packed FMAs
+// per pair), their minimum and one compare set the step's bit of pend[q].
+// Rows of 2^KL_SB steps with compile-time slot offsets (the stage swizzle).
+template <int NQ, int KL_QL, int KL_SB>
+__device__ __forceinline__ void lane_pass1(const float4 *ck, int nsteps,
+                                           const float2 (&ax)[KL_QL],
+                                           const float2 (&ay)[KL_QL],
+                                           const float2 (&az)[KL_QL],
+                                           const float (&thr)[KL_QL],
+                                           unsigned (&pend)[KL_QL]) {
+    constexpr int KL_ROW = 1 << KL_SB;
+    static_assert(8 % KL_ROW == 0, "rows of steps divide 8");
+    for (int s0 = 0; s0 < nsteps; s0 += KL_ROW) {
+#pragma unroll
+        for (int ss = 0; ss < KL_ROW; ++ss) {
+            const int step = s0 + ss;
+            const float4 *row = ck + 8 * step;
+            const int x = ss << (3 - KL_SB);  // the row's slot swizzle
+            float mu[NQ][4];  // min of t' over each pair of points
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 A = row[(2 * u) ^ x];
+                const float4 Z = row[(2 * u + 1) ^ x];
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    float2 v = __ffma2_rn(make_float2(A.x, A.y), ax[q],
+                                          make_float2(Z.z, Z.w));
+                    v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
+                    v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
+                    mu[q][u] = fminf(v.x, v.y);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float mn = fminf(fminf(mu[q][0], mu[q][1]), fminf(mu[q][2], mu[q][3]));
+                pend[q] |= (mn <= thr[q] ? 1u : 0u) << step;
+            }
+        }
+    }
+}
+
 // Two problems with the same k can share one launch: block rows
 // blockIdx.y < B0 run a0 (cloud blockIdx.y), the rest a1 (cloud
 // blockIdx.y - B0) -- used for the two directions of the Chamfer distance.
 //
 // ORDERED: the clouds come in the spatial order of the cell codes (sref,
-// squery); a block owns consecutive query groups (a compact region) and
+// squery); a block owns `upb` consecutive units of 32 queries (a compact
+// region; warp w takes units w * KL_QL .. w * KL_QL + KL_QL - 1 of them) and
 // visits the reference tiles outwards from the tile where its region's
 // middle query would sit (home, home + 1, home - 1, ...), so the k best
 // (s, j) are found in the first few tiles and the later tiles rarely let a
-// pair through.  Keys carry the original indices, so the result is that of
-// the input order.
+// pair through.  With two slots per lane an odd `upb` leaves the last warp
+// one unit: it runs the tile loop for one query per lane, pass 1 at about
+// half the cost, so the launch can balance the SMs to half a warp.  Keys
+// carry the original indices, so the result is that of the input order.
 template <int KL_QL, bool ORDERED>
 __global__ void __launch_bounds__(32 * (kl_wmax(KL_QL) + 1), 1)
-knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
+knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
     constexpr int GQ = 32 * KL_QL;  // queries per group (warp)
     // cooked-tile swizzle bits and steps per hot-loop iteration: 3 and 8 for
     // one query per lane, 2 and 4 for two (registers)
     constexpr int KL_SB = KL_QL == 1 ? 3 : 2;
-    constexpr int KL_ROW = 1 << KL_SB;
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -663,12 +708,14 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     const int nwarps = static_cast<int>(blockDim.x >> 5) - 1;  // consumers
     const int nbx = static_cast<int>(gridDim.x);
     const int bx = static_cast<int>(blockIdx.x);
-    // this warp's group (ORDERED: consecutive groups per block, else strided
-    // over the cloud); the warps whose group holds a valid query (a prefix of
-    // the block's warps) consume the stream
-    const int g = ORDERED ? bx * nwarps + warp : warp * nbx + bx;
+    // ORDERED: the block's units [u0, u1) of the valid queries; else this
+    // warp's group, strided over the cloud.  The warps that hold a valid
+    // query (a prefix of the block's warps) consume the stream.
+    const int u0 = ORDERED ? bx * upb : 0;
+    const int u1 = ORDERED ? min(u0 + upb, (Qb + 31) / 32) : 0;
+    const int g = warp * nbx + bx;
     const int gvalid = (Qb + GQ - 1) / GQ;
-    const int nact = ORDERED ? max(0, min(nwarps, gvalid - bx * nwarps))
+    const int nact = ORDERED ? max(0, min(nwarps, (u1 - u0 + KL_QL - 1) / KL_QL))
                              : (bx < gvalid ? min(nwarps, (gvalid - bx + nbx - 1) / nbx) : 0);
     if (ORDERED) {
         // rows past the cloud's valid length: padding, spread over the blocks
@@ -705,7 +752,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     // would sit among the references
     int home = 0;
     if (ORDERED && ntiles > 0) {
-        const int pm = min(Qb - 1, bx * nwarps * GQ + (nact * GQ) / 2);
+        const int pm = min(Qb - 1, u0 * 32 + (u1 - u0) * 16);
         const float *qm = a.squery + (size_t(b) * a.Q + pm) * 4;
         const unsigned code = mc_code(a.cframe + size_t(b) * 8, qm[0], qm[1], qm[2]);
         home = min(ntiles - 1, a.cstart[size_t(b) * (MC_CELLS + 1) + code] / ST_T);
@@ -729,20 +776,26 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         return;
     }
 
-    // query q of this lane: g * GQ + q * 32 + lane; its heap is at slot
-    // (warp * KL_QL + q) * 32 + lane, entries 32 apart
-    int qi[KL_QL], orow[KL_QL];  // position in the query set, output row
+    // query q of this lane: unit u0 + warp * KL_QL + q (ORDERED) or
+    // g * KL_QL + q, query 32 * unit + lane; its heap is at slot
+    // (warp * KL_QL + q) * 32 + lane, entries 32 apart.  The position (and
+    // the output row) is recomputed at the end, not kept live through the
+    // tile loop.
+    auto query_pos = [&](int q) {
+        const int unit = ORDERED ? u0 + warp * KL_QL + q : g * KL_QL + q;
+        return unit * 32 + lane;
+    };
+    int qi[KL_QL];
     bool valid[KL_QL];
     float qx[KL_QL], qy[KL_QL], qz[KL_QL], qq[KL_QL], thr[KL_QL];
     float thr0[KL_QL];  // threshold of the seed bound (below)
-    int seed_lo[KL_QL], seed_hi[KL_QL];  // ORDERED: seeded tiles, skipped here
+    int seed_t[KL_QL];  // ORDERED: the seeded tile (-1: none), skipped here
     unsigned long long tk[KL_QL];  // heap root: the k-th best so far
     float2 ax[KL_QL], ay[KL_QL], az[KL_QL];
 #pragma unroll
     for (int q = 0; q < KL_QL; ++q) {
-        qi[q] = g * GQ + q * 32 + lane;
-        valid[q] = qi[q] < Qb;
-        orow[q] = qi[q];
+        qi[q] = query_pos(q);
+        valid[q] = qi[q] < Qb && (!ORDERED || (qi[q] >> 5) < u1);
         qx[q] = qy[q] = qz[q] = 0.f;
         if (valid[q]) {
             if (ORDERED) {
@@ -751,7 +804,6 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
                 qx[q] = p.x;
                 qy[q] = p.y;
                 qz[q] = p.z;
-                orow[q] = __float_as_int(p.w);
             } else {
                 const float *p = a.query + (size_t(b) * a.Q + qi[q]) * 3;
                 qx[q] = p[0];
@@ -769,17 +821,16 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         tk[q] = KEY_EMPTY;
         unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
         for (int e = 0; e < k; ++e) hk[e * 32] = KEY_EMPTY;
-        // ORDERED: the query's seeded tiles were searched exactly by
+        // ORDERED: the query's seeded tile was searched exactly by
         // knn_seed_kernel; part 0 starts from that heap, and every part skips
-        // those tiles.  The seed heap's root bounds the k-th smallest s32
+        // that tile.  The seed heap's root bounds the k-th smallest s32
         // (the s32 of the k-th of k distinct references), so until a part's
         // own heap is full its filter threshold is that bound instead of
         // +inf; afterwards the smaller of the two.
         float tau0 = inf;
-        seed_lo[q] = 0;
-        seed_hi[q] = -1;
+        seed_t[q] = -1;
         if (ORDERED && valid[q]) {
-            seed_tiles(a, b, qi[q], qx[q], qy[q], qz[q], ntiles, seed_lo[q], seed_hi[q]);
+            seed_t[q] = seed_tile(a, b, qi[q], qx[q], qy[q], qz[q], ntiles);
             const unsigned long long *sk = a.seed + (size_t(b) * a.Q + qi[q]) * k;
             const unsigned long long root = sk[0];
             if (key_j(root) != INT_MAX) tau0 = key_s(root);
@@ -792,96 +843,82 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         thr[q] = thr0[q];
     }
 
-    bool failed = false;
-    for (int it = 0; it < nsteps_part; ++it) {
-        const int st = it % ST_STAGES;
-        const WaitResult w = warp_wait(&ring.ready[st], unsigned((it / ST_STAGES) & 1),
-                                       s_err, a.timeout_ns);
-        if (w != WAIT_OK) {
-            failed = true;
-            break;
-        }
-        const float4 *ck = ring.cooked_tile(st);
-        const int j0 = tile_at(it) * ST_T;
-        const int cnt = min(ST_T, Nb - j0);
-        const float4 *raw = ring.raw_copy(st);
-        // whole rows of 8 steps (64 points); the cooked tile is padded to
-        // ST_T points with points that pass only an infinite threshold
-        const int nsteps = ((cnt + 63) >> 6) << 3;
-        static_assert(8 % KL_ROW == 0, "rows of steps divide 8");
-        // pass 1: filter the whole tile, remembering which 8-point steps let
-        // something through for which query (32 steps per tile)
-        unsigned pend[KL_QL];
+    // The tile loop for the first NQ query slots of each lane; returns true
+    // when a wait for a stage ran out.  ORDERED with two slots, a warp left
+    // with one unit (its second slot holds no valid query) runs it for one
+    // slot: pass 1 at about half the cost, and half the live state.
+    auto tile_loop = [&](auto nq_c) -> bool {
+        constexpr int NQ = decltype(nq_c)::value;
+        for (int it = 0; it < nsteps_part; ++it) {
+            const int st = it % ST_STAGES;
+            const WaitResult w = warp_wait(&ring.ready[st], unsigned((it / ST_STAGES) & 1),
+                                           s_err, a.timeout_ns);
+            if (w != WAIT_OK) return true;
+            const float4 *ck = ring.cooked_tile(st);
+            const int j0 = tile_at(it) * ST_T;
+            const int cnt = min(ST_T, Nb - j0);
+            const float4 *raw = ring.raw_copy(st);
+            // whole rows of 8 steps (64 points); the cooked tile is padded to
+            // ST_T points with points that pass only an infinite threshold
+            const int nsteps = ((cnt + 63) >> 6) << 3;
+            // pass 1: filter the whole tile, remembering which 8-point steps
+            // let something through for which query (32 steps per tile)
+            unsigned pend[KL_QL];
 #pragma unroll
-        for (int q = 0; q < KL_QL; ++q) pend[q] = 0;
-        for (int s0 = 0; s0 < nsteps; s0 += KL_ROW) {
+            for (int q = 0; q < KL_QL; ++q) pend[q] = 0;
+            lane_pass1<NQ, KL_QL, KL_SB>(ck, nsteps, ax, ay, az, thr, pend);
+            // ORDERED: a query's seeded tile is already in its heap (part 0)
+            if (ORDERED) {
+                const int tcur = j0 / ST_T;
 #pragma unroll
-            for (int ss = 0; ss < KL_ROW; ++ss) {
-                const int step = s0 + ss;
-                const float4 *row = ck + 8 * step;
-                const int x = ss << (3 - KL_SB);  // the row's slot swizzle
-                float mu[KL_QL][4];  // min of t' over each pair of points
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 A = row[(2 * u) ^ x];
-                    const float4 Z = row[(2 * u + 1) ^ x];
-#pragma unroll
-                    for (int q = 0; q < KL_QL; ++q) {
-                        float2 v = __ffma2_rn(make_float2(A.x, A.y), ax[q],
-                                              make_float2(Z.z, Z.w));
-                        v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
-                        v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
-                        mu[q][u] = fminf(v.x, v.y);
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < KL_QL; ++q) {
-                    const float mn =
-                        fminf(fminf(mu[q][0], mu[q][1]), fminf(mu[q][2], mu[q][3]));
-                    pend[q] |= (mn <= thr[q] ? 1u : 0u) << step;
-                }
+                for (int q = 0; q < NQ; ++q)
+                    if (tcur == seed_t[q]) pend[q] = 0;
             }
-        }
-        // ORDERED: a query's seeded tiles are already in its heap (part 0)
-        if (ORDERED) {
-            const int tcur = j0 / ST_T;
+            // pass 2: the lanes with pending steps process them together (one
+            // step per lane per round), exact s32 and heap insertion;
+            // thresholds only tighten, so re-filtering with the current one is
+            // still safe
 #pragma unroll
-            for (int q = 0; q < KL_QL; ++q)
-                if (tcur >= seed_lo[q] && tcur <= seed_hi[q]) pend[q] = 0;
-        }
-        // pass 2: the lanes with pending steps process them together (one
-        // step per lane per round), exact s32 and heap insertion; thresholds
-        // only tighten, so re-filtering with the current one is still safe
-#pragma unroll
-        for (int q = 0; q < KL_QL; ++q) {
-            if (!valid[q]) pend[q] = 0;
-            unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
-            while (__any_sync(FULL, pend[q] != 0)) {
-                if (pend[q] == 0) continue;
-                const int p = 4 * (__ffs(pend[q]) - 1);
-                pend[q] &= pend[q] - 1;
-                unsigned m = stream_mask<KL_SB, 4>(ck, p, ax[q], ay[q], az[q], thr[q]);
-                while (m) {
-                    const int i = 2 * p + __ffs(m) - 1;
-                    m &= m - 1;
-                    if (i >= cnt) continue;
-                    const float4 P = raw[raw_slot(i)];
-                    const float sv = sqdist(qx[q], qy[q], qz[q], P.x, P.y, P.z);
-                    // s32 >= +0; a NaN s32 has a key above KEY_EMPTY and is
-                    // never accepted
-                    const unsigned long long key =
-                        sj_key(sv, ORDERED ? __float_as_int(P.w) : j0 + i);
-                    if (key < tk[q]) {
-                        tk[q] = heap_sift(hk, k, 0, key);
-                        if (key_j(tk[q]) != INT_MAX)
-                            thr[q] = fminf(thr0[q],
-                                           filter_threshold(key_s(tk[q]), qq[q]));
+            for (int q = 0; q < NQ; ++q) {
+                if (!valid[q]) pend[q] = 0;
+                unsigned long long *hk = hk_all + size_t(warp * KL_QL + q) * 32 * k + lane;
+                while (__any_sync(FULL, pend[q] != 0)) {
+                    if (pend[q] == 0) continue;
+                    const int p = 4 * (__ffs(pend[q]) - 1);
+                    pend[q] &= pend[q] - 1;
+                    unsigned m = stream_mask<KL_SB, 4>(ck, p, ax[q], ay[q], az[q], thr[q]);
+                    while (m) {
+                        const int i = 2 * p + __ffs(m) - 1;
+                        m &= m - 1;
+                        if (i >= cnt) continue;
+                        const float4 P = raw[raw_slot(i)];
+                        const float sv = sqdist(qx[q], qy[q], qz[q], P.x, P.y, P.z);
+                        // s32 >= +0; a NaN s32 has a key above KEY_EMPTY and
+                        // is never accepted
+                        const unsigned long long key =
+                            sj_key(sv, ORDERED ? __float_as_int(P.w) : j0 + i);
+                        if (key < tk[q]) {
+                            tk[q] = heap_sift(hk, k, 0, key);
+                            if (key_j(tk[q]) != INT_MAX)
+                                thr[q] = fminf(thr0[q],
+                                               filter_threshold(key_s(tk[q]), qq[q]));
+                        }
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ring.empty[st]);  // tile no longer read
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ring.empty[st]);  // tile no longer read
+        return false;
+    };
+    bool failed;
+    if constexpr (ORDERED && KL_QL == 2) {
+        if (u0 + warp * KL_QL + 1 >= u1)
+            failed = tile_loop(std::integral_constant<int, 1>{});
+        else
+            failed = tile_loop(std::integral_constant<int, 2>{});
+    } else {
+        failed = tile_loop(std::integral_constant<int, KL_QL>{});
     }
 
     if (failed) {
@@ -890,12 +927,16 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
     }
 #pragma unroll
     for (int q = 0; q < KL_QL; ++q) {
-        if (qi[q] >= a.Q || (ORDERED && !valid[q])) continue;
-        const size_t row = size_t(b) * a.Q + orow[q];
+        const int qp = query_pos(q);
+        if (qp >= a.Q || (ORDERED && !valid[q])) continue;
+        // output row: ORDERED, the query's original index
+        const float4 *sq = reinterpret_cast<const float4 *>(a.squery);
+        const int orow = ORDERED ? __float_as_int(sq[size_t(b) * a.Q + qp].w) : qp;
+        const size_t row = size_t(b) * a.Q + orow;
         if (failed) {
             if (ORDERED && nparts > 1) {
                 unsigned long long *pk =
-                    a.part_keys + ((size_t(part) * gridDim.y + b) * a.Q + orow[q]) * k;
+                    a.part_keys + ((size_t(part) * gridDim.y + b) * a.Q + orow) * k;
                 for (int e = 0; e < k; ++e) pk[e] = KEY_EMPTY;
             } else {
                 for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
@@ -911,7 +952,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0) {
         }
         if (ORDERED && nparts > 1) {  // this part's sorted keys, merged later
             unsigned long long *pk =
-                a.part_keys + ((size_t(part) * gridDim.y + b) * a.Q + orow[q]) * k;
+                a.part_keys + ((size_t(part) * gridDim.y + b) * a.Q + orow) * k;
             for (int e = 0; e < k; ++e) pk[e] = hk[e * 32];
             continue;
         }
@@ -973,10 +1014,22 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
     const int64_t wmax = std::max<int64_t>(
         1, std::min<int64_t>(kl_wmax(QL), (int64_t(dev.smem_per_block_optin) -
                                        int64_t(stream_smem_bytes())) / per_warp));
-    const int64_t waves = (total + nsm * wmax - 1) / (nsm * wmax);
-    const int64_t W =
-        std::min(std::min(wmax, G), (total + nsm * waves - 1) / (nsm * waves));
-    const int64_t nbx = (G + W - 1) / W;
+    int64_t W, nbx, upb = 0;
+    if (ORDERED) {
+        // units of 32 queries: a block takes upb consecutive units, about the
+        // same number per SM (to half a warp with two slots per lane)
+        const int64_t U = (Q + 31) / 32;  // units per cloud
+        const int64_t utotal = U * (B0 + B1) * nparts;
+        const int64_t umax = wmax * QL;
+        const int64_t waves = (utotal + nsm * umax - 1) / (nsm * umax);
+        upb = std::min(std::min(umax, U), (utotal + nsm * waves - 1) / (nsm * waves));
+        W = (upb + QL - 1) / QL;
+        nbx = (U + upb - 1) / upb;
+    } else {
+        const int64_t waves = (total + nsm * wmax - 1) / (nsm * wmax);
+        W = std::min(std::min(wmax, G), (total + nsm * waves - 1) / (nsm * waves));
+        nbx = (G + W - 1) / W;
+    }
     const size_t smem = knn_lane_smem(a0.k, QL, int(W));
     cudaError_t e = cudaFuncSetAttribute(
         knn_lane_kernel<QL, ORDERED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -985,7 +1038,7 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
     dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(B0 + B1),
               static_cast<unsigned>(nparts));
     knn_lane_kernel<QL, ORDERED>
-        <<<grid, unsigned(32 * (W + 1)), smem, stream>>>(a0, a1, int(B0));
+        <<<grid, unsigned(32 * (W + 1)), smem, stream>>>(a0, a1, int(B0), int(upb));
     return cudaGetLastError();
 }
 
