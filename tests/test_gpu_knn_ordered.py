@@ -107,3 +107,25 @@ def test_sm_reserve_only_changes_the_plan():
             assert torch.equal(j0, j1) and torch.equal(b0, b1), reserve
     finally:
         pc.pc_set_sm_reserve(0)
+
+
+@pytest.mark.parametrize("k", [4, 16])
+def test_ordered_unit_plans_agree(k):
+    """The launch splits the queries into blocks of 32-query units; SM counts
+    that make the units per block odd leave warps with one query per lane.
+    Every plan gives the oracle's result, on a ragged query count."""
+    rng = np.random.default_rng(23 + k)
+    x = grid_cloud(rng, 1, 16384, step=1.0 / 96)
+    q = rng.random((1, 4133, 3), dtype=np.float32)
+    q[0, :200] = x[0, rng.choice(16384, 200, replace=False)]  # exact matches
+    wd, wi = oracle.knn(q, x, k, threads=THREADS)
+    qd, xd = to_dev(q), to_dev(x)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    try:
+        for reserve in (0, sms - 92, sms - 12, sms - 1):
+            pc.pc_set_sm_reserve(max(0, reserve))
+            d, i = pc.pc_knn(qd, xd, k)
+            compare(d.cpu().numpy(), i.cpu().numpy(), wd, wi,
+                    f"ordered kNN k={k}, reserve {reserve}")
+    finally:
+        pc.pc_set_sm_reserve(0)
