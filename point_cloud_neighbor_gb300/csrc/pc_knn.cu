@@ -550,25 +550,34 @@ __device__ __forceinline__ unsigned long long heap_sift(unsigned long long *h, i
     return top;
 }
 
-// ORDERED: the reference tile seeded for the query at position qpos of the
-// query order: the tile of its place among the references (qpos itself when
-// the query set is the reference set, else the start of its cell); -1
-// without references.  (Seeding the two tiles next to it as well measured
-// slower at 100k points, k = 16: 2.21 vs 2.11 ms.)
+// ORDERED: the place among the references of the query at position qpos of
+// the query order: qpos itself when the query set is the reference set, else
+// the start of its cell.
+__device__ __forceinline__ int seed_pos(const KnnArgs &a, int b, int qpos, float qx,
+                                        float qy, float qz) {
+    const bool self = a.squery == a.sref && a.Q == a.N && a.q_len == a.r_len;
+    return self ? qpos
+                : a.cstart[size_t(b) * (MC_CELLS + 1) +
+                           mc_code(a.cframe + size_t(b) * 8, qx, qy, qz)];
+}
+
+// ORDERED: the reference tile seeded for that query, the tile of its place;
+// -1 without references.  (Seeding the two tiles next to it as well
+// measured slower at 100k points, k = 16: 2.21 vs 2.11 ms.)
 __device__ __forceinline__ int seed_tile(const KnnArgs &a, int b, int qpos, float qx,
                                          float qy, float qz, int ntiles) {
-    const bool self = a.squery == a.sref && a.Q == a.N && a.q_len == a.r_len;
-    const int pos = self ? qpos
-                         : a.cstart[size_t(b) * (MC_CELLS + 1) +
-                                    mc_code(a.cframe + size_t(b) * 8, qx, qy, qz)];
-    return min(pos / ST_T, ntiles - 1);
+    return min(seed_pos(a, b, qpos, qx, qy, qz) / ST_T, ntiles - 1);
 }
 
 // ORDERED: one thread per valid query: the exact k best (s, j) over its
 // seeded tile (up to ST_T references), kept as a max-heap of keys in
 // shared memory (entry e of a warp's lane l at [e * 32 + l]) and written out
-// as it stands.  Lanes of a warp hold neighbouring queries, so they read the
-// same references (broadcast loads).
+// as it stands.  The tile is read outwards from the query's own place
+// (o, o - 1, o + 1, o - 2, ..., then the rest of the longer side): in the
+// spatial order the nearest references come first, so the heap root falls
+// early and few later references need a sift.  The heap holds the k
+// smallest keys whatever the order.  Lanes of a warp hold neighbouring
+// queries, so they read neighbouring references.
 constexpr int SEED_THREADS = 256;
 constexpr int SEED_UNROLL = 4;
 
@@ -585,18 +594,30 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
     unsigned long long *h = seed_heaps + size_t(threadIdx.x >> 5) * 32 * k + (threadIdx.x & 31);
     for (int e = 0; e < k; ++e) h[e * 32] = KEY_EMPTY;
     const float4 qv = reinterpret_cast<const float4 *>(a.squery)[size_t(b) * a.Q + i];
-    const int t = seed_tile(a, b, i, qv.x, qv.y, qv.z, ntiles);
+    const int pos = seed_pos(a, b, i, qv.x, qv.y, qv.z);
+    const int t = min(pos / ST_T, ntiles - 1);  // as seed_tile
     const float4 *rp = reinterpret_cast<const float4 *>(a.sref) + size_t(b) * a.N;
     unsigned long long root = KEY_EMPTY;
+    const int jlo = max(t, 0) * ST_T;
     const int j1 = min(Nb, (t + 1) * ST_T);
-    int j = max(t, 0) * ST_T;
+    const int cnt = j1 - jlo;  // 0 without references
+    // visit m of the tile -> reference: alternately right (from o) and left
+    // (from o - 1) while both sides last, then the longer side on its own
+    const int o = min(max(pos, jlo), j1 - 1);
+    const int L = o - jlo, R = j1 - o, mm = min(L, R);
+    auto ref_at = [&](int m) {
+        if (m < 2 * mm) return (m & 1) ? o - 1 - (m >> 1) : o + (m >> 1);
+        const int rem = m - 2 * mm;
+        return R > L ? o + mm + rem : o - 1 - mm - rem;
+    };
+    int m = 0;
     // SEED_UNROLL references at a time: their loads and distances are
     // independent
-    for (; j + SEED_UNROLL <= j1; j += SEED_UNROLL) {
+    for (; m + SEED_UNROLL <= cnt; m += SEED_UNROLL) {
         unsigned long long key[SEED_UNROLL];
 #pragma unroll
         for (int u = 0; u < SEED_UNROLL; ++u) {
-            const float4 r = rp[j + u];
+            const float4 r = rp[ref_at(m + u)];
             // s32 >= +0; a NaN s32 has a key above KEY_EMPTY: never taken
             key[u] = sj_key(sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z), __float_as_int(r.w));
         }
@@ -604,8 +625,8 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
         for (int u = 0; u < SEED_UNROLL; ++u)
             if (key[u] < root) root = heap_sift(h, k, 0, key[u]);
     }
-    for (; j < j1; ++j) {
-        const float4 r = rp[j];
+    for (; m < cnt; ++m) {
+        const float4 r = rp[ref_at(m)];
         const unsigned long long key =
             sj_key(sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z), __float_as_int(r.w));
         if (key < root) root = heap_sift(h, k, 0, key);
