@@ -161,6 +161,16 @@ int pc_fps_grid_static(const float *xyz, int64_t B, int64_t N, int64_t npoint,
  *             increasing (s, j) order; indices are into cloud b of ref.
  *   k         1 <= k <= N ("Contracts": k <= N), and k <= 256.
  *
+ * Scratch: with at least 16,384 references and 4,096 queries per cloud and
+ * 2 <= k <= 32 the call first puts the points in a spatial order.  It takes
+ * that scratch -- ordered copies of the references (and of the queries
+ * unless they are the references), 16 bytes a point; cell tables of about
+ * 640 KB per cloud; a seed heap of k 8-byte keys per query; with few queries
+ * against many references, up to 8 parts' k keys per query -- from the
+ * stream-ordered allocator (cudaMallocAsync) on `stream` and frees it there
+ * after its kernels; an allocation failure returns PC_ERR_CUDA.  Results do
+ * not depend on the path taken.
+ *
  * Returns PC_OK, PC_ERR_INVALID_ARGUMENT (k > N, k < 1, bad pointer ...),
  * PC_ERR_UNSUPPORTED (k > 256), PC_ERR_CUDA or PC_ERR_NO_DEVICE.
  */
