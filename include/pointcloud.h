@@ -139,7 +139,10 @@ size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
  *
  * The first call on a device (while it is current) looks up the array's
  * device address with cudaGetSymbolAddress; make that first call before any
- * stream capture.  Every call on a device uses the same array, and each call
+ * stream capture.  The address is cached for the life of the process: after
+ * a cudaDeviceReset the entry point must not be called again.  Devices with
+ * ordinals of 64 and above get PC_ERR_UNSUPPORTED.  Every call on a device
+ * uses the same array, and each call
  * clears the words it needs (stream-ordered) before its kernel.  Calls whose
  * work may overlap on the GPU (different streams without ordering between
  * them) race on the array and must not be issued.
@@ -359,9 +362,15 @@ int pc_three_interpolate(const float *features, int64_t B, int64_t C,
  * the input features):
  *   grad_features[b,c,m] = sum over (i, t) with idx[b,i,t] = m of
  *                          weight[b,i,t] * grad_out[b,c,i].
- * grad_features [B, C, M] is overwritten (zeroed, then accumulated with
- * float32 atomic adds: the summation order is not fixed).  Index rules as
- * pc_three_interpolate.
+ * grad_features [B, C, M] is overwritten.  For M <= 16384 and n <= 8192 each
+ * sum is formed from 0 in increasing (i, t) order, every product and
+ * addition rounded to float32 (deterministic; bit-identical run to run): three
+ * kernels build and sort a per-cloud list of the entries of every known
+ * point, in stream-ordered scratch (cudaMallocAsync, 8 bytes per entry plus
+ * M + 1 ints per cloud), then sum each list in order.  Larger sizes zero
+ * grad_features and accumulate with float32 atomic adds, whose summation
+ * order is not fixed ("Numerical contracts", "Differentiation": the order
+ * may vary).  Index rules as pc_three_interpolate.
  */
 int pc_three_interpolate_backward(const float *grad_out, int64_t B, int64_t C,
                                   int64_t n, const int64_t *idx,

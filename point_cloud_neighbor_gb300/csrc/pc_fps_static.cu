@@ -33,8 +33,17 @@ constexpr int kMaxDevices = 64;
 std::mutex g_static_mutex;
 void *g_static_addr[kMaxDevices] = {};
 
-// Device address of this device's scratch array (resolved once per device).
+// Device address of this device's scratch array (resolved once per device
+// and kept until the process exits: a cudaDeviceReset, which unloads the
+// library's device code, leaves the cached address stale).
 int static_scratch_address(int device, void **out) {
+    if (device < 0 || device >= kMaxDevices) {
+        char msg[128];
+        std::snprintf(msg, sizeof(msg),
+                      "fps_grid_static: device ordinal %d beyond the %d this "
+                      "entry point serves", device, kMaxDevices);
+        return pcn::api_fail(PC_ERR_UNSUPPORTED, msg);
+    }
     std::lock_guard<std::mutex> lock(g_static_mutex);
     if (g_static_addr[device] == nullptr) {
         void *p = nullptr;

@@ -72,3 +72,41 @@ def sd_exact(q, x) -> np.float32:
         t2 = round_f32(F(t) * F(t))
         s = round_f32(F(s) + F(t2))
     return s
+
+
+def fma_exact(a, b, c) -> np.float32:
+    """fl32(a*b + c) with a single rounding (the FMA instruction), exactly."""
+    return round_f32(F(a) * F(b) + F(c))
+
+
+def fma_f32(a, b, c) -> np.ndarray:
+    """Vectorised fl32(a*b + c) with one rounding, for float32 arrays.
+
+    a*b is exact in float64 (48 significant bits, and every float32 product
+    lies inside float64's normal range).  A two-sum gives the exact sum as
+    hi + lo with hi = fl64(a*b + c).  Rounding hi to float32 then gives the
+    correctly rounded result except when hi sits exactly on a midpoint of two
+    float32 neighbours while lo != 0: a float64 value strictly between the
+    exact sum and hi would be nearer the sum than hi is.  That case is
+    decided by the sign of lo.  Checked against ``fma_exact`` in the tests.
+    """
+    a = np.asarray(a, np.float32).astype(np.float64)
+    b = np.asarray(b, np.float32).astype(np.float64)
+    c = np.asarray(c, np.float32).astype(np.float64)
+    p = a * b
+    with np.errstate(invalid="ignore", over="ignore"):
+        hi = p + c
+        bb = hi - p
+        lo = (p - (hi - bb)) + (c - bb)
+        r = hi.astype(np.float32)
+        r64 = r.astype(np.float64)
+        toward = np.where(hi > r64, np.inf, -np.inf).astype(np.float32)
+        other = np.nextafter(r, toward)
+        mid = (r64 + other.astype(np.float64)) * 0.5
+        fix = np.isfinite(hi) & (r64 != hi) & (hi == mid) & (lo != 0)
+    if fix.any():
+        up = lo > 0
+        hi_side = np.where(r64 > other.astype(np.float64), r, other)
+        lo_side = np.where(r64 > other.astype(np.float64), other, r)
+        r = np.where(fix, np.where(up, hi_side, lo_side), r)
+    return r.astype(np.float32)

@@ -1,0 +1,53 @@
+"""Oracle results of the large workloads, computed once per test session.
+
+The full-row comparisons of the 100k- and 1M-point clouds take the oracle
+minutes on the host cores; the brute-force and grid parity tests compare
+against the same rows, so each result is computed once and shared.
+"""
+import functools
+
+import numpy as np
+
+import oracle
+from point_cloud_neighbor_gb300 import inputs
+
+THREADS = oracle.default_threads()
+
+
+@functools.lru_cache(maxsize=None)
+def large(morton: bool):
+    x = inputs.large(morton=morton)
+    x.setflags(write=False)
+    return x
+
+
+@functools.lru_cache(maxsize=None)
+def large_knn(morton: bool):
+    k = inputs.CONFIGS["large"]["knn_k"]
+    x = large(morton)
+    return oracle.knn(x, x, k, threads=THREADS)
+
+
+@functools.lru_cache(maxsize=None)
+def large_ball_query(morton: bool):
+    (r, K), = inputs.CONFIGS["large"]["bq"]
+    x = large(morton)
+    return oracle.ball_query(x, x, r, K, threads=THREADS)
+
+
+@functools.lru_cache(maxsize=None)
+def very_large():
+    """(cloud, the oracle's FPS centre indices, the centres as queries)."""
+    cfg = inputs.CONFIGS["very_large"]
+    x = inputs.very_large()
+    cidx = oracle.fps(x, cfg["npoint"], 0)[0]
+    q = np.ascontiguousarray(x[:, cidx])
+    for a in (x, cidx, q):
+        a.setflags(write=False)
+    return x, cidx, q
+
+
+@functools.lru_cache(maxsize=None)
+def very_large_knn():
+    x, _, q = very_large()
+    return oracle.knn(q, x, inputs.CONFIGS["very_large"]["knn_k"], threads=THREADS)

@@ -116,7 +116,7 @@ def test_fuzz_knn_spatially_ordered(case):
     if case % 4 == 1:
         ql = rng.integers(Q // 2, Q + 1, B).astype(np.int64)
         rl = rng.integers(N // 2, N + 1, B).astype(np.int64)
-    rows = np.unique(rng.integers(0, B * Q, 600))
+    rows = np.unique(rng.integers(0, B * Q, 2000))
     if ql is None:
         d, i = pc.pc_knn(to_dev(q), to_dev(x), k)
         wd, wi = oracle.knn(q, x, k, rows=rows, threads=THREADS)

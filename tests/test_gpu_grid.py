@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import _oracle_cache as cache
 import oracle
 import point_cloud_neighbor_gb300 as pc
 from point_cloud_neighbor_gb300 import inputs
@@ -79,41 +80,42 @@ def test_grid_point_mae_and_pointnet2():
     check_grid_knn(x3, c3, 3, what="grid knn three_nn")
 
 
+@pytest.mark.slow
 @pytest.mark.parametrize("morton", [False, True], ids=["random", "morton"])
-def test_grid_large_sampled_equals_bruteforce(morton):
-    x = inputs.large(morton=morton)
+def test_grid_large_full(morton):
+    """Grid kNN k=16 and Ball Query r=0.02 K=32 over the 100k cloud: every
+    row against the oracle, and equal to the brute-force kernels."""
+    x = cache.large(morton)
     xd = to_dev(x)
     g = pc.pc_grid_build(xd)
     d, i = pc.pc_knn_grid(xd, g, 16)
-    bd, bi = pc.pc_knn(xd, xd, 16)
-    assert torch.equal(i, bi), f"{int((i != bi).sum())} grid kNN indices differ from brute force"
-    assert torch.equal(d.view(torch.int32), bd.view(torch.int32))
     d2, i2 = pc.pc_ball_query_grid(xd, g, 0.02, 32)
+    wd, wi = cache.large_knn(morton)
+    assert_idx_equal(i.cpu().numpy().reshape(-1, 16), wi, "grid knn large, every row")
+    assert_dist_equal(d.cpu().numpy().reshape(-1, 16), wd, "grid knn large, every row")
+    wd2, wi2 = cache.large_ball_query(morton)
+    assert_idx_equal(i2.cpu().numpy().reshape(-1, 32), wi2, "grid bq large, every row")
+    assert_dist_equal(d2.cpu().numpy().reshape(-1, 32), wd2, "grid bq large, every row")
+    bd, bi = pc.pc_knn(xd, xd, 16)
+    assert torch.equal(i, bi) and torch.equal(d.view(torch.int32), bd.view(torch.int32))
     bd2, bi2 = pc.pc_ball_query(xd, xd, 0.02, 32)
-    assert torch.equal(i2, bi2), f"{int((i2 != bi2).sum())} grid BQ indices differ"
-    assert torch.equal(d2.view(torch.int32), bd2.view(torch.int32))
-    rows = inputs.sample_rows(40 + morton, x.shape[1], 256)
-    wd, wi = oracle.knn(x, x, 16, rows=rows, threads=THREADS)
-    assert_idx_equal(i.cpu().numpy().reshape(-1, 16)[rows], wi, "grid knn large")
-    knn_row_properties(x, x, d.cpu().numpy().reshape(-1, 16),
-                       i.cpu().numpy().reshape(-1, 16))
-    bq_row_properties(x, x, 0.02, d2.cpu().numpy().reshape(-1, 32),
-                      i2.cpu().numpy().reshape(-1, 32))
+    assert torch.equal(i2, bi2) and torch.equal(d2.view(torch.int32), bd2.view(torch.int32))
 
 
 @pytest.mark.slow
-def test_grid_very_large_sampled():
-    x = inputs.very_large()
-    q = np.ascontiguousarray(x[:, ::61][:, :16384])
+def test_grid_very_large_full():
+    """Grid kNN k=32 and Ball Query r=0.01 K=64 of the 16,384 FPS centres
+    against the 1M-point cloud, every row against the oracle."""
+    x, _, q = cache.very_large()
     d, i = grid_knn(q, x, 32)
-    rows = inputs.sample_rows(41, q.shape[1], 48)
-    wd, wi = oracle.knn(q, x, 32, rows=rows, threads=THREADS)
-    assert_idx_equal(i[rows], wi, "grid knn 1M")
-    assert_dist_equal(d[rows], wd, "grid knn 1M")
+    wd, wi = cache.very_large_knn()
+    assert_idx_equal(i, wi, "grid knn 1M, every row")
+    assert_dist_equal(d, wd, "grid knn 1M, every row")
     knn_row_properties(q, x, d, i)
     d2, i2 = grid_bq(q, x, 0.01, 64)
-    wd2, wi2 = oracle.ball_query(q, x, 0.01, 64, rows=rows, threads=THREADS)
-    assert_idx_equal(i2[rows], wi2, "grid bq 1M")
+    wd2, wi2 = oracle.ball_query(q, x, 0.01, 64, threads=THREADS)
+    assert_idx_equal(i2, wi2, "grid bq 1M, every row")
+    assert_dist_equal(d2, wd2, "grid bq 1M, every row")
     bq_row_properties(q, x, 0.01, d2, i2)
 
 

@@ -7,14 +7,17 @@ the 1e-6 relative bound the contract allows.  Mismatches are reported as
 counts.
 
 Sizes: every workload runs on the GPU at its full size in the same launch
-configuration as the benchmark; the oracle checks every output where it
-finishes in seconds, and sampled rows plus properties of every row where it
-does not (kNN and Ball Query at 100k and 1M points).
+configuration as the benchmark, and the oracle checks every output row,
+including all 100,000 kNN and Ball Query rows of the 100k-point cloud (random
+and Morton order) and all 16,384 rows of the 1M-point cloud (the kNN ones take
+the oracle minutes on the host cores: they are marked slow).  Properties that
+hold at any size are checked on every row as a second line.
 """
 import numpy as np
 import pytest
 import torch
 
+import _oracle_cache as cache
 import oracle
 import point_cloud_neighbor_gb300 as pc
 from point_cloud_neighbor_gb300 import inputs
@@ -29,7 +32,10 @@ def dev():
 
 
 def to_dev(a):
-    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+    a = np.ascontiguousarray(a)
+    if not a.flags.writeable:       # cached oracle inputs are read-only
+        a = a.copy()
+    return torch.from_numpy(a).to(dev())
 
 
 def same_bits(a, b):
@@ -208,32 +214,33 @@ def test_large_fps_full(morton):
     assert_idx_equal(idx, oracle.fps(x, cfg["npoint"], 0), "fps large")
 
 
+@pytest.mark.slow
 @pytest.mark.parametrize("morton", [False, True], ids=["random", "morton"])
-def test_large_knn_sampled_and_properties(morton):
+def test_large_knn_full(morton):
+    """All 100,000 rows of the 100k x 100k kNN against the oracle (the
+    spatially ordered kernel with its seed pass), then the row properties."""
     cfg = inputs.CONFIGS["large"]
-    x = inputs.large(morton=morton)
+    x = cache.large(morton)
     k = cfg["knn_k"]
     d, i = gpu_knn(x, x, k)                       # all 100k queries
-    rows = inputs.sample_rows(10 + morton, x.shape[1], 384)
-    rows = np.unique(np.concatenate([rows, [0, 1, x.shape[1] - 1]]))
-    wd, wi = oracle.knn(x, x, k, rows=rows, threads=THREADS)
-    assert_idx_equal(i[rows], wi, "knn large sampled")
-    assert_dist_equal(d[rows], wd, "knn large sampled")
+    wd, wi = cache.large_knn(morton)
+    assert_idx_equal(i, wi, "knn large, every row")
+    assert_dist_equal(d, wd, "knn large, every row")
     knn_row_properties(x, x, d, i)
     # a point is its own nearest neighbor unless a smaller-index duplicate exists
     assert (d[:, 0] == 0).all()
 
 
 @pytest.mark.parametrize("morton", [False, True], ids=["random", "morton"])
-def test_large_ball_query_sampled_and_properties(morton):
+def test_large_ball_query_full(morton):
+    """All 100,000 rows of the Ball Query r=0.02 K=32 against the oracle."""
     cfg = inputs.CONFIGS["large"]
-    x = inputs.large(morton=morton)
+    x = cache.large(morton)
     (r, K), = cfg["bq"]
     d2, i = gpu_bq(x, x, r, K)
-    rows = inputs.sample_rows(20 + morton, x.shape[1], 4096)
-    wd2, wi = oracle.ball_query(x, x, r, K, rows=rows, threads=THREADS)
-    assert_idx_equal(i[rows], wi, "bq large sampled")
-    assert_dist_equal(d2[rows], wd2, "bq large sampled")
+    wd2, wi = cache.large_ball_query(morton)
+    assert_idx_equal(i, wi, "bq large, every row")
+    assert_dist_equal(d2, wd2, "bq large, every row")
     bq_row_properties(x, x, r, d2, i)
 
 
@@ -242,10 +249,8 @@ def test_large_ball_query_sampled_and_properties(morton):
 # --------------------------------------------------------------------------
 @pytest.fixture(scope="module")
 def very_large():
-    cfg = inputs.CONFIGS["very_large"]
-    x = inputs.very_large()
-    centers_idx = oracle.fps(x, cfg["npoint"], 0)[0]   # the oracle's centers
-    return cfg, x, centers_idx
+    x, centers_idx, _ = cache.very_large()         # the oracle's centers
+    return inputs.CONFIGS["very_large"], x, centers_idx
 
 
 @pytest.mark.slow
@@ -256,15 +261,16 @@ def test_very_large_fps_full(very_large):
 
 
 @pytest.mark.slow
-def test_very_large_knn_sampled_and_properties(very_large):
+def test_very_large_knn_full(very_large):
+    """kNN k=32 of all 16,384 centres against the 1M-point cloud (the ordered
+    kernel splits the references into parts), every row against the oracle."""
     cfg, x, cidx = very_large
     q = np.ascontiguousarray(x[:, cidx])
     k = cfg["knn_k"]
     d, i = gpu_knn(q, x, k)
-    rows = inputs.sample_rows(30, q.shape[1], 48)
-    wd, wi = oracle.knn(q, x, k, rows=rows, threads=THREADS)
-    assert_idx_equal(i[rows], wi, "knn very_large sampled")
-    assert_dist_equal(d[rows], wd, "knn very_large sampled")
+    wd, wi = cache.very_large_knn()
+    assert_idx_equal(i, wi, "knn very_large, every row")
+    assert_dist_equal(d, wd, "knn very_large, every row")
     knn_row_properties(q, x, d, i)
 
 
@@ -288,12 +294,9 @@ def test_very_large_ball_query_boundary(very_large):
     q = np.ascontiguousarray(x[:, cidx])
     d2, i = gpu_bq(q, ref, r, K)
     bq_row_properties(q, ref, r, d2, i)
-    owner = [c for c, _ in reject + accept]
-    rows = np.unique(np.concatenate([np.array(owner, np.int64),
-                                     inputs.sample_rows(7, q.shape[1], 256)]))
-    wd2, wi = oracle.ball_query(q, ref, r, K, rows=rows, threads=THREADS)
-    assert_idx_equal(i[rows], wi, "bq very_large boundary rows")
-    assert_dist_equal(d2[rows], wd2, "bq very_large boundary rows")
+    wd2, wi = oracle.ball_query(q, ref, r, K, threads=THREADS)
+    assert_idx_equal(i, wi, "bq very_large, every row")
+    assert_dist_equal(d2, wd2, "bq very_large, every row")
     # every boundary point is decided the way the contract says
     nrej = nacc = 0
     for p, (c, _) in zip(pos[:len(reject)], reject):
@@ -305,6 +308,50 @@ def test_very_large_ball_query_boundary(very_large):
             assert p in set(row.tolist())
             nacc += 1
     assert nrej >= 500 and nacc >= 400
+
+
+# --------------------------------------------------------------------------
+# clouds translated far from the origin: the filter's frame is centred on
+# the cloud, but the slack of its bound grows with the squared distance of
+# the points from that centre relative to the selection bound, and far from
+# the origin coordinates are coarse (spacing 1/1024 at 1e4, 1/32 at 3e5,
+# 1/16 at 1e6), so exact ties abound
+# --------------------------------------------------------------------------
+def translated(x, offset):
+    return (x.astype(np.float64) + offset).astype(np.float32)
+
+
+@pytest.mark.parametrize("offset", [1e4, 3e5, 1e6])
+def test_translated_pointnet2_all_kernels(offset):
+    """Workload-3 geometry (16 clouds of 4096 points) moved by `offset`:
+    FPS, the lane kNN (k=16 of the centres, three_nn k=3), the warp-list kNN
+    (k=64) and Ball Query (r=0.1 K=32, r=0.2 K=64), every row against the
+    oracle."""
+    cfg = inputs.CONFIGS["pointnet2"]
+    x = translated(inputs.pointnet2(), offset)
+    want = oracle.fps(x, cfg["npoint"], 0, threads=THREADS)
+    assert_idx_equal(gpu_fps(x, cfg["npoint"], 0), want, f"fps +{offset:g}")
+    c = np.ascontiguousarray(np.take_along_axis(x, want[..., None], axis=1))
+    check_knn(c, x, 16, what=f"lane knn +{offset:g}")
+    check_knn(x, c, 3, what=f"three_nn +{offset:g}")
+    check_knn(c, x, 64, what=f"warp-list knn k=64 +{offset:g}")
+    for r, K in cfg["bq"]:
+        check_bq(c, x, r, K, what=f"bq +{offset:g} r={r}")
+
+
+@pytest.mark.parametrize("offset", [1e4, 3e5, -1e6])
+def test_translated_ordered_knn_and_ball_query(offset):
+    """A 20,000-point mixture cloud moved by `offset`, every point a query:
+    the spatially ordered kNN (k=16) and Ball Query (r=0.02 scaled to the
+    coordinate spacing), every row against the oracle."""
+    rng = np.random.default_rng(int(abs(offset)) % 1000 + 31)
+    means = rng.random((16, 3))
+    pick = rng.integers(0, 16, 20000)
+    x = (means[pick] + rng.standard_normal((20000, 3)) * 0.05)[None]
+    x = translated(x.astype(np.float32), offset)
+    check_knn(x, x, 16, what=f"ordered knn +{offset:g}")
+    r = max(0.02, 4 * float(np.spacing(np.float32(abs(offset)))))
+    check_bq(x, x, r, 32, what=f"bq +{offset:g} r={r}")
 
 
 # --------------------------------------------------------------------------

@@ -6,13 +6,14 @@ nor allocate a workspace for it.  This entry point keeps the grid schedule's
 scratch in a fixed array inside the library.  The test calls it through the
 C ABI twice in a row -- on two different clouds, so the second call runs on
 whatever the first left in the array -- and compares each result with the
-regular entry point (pc_fps_ex, grid schedule, library-allocated scratch).
-Indices must be identical.  This file is collected last on purpose.
+regular entry point (pc_fps_ex, grid schedule, library-allocated scratch) and
+with the oracle.  Indices must be identical.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from point_cloud_neighbor_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
@@ -35,14 +36,17 @@ def _static(x, npoint, start, bpc):
 
 def test_static_scratch_fps_matches_regular_entry_point_twice():
     dev = torch.device("cuda:0")
-    first = torch.from_numpy(inputs.large()).to(dev)                 # 1 x 100k
-    second = torch.from_numpy(inputs.random_cloud(21, 2, 7001)).to(dev)
-    for x, npoint, start, bpc in ((first, 1000, 5, 0), (second, 600, 3, 9)):
+    first = inputs.large()                                  # 1 x 100k
+    second = inputs.random_cloud(21, 2, 7001)
+    for xh, npoint, start, bpc in ((first, 1000, 5, 0), (second, 600, 3, 9)):
+        x = torch.from_numpy(xh).to(dev)
         want = _regular(x, npoint, start, bpc)
         got = _static(x, npoint, start, bpc)
         torch.cuda.synchronize(dev)
         g, w = got.cpu().numpy(), want.cpu().numpy()
         assert np.array_equal(g, w), f"{int((g != w).sum())} of {g.size} indices differ"
+        o = oracle.fps(xh, npoint, start, threads=oracle.default_threads())
+        assert np.array_equal(g, o), f"{int((g != o).sum())} of {g.size} differ from the oracle"
     assert binding.pc_device_status(reset=True) == 0
 
 
