@@ -350,7 +350,6 @@ def run_gpu(args):
     clk = clocks.summary()
     max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     alu_peak = fp32_alu_peak_tflops(sm_count, max_mhz)
-    hbm_peak = float(peaks["hbm_gbs"])
 
     per = {
         "fps": fps_ms / args.steps, "knn": knn_ms / args.steps,
@@ -360,10 +359,10 @@ def run_gpu(args):
         "fps": {
             "samples_per_s": npoint * world / (per["fps"] / 1e3),
             "ms": per["fps"],
-            "algorithmic_bytes": fps_bytes,
-            "achieved_gbs": fps_bytes / (per["fps"] / 1e3) / 1e9,
-            "hbm_frac": fps_bytes / (per["fps"] / 1e3) / 1e9 / hbm_peak,
             "us_per_sample": per["fps"] * 1e3 / (npoint - 1),
+            # what a kernel streaming coordinates and minima through HBM every
+            # step would move; this one keeps them on chip (context only)
+            "streamed_equivalent_gbs": fps_bytes / (per["fps"] / 1e3) / 1e9,
         },
         "knn": {
             "queries_per_s": N * world / (per["knn"] / 1e3),
@@ -381,8 +380,9 @@ def run_gpu(args):
     # same cluster schedule on 1024 points per block
     fps_sms = B * STEP_FPS_CLUSTER
     ops["fps"]["cluster"] = STEP_FPS_CLUSTER
-    ops["fps"]["alu_bound_ms"] = (float(N) * (npoint - 1) * 10 /
+    ops["fps"]["alu_bound_ms"] = (float(N) * (npoint - 1) * FPS_INSTR_PER_POINT_STEP /
                                   (max(fps_sms, 1) * 128 * max_mhz * 1e6) * 1e3)
+    ops["fps"]["alu_frac"] = ops["fps"]["alu_bound_ms"] / per["fps"]
     if fps_sms > 1:
         fx = torch.from_numpy(inputs.random_cloud(7, 1, 1024 * fps_sms)).to(device)
         try:
@@ -390,6 +390,7 @@ def run_gpu(args):
                                                 cluster_size=fps_sms),
                               3, 3, flush, stream)
             ops["fps"]["sync_floor_ms"] = floor_ms
+            ops["fps"]["sync_floor_frac"] = floor_ms / per["fps"]
             ops["fps"]["sync_floor_note"] = (
                 f"the same cluster of {fps_sms} on 1024 points per block, npoint={npoint}")
         except pc.PointCloudError as err:
@@ -403,9 +404,17 @@ def run_gpu(args):
 
     def roof_of(op):
         if op == "fps":
-            r = {"bound": "hbm", "achieved": ops["fps"]["achieved_gbs"],
-                 "peak": hbm_peak, "unit": "GB/s",
-                 "frac": ops["fps"]["achieved_gbs"] / hbm_peak}
+            f = ops["fps"]
+            floor = f.get("sync_floor_ms")
+            r = {"bound": "latency", "achieved": f["us_per_sample"],
+                 "peak": floor * 1e3 / (npoint - 1) if floor else None,
+                 "unit": "us per step", "frac": (floor / per["fps"]) if floor else None,
+                 "alu_frac": f["alu_frac"],
+                 "note": "measured floor of the cluster's per-step reduction and "
+                         "exchange; points and minima stay on chip (no HBM stream)"}
+            r["traffic"] = recorded_traffic(op)
+            r["kernel"] = op
+            return r
         else:
             r = {"bound": "alu", "achieved": ops[op]["achieved_tflops"],
                  "peak": alu_peak, "unit": "TFLOP/s",
@@ -430,12 +439,12 @@ def run_gpu(args):
                     "largest kernel of the serial step")
     roof_all = {op: roof_of(op) for op in ("fps", "knn", "ball_query")}
 
-    grid = next_rows = None
+    grid = next_rows = configs = None
     if not args.step_only:
+        with_oracle = rank == 0 and world == 1 and not args.no_cpu_baseline
         grid = run_grid(args, pc, x, flush, device, world)
-        next_rows = run_next_rows(args, pc, flush, device, world,
-                                  with_oracle=(rank == 0 and world == 1
-                                               and not args.no_cpu_baseline))
+        next_rows = run_next_rows(args, pc, flush, device, world, with_oracle=with_oracle)
+        configs = run_configs(args, pc, flush, device, world, with_oracle=with_oracle)
 
     # end to end through the public API: pinned host in, pinned host out
     e2e = None if args.step_only else run_e2e(args, pc, x_host, device, world)
@@ -450,7 +459,7 @@ def run_gpu(args):
                                                "2: FPS concurrent with kNN then Ball Query"),
                                    "fps_cluster": STEP_FPS_CLUSTER}),
         "roofline": roof, "roofline_per_kernel": roof_all, "ops": ops,
-        "grid": grid, "next_rows": next_rows,
+        "grid": grid, "next_rows": next_rows, "configs": configs,
         "e2e": e2e,
         "gpu_launches": launches,
         "gpu_launches_note": "the timed FPS + kNN + Ball Query step; the grid and "
@@ -504,17 +513,10 @@ def run_only(args):
         calls["three_interpolate_backward"] = lambda: pc.pc_three_interpolate_backward(
             gup, idx, w, 1024)
     fn = calls[args.only]
-    for _ in range(args.warmup):
-        fn()
-    torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        fn()
-    e1.record()
-    torch.cuda.synchronize(device)
-    print(json.dumps({"op": args.only, "ms": e0.elapsed_time(e1) / args.steps,
-                      "calls": args.steps}))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    ms = _timed(fn, args.steps, args.warmup, flush, torch.cuda.current_stream(device))
+    print(json.dumps({"op": args.only, "ms": ms, "calls": args.steps,
+                      "l2": "flushed before every call (outside the events)"}))
 
 
 def run_grid(args, pc, x, flush, device, world):
@@ -649,7 +651,8 @@ def run_next_rows(args, pc, flush, device, world, with_oracle):
         "backward_roofline": {"bound": "hbm", "achieved": bwd_bytes / (bwd / 1e3) / 1e9,
                               "peak": hbm, "unit": "GB/s",
                               "frac": bwd_bytes / (bwd / 1e3) / 1e9 / hbm},
-        "launches": {"forward": 1, "backward": "1 + memset"}}
+        "launches": {"forward": 1,
+                     "backward": "3 (entry lists, segment sort, ordered sums)"}}
 
     # PyTorch3D-style Ball Query with return_nn
     bq_ms = _timed(lambda: p3d_ball_query(centers, px, K=64, radius=0.2), steps, warm,
@@ -667,17 +670,12 @@ def run_next_rows(args, pc, flush, device, world, with_oracle):
                            256), dtype=torch.uint8, device=device)
     fv_ms = _timed(lambda: pc.pc_fps(vx, 16384, 0, out=fps_out_v, workspace=ws_v),
                    max(3, min(steps, 5)), 3, flush, stream)
-    fv_bytes = float(vx_h.shape[1]) * 16383 * FPS_BYTES_PER_POINT_STEP
     out["fps_1m"] = {
         "workload": "N=1,000,000 uniform in [0,1)^3 with 1% duplicates, 16384 samples",
-        "ms": fv_ms, "us_per_sample": fv_ms * 1e3 / 16383,
-        "samples_per_s": 16384 * world / (fv_ms / 1e3),
-        "roofline": {"bound": "hbm", "achieved": fv_bytes / (fv_ms / 1e3) / 1e9,
-                     "peak": hbm, "unit": "GB/s",
-                     "frac": fv_bytes / (fv_ms / 1e3) / 1e9 / hbm,
-                     "note": "20 B per point-step if streamed; the kernel keeps "
-                             "points and minima on chip"},
-        "launches": 1}
+        "samples_per_s": 16384 * world / (fv_ms / 1e3), "launches": 1}
+    out["fps_1m"].update(_fps_bounds(pc, vx_h.shape, 16384, fv_ms, device, flush, stream,
+                                     float(peaks.get("sm_max_mhz", 2070.0)),
+                                     max(3, min(steps, 5))))
     del vx, ws_v
 
     # kNN in D dimensions at the DGCNN EdgeConv feature shape
@@ -733,6 +731,203 @@ def run_next_rows(args, pc, flush, device, world, with_oracle):
         out["pytorch3d_ball_query"]["oracle"] = {
             "ms_extrapolated": (t1 - t0) / len(qrows) * TB * TM * 1e3, "cores": 1,
             "sample": f"{len(qrows)} query rows (gather not included), extrapolated"}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# every workload: FPS, kNN and Ball Query of each configuration, timed alone
+# ---------------------------------------------------------------------------
+FPS_INSTR_PER_POINT_STEP = 10   # min update, compare and select per point-step
+
+
+def _fps_bounds(pc, x_shape, npoint, ms, device, flush, stream, max_mhz, steps):
+    """FPS against the bounds it does face: the ALU work on the SMs its
+    schedule holds, and the measured floor of its per-step reduction and
+    exchange (the same schedule, same sample count, 1024 points per block)."""
+    import torch
+    from point_cloud_neighbor_gb300 import inputs
+    B, N = int(x_shape[0]), int(x_shape[1])
+    strategy, bpc = pc.pc_fps_plan(B, N)
+    sms = pc.pc_fps_sm_count(B, N, npoint)
+    alu_ms = (float(B) * N * (npoint - 1) * FPS_INSTR_PER_POINT_STEP /
+              (max(sms, 1) * 128 * max_mhz * 1e6) * 1e3)
+    n_floor = 1024 * bpc
+    fx = torch.from_numpy(inputs.random_cloud(7, B, n_floor)).to(device)
+    kw = {"strategy": strategy}
+    if strategy == pc.PC_FPS_CLUSTER:
+        kw["cluster_size"] = bpc
+    elif strategy == pc.PC_FPS_GRID:
+        kw["blocks_per_cloud"] = bpc
+    try:
+        floor_ms = _timed(lambda: pc.pc_fps(fx, npoint, 0, **kw), steps, 3, flush, stream)
+    except pc.PointCloudError as err:
+        floor_ms = None
+        note = f"floor not measured: {err}"
+    else:
+        note = (f"the same schedule on {n_floor} points per cloud "
+                f"(1024 per block), npoint={npoint}")
+    names = {pc.PC_FPS_BLOCK: "block", pc.PC_FPS_CLUSTER: "cluster",
+             pc.PC_FPS_GRID: "grid"}
+    out = {"schedule": names.get(strategy, str(strategy)), "blocks_per_cloud": bpc,
+           "sms": sms, "ms": ms, "us_per_step": ms * 1e3 / max(npoint - 1, 1),
+           "alu_bound_ms": alu_ms, "alu_frac": alu_ms / ms,
+           "floor_ms": floor_ms, "floor_frac": (floor_ms / ms) if floor_ms else None,
+           "floor_note": note,
+           "streamed_equivalent_gbs": float(B) * N * (npoint - 1) *
+           FPS_BYTES_PER_POINT_STEP / (ms / 1e3) / 1e9}
+    out["roofline"] = {
+        "bound": "latency", "achieved": out["us_per_step"],
+        "peak": (floor_ms * 1e3 / max(npoint - 1, 1)) if floor_ms else None,
+        "unit": "us per step", "frac": out["floor_frac"],
+        "note": "measured floor of the schedule's per-step reduction and exchange "
+                "(the kernel keeps points and minima on chip: no HBM stream)"}
+    return out
+
+
+def _oracle_timing(fn, units, budget_s):
+    """Seconds per unit of one oracle call on a bounded sample: fn(n) runs the
+    oracle on n units; n doubles from 1 until a call takes budget_s / 4."""
+    n = 1
+    while True:
+        t0 = time.perf_counter()
+        fn(n)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or n >= units:
+            return dt / n, n
+        n = min(units, n * max(2, int(budget_s / 4 / max(dt, 1e-4))))
+
+
+def run_configs(args, pc, flush, device, world, with_oracle):
+    """The five workloads, each operator timed alone (CUDA events on the
+    launching stream, L2 flushed before every call), with its roofline
+    fraction and, on rank 0, the oracle timed on the host cores single-threaded
+    and on all cores (bounded samples, extrapolated per unit)."""
+    import torch
+    from point_cloud_neighbor_gb300 import inputs
+    stream = torch.cuda.current_stream(device)
+    steps, warm = max(3, min(args.steps, 10)), 3
+    peaks, peak_kind = measured_peaks()
+    max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    sm_count = torch.cuda.get_device_properties(device).multi_processor_count
+    alu = fp32_alu_peak_tflops(sm_count, max_mhz)
+    threads = os.cpu_count() or 1
+    if with_oracle:
+        import oracle
+        oracle.build()
+    out = {}
+    plan = [
+        ("tiny", "tiny", False),
+        ("point_mae", "point_mae", False),
+        ("pointnet2", "pointnet2", False),
+        ("large_morton", "large", True),
+        ("very_large", "very_large", False),
+    ]
+    for name, base, morton in plan:
+        cfg = inputs.CONFIGS[base]
+        xh = inputs.large(morton=True) if morton else inputs.make(base)
+        x = torch.from_numpy(xh).to(device)
+        B, N = xh.shape[0], xh.shape[1]
+        npoint = cfg["npoint"]
+        entry = {"B": B, "N": N}
+        fo = torch.empty((B, npoint), dtype=torch.int64, device=device)
+        ms = _timed(lambda: pc.pc_fps(x, npoint, 0, out=fo), steps, warm, flush, stream)
+        fps = {"npoint": npoint, "samples_per_s": B * npoint * world / (ms / 1e3)}
+        fps.update(_fps_bounds(pc, xh.shape, npoint, ms, device, flush, stream,
+                               max_mhz, steps))
+        entry["fps"] = fps
+        cen = torch.gather(x, 1, fo.unsqueeze(-1).expand(B, npoint, 3)).contiguous()
+        centers_h = cen.cpu().numpy()
+        # kNN: queries and references of the workload
+        k = cfg["knn_k"]
+        if name == "pointnet2":          # three_nn shape: points vs centres
+            kq, kr, kq_h, kr_h = x, cen, xh, centers_h
+        elif name == "large_morton":     # every point a query
+            kq, kr, kq_h, kr_h = x, x, xh, xh
+        else:                            # the FPS centres as queries
+            kq, kr, kq_h, kr_h = cen, x, centers_h, xh
+        Q, Nr = kq.shape[1], kr.shape[1]
+        kd = torch.empty((B, Q, k), dtype=torch.float32, device=device)
+        ki = torch.empty((B, Q, k), dtype=torch.int64, device=device)
+        ms = _timed(lambda: pc.pc_knn(kq, kr, k, out_dist=kd, out_idx=ki), steps, warm,
+                    flush, stream)
+        pairs = float(B) * Q * Nr
+        tfl = pairs * FLOPS_PER_PAIR / (ms / 1e3) / 1e12
+        entry["knn"] = {"k": k, "queries": B * Q, "references_per_cloud": Nr, "ms": ms,
+                        "queries_per_s": B * Q * world / (ms / 1e3), "pairs": pairs,
+                        "roofline": {"bound": "alu", "achieved": tfl, "peak": alu,
+                                     "unit": "TFLOP/s", "frac": tfl / alu}}
+        if with_oracle:
+            rows_total = B * Q
+            rng = np.random.default_rng(11)
+            perm = rng.permutation(rows_total).astype(np.int64)
+            per1, n1 = _oracle_timing(
+                lambda n: oracle.knn(kq_h, kr_h, k, rows=np.sort(perm[:n])),
+                rows_total, 2.0)
+            perT, nT = _oracle_timing(
+                lambda n: oracle.knn(kq_h, kr_h, k, rows=np.sort(perm[:n]), threads=threads),
+                rows_total, 2.0)
+            entry["knn"]["oracle"] = {
+                "single_thread_ms": per1 * rows_total * 1e3,
+                "all_cores_ms": perT * rows_total * 1e3, "cores": threads,
+                "sample": f"{n1} rows on 1 thread, {nT} rows on {threads}, "
+                          "extrapolated to all rows"}
+        # Ball Query: the workload's radii on the FPS centres (every point
+        # a query on the 100k cloud)
+        bqs = []
+        for r, K in cfg["bq"]:
+            bq_q, bq_q_h = (x, xh) if name == "large_morton" else (cen, centers_h)
+            Qb = bq_q.shape[1]
+            bd = torch.empty((B, Qb, K), dtype=torch.float32, device=device)
+            bi = torch.empty((B, Qb, K), dtype=torch.int64, device=device)
+            ms = _timed(lambda: pc.pc_ball_query(bq_q, x, r, K, out_dist2=bd, out_idx=bi),
+                        steps, warm, flush, stream)
+            last = bi.cpu().numpy().reshape(-1, K)[:, K - 1]
+            bpairs = float(np.where(last >= 0, last + 1, N).sum())
+            tfl = bpairs * FLOPS_PER_PAIR / (ms / 1e3) / 1e12
+            e = {"radius": r, "K": K, "queries": B * Qb, "ms": ms,
+                 "queries_per_s": B * Qb * world / (ms / 1e3), "pairs": bpairs,
+                 "roofline": {"bound": "alu", "achieved": tfl, "peak": alu,
+                              "unit": "TFLOP/s", "frac": tfl / alu}}
+            if with_oracle:
+                rows_total = B * Qb
+                perm = np.random.default_rng(12).permutation(rows_total).astype(np.int64)
+                per1, n1 = _oracle_timing(
+                    lambda n: oracle.ball_query(bq_q_h, xh, r, K, rows=np.sort(perm[:n])),
+                    rows_total, 2.0)
+                perT, nT = _oracle_timing(
+                    lambda n: oracle.ball_query(bq_q_h, xh, r, K, rows=np.sort(perm[:n]),
+                                                threads=threads),
+                    rows_total, 2.0)
+                e["oracle"] = {"single_thread_ms": per1 * rows_total * 1e3,
+                               "all_cores_ms": perT * rows_total * 1e3, "cores": threads,
+                               "sample": f"{n1} rows on 1 thread, {nT} rows on {threads}, "
+                                         "extrapolated to all rows"}
+            bqs.append(e)
+        if bqs:
+            entry["ball_query"] = bqs
+        if with_oracle:
+            # FPS: the first few samples of every cloud, extrapolated per sample
+            def fps1(n, xh=xh):
+                oracle.fps(xh, n + 1, 0)
+
+            # all cores: several clouds run in parallel, one cloud's steps
+            # split their points over the threads
+            def fpsT(n, xh=xh):
+                if B > 1:
+                    oracle.fps(xh, n + 1, 0, threads=threads)
+                else:
+                    oracle.fps_all_cores(xh, n + 1, 0, threads=threads)
+            per1, n1 = _oracle_timing(fps1, npoint - 1, 2.0)
+            perT, nT = _oracle_timing(fpsT, npoint - 1, 2.0)
+            how = (f"the {B} clouds over {threads} threads" if B > 1 else
+                   f"each step's points split over {threads} threads")
+            fps["oracle"] = {
+                "single_thread_ms": per1 * (npoint - 1) * 1e3,
+                "all_cores_ms": perT * (npoint - 1) * 1e3, "cores": threads,
+                "sample": f"{n1} samples on 1 thread, {nT} samples with {how}, "
+                          f"extrapolated to {npoint - 1} samples"}
+        out[name] = entry
+        del x
     return out
 
 
@@ -820,7 +1015,10 @@ def oracle_step_costs(x_host, knn_rows, bq_rows, fps_steps, threads, seed=0):
     oracle.ball_query(x_host, x_host, W["bq_radius"], W["bq_K"], rows=rb,
                       threads=threads)
     t2 = time.perf_counter()
-    oracle.fps(x_host, fps_steps + 1, 0)
+    if threads > 1:       # each step's points split over the threads
+        oracle.fps_all_cores(x_host, fps_steps + 1, 0, threads=threads)
+    else:
+        oracle.fps(x_host, fps_steps + 1, 0)
     t3 = time.perf_counter()
     return {"knn_s_per_query": (t1 - t0) / knn_rows,
             "bq_s_per_query": (t2 - t1) / bq_rows,
@@ -846,14 +1044,57 @@ def cpu_baseline(x_host, budget_s=20.0):
     fps_steps = int(max(8, min(4095, share / max(probe["fps_s_per_sample"], 1e-9))))
     c = oracle_step_costs(x_host, knn_rows, bq_rows, fps_steps, threads, seed=1)
     step_s = extrapolated_step_s(c)
+    # the same oracle on one thread (smaller samples)
+    one = oracle_step_costs(x_host, max(2, knn_rows // (2 * threads)),
+                            max(16, bq_rows // (2 * threads)), max(8, fps_steps // 4),
+                            1, seed=2)
+    step1_s = extrapolated_step_s(one)
     return {"value": 2 * WORKLOAD["N"] / step_s, "unit": UNIT, "cores": threads,
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": (f"{knn_rows} kNN queries and {bq_rows} Ball Query queries "
-                       f"on {threads} threads, {fps_steps} FPS samples on 1 thread "
-                       f"(FPS is sequential), extrapolated to the full step"),
+                       f"on {threads} threads, {fps_steps} FPS samples with each "
+                       f"step's points split over {threads} threads, extrapolated "
+                       f"to the full step"),
             "step_s_extrapolated": step_s, "measured_s": c["elapsed_s"],
             "per_unit_s": {k: c[k] for k in ("knn_s_per_query", "bq_s_per_query",
-                                             "fps_s_per_sample")}}
+                                             "fps_s_per_sample")},
+            "single_thread": {
+                "value": 2 * WORKLOAD["N"] / step1_s, "step_s_extrapolated": step1_s,
+                "sample": (f"{one['knn_rows']} kNN queries, {one['bq_rows']} Ball Query "
+                           f"queries and {one['fps_steps']} FPS samples on 1 thread, "
+                           f"extrapolated to the full step"),
+                "per_unit_s": {k: one[k] for k in ("knn_s_per_query", "bq_s_per_query",
+                                                   "fps_s_per_sample")}}}
+
+
+ARM_PARTS = {(0x41, 0xd4f): "Arm Neoverse V2", (0x41, 0xd40): "Arm Neoverse V1",
+             (0x41, 0xd0c): "Arm Neoverse N1", (0x41, 0xd8e): "Arm Neoverse N3",
+             (0x41, 0xd84): "Arm Neoverse V3"}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name from /proc/cpuinfo ("model name" on x86;
+    the implementer and part numbers on Arm), else the architecture."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    key, val = line.split(":", 1)
+                    fields.setdefault(key.strip().lower(), val.strip())
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "cpu model", "hardware"):
+        if fields.get(key):
+            return fields[key]
+    try:
+        impl = int(fields["cpu implementer"], 16)
+        part = int(fields["cpu part"], 16)
+    except (KeyError, ValueError):
+        return platform.machine()
+    return ARM_PARTS.get((impl, part),
+                         f"{platform.machine()} implementer {impl:#x} part {part:#x}")
 
 
 def run_reference(args):
@@ -873,8 +1114,8 @@ def run_reference(args):
     step_s = extrapolated_step_s(agg)
     value = 2 * WORKLOAD["N"] / step_s
     sample = (f"per step {knn_rows} kNN queries and {bq_rows} Ball Query queries "
-              f"on {threads} threads and {fps_steps} FPS samples on 1 thread, "
-              f"extrapolated to the full step")
+              f"on {threads} threads and {fps_steps} FPS samples with each step's "
+              f"points split over {threads} threads, extrapolated to the full step")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -882,7 +1123,7 @@ def run_reference(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": workload_config({"parallelism": "host cores, oracle"}),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

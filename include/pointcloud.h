@@ -122,6 +122,15 @@ int pc_fps_ex(const float *xyz, int64_t B, int64_t N, int64_t npoint,
 size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
                                  int strategy, int blocks_per_cloud);
 
+/* The schedule pc_fps_ex would run for these sizes and arguments on the
+ * current device: *out_strategy (PC_FPS_BLOCK, _CLUSTER or _GRID) and
+ * *out_blocks_per_cloud (the cluster size, or the grid's blocks per cloud;
+ * 1 for PC_FPS_BLOCK).  Nothing is enqueued.  Returns PC_OK,
+ * PC_ERR_INVALID_ARGUMENT (B or N < 1, null outputs), PC_ERR_UNSUPPORTED (no
+ * schedule fits) or PC_ERR_NO_DEVICE. */
+int pc_fps_plan(int64_t B, int64_t N, int strategy, int cluster_size,
+                int blocks_per_cloud, int *out_strategy, int *out_blocks_per_cloud);
+
 /*
  * pc_fps_grid_static: pc_fps with the PC_FPS_GRID schedule for callers that
  * cannot allocate device memory at call time (for instance a host program

@@ -49,7 +49,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm", "-lpthread"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -64,6 +64,8 @@ def _bind(lib):
     lib.orc_radius_threshold.argtypes = [ctypes.c_double]
     lib.orc_fps.restype = ctypes.c_int
     lib.orc_fps.argtypes = [P, I, I, I, I, P]
+    lib.orc_fps_threads.restype = ctypes.c_int
+    lib.orc_fps_threads.argtypes = [P, I, I, I, I, I, P]
     lib.orc_min_dist_to_set.restype = ctypes.c_int
     lib.orc_min_dist_to_set.argtypes = [P, I, P, I, P, I, P]
     lib.orc_knn_rows.restype = ctypes.c_int
@@ -109,7 +111,7 @@ def compile_variant(source_text: str, out_path: str) -> str:
     src = out_path + ".c"
     with open(src, "w") as f:
         f.write(source_text)
-    subprocess.run(["gcc", *CFLAGS, src, "-o", out_path, "-lm"], check=True)
+    subprocess.run(["gcc", *CFLAGS, src, "-o", out_path, "-lm", "-lpthread"], check=True)
     return out_path
 
 
@@ -204,6 +206,20 @@ def fps(xyz, npoint: int, start_idx: int = 0, threads: int = 1) -> np.ndarray:
     else:
         with ThreadPoolExecutor(len(chunks)) as ex:
             list(ex.map(lambda c: run(*c), chunks))
+    return out
+
+
+def fps_all_cores(xyz, npoint: int, start_idx: int = 0,
+                  threads: int | None = None) -> np.ndarray:
+    """Farthest point sampling with each step's points split over host
+    threads (one cloud after another): the all-core CPU baseline.  Returns
+    what ``fps`` returns; the tests check the two are equal."""
+    xyz = _f32(xyz)
+    B, N, _ = xyz.shape
+    threads = default_threads() if threads is None else int(threads)
+    out = np.empty((B, npoint), dtype=np.int64)
+    _check(_load().orc_fps_threads(_ptr(xyz), B, N, npoint, start_idx,
+                                   max(1, threads), _ptr(out)), "fps_all_cores")
     return out
 
 

@@ -22,10 +22,12 @@
  *
  * Inputs are finite float32 coordinates, row-major [B, N, 3]; indices int64.
  */
+#define _POSIX_C_SOURCE 200809L  /* pthread barriers under -std=c11 */
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #include <math.h>
+#include <pthread.h>
 
 #if defined(__FAST_MATH__)
 #error "the oracle must not be built with fast-math"
@@ -108,6 +110,120 @@ int orc_fps(const float *xyz, int64_t B, int64_t N, int64_t npoint,
     }
     free(m);
     return ORC_OK;
+}
+
+/*
+ * Farthest point sampling with the points of each step split over T host
+ * threads (the all-core CPU baseline).  Same definition as orc_fps (project
+ * page, "Farthest point sampling"), same arithmetic per point: thread t owns
+ * the points [lo_t, hi_t) of a contiguous split in increasing order; in each
+ * step it updates m_j = min(m_j, s(x_j, x_c)) for its points and keeps the
+ * first j of its range attaining its maximum; after a barrier one thread takes
+ * the largest of those maxima, scanning the threads in increasing order and
+ * replacing only on a strictly larger value, which is the smallest index
+ * attaining the global maximum; a second barrier publishes the new center.
+ */
+typedef struct {
+    const float *x;
+    float *m;
+    int64_t N, npoint, T;
+    int64_t *sel;            /* out_idx of the current cloud */
+    int64_t c;               /* current center */
+    float *best_v;           /* [T] */
+    int64_t *best_j;         /* [T] */
+    pthread_barrier_t *bar;
+} orc_fps_shared;
+
+typedef struct {
+    orc_fps_shared *sh;
+    int64_t t;
+} orc_fps_task;
+
+static void *orc_fps_worker(void *arg)
+{
+    orc_fps_task *task = (orc_fps_task *)arg;
+    orc_fps_shared *sh = task->sh;
+    const int64_t t = task->t, T = sh->T, N = sh->N;
+    const int64_t lo = N * t / T, hi = N * (t + 1) / T;
+    const float *x = sh->x;
+    float *m = sh->m;
+    for (int64_t step = 0; step < sh->npoint; ++step) {
+        const int64_t c = sh->c;
+        /* m_j = s(x_j, x_{c_0}) on the first step, min with s(x_j, x_c) after */
+        float bv = 0.0f;
+        int64_t bj = -1;
+        for (int64_t j = lo; j < hi; ++j) {
+            float s = orc_s32(x + 3 * j, x + 3 * c);
+            if (step == 0 || s < m[j]) m[j] = s;
+            if (bj < 0 || m[j] > bv) {
+                bv = m[j];
+                bj = j;
+            }
+        }
+        sh->best_v[t] = bv;
+        sh->best_j[t] = bj;
+        pthread_barrier_wait(sh->bar);
+        if (t == 0 && step + 1 < sh->npoint) {
+            int64_t best = -1;
+            float v = 0.0f;
+            for (int64_t u = 0; u < T; ++u)
+                if (sh->best_j[u] >= 0 && (best < 0 || sh->best_v[u] > v)) {
+                    v = sh->best_v[u];
+                    best = sh->best_j[u];
+                }
+            sh->c = best;
+            sh->sel[step + 1] = best;
+        }
+        pthread_barrier_wait(sh->bar);
+    }
+    return NULL;
+}
+
+int orc_fps_threads(const float *xyz, int64_t B, int64_t N, int64_t npoint,
+                    int64_t start_idx, int64_t nthreads, int64_t *out_idx)
+{
+    if (B < 0 || N < 1 || npoint < 1 || start_idx < 0 || start_idx >= N ||
+        nthreads < 1 || nthreads > 1024)
+        return ORC_BAD_ARGUMENT;
+    const int64_t T = nthreads;
+    float *m = (float *)malloc((size_t)N * sizeof(float));
+    float *bv = (float *)malloc((size_t)T * sizeof(float));
+    int64_t *bj = (int64_t *)malloc((size_t)T * sizeof(int64_t));
+    pthread_t *th = (pthread_t *)malloc((size_t)T * sizeof(pthread_t));
+    orc_fps_task *tasks = (orc_fps_task *)malloc((size_t)T * sizeof(orc_fps_task));
+    if (!m || !bv || !bj || !th || !tasks) {
+        free(m); free(bv); free(bj); free(th); free(tasks);
+        return ORC_NO_MEMORY;
+    }
+    pthread_barrier_t bar;
+    pthread_barrier_init(&bar, NULL, (unsigned)T);
+    int rc = ORC_OK;
+    for (int64_t b = 0; b < B && rc == ORC_OK; ++b) {
+        orc_fps_shared sh = {xyz + (size_t)b * (size_t)N * 3, m, N, npoint, T,
+                             out_idx + (size_t)b * (size_t)npoint, start_idx,
+                             bv, bj, &bar};
+        sh.sel[0] = start_idx;
+        int64_t started = 0;
+        for (int64_t t = 1; t < T; ++t) {
+            tasks[t].sh = &sh;
+            tasks[t].t = t;
+            if (pthread_create(&th[t], NULL, orc_fps_worker, &tasks[t]) != 0) break;
+            ++started;
+        }
+        if (started != T - 1) {
+            /* cannot run short of threads: the barrier counts T */
+            for (int64_t t = 1; t <= started; ++t) pthread_cancel(th[t]);
+            rc = ORC_NO_MEMORY;
+            break;
+        }
+        tasks[0].sh = &sh;
+        tasks[0].t = 0;
+        orc_fps_worker(&tasks[0]);
+        for (int64_t t = 1; t < T; ++t) pthread_join(th[t], NULL);
+    }
+    pthread_barrier_destroy(&bar);
+    free(m); free(bv); free(bj); free(th); free(tasks);
+    return rc;
 }
 
 /*

@@ -15,7 +15,7 @@ from .binding import (PC_FPS_AUTO, PC_FPS_BLOCK, PC_FPS_CLUSTER, PC_FPS_GRID,
                       pc_gather_points, pc_grid_build, pc_knn, pc_knn_d,
                       pc_knn_grid,
                       pc_set_wait_timeout_ns, pc_set_sm_reserve,
-                      pc_fps_sm_count, pc_three_interpolate,
+                      pc_fps_sm_count, pc_fps_plan, pc_three_interpolate,
                       pc_three_interpolate_backward, three_interpolate,
                       three_nn)
 
@@ -27,5 +27,5 @@ __all__ = [
     "pc_grid_build", "pc_knn_grid", "pc_ball_query_grid", "pc_chamfer",
     "chamfer_distance", "pc_three_interpolate", "pc_three_interpolate_backward",
     "three_interpolate", "three_nn", "pc_gather_points", "pc_knn_d",
-    "pc_set_sm_reserve", "pc_fps_sm_count",
+    "pc_set_sm_reserve", "pc_fps_sm_count", "pc_fps_plan",
 ]

@@ -75,6 +75,10 @@ _SIGNATURES = {
     "pc_debug_set_fps_grid_stall": (None, [ctypes.c_int]),
     "pc_set_sm_reserve": (None, [ctypes.c_int]),
     "pc_fps_sm_count": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
+    "pc_fps_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int,
+                                   ctypes.POINTER(ctypes.c_int),
+                                   ctypes.POINTER(ctypes.c_int)]),
 }
 
 _lib = None
@@ -564,6 +568,16 @@ def pc_set_sm_reserve(sms: int):
 def pc_fps_sm_count(B: int, N: int, npoint: int) -> int:
     """SMs an FPS launch of these sizes occupies on the current device."""
     return int(lib().pc_fps_sm_count(int(B), int(N), int(npoint)))
+
+
+def pc_fps_plan(B: int, N: int, strategy: int = PC_FPS_AUTO, cluster_size: int = 0,
+                blocks_per_cloud: int = 0):
+    """(strategy, blocks per cloud) of the FPS schedule for these sizes."""
+    st, bpc = ctypes.c_int(0), ctypes.c_int(0)
+    _raise_on(lib().pc_fps_plan(int(B), int(N), int(strategy), int(cluster_size),
+                                int(blocks_per_cloud), ctypes.byref(st),
+                                ctypes.byref(bpc)), "pc_fps_plan")
+    return st.value, bpc.value
 
 
 # mps-pointops-style names

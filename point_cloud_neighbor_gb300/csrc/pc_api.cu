@@ -173,6 +173,29 @@ int pc_fps_sm_count(int64_t B, int64_t N, int64_t npoint) {
     return int(std::min<int64_t>(dev->sm_count, B * int64_t(p.blocks_per_cloud)));
 }
 
+int pc_fps_plan(int64_t B, int64_t N, int strategy, int cluster_size,
+                int blocks_per_cloud, int *out_strategy, int *out_blocks_per_cloud) {
+    if (out_strategy == nullptr || out_blocks_per_cloud == nullptr)
+        return pcn::api_fail(PC_ERR_INVALID_ARGUMENT, "fps_plan: null output pointer");
+    *out_strategy = 0;
+    *out_blocks_per_cloud = 0;
+    if (B <= 0 || N <= 0)
+        return pcn::api_fail(PC_ERR_INVALID_ARGUMENT, "fps_plan: need B > 0 and N > 0");
+    const pcn::DeviceInfo *dev = nullptr;
+    const int rc = current_device(&dev);
+    if (rc != PC_OK) return rc;
+    const pcn::FpsPlan p = pcn::plan_fps(*dev, B, N, strategy, cluster_size,
+                                         blocks_per_cloud);
+    if (!p.ok) {
+        char msg[256];
+        std::snprintf(msg, sizeof(msg), "fps_plan: %s", p.why);
+        return pcn::api_fail(PC_ERR_UNSUPPORTED, msg);
+    }
+    *out_strategy = p.strategy;
+    *out_blocks_per_cloud = p.blocks_per_cloud;
+    return PC_OK;
+}
+
 size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
                                  int strategy, int blocks_per_cloud) {
     (void)npoint;

@@ -40,7 +40,8 @@ def very_large():
     """(cloud, the oracle's FPS centre indices, the centres as queries)."""
     cfg = inputs.CONFIGS["very_large"]
     x = inputs.very_large()
-    cidx = oracle.fps(x, cfg["npoint"], 0)[0]
+    # the all-core FPS oracle (pinned equal to the plain one on the CPU)
+    cidx = oracle.fps_all_cores(x, cfg["npoint"], 0, threads=THREADS)[0]
     q = np.ascontiguousarray(x[:, cidx])
     for a in (x, cidx, q):
         a.setflags(write=False)

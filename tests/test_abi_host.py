@@ -143,6 +143,16 @@ def test_sm_reserve_and_fps_sm_count_without_device(L):
     assert L.pc_fps_sm_count(1, 0, 4096) == 0
 
 
+def test_fps_plan_without_device(L):
+    import ctypes
+    st, bpc = ctypes.c_int(7), ctypes.c_int(7)
+    assert L.pc_fps_plan(1, 100000, 0, 0, 0, None, None) == 1
+    assert L.pc_fps_plan(0, 100000, 0, 0, 0, ctypes.byref(st), ctypes.byref(bpc)) == 1
+    assert (st.value, bpc.value) == (0, 0)
+    # sizes are valid, but there is no device to plan for
+    assert L.pc_fps_plan(1, 100000, 0, 0, 0, ctypes.byref(st), ctypes.byref(bpc)) == 5
+
+
 def test_knn_ex_validation(L):
     # k > N is allowed in the ex form (padded); k above 256 is unsupported
     assert L.pc_knn_ex(None, 0, 4, None, 8, 300, None, None, 0, None, None, None) == 2

@@ -433,3 +433,38 @@ def test_ball_query_scan_length(oracle_mod):
             hits = np.nonzero(s < R2)[0]
             want = hits[K - 1] + 1 if len(hits) >= K else 60
             assert got[b * 9 + i] == want
+
+
+# --------------------------------------------------------------------------
+# the all-core FPS (points of each step split over host threads) is the
+# plain FPS: same pins, and equal to it on ties, exhaustion and thread
+# counts above the number of points
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("threads", [1, 2, 3, 8, 33])
+def test_fps_all_cores_equals_plain(oracle_mod, threads):
+    cases = [(inputs.random_cloud(40, 3, 500), 120, 7),
+             (inputs.random_cloud(41, 2, 300, grid=1 / 4), 310, 0),   # ties, exhausted
+             (inputs.tiny(), 64, 0),                                  # duplicates
+             (inputs.random_cloud(42, 1, 5), 9, 2)]                   # N < threads
+    for x, npoint, start in cases:
+        want = oracle_mod.fps(x, npoint, start)
+        got = oracle_mod.fps_all_cores(x, npoint, start, threads=threads)
+        assert np.array_equal(got, want), (x.shape, npoint, start, threads)
+
+
+@pytest.mark.parametrize("L", [3, 5])
+def test_fps_all_cores_uniform_grid_closed_form(oracle_mod, L):
+    n = 2 ** L + 1
+    want = [0, n - 1]
+    for lev in range(1, L + 1):
+        step = (n - 1) >> lev
+        want += [m * step for m in range(1, 2 ** lev, 2)]
+    got = oracle_mod.fps_all_cores(_line(n), n, 0, threads=4)
+    assert got[0].tolist() == want
+
+
+def test_fps_all_cores_matches_brute_force(oracle_mod):
+    x = inputs.random_cloud(1, 2, 24, grid=1 / 4)
+    got = oracle_mod.fps_all_cores(x, 30, 3, threads=5)
+    for b in range(2):
+        assert got[b].tolist() == _fps_from_scratch(x[b], 30, 3)
