@@ -410,11 +410,31 @@ int pc_device_status(void *stream, int reset, int32_t *out_status);
 /*
  * Bound on each device-side wait, in nanoseconds (default 2e9).  Applies to
  * launches enqueued after the call, on every device.  Values below 1000 are
- * raised to 1000.  Testing hook: pc_debug_set_fps_grid_stall(1) makes the
- * next PC_FPS_GRID launches withhold block 0's first exchange, so that every
- * waiting block runs out its bound; 0 restores normal operation.
+ * raised to 1000.
+ *
+ * Testing hooks, so that every bounded wait can be made to run out without
+ * a fault: pc_debug_set_stall(mask) applies to launches enqueued after the
+ * call (0 restores normal operation):
+ *   PC_STALL_FPS_GRID     block 0 of each cloud of a PC_FPS_GRID launch
+ *                         withholds its first exchange word: every block's
+ *                         wait for that step runs out;
+ *   PC_STALL_FPS_CLUSTER  block 0 of the first cloud of a PC_FPS_CLUSTER
+ *                         launch withholds its first candidate: every block
+ *                         of that cluster runs out its wait for that step;
+ *   PC_STALL_TILE_STREAM  the producer warp of the first thread block of a
+ *                         brute-force kNN or Ball Query launch never issues
+ *                         its first tile's copy (nothing is left in flight):
+ *                         the producer and that block's consumers run out
+ *                         their waits.
+ * Each ends as a real timeout does: PC_ERR_DEVICE_TIMEOUT in the status
+ * word, -1 in the outputs the stopped blocks did not finish.
+ * pc_debug_set_fps_grid_stall(e) sets or clears PC_STALL_FPS_GRID alone.
  */
+#define PC_STALL_FPS_GRID 1
+#define PC_STALL_FPS_CLUSTER 2
+#define PC_STALL_TILE_STREAM 4
 void pc_set_wait_timeout_ns(uint64_t ns);
+void pc_debug_set_stall(int mask);
 void pc_debug_set_fps_grid_stall(int enable);
 
 /*

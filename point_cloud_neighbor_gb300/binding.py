@@ -73,6 +73,7 @@ _SIGNATURES = {
                                         ctypes.POINTER(ctypes.c_int32)]),
     "pc_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "pc_debug_set_fps_grid_stall": (None, [ctypes.c_int]),
+    "pc_debug_set_stall": (None, [ctypes.c_int]),
     "pc_set_sm_reserve": (None, [ctypes.c_int]),
     "pc_fps_sm_count": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
     "pc_fps_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
@@ -557,6 +558,15 @@ def pc_set_wait_timeout_ns(ns: int):
 
 def pc_debug_set_fps_grid_stall(enable: bool):
     lib().pc_debug_set_fps_grid_stall(int(bool(enable)))
+
+
+PC_STALL_FPS_GRID, PC_STALL_FPS_CLUSTER, PC_STALL_TILE_STREAM = 1, 2, 4
+
+
+def pc_debug_set_stall(mask: int):
+    """Testing hooks that make a bounded device wait run out (PC_STALL_*
+    flags; 0 restores normal operation)."""
+    lib().pc_debug_set_stall(int(mask))
 
 
 def pc_set_sm_reserve(sms: int):

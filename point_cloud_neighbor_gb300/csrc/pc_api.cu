@@ -24,7 +24,7 @@ constexpr int kVersion = 10000 * 0 + 100 * 1 + 0;  // 0.1.0
 thread_local std::string t_error;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_sm_reserve{0};
-std::atomic<int> g_fps_stall{0};
+std::atomic<int> g_stall{0};  // PC_STALL_* testing flags
 std::mutex g_dev_mutex;
 pcn::DeviceInfo g_devices[kMaxDevices];
 bool g_device_ready[kMaxDevices] = {};
@@ -129,7 +129,7 @@ bool mul_ok(int64_t a, int64_t b, int64_t c) {
 namespace pcn {
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 int sm_reserve() { return g_sm_reserve.load(); }
-int fps_grid_stall() { return g_fps_stall.load(); }
+int debug_stall() { return g_stall.load(); }
 int api_current_device(const DeviceInfo **out) { return current_device(out); }
 int api_check_ptr(const void *p, int dev, size_t align, const char *name) {
     return check_ptr(p, dev, align, name);
@@ -159,7 +159,16 @@ void pc_set_wait_timeout_ns(uint64_t ns) {
     g_timeout_ns.store(ns < 1000 ? 1000 : ns);
 }
 
-void pc_debug_set_fps_grid_stall(int enable) { g_fps_stall.store(enable ? 1 : 0); }
+void pc_debug_set_fps_grid_stall(int enable) {
+    if (enable)
+        g_stall.fetch_or(PC_STALL_FPS_GRID);
+    else
+        g_stall.fetch_and(~PC_STALL_FPS_GRID);
+}
+
+void pc_debug_set_stall(int mask) {
+    g_stall.store(mask & (PC_STALL_FPS_GRID | PC_STALL_FPS_CLUSTER | PC_STALL_TILE_STREAM));
+}
 
 void pc_set_sm_reserve(int sms) { g_sm_reserve.store(sms < 0 ? 0 : sms); }
 

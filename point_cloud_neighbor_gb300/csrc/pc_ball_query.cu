@@ -31,6 +31,7 @@
 //    of a block is full, a stop flag ends the block: the producer stops
 //    issuing tiles (after letting its copies in flight land) and the
 //    consumers leave the tile loop.
+#include "pointcloud.h"
 #include "pc_device.cuh"
 #include "pc_filter.cuh"
 #include "pc_internal.h"
@@ -61,6 +62,7 @@ struct BqArgs {
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
+    int stall;  // PC_STALL_* testing flags
 };
 
 struct __align__(16) BqSlot {
@@ -183,8 +185,10 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     __syncthreads();
 
     if (warp == BQ_CWARPS) {  // producer warp: tiles strictly in input order
+        const bool withhold = (a.stall & PC_STALL_TILE_STREAM) && blockIdx.x == 0 &&
+                              blockIdx.y == 0;
         stream_produce<BQ_SB, false>(ring, cref, Nb, ntiles, [](int it) { return it; },
-                                     fr, s_stop, s_err, a.timeout_ns);
+                                     fr, s_stop, s_err, a.timeout_ns, withhold);
         return;
     }
 
@@ -350,6 +354,7 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
+    a.stall = debug_stall();
 
     // one wave of two blocks per SM, less the SMs other work holds
     const int slots = std::max(1, dev.sm_count - sm_reserve()) * 2;

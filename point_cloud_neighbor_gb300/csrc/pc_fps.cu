@@ -65,7 +65,7 @@ struct FpsArgs {
     uint64_t *slots;
     int *status;
     uint64_t timeout_ns;
-    int stall;
+    int stall;      // PC_STALL_* testing flags
     float negzero;  // -0.0f, see sq2_rn
 };
 
@@ -216,7 +216,9 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
             }
             ClusterSlot *mine = &cslot[par * FPS_MAX_CLUSTER + rank];
             if (CLUSTER) {
-                if (lane < a.nblocks) {
+                // testing hook: block 0 of the first cloud withholds step 1
+                const bool withhold = (a.stall & 2) && b == 0 && rank == 0 && t == 1;
+                if (lane < a.nblocks && !withhold) {
                     const uint32_t ra = map_shared_rank(mine, unsigned(lane));
                     const uint32_t rb = map_shared_rank(&xbar[par], unsigned(lane));
                     st_async_v4(ra, bhi, bj, __float_as_uint(wx),
@@ -233,11 +235,13 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
         }
         if (CLUSTER) {
             const unsigned ph = unsigned((t - 1) >> 1) & 1u;
-            if (!mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns))
-                *s_fail = 1;
+            const bool got = mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns);
+            if (!got) *s_fail = 1;
             // re-arm this parity's barrier for step t + 2 (its next phase
-            // cannot complete before every block has passed this point)
-            if (threadIdx.x == 0) mbar_arrive_expect_tx(&xbar[par], xbytes);
+            // cannot complete before every block has passed this point);
+            // only after seeing this phase complete: a phase that ran out
+            // still holds its arrival, and the kernel stops anyway
+            if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&xbar[par], xbytes);
             if (__syncthreads_or(*s_fail)) {
                 raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
                 if (rank == 0)
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
                             wslot, bhi, bj);
         if (warp == 0) {
             uint64_t *ps = slots + size_t(par) * a.nblocks;
-            if (lane == 0 && !(a.stall && r == 0 && t == 1)) {
+            if (lane == 0 && !((a.stall & 1) && r == 0 && t == 1)) {
                 const uint64_t key =
                     (uint64_t(bhi) << 33) |
                     (uint64_t((FPS_GRID_MAX_N - 1) - (bhi ? bj : 0u)) << 9) |
@@ -599,7 +603,7 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
     a.slots = static_cast<uint64_t *>(workspace);
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
-    a.stall = plan.strategy == 3 ? fps_grid_stall() : 0;
+    a.stall = debug_stall();
     a.negzero = -0.0f;
 
     const void *fn = fps_kernel_ptr(plan.strategy, plan.ppt);

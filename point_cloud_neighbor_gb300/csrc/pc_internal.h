@@ -26,8 +26,8 @@ struct DeviceInfo {
 uint64_t wait_timeout_ns();
 // SMs taken by concurrent work (see pc_set_sm_reserve).
 int sm_reserve();
-// Testing hook for the FPS grid exchange (see pc_debug_set_fps_grid_stall).
-int fps_grid_stall();
+// Testing hooks: the PC_STALL_* flags set by pc_debug_set_stall.
+int debug_stall();
 
 // Device resolution, pointer checks and error messages of the C ABI, for
 // entry points defined outside pc_api.cu.

@@ -39,6 +39,7 @@
 //    with the tile count) so that spatially sorted inputs do not feed each
 //    query a stream of ever-closer candidates (the project page's kNN kernel
 //    notes report a 6-8x slowdown from storage order on sorted input).
+#include "pointcloud.h"
 #include "pc_device.cuh"
 #include "pc_filter.cuh"
 #include "pc_internal.h"
@@ -71,6 +72,7 @@ struct KnnArgs {
     int64_t *out_idx;
     int *status;
     uint64_t timeout_ns;
+    int stall;  // PC_STALL_* testing flags
     // spatial order (lane kernel, ORDERED): per cloud the valid references
     // and queries as 16-byte points (x, y, z, original index bits) sorted by
     // cell code, the starts of the reference cells and the cell frame
@@ -336,12 +338,13 @@ __global__ void __launch_bounds__(KNN_THREADS, 2) knn_kernel(const KnnArgs a) {
 
     if (warp == KNN_CWARPS) {  // producer warp
         __syncthreads();
+        const bool withhold = (a.stall & PC_STALL_TILE_STREAM) && blockIdx.x == 0 &&
+                              blockIdx.y == 0;
         if (lane == 0)
             ring_produce<KNN_STAGES>(
                 ring, cref, Nb, KNN_T, ntiles,
                 [&](int it) { return knn_tile_at(it, tstride, ntiles); }, s_err,
-                s_err,
-                a.timeout_ns);
+                s_err, a.timeout_ns, withhold);
         return;
     }
 
@@ -521,6 +524,9 @@ __device__ __forceinline__ int key_j(unsigned long long key) {
     return static_cast<int>(static_cast<unsigned>(key));
 }
 constexpr unsigned long long KEY_EMPTY = 0x7f8000007fffffffull;
+// A part that stopped on a device timeout marks its rows with this key (above
+// every real or empty key); the merge then writes the row as -1.
+constexpr unsigned long long KEY_FAILED = ~0ull;
 
 // Sift `key` down from `pos` in the max-heap h of n keys (stride 32);
 // returns the key then at `pos`.
@@ -792,8 +798,10 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
     };
 
     if (warp == nwarps) {  // producer warp
+        const bool withhold = (a.stall & PC_STALL_TILE_STREAM) && blockIdx.x == 0 &&
+                              blockIdx.y == 0 && blockIdx.z == 0;
         stream_produce<KL_SB, ORDERED>(ring, cref, Nb, nsteps_part, tile_at, fr, s_err,
-                                       s_err, a.timeout_ns);
+                                       s_err, a.timeout_ns, withhold);
         return;
     }
 
@@ -958,7 +966,7 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
             if (ORDERED && nparts > 1) {
                 unsigned long long *pk =
                     a.part_keys + ((size_t(part) * gridDim.y + b) * a.Q + orow) * k;
-                for (int e = 0; e < k; ++e) pk[e] = KEY_EMPTY;
+                for (int e = 0; e < k; ++e) pk[e] = KEY_FAILED;
             } else {
                 for (int e = 0; e < k; ++e) a.out_idx[row * k + e] = -1;
             }
@@ -1001,6 +1009,14 @@ __global__ void __launch_bounds__(256) knn_merge_parts_kernel(const KnnArgs a, i
     int ptr[8];
     for (int p = 0; p < nparts; ++p) ptr[p] = 0;
     const size_t row = size_t(b) * a.Q + r;
+    for (int p = 0; p < nparts; ++p)
+        if (pk[p * stride] == KEY_FAILED) {  // a part stopped: unfinished row
+            for (int e = 0; e < k; ++e) {
+                a.out_idx[row * k + e] = -1;
+                a.out_dist[row * k + e] = 0.0f;
+            }
+            return;
+        }
     for (int e = 0; e < k; ++e) {
         unsigned long long best = KEY_EMPTY;
         int bp = -1;
@@ -1343,6 +1359,7 @@ KnnArgs make_knn_args(const DeviceInfo &dev, const float *query, int64_t Q,
     a.out_idx = out_idx;
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
+    a.stall = debug_stall();
     return a;
 }
 

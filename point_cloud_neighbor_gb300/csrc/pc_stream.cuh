@@ -129,7 +129,8 @@ __device__ __forceinline__ WaitResult warp_wait(uint64_t *bar, unsigned parity,
 // whose index goes to the fourth component of the raw copy (0 otherwise).
 // Stops when *stop becomes non-zero; a timeout raises *err.  Before
 // returning it waits (bounded) for every raw copy it issued, so none is in
-// flight when the block exits.
+// flight when the block exits.  withhold_first (a testing hook) skips the
+// first tile's copy altogether: its wait, and the consumers', run out.
 template <int SB, bool F4, class TileAt>
 __device__ __forceinline__ void stream_produce(const StreamRing &ring,
                                                const float *cref, int N,
@@ -137,7 +138,8 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
                                                FilterFrame fr,
                                                volatile int *stop,
                                                volatile int *err,
-                                               uint64_t timeout_ns) {
+                                               uint64_t timeout_ns,
+                                               bool withhold_first = false) {
     const int lane = static_cast<int>(lane_id());
     const float inf = __int_as_float(0x7f800000);
     int issued = 0, landed = 0;
@@ -152,7 +154,8 @@ __device__ __forceinline__ void stream_produce(const StreamRing &ring,
                        &ring.raw_full[slot]);
     };
     if (lane == 0)
-        for (; issued < ntiles && issued < ST_RAW_STAGES; ++issued) issue(issued, issued);
+        for (; issued < ntiles && issued < ST_RAW_STAGES; ++issued)
+            if (!(withhold_first && issued == 0)) issue(issued, issued);
     issued = __shfl_sync(0xffffffffu, issued, 0);
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % ST_STAGES, rs = it % ST_RAW_STAGES;

@@ -106,14 +106,16 @@ __device__ __forceinline__ WaitResult mbar_wait_or_stop(uint64_t *bar,
 // points [tile_at(it) * T, ...) of the cloud starting at `cref`.  Stops early
 // when `*stop` becomes non-zero; on a timeout it raises *err.  Before
 // returning it waits (bounded) until every copy it issued has landed, so no
-// copy is in flight when the block exits.
+// copy is in flight when the block exits.  withhold_first (a testing hook)
+// skips the first tile's copy altogether: the waits for it run out.
 template <int STAGES, class TileAt>
 __device__ __forceinline__ void ring_produce(const TileRing &ring,
                                              const float *cref, int N, int T,
                                              int ntiles, TileAt tile_at,
                                              volatile int *stop,
                                              volatile int *err,
-                                             uint64_t timeout_ns) {
+                                             uint64_t timeout_ns,
+                                             bool withhold_first = false) {
     int issued = 0;
     for (int it = 0; it < ntiles; ++it) {
         const int st = it % STAGES;
@@ -126,8 +128,9 @@ __device__ __forceinline__ void ring_produce(const TileRing &ring,
         }
         if (*stop || *err) break;
         const int j0 = tile_at(it) * T;
-        issue_tile(ring.buf(st), cref + size_t(j0) * 3, min(T, N - j0),
-                   &ring.full[st]);
+        if (!(withhold_first && it == 0))
+            issue_tile(ring.buf(st), cref + size_t(j0) * 3, min(T, N - j0),
+                       &ring.full[st]);
         issued = it + 1;
     }
     for (int st = 0; st < STAGES; ++st) {

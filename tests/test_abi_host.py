@@ -130,6 +130,8 @@ def test_wait_timeout_setter_accepts_any_value(L):
     L.pc_set_wait_timeout_ns(0)
     L.pc_set_wait_timeout_ns(2_000_000_000)
     L.pc_debug_set_fps_grid_stall(0)
+    for mask in (1, 2, 4, 7, 0):
+        L.pc_debug_set_stall(mask)
 
 
 def test_sm_reserve_and_fps_sm_count_without_device(L):

@@ -535,6 +535,78 @@ def test_fps_grid_wait_timeout_is_reported():
     assert_idx_equal(idx, oracle.fps(x, 20, 0), "fps after timeout")
 
 
+def _rows_stopped_or_exact(i, wi, what):
+    """Every row is either the oracle's or all -1 (a block that stopped);
+    returns the number of stopped rows."""
+    i = np.asarray(i).reshape(wi.shape)
+    stopped = (i == -1).all(axis=1)
+    bad = int((~stopped & (i != wi).any(axis=1)).sum())
+    assert bad == 0, f"{what}: {bad} rows neither stopped nor the oracle's"
+    return int(stopped.sum())
+
+
+@pytest.mark.parametrize("case", ["lane", "ordered", "warp_list", "ball_query"])
+def test_tile_stream_wait_timeout_is_reported(case):
+    """The producer of the first thread block never issues its first tile's
+    copy (nothing is left in flight): its wait and its consumers' run out,
+    the kernel returns, the status word says so, the stopped block's rows are
+    -1, every other row is the oracle's, and the next call is correct."""
+    if case == "ordered":        # spatially ordered kNN: many blocks
+        x = cache.large(False)[:, :20000].copy()
+        q, k = x, 16
+    else:                        # one thread block
+        x = inputs.random_cloud(30, 1, 3000)
+        q = inputs.random_cloud(31, 1, 8 if case in ("warp_list", "ball_query") else 64)
+        k = 40 if case == "warp_list" else 8
+    pc.pc_set_wait_timeout_ns(2_000_000)       # 2 ms
+    pc.pc_debug_set_stall(pc.PC_STALL_TILE_STREAM)
+    try:
+        if case == "ball_query":
+            _, got = pc.pc_ball_query(to_dev(q), to_dev(x), 0.5, 16)
+        else:
+            _, got = pc.pc_knn(to_dev(q), to_dev(x), k)
+        got = got.cpu().numpy()
+    finally:
+        pc.pc_debug_set_stall(0)
+        pc.pc_set_wait_timeout_ns(2_000_000_000)
+    assert pc.pc_device_status(reset=True) == 4
+    if case == "ball_query":
+        _, wi = oracle.ball_query(q, x, 0.5, 16)
+    else:
+        _, wi = oracle.knn(q, x, k, threads=THREADS)
+    stopped = _rows_stopped_or_exact(got, wi, case)
+    assert stopped >= 1
+    if case != "ordered":
+        assert stopped == wi.shape[0]          # the only block stopped
+    # the context is still usable and the next call is correct
+    if case == "ball_query":
+        check_bq(q, x, 0.5, 16, what="bq after timeout")
+    else:
+        check_knn(q, x, k, what=f"{case} knn after timeout")
+
+
+def test_fps_cluster_wait_timeout_is_reported():
+    """Block 0 of the first cloud's cluster withholds its first candidate:
+    every block of that cluster runs out its wait, the cloud's remaining
+    slots are -1, the other cloud is unaffected, and the next call is
+    correct."""
+    x = inputs.random_cloud(32, 2, 8000)
+    pc.pc_set_wait_timeout_ns(2_000_000)       # 2 ms
+    pc.pc_debug_set_stall(pc.PC_STALL_FPS_CLUSTER)
+    try:
+        idx = pc.pc_fps(to_dev(x), 20, 0, strategy=pc.PC_FPS_CLUSTER,
+                        cluster_size=4).cpu().numpy()
+    finally:
+        pc.pc_debug_set_stall(0)
+        pc.pc_set_wait_timeout_ns(2_000_000_000)
+    assert pc.pc_device_status(reset=True) == 4
+    want = oracle.fps(x, 20, 0)
+    assert idx[0, 0] == 0 and (idx[0, 1:] == -1).all()
+    assert_idx_equal(idx[1], want[1], "fps cluster, the cloud that did not stall")
+    idx = gpu_fps(x, 20, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=4)
+    assert_idx_equal(idx, want, "fps cluster after timeout")
+
+
 def test_concurrent_streams_equal_serial():
     """FPS, kNN and Ball Query issued on three streams at once (the benchmark
     step) give exactly the results of the same calls one after another."""
