@@ -747,7 +747,7 @@ def _fps_bounds(pc, x_shape, npoint, ms, device, flush, stream, max_mhz, steps):
     import torch
     from point_cloud_neighbor_gb300 import inputs
     B, N = int(x_shape[0]), int(x_shape[1])
-    strategy, bpc = pc.pc_fps_plan(B, N)
+    strategy, cs, bpc = pc.pc_fps_plan(B, N)
     sms = pc.pc_fps_sm_count(B, N, npoint)
     alu_ms = (float(B) * N * (npoint - 1) * FPS_INSTR_PER_POINT_STEP /
               (max(sms, 1) * 128 * max_mhz * 1e6) * 1e3)
@@ -758,6 +758,7 @@ def _fps_bounds(pc, x_shape, npoint, ms, device, flush, stream, max_mhz, steps):
         kw["cluster_size"] = bpc
     elif strategy == pc.PC_FPS_GRID:
         kw["blocks_per_cloud"] = bpc
+        kw["cluster_size"] = cs
     try:
         floor_ms = _timed(lambda: pc.pc_fps(fx, npoint, 0, **kw), steps, 3, flush, stream)
     except pc.PointCloudError as err:
@@ -768,7 +769,8 @@ def _fps_bounds(pc, x_shape, npoint, ms, device, flush, stream, max_mhz, steps):
                 f"(1024 per block), npoint={npoint}")
     names = {pc.PC_FPS_BLOCK: "block", pc.PC_FPS_CLUSTER: "cluster",
              pc.PC_FPS_GRID: "grid"}
-    out = {"schedule": names.get(strategy, str(strategy)), "blocks_per_cloud": bpc,
+    out = {"schedule": names.get(strategy, str(strategy)), "cluster_size": cs,
+           "blocks_per_cloud": bpc,
            "sms": sms, "ms": ms, "us_per_step": ms * 1e3 / max(npoint - 1, 1),
            "alu_bound_ms": alu_ms, "alu_frac": alu_ms / ms,
            "floor_ms": floor_ms, "floor_frac": (floor_ms / ms) if floor_ms else None,

@@ -86,11 +86,16 @@ int pc_version(void);
  *
  * Schedules (chosen from B and N): one thread block per cloud, one thread
  * block cluster per cloud (distributed shared memory), or -- for clouds too
- * large for one cluster -- a cooperative grid per cloud that exchanges one
- * 64-bit key per block and step through the workspace.  Only the grid
- * schedule uses scratch and bounded device-side waits; if a wait runs out the
- * kernel stops, writes -1 into the remaining out_idx slots of that cloud
- * and raises the device status word (PC_ERR_DEVICE_TIMEOUT).
+ * large for one cluster -- a cooperative grid of clusters per cloud: the
+ * blocks of each cluster exchange through distributed shared memory and each
+ * cluster's first block publishes the cluster's best candidate (a tagged key
+ * and the point's coordinates, four 64-bit words) per step through the
+ * workspace and sends the winner back to its cluster (with
+ * cluster_size 1 in pc_fps_ex, one level: one 64-bit key per block and
+ * step).  Only the grid schedule uses scratch; the cluster and grid
+ * schedules bound their device-side waits: if a wait runs out the kernel
+ * stops, writes -1 into the remaining out_idx slots of that cloud and raises
+ * the device status word (PC_ERR_DEVICE_TIMEOUT).
  *
  * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_UNSUPPORTED (cloud too large
  * for the on-chip schedules), PC_ERR_CUDA or PC_ERR_NO_DEVICE.
@@ -111,9 +116,11 @@ typedef enum pc_fps_strategy {
 } pc_fps_strategy;
 
 /* pc_fps with an explicit schedule (results are identical for every
- * schedule).  `cluster_size` (1..16, 0 = automatic) applies to
- * PC_FPS_CLUSTER; `blocks_per_cloud` (0 = automatic) to PC_FPS_GRID.  The
- * workspace size for PC_FPS_GRID is pc_fps_workspace_bytes_ex. */
+ * schedule).  `cluster_size` (0 = automatic) is the cluster of
+ * PC_FPS_CLUSTER (1..16) or the cluster of the two-level PC_FPS_GRID (1 = one
+ * level, 2..16; blocks_per_cloud must then be a multiple of it);
+ * `blocks_per_cloud` (0 = automatic) applies to PC_FPS_GRID.  The workspace
+ * size for PC_FPS_GRID with cluster_size 0 is pc_fps_workspace_bytes_ex. */
 int pc_fps_ex(const float *xyz, int64_t B, int64_t N, int64_t npoint,
               int64_t start_idx, int64_t *out_idx, void *workspace,
               size_t workspace_bytes, int strategy, int cluster_size,
@@ -123,13 +130,14 @@ size_t pc_fps_workspace_bytes_ex(int64_t B, int64_t N, int64_t npoint,
                                  int strategy, int blocks_per_cloud);
 
 /* The schedule pc_fps_ex would run for these sizes and arguments on the
- * current device: *out_strategy (PC_FPS_BLOCK, _CLUSTER or _GRID) and
- * *out_blocks_per_cloud (the cluster size, or the grid's blocks per cloud;
- * 1 for PC_FPS_BLOCK).  Nothing is enqueued.  Returns PC_OK,
- * PC_ERR_INVALID_ARGUMENT (B or N < 1, null outputs), PC_ERR_UNSUPPORTED (no
- * schedule fits) or PC_ERR_NO_DEVICE. */
+ * current device: *out_strategy (PC_FPS_BLOCK, _CLUSTER or _GRID),
+ * *out_cluster_size (blocks per thread block cluster; 1 for PC_FPS_BLOCK and
+ * for the one-level grid) and *out_blocks_per_cloud.  Nothing is enqueued.
+ * Returns PC_OK, PC_ERR_INVALID_ARGUMENT (B or N < 1, null outputs),
+ * PC_ERR_UNSUPPORTED (no schedule fits) or PC_ERR_NO_DEVICE. */
 int pc_fps_plan(int64_t B, int64_t N, int strategy, int cluster_size,
-                int blocks_per_cloud, int *out_strategy, int *out_blocks_per_cloud);
+                int blocks_per_cloud, int *out_strategy, int *out_cluster_size,
+                int *out_blocks_per_cloud);
 
 /*
  * pc_fps_grid_static: pc_fps with the PC_FPS_GRID schedule for callers that
@@ -141,10 +149,13 @@ int pc_fps_plan(int64_t B, int64_t N, int strategy, int cluster_size,
  * The grid schedule's exchange scratch is a fixed array of 4096 64-bit words
  * (32 KiB) inside the library, present on every device that loads the
  * library until the process exits; the call allocates nothing.  Limit: the
- * schedule needs 2 * blocks_per_cloud * B words, so B * blocks_per_cloud
- * must not exceed 2048 (it is also bounded by the SM count); larger requests
- * return PC_ERR_INVALID_ARGUMENT.  Arguments and results are those of
- * pc_fps_ex with strategy PC_FPS_GRID (blocks_per_cloud 0 = automatic).
+ * schedule needs B * max(2 * blocks_per_cloud, 32 * clusters per cloud)
+ * words (one 128-byte line per cluster and step parity with two levels; 2
+ * words per block with one level, when blocks_per_cloud is not a multiple
+ * of 4), at most 4096 in all, and the blocks are bounded by the SM count;
+ * larger requests return PC_ERR_INVALID_ARGUMENT.  Arguments and results are
+ * those of pc_fps_ex with strategy PC_FPS_GRID and cluster_size 0
+ * (blocks_per_cloud 0 = automatic).
  *
  * The first call on a device (while it is current) looks up the array's
  * device address with cudaGetSymbolAddress; make that first call before any

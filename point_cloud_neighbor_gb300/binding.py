@@ -79,6 +79,7 @@ _SIGNATURES = {
     "pc_fps_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(ctypes.c_int),
+                                   ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int)]),
 }
 
@@ -156,7 +157,8 @@ def pc_fps(xyz: torch.Tensor, npoint: int, start_idx: int = 0, *,
         if out is None:
             out = torch.empty((B, npoint), dtype=torch.int64, device=xyz.device)
         ws_ptr, ws_bytes = None, 0
-        if B > 0 and N > 0:
+        if B > 0 and N > 0 and cluster_size == 0:
+            # (an explicit cluster size: the library sizes the scratch)
             need = L.pc_fps_workspace_bytes_ex(B, N, npoint, strategy,
                                                blocks_per_cloud)
             if need:
@@ -582,12 +584,13 @@ def pc_fps_sm_count(B: int, N: int, npoint: int) -> int:
 
 def pc_fps_plan(B: int, N: int, strategy: int = PC_FPS_AUTO, cluster_size: int = 0,
                 blocks_per_cloud: int = 0):
-    """(strategy, blocks per cloud) of the FPS schedule for these sizes."""
-    st, bpc = ctypes.c_int(0), ctypes.c_int(0)
+    """(strategy, cluster size, blocks per cloud) of the FPS schedule for
+    these sizes on the current device."""
+    st, cs, bpc = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     _raise_on(lib().pc_fps_plan(int(B), int(N), int(strategy), int(cluster_size),
                                 int(blocks_per_cloud), ctypes.byref(st),
-                                ctypes.byref(bpc)), "pc_fps_plan")
-    return st.value, bpc.value
+                                ctypes.byref(cs), ctypes.byref(bpc)), "pc_fps_plan")
+    return st.value, cs.value, bpc.value
 
 
 # mps-pointops-style names

@@ -183,10 +183,13 @@ int pc_fps_sm_count(int64_t B, int64_t N, int64_t npoint) {
 }
 
 int pc_fps_plan(int64_t B, int64_t N, int strategy, int cluster_size,
-                int blocks_per_cloud, int *out_strategy, int *out_blocks_per_cloud) {
-    if (out_strategy == nullptr || out_blocks_per_cloud == nullptr)
+                int blocks_per_cloud, int *out_strategy, int *out_cluster_size,
+                int *out_blocks_per_cloud) {
+    if (out_strategy == nullptr || out_cluster_size == nullptr ||
+        out_blocks_per_cloud == nullptr)
         return pcn::api_fail(PC_ERR_INVALID_ARGUMENT, "fps_plan: null output pointer");
     *out_strategy = 0;
+    *out_cluster_size = 0;
     *out_blocks_per_cloud = 0;
     if (B <= 0 || N <= 0)
         return pcn::api_fail(PC_ERR_INVALID_ARGUMENT, "fps_plan: need B > 0 and N > 0");
@@ -201,6 +204,7 @@ int pc_fps_plan(int64_t B, int64_t N, int strategy, int cluster_size,
         return pcn::api_fail(PC_ERR_UNSUPPORTED, msg);
     }
     *out_strategy = p.strategy;
+    *out_cluster_size = p.cluster;
     *out_blocks_per_cloud = p.blocks_per_cloud;
     return PC_OK;
 }

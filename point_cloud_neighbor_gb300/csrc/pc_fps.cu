@@ -49,6 +49,7 @@ constexpr unsigned FULL = 0xffffffffu;
 constexpr int FPS_MAX_CLUSTER = 16;
 constexpr int FPS_GRID_MAX_N = 1 << 24;  // index field of the exchange word
 constexpr int FPS_CAND_BYTES = 20;       // key, index, x, y, z sent per block
+constexpr int CG_SLOT_WORDS = 16;        // a cluster's four words, one 128-byte line
 
 // Threads per block a kernel with PPT points per thread may use: the points'
 // registers (4 per point) must fit next to the working set.
@@ -62,6 +63,8 @@ struct FpsArgs {
     int64_t *out;
     int chunk;     // points per block
     int nblocks;   // blocks per cloud (cluster size or grid blocks per cloud)
+    int cs;        // two-level GRID: blocks per cluster
+    int ncl;       // two-level GRID: clusters per cloud
     uint64_t *slots;
     int *status;
     uint64_t timeout_ns;
@@ -373,6 +376,223 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
     }
 }
 
+// GRID schedule in two levels: a cooperative launch of thread block
+// clusters of a.cs blocks, a.ncl clusters (a.nblocks = a.cs * a.ncl blocks)
+// per cloud.  Per step:
+//   1. the blocks of a cluster exchange their candidates (key, coordinates)
+//      through distributed shared memory exactly as the CLUSTER schedule
+//      does, and every block reduces them to the cluster's best;
+//   2. block 0 of each cluster (its leader) publishes that best into the
+//      cluster's slot of the workspace -- four 64-bit words on a 128-byte
+//      line of their own, each carrying the step's tag in its low 9 bits:
+//          key  [bits(m)+1 : 31 | 2^24-1-j : 24 | step mod 512 : 9]
+//          x, y, z  [float bits : 32 | 0 : 23 | step mod 512 : 9]
+//      -- and polls the cloud's a.ncl slots until every word carries this
+//      step's tag (each word is checked on its own, so the stores need no
+//      ordering, and the winner's coordinates arrive with its key);
+//   3. the leader sends the winner to every block of its cluster through
+//      distributed shared memory (st.async on a second mbarrier pair).
+// Only the a.ncl leaders touch the workspace, so a step's global exchange is
+// a.ncl writers and a.ncl readers of a.ncl lines.  Double buffering by step
+// parity holds at every level: a block sends step t + 2 only after its
+// leader read every cluster's step t + 1, which each cluster publishes only
+// after all its blocks finished step t.  Every wait is bounded.
+template <int PPT>
+__global__ void __launch_bounds__(fps_max_threads(PPT), 1)
+    fps_cgrid_kernel(const FpsArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float *scoord = reinterpret_cast<float *>(smem);
+    uint2 *wslot = reinterpret_cast<uint2 *>(smem + fps_coords_bytes(a.chunk));
+    ClusterSlot *cslot = reinterpret_cast<ClusterSlot *>(
+        smem + fps_coords_bytes(a.chunk) + 32 * sizeof(uint2));
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(cslot + 2 * FPS_MAX_CLUSTER);
+    int *s_fail = reinterpret_cast<int *>(xbar + 2);
+    uint64_t *bbar = xbar + 4;                                   // [2]
+    ClusterSlot *bslot = reinterpret_cast<ClusterSlot *>(xbar + 6);  // [2]
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int T = blockDim.x;
+    const unsigned rank = cluster_ctarank();
+    const int b = blockIdx.x / a.nblocks;
+    const int r = blockIdx.x % a.nblocks;  // block of the cloud
+    const int cl = r / a.cs;               // cluster of the cloud
+    const float *x = a.xyz + size_t(b) * size_t(a.N) * 3;
+    const int lo = r * a.chunk;
+    const int hi = min(a.N, lo + a.chunk);
+    // slot i of parity p: words [(p * ncl + i) * CG_SLOT_WORDS, + 4)
+    uint64_t *slots = a.slots + size_t(b) * 2 * a.ncl * CG_SLOT_WORDS;
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
+    const unsigned xbytes = unsigned(FPS_CAND_BYTES * a.cs);
+
+    ThreadPoints<PPT> pt;
+    fps_load_points<PPT>(x, lo, hi, T, pt, scoord);
+    float cx = x[size_t(a.start) * 3 + 0];
+    float cy = x[size_t(a.start) * 3 + 1];
+    float cz = x[size_t(a.start) * 3 + 2];
+    int64_t *out = a.out + size_t(b) * a.npoint;
+    if (r == 0 && threadIdx.x == 0) out[0] = a.start;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&xbar[i], 1);
+            mbar_init(&bbar[i], 1);
+        }
+        *s_fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int i = 0; i < 2; ++i) {
+            mbar_arrive_expect_tx(&xbar[i], xbytes);
+            mbar_arrive_expect_tx(&bbar[i], FPS_CAND_BYTES);
+        }
+    }
+    __syncthreads();
+    cluster_sync_all();  // every block's barriers exist before use
+
+    bool failed = false;
+    int t = 1;
+    for (; t < a.npoint; ++t) {
+        const int par = t & 1;
+        const unsigned tag = unsigned(t) & 511u;
+        const unsigned ph = unsigned((t - 1) >> 1) & 1u;
+        unsigned bhi, bj;
+        fps_local_step<PPT>(pt, cx, cy, cz, nz0, lo + int(threadIdx.x), T,
+                            wslot, bhi, bj);
+        // 1. the block's candidate to every block of the cluster
+        if (warp == 0) {
+            float wx = 0.f, wy = 0.f, wz = 0.f;
+            if (bhi) {
+                const float *c = scoord + (int(bj) - lo) * 3;
+                wx = c[0];
+                wy = c[1];
+                wz = c[2];
+            }
+            ClusterSlot *mine = &cslot[par * FPS_MAX_CLUSTER + rank];
+            if (lane < a.cs) {
+                const uint32_t ra = map_shared_rank(mine, unsigned(lane));
+                const uint32_t rb = map_shared_rank(&xbar[par], unsigned(lane));
+                st_async_v4(ra, bhi, bj, __float_as_uint(wx), __float_as_uint(wy), rb);
+                st_async_b32(ra + 16, __float_as_uint(wz), rb);
+            }
+        }
+        if (rank == 0) {  // the leader: steps 1 to 3
+            const bool got = mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns);
+            if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&xbar[par], xbytes);
+            if (__syncthreads_or(!got)) {
+                if (threadIdx.x == 0) raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
+                failed = true;
+                break;
+            }
+            if (warp == 0) {
+                const ClusterSlot *cs = &cslot[par * FPS_MAX_CLUSTER];
+                unsigned vhi = 0u, vj = FULL;
+                float vx = 0.f, vy = 0.f, vz = 0.f;
+                if (lane < a.cs) {
+                    vhi = cs[lane].hi;
+                    vj = cs[lane].j;
+                    vx = cs[lane].x;
+                    vy = cs[lane].y;
+                    vz = cs[lane].z;
+                }
+                unsigned chi, cj;
+                warp_argmax_hi_min_lo(vhi, vj, chi, cj);
+                const int who = __ffs(__ballot_sync(FULL, vhi == chi && vj == cj)) - 1;
+                const float kx = __shfl_sync(FULL, vx, who);
+                const float ky = __shfl_sync(FULL, vy, who);
+                const float kz = __shfl_sync(FULL, vz, who);
+                uint64_t *gs = slots + size_t(par) * a.ncl * CG_SLOT_WORDS;
+                // testing hook: cluster 0 of the first cloud withholds step 1
+                const bool withhold = (a.stall & 1) && b == 0 && cl == 0 && t == 1;
+                if (lane == 0 && !withhold) {
+                    uint64_t *w = gs + size_t(cl) * CG_SLOT_WORDS;
+                    st_relaxed_gpu_u64(w + 1, (uint64_t(__float_as_uint(kx)) << 32) | tag);
+                    st_relaxed_gpu_u64(w + 2, (uint64_t(__float_as_uint(ky)) << 32) | tag);
+                    st_relaxed_gpu_u64(w + 3, (uint64_t(__float_as_uint(kz)) << 32) | tag);
+                    st_relaxed_gpu_u64(
+                        w, (uint64_t(chi) << 33) |
+                               (uint64_t((FPS_GRID_MAX_N - 1) - (chi ? cj : 0u)) << 9) | tag);
+                }
+                uint64_t mk = 0;
+                float mx = 0.f, my = 0.f, mz = 0.f;
+                bool ok = false;
+                const uint64_t t0 = global_timer_ns();
+                for (int spin = 0;; ++spin) {
+                    bool mine_ok = true;
+                    mk = 0;
+                    for (int i = lane; i < a.ncl; i += 32) {
+                        const uint64_t *w = gs + size_t(i) * CG_SLOT_WORDS;
+                        const uint64_t w0 = ld_relaxed_gpu_u64(w);
+                        const uint64_t w1 = ld_relaxed_gpu_u64(w + 1);
+                        const uint64_t w2 = ld_relaxed_gpu_u64(w + 2);
+                        const uint64_t w3 = ld_relaxed_gpu_u64(w + 3);
+                        if ((w0 & 511u) != tag || (w1 & 511u) != tag ||
+                            (w2 & 511u) != tag || (w3 & 511u) != tag) {
+                            mine_ok = false;
+                        } else if (w0 > mk) {
+                            mk = w0;
+                            mx = __uint_as_float(unsigned(w1 >> 32));
+                            my = __uint_as_float(unsigned(w2 >> 32));
+                            mz = __uint_as_float(unsigned(w3 >> 32));
+                        }
+                    }
+                    if (__all_sync(FULL, mine_ok)) {
+                        ok = true;
+                        break;
+                    }
+                    if ((spin & 63) == 63 && global_timer_ns() - t0 > a.timeout_ns) break;
+                }
+                if (ok) {
+                    // the largest key, and the coordinates that came with it
+                    const unsigned mhi = __reduce_max_sync(FULL, unsigned(mk >> 32));
+                    const unsigned lo32 = __reduce_max_sync(
+                        FULL, unsigned(mk >> 32) == mhi ? unsigned(mk) : 0u);
+                    const int wl = __ffs(__ballot_sync(FULL, unsigned(mk >> 32) == mhi &&
+                                                                 unsigned(mk) == lo32)) - 1;
+                    const float fx = __shfl_sync(FULL, mx, wl);
+                    const float fy = __shfl_sync(FULL, my, wl);
+                    const float fz = __shfl_sync(FULL, mz, wl);
+                    const uint64_t wk = (uint64_t(mhi) << 32) | lo32;
+                    const unsigned wj =
+                        (FPS_GRID_MAX_N - 1) - unsigned((wk >> 9) & 0xffffffu);
+                    // 3. the winner to every block of the cluster
+                    if (lane < a.cs) {
+                        const uint32_t ra = map_shared_rank(&bslot[par], unsigned(lane));
+                        const uint32_t rb = map_shared_rank(&bbar[par], unsigned(lane));
+                        st_async_v4(ra, mhi, wj, __float_as_uint(fx), __float_as_uint(fy),
+                                    rb);
+                        st_async_b32(ra + 16, __float_as_uint(fz), rb);
+                    }
+                    if (lane == 0 && r == 0) out[t] = int64_t(wj);
+                } else if (lane == 0) {
+                    raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
+                }
+            }
+        } else {
+            // the other blocks only take part in step 1: re-arm its barrier
+            // once its phase is seen complete
+            const bool got = mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns);
+            if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&xbar[par], xbytes);
+            if (__syncthreads_or(!got)) {
+                if (threadIdx.x == 0) raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
+                failed = true;
+                break;
+            }
+        }
+        // every block: the winner from the leader
+        const bool got = mbar_wait_cluster_bounded(&bbar[par], ph, a.timeout_ns);
+        if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&bbar[par], FPS_CAND_BYTES);
+        if (__syncthreads_or(!got)) {
+            if (threadIdx.x == 0) raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
+            failed = true;
+            break;
+        }
+        const ClusterSlot w = bslot[par];
+        cx = w.x;
+        cy = w.y;
+        cz = w.z;
+    }
+    if (failed && r == 0)
+        for (int i = t + int(threadIdx.x); i < a.npoint; i += T) out[i] = -1;
+    cluster_sync_all();  // no block exits while peers may write
+}
+
 template <int PPT>
 const void *cluster_kernel_ptr(bool cluster) {
     return cluster ? reinterpret_cast<const void *>(&fps_cluster_kernel<PPT, true>)
@@ -441,11 +661,10 @@ int64_t block_capacity() {
 // 0.99 at 128 and at 1024).
 constexpr int kTargetThreads = 256;
 
-bool cluster_fits(const DeviceInfo &dev, int cs, int threads, size_t smem,
-                  int ppt) {
-    // cudaOccupancyMaxActiveClusters: can at least one cluster of `cs` blocks
-    // of this kernel be resident at once?
-    const void *fn = fps_kernel_ptr(2, ppt);
+// Clusters of `cs` blocks of kernel `fn` (threads, dynamic shared memory)
+// that can be resident at once: cudaOccupancyMaxActiveClusters, 0 when none
+// or when the query fails.
+int max_active_clusters(const void *fn, int cs, int threads, size_t smem) {
     if (cs > 8 &&
         cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed,
                              1) != cudaSuccess) {
@@ -471,14 +690,86 @@ bool cluster_fits(const DeviceInfo &dev, int cs, int threads, size_t smem,
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
         cudaGetLastError();
-        return false;
+        return 0;
     }
-    return n >= 1;
+    return n;
+}
+
+bool cluster_fits(const DeviceInfo &dev, int cs, int threads, size_t smem,
+                  int ppt) {
+    (void)dev;
+    return max_active_clusters(fps_kernel_ptr(2, ppt), cs, threads, smem) >= 1;
 }
 
 size_t cluster_smem(int chunk) {
     return fps_coords_bytes(chunk) + 32 * sizeof(uint2) +
            2 * FPS_MAX_CLUSTER * sizeof(ClusterSlot) + 2 * sizeof(uint64_t) + 16;
+}
+
+// The two-level grid kernel adds the winner's mbarrier pair and slots.
+size_t cgrid_smem(int chunk) {
+    return cluster_smem(chunk) + 2 * sizeof(uint64_t) + 2 * sizeof(ClusterSlot);
+}
+
+const void *fps_cgrid_ptr(int ppt) {
+    switch (ppt) {
+        case 2: return reinterpret_cast<const void *>(&fps_cgrid_kernel<2>);
+        case 4: return reinterpret_cast<const void *>(&fps_cgrid_kernel<4>);
+        case 8: return reinterpret_cast<const void *>(&fps_cgrid_kernel<8>);
+        case 16: return reinterpret_cast<const void *>(&fps_cgrid_kernel<16>);
+        case 24: return reinterpret_cast<const void *>(&fps_cgrid_kernel<24>);
+        default: return reinterpret_cast<const void *>(&fps_cgrid_kernel<32>);
+    }
+}
+
+// The two-level GRID plan for clusters of `cs` blocks: with bpc_req > 0 that
+// many blocks per cloud (a multiple of cs), else as many clusters as can be
+// resident with every cloud holding the same number.  p.ok = false when the
+// clusters cannot all be resident.
+FpsPlan plan_cgrid(const DeviceInfo &dev, int64_t B, int64_t N, int cs, int bpc_req) {
+    FpsPlan p;
+    p.strategy = 3;
+    p.cluster = cs;
+    if (bpc_req > 0 && bpc_req % cs != 0) {
+        p.why = "blocks_per_cloud is not a multiple of the cluster size";
+        return p;
+    }
+    const int nsm = std::max(1, dev.sm_count);
+    int64_t bpc = bpc_req > 0 ? bpc_req : (nsm / std::max<int64_t>(B, 1)) / cs * cs;
+    for (int iter = 0; iter < 3 && bpc >= cs; ++iter) {
+        if (bpc > N) bpc = std::max<int64_t>(cs, N / cs * cs);
+        p.chunk = int((N + bpc - 1) / bpc);
+        if (!pick_shape(p.chunk, kTargetThreads, p.ppt, p.threads)) {
+            p.why = "cloud too large for the on-chip FPS schedules";
+            return p;
+        }
+        p.smem_bytes = cgrid_smem(p.chunk);
+        if (p.smem_bytes > dev.smem_per_block_optin) {
+            p.why = "block's share of the cloud exceeds shared memory";
+            return p;
+        }
+        const int n = max_active_clusters(fps_cgrid_ptr(p.ppt), cs, p.threads,
+                                          p.smem_bytes);
+        const int64_t ncl_fit = n / std::max<int64_t>(B, 1);
+        if (ncl_fit * cs >= bpc) {
+            if (bpc_req > 0 || ncl_fit * cs == bpc) {
+                p.blocks_per_cloud = int(bpc);
+                // 8 words per cluster and cloud; sized as the one-level
+                // schedule's 2 words per block when that is more (cs >= 4),
+                // so that the size does not depend on the cluster chosen
+                const size_t words =
+                    size_t(B) * std::max<size_t>(2 * CG_SLOT_WORDS * size_t(bpc / cs),
+                                                 2 * size_t(bpc));
+                p.workspace_bytes = (words * sizeof(uint64_t) + 255) & ~size_t(255);
+                p.ok = true;
+                return p;
+            }
+        }
+        if (bpc_req > 0 || ncl_fit == 0) break;
+        bpc = ncl_fit * cs;  // as many as fit with this shape; check again
+    }
+    p.why = "two-level grid clusters cannot all be resident";
+    return p;
 }
 
 }  // namespace
@@ -553,6 +844,30 @@ FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
             p.why = "device has no cooperative launch";
             return p;
         }
+        // two levels (clusters exchanging through distributed shared memory,
+        // then one slot per cluster in the workspace) unless cluster_size is
+        // 1: the cluster size that keeps the most blocks resident
+        if (cluster_size != 1) {
+            // the largest cluster that fits: fewest slots and leaders in the
+            // global exchange (GB300, 1M points: 2.0 us per step with 7
+            // clusters of 16, 2.7 with 15 of 8, 6.9 with 36 of 4, when every
+            // block polled every slot)
+            FpsPlan best;
+            const int sizes[3] = {16, 8, 4};
+            for (int cs : sizes) {
+                if (cluster_size > 1 && cs != cluster_size) continue;
+                best = plan_cgrid(dev, B, N, cs, blocks_per_cloud);
+                if (best.ok) break;
+            }
+            if (cluster_size > 1 && !best.ok && cluster_size != 16 &&
+                cluster_size != 8 && cluster_size != 4)
+                best = plan_cgrid(dev, B, N, cluster_size, blocks_per_cloud);
+            if (best.ok) return best;
+            if (cluster_size > 1) {
+                p.why = "two-level grid with this cluster size cannot be resident";
+                return p;
+            }
+        }
         int bpc = blocks_per_cloud;
         if (bpc <= 0) bpc = int(std::max<int64_t>(1, nsm / std::max<int64_t>(B, 1)));
         bpc = int(std::min<int64_t>(bpc, N));
@@ -600,22 +915,56 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
     a.out = out_idx;
     a.chunk = plan.chunk;
     a.nblocks = plan.blocks_per_cloud;
+    a.cs = plan.strategy == 3 ? plan.cluster : 1;
+    a.ncl = plan.blocks_per_cloud / std::max(1, a.cs);
     a.slots = static_cast<uint64_t *>(workspace);
     a.status = dev.status_word;
     a.timeout_ns = wait_timeout_ns();
     a.stall = debug_stall();
     a.negzero = -0.0f;
 
-    const void *fn = fps_kernel_ptr(plan.strategy, plan.ppt);
+    const bool cgrid = plan.strategy == 3 && plan.cluster > 1;
+    const void *fn = cgrid ? fps_cgrid_ptr(plan.ppt) : fps_kernel_ptr(plan.strategy, plan.ppt);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(B * plan.blocks_per_cloud));
     cfg.blockDim = dim3(unsigned(plan.threads));
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.attrs = attr;
     cfg.numAttrs = 0;
+    void *args[] = {&a};
     cudaError_t e;
+    if (cgrid) {
+        e = cudaMemsetAsync(workspace, 0, plan.workspace_bytes, stream);
+        if (e != cudaSuccess) return e;
+        if (plan.cluster > 8) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(plan.smem_bytes));
+        if (e != cudaSuccess) return e;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(plan.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        // cooperative: every cluster resident at once, or no launch; where
+        // the runtime refuses cooperative cluster launches, the plan's
+        // occupancy check alone stands behind co-residency (and every wait
+        // is bounded)
+        attr[1].id = cudaLaunchAttributeCooperative;
+        attr[1].val.cooperative = 1;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelExC(&cfg, fn, args);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelExC(&cfg, fn, args);
+        }
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     if (plan.strategy == 3) {
         e = cudaMemsetAsync(workspace, 0, plan.workspace_bytes, stream);
         if (e != cudaSuccess) return e;
@@ -639,7 +988,6 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
             cfg.numAttrs = 1;
         }
     }
-    void *args[] = {&a};
     e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -24,8 +24,9 @@
 namespace {
 
 // 4096 exchange words (32 KiB) per device.  The grid schedule uses
-// 2 * blocks_per_cloud * B words, and B * blocks_per_cloud never exceeds the
-// SM count, so this covers any device with up to 2048 SMs.
+// B * max(2 * blocks per cloud, 32 * clusters per cloud) words, and the
+// blocks never exceed the SM count, so this covers any device with up to
+// 2048 SMs.
 constexpr size_t kStaticScratchWords = 4096;
 static __device__ __align__(256) uint64_t g_fps_static_scratch[kStaticScratchWords];
 
@@ -95,10 +96,10 @@ extern "C" int pc_fps_grid_static(const float *xyz, int64_t B, int64_t N,
     if (plan.workspace_bytes > sizeof(uint64_t) * kStaticScratchWords) {
         std::snprintf(msg, sizeof(msg),
                       "fps_grid_static: needs %zu bytes of scratch but the static "
-                      "array holds %zu (B * blocks_per_cloud <= %zu)",
+                      "array holds %zu (%zu words: B * max(2 * blocks per cloud, "
+                      "32 * clusters per cloud))",
                       plan.workspace_bytes,
-                      sizeof(uint64_t) * kStaticScratchWords,
-                      kStaticScratchWords / 2);
+                      sizeof(uint64_t) * kStaticScratchWords, kStaticScratchWords);
         return pcn::api_fail(PC_ERR_INVALID_ARGUMENT, msg);
     }
     void *scratch = nullptr;

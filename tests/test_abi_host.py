@@ -147,12 +147,14 @@ def test_sm_reserve_and_fps_sm_count_without_device(L):
 
 def test_fps_plan_without_device(L):
     import ctypes
-    st, bpc = ctypes.c_int(7), ctypes.c_int(7)
-    assert L.pc_fps_plan(1, 100000, 0, 0, 0, None, None) == 1
-    assert L.pc_fps_plan(0, 100000, 0, 0, 0, ctypes.byref(st), ctypes.byref(bpc)) == 1
-    assert (st.value, bpc.value) == (0, 0)
+    st, cs, bpc = ctypes.c_int(7), ctypes.c_int(7), ctypes.c_int(7)
+    assert L.pc_fps_plan(1, 100000, 0, 0, 0, None, None, None) == 1
+    assert L.pc_fps_plan(0, 100000, 0, 0, 0, ctypes.byref(st), ctypes.byref(cs),
+                         ctypes.byref(bpc)) == 1
+    assert (st.value, cs.value, bpc.value) == (0, 0, 0)
     # sizes are valid, but there is no device to plan for
-    assert L.pc_fps_plan(1, 100000, 0, 0, 0, ctypes.byref(st), ctypes.byref(bpc)) == 5
+    assert L.pc_fps_plan(1, 100000, 0, 0, 0, ctypes.byref(st), ctypes.byref(cs),
+                         ctypes.byref(bpc)) == 5
 
 
 def test_knn_ex_validation(L):

@@ -442,6 +442,9 @@ def test_outputs_fully_written_over_sentinels():
     (pc.PC_FPS_BLOCK, 0, 0), (pc.PC_FPS_CLUSTER, 1, 0), (pc.PC_FPS_CLUSTER, 2, 0),
     (pc.PC_FPS_CLUSTER, 4, 0), (pc.PC_FPS_CLUSTER, 8, 0), (pc.PC_FPS_CLUSTER, 3, 0),
     (pc.PC_FPS_GRID, 0, 2), (pc.PC_FPS_GRID, 0, 7), (pc.PC_FPS_GRID, 0, 0),
+    # the two-level grid (clusters, then one slot per cluster) and one level
+    (pc.PC_FPS_GRID, 4, 8), (pc.PC_FPS_GRID, 8, 0), (pc.PC_FPS_GRID, 16, 0),
+    (pc.PC_FPS_GRID, 1, 0), (pc.PC_FPS_GRID, 1, 12),
 ])
 def test_fps_schedules_agree_with_oracle(strategy, cs, bpc):
     x = inputs.random_cloud(13, 2, 5000, grid=1 / 32)
@@ -457,10 +460,19 @@ def test_fps_cluster_on_100k(cs):
     assert_idx_equal(idx, oracle.fps(x, 600, 3), f"fps cluster {cs}")
 
 
-def test_fps_grid_on_100k():
+@pytest.mark.parametrize("cs", [0, 1, 8])
+def test_fps_grid_on_100k(cs):
     x = inputs.large()
-    idx = gpu_fps(x, 600, 3, strategy=pc.PC_FPS_GRID)
-    assert_idx_equal(idx, oracle.fps(x, 600, 3), "fps grid")
+    idx = gpu_fps(x, 600, 3, strategy=pc.PC_FPS_GRID, cluster_size=cs)
+    assert_idx_equal(idx, oracle.fps(x, 600, 3), f"fps grid, cluster size {cs}")
+
+
+def test_fps_grid_plan_reports_two_levels():
+    st, cs, bpc = pc.pc_fps_plan(1, 1_000_000)
+    assert st == pc.PC_FPS_GRID and cs in (4, 8, 16) and bpc % cs == 0
+    assert pc.pc_fps_plan(1, 1_000_000, pc.PC_FPS_GRID, 1)[1] == 1
+    with pytest.raises(pc.PointCloudError):
+        pc.pc_fps_plan(1, 1_000_000, pc.PC_FPS_GRID, 8, 12)   # 12 not a multiple of 8
 
 
 @pytest.mark.parametrize("N,npoint,start", [(1, 4, 0), (5, 9, 2), (7, 7, 6),
