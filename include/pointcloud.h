@@ -239,6 +239,14 @@ int pc_knn_ex(const float *query, int64_t B, int64_t Q, const float *ref,
  *   K          >= 1.  N = 0 is allowed (all slots padded).
  *   out_dist2  [B, Q, K] float32, device.  out_idx [B, Q, K] int64, device.
  *
+ * Scratch: with few queries against many references (under 24 queries per
+ * warp of the GPU-wide launch and at least 64 tiles of 256 references) the
+ * references are split into P <= 8 parts that run side by side and whose
+ * first-K hits are then joined in part order; that takes P * B * Q * (12 K
+ * + 4) bytes (at most 1 GiB) from the stream-ordered allocator
+ * (cudaMallocAsync) on `stream`, freed there after the merge; an allocation
+ * failure returns PC_ERR_CUDA.  Results do not depend on the path taken.
+ *
  * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_CUDA or PC_ERR_NO_DEVICE.
  */
 int pc_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,

@@ -6,7 +6,8 @@
 // first K accepted indices in input order are returned with their squared
 // distances, unused slots hold (-1, 0).
 //
-// Design (one launch, no scratch memory):
+// Design (one launch, no scratch memory; with few queries against many
+// references, the references split into parts plus a merge, see below):
 //  * A block has BQ_CWARPS consumer warps and one producer warp.  Consumer
 //    warp w owns G queries of one cloud, kept in shared memory as the filter
 //    constants of pc_filter.cuh duplicated for the packed instructions,
@@ -45,6 +46,9 @@ namespace {
 
 constexpr int BQ_R = 8;  // reference points per lane per tile
 constexpr int BQ_CWARPS = 8;
+// references split into parts when a warp would hold fewer queries than this
+constexpr int BQ_MIN_QUERIES_PER_WARP = 24;
+constexpr int64_t BQ_MAX_PARTS = 8;
 constexpr int BQ_THREADS = 32 * (BQ_CWARPS + 1);
 constexpr unsigned FULL = 0xffffffffu;
 static_assert(32 * BQ_R == ST_T, "a lane holds 8 of a stream tile's points");
@@ -63,6 +67,13 @@ struct BqArgs {
     int *status;
     uint64_t timeout_ns;
     int stall;  // PC_STALL_* testing flags
+    // references split into gridDim.z parts (few queries against many
+    // references): part p records its first K hits per row in
+    // part_idx/part_d2 [p][B][Q][K] and their number in part_cnt [p][B][Q]
+    // (-1: the part stopped on a timeout); bq_merge_parts_kernel joins them
+    int64_t *part_idx;
+    float *part_d2;
+    int *part_cnt;
 };
 
 struct __align__(16) BqSlot {
@@ -160,9 +171,18 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
     const float *cref = a.ref + size_t(b) * size_t(a.N) * 3;
     const int Nb = valid_len(a.r_len, b, a.N);
     const int Qb = valid_len(a.q_len, b, a.Q);
-    const int ntiles = (Nb + ST_T - 1) / ST_T;
+    const int ntiles_all = (Nb + ST_T - 1) / ST_T;
+    // part blockIdx.z of gridDim.z: tiles [t0, t0 + ntiles) of the cloud
+    const int part = static_cast<int>(blockIdx.z), nparts = static_cast<int>(gridDim.z);
+    const int t0 = static_cast<int>((static_cast<long long>(ntiles_all) * part) / nparts);
+    const int ntiles =
+        static_cast<int>((static_cast<long long>(ntiles_all) * (part + 1)) / nparts) - t0;
+    const bool parts = nparts > 1;
+    float *dst_d2 = parts ? a.part_d2 + size_t(part) * gridDim.y * a.Q * K : a.out_dist2;
+    int64_t *dst_idx = parts ? a.part_idx + size_t(part) * gridDim.y * a.Q * K : a.out_idx;
 
     if (blockIdx.x * BQ_CWARPS * G >= Qb) {
+        if (part != 0) return;
         // every query of this block is past the cloud's valid length
         const int r0 = blockIdx.x * BQ_CWARPS * G;
         const int r1 = min(a.Q, r0 + BQ_CWARPS * G);
@@ -186,8 +206,8 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
 
     if (warp == BQ_CWARPS) {  // producer warp: tiles strictly in input order
         const bool withhold = (a.stall & PC_STALL_TILE_STREAM) && blockIdx.x == 0 &&
-                              blockIdx.y == 0;
-        stream_produce<BQ_SB, false>(ring, cref, Nb, ntiles, [](int it) { return it; },
+                              blockIdx.y == 0 && blockIdx.z == 0;
+        stream_produce<BQ_SB, false>(ring, cref, Nb, ntiles, [t0](int it) { return t0 + it; },
                                      fr, s_stop, s_err, a.timeout_ns, withhold);
         return;
     }
@@ -231,7 +251,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             failed = w == WAIT_TIMEOUT;
             break;
         }
-        const int j0 = it * ST_T;
+        const int j0 = (t0 + it) * ST_T;
         const int cnt = min(ST_T, Nb - j0);
         const float4 *ck = ring.cooked_tile(st);
         const float4 *raw = ring.raw_copy(st);
@@ -256,7 +276,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
                 const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(azt.w);
                 const int h = bq_record(raw, rx, ry, rz, rw, axy, azt, q,
                                         __float_as_int(q.w), j0, cnt, a.R2, K, row,
-                                        a.out_dist2, a.out_idx);
+                                        dst_d2, dst_idx);
                 if (lane == 0) sp->raw.w = __int_as_float(h);
                 any_full |= h >= K;
             };
@@ -312,8 +332,18 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
         raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
     }
     // pad the unused slots with (-1, 0); after a failure every slot; rows
-    // past the valid length in full
+    // past the valid length in full.  Parts record their hit counts instead
+    // (-1 after a failure); the merge pads.
     __syncwarp();
+    if (parts) {
+        for (int g = lane; g < nq; g += 32) {
+            const BqSlot q = slots[g];
+            const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(q.azt.w);
+            a.part_cnt[size_t(part) * gridDim.y * a.Q + row] =
+                failed ? -1 : __float_as_int(q.raw.w);
+        }
+        if (part != 0) return;
+    }
     const int nrows = max(0, min(G, a.Q - q_warp0));
     for (int g = nq; g < nrows; ++g) {
         const size_t row = size_t(b) * a.Q + q_warp0 + g;
@@ -322,6 +352,7 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             a.out_dist2[row * K + e] = 0.0f;
         }
     }
+    if (parts) return;
     for (int g = 0; g < nq; ++g) {
         const BqSlot q = slots[g];
         const size_t row = size_t(b) * a.Q + q_warp0 + __float_as_int(q.azt.w);
@@ -330,6 +361,51 @@ __global__ void __launch_bounds__(BQ_THREADS, 2) bq_kernel(const BqArgs a) {
             a.out_idx[row * K + e] = -1;
             a.out_dist2[row * K + e] = 0.0f;
         }
+    }
+}
+
+// The first K hits of a valid query row over the parts, in part order (a
+// part covers the references after the previous part's): one warp per row.
+// Slot e takes entry e - (hits of the parts before) of the part it falls
+// in; past the total, (-1, 0).  A row with a stopped part is -1 throughout.
+constexpr int BQ_MERGE_WARPS = 8;
+__global__ void __launch_bounds__(32 * BQ_MERGE_WARPS) bq_merge_parts_kernel(const BqArgs a,
+                                                                            int nparts) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * BQ_MERGE_WARPS + (threadIdx.x >> 5);
+    const int b = blockIdx.y;
+    const int B = gridDim.y;
+    if (r >= valid_len(a.q_len, b, a.Q)) return;  // padded by the query kernel
+    const int K = a.K;
+    const size_t row = size_t(b) * a.Q + r;
+    const int c = lane < nparts ? a.part_cnt[size_t(lane) * B * a.Q + row] : 0;
+    const bool failed = __any_sync(FULL, c < 0);
+    // inclusive prefix of the parts' hit counts over lanes 0 .. nparts - 1
+    int incl = c < 0 ? 0 : c;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        const int y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int upto[8];  // hits of parts 0 .. p, every lane
+#pragma unroll
+    for (int p = 0; p < 8; ++p) upto[p] = __shfl_sync(FULL, incl, p);
+    const int total = upto[7];
+    for (int e = lane; e < K; e += 32) {
+        int64_t idx = -1;
+        float d2 = 0.0f;
+        if (!failed && e < total) {
+            int p = 0, before = 0;
+            for (; p < nparts; ++p) {
+                if (e < upto[p]) break;
+                before = upto[p];
+            }
+            const size_t src = (size_t(p) * B * a.Q + row) * K + (e - before);
+            idx = a.part_idx[src];
+            d2 = a.part_d2[src];
+        }
+        a.out_idx[row * K + e] = idx;
+        a.out_dist2[row * K + e] = d2;
     }
 }
 
@@ -358,8 +434,26 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
 
     // one wave of two blocks per SM, less the SMs other work holds
     const int slots = std::max(1, dev.sm_count - sm_reserve()) * 2;
-    const int64_t bpc_target = std::max<int64_t>(1, slots / std::max<int64_t>(B, 1));
-    int64_t G = (Q + BQ_CWARPS * bpc_target - 1) / (BQ_CWARPS * bpc_target);
+    auto queries_per_warp = [&](int64_t parts) {
+        const int64_t bpc_target =
+            std::max<int64_t>(1, slots / std::max<int64_t>(B * parts, 1));
+        return (Q + BQ_CWARPS * bpc_target - 1) / (BQ_CWARPS * bpc_target);
+    };
+    // Few queries against many references: a warp would hold too few queries
+    // to spread each tile's cost over, so the references are split into
+    // parts (blocks of the same queries, other tiles) and the parts' hits
+    // merged in order (GB300, 16,384 queries vs 1M points, r = 0.01, K = 64:
+    // 7 queries per warp in one part).
+    const int64_t ntiles = (N + ST_T - 1) / ST_T;
+    int64_t P = 1;
+    const int64_t g1 = queries_per_warp(1);
+    if (g1 < BQ_MIN_QUERIES_PER_WARP && ntiles >= 64)
+        P = std::max<int64_t>(1, std::min<int64_t>(
+                                     {BQ_MAX_PARTS,
+                                      (BQ_MIN_QUERIES_PER_WARP + g1 - 1) / g1, ntiles / 16}));
+    const size_t part_rows = size_t(P) * size_t(B) * size_t(Q);
+    if (P > 1 && part_rows * size_t(K) * 12 > (size_t(1) << 30)) P = 1;  // scratch cap
+    int64_t G = queries_per_warp(P);
     const size_t budget =
         std::min<size_t>(dev.smem_per_block_optin, dev.smem_per_sm / 2 - 2048);
     const int64_t gmax = std::max<int64_t>(
@@ -372,9 +466,32 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
         bq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>(bpc), static_cast<unsigned>(B));
+    dim3 grid(static_cast<unsigned>(bpc), static_cast<unsigned>(B), static_cast<unsigned>(P));
+    if (P == 1) {
+        bq_kernel<<<grid, BQ_THREADS, smem, stream>>>(a);
+        return cudaGetLastError();
+    }
+    // the parts' hits and counts in stream-ordered scratch
+    const size_t rows = size_t(P) * size_t(B) * size_t(Q);
+    const size_t off_d2 = (rows * size_t(K) * sizeof(int64_t) + 255) & ~size_t(255);
+    const size_t off_cnt = (off_d2 + rows * size_t(K) * sizeof(float) + 255) & ~size_t(255);
+    const size_t total = off_cnt + rows * sizeof(int);
+    char *base = nullptr;
+    e = cudaMallocAsync(reinterpret_cast<void **>(&base), total, stream);
+    if (e != cudaSuccess) return e;
+    a.part_idx = reinterpret_cast<int64_t *>(base);
+    a.part_d2 = reinterpret_cast<float *>(base + off_d2);
+    a.part_cnt = reinterpret_cast<int *>(base + off_cnt);
     bq_kernel<<<grid, BQ_THREADS, smem, stream>>>(a);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        const dim3 gm(static_cast<unsigned>((Q + BQ_MERGE_WARPS - 1) / BQ_MERGE_WARPS),
+                      static_cast<unsigned>(B));
+        bq_merge_parts_kernel<<<gm, 32 * BQ_MERGE_WARPS, 0, stream>>>(a, int(P));
+        e = cudaGetLastError();
+    }
+    const cudaError_t f = cudaFreeAsync(base, stream);
+    return e != cudaSuccess ? e : f;
 }
 
 }  // namespace pcn

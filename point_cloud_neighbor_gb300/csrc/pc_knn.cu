@@ -9,8 +9,9 @@
 // lane with per-lane heaps, fed by a producer warp that prepares the tiles
 // (pc_stream.cuh); large clouds are first put in a spatial order (a few
 // small kernels and stream-ordered scratch) that the kernel visits outwards
-// from each block's region.  k > 32: knn_kernel, described here (one launch,
-// no scratch memory):
+// from each block's region.  k > 32, and launches with too few queries to
+// give every SM a warp of the lane kernel: knn_kernel, described here (one
+// launch, no scratch memory):
 //  * A block has KNN_CWARPS consumer warps and one producer warp.  Consumer
 //    warp w owns G queries of one cloud.  Per query, shared memory holds the
 //    filter constants (-2q', -2q', thr, thr; pc_filter.cuh), the raw
@@ -1395,6 +1396,15 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     // large clouds with k >= 2: the spatial order (a few extra launches)
     // pays for itself many times over in candidate insertions
     const bool ordered = k >= 2 && k <= 32 && N >= 16384 && Q >= 4096 && B <= 64;
+    // few query groups (under a quarter of the SMs would hold a warp): one
+    // warp per query with the warp-list kernel keeps every SM busy (GB300,
+    // 64 queries vs 1024 points, k = 16: 0.045 ms vs 0.21 ms with the lane
+    // kernel's single warp)
+    if (B * ((Q + 31) / 32) * 4 < dev.sm_count) {
+        if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
+        if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
+        return launch_knn_t<8>(dev, a, B, Q, stream);
+    }
     if (ordered && k <= 16) return launch_knn_ordered<2>(dev, a, B, stream);
     if (ordered) return launch_knn_ordered<1>(dev, a, B, stream);
     if (k <= 16) return launch_knn_lane<2>(dev, a, B, a, 0, stream);

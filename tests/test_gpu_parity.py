@@ -391,6 +391,28 @@ def test_random_coordinates_bit_exact(B, Q, N):
     assert_idx_equal(idx, oracle.fps(x, 200, 1), "fps random coordinates")
 
 
+@pytest.mark.parametrize("B,Q,N,r,K", [
+    (1, 64, 100_000, 0.05, 40),     # few hits: every part scans its range
+    (2, 300, 70_000, 0.35, 16),     # many hits: the first parts fill K
+    (3, 41, 33_000, 0.12, 64),      # ragged tiles and parts
+])
+def test_ball_query_reference_parts(B, Q, N, r, K):
+    """Few queries against many references: the references are split into
+    parts whose first-K hits are joined in order; every row against the
+    oracle, also with lengths masks."""
+    x = inputs.random_cloud(900 + N, B, N)
+    q = inputs.random_cloud(901 + Q, B, Q)
+    q[:, :5] = x[:, :5]                       # exact matches (distance 0)
+    check_bq(q, x, r, K, what=f"bq parts B={B} Q={Q} N={N}")
+    ql = np.array([Q, Q - 7, 3][:B], np.int64)
+    rl = np.array([N, N // 2 + 11, 200][:B], np.int64)
+    d2, i = pc.pc_ball_query(to_dev(q), to_dev(x), r, K, query_lengths=to_dev(ql),
+                             ref_lengths=to_dev(rl))
+    wd2, wi = oracle.ball_query_masked(q, x, r, K, ql, rl)
+    assert_idx_equal(i.cpu().numpy().reshape(-1, K), wi, "bq parts with lengths")
+    assert_dist_equal(d2.cpu().numpy().reshape(-1, K), wd2, "bq parts with lengths")
+
+
 def test_ball_query_large_radius_early_exit():
     x = inputs.random_cloud(5, 2, 20000)
     q = inputs.random_cloud(6, 2, 500)
@@ -557,7 +579,8 @@ def _rows_stopped_or_exact(i, wi, what):
     return int(stopped.sum())
 
 
-@pytest.mark.parametrize("case", ["lane", "ordered", "warp_list", "ball_query"])
+@pytest.mark.parametrize("case", ["lane", "few_queries", "ordered", "warp_list",
+                                  "ball_query", "ball_query_parts"])
 def test_tile_stream_wait_timeout_is_reported(case):
     """The producer of the first thread block never issues its first tile's
     copy (nothing is left in flight): its wait and its consumers' run out,
@@ -566,14 +589,20 @@ def test_tile_stream_wait_timeout_is_reported(case):
     if case == "ordered":        # spatially ordered kNN: many blocks
         x = cache.large(False)[:, :20000].copy()
         q, k = x, 16
-    else:                        # one thread block
+    elif case == "ball_query_parts":   # references split into parts
+        x = cache.large(False).copy()
+        q, k = np.ascontiguousarray(x[:, :64]), 16
+    else:
+        # lane: the lane kernel over 32 blocks; few_queries: 64 queries go to
+        # the warp-list kernel (8 blocks); warp_list and ball_query: one block
+        nq = {"lane": 2000, "few_queries": 64}.get(case, 8)
         x = inputs.random_cloud(30, 1, 3000)
-        q = inputs.random_cloud(31, 1, 8 if case in ("warp_list", "ball_query") else 64)
+        q = inputs.random_cloud(31, 1, nq)
         k = 40 if case == "warp_list" else 8
     pc.pc_set_wait_timeout_ns(2_000_000)       # 2 ms
     pc.pc_debug_set_stall(pc.PC_STALL_TILE_STREAM)
     try:
-        if case == "ball_query":
+        if case.startswith("ball_query"):
             _, got = pc.pc_ball_query(to_dev(q), to_dev(x), 0.5, 16)
         else:
             _, got = pc.pc_knn(to_dev(q), to_dev(x), k)
@@ -582,16 +611,18 @@ def test_tile_stream_wait_timeout_is_reported(case):
         pc.pc_debug_set_stall(0)
         pc.pc_set_wait_timeout_ns(2_000_000_000)
     assert pc.pc_device_status(reset=True) == 4
-    if case == "ball_query":
-        _, wi = oracle.ball_query(q, x, 0.5, 16)
+    if case.startswith("ball_query"):
+        _, wi = oracle.ball_query(q, x, 0.5, 16, threads=THREADS)
     else:
         _, wi = oracle.knn(q, x, k, threads=THREADS)
     stopped = _rows_stopped_or_exact(got, wi, case)
     assert stopped >= 1
-    if case != "ordered":
+    if case in ("warp_list", "ball_query"):
         assert stopped == wi.shape[0]          # the only block stopped
+    else:
+        assert stopped < wi.shape[0]           # only the first block stopped
     # the context is still usable and the next call is correct
-    if case == "ball_query":
+    if case.startswith("ball_query"):
         check_bq(q, x, 0.5, 16, what="bq after timeout")
     else:
         check_knn(q, x, k, what=f"{case} knn after timeout")
