@@ -128,21 +128,47 @@ three_interpolate_staged_kernel(const float *__restrict__ f,
     const int c0 = blockIdx.y * CC;
     const int cc = min(CC, C - c0);
     const float *fb = f + (size_t(b) * C + c0) * size_t(M);
-    for (int e = threadIdx.x; e < cc * M; e += STG_THREADS) tile[e] = __ldg(fb + e);
+    const int ne = cc * M;
+    if ((reinterpret_cast<uintptr_t>(fb) & 15) == 0) {  // 128-bit loads
+        const float4 *f4 = reinterpret_cast<const float4 *>(fb);
+        float4 *t4 = reinterpret_cast<float4 *>(tile);
+        for (int e = threadIdx.x; e < ne / 4; e += STG_THREADS) t4[e] = __ldg(f4 + e);
+        for (int e = (ne & ~3) + threadIdx.x; e < ne; e += STG_THREADS) tile[e] = __ldg(fb + e);
+    } else {
+        for (int e = threadIdx.x; e < ne; e += STG_THREADS) tile[e] = __ldg(fb + e);
+    }
+    // the (index, weight) triplets of this thread's points, all loads in
+    // flight at once while the features are staged
+    constexpr int PPT = STG_POINTS / STG_THREADS;
+    const int i0 = blockIdx.x * STG_POINTS + threadIdx.x;
+    int m[PPT][3];
+    float wt[PPT][3];
+#pragma unroll
+    for (int p = 0; p < PPT; ++p) {
+        const int i = i0 + p * STG_THREADS;
+        if (i < n) {
+            load_triplet(idx, w, (size_t(b) * n + i) * 3, M, m[p], wt[p], status);
+        } else {
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+                m[p][t] = -1;
+                wt[p][t] = 0.0f;
+            }
+        }
+    }
     __syncthreads();
-    const int i1 = min(n, (blockIdx.x + 1) * STG_POINTS);
-    for (int i = blockIdx.x * STG_POINTS + threadIdx.x; i < i1; i += STG_THREADS) {
-        int m[3];
-        float wt[3];
-        load_triplet(idx, w, (size_t(b) * n + i) * 3, M, m, wt, status);
-        for (int c = 0; c < cc; ++c) {
-            const float *tr = tile + c * M;
-            const float v0 = m[0] >= 0 ? tr[m[0]] : 0.0f;
-            const float v1 = m[1] >= 0 ? tr[m[1]] : 0.0f;
-            const float v2 = m[2] >= 0 ? tr[m[2]] : 0.0f;
-            const float s01 = __fadd_rn(__fmul_rn(wt[0], v0), __fmul_rn(wt[1], v1));
-            out[(size_t(b) * C + c0 + c) * size_t(n) + i] =
-                __fadd_rn(s01, __fmul_rn(wt[2], v2));
+    for (int c = 0; c < cc; ++c) {
+        const float *tr = tile + c * M;
+        float *oc = out + (size_t(b) * C + c0 + c) * size_t(n);
+#pragma unroll
+        for (int p = 0; p < PPT; ++p) {
+            const int i = i0 + p * STG_THREADS;
+            const float v0 = m[p][0] >= 0 ? tr[m[p][0]] : 0.0f;
+            const float v1 = m[p][1] >= 0 ? tr[m[p][1]] : 0.0f;
+            const float v2 = m[p][2] >= 0 ? tr[m[p][2]] : 0.0f;
+            const float s01 =
+                __fadd_rn(__fmul_rn(wt[p][0], v0), __fmul_rn(wt[p][1], v1));
+            if (i < n) oc[i] = __fadd_rn(s01, __fmul_rn(wt[p][2], v2));
         }
     }
 }
@@ -220,15 +246,37 @@ interp_csr_kernel(const int64_t *__restrict__ idx, const float *__restrict__ w,
 }
 
 // One thread per (b, m): insertion sort of m's segment by entry e (segments
-// hold ~3n/M entries), so the sums run in increasing (i, t) order.
-__global__ void interp_sort_kernel(const int *__restrict__ start,
-                                   int2 *__restrict__ list, int B, int M, int n) {
+// hold ~3n/M entries), so the sums run in increasing (i, t) order.  A
+// segment of up to SORT_LOCAL entries is sorted in the thread's slice of
+// shared memory (one global read and write per entry); longer ones in place.
+constexpr int SORT_THREADS = 128;
+constexpr int SORT_LOCAL = 32;
+__global__ void __launch_bounds__(SORT_THREADS)
+interp_sort_kernel(const int *__restrict__ start, int2 *__restrict__ list, int B, int M,
+                   int n) {
+    __shared__ int2 buf[SORT_THREADS * (SORT_LOCAL + 1)];
     const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (t >= int64_t(B) * M) return;
     const int b = int(t / M), m = int(t % M);
     const int *sb = start + size_t(b) * (M + 1);
     int2 *lb = list + size_t(b) * 3 * n;
     const int p0 = sb[m], p1 = sb[m + 1];
+    const int L = p1 - p0;
+    if (L <= SORT_LOCAL) {
+        int2 *mine = buf + threadIdx.x * (SORT_LOCAL + 1);
+        for (int u = 0; u < L; ++u) mine[u] = lb[p0 + u];
+        for (int p = 1; p < L; ++p) {
+            const int2 v = mine[p];
+            int q = p - 1;
+            while (q >= 0 && mine[q].x > v.x) {
+                mine[q + 1] = mine[q];
+                --q;
+            }
+            mine[q + 1] = v;
+        }
+        for (int u = 0; u < L; ++u) lb[p0 + u] = mine[u];
+        return;
+    }
     for (int p = p0 + 1; p < p1; ++p) {
         const int2 v = lb[p];
         int q = p - 1;
@@ -259,11 +307,12 @@ interp_gather_kernel(const float *__restrict__ g, const int *__restrict__ start,
     const int c0 = blockIdx.x * GATH_CC;
     const int cc = min(GATH_CC, C - c0);
     const float *gb = g + (size_t(b) * C + c0) * size_t(n);
-    float *gts = reinterpret_cast<float *>(gt4);
-#pragma unroll 4
-    for (int e = threadIdx.x; e < GATH_CC * n; e += GATH_THREADS) {
-        const int c = e / n, i = e - c * n;
-        gts[i * GATH_CC + c] = c < cc ? __ldg(gb + e) : 0.0f;
+    // point-major staging: the 4 channels of point i as one 16-byte word
+    for (int i = threadIdx.x; i < n; i += GATH_THREADS) {
+        float v[GATH_CC];
+#pragma unroll
+        for (int c = 0; c < GATH_CC; ++c) v[c] = c < cc ? __ldg(gb + size_t(c) * n + i) : 0.0f;
+        gt4[i] = make_float4(v[0], v[1], v[2], v[3]);
     }
     __syncthreads();
     const int *sb = start + size_t(b) * (M + 1);
@@ -433,7 +482,9 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         }
         if (e == cudaSuccess) {
             const int64_t segs = B * M;
-            pcn::interp_sort_kernel<<<unsigned((segs + 255) / 256), 256, 0, st>>>(
+            pcn::interp_sort_kernel<<<unsigned((segs + pcn::SORT_THREADS - 1) /
+                                               pcn::SORT_THREADS),
+                                      pcn::SORT_THREADS, 0, st>>>(
                 start, list, int(B), int(M), int(n));
             e = cudaGetLastError();
         }
