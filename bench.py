@@ -498,6 +498,13 @@ def run_only(args):
     if args.only == "knn_d":
         fx = torch.randn((32, 1024, 64), device=device)
         calls["knn_d"] = lambda: pc.pc_knn_d(fx, fx, 20)
+    if args.only in ("fps_1m", "knn_1m", "ball_query_1m"):
+        # the 1M-point cloud; queries: 16,384 points spread over it
+        vx = torch.from_numpy(inputs.very_large()).to(device)
+        vq = vx[:, ::61][:, :16384].contiguous()
+        calls["fps_1m"] = lambda: pc.pc_fps(vx, 16384, 0)
+        calls["knn_1m"] = lambda: pc.pc_knn(vq, vx, 32)
+        calls["ball_query_1m"] = lambda: pc.pc_ball_query(vq, vx, 0.01, 64)
     if args.only in ("chamfer", "three_interpolate", "three_interpolate_backward"):
         cx = torch.from_numpy(inputs.random_cloud(5, 4, 16384)).to(device)
         cy = torch.from_numpy(inputs.random_cloud(6, 4, 16384)).to(device)
@@ -1151,7 +1158,8 @@ def main():
     ap.add_argument("--only", choices=["fps", "knn", "ball_query", "grid_build",
                                        "grid_knn", "grid_ball_query", "chamfer",
                                        "three_interpolate",
-                                       "three_interpolate_backward", "knn_d"],
+                                       "three_interpolate_backward", "knn_d",
+                                       "fps_1m", "knn_1m", "ball_query_1m"],
                     help="run one operator of the step W + K times and print "
                          "its mean CUDA-event time (for profiler captures)")
     args = ap.parse_args()

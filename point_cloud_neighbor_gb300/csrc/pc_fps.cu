@@ -177,6 +177,12 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T = blockDim.x;
+    // CLUSTER: every distributed-shared-memory address below targets ranks
+    // < a.nblocks; a launch without that cluster shape stops here (uniform)
+    if (CLUSTER && cluster_nctarank() != unsigned(a.nblocks)) {
+        if (threadIdx.x == 0) raise_status(a.status, 3 /* PC_ERR_CUDA */);
+        return;
+    }
     const unsigned rank = CLUSTER ? cluster_ctarank() : 0u;
     const int b = blockIdx.x / a.nblocks;
     const float *x = a.xyz + size_t(b) * size_t(a.N) * 3;
@@ -412,6 +418,13 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int T = blockDim.x;
+    // every distributed-shared-memory address below targets ranks < a.cs:
+    // a launch without that cluster shape stops here, before any access
+    // (uniform over the launch, so no block is left waiting)
+    if (cluster_nctarank() != unsigned(a.cs)) {
+        if (threadIdx.x == 0) raise_status(a.status, 3 /* PC_ERR_CUDA */);
+        return;
+    }
     const unsigned rank = cluster_ctarank();
     const int b = blockIdx.x / a.nblocks;
     const int r = blockIdx.x % a.nblocks;  // block of the cloud
