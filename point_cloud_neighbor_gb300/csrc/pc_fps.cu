@@ -385,9 +385,9 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
 // GRID schedule in two levels: a cooperative launch of thread block
 // clusters of a.cs blocks, a.ncl clusters (a.nblocks = a.cs * a.ncl blocks)
 // per cloud.  Per step:
-//   1. the blocks of a cluster exchange their candidates (key, coordinates)
-//      through distributed shared memory exactly as the CLUSTER schedule
-//      does, and every block reduces them to the cluster's best;
+//   1. every block of a cluster sends its candidate (key, coordinates) to
+//      the cluster's block 0 (its leader) through distributed shared memory
+//      with st.async, and the leader reduces them to the cluster's best;
 //   2. block 0 of each cluster (its leader) publishes that best into the
 //      cluster's slot of the workspace -- four 64-bit words on a 128-byte
 //      line of their own, each carrying the step's tag in its low 9 bits:
@@ -399,7 +399,9 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
 //   3. the leader sends the winner to every block of its cluster through
 //      distributed shared memory (st.async on a second mbarrier pair).
 // Only the a.ncl leaders touch the workspace, so a step's global exchange is
-// a.ncl writers and a.ncl readers of a.ncl lines.  Double buffering by step
+// a.ncl writers and a.ncl readers of a.ncl lines (GB300, 1M points, 16,384
+// samples: 31.7 ms with every block's candidate sent to every block of its
+// cluster, 30.9 ms with it sent to the leader only).  Double buffering by step
 // parity holds at every level: a block sends step t + 2 only after its
 // leader read every cluster's step t + 1, which each cluster publishes only
 // after all its blocks finished step t.  Every wait is bounded.
@@ -468,8 +470,8 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
         unsigned bhi, bj;
         fps_local_step<PPT>(pt, cx, cy, cz, nz0, lo + int(threadIdx.x), T,
                             wslot, bhi, bj);
-        // 1. the block's candidate to every block of the cluster
-        if (warp == 0) {
+        // 1. the block's candidate to the cluster's leader (rank 0)
+        if (warp == 0 && lane == 0) {
             float wx = 0.f, wy = 0.f, wz = 0.f;
             if (bhi) {
                 const float *c = scoord + (int(bj) - lo) * 3;
@@ -478,12 +480,10 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
                 wz = c[2];
             }
             ClusterSlot *mine = &cslot[par * FPS_MAX_CLUSTER + rank];
-            if (lane < a.cs) {
-                const uint32_t ra = map_shared_rank(mine, unsigned(lane));
-                const uint32_t rb = map_shared_rank(&xbar[par], unsigned(lane));
-                st_async_v4(ra, bhi, bj, __float_as_uint(wx), __float_as_uint(wy), rb);
-                st_async_b32(ra + 16, __float_as_uint(wz), rb);
-            }
+            const uint32_t ra = map_shared_rank(mine, 0u);
+            const uint32_t rb = map_shared_rank(&xbar[par], 0u);
+            st_async_v4(ra, bhi, bj, __float_as_uint(wx), __float_as_uint(wy), rb);
+            st_async_b32(ra + 16, __float_as_uint(wz), rb);
         }
         if (rank == 0) {  // the leader: steps 1 to 3
             const bool got = mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns);
@@ -576,16 +576,6 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
                 } else if (lane == 0) {
                     raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
                 }
-            }
-        } else {
-            // the other blocks only take part in step 1: re-arm its barrier
-            // once its phase is seen complete
-            const bool got = mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns);
-            if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&xbar[par], xbytes);
-            if (__syncthreads_or(!got)) {
-                if (threadIdx.x == 0) raise_status(a.status, 4 /* PC_ERR_DEVICE_TIMEOUT */);
-                failed = true;
-                break;
             }
         }
         // every block: the winner from the leader
