@@ -940,10 +940,13 @@ def run_configs(args, pc, flush, device, world, with_oracle):
     return out
 
 
-def run_e2e(args, pc, x_host, device, world):
+def run_e2e(args, pc, x_host, device, world, bq_first=True):
     """Same step through the public API with host buffers: the input is copied
     from pinned host memory each step and every result is read back into
-    pinned host memory; wall time around each synchronized step."""
+    pinned host memory; wall time around each synchronized step.  With
+    bq_first the side stream runs Ball Query before kNN, so that the larger
+    read-back (Ball Query's K = 32 slots per query) overlaps kNN and only
+    kNN's follows the last kernel."""
     import torch
     W = WORKLOAD
     N, npoint, k, r, K = W["N"], W["npoint"], W["knn_k"], W["bq_radius"], W["bq_K"]
@@ -960,8 +963,9 @@ def run_e2e(args, pc, x_host, device, world):
 
     main = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device) if not args.serial else main
-    # the kNN results are read back while Ball Query runs, the FPS result
-    # once FPS ends; only the Ball Query read-back follows the last kernel
+    # the first operator's results are read back while the second runs, the
+    # FPS result once FPS ends; only the second's read-back follows the last
+    # kernel
     copy = torch.cuda.Stream(device) if not args.serial else main
     reserve = 0 if args.serial else STEP_FPS_CLUSTER
 
@@ -971,22 +975,25 @@ def run_e2e(args, pc, x_host, device, world):
         f = pc.pc_fps(xd, npoint, 0, strategy=pc.PC_FPS_CLUSTER,
                       cluster_size=STEP_FPS_CLUSTER)
         outs["fps"].copy_(f, non_blocking=True)
+        ops = [("knn", lambda: pc.pc_knn(xd, xd, k)),
+               ("bq", lambda: pc.pc_ball_query(xd, xd, r, K))]
+        if bq_first:
+            ops.reverse()
         with torch.cuda.stream(side):
             pc.pc_set_sm_reserve(reserve)
-            d, i = pc.pc_knn(xd, xd, k)
+            first = ops[0][1]()
             copy.wait_stream(side)
-            d2, i2 = pc.pc_ball_query(xd, xd, r, K)
+            second = ops[1][1]()
             pc.pc_set_sm_reserve(0)
+        names = {"knn": ("knn_d", "knn_i"), "bq": ("bq_d", "bq_i")}
         with torch.cuda.stream(copy):
-            for t in (d, i):
+            for t, name in zip(first, names[ops[0][0]]):
                 t.record_stream(copy)
-            outs["knn_d"].copy_(d, non_blocking=True)
-            outs["knn_i"].copy_(i, non_blocking=True)
+                outs[name].copy_(t, non_blocking=True)
         main.wait_stream(side)
-        for t in (d2, i2):
+        for t, name in zip(second, names[ops[1][0]]):
             t.record_stream(main)
-        outs["bq_d"].copy_(d2, non_blocking=True)
-        outs["bq_i"].copy_(i2, non_blocking=True)
+            outs[name].copy_(t, non_blocking=True)
         torch.cuda.synchronize(device)
 
     for _ in range(max(1, args.warmup)):
