@@ -34,6 +34,14 @@
  *  - Inputs must be finite.  Ball Query never accepts a NaN distance; FPS and
  *    kNN results for non-finite coordinates are unspecified.
  *  - Sizes: B, N, Q >= 0 with N < 2^31 and every output size < 2^62 elements.
+ *  - Scratch memory: calls that need scratch (stated per call) take it,
+ *    stream-ordered on the call's stream, from a memory pool the library
+ *    creates per device on first use (cudaMemPoolCreate +
+ *    cudaMallocFromPoolAsync) and return it there after their kernels.  The
+ *    pool keeps up to 256 MiB reserved between calls, so a caller that
+ *    synchronizes after every call does not pay for mapping the memory again
+ *    each time; where the device has no memory pools the device's default
+ *    pool (cudaMallocAsync) is used.  pc_fps_grid_static allocates nothing.
  */
 #ifndef POINTCLOUD_H
 #define POINTCLOUD_H
@@ -80,7 +88,8 @@ int pc_version(void);
  *   workspace  device scratch of at least pc_fps_workspace_bytes(B, N,
  *              npoint) bytes, 256-byte aligned, or NULL.  When the chosen
  *              schedule needs scratch and workspace is NULL the library takes
- *              it from the stream-ordered allocator (cudaMallocAsync) and
+ *              it from the library's stream-ordered scratch pool (see
+ *              "Scratch memory" above) and
  *              frees it after the launch on the same stream.  A workspace must
  *              not be shared by calls that may run concurrently.
  *
@@ -190,7 +199,7 @@ int pc_fps_grid_static(const float *xyz, int64_t B, int64_t N, int64_t npoint,
  * unless they are the references), 16 bytes a point; cell tables of about
  * 640 KB per cloud; a seed heap of k 8-byte keys per query; with few queries
  * against many references, up to 8 parts' k keys per query -- from the
- * stream-ordered allocator (cudaMallocAsync) on `stream` and frees it there
+ * library's stream-ordered scratch pool on `stream` and frees it there
  * after its kernels; an allocation failure returns PC_ERR_CUDA.  Results do
  * not depend on the path taken.
  *
@@ -243,8 +252,8 @@ int pc_knn_ex(const float *query, int64_t B, int64_t Q, const float *ref,
  * warp of the GPU-wide launch and at least 64 tiles of 256 references) the
  * references are split into P <= 8 parts that run side by side and whose
  * first-K hits are then joined in part order; that takes P * B * Q * (12 K
- * + 4) bytes (at most 1 GiB) from the stream-ordered allocator
- * (cudaMallocAsync) on `stream`, freed there after the merge; an allocation
+ * + 4) bytes (at most 1 GiB) from the library's stream-ordered scratch pool
+ * on `stream`, freed there after the merge; an allocation
  * failure returns PC_ERR_CUDA.  Results do not depend on the path taken.
  *
  * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_CUDA or PC_ERR_NO_DEVICE.
@@ -394,7 +403,7 @@ int pc_three_interpolate(const float *features, int64_t B, int64_t C,
  * sum is formed from 0 in increasing (i, t) order, every product and
  * addition rounded to float32 (deterministic; bit-identical run to run): three
  * kernels build and sort a per-cloud list of the entries of every known
- * point, in stream-ordered scratch (cudaMallocAsync, 8 bytes per entry plus
+ * point, in stream-ordered scratch (the library's pool, 8 bytes per entry plus
  * M + 1 ints per cloud), then sum each list in order.  Larger sizes zero
  * grad_features and accumulate with float32 atomic adds, whose summation
  * order is not fixed ("Numerical contracts", "Differentiation": the order

@@ -84,6 +84,22 @@ int current_device(const pcn::DeviceInfo **out) {
         e = cudaGetSymbolAddress(&p, g_device_status);
         if (e != cudaSuccess) return cuda_fail(e, "status word address");
         d.status_word = static_cast<int *>(p);
+        // the scratch pool: device memory, kept up to 256 MiB between calls;
+        // without it (pools unsupported) scratch comes from the default pool
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) == cudaSuccess) {
+            uint64_t keep = uint64_t(256) << 20;
+            if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) ==
+                cudaSuccess)
+                d.scratch_pool = pool;
+            else
+                cudaMemPoolDestroy(pool);
+        }
+        cudaGetLastError();
         g_devices[dev] = d;
         g_device_ready[dev] = true;
     }
@@ -127,6 +143,14 @@ bool mul_ok(int64_t a, int64_t b, int64_t c) {
 }  // namespace
 
 namespace pcn {
+cudaError_t scratch_alloc(const DeviceInfo &dev, void **p, size_t bytes,
+                          cudaStream_t stream) {
+    if (dev.scratch_pool != nullptr)
+        return cudaMallocFromPoolAsync(p, bytes, dev.scratch_pool, stream);
+    return cudaMallocAsync(p, bytes, stream);
+}
+cudaError_t scratch_free(void *p, cudaStream_t stream) { return cudaFreeAsync(p, stream); }
+
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 int sm_reserve() { return g_sm_reserve.load(); }
 int debug_stall() { return g_stall.load(); }
@@ -266,7 +290,7 @@ int pc_fps_ex(const float *xyz, int64_t B, int64_t N, int64_t npoint,
             if ((rc = check_ptr(ws, dev->device, 256, "workspace")) != PC_OK)
                 return rc;
         } else {
-            cudaError_t e = cudaMallocAsync(&ws, plan.workspace_bytes, st);
+            cudaError_t e = pcn::scratch_alloc(*dev, &ws, plan.workspace_bytes, st);
             if (e != cudaSuccess) return cuda_fail(e, "fps: workspace allocation");
             owned = true;
         }
@@ -274,7 +298,7 @@ int pc_fps_ex(const float *xyz, int64_t B, int64_t N, int64_t npoint,
     cudaError_t e = pcn::launch_fps(*dev, plan, xyz, B, N, npoint, start_idx,
                                     out_idx, ws, st);
     if (owned) {
-        cudaError_t e2 = cudaFreeAsync(ws, st);
+        cudaError_t e2 = pcn::scratch_free(ws, st);
         if (e == cudaSuccess) e = e2;
     }
     if (e != cudaSuccess) return cuda_fail(e, "fps: launch");

@@ -477,7 +477,7 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
     const size_t off_cnt = (off_d2 + rows * size_t(K) * sizeof(float) + 255) & ~size_t(255);
     const size_t total = off_cnt + rows * sizeof(int);
     char *base = nullptr;
-    e = cudaMallocAsync(reinterpret_cast<void **>(&base), total, stream);
+    e = scratch_alloc(dev, reinterpret_cast<void **>(&base), total, stream);
     if (e != cudaSuccess) return e;
     a.part_idx = reinterpret_cast<int64_t *>(base);
     a.part_d2 = reinterpret_cast<float *>(base + off_d2);
@@ -490,7 +490,7 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
         bq_merge_parts_kernel<<<gm, 32 * BQ_MERGE_WARPS, 0, stream>>>(a, int(P));
         e = cudaGetLastError();
     }
-    const cudaError_t f = cudaFreeAsync(base, stream);
+    const cudaError_t f = scratch_free(base, stream);
     return e != cudaSuccess ? e : f;
 }
 

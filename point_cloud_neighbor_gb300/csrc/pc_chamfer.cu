@@ -212,15 +212,15 @@ extern "C" int pc_chamfer(const float *x, int64_t B, int64_t P1,
         } else {
             // the clouds' losses in stream-ordered scratch, then their sum
             double *cl = nullptr;
-            e = cudaMallocAsync(reinterpret_cast<void **>(&cl),
-                                size_t(B > 0 ? B : 1) * sizeof(double), st);
+            e = pcn::scratch_alloc(*dev, reinterpret_cast<void **>(&cl),
+                                   size_t(B > 0 ? B : 1) * sizeof(double), st);
             if (e == cudaSuccess) {
                 a.cloud_loss = cl;
                 if (B > 0)
                     pcn::chamfer_reduce_kernel<<<unsigned(B), pcn::RED_THREADS, 0, st>>>(a);
                 pcn::chamfer_batch_kernel<<<1, pcn::RED_THREADS, 0, st>>>(a);
                 e = cudaGetLastError();
-                const cudaError_t f = cudaFreeAsync(cl, st);
+                const cudaError_t f = pcn::scratch_free(cl, st);
                 if (e == cudaSuccess) e = f;
             }
         }

@@ -20,7 +20,19 @@ struct DeviceInfo {
     int max_threads_per_sm = 0;
     int cooperative = 0;
     int *status_word = nullptr;  // device address of the status word
+    // the library's stream-ordered pool for kernel scratch (nullptr: the
+    // device's default pool)
+    cudaMemPool_t scratch_pool = nullptr;
 };
+
+// Scratch memory for the library's own kernels, stream-ordered on `stream`:
+// from the device's library pool, which keeps up to 256 MiB reserved
+// between calls (the default pool returns freed memory at every
+// synchronization, so a caller that synchronizes after each call would pay
+// for mapping it again on every call).
+cudaError_t scratch_alloc(const DeviceInfo &dev, void **p, size_t bytes,
+                          cudaStream_t stream);
+cudaError_t scratch_free(void *p, cudaStream_t stream);
 
 // Device-side wait bound, in ns (see pc_set_wait_timeout_ns).
 uint64_t wait_timeout_ns();

@@ -467,7 +467,7 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
         const size_t start_bytes = (size_t(B) * (size_t(M) + 1) * sizeof(int) + 15) & ~size_t(15);
         const size_t bytes = start_bytes + size_t(B) * E * sizeof(int2);
         void *scratch = nullptr;
-        cudaError_t e = cudaMallocAsync(&scratch, bytes, st);
+        cudaError_t e = pcn::scratch_alloc(*dev, &scratch, bytes, st);
         if (e != cudaSuccess) return cuda_err(e, "three_interpolate_backward: scratch");
         int *start = static_cast<int *>(scratch);
         int2 *list = reinterpret_cast<int2 *>(static_cast<char *>(scratch) + start_bytes);
@@ -500,7 +500,7 @@ extern "C" int pc_three_interpolate_backward(const float *grad_out, int64_t B,
                 grad_out, start, list, int(C), int(M), int(n), grad_features);
             e = cudaGetLastError();
         }
-        const cudaError_t ef = cudaFreeAsync(scratch, st);
+        const cudaError_t ef = pcn::scratch_free(scratch, st);
         if (e == cudaSuccess) e = ef;
         return e == cudaSuccess ? PC_OK : cuda_err(e, "three_interpolate_backward");
     }

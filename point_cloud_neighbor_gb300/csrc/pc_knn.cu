@@ -1252,7 +1252,7 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
                   ~size_t(255));
     const size_t total = off_seed + size_t(B) * a.Q * size_t(a.k) * 8;
     char *base = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&base), total, stream);
+    cudaError_t e = scratch_alloc(dev, reinterpret_cast<void **>(&base), total, stream);
     if (e != cudaSuccess) return e;
     float *frame = reinterpret_cast<float *>(base + off_frame);
     int *hist = reinterpret_cast<int *>(base + off_hist);
@@ -1309,7 +1309,7 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
             e = cudaGetLastError();
         }
     }
-    const cudaError_t f = cudaFreeAsync(base, stream);
+    const cudaError_t f = scratch_free(base, stream);
     return e != cudaSuccess ? e : f;
 }
 
