@@ -41,6 +41,9 @@
 #include "pc_internal.h"
 
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 namespace pcn {
 namespace {
@@ -775,10 +778,35 @@ FpsPlan plan_cgrid(const DeviceInfo &dev, int64_t B, int64_t N, int cs, int bpc_
     return p;
 }
 
+FpsPlan plan_fps_uncached(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
+                          int cluster_size, int blocks_per_cloud);
+
 }  // namespace
 
+// Plans depend only on the device and the arguments; the occupancy queries
+// behind them cost host time on every call, so they are kept (each process
+// sees few distinct shapes).
 FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
                  int cluster_size, int blocks_per_cloud) {
+    using Key = std::tuple<int, int64_t, int64_t, int, int, int>;
+    static std::mutex mu;
+    static std::map<Key, FpsPlan> cache;
+    const Key key{dev.device, B, N, strategy, cluster_size, blocks_per_cloud};
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        const auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const FpsPlan p = plan_fps_uncached(dev, B, N, strategy, cluster_size, blocks_per_cloud);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() < 4096) cache.emplace(key, p);
+    return p;
+}
+
+namespace {
+
+FpsPlan plan_fps_uncached(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
+                          int cluster_size, int blocks_per_cloud) {
     FpsPlan p;
     const int64_t cap_block = block_capacity();
     const int nsm = std::max(1, dev.sm_count);
@@ -904,6 +932,8 @@ FpsPlan plan_fps(const DeviceInfo &dev, int64_t B, int64_t N, int strategy,
     p.why = "unknown FPS strategy";
     return p;
 }
+
+}  // namespace
 
 cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
                        const float *xyz, int64_t B, int64_t N, int64_t npoint,
