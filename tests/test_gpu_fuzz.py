@@ -127,3 +127,51 @@ def test_fuzz_knn_spatially_ordered(case):
     what = f"fuzz ordered knn B={B} Q={Q} N={N} k={k} same={same} lengths={ql is not None}"
     assert_idx_equal(i.cpu().numpy().reshape(-1, k)[rows], wi, what)
     assert_dist_equal(d.cpu().numpy().reshape(-1, k)[rows], wd, what)
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_fuzz_ball_query_reference_parts(case):
+    # few queries against many references: the references split into parts
+    # (blockIdx.z) whose first-K hits are joined in order; lengths masks on
+    # half of the cases; every row against the oracle
+    rng = np.random.default_rng(8000 + case)
+    B = int(rng.integers(1, 3))
+    N = int(rng.choice([16384 + 1, 20000, 40011]))
+    Q = int(rng.choice([1, 9, 64, 200]))
+    K = int(rng.choice([1, 7, 32, 64, 100]))
+    x = cloud(rng, B, N)
+    q = cloud(rng, B, Q)
+    r = float(rng.choice([0.05, 0.2, 0.6]))
+    if case % 2 == 0:
+        d2, i = pc.pc_ball_query(to_dev(q), to_dev(x), r, K)
+        wd2, wi = oracle.ball_query(q, x, r, K, threads=THREADS)
+    else:
+        ql = rng.integers(0, Q + 1, B).astype(np.int64)
+        rl = rng.integers(0, N + 1, B).astype(np.int64)
+        d2, i = pc.pc_ball_query(to_dev(q), to_dev(x), r, K, query_lengths=to_dev(ql),
+                                 ref_lengths=to_dev(rl))
+        wd2, wi = oracle.ball_query_masked(q, x, r, K, ql, rl)
+    what = f"fuzz bq parts B={B} Q={Q} N={N} r={r} K={K} case={case}"
+    assert_idx_equal(i.cpu().numpy().reshape(-1, K), wi, what)
+    assert_dist_equal(d2.cpu().numpy().reshape(-1, K), wd2, what)
+
+
+@pytest.mark.parametrize("case", range(8))
+def test_fuzz_fps_grid_two_levels(case):
+    # the two-level grid schedule (clusters, one slot per cluster) and the
+    # one-level grid on random clouds, sizes, starts and cluster sizes
+    rng = np.random.default_rng(9000 + case)
+    B = int(rng.integers(1, 4))
+    N = int(rng.choice([3000, 5001, 12345, 40000]))
+    npoint = int(rng.choice([2, 50, 513, 1200]))
+    start = int(rng.integers(0, N))
+    cs = int(rng.choice([0, 1, 4, 8, 16]))
+    x = cloud(rng, B, N)
+    try:
+        idx = pc.pc_fps(to_dev(x), npoint, start, strategy=pc.PC_FPS_GRID,
+                        cluster_size=cs).cpu().numpy()
+    except pc.PointCloudError as e:       # a cluster size that cannot be resident
+        assert e.status == 2, e
+        pytest.skip(f"cluster size {cs} unsupported for B={B}: {e}")
+    want = oracle.fps(x, npoint, start, threads=THREADS)
+    assert_idx_equal(idx, want, f"fuzz fps grid B={B} N={N} npoint={npoint} cs={cs}")
