@@ -195,6 +195,8 @@ KERNEL_SOURCES = {
     "ball_query": ["pc_ball_query.cu", "pc_device.cuh", "pc_filter.cuh",
                    "pc_stream.cuh", "pc_tiles.cuh"],
     "fps": ["pc_fps.cu", "pc_device.cuh"],
+    "knn_ball_query": ["pc_knn.cu", "pc_device.cuh", "pc_filter.cuh", "pc_stream.cuh",
+                       "pc_tiles.cuh"],
     "grid_knn": ["pc_grid.cu", "pc_device.cuh"],
     "grid_ball_query": ["pc_grid.cu", "pc_device.cuh"],
 }
@@ -275,9 +277,13 @@ def run_gpu(args):
     # the kNN and Ball Query grids (one wave) are planned around the SMs
     # FPS holds while it runs
     reserve = 0 if args.serial else B * STEP_FPS_CLUSTER
+    # kNN and Ball Query of the same queries: one fused call (each pair
+    # filtered once for both), or with --separate pc_knn then pc_ball_query
+    fused = not args.separate
 
     def step(ev=None):
         # ev: [start, fps_end, knn_start (side), knn_end, bq_end, step_end]
+        # (fused: knn_end = bq_end, the end of the one call)
         if ev is not None:
             ev[0].record(stream)
         fork.record(stream)
@@ -290,10 +296,14 @@ def run_gpu(args):
             if ev is not None:
                 ev[2].record(side)
             pc.pc_set_sm_reserve(reserve)
-            pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
+            if fused:
+                pc.pc_knn_ball_query(x, x, k, r, K, out=(knn_d, knn_i, bq_d, bq_i))
+            else:
+                pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i)
             if ev is not None:
                 ev[3].record(side)
-            pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
+            if not fused:
+                pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i)
             pc.pc_set_sm_reserve(0)
             if ev is not None:
                 ev[4].record(side)
@@ -322,7 +332,7 @@ def run_gpu(args):
     # kernels of one step: FPS 1; kNN on this cloud (spatially ordered: the
     # query set is the reference set) frame, count, chunk sums, scan,
     # scatter, seed and the lane kernel = 7 (plus a memset of the cell
-    # counts); Ball Query 1
+    # counts); Ball Query 1 (fused: the kernel that sorts its hits into rows)
     launches = (1 + 7 + 1) * args.steps
 
     # each operator timed on the stream it runs on
@@ -351,10 +361,22 @@ def run_gpu(args):
     max_mhz = float(peaks.get("sm_max_mhz", 2070.0))
     alu_peak = fp32_alu_peak_tflops(sm_count, max_mhz)
 
-    per = {
-        "fps": fps_ms / args.steps, "knn": knn_ms / args.steps,
-        "ball_query": bq_ms / args.steps,
-    }
+    if fused:
+        per = {"fps": fps_ms / args.steps, "knn_ball_query": (knn_ms + bq_ms) / args.steps}
+        # each operator alone, outside the timed step, on the SMs FPS leaves
+        # (context: the separate kernels' fractions)
+        pc.pc_set_sm_reserve(reserve)
+        try:
+            per["knn"] = _timed(lambda: pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i),
+                                5, 3, flush, stream)
+            per["ball_query"] = _timed(
+                lambda: pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i),
+                5, 3, flush, stream)
+        finally:
+            pc.pc_set_sm_reserve(0)
+    else:
+        per = {"fps": fps_ms / args.steps, "knn": knn_ms / args.steps,
+               "ball_query": bq_ms / args.steps}
     ops = {
         "fps": {
             "samples_per_s": npoint * world / (per["fps"] / 1e3),
@@ -375,6 +397,18 @@ def run_gpu(args):
             "achieved_tflops": bq_pairs * FLOPS_PER_PAIR / (per["ball_query"] / 1e3) / 1e12,
         },
     }
+    if fused:
+        for op in ("knn", "ball_query"):
+            ops[op]["timed"] = "alone on the SMs FPS leaves, outside the timed step"
+        ops["knn_ball_query"] = {
+            "queries_per_s": 2 * N * world / (per["knn_ball_query"] / 1e3),
+            "ms": per["knn_ball_query"], "pairs": knn_pairs,
+            "achieved_tflops": knn_pairs * FLOPS_PER_PAIR /
+            (per["knn_ball_query"] / 1e3) / 1e12,
+            "note": "one pass filters every (query, reference) pair once for both "
+                    "operators; its algorithmic work is the kNN's N^2 pairs, which "
+                    "contain the Ball Query's first-K scan",
+        }
     # FPS against its two other bounds: ~10 instructions per point-step on the
     # SMs its schedule uses, and the per-step exchange floor measured with the
     # same cluster schedule on 1024 points per block
@@ -396,7 +430,7 @@ def run_gpu(args):
         except pc.PointCloudError as err:
             ops["fps"]["sync_floor_ms"] = None
             ops["fps"]["sync_floor_note"] = f"not measured: {err}"
-    for op in ("knn", "ball_query"):
+    for op in ("knn", "ball_query") + (("knn_ball_query",) if fused else ()):
         ops[op]["alu_frac_max_clock"] = ops[op]["achieved_tflops"] / alu_peak
         if clk["sm_mhz"]:
             ops[op]["alu_frac_load_clock"] = (
@@ -430,14 +464,21 @@ def run_gpu(args):
     # The dominant kernel is the largest one on the step's critical path: with
     # FPS overlapped (it runs concurrently and ends first), kNN or Ball Query;
     # serially, the largest of the three.
-    overlapped = (not args.serial) and per["fps"] <= per["knn"] + per["ball_query"]
-    candidates = ("knn", "ball_query") if overlapped else ("fps", "knn", "ball_query")
+    side_ops = ("knn_ball_query",) if fused else ("knn", "ball_query")
+    side_ms = sum(per[op] for op in side_ops)
+    if args.serial:
+        candidates, why = ("fps",) + side_ops, "largest kernel of the serial step"
+    elif per["fps"] <= side_ms:
+        candidates, why = side_ops, ("largest kernel on the step's critical path; "
+                                     "FPS runs concurrently with kNN + Ball Query")
+    else:
+        candidates, why = ("fps",), ("FPS, concurrent with kNN + Ball Query on the "
+                                     "other SMs, ends last: the step's critical path")
     dominant = max(candidates, key=per.get)
     roof = roof_of(dominant)
-    roof["note"] = ("largest kernel on the step's critical path; FPS runs "
-                    "concurrently with kNN + Ball Query" if overlapped else
-                    "largest kernel of the serial step")
-    roof_all = {op: roof_of(op) for op in ("fps", "knn", "ball_query")}
+    roof["note"] = why
+    roof_all = {op: roof_of(op) for op in ("fps", "knn", "ball_query") + side_ops
+                if op in per}
 
     grid = next_rows = configs = None
     if not args.step_only:
@@ -456,7 +497,9 @@ def run_gpu(args):
         "dtype": "f32", "data": "synthetic",
         "config": workload_config({"parallelism": f"replicas x{world}",
                                    "streams": ("1 (serial)" if args.serial else
-                                               "2: FPS concurrent with kNN then Ball Query"),
+                                               "2: FPS concurrent with kNN and Ball Query"),
+                                   "knn_ball_query": ("one fused call" if fused else
+                                                      "pc_knn then pc_ball_query"),
                                    "fps_cluster": STEP_FPS_CLUSTER}),
         "roofline": roof, "roofline_per_kernel": roof_all, "ops": ops,
         "grid": grid, "next_rows": next_rows, "configs": configs,
@@ -943,7 +986,9 @@ def run_configs(args, pc, flush, device, world, with_oracle):
 def run_e2e(args, pc, x_host, device, world, bq_first=True):
     """Same step through the public API with host buffers: the input is copied
     from pinned host memory each step and every result is read back into
-    pinned host memory; wall time around each synchronized step.  With
+    pinned host memory; wall time around each synchronized step.  Fused, the
+    kNN and Ball Query results are read back on a copy stream as soon as
+    their call ends, while FPS may still run.  Separate (--separate), with
     bq_first the side stream runs Ball Query before kNN, so that the larger
     read-back (Ball Query's K = 32 slots per query) overlaps kNN and only
     kNN's follows the last kernel."""
@@ -969,7 +1014,27 @@ def run_e2e(args, pc, x_host, device, world, bq_first=True):
     copy = torch.cuda.Stream(device) if not args.serial else main
     reserve = 0 if args.serial else STEP_FPS_CLUSTER
 
+    def one_fused():
+        xd = x_pin.to(device, non_blocking=True)
+        side.wait_stream(main)
+        f = pc.pc_fps(xd, npoint, 0, strategy=pc.PC_FPS_CLUSTER,
+                      cluster_size=STEP_FPS_CLUSTER)
+        outs["fps"].copy_(f, non_blocking=True)
+        with torch.cuda.stream(side):
+            pc.pc_set_sm_reserve(reserve)
+            res = pc.pc_knn_ball_query(xd, xd, k, r, K)
+            pc.pc_set_sm_reserve(0)
+        copy.wait_stream(side)
+        with torch.cuda.stream(copy):
+            for t, name in zip(res, ("knn_d", "knn_i", "bq_d", "bq_i")):
+                t.record_stream(copy)
+                outs[name].copy_(t, non_blocking=True)
+        torch.cuda.synchronize(device)
+
     def one():
+        if not args.separate:
+            one_fused()
+            return
         xd = x_pin.to(device, non_blocking=True)
         side.wait_stream(main)
         f = pc.pc_fps(xd, npoint, 0, strategy=pc.PC_FPS_CLUSTER,
@@ -1009,7 +1074,8 @@ def run_e2e(args, pc, x_host, device, world, bq_first=True):
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": elapsed / steps * 1e3,
-            "note": "pinned host input copied in and all outputs read back every step"}
+            "note": "pinned host input copied in and all outputs read back every step",
+            "knn_ball_query": "pc_knn then pc_ball_query" if args.separate else "one fused call"}
 
 
 # ---------------------------------------------------------------------------
@@ -1159,6 +1225,9 @@ def main():
     ap.add_argument("--step-only", action="store_true",
                     help="time only the FPS + kNN + Ball Query step (no grid, "
                          "next-row or end-to-end sections; for profiler captures)")
+    ap.add_argument("--separate", action="store_true",
+                    help="run kNN and Ball Query of the step as two calls "
+                         "(pc_knn, pc_ball_query) instead of one fused call")
     ap.add_argument("--serial", action="store_true",
                     help="run FPS, kNN and Ball Query one after another on one "
                          "stream instead of FPS concurrently on a side stream")

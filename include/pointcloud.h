@@ -278,6 +278,50 @@ int pc_ball_query_ex(const float *query, int64_t B, int64_t Q,
                      float *out_dist2, int64_t *out_idx, void *stream);
 
 /*
+ * kNN and Ball Query of the same queries against the same references in one
+ * call: the results of pc_knn(query, ref, k) and pc_ball_query(query, ref,
+ * radius, K), bit for bit (project page, "k nearest neighbors" and "Ball
+ * Query: first K within a radius"; "Numerical contracts").  A
+ * set-abstraction layer asks both of one cloud; both read every (query,
+ * reference) pair's squared distance, and here each pair is filtered and,
+ * where it may matter to either, computed once.
+ *
+ *   query      [B, Q, 3] float32, device.  ref [B, N, 3] float32, device.
+ *   k          1 <= k <= N, k <= 256.  knn_dist / knn_idx [B, Q, k]: as
+ *              pc_knn's out_dist (Euclidean) / out_idx.
+ *   radius     finite and > 0; K >= 1.  bq_dist2 / bq_idx [B, Q, K]: as
+ *              pc_ball_query's out_dist2 / out_idx.
+ *
+ * One fused pass runs where pc_knn_ball_query_plan says so: 2 <= k <= 32,
+ * K <= 64, at least 16,384 references and 4,096 queries per cloud, B <= 64,
+ * R2 = fl32(fl32(r)^2) > 0, and the references are not split into parts
+ * (enough queries to fill the GPU).  Otherwise the call runs pc_knn's and
+ * pc_ball_query's kernels one after the other.  The fused pass takes
+ * pc_knn's ordered-path scratch plus B * Q * (8 K + 16) bytes from the
+ * library's stream-ordered scratch pool on `stream`; an allocation failure
+ * returns PC_ERR_CUDA.  A wait that runs out (PC_ERR_DEVICE_TIMEOUT in the
+ * status word, pc_device_status) leaves the stopped queries' rows of both
+ * outputs at index -1 (kNN distances unspecified there, as pc_knn; Ball
+ * Query distances 0).
+ *
+ * Returns PC_OK, PC_ERR_INVALID_ARGUMENT, PC_ERR_UNSUPPORTED, PC_ERR_CUDA or
+ * PC_ERR_NO_DEVICE.
+ */
+int pc_knn_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
+                      int64_t N, int64_t k, float *knn_dist, int64_t *knn_idx,
+                      double radius, int64_t K, float *bq_dist2, int64_t *bq_idx,
+                      void *stream);
+
+/*
+ * Whether pc_knn_ball_query with these sizes runs the fused pass on the
+ * current device: *out_fused = 1 (fused) or 0 (pc_knn's and pc_ball_query's
+ * kernels).  Arguments are checked as by pc_knn_ball_query.  Returns PC_OK,
+ * PC_ERR_INVALID_ARGUMENT, PC_ERR_UNSUPPORTED or PC_ERR_NO_DEVICE.
+ */
+int pc_knn_ball_query_plan(int64_t B, int64_t Q, int64_t N, int64_t k, double radius,
+                           int64_t K, int *out_fused);
+
+/*
  * Exact grid-accelerated kNN and Ball Query.
  * mps-pointops project page, "Roadmap" (Phase 4: spatial acceleration
  * structures, a uniform grid or BVH, for large clouds): the same operators

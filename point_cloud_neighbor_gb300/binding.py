@@ -56,6 +56,10 @@ _SIGNATURES = {
                                           _I, _P, _P, _P]),
     "pc_ball_query": (ctypes.c_int, [_P, _I, _I, _P, _I, ctypes.c_double, _I,
                                      _P, _P, _P]),
+    "pc_knn_ball_query": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _P, _P,
+                                         ctypes.c_double, _I, _P, _P, _P]),
+    "pc_knn_ball_query_plan": (ctypes.c_int, [_I, _I, _I, _I, ctypes.c_double,
+                                              _I, ctypes.POINTER(ctypes.c_int)]),
     "pc_knn_ex": (ctypes.c_int, [_P, _I, _I, _P, _I, _I, _P, _P, ctypes.c_int,
                                  _P, _P, _P]),
     "pc_ball_query_ex": (ctypes.c_int, [_P, _I, _I, _P, _I, _P, _P,
@@ -273,6 +277,58 @@ def pc_ball_query(query: torch.Tensor, ref: torch.Tensor, radius: float,
                                     out_idx.data_ptr(), _stream_ptr(query.device))
     _raise_on(st, "pc_ball_query")
     return out_dist2, out_idx
+
+
+def pc_knn_ball_query(query: torch.Tensor, ref: torch.Tensor, k: int,
+                      radius: float, K: int, *,
+                      out: tuple | None = None):
+    """kNN and first-K Ball Query of the same queries against the same
+    references in one call: returns (knn_dist [B,Q,k], knn_idx [B,Q,k],
+    bq_dist2 [B,Q,K], bq_idx [B,Q,K]), identical to :func:`pc_knn` and
+    :func:`pc_ball_query`.  ``out`` may hold those four tensors."""
+    _check_cloud(query, "query")
+    _check_cloud(ref, "ref")
+    B, Q, _ = query.shape
+    if ref.shape[0] != B:
+        raise ValueError("query and ref must have the same batch size")
+    if ref.device != query.device:
+        raise ValueError("query and ref must be on the same device")
+    N = ref.shape[1]
+    L = lib()
+    with torch.cuda.device(query.device):
+        if out is None:
+            dev = query.device
+            out = (torch.empty((B, Q, k), dtype=torch.float32, device=dev),
+                   torch.empty((B, Q, k), dtype=torch.int64, device=dev),
+                   torch.empty((B, Q, K), dtype=torch.float32, device=dev),
+                   torch.empty((B, Q, K), dtype=torch.int64, device=dev))
+        kd, ki, bd, bi = out
+        for t, shape, dt, name in ((kd, (B, Q, k), torch.float32, "knn_dist"),
+                                   (ki, (B, Q, k), torch.int64, "knn_idx"),
+                                   (bd, (B, Q, K), torch.float32, "bq_dist2"),
+                                   (bi, (B, Q, K), torch.int64, "bq_idx")):
+            if (tuple(t.shape) != shape or t.dtype != dt or
+                    t.device != query.device or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous {dt} tensor of "
+                                 f"shape {shape} on {query.device}")
+        st = L.pc_knn_ball_query(query.data_ptr(), B, Q,
+                                 ref.data_ptr() if N > 0 else None, N, k,
+                                 kd.data_ptr(), ki.data_ptr(), float(radius), K,
+                                 bd.data_ptr(), bi.data_ptr(),
+                                 _stream_ptr(query.device))
+    _raise_on(st, "pc_knn_ball_query")
+    return kd, ki, bd, bi
+
+
+def pc_knn_ball_query_plan(B: int, Q: int, N: int, k: int, radius: float,
+                           K: int) -> bool:
+    """Whether :func:`pc_knn_ball_query` runs its fused pass for these sizes
+    on the current device."""
+    fused = ctypes.c_int(0)
+    st = lib().pc_knn_ball_query_plan(B, Q, N, k, float(radius), K,
+                                      ctypes.byref(fused))
+    _raise_on(st, "pc_knn_ball_query_plan")
+    return bool(fused.value)
 
 
 class PointGrid:

@@ -424,6 +424,70 @@ int pc_ball_query_ex(const float *query, int64_t B, int64_t Q,
                      ref_lengths, radius, K, out_dist2, out_idx, stream);
 }
 
+// kNN and Ball Query of one query set against one reference set: the checks
+// of pc_knn and pc_ball_query together.
+static int knn_bq_check(const char *name, int64_t B, int64_t Q, int64_t N, int64_t k,
+                        double radius, int64_t K) {
+    if (B < 0 || Q < 0 || N < 0)
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s: negative size", name);
+    if (k < 1 || k > N)
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "%s: need 1 <= k <= N (got k=%lld, N=%lld)", name, (long long)k,
+                    (long long)N);
+    if (!std::isfinite(radius) || !(radius > 0.0))
+        return fail(PC_ERR_INVALID_ARGUMENT,
+                    "%s: radius must be finite and > 0 (got %g)", name, radius);
+    if (K < 1)
+        return fail(PC_ERR_INVALID_ARGUMENT, "%s: need K >= 1 (got %lld)", name,
+                    (long long)K);
+    if (k > 256)
+        return fail(PC_ERR_UNSUPPORTED, "%s: k=%lld above the maximum 256", name,
+                    (long long)k);
+    if (B > 65535)
+        return fail(PC_ERR_UNSUPPORTED, "%s: B=%lld above 65535", name, (long long)B);
+    if (Q > kMaxInt || N > kMaxInt || K > kMaxInt || !mul_ok(B, Q, k) ||
+        !mul_ok(B, Q, K) || !mul_ok(B, N, 3) || !mul_ok(B, Q, 3))
+        return fail(PC_ERR_UNSUPPORTED, "%s: sizes beyond 32-bit indexing", name);
+    return PC_OK;
+}
+
+int pc_knn_ball_query(const float *query, int64_t B, int64_t Q, const float *ref,
+                      int64_t N, int64_t k, float *knn_dist, int64_t *knn_idx,
+                      double radius, int64_t K, float *bq_dist2, int64_t *bq_idx,
+                      void *stream) {
+    int rc = knn_bq_check("knn_ball_query", B, Q, N, k, radius, K);
+    if (rc != PC_OK) return rc;
+    if (B == 0 || Q == 0) return PC_OK;
+    const pcn::DeviceInfo *dev = nullptr;
+    if ((rc = current_device(&dev)) != PC_OK) return rc;
+    if ((rc = check_ptr(query, dev->device, 4, "query")) != PC_OK) return rc;
+    if ((rc = check_ptr(ref, dev->device, 4, "ref")) != PC_OK) return rc;
+    if ((rc = check_ptr(knn_dist, dev->device, 4, "knn_dist")) != PC_OK) return rc;
+    if ((rc = check_ptr(knn_idx, dev->device, 8, "knn_idx")) != PC_OK) return rc;
+    if ((rc = check_ptr(bq_dist2, dev->device, 4, "bq_dist2")) != PC_OK) return rc;
+    if ((rc = check_ptr(bq_idx, dev->device, 8, "bq_idx")) != PC_OK) return rc;
+    const cudaError_t e = pcn::launch_knn_ball_query(
+        *dev, query, B, Q, ref, N, int(k), knn_dist, knn_idx, static_cast<float>(radius),
+        K, bq_dist2, bq_idx, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "knn_ball_query: launch");
+    return PC_OK;
+}
+
+int pc_knn_ball_query_plan(int64_t B, int64_t Q, int64_t N, int64_t k, double radius,
+                           int64_t K, int *out_fused) {
+    if (out_fused == nullptr)
+        return fail(PC_ERR_INVALID_ARGUMENT, "knn_ball_query_plan: out_fused is NULL");
+    *out_fused = 0;
+    int rc = knn_bq_check("knn_ball_query_plan", B, Q, N, k, radius, K);
+    if (rc != PC_OK) return rc;
+    const pcn::DeviceInfo *dev = nullptr;
+    if ((rc = current_device(&dev)) != PC_OK) return rc;
+    *out_fused = B > 0 && Q > 0 &&
+                 pcn::knn_ball_query_fused(*dev, B, Q, N, int(k),
+                                           static_cast<float>(radius), K);
+    return PC_OK;
+}
+
 int pc_device_status(void *stream, int reset, int32_t *out_status) {
     if (out_status == nullptr)
         return fail(PC_ERR_INVALID_ARGUMENT, "device_status: out_status is NULL");

@@ -82,6 +82,16 @@ cudaError_t launch_ball_query(const DeviceInfo &dev, const float *query,
                               float *out_dist2, int64_t *out_idx,
                               cudaStream_t stream);
 
+// kNN and Ball Query of the same queries against the same references; one
+// fused launch where knn_ball_query_fused holds, else launch_knn then
+// launch_ball_query.  No lengths; kNN distances are sqrt(s).
+bool knn_ball_query_fused(const DeviceInfo &dev, int64_t B, int64_t Q, int64_t N,
+                          int k, float r32, int64_t K);
+cudaError_t launch_knn_ball_query(const DeviceInfo &dev, const float *query, int64_t B,
+                                  int64_t Q, const float *ref, int64_t N, int k,
+                                  float *knn_dist, int64_t *knn_idx, float r32, int64_t K,
+                                  float *bq_dist2, int64_t *bq_idx, cudaStream_t stream);
+
 struct FpsPlan {
     int strategy = 0;       // PC_FPS_BLOCK / CLUSTER / GRID
     int cluster = 1;        // blocks per cluster (BLOCK: 1)

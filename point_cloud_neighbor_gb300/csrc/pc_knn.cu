@@ -87,7 +87,47 @@ struct KnnArgs {
     // ORDERED: per query (in the query order) the exact k best keys over its
     // seeded tile, as a max-heap [B][Q][k] (knn_seed_kernel)
     const unsigned long long *seed;
+    // ORDERED, Ball Query fused in (bq_rows != NULL; one part): per query
+    // (in the query order) the bq_K smallest indices j with s32 < bq_R2 seen
+    // so far, as (j, s32 bits) in bq_rows [B][Q][bq_K] in no order, and its
+    // state in bq_state [B][Q]: (hits seen, largest kept j, its slot, -) --
+    // hits -1 when the query's search stopped on a timeout.
+    // knn_bq_finish_kernel sorts each row by j into bq_out_*.
+    int2 *bq_rows;
+    int4 *bq_state;
+    float bq_R2;
+    int bq_K;
+    float *bq_out_d2;
+    int64_t *bq_out_idx;
 };
+
+// A Ball Query hit (j, s) of a query whose bq_K slots are `row`: the slots
+// keep the K smallest indices among all hits seen, in no order; (hits,
+// maxj, maxpos) is the query's state (hits seen, largest kept index, its
+// slot).  Once K slots are full, a smaller index replaces the largest and the
+// slots are scanned for the new largest (a query has that many hits only
+// where the cloud is dense).
+__device__ __forceinline__ void bq_keep(int2 *row, int K, int &hits, int &maxj,
+                                        int &maxpos, int j, float s) {
+    if (hits < K) {
+        row[hits] = make_int2(j, __float_as_int(s));
+        if (j > maxj) {
+            maxj = j;
+            maxpos = hits;
+        }
+    } else if (j < maxj) {
+        row[maxpos] = make_int2(j, __float_as_int(s));
+        maxj = -1;
+        for (int e = 0; e < K; ++e) {
+            const int je = row[e].x;
+            if (je > maxj) {
+                maxj = je;
+                maxpos = e;
+            }
+        }
+    }
+    ++hits;
+}
 
 // Cell codes of the spatial order: MC_BITS bits per axis, interleaved
 // (Morton order), so that a run of consecutive cells is a compact block.
@@ -617,6 +657,10 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
         const int rem = m - 2 * mm;
         return R > L ? o + mm + rem : o - 1 - mm - rem;
     };
+    // Ball Query fused in: this tile's hits (the lane kernel skips the tile)
+    const bool bq = a.bq_rows != nullptr;
+    int2 *bq_row = bq ? a.bq_rows + (size_t(b) * a.Q + i) * a.bq_K : nullptr;
+    int bq_hits = 0, bq_maxj = -1, bq_maxpos = 0;
     int m = 0;
     // SEED_UNROLL references at a time: their loads and distances are
     // independent
@@ -625,8 +669,11 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
 #pragma unroll
         for (int u = 0; u < SEED_UNROLL; ++u) {
             const float4 r = rp[ref_at(m + u)];
+            const float s = sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z);
             // s32 >= +0; a NaN s32 has a key above KEY_EMPTY: never taken
-            key[u] = sj_key(sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z), __float_as_int(r.w));
+            key[u] = sj_key(s, __float_as_int(r.w));
+            if (bq && s < a.bq_R2)
+                bq_keep(bq_row, a.bq_K, bq_hits, bq_maxj, bq_maxpos, __float_as_int(r.w), s);
         }
 #pragma unroll
         for (int u = 0; u < SEED_UNROLL; ++u)
@@ -634,12 +681,15 @@ __global__ void __launch_bounds__(SEED_THREADS) knn_seed_kernel(const KnnArgs a,
     }
     for (; m < cnt; ++m) {
         const float4 r = rp[ref_at(m)];
-        const unsigned long long key =
-            sj_key(sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z), __float_as_int(r.w));
+        const float s = sqdist(qv.x, qv.y, qv.z, r.x, r.y, r.z);
+        const unsigned long long key = sj_key(s, __float_as_int(r.w));
+        if (bq && s < a.bq_R2)
+            bq_keep(bq_row, a.bq_K, bq_hits, bq_maxj, bq_maxpos, __float_as_int(r.w), s);
         if (key < root) root = heap_sift(h, k, 0, key);
     }
     unsigned long long *out = seed + (size_t(b) * a.Q + i) * k;
     for (int e = 0; e < k; ++e) out[e] = h[e * 32];
+    if (bq) a.bq_state[size_t(b) * a.Q + i] = make_int4(bq_hits, bq_maxj, bq_maxpos, 0);
 }
 
 // Pass 1 over one prepared tile for the first NQ query slots of a lane: per
@@ -698,9 +748,16 @@ __device__ __forceinline__ void lane_pass1(const float4 *ck, int nsteps,
 // one unit: it runs the tile loop for one query per lane, pass 1 at about
 // half the cost, so the launch can balance the SMs to half a warp.  Keys
 // carry the original indices, so the result is that of the input order.
-template <int KL_QL, bool ORDERED>
+//
+// BQ (ORDERED, one part): Ball Query of the same queries and references in
+// the same pass.  Its filter bound is R2, so a query's threshold is the
+// larger of its kNN bound and R2's; in pass 2 every exact s32 goes to both
+// rules (heap insertion for kNN, s32 < R2 for Ball Query, whose hits are
+// kept with bq_keep from the state left by knn_seed_kernel).
+template <int KL_QL, bool ORDERED, bool BQ = false>
 __global__ void __launch_bounds__(32 * (kl_wmax(KL_QL) + 1), 1)
 knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
+    static_assert(ORDERED || !BQ, "Ball Query is fused into the ordered kernel only");
     constexpr int GQ = 32 * KL_QL;  // queries per group (warp)
     // cooked-tile swizzle bits and steps per hot-loop iteration: 3 and 8 for
     // one query per lane, 2 and 4 for two (registers)
@@ -719,6 +776,11 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
     int *s_err = flags;
     unsigned long long *hk_all =
         reinterpret_cast<unsigned long long *>(smem + stream_smem_bytes());
+    // BQ: per query slot its Ball Query state (hits, largest kept j, its
+    // slot), after the heaps
+    int4 *bq_st = reinterpret_cast<int4 *>(
+        smem + stream_smem_bytes() +
+        size_t(blockDim.x / 32 - 1) * 32 * KL_QL * size_t(k) * 8);
 
     const float *cref = ORDERED ? a.sref + size_t(b) * size_t(a.N) * 4
                                 : a.ref + size_t(b) * size_t(a.N) * 3;
@@ -871,6 +933,12 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
         }
         thr0[q] = valid[q] ? filter_threshold(tau0, qq[q]) : -inf;
         thr[q] = thr0[q];
+        if constexpr (BQ) {
+            if (valid[q]) {
+                bq_st[(warp * KL_QL + q) * 32 + lane] = a.bq_state[size_t(b) * a.Q + qi[q]];
+                thr[q] = fmaxf(thr0[q], filter_threshold(a.bq_R2, qq[q]));
+            }
+        }
     }
 
     // The tile loop for the first NQ query slots of each lane; returns true
@@ -929,9 +997,21 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
                             sj_key(sv, ORDERED ? __float_as_int(P.w) : j0 + i);
                         if (key < tk[q]) {
                             tk[q] = heap_sift(hk, k, 0, key);
-                            if (key_j(tk[q]) != INT_MAX)
+                            if (key_j(tk[q]) != INT_MAX) {
                                 thr[q] = fminf(thr0[q],
                                                filter_threshold(key_s(tk[q]), qq[q]));
+                                if constexpr (BQ)
+                                    thr[q] = fmaxf(thr[q], filter_threshold(a.bq_R2, qq[q]));
+                            }
+                        }
+                        if constexpr (BQ) {
+                            if (sv < a.bq_R2) {
+                                int4 &st = bq_st[(warp * KL_QL + q) * 32 + lane];
+                                int hits = st.x, maxj = st.y, maxpos = st.z;
+                                bq_keep(a.bq_rows + (size_t(b) * a.Q + query_pos(q)) * a.bq_K,
+                                        a.bq_K, hits, maxj, maxpos, __float_as_int(P.w), sv);
+                                st = make_int4(hits, maxj, maxpos, 0);
+                            }
                         }
                     }
                 }
@@ -963,6 +1043,11 @@ knn_lane_kernel(const KnnArgs a0, const KnnArgs a1, int B0, int upb) {
         const float4 *sq = reinterpret_cast<const float4 *>(a.squery);
         const int orow = ORDERED ? __float_as_int(sq[size_t(b) * a.Q + qp].w) : qp;
         const size_t row = size_t(b) * a.Q + orow;
+        if constexpr (BQ) {  // the state for knn_bq_finish_kernel
+            int4 st = bq_st[(warp * KL_QL + q) * 32 + lane];
+            if (failed) st.x = -1;
+            a.bq_state[size_t(b) * a.Q + qp] = st;
+        }
         if (failed) {
             if (ORDERED && nparts > 1) {
                 unsigned long long *pk =
@@ -1036,7 +1121,49 @@ __global__ void __launch_bounds__(256) knn_merge_parts_kernel(const KnnArgs a, i
     }
 }
 
-template <int QL, bool ORDERED = false>
+// Ball Query fused into the ordered lane kNN: a query's kept hits (the bq_K
+// smallest indices with s32 < R2, in no order) sorted by index into its
+// output row, (-1, 0) in the slots after them; a query whose search stopped
+// on a timeout gets (-1, 0) throughout.  One warp per query (in the query
+// order), at most 64 hits: a hit's place is the number of kept indices
+// below its own (the indices are distinct).
+constexpr int BQ_FUSE_MAX_K = 64;
+
+__global__ void __launch_bounds__(256) knn_bq_finish_kernel(const KnnArgs a) {
+    const int b = blockIdx.y;
+    const int qp = blockIdx.x * 8 + static_cast<int>(threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (qp >= a.Q) return;
+    const int K = a.bq_K;
+    const size_t at = size_t(b) * a.Q + qp;
+    const int4 st = a.bq_state[at];
+    const int orow = __float_as_int(reinterpret_cast<const float4 *>(a.squery)[at].w);
+    const size_t row = (size_t(b) * a.Q + orow) * K;
+    const int cnt = st.x < 0 ? 0 : min(st.x, K);
+    const int2 *src = a.bq_rows + at * K;
+    const int2 e0 = lane < cnt ? src[lane] : make_int2(INT_MAX, 0);
+    const int2 e1 = lane + 32 < cnt ? src[lane + 32] : make_int2(INT_MAX, 0);
+    int r0 = 0, r1 = 0;
+    for (int m = 0; m < cnt; ++m) {
+        const int jm = __shfl_sync(FULL, m < 32 ? e0.x : e1.x, m & 31);
+        r0 += jm < e0.x ? 1 : 0;
+        r1 += jm < e1.x ? 1 : 0;
+    }
+    if (lane < cnt) {
+        a.bq_out_idx[row + r0] = e0.x;
+        a.bq_out_d2[row + r0] = __int_as_float(e0.y);
+    }
+    if (lane + 32 < cnt) {
+        a.bq_out_idx[row + r1] = e1.x;
+        a.bq_out_d2[row + r1] = __int_as_float(e1.y);
+    }
+    for (int e = cnt + lane; e < K; e += 32) {
+        a.bq_out_idx[row + e] = -1;
+        a.bq_out_d2[row + e] = 0.0f;
+    }
+}
+
+template <int QL, bool ORDERED = false, bool BQ = false>
 cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0,
                             const KnnArgs &a1, int64_t B1, cudaStream_t stream,
                             int nparts = 1) {
@@ -1047,8 +1174,8 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
     if (total == 0) return cudaSuccess;
     const int64_t nsm = std::max(1, dev.sm_count - sm_reserve());
     // consumer warps per block: shared memory bounds it too (k * 8 bytes per
-    // query); a block per SM and wave
-    const int64_t per_warp = GQ * int64_t(a0.k) * 8;
+    // query, and 16 for the fused Ball Query's state); a block per SM and wave
+    const int64_t per_warp = GQ * (int64_t(a0.k) * 8 + (BQ ? 16 : 0));
     const int64_t wmax = std::max<int64_t>(
         1, std::min<int64_t>(kl_wmax(QL), (int64_t(dev.smem_per_block_optin) -
                                        int64_t(stream_smem_bytes())) / per_warp));
@@ -1068,14 +1195,14 @@ cudaError_t launch_knn_lane(const DeviceInfo &dev, const KnnArgs &a0, int64_t B0
         W = std::min(std::min(wmax, G), (total + nsm * waves - 1) / (nsm * waves));
         nbx = (G + W - 1) / W;
     }
-    const size_t smem = knn_lane_smem(a0.k, QL, int(W));
+    const size_t smem = knn_lane_smem(a0.k, QL, int(W)) + (BQ ? size_t(W) * GQ * 16 : 0);
     cudaError_t e = cudaFuncSetAttribute(
-        knn_lane_kernel<QL, ORDERED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        knn_lane_kernel<QL, ORDERED, BQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     dim3 grid(static_cast<unsigned>(nbx), static_cast<unsigned>(B0 + B1),
               static_cast<unsigned>(nparts));
-    knn_lane_kernel<QL, ORDERED>
+    knn_lane_kernel<QL, ORDERED, BQ>
         <<<grid, unsigned(32 * (W + 1)), smem, stream>>>(a0, a1, int(B0), int(upb));
     return cudaGetLastError();
 }
@@ -1222,11 +1349,31 @@ __global__ void __launch_bounds__(256) mc_scatter_kernel(const float *pts,
     out[size_t(b) * n + pos] = make_float4(x, y, z, __int_as_float(i));
 }
 
-// The ORDERED lane kNN: order the clouds, then one lane-kernel launch.  The
+// Parts of the ORDERED lane kNN: with few queries against many references
+// the references are split into parts (blocks of the same queries, other
+// tiles), about 10 warps per SM.
+int ordered_nparts(const DeviceInfo &dev, int64_t B, int64_t Q, int64_t N, int QL) {
+    const int64_t groups = B * ((Q + 32 * QL - 1) / (32 * QL));
+    const int64_t ntiles = (N + ST_T - 1) / ST_T;
+    const int64_t want =
+        (int64_t(std::max(1, dev.sm_count - sm_reserve())) * 10 + groups - 1) / groups;
+    return int(std::max<int64_t>(1, std::min<int64_t>({8, want, ntiles / 8})));
+}
+
+// Ball Query fused into the ORDERED lane kNN (one part, K <= 64).
+struct BqFuse {
+    float R2;
+    int K;
+    float *out_d2;
+    int64_t *out_idx;
+};
+
+// The ORDERED lane kNN: order the clouds, then one lane-kernel launch (and
+// with `fuse`, the Ball Query of the same queries in the same launch).  The
 // scratch memory is stream-ordered (allocated and freed on `stream`).
 template <int QL>
 cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, const BqFuse *fuse = nullptr) {
     const bool self = a.query == a.ref && a.Q == a.N && a.q_len == a.r_len;
     const size_t cells = size_t(B) * (MC_CELLS + 1) * sizeof(int);
     const size_t off_frame = 0;
@@ -1239,18 +1386,18 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
     const size_t off_sref =
         (off_chunk + 2 * size_t(B) * MC_CHUNKS * sizeof(int) + 255) & ~size_t(255);
     const size_t off_sq = off_sref + ((size_t(B) * a.N * 16 + 255) & ~size_t(255));
-    // few queries against many references: split the references into parts
-    // (blocks of the same queries, other tiles), about 10 warps per SM
-    const int64_t groups = B * ((int64_t(a.Q) + 32 * QL - 1) / (32 * QL));
-    const int64_t ntiles = (int64_t(a.N) + ST_T - 1) / ST_T;
-    const int64_t want =
-        (int64_t(std::max(1, dev.sm_count - sm_reserve())) * 10 + groups - 1) / groups;
-    const int nparts = int(std::max<int64_t>(1, std::min<int64_t>({8, want, ntiles / 8})));
+    const int nparts = ordered_nparts(dev, B, a.Q, a.N, QL);
+    if (fuse && (nparts != 1 || fuse->K > BQ_FUSE_MAX_K)) return cudaErrorInvalidValue;
     const size_t off_pk = off_sq + ((self ? 0 : size_t(B) * a.Q * 16 + 255) & ~size_t(255));
     const size_t off_seed =
         off_pk + ((nparts > 1 ? size_t(nparts) * B * a.Q * size_t(a.k) * 8 : 0) + 255 &
                   ~size_t(255));
-    const size_t total = off_seed + size_t(B) * a.Q * size_t(a.k) * 8;
+    // the fused Ball Query: kept hits [B][Q][K] (8 bytes each), state [B][Q]
+    const size_t off_bq_rows =
+        (off_seed + size_t(B) * a.Q * size_t(a.k) * 8 + 255) & ~size_t(255);
+    const size_t off_bq_state =
+        off_bq_rows + ((fuse ? size_t(B) * a.Q * size_t(fuse->K) * 8 : 0) + 255 & ~size_t(255));
+    const size_t total = off_bq_state + (fuse ? size_t(B) * a.Q * 16 : 0);
     char *base = nullptr;
     cudaError_t e = scratch_alloc(dev, reinterpret_cast<void **>(&base), total, stream);
     if (e != cudaSuccess) return e;
@@ -1293,6 +1440,14 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
             nparts > 1 ? reinterpret_cast<unsigned long long *>(base + off_pk) : nullptr;
         unsigned long long *seed = reinterpret_cast<unsigned long long *>(base + off_seed);
         a.seed = seed;
+        if (fuse) {
+            a.bq_rows = reinterpret_cast<int2 *>(base + off_bq_rows);
+            a.bq_state = reinterpret_cast<int4 *>(base + off_bq_state);
+            a.bq_R2 = fuse->R2;
+            a.bq_K = fuse->K;
+            a.bq_out_d2 = fuse->out_d2;
+            a.bq_out_idx = fuse->out_idx;
+        }
         const size_t seed_smem = size_t(SEED_THREADS) * size_t(a.k) * 8;
         e = cudaFuncSetAttribute(knn_seed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(seed_smem));
@@ -1302,7 +1457,14 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
                               SEED_THREADS, seed_smem, stream>>>(a, seed);
             e = cudaGetLastError();
         }
-        if (e == cudaSuccess) e = launch_knn_lane<QL, true>(dev, a, B, a, 0, stream, nparts);
+        if (e == cudaSuccess)
+            e = fuse ? launch_knn_lane<QL, true, true>(dev, a, B, a, 0, stream, 1)
+                     : launch_knn_lane<QL, true>(dev, a, B, a, 0, stream, nparts);
+        if (e == cudaSuccess && fuse) {
+            knn_bq_finish_kernel<<<dim3(unsigned((a.Q + 7) / 8), unsigned(B)), 256, 0,
+                                   stream>>>(a);
+            e = cudaGetLastError();
+        }
         if (e == cudaSuccess && nparts > 1) {
             const dim3 gm(unsigned((a.Q + 255) / 256), unsigned(B));
             knn_merge_parts_kernel<<<gm, 256, 0, stream>>>(a, int(B), nparts);
@@ -1412,6 +1574,33 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
     if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
     return launch_knn_t<8>(dev, a, B, Q, stream);
+}
+
+bool knn_ball_query_fused(const DeviceInfo &dev, int64_t B, int64_t Q, int64_t N,
+                          int k, float r32, int64_t K) {
+    const float R2 = r32 * r32;
+    const int QL = k <= 16 ? 2 : 1;
+    return k >= 2 && k <= 32 && N >= 16384 && Q >= 4096 && B <= 64 &&
+           K <= BQ_FUSE_MAX_K && R2 > 0.0f && R2 <= 3e38f &&
+           ordered_nparts(dev, B, Q, N, QL) == 1;
+}
+
+cudaError_t launch_knn_ball_query(const DeviceInfo &dev, const float *query, int64_t B,
+                                  int64_t Q, const float *ref, int64_t N, int k,
+                                  float *knn_dist, int64_t *knn_idx, float r32, int64_t K,
+                                  float *bq_dist2, int64_t *bq_idx, cudaStream_t stream) {
+    if (!knn_ball_query_fused(dev, B, Q, N, k, r32, K)) {
+        const cudaError_t e = launch_knn(dev, query, B, Q, ref, N, k, nullptr, nullptr,
+                                         false, knn_dist, knn_idx, stream);
+        if (e != cudaSuccess) return e;
+        return launch_ball_query(dev, query, B, Q, ref, N, nullptr, nullptr, r32, K,
+                                 bq_dist2, bq_idx, stream);
+    }
+    const KnnArgs a = make_knn_args(dev, query, Q, ref, N, k, nullptr, nullptr, false,
+                                    knn_dist, knn_idx);
+    const BqFuse fuse{r32 * r32, int(K), bq_dist2, bq_idx};
+    if (k <= 16) return launch_knn_ordered<2>(dev, a, B, stream, &fuse);
+    return launch_knn_ordered<1>(dev, a, B, stream, &fuse);
 }
 
 }  // namespace pcn
