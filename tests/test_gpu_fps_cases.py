@@ -1,0 +1,95 @@
+"""FPS of the BLOCK and CLUSTER schedules against the oracle on the cases
+where a per-block reduction or the exchange between blocks could go wrong.
+
+The operator (mps-pointops project page, "Farthest point sampling";
+"Contracts"): c_0 = start; each step takes the point with the largest
+minimum squared distance to the centers so far, the smallest index on an
+exact tie.  Cases: exact ties between points of different blocks
+(coordinates on a grid, duplicates) for every cluster size up to 16,
+clouds exhausted to m = 0 everywhere, coarse coordinates far from the
+origin, the 100k-point cloud on the benchmark step's 13-block cluster in
+both storage orders, and many clouds on the BLOCK schedule.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import point_cloud_neighbor_gb300 as pc
+from point_cloud_neighbor_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+THREADS = oracle.default_threads()
+
+
+@pytest.fixture(autouse=True)
+def clean_status():
+    yield
+    assert pc.pc_device_status(reset=True) == 0
+
+
+def gpu_fps(x, npoint, start=0, **kw):
+    xd = torch.from_numpy(np.ascontiguousarray(x)).to("cuda:0")
+    return pc.pc_fps(xd, npoint, start, **kw).cpu().numpy()
+
+
+def assert_idx_equal(got, want, what):
+    assert got.shape == want.shape, f"{what}: shape {got.shape} vs {want.shape}"
+    bad = int((got != want).sum())
+    assert bad == 0, f"{what}: {bad} of {got.size} indices differ"
+
+
+@pytest.mark.parametrize("strategy,cs", [
+    (pc.PC_FPS_BLOCK, 0), (pc.PC_FPS_CLUSTER, 1), (pc.PC_FPS_CLUSTER, 2),
+    (pc.PC_FPS_CLUSTER, 3), (pc.PC_FPS_CLUSTER, 8), (pc.PC_FPS_CLUSTER, 13),
+    (pc.PC_FPS_CLUSTER, 16),
+])
+def test_grid_ties_every_cluster_size(strategy, cs):
+    """Two clouds of 6,000 points on a 1/32 grid (duplicates and equal
+    distances everywhere), 700 samples from start 11."""
+    x = inputs.random_cloud(60, 2, 6000, grid=1 / 32)
+    want = oracle.fps(x, 700, 11, threads=THREADS)
+    got = gpu_fps(x, 700, 11, strategy=strategy, cluster_size=cs)
+    assert_idx_equal(got, want, f"grid ties {strategy}/{cs}")
+
+
+def test_exhausted_cloud():
+    """8,192 points at 40 distinct places (each repeated): after 40 samples
+    every minimum is 0 and the rest repeat the smallest index, 0."""
+    rng = np.random.default_rng(61)
+    places = rng.random((40, 3)).astype(np.float32)
+    x = places[rng.integers(0, 40, size=(1, 8192))]
+    want = oracle.fps(x, 120, 5, threads=THREADS)
+    got = gpu_fps(x, 120, 5, strategy=pc.PC_FPS_CLUSTER, cluster_size=4)
+    assert_idx_equal(got, want, "exhausted")
+    assert (got[0, 40:] == 0).all()
+
+
+@pytest.mark.parametrize("offset", [1e4, 1e6])
+def test_far_from_the_origin(offset):
+    """Coordinates of 1e4 and 1e6 (spacing 1/1024 and 1/16): few distinct
+    distances, many exact ties, boxes whose bound is often exactly tight."""
+    x = (inputs.random_cloud(62, 2, 12_000, lo=0.0, hi=64.0).astype(np.float64) +
+         offset).astype(np.float32)
+    want = oracle.fps(x, 900, 0, threads=THREADS)
+    got = gpu_fps(x, 900, 0)
+    assert_idx_equal(got, want, f"offset {offset:g}")
+
+
+@pytest.mark.parametrize("morton", [False, True], ids=["random", "morton"])
+def test_large_cloud_step_schedule(morton):
+    """The 100k-point cloud, 4,096 samples, on a cluster of 13 blocks (the
+    schedule of the benchmark step)."""
+    x = inputs.large(morton=morton)
+    want = oracle.fps(x, 4096, 0, threads=THREADS)
+    got = gpu_fps(x, 4096, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=13)
+    assert_idx_equal(got, want, "large, cluster 13")
+
+
+def test_many_clouds_block_schedule():
+    """96 clouds of 4,096 points (one block each: the BLOCK schedule)."""
+    x = inputs.random_cloud(63, 96, 4096)
+    want = oracle.fps(x, 256, 3, threads=THREADS)
+    got = gpu_fps(x, 256, 3, strategy=pc.PC_FPS_BLOCK)
+    assert_idx_equal(got, want, "96 clouds")
