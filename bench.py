@@ -533,6 +533,8 @@ def run_only(args):
         "fps": lambda: pc.pc_fps(x, W["npoint"], 0),
         "knn": lambda: pc.pc_knn(x, x, W["knn_k"]),
         "ball_query": lambda: pc.pc_ball_query(x, x, W["bq_radius"], W["bq_K"]),
+        "knn_ball_query": lambda: pc.pc_knn_ball_query(x, x, W["knn_k"], W["bq_radius"],
+                                                       W["bq_K"]),
         "grid_build": lambda: pc.pc_grid_build(x),
         "grid_knn": lambda: pc.pc_knn_grid(x, g, W["knn_k"]),
         "grid_ball_query": lambda: pc.pc_ball_query_grid(x, g, W["bq_radius"],
@@ -1231,7 +1233,8 @@ def main():
     ap.add_argument("--serial", action="store_true",
                     help="run FPS, kNN and Ball Query one after another on one "
                          "stream instead of FPS concurrently on a side stream")
-    ap.add_argument("--only", choices=["fps", "knn", "ball_query", "grid_build",
+    ap.add_argument("--only", choices=["fps", "knn", "ball_query", "knn_ball_query",
+                                       "grid_build",
                                        "grid_knn", "grid_ball_query", "chamfer",
                                        "three_interpolate",
                                        "three_interpolate_backward", "knn_d",
