@@ -400,14 +400,19 @@ def run_gpu(args):
     if fused:
         for op in ("knn", "ball_query"):
             ops[op]["timed"] = "alone on the SMs FPS leaves, outside the timed step"
+        t_fused = per["knn_ball_query"] / 1e3
         ops["knn_ball_query"] = {
-            "queries_per_s": 2 * N * world / (per["knn_ball_query"] / 1e3),
-            "ms": per["knn_ball_query"], "pairs": knn_pairs,
-            "achieved_tflops": knn_pairs * FLOPS_PER_PAIR /
-            (per["knn_ball_query"] / 1e3) / 1e12,
+            "queries_per_s": 2 * N * world / t_fused,
+            "ms": per["knn_ball_query"], "pairs": knn_pairs + bq_pairs,
+            # the two operators' algorithmic work (kNN: every pair; Ball
+            # Query: its first-K scan), as for the separate kernels
+            "achieved_tflops": (knn_pairs + bq_pairs) * FLOPS_PER_PAIR / t_fused / 1e12,
+            # every pair counted once: the work of the one filter pass
+            "achieved_tflops_pairs_once": knn_pairs * FLOPS_PER_PAIR / t_fused / 1e12,
             "note": "one pass filters every (query, reference) pair once for both "
-                    "operators; its algorithmic work is the kNN's N^2 pairs, which "
-                    "contain the Ball Query's first-K scan",
+                    "operators; achieved_tflops counts both operators' algorithmic "
+                    "work (kNN N^2 pairs + the Ball Query first-K scan), "
+                    "achieved_tflops_pairs_once the N^2 pairs once",
         }
     # FPS against its two other bounds: ~10 instructions per point-step on the
     # SMs its schedule uses, and the per-step exchange floor measured with the
@@ -430,6 +435,9 @@ def run_gpu(args):
         except pc.PointCloudError as err:
             ops["fps"]["sync_floor_ms"] = None
             ops["fps"]["sync_floor_note"] = f"not measured: {err}"
+    if fused:
+        ops["knn_ball_query"]["alu_frac_pairs_once"] = (
+            ops["knn_ball_query"]["achieved_tflops_pairs_once"] / alu_peak)
     for op in ("knn", "ball_query") + (("knn_ball_query",) if fused else ()):
         ops[op]["alu_frac_max_clock"] = ops[op]["achieved_tflops"] / alu_peak
         if clk["sm_mhz"]:
@@ -453,6 +461,8 @@ def run_gpu(args):
             r = {"bound": "alu", "achieved": ops[op]["achieved_tflops"],
                  "peak": alu_peak, "unit": "TFLOP/s",
                  "frac": ops[op]["achieved_tflops"] / alu_peak}
+            if "alu_frac_pairs_once" in ops[op]:
+                r["frac_pairs_once"] = ops[op]["alu_frac_pairs_once"]
         r["traffic"] = recorded_traffic(op)
         r["kernel"] = op
         r["peak_source"] = (f"FP32 CUDA cores: {sm_count} SMs x 128 x 2 flop x "
@@ -462,8 +472,8 @@ def run_gpu(args):
         return r
 
     # The dominant kernel is the largest one on the step's critical path: with
-    # FPS overlapped (it runs concurrently and ends first), kNN or Ball Query;
-    # serially, the largest of the three.
+    # FPS overlapped, the longer of FPS and the kNN + Ball Query stream;
+    # serially, the largest of all.
     side_ops = ("knn_ball_query",) if fused else ("knn", "ball_query")
     side_ms = sum(per[op] for op in side_ops)
     if args.serial:

@@ -1368,11 +1368,12 @@ struct BqFuse {
     int64_t *out_idx;
 };
 
-// The ORDERED lane kNN: order the clouds, then one lane-kernel launch (and
-// with `fuse`, the Ball Query of the same queries in the same launch).  The
-// scratch memory is stream-ordered (allocated and freed on `stream`).
+// The ORDERED lane kNN: order the clouds, then one lane-kernel launch over
+// `nparts` parts of the references (ordered_nparts; one with `fuse`, which
+// adds the Ball Query of the same queries to the same launch).  The scratch
+// memory is stream-ordered (allocated and freed on `stream`).
 template <int QL>
-cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
+cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B, int nparts,
                                cudaStream_t stream, const BqFuse *fuse = nullptr) {
     const bool self = a.query == a.ref && a.Q == a.N && a.q_len == a.r_len;
     const size_t cells = size_t(B) * (MC_CELLS + 1) * sizeof(int);
@@ -1386,7 +1387,6 @@ cudaError_t launch_knn_ordered(const DeviceInfo &dev, KnnArgs a, int64_t B,
     const size_t off_sref =
         (off_chunk + 2 * size_t(B) * MC_CHUNKS * sizeof(int) + 255) & ~size_t(255);
     const size_t off_sq = off_sref + ((size_t(B) * a.N * 16 + 255) & ~size_t(255));
-    const int nparts = ordered_nparts(dev, B, a.Q, a.N, QL);
     if (fuse && (nparts != 1 || fuse->K > BQ_FUSE_MAX_K)) return cudaErrorInvalidValue;
     const size_t off_pk = off_sq + ((self ? 0 : size_t(B) * a.Q * 16 + 255) & ~size_t(255));
     const size_t off_seed =
@@ -1567,8 +1567,10 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
         if (k <= 128) return launch_knn_t<4>(dev, a, B, Q, stream);
         return launch_knn_t<8>(dev, a, B, Q, stream);
     }
-    if (ordered && k <= 16) return launch_knn_ordered<2>(dev, a, B, stream);
-    if (ordered) return launch_knn_ordered<1>(dev, a, B, stream);
+    if (ordered && k <= 16)
+        return launch_knn_ordered<2>(dev, a, B, ordered_nparts(dev, B, Q, N, 2), stream);
+    if (ordered)
+        return launch_knn_ordered<1>(dev, a, B, ordered_nparts(dev, B, Q, N, 1), stream);
     if (k <= 16) return launch_knn_lane<2>(dev, a, B, a, 0, stream);
     if (k <= 32) return launch_knn_lane<1>(dev, a, B, a, 0, stream);
     if (k <= 64) return launch_knn_t<2>(dev, a, B, Q, stream);
@@ -1576,20 +1578,27 @@ cudaError_t launch_knn(const DeviceInfo &dev, const float *query, int64_t B,
     return launch_knn_t<8>(dev, a, B, Q, stream);
 }
 
+namespace {
+// The fused pass's conditions, given the ordered kNN's part count.
+bool fused_applies(int64_t B, int64_t Q, int64_t N, int k, float r32, int64_t K,
+                   int nparts) {
+    const float R2 = r32 * r32;
+    return k >= 2 && k <= 32 && N >= 16384 && Q >= 4096 && B <= 64 &&
+           K <= BQ_FUSE_MAX_K && R2 > 0.0f && R2 <= 3e38f && nparts == 1;
+}
+}  // namespace
+
 bool knn_ball_query_fused(const DeviceInfo &dev, int64_t B, int64_t Q, int64_t N,
                           int k, float r32, int64_t K) {
-    const float R2 = r32 * r32;
-    const int QL = k <= 16 ? 2 : 1;
-    return k >= 2 && k <= 32 && N >= 16384 && Q >= 4096 && B <= 64 &&
-           K <= BQ_FUSE_MAX_K && R2 > 0.0f && R2 <= 3e38f &&
-           ordered_nparts(dev, B, Q, N, QL) == 1;
+    return fused_applies(B, Q, N, k, r32, K, ordered_nparts(dev, B, Q, N, k <= 16 ? 2 : 1));
 }
 
 cudaError_t launch_knn_ball_query(const DeviceInfo &dev, const float *query, int64_t B,
                                   int64_t Q, const float *ref, int64_t N, int k,
                                   float *knn_dist, int64_t *knn_idx, float r32, int64_t K,
                                   float *bq_dist2, int64_t *bq_idx, cudaStream_t stream) {
-    if (!knn_ball_query_fused(dev, B, Q, N, k, r32, K)) {
+    const int nparts = ordered_nparts(dev, B, Q, N, k <= 16 ? 2 : 1);
+    if (!fused_applies(B, Q, N, k, r32, K, nparts)) {
         const cudaError_t e = launch_knn(dev, query, B, Q, ref, N, k, nullptr, nullptr,
                                          false, knn_dist, knn_idx, stream);
         if (e != cudaSuccess) return e;
@@ -1599,8 +1608,8 @@ cudaError_t launch_knn_ball_query(const DeviceInfo &dev, const float *query, int
     const KnnArgs a = make_knn_args(dev, query, Q, ref, N, k, nullptr, nullptr, false,
                                     knn_dist, knn_idx);
     const BqFuse fuse{r32 * r32, int(K), bq_dist2, bq_idx};
-    if (k <= 16) return launch_knn_ordered<2>(dev, a, B, stream, &fuse);
-    return launch_knn_ordered<1>(dev, a, B, stream, &fuse);
+    if (k <= 16) return launch_knn_ordered<2>(dev, a, B, nparts, stream, &fuse);
+    return launch_knn_ordered<1>(dev, a, B, nparts, stream, &fuse);
 }
 
 }  // namespace pcn
