@@ -260,3 +260,44 @@ def test_stopped_block_is_reported():
     assert_idx_equal(ki[rows][keep], wki[keep], "knn rows that ran")
     assert_idx_equal(bi[rows][keep], wbi[keep], "bq rows that ran")
     check_against_oracle(x, x, k, r, K, rows=rows, what="after timeout")
+
+
+def test_benchmark_step_configuration():
+    """The benchmark's step as it launches it: FPS 4096 on a 13-block
+    cluster on the main stream, the fused call on a side stream planned for
+    the SMs FPS leaves (pc_set_sm_reserve(13)), both running at once: FPS
+    and every Ball Query row equal the oracle's, kNN on sampled rows and on
+    every row against pc_knn."""
+    cfg = inputs.CONFIGS["large"]
+    x = cache.large(False)
+    k = cfg["knn_k"]
+    (r, K), = cfg["bq"]
+    xd = to_dev(x)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    fork = torch.cuda.Event()
+    fork.record(main)
+    fps = pc.pc_fps(xd, cfg["npoint"], 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=13)
+    side.wait_event(fork)
+    with torch.cuda.stream(side):
+        pc.pc_set_sm_reserve(13)
+        try:
+            kd, ki, bd, bi = pc.pc_knn_ball_query(xd, xd, k, r, K)
+        finally:
+            pc.pc_set_sm_reserve(0)
+    torch.cuda.synchronize()
+    assert_idx_equal(fps.cpu().numpy(), oracle.fps(x, cfg["npoint"], 0, threads=THREADS),
+                     "fps, 13-block cluster")
+    N = x.shape[1]
+    wbd, wbi = cache.large_ball_query(False)
+    assert_idx_equal(bi.cpu().numpy().reshape(N, K), wbi, "bq, every row")
+    assert_bits_equal(bd.cpu().numpy().reshape(N, K), wbd, "bq, every row")
+    rows = inputs.sample_rows(55, N, 2000)
+    wkd, wki = oracle.knn(x, x, k, rows=rows, threads=THREADS)
+    kd = kd.cpu().numpy().reshape(N, k)
+    ki = ki.cpu().numpy().reshape(N, k)
+    assert_idx_equal(ki[rows], wki, "knn, sampled rows")
+    assert_bits_equal(kd[rows], wkd, "knn, sampled rows")
+    sd, si = pc.pc_knn(xd, xd, k)
+    assert_idx_equal(ki, si.cpu().numpy().reshape(N, k), "knn vs pc_knn, every row")
+    assert_bits_equal(kd, sd.cpu().numpy().reshape(N, k), "knn vs pc_knn, every row")
