@@ -520,6 +520,17 @@ void pc_debug_set_fps_grid_stall(int enable);
  */
 void pc_set_sm_reserve(int sms);
 
+/*
+ * FPS of the CLUSTER schedule in rounds (default on): per exchange between
+ * the blocks of a cloud, a run of several centers is certified from each
+ * warp's listed points and the bound of its other points (project page,
+ * "Farthest point sampling": the same centers as one step at a time).
+ * pc_fps_set_batched(0) makes every exchange take one center, 1 restores
+ * the rounds; applies to launches enqueued after the call on every device.
+ * Returns the previous setting.
+ */
+int pc_fps_set_batched(int enable);
+
 /* The number of SMs an FPS launch of these sizes occupies while it runs (its
  * resident thread blocks, at most the SM count), or 0 when the sizes have no
  * schedule or there is no device.  npoint does not change it. */

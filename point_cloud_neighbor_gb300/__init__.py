@@ -16,6 +16,7 @@ from .binding import (PC_FPS_AUTO, PC_FPS_BLOCK, PC_FPS_CLUSTER, PC_FPS_GRID,
                       pc_device_status, pc_fps,
                       pc_gather_points, pc_grid_build, pc_knn, pc_knn_d,
                       pc_knn_ball_query, pc_knn_ball_query_plan,
+                      pc_fps_set_batched,
                       pc_knn_grid,
                       pc_set_wait_timeout_ns, pc_set_sm_reserve,
                       pc_fps_sm_count, pc_fps_plan, pc_three_interpolate,
@@ -32,5 +33,5 @@ __all__ = [
     "three_interpolate", "three_nn", "pc_gather_points", "pc_knn_d",
     "pc_set_sm_reserve", "pc_fps_sm_count", "pc_fps_plan", "pc_debug_set_stall",
     "PC_STALL_FPS_GRID", "PC_STALL_FPS_CLUSTER", "PC_STALL_TILE_STREAM",
-    "pc_knn_ball_query", "pc_knn_ball_query_plan",
+    "pc_knn_ball_query", "pc_knn_ball_query_plan", "pc_fps_set_batched",
 ]

@@ -79,6 +79,7 @@ _SIGNATURES = {
     "pc_debug_set_fps_grid_stall": (None, [ctypes.c_int]),
     "pc_debug_set_stall": (None, [ctypes.c_int]),
     "pc_set_sm_reserve": (None, [ctypes.c_int]),
+    "pc_fps_set_batched": (ctypes.c_int, [ctypes.c_int]),
     "pc_fps_sm_count": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]),
     "pc_fps_plan": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int,
@@ -625,6 +626,13 @@ def pc_debug_set_stall(mask: int):
     """Testing hooks that make a bounded device wait run out (PC_STALL_*
     flags; 0 restores normal operation)."""
     lib().pc_debug_set_stall(int(mask))
+
+
+def pc_fps_set_batched(enable: bool) -> bool:
+    """FPS in rounds of several centers per exchange (default) or one center
+    per exchange; returns the previous setting.  Results do not depend on
+    it."""
+    return bool(lib().pc_fps_set_batched(1 if enable else 0))
 
 
 def pc_set_sm_reserve(sms: int):

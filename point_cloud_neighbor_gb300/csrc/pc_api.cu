@@ -24,6 +24,7 @@ constexpr int kVersion = 10000 * 0 + 100 * 1 + 0;  // 0.1.0
 thread_local std::string t_error;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<int> g_sm_reserve{0};
+std::atomic<int> g_fps_batched{1};
 std::atomic<int> g_stall{0};  // PC_STALL_* testing flags
 std::mutex g_dev_mutex;
 pcn::DeviceInfo g_devices[kMaxDevices];
@@ -153,6 +154,7 @@ cudaError_t scratch_free(void *p, cudaStream_t stream) { return cudaFreeAsync(p,
 
 uint64_t wait_timeout_ns() { return g_timeout_ns.load(); }
 int sm_reserve() { return g_sm_reserve.load(); }
+int fps_batched() { return g_fps_batched.load(); }
 int debug_stall() { return g_stall.load(); }
 int api_current_device(const DeviceInfo **out) { return current_device(out); }
 int api_check_ptr(const void *p, int dev, size_t align, const char *name) {
@@ -195,6 +197,8 @@ void pc_debug_set_stall(int mask) {
 }
 
 void pc_set_sm_reserve(int sms) { g_sm_reserve.store(sms < 0 ? 0 : sms); }
+
+int pc_fps_set_batched(int enable) { return g_fps_batched.exchange(enable ? 1 : 0); }
 
 int pc_fps_sm_count(int64_t B, int64_t N, int64_t npoint) {
     (void)npoint;

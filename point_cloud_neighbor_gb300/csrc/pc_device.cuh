@@ -233,6 +233,33 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v,
         : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from this block's shared memory to the shared memory of a block of the
+// cluster, completing as transaction bytes on an mbarrier in that block.
+// dst and bar are shared::cluster addresses (map_shared_rank).  The source
+// must have been made visible to the async proxy (fence_proxy_async_smem
+// after the writes) and must not be written again before
+// bulk_wait_read_all() in the issuing thread.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, const void *src,
+                                                     unsigned bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes "
+        "[%0], [%1], %2, [%3];" ::"r"(dst),
+        "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the issuing thread's committed bulk copies have read their sources
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// the issuing thread's committed bulk copies are complete
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // try_wait with cluster-scope acquire: data that other blocks of the cluster
 // delivered with st.async is visible once the phase completes.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar,

@@ -19,7 +19,11 @@
 //      coordinates up in the block's shared-memory copy of its points;
 //   4. blocks of a cloud exchange their candidates:
 //      - BLOCK schedule (one block per cloud): nothing to exchange;
-//      - CLUSTER schedule (one thread block cluster per cloud): warp 0 sends
+//      - CLUSTER schedule (one thread block cluster per cloud), by default in
+//        rounds of several centers per exchange (fps_rounds_kernel: each
+//        warp lists its best points and bounds the rest, and every block
+//        certifies the same run of centers from the cloud's lists); one
+//        center per exchange (pc_fps_set_batched(0)): warp 0 sends
 //        the candidate (key, coordinates) into slot [step parity][its rank]
 //        of every block of the cluster with st.async, which completes as
 //        transaction bytes on that block's own mbarrier for this step
@@ -284,6 +288,373 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
         if (rank == 0 && threadIdx.x == 0) out[t] = int64_t(cj);
     }
     if (CLUSTER) cluster_sync_all();  // no block exits while peers may write
+}
+
+// ---------------------------------------------------------------------------
+// CLUSTER schedule in rounds: several centers per exchange.
+//
+// The sequential rule takes, at every step, the point of largest m (smallest
+// index on a tie).  A round certifies a run of such steps from a short list:
+//   * every warp lists its own best point (largest m, smallest index) and up
+//     to FR_CW - 1 more lane-best points, and bounds every point it does not
+//     list: a point that is not its lane's best is at most the lane's second
+//     largest m, and a lane-best point that is not listed is at most the
+//     warp's bound by construction (lanes whose best exceeds the bound are
+//     listed, those past FR_CW raise the bound to their m);
+//   * the blocks of the cloud exchange their lists and bounds (one bulk copy
+//     into every block's shared memory), and every block resolves the same
+//     run: the first center is the largest listed point -- the cloud's
+//     largest, since every warp's best is listed; after it the listed points'
+//     m are lowered by the new center exactly as the step would lower them,
+//     and the next largest listed point is the next center as long as its m
+//     is strictly above B, the largest bound, which every unlisted point's m
+//     stays at or below.  The run ends at the first point that is not above
+//     B (or after FR_RMAX centers);
+//   * every block then lowers its points' m by the run's centers (min is
+//     exact in any order) and lists again.
+// Each accepted center is the one the step-by-step rule takes, so the
+// output is identical; a round costs one exchange for the whole run (100k
+// points, 4096 samples: about 27 centers a round).
+constexpr int FR_CW = 8;     // entries a warp lists per round (its best first)
+constexpr int FR_RMAX = 64;  // centers a round takes at most
+constexpr int FR_LIST = 4;   // certified candidates a lane of the resolving warp holds
+
+// A listed point: key (bits(m) + 1; 0 = empty), original index, coordinates.
+struct __align__(16) FrEntry {
+    unsigned hi, j;
+    float x, y;
+    float z, pad0, pad1, pad2;
+};
+
+// A block's list: [W warps][FR_CW] entries, then [W] bounds (uint4: key, -).
+__host__ __device__ constexpr unsigned fr_msg_bytes(int warps) {
+    return unsigned(warps) * FR_CW * 32u + unsigned(warps) * 16u;
+}
+
+__host__ __device__ constexpr size_t fr_align16(size_t v) { return (v + 15) & ~size_t(15); }
+
+// Shared memory: the block's points (12 B each), its list, the lists of the
+// cloud's blocks by round parity, the run's centers, the candidate
+// offsets, each warp's largest entry, the exchange mbarriers and four
+// counters/flags.
+__host__ __device__ constexpr size_t fps_rounds_smem(int chunk, int warps, int nblocks) {
+    return fr_align16(size_t(chunk) * 12) + fr_msg_bytes(warps) +
+           2 * size_t(nblocks) * fr_msg_bytes(warps) +
+           size_t(FR_RMAX) * 16 + 32 * FR_LIST * sizeof(int) + 32 * sizeof(uint4) +
+           2 * sizeof(uint64_t) + 16;
+}
+
+// Every warp of a block, once the round's lists are in: B, the largest bound
+// of an unlisted point (returned), and the scan of lists warp, warp + W, ...:
+// each entry above B gets a candidate position (1, 2, ... from *s_total;
+// position 0 is the run's first center) and its byte offset in cidx, the
+// ones past 32 * FR_LIST raise *s_over to their m instead; the warp's largest
+// entry (smallest index on a tie) goes to *wfirst as (key, index, offset).
+__device__ __forceinline__ unsigned fr_scan(const unsigned char *lists, int nl, int W,
+                                            unsigned msg, int *cidx, uint4 *wfirst,
+                                            int *s_total, unsigned *s_over) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = W * FR_CW;  // entries per list
+    constexpr int CAP = 32 * FR_LIST;
+    unsigned bnd = 0u;
+    for (int l = 0; l < nl; ++l)
+        if (lane < W)
+            bnd = max(bnd, reinterpret_cast<const uint4 *>(lists + size_t(l) * msg +
+                                                           size_t(per) * 32)[lane].x);
+    bnd = __reduce_max_sync(FULL, bnd);
+    unsigned gh = 0u, gj = FULL, over = 0u;
+    int go = 0;
+    for (int l = warp; l < nl; l += W) {
+        for (int k0 = 0; k0 < per; k0 += 32) {
+            const int k = k0 + lane;
+            const int off = l * int(msg) + k * 32;
+            unsigned h = 0u, j = FULL;
+            if (k < per) {
+                const uint2 hj = *reinterpret_cast<const uint2 *>(lists + off);
+                h = hj.x;
+                j = hj.y;
+            }
+            if (h > gh || (h == gh && h != 0u && j < gj)) {
+                gh = h;
+                gj = j;
+                go = off;
+            }
+            const bool keep = h > bnd;
+            const unsigned bal = __ballot_sync(FULL, keep);
+            if (bal != 0u) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(s_total, __popc(bal));
+                base = __shfl_sync(FULL, base, 0);
+                const int pos = base + __popc(bal & lanemask_lt());
+                if (keep) {
+                    if (pos < CAP)
+                        cidx[pos] = off;
+                    else
+                        over = max(over, h);
+                }
+            }
+        }
+    }
+    unsigned wh, wj;
+    warp_argmax_hi_min_lo(gh, gj, wh, wj);
+    const unsigned holder = __ballot_sync(FULL, gh == wh && gj == wj);
+    if (lane == __ffs(holder) - 1) *wfirst = make_uint4(wh, wj, unsigned(go), 0u);
+    over = __reduce_max_sync(FULL, over);
+    if (lane == 0 && over != 0u) atomicMax(s_over, over);
+    return bnd;
+}
+
+// Warp 0 of a block, after fr_scan: the run of centers the lists certify
+// (see above).  Writes the centers to cen[0 .. k), their indices to
+// out[0 .. k) when out is given, and k to *s_nc.
+__device__ __forceinline__ void fr_pick(const unsigned char *lists, int W, unsigned bnd,
+                                        int rmax, const int *cidx, const uint4 *wfirst,
+                                        int total, unsigned over, float4 *cen, int *s_nc,
+                                        int64_t *out) {
+    const int lane = threadIdx.x & 31;
+    constexpr int CAP = 32 * FR_LIST;
+    bnd = max(bnd, over);
+    // the first center: the largest of the warps' largest entries
+    const uint4 f = lane < W ? wfirst[lane] : make_uint4(0u, FULL, 0u, 0u);
+    unsigned fh, fj;
+    warp_argmax_hi_min_lo(f.x, f.y, fh, fj);
+    if (fh == 0u) {  // no point at all (cannot happen for N >= 1): stop the run
+        if (lane == 0) *s_nc = 0;
+        return;
+    }
+    const int first = int(__shfl_sync(
+        FULL, f.z, __ffs(__ballot_sync(FULL, f.x == fh && f.y == fj)) - 1));
+    const int nlist = min(total, CAP);
+    unsigned lh[FR_LIST], lj[FR_LIST];
+    float lx[FR_LIST], ly[FR_LIST], lz[FR_LIST];
+#pragma unroll
+    for (int s = 0; s < FR_LIST; ++s) {
+        const int q = lane + 32 * s;
+        const int off = q == 0 ? first : (q < nlist ? cidx[q] : -1);
+        lh[s] = 0u;
+        lj[s] = FULL;
+        lx[s] = ly[s] = lz[s] = 0.f;
+        if (off >= 0 && (q == 0 || off != first)) {  // the first center also above B: once
+            const FrEntry *e = reinterpret_cast<const FrEntry *>(lists + off);
+            lh[s] = e->hi;
+            lj[s] = e->j;
+            lx[s] = e->x;
+            ly[s] = e->y;
+            lz[s] = e->z;
+        }
+    }
+    int k = 0;
+    for (; k < rmax; ++k) {
+        // the lane's largest candidate (smallest index on a tie): slots 0-1
+        // and 2-3, then the two winners
+        static_assert(FR_LIST == 4, "the pairwise choice below takes four slots");
+        const bool r01 = lh[1] > lh[0] || (lh[1] == lh[0] && lj[1] < lj[0]);
+        const bool r23 = lh[3] > lh[2] || (lh[3] == lh[2] && lj[3] < lj[2]);
+        const unsigned ha = r01 ? lh[1] : lh[0], ja = r01 ? lj[1] : lj[0];
+        const unsigned hb = r23 ? lh[3] : lh[2], jb = r23 ? lj[3] : lj[2];
+        const bool rab = hb > ha || (hb == ha && jb < ja);
+        const unsigned bh = rab ? hb : ha, bj = rab ? jb : ja;
+        const unsigned wh = __reduce_max_sync(FULL, bh);
+        // the first center is the cloud's largest; a later one must be above
+        // every unlisted point's m
+        if (wh == 0u || (k > 0 && wh <= bnd)) break;
+        unsigned top = __ballot_sync(FULL, bh == wh);
+        if (__popc(top) > 1) {  // equal m in several lanes: the smallest index
+            const unsigned wj = __reduce_min_sync(FULL, bh == wh ? bj : FULL);
+            top = __ballot_sync(FULL, bh == wh && bj == wj);
+        }
+        const int wl = __ffs(top) - 1;
+        const float xa = r01 ? lx[1] : lx[0], ya = r01 ? ly[1] : ly[0], za = r01 ? lz[1] : lz[0];
+        const float xb = r23 ? lx[3] : lx[2], yb = r23 ? ly[3] : ly[2], zb = r23 ? lz[3] : lz[2];
+        const float cx = __shfl_sync(FULL, rab ? xb : xa, wl);
+        const float cy = __shfl_sync(FULL, rab ? yb : ya, wl);
+        const float cz = __shfl_sync(FULL, rab ? zb : za, wl);
+        const unsigned cj = __shfl_sync(FULL, bj, wl);
+        if (lane == 0) {
+            cen[k] = make_float4(cx, cy, cz, 0.f);
+            if (out) out[k] = int64_t(cj);
+        }
+        // lower the candidates' m by the new center, as the step would (a
+        // NaN distance leaves m, as fminf does)
+#pragma unroll
+        for (int s = 0; s < FR_LIST; ++s) {
+            const float sv = sqdist(lx[s], ly[s], lz[s], cx, cy, cz);
+            const unsigned kv = sv >= 0.0f ? __float_as_uint(sv) + 1u : FULL;
+            lh[s] = lh[s] != 0u ? min(lh[s], kv) : 0u;
+        }
+    }
+    if (lane == 0) *s_nc = k;
+}
+
+// Threads a rounds kernel with PPT points per thread may use (the schedules
+// take at most 256 with 32 points, 384 with fewer).
+__host__ __device__ constexpr int fr_max_threads(int ppt) { return ppt >= 32 ? 256 : 384; }
+
+template <int PPT>
+__global__ void __launch_bounds__(fr_max_threads(PPT), 1)
+    fps_rounds_kernel(const FpsArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int T = blockDim.x;
+    const int W = T >> 5;
+    const unsigned msg = fr_msg_bytes(W);
+    float *scoord = reinterpret_cast<float *>(smem);
+    unsigned char *sbuf = smem + fr_align16(size_t(a.chunk) * 12);
+    unsigned char *recv = sbuf + msg;  // [2 parities][nblocks] lists
+    float4 *cen = reinterpret_cast<float4 *>(recv + 2 * size_t(a.nblocks) * msg);
+    int *cidx = reinterpret_cast<int *>(cen + FR_RMAX);
+    uint4 *wfirst = reinterpret_cast<uint4 *>(cidx + 32 * FR_LIST);
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(wfirst + 32);
+    int *s_nc = reinterpret_cast<int *>(xbar + 2);
+    int *s_fail = s_nc + 1;
+    int *s_total = s_nc + 2;  // candidate positions taken (position 0: the first center)
+    unsigned *s_over = reinterpret_cast<unsigned *>(s_nc + 3);
+
+    // every distributed-shared-memory address below targets ranks
+    // < a.nblocks; a launch without that cluster shape stops here (uniform)
+    if (cluster_nctarank() != unsigned(a.nblocks)) {
+        if (threadIdx.x == 0) raise_status(a.status, 3 /* PC_ERR_CUDA */);
+        return;
+    }
+    const unsigned rank = cluster_ctarank();
+    const int b = blockIdx.x / a.nblocks;
+    const float *x = a.xyz + size_t(b) * size_t(a.N) * 3;
+    const int lo = int(rank) * a.chunk;
+    const int hi = min(a.N, lo + a.chunk);
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
+    const unsigned xbytes = unsigned(a.nblocks) * msg;
+
+    ThreadPoints<PPT> pt;
+    fps_load_points<PPT>(x, lo, hi, T, pt, scoord);
+    int64_t *out = a.out + size_t(b) * a.npoint;
+    if (threadIdx.x == 0) {
+        cen[0] = make_float4(x[size_t(a.start) * 3 + 0], x[size_t(a.start) * 3 + 1],
+                             x[size_t(a.start) * 3 + 2], 0.f);
+        *s_nc = 1;
+        *s_fail = 0;
+        *s_total = 1;
+        *s_over = 0u;
+        if (rank == 0) out[0] = a.start;
+        // one exchange mbarrier per round parity, armed for its first round
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(&xbar[0], xbytes);
+        mbar_arrive_expect_tx(&xbar[1], xbytes);
+    }
+    __syncthreads();
+    cluster_sync_all();  // every block's barriers exist before use
+
+    FrEntry *mine = reinterpret_cast<FrEntry *>(sbuf) + warp * FR_CW;
+    uint4 *mybound = reinterpret_cast<uint4 *>(sbuf + size_t(W) * FR_CW * 32) + warp;
+    int t = 1;  // centers output so far
+    for (int round = 0; t < a.npoint; ++round) {
+        const int par = round & 1;
+        // 1. lower the points' m by the last run's centers
+        const int nc = *s_nc;
+        for (int c = 0; c < nc; ++c) {
+            const float4 cc = cen[c];
+            const float2 ncx = make_float2(-cc.x, -cc.x);
+            const float2 ncy = make_float2(-cc.y, -cc.y);
+            const float2 ncz = make_float2(-cc.z, -cc.z);
+#pragma unroll
+            for (int i = 0; i < PPT / 2; ++i) {
+                const float2 s = sqdist2(pt.x[i], pt.y[i], pt.z[i], ncx, ncy, ncz, nz0);
+                pt.m[2 * i] = fminf(pt.m[2 * i], s.x);
+                pt.m[2 * i + 1] = fminf(pt.m[2 * i + 1], s.y);
+            }
+        }
+        // 2. the lane's best point (its slots are in increasing index, so a
+        // strict ">" keeps the smaller index on a tie) and its second largest m
+        float best = -1.0f, second = -1.0f;
+        int bp = 0;
+#pragma unroll
+        for (int p = 0; p < PPT; ++p) {
+            const float v = pt.m[p];
+            if (v > best) {
+                second = best;
+                best = v;
+                bp = p;
+            } else {
+                second = fmaxf(second, v);
+            }
+        }
+        const unsigned khi = best >= 0.0f ? __float_as_uint(best) + 1u : 0u;
+        const unsigned kj = khi ? unsigned(lo + bp * T + int(threadIdx.x)) : FULL;
+        const unsigned shi = second >= 0.0f ? __float_as_uint(second) + 1u : 0u;
+        // 3. the warp's list (its best first, then lanes whose best is above
+        // the bound, in lane order) and its bound
+        unsigned whi, wj;
+        warp_argmax_hi_min_lo(khi, kj, whi, wj);
+        const int wl = __ffs(__ballot_sync(FULL, khi == whi && kj == wj)) - 1;
+        unsigned bw = __reduce_max_sync(FULL, shi);
+        const unsigned cand = __ballot_sync(FULL, khi > bw && lane != wl);
+        const int crank = __popc(cand & lanemask_lt());
+        const bool is_c = (cand >> lane) & 1u;
+        bw = max(bw, __reduce_max_sync(FULL, is_c && crank >= FR_CW - 1 ? khi : 0u));
+        const bool listed = (lane == wl && whi != 0u) || (is_c && crank < FR_CW - 1);
+        if (listed) {
+            const float *c = scoord + (int(kj) - lo) * 3;
+            FrEntry *e = mine + (lane == wl ? 0 : 1 + crank);
+            e->hi = khi;
+            e->j = kj;
+            e->x = c[0];
+            e->y = c[1];
+            e->z = c[2];
+        }
+        const int nlisted = (whi != 0u ? 1 : 0) + min(__popc(cand), FR_CW - 1);
+        if (lane >= nlisted && lane < FR_CW) mine[lane].hi = 0u;
+        if (lane == 0) *mybound = make_uint4(bw, 0u, 0u, 0u);
+        fence_proxy_async_smem();  // the list, for the bulk copies
+        __syncthreads();
+        if (warp == 0) {
+            // testing hook: block 0 of the first cloud withholds round 0
+            const bool withhold = (a.stall & 2) && b == 0 && rank == 0 && round == 0;
+            if (lane < a.nblocks && !withhold) {
+                const uint32_t dst = map_shared_rank(
+                    recv + (size_t(par) * a.nblocks + rank) * msg, unsigned(lane));
+                const uint32_t bar = map_shared_rank(&xbar[par], unsigned(lane));
+                bulk_copy_to_cluster(dst, sbuf, msg, bar);
+                bulk_commit();
+            }
+        }
+        // 4. the round's lists are in: every warp waits (bounded); thread 0
+        // re-arms this parity for round + 2 (its next phase cannot complete
+        // before every block has passed this round)
+        {
+            const unsigned ph = unsigned(round >> 1) & 1u;
+            const bool got =
+                __all_sync(FULL, mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns));
+            if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&xbar[par], xbytes);
+            // the list may be rewritten once this round is over
+            if (warp == 0 && lane < a.nblocks) bulk_wait_read_all();
+            if (!got && lane == 0) *s_fail = 1;
+        }
+        // 5. every warp scans its share of the lists; warp 0 resolves the run
+        const unsigned char *lists = recv + size_t(par) * a.nblocks * msg;
+        const unsigned bnd = fr_scan(lists, a.nblocks, W, msg, cidx,
+                                     wfirst + warp, s_total, s_over);
+        __syncthreads();
+        if (warp == 0 && !*s_fail)
+            fr_pick(lists, W, bnd, min(FR_RMAX, a.npoint - t), cidx, wfirst, *s_total,
+                    *s_over, cen, s_nc, rank == 0 ? out + t : nullptr);
+        __syncthreads();
+        const int taken = *s_nc;
+        if (*s_fail || taken <= 0) {
+            raise_status(a.status, *s_fail ? 4 /* PC_ERR_DEVICE_TIMEOUT */ : 3 /* PC_ERR_CUDA */);
+            if (rank == 0)
+                for (int i = t + int(threadIdx.x); i < a.npoint; i += T) out[i] = -1;
+            break;
+        }
+        t += taken;
+        if (threadIdx.x == 0) {  // for the next round's scan
+            *s_total = 1;
+            *s_over = 0u;
+        }
+    }
+    // no copy in flight and no block exits while peers may write
+    if (warp == 0 && lane < a.nblocks) bulk_wait_all();
+    cluster_sync_all();
 }
 
 // GRID schedule: cooperative launch, a.nblocks blocks per cloud.
@@ -597,6 +968,17 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
     if (failed && r == 0)
         for (int i = t + int(threadIdx.x); i < a.npoint; i += T) out[i] = -1;
     cluster_sync_all();  // no block exits while peers may write
+}
+
+const void *fps_rounds_ptr(int ppt) {
+    switch (ppt) {
+        case 2: return reinterpret_cast<const void *>(&fps_rounds_kernel<2>);
+        case 4: return reinterpret_cast<const void *>(&fps_rounds_kernel<4>);
+        case 8: return reinterpret_cast<const void *>(&fps_rounds_kernel<8>);
+        case 16: return reinterpret_cast<const void *>(&fps_rounds_kernel<16>);
+        case 24: return reinterpret_cast<const void *>(&fps_rounds_kernel<24>);
+        default: return reinterpret_cast<const void *>(&fps_rounds_kernel<32>);
+    }
 }
 
 template <int PPT>
@@ -939,7 +1321,6 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
                        const float *xyz, int64_t B, int64_t N, int64_t npoint,
                        int64_t start_idx, int64_t *out_idx, void *workspace,
                        cudaStream_t stream) {
-    (void)dev;
     FpsArgs a{};
     a.xyz = xyz;
     a.N = int(N);
@@ -958,10 +1339,25 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
 
     const bool cgrid = plan.strategy == 3 && plan.cluster > 1;
     const void *fn = cgrid ? fps_cgrid_ptr(plan.ppt) : fps_kernel_ptr(plan.strategy, plan.ppt);
+    size_t smem = plan.smem_bytes;
+    // CLUSTER: several centers per exchange (fps_rounds_kernel) where its
+    // lists fit; the step-by-step kernel otherwise.  (With one block per
+    // cloud there is no exchange to share: one center per step is faster --
+    // GB300, 96 clouds of 4096 points, 1024 samples: 0.41 ms vs 0.54.)
+    if (fps_batched() && plan.strategy == 2 && plan.threads <= fr_max_threads(plan.ppt)) {
+        const size_t need = fps_rounds_smem(plan.chunk, plan.threads / 32, plan.cluster);
+        const size_t rsmem = std::max(smem, need);
+        const void *rfn = fps_rounds_ptr(plan.ppt);
+        if (rsmem <= dev.smem_per_block_optin &&
+            (rsmem == smem || max_active_clusters(rfn, plan.cluster, plan.threads, rsmem) >= 1)) {
+            fn = rfn;
+            smem = rsmem;
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(B * plan.blocks_per_cloud));
     cfg.blockDim = dim3(unsigned(plan.threads));
-    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     cfg.attrs = attr;
@@ -1005,8 +1401,7 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
         attr[0].val.cooperative = 1;
         cfg.numAttrs = 1;
     } else {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(plan.smem_bytes));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         if (plan.strategy == 2) {
             if (plan.cluster > 8) {

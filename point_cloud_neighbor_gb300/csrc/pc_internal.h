@@ -92,6 +92,10 @@ cudaError_t launch_knn_ball_query(const DeviceInfo &dev, const float *query, int
                                   float *knn_dist, int64_t *knn_idx, float r32, int64_t K,
                                   float *bq_dist2, int64_t *bq_idx, cudaStream_t stream);
 
+// FPS of the CLUSTER schedule in rounds of several centers per exchange: 1
+// (default) or 0 = one center per exchange (pc_fps_set_batched).
+int fps_batched();
+
 struct FpsPlan {
     int strategy = 0;       // PC_FPS_BLOCK / CLUSTER / GRID
     int cluster = 1;        // blocks per cluster (BLOCK: 1)

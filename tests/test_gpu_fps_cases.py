@@ -1,5 +1,8 @@
 """FPS of the BLOCK and CLUSTER schedules against the oracle on the cases
 where a per-block reduction or the exchange between blocks could go wrong.
+The CLUSTER cases run both kernels: the rounds kernel (default; several
+centers certified per exchange) and one center per exchange
+(pc_fps_set_batched(False)).
 
 The operator (mps-pointops project page, "Farthest point sampling";
 "Contracts"): c_0 = start; each step takes the point with the largest
@@ -21,6 +24,13 @@ from point_cloud_neighbor_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 THREADS = oracle.default_threads()
+
+
+@pytest.fixture(params=[True, False], ids=["rounds", "per_step"])
+def batched(request):
+    prev = pc.pc_fps_set_batched(request.param)
+    yield request.param
+    pc.pc_fps_set_batched(prev)
 
 
 @pytest.fixture(autouse=True)
@@ -45,7 +55,7 @@ def assert_idx_equal(got, want, what):
     (pc.PC_FPS_CLUSTER, 3), (pc.PC_FPS_CLUSTER, 8), (pc.PC_FPS_CLUSTER, 13),
     (pc.PC_FPS_CLUSTER, 16),
 ])
-def test_grid_ties_every_cluster_size(strategy, cs):
+def test_grid_ties_every_cluster_size(batched, strategy, cs):
     """Two clouds of 6,000 points on a 1/32 grid (duplicates and equal
     distances everywhere), 700 samples from start 11."""
     x = inputs.random_cloud(60, 2, 6000, grid=1 / 32)
@@ -54,7 +64,7 @@ def test_grid_ties_every_cluster_size(strategy, cs):
     assert_idx_equal(got, want, f"grid ties {strategy}/{cs}")
 
 
-def test_exhausted_cloud():
+def test_exhausted_cloud(batched):
     """8,192 points at 40 distinct places (each repeated): after 40 samples
     every minimum is 0 and the rest repeat the smallest index, 0."""
     rng = np.random.default_rng(61)
@@ -67,7 +77,7 @@ def test_exhausted_cloud():
 
 
 @pytest.mark.parametrize("offset", [1e4, 1e6])
-def test_far_from_the_origin(offset):
+def test_far_from_the_origin(batched, offset):
     """Coordinates of 1e4 and 1e6 (spacing 1/1024 and 1/16): few distinct
     distances, many exact ties, boxes whose bound is often exactly tight."""
     x = (inputs.random_cloud(62, 2, 12_000, lo=0.0, hi=64.0).astype(np.float64) +
@@ -78,7 +88,7 @@ def test_far_from_the_origin(offset):
 
 
 @pytest.mark.parametrize("morton", [False, True], ids=["random", "morton"])
-def test_large_cloud_step_schedule(morton):
+def test_large_cloud_step_schedule(batched, morton):
     """The 100k-point cloud, 4,096 samples, on a cluster of 13 blocks (the
     schedule of the benchmark step)."""
     x = inputs.large(morton=morton)
@@ -93,3 +103,41 @@ def test_many_clouds_block_schedule():
     want = oracle.fps(x, 256, 3, threads=THREADS)
     got = gpu_fps(x, 256, 3, strategy=pc.PC_FPS_BLOCK)
     assert_idx_equal(got, want, "96 clouds")
+
+
+def test_switch_returns_previous():
+    prev = pc.pc_fps_set_batched(False)
+    try:
+        assert pc.pc_fps_set_batched(True) is False
+        assert pc.pc_fps_set_batched(True) is True
+    finally:
+        pc.pc_fps_set_batched(prev)
+
+
+def test_cluster_wait_timeout(batched):
+    """Block 0 of the first cloud withholds its first candidates (its first
+    round's list): that cloud's slots after the start are -1, the other
+    cloud is exact, the status word says PC_ERR_DEVICE_TIMEOUT, and the next
+    call is correct."""
+    x = inputs.random_cloud(64, 2, 8000)
+    pc.pc_set_wait_timeout_ns(2_000_000)
+    pc.pc_debug_set_stall(pc.PC_STALL_FPS_CLUSTER)
+    try:
+        idx = gpu_fps(x, 20, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=4)
+    finally:
+        pc.pc_debug_set_stall(0)
+        pc.pc_set_wait_timeout_ns(2_000_000_000)
+    assert pc.pc_device_status(reset=True) == 4
+    want = oracle.fps(x, 20, 0)
+    assert idx[0, 0] == 0 and (idx[0, 1:] == -1).all()
+    assert_idx_equal(idx[1], want[1], "the cloud that did not stall")
+    assert_idx_equal(gpu_fps(x, 20, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=4), want,
+                     "after the timeout")
+
+
+@pytest.mark.parametrize("npoint", [1, 2, 65, 300])
+def test_short_runs(batched, npoint):
+    """Few samples (a run cut by npoint), 3 clouds on clusters of 8."""
+    x = inputs.random_cloud(65, 3, 9000)
+    assert_idx_equal(gpu_fps(x, npoint, 7, strategy=pc.PC_FPS_CLUSTER, cluster_size=8),
+                     oracle.fps(x, npoint, 7), f"npoint={npoint}")
