@@ -276,7 +276,7 @@ def run_gpu(args):
     fork = torch.cuda.Event()
     # the kNN and Ball Query grids (one wave) are planned around the SMs
     # FPS holds while it runs
-    reserve = 0 if args.serial else B * STEP_FPS_CLUSTER
+    reserve = 0 if args.serial else B * args.fps_cluster
     # kNN and Ball Query of the same queries: one fused call (each pair
     # filtered once for both), or with --separate pc_knn then pc_ball_query
     fused = not args.separate
@@ -287,7 +287,7 @@ def run_gpu(args):
         if ev is not None:
             ev[0].record(stream)
         fork.record(stream)
-        pc.pc_fps(x, npoint, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=STEP_FPS_CLUSTER,
+        pc.pc_fps(x, npoint, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=args.fps_cluster,
                   out=fps_out, workspace=ws)
         if ev is not None:
             ev[1].record(stream)
@@ -417,8 +417,8 @@ def run_gpu(args):
     # FPS against its two other bounds: ~10 instructions per point-step on the
     # SMs its schedule uses, and the per-step exchange floor measured with the
     # same cluster schedule on 1024 points per block
-    fps_sms = B * STEP_FPS_CLUSTER
-    ops["fps"]["cluster"] = STEP_FPS_CLUSTER
+    fps_sms = B * args.fps_cluster
+    ops["fps"]["cluster"] = args.fps_cluster
     ops["fps"]["alu_bound_ms"] = (float(N) * (npoint - 1) * FPS_INSTR_PER_POINT_STEP /
                                   (max(fps_sms, 1) * 128 * max_mhz * 1e6) * 1e3)
     ops["fps"]["alu_frac"] = ops["fps"]["alu_bound_ms"] / per["fps"]
@@ -510,7 +510,7 @@ def run_gpu(args):
                                                "2: FPS concurrent with kNN and Ball Query"),
                                    "knn_ball_query": ("one fused call" if fused else
                                                       "pc_knn then pc_ball_query"),
-                                   "fps_cluster": STEP_FPS_CLUSTER}),
+                                   "fps_cluster": args.fps_cluster}),
         "roofline": roof, "roofline_per_kernel": roof_all, "ops": ops,
         "grid": grid, "next_rows": next_rows, "configs": configs,
         "e2e": e2e,
@@ -1024,13 +1024,13 @@ def run_e2e(args, pc, x_host, device, world, bq_first=True):
     # FPS result once FPS ends; only the second's read-back follows the last
     # kernel
     copy = torch.cuda.Stream(device) if not args.serial else main
-    reserve = 0 if args.serial else STEP_FPS_CLUSTER
+    reserve = 0 if args.serial else args.fps_cluster
 
     def one_fused():
         xd = x_pin.to(device, non_blocking=True)
         side.wait_stream(main)
         f = pc.pc_fps(xd, npoint, 0, strategy=pc.PC_FPS_CLUSTER,
-                      cluster_size=STEP_FPS_CLUSTER)
+                      cluster_size=args.fps_cluster)
         outs["fps"].copy_(f, non_blocking=True)
         with torch.cuda.stream(side):
             pc.pc_set_sm_reserve(reserve)
@@ -1050,7 +1050,7 @@ def run_e2e(args, pc, x_host, device, world, bq_first=True):
         xd = x_pin.to(device, non_blocking=True)
         side.wait_stream(main)
         f = pc.pc_fps(xd, npoint, 0, strategy=pc.PC_FPS_CLUSTER,
-                      cluster_size=STEP_FPS_CLUSTER)
+                      cluster_size=args.fps_cluster)
         outs["fps"].copy_(f, non_blocking=True)
         ops = [("knn", lambda: pc.pc_knn(xd, xd, k)),
                ("bq", lambda: pc.pc_ball_query(xd, xd, r, K))]
@@ -1237,6 +1237,9 @@ def main():
     ap.add_argument("--step-only", action="store_true",
                     help="time only the FPS + kNN + Ball Query step (no grid, "
                          "next-row or end-to-end sections; for profiler captures)")
+    ap.add_argument("--fps-cluster", type=int, default=STEP_FPS_CLUSTER,
+                    help="blocks of the FPS cluster in the step (its SMs are "
+                         "reserved from the kNN + Ball Query grid)")
     ap.add_argument("--separate", action="store_true",
                     help="run kNN and Ball Query of the step as two calls "
                          "(pc_knn, pc_ball_query) instead of one fused call")

@@ -315,6 +315,14 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
 // Each accepted center is the one the step-by-step rule takes, so the
 // output is identical; a round costs one exchange for the whole run (100k
 // points, 4096 samples: about 27 centers a round).
+//
+// A block has one more warp than it needs for its points: that warp holds
+// none; it sends the block's list, and after the scan (every warp's share)
+// it certifies the run and publishes each center in shared memory as it is
+// taken, while the point warps lower their m by the published centers -- the
+// sequential picks overlap the point work (GB300, 100k points on 13 blocks:
+// 2.56 ms with warp 0 picking and updating its own points afterwards, 2.20
+// with the extra warp).
 constexpr int FR_CW = 8;     // entries a warp lists per round (its best first)
 constexpr int FR_RMAX = 64;  // centers a round takes at most
 constexpr int FR_LIST = 4;   // certified candidates a lane of the resolving warp holds
@@ -335,36 +343,35 @@ __host__ __device__ constexpr size_t fr_align16(size_t v) { return (v + 15) & ~s
 
 // Shared memory: the block's points (12 B each), its list, the lists of the
 // cloud's blocks by round parity, the run's centers, the candidate
-// offsets, each warp's largest entry, the exchange mbarriers and four
-// counters/flags.
+// offsets, each warp's largest entry, the lists' counts of candidates, the
+// exchange mbarriers and six counters/flags.
 __host__ __device__ constexpr size_t fps_rounds_smem(int chunk, int warps, int nblocks) {
     return fr_align16(size_t(chunk) * 12) + fr_msg_bytes(warps) +
            2 * size_t(nblocks) * fr_msg_bytes(warps) +
            size_t(FR_RMAX) * 16 + 32 * FR_LIST * sizeof(int) + 32 * sizeof(uint4) +
-           2 * sizeof(uint64_t) + 16;
+           FPS_MAX_CLUSTER * sizeof(int) + 2 * sizeof(uint64_t) + 32;
 }
 
-// Every warp of a block, once the round's lists are in: B, the largest bound
-// of an unlisted point (returned), and the scan of lists warp, warp + W, ...:
-// each entry above B gets a candidate position (1, 2, ... from *s_total;
-// position 0 is the run's first center) and its byte offset in cidx, the
-// ones past 32 * FR_LIST raise *s_over to their m instead; the warp's largest
-// entry (smallest index on a tie) goes to *wfirst as (key, index, offset).
-__device__ __forceinline__ unsigned fr_scan(const unsigned char *lists, int nl, int W,
-                                            unsigned msg, int *cidx, uint4 *wfirst,
-                                            int *s_total, unsigned *s_over) {
+// Every warp of a block (nscan of them), once the round's lists are in,
+// pass 1: B, the largest bound of an unlisted point (returned); for lists
+// warp, warp + nscan, ... (W: the listing warps of a block) the number of
+// entries above B (cnt[list]) and the warp's largest entry (smallest index on
+// a tie) in *wfirst as (key, index, offset).
+__device__ __forceinline__ unsigned fr_count(const unsigned char *lists, int nl, int W,
+                                             int nscan, unsigned msg, int *cnt,
+                                             uint4 *wfirst) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per = W * FR_CW;  // entries per list
-    constexpr int CAP = 32 * FR_LIST;
     unsigned bnd = 0u;
     for (int l = 0; l < nl; ++l)
         if (lane < W)
             bnd = max(bnd, reinterpret_cast<const uint4 *>(lists + size_t(l) * msg +
                                                            size_t(per) * 32)[lane].x);
     bnd = __reduce_max_sync(FULL, bnd);
-    unsigned gh = 0u, gj = FULL, over = 0u;
+    unsigned gh = 0u, gj = FULL;
     int go = 0;
-    for (int l = warp; l < nl; l += W) {
+    for (int l = warp; l < nl; l += nscan) {
+        int n = 0;
         for (int k0 = 0; k0 < per; k0 += 32) {
             const int k = k0 + lane;
             const int off = l * int(msg) + k * 32;
@@ -379,47 +386,76 @@ __device__ __forceinline__ unsigned fr_scan(const unsigned char *lists, int nl, 
                 gj = j;
                 go = off;
             }
-            const bool keep = h > bnd;
-            const unsigned bal = __ballot_sync(FULL, keep);
-            if (bal != 0u) {
-                int base = 0;
-                if (lane == 0) base = atomicAdd(s_total, __popc(bal));
-                base = __shfl_sync(FULL, base, 0);
-                const int pos = base + __popc(bal & lanemask_lt());
-                if (keep) {
-                    if (pos < CAP)
-                        cidx[pos] = off;
-                    else
-                        over = max(over, h);
-                }
-            }
+            n += __popc(__ballot_sync(FULL, h > bnd));
         }
+        if (lane == 0) cnt[l] = n;
     }
     unsigned wh, wj;
     warp_argmax_hi_min_lo(gh, gj, wh, wj);
     const unsigned holder = __ballot_sync(FULL, gh == wh && gj == wj);
     if (lane == __ffs(holder) - 1) *wfirst = make_uint4(wh, wj, unsigned(go), 0u);
-    over = __reduce_max_sync(FULL, over);
-    if (lane == 0 && over != 0u) atomicMax(s_over, over);
     return bnd;
 }
 
-// Warp 0 of a block, after fr_scan: the run of centers the lists certify
-// (see above).  Writes the centers to cen[0 .. k), their indices to
-// out[0 .. k) when out is given, and k to *s_nc.
-__device__ __forceinline__ void fr_pick(const unsigned char *lists, int W, unsigned bnd,
+// Pass 2, after a barrier: every entry above B gets the candidate position
+// 1 + (entries above B in the lists before its own) + (those before it in its
+// list) -- the same in every block of the cloud, whatever the warps' timing
+// -- and its byte offset goes to cidx; the ones at positions past
+// 32 * FR_LIST raise *s_over to their m instead (every block then keeps the
+// same candidates and the same bound, and certifies the same run).
+__device__ __forceinline__ void fr_place(const unsigned char *lists, int nl, int W,
+                                         int nscan, unsigned msg, unsigned bnd,
+                                         const int *cnt, int *cidx, unsigned *s_over) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = W * FR_CW;
+    constexpr int CAP = 32 * FR_LIST;
+    unsigned over = 0u;
+    for (int l = warp; l < nl; l += nscan) {
+        int base = 1;
+        for (int i = 0; i < l; ++i) base += cnt[i];
+        for (int k0 = 0; k0 < per; k0 += 32) {
+            const int k = k0 + lane;
+            const int off = l * int(msg) + k * 32;
+            const unsigned h = k < per ? *reinterpret_cast<const unsigned *>(lists + off) : 0u;
+            const bool keep = h > bnd;
+            const unsigned bal = __ballot_sync(FULL, keep);
+            const int pos = base + __popc(bal & lanemask_lt());
+            if (keep) {
+                if (pos < CAP)
+                    cidx[pos] = off;
+                else
+                    over = max(over, h);
+            }
+            base += __popc(bal);
+        }
+    }
+    over = __reduce_max_sync(FULL, over);
+    if (lane == 0 && over != 0u) atomicMax(s_over, over);
+}
+
+// The resolving warp of a block, after fr_count and fr_place:
+// the run of centers the lists certify (see above).  Writes the centers to
+// cen[0 .. k), publishing each in *s_pub as it is taken (the point warps
+// apply it meanwhile), their indices to out[0 .. k) when out is given, k to
+// *s_nc, and sets *s_fin at the end.
+__device__ __forceinline__ void fr_pick(const unsigned char *lists, int nscan, unsigned bnd,
                                         int rmax, const int *cidx, const uint4 *wfirst,
                                         int total, unsigned over, float4 *cen, int *s_nc,
+                                        volatile int *s_pub, volatile int *s_fin,
                                         int64_t *out) {
     const int lane = threadIdx.x & 31;
     constexpr int CAP = 32 * FR_LIST;
     bnd = max(bnd, over);
     // the first center: the largest of the warps' largest entries
-    const uint4 f = lane < W ? wfirst[lane] : make_uint4(0u, FULL, 0u, 0u);
+    const uint4 f = lane < nscan ? wfirst[lane] : make_uint4(0u, FULL, 0u, 0u);
     unsigned fh, fj;
     warp_argmax_hi_min_lo(f.x, f.y, fh, fj);
     if (fh == 0u) {  // no point at all (cannot happen for N >= 1): stop the run
-        if (lane == 0) *s_nc = 0;
+        if (lane == 0) {
+            *s_nc = 0;
+            __threadfence_block();
+            *s_fin = 1;
+        }
         return;
     }
     const int first = int(__shfl_sync(
@@ -470,8 +506,10 @@ __device__ __forceinline__ void fr_pick(const unsigned char *lists, int W, unsig
         const float cy = __shfl_sync(FULL, rab ? yb : ya, wl);
         const float cz = __shfl_sync(FULL, rab ? zb : za, wl);
         const unsigned cj = __shfl_sync(FULL, bj, wl);
-        if (lane == 0) {
+        if (lane == 0) {  // the center, then its publication
             cen[k] = make_float4(cx, cy, cz, 0.f);
+            __threadfence_block();
+            *s_pub = k + 1;
             if (out) out[k] = int64_t(cj);
         }
         // lower the candidates' m by the new center, as the step would (a
@@ -483,20 +521,27 @@ __device__ __forceinline__ void fr_pick(const unsigned char *lists, int W, unsig
             lh[s] = lh[s] != 0u ? min(lh[s], kv) : 0u;
         }
     }
-    if (lane == 0) *s_nc = k;
+    if (lane == 0) {
+        *s_nc = k;
+        __threadfence_block();
+        *s_fin = 1;
+    }
 }
 
-// Threads a rounds kernel with PPT points per thread may use (the schedules
-// take at most 256 with 32 points, 384 with fewer).
-__host__ __device__ constexpr int fr_max_threads(int ppt) { return ppt >= 32 ? 256 : 384; }
+// Threads a rounds kernel with PPT points per thread may use: the point
+// threads of the schedules (at most 256 with 32 points, 384 with fewer) and
+// the resolving warp.
+__host__ __device__ constexpr int fr_max_threads(int ppt) { return ppt >= 32 ? 288 : 416; }
 
 template <int PPT>
 __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
     fps_rounds_kernel(const FpsArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int T = blockDim.x;
-    const int W = T >> 5;
+    const int T = int(blockDim.x) - 32;  // threads holding points
+    const int W = T >> 5;                // their warps, which list
+    const int NW = W + 1;                // and the resolving warp
+    const bool rw = warp == W;
     const unsigned msg = fr_msg_bytes(W);
     float *scoord = reinterpret_cast<float *>(smem);
     unsigned char *sbuf = smem + fr_align16(size_t(a.chunk) * 12);
@@ -504,11 +549,14 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
     float4 *cen = reinterpret_cast<float4 *>(recv + 2 * size_t(a.nblocks) * msg);
     int *cidx = reinterpret_cast<int *>(cen + FR_RMAX);
     uint4 *wfirst = reinterpret_cast<uint4 *>(cidx + 32 * FR_LIST);
-    uint64_t *xbar = reinterpret_cast<uint64_t *>(wfirst + 32);
+    int *lcnt = reinterpret_cast<int *>(wfirst + 32);  // [nblocks] candidates per list
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(lcnt + FPS_MAX_CLUSTER);
     int *s_nc = reinterpret_cast<int *>(xbar + 2);
     int *s_fail = s_nc + 1;
     int *s_total = s_nc + 2;  // candidate positions taken (position 0: the first center)
     unsigned *s_over = reinterpret_cast<unsigned *>(s_nc + 3);
+    volatile int *s_pub = s_nc + 4;  // centers of the run published so far
+    volatile int *s_fin = s_nc + 5;  // the run is complete
 
     // every distributed-shared-memory address below targets ranks
     // < a.nblocks; a launch without that cluster shape stops here (uniform)
@@ -525,7 +573,14 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
     const unsigned xbytes = unsigned(a.nblocks) * msg;
 
     ThreadPoints<PPT> pt;
-    fps_load_points<PPT>(x, lo, hi, T, pt, scoord);
+    if (!rw) {
+        fps_load_points<PPT>(x, lo, hi, T, pt, scoord);
+    } else {
+#pragma unroll
+        for (int p = 0; p < PPT; ++p) pt.m[p] = -1.0f;
+#pragma unroll
+        for (int i = 0; i < PPT / 2; ++i) pt.x[i] = pt.y[i] = pt.z[i] = make_float2(0.f, 0.f);
+    }
     int64_t *out = a.out + size_t(b) * a.npoint;
     if (threadIdx.x == 0) {
         cen[0] = make_float4(x[size_t(a.start) * 3 + 0], x[size_t(a.start) * 3 + 1],
@@ -534,6 +589,8 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
         *s_fail = 0;
         *s_total = 1;
         *s_over = 0u;
+        *s_pub = 0;
+        *s_fin = 0;
         if (rank == 0) out[0] = a.start;
         // one exchange mbarrier per round parity, armed for its first round
         mbar_init(&xbar[0], 1);
@@ -545,69 +602,72 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
     __syncthreads();
     cluster_sync_all();  // every block's barriers exist before use
 
+    // lower the thread's points' m by the center cc
+    auto apply = [&](const float4 cc) {
+        const float2 ncx = make_float2(-cc.x, -cc.x);
+        const float2 ncy = make_float2(-cc.y, -cc.y);
+        const float2 ncz = make_float2(-cc.z, -cc.z);
+#pragma unroll
+        for (int i = 0; i < PPT / 2; ++i) {
+            const float2 s = sqdist2(pt.x[i], pt.y[i], pt.z[i], ncx, ncy, ncz, nz0);
+            pt.m[2 * i] = fminf(pt.m[2 * i], s.x);
+            pt.m[2 * i + 1] = fminf(pt.m[2 * i + 1], s.y);
+        }
+    };
     FrEntry *mine = reinterpret_cast<FrEntry *>(sbuf) + warp * FR_CW;
     uint4 *mybound = reinterpret_cast<uint4 *>(sbuf + size_t(W) * FR_CW * 32) + warp;
     int t = 1;  // centers output so far
     for (int round = 0; t < a.npoint; ++round) {
         const int par = round & 1;
-        // 1. lower the points' m by the last run's centers
-        const int nc = *s_nc;
-        for (int c = 0; c < nc; ++c) {
-            const float4 cc = cen[c];
-            const float2 ncx = make_float2(-cc.x, -cc.x);
-            const float2 ncy = make_float2(-cc.y, -cc.y);
-            const float2 ncz = make_float2(-cc.z, -cc.z);
-#pragma unroll
-            for (int i = 0; i < PPT / 2; ++i) {
-                const float2 s = sqdist2(pt.x[i], pt.y[i], pt.z[i], ncx, ncy, ncz, nz0);
-                pt.m[2 * i] = fminf(pt.m[2 * i], s.x);
-                pt.m[2 * i + 1] = fminf(pt.m[2 * i + 1], s.y);
+        // 1. the start lowers the points' m (later centers were applied while
+        // the resolving warp picked them)
+        if (round == 0 && !rw) apply(cen[0]);
+        if (!rw) {
+            // 2. the lane's best point (its slots are in increasing index, so a
+            // strict ">" keeps the smaller index on a tie) and its second largest m
+            float best = -1.0f, second = -1.0f;
+            int bp = 0;
+    #pragma unroll
+            for (int p = 0; p < PPT; ++p) {
+                const float v = pt.m[p];
+                if (v > best) {
+                    second = best;
+                    best = v;
+                    bp = p;
+                } else {
+                    second = fmaxf(second, v);
+                }
             }
-        }
-        // 2. the lane's best point (its slots are in increasing index, so a
-        // strict ">" keeps the smaller index on a tie) and its second largest m
-        float best = -1.0f, second = -1.0f;
-        int bp = 0;
-#pragma unroll
-        for (int p = 0; p < PPT; ++p) {
-            const float v = pt.m[p];
-            if (v > best) {
-                second = best;
-                best = v;
-                bp = p;
-            } else {
-                second = fmaxf(second, v);
+            const unsigned khi = best >= 0.0f ? __float_as_uint(best) + 1u : 0u;
+            const unsigned kj = khi ? unsigned(lo + bp * T + int(threadIdx.x)) : FULL;
+            const unsigned shi = second >= 0.0f ? __float_as_uint(second) + 1u : 0u;
+            // 3. the warp's list (its best first, then lanes whose best is above
+            // the bound, in lane order) and its bound
+            unsigned whi, wj;
+            warp_argmax_hi_min_lo(khi, kj, whi, wj);
+            const int wl = __ffs(__ballot_sync(FULL, khi == whi && kj == wj)) - 1;
+            unsigned bw = __reduce_max_sync(FULL, shi);
+            const unsigned cand = __ballot_sync(FULL, khi > bw && lane != wl);
+            const int crank = __popc(cand & lanemask_lt());
+            const bool is_c = (cand >> lane) & 1u;
+            bw = max(bw, __reduce_max_sync(FULL, is_c && crank >= FR_CW - 1 ? khi : 0u));
+            const bool listed = (lane == wl && whi != 0u) || (is_c && crank < FR_CW - 1);
+            if (listed) {
+                const float *c = scoord + (int(kj) - lo) * 3;
+                FrEntry *e = mine + (lane == wl ? 0 : 1 + crank);
+                e->hi = khi;
+                e->j = kj;
+                e->x = c[0];
+                e->y = c[1];
+                e->z = c[2];
             }
+            const int nlisted = (whi != 0u ? 1 : 0) + min(__popc(cand), FR_CW - 1);
+            if (lane >= nlisted && lane < FR_CW) mine[lane].hi = 0u;
+            if (lane == 0) *mybound = make_uint4(bw, 0u, 0u, 0u);
         }
-        const unsigned khi = best >= 0.0f ? __float_as_uint(best) + 1u : 0u;
-        const unsigned kj = khi ? unsigned(lo + bp * T + int(threadIdx.x)) : FULL;
-        const unsigned shi = second >= 0.0f ? __float_as_uint(second) + 1u : 0u;
-        // 3. the warp's list (its best first, then lanes whose best is above
-        // the bound, in lane order) and its bound
-        unsigned whi, wj;
-        warp_argmax_hi_min_lo(khi, kj, whi, wj);
-        const int wl = __ffs(__ballot_sync(FULL, khi == whi && kj == wj)) - 1;
-        unsigned bw = __reduce_max_sync(FULL, shi);
-        const unsigned cand = __ballot_sync(FULL, khi > bw && lane != wl);
-        const int crank = __popc(cand & lanemask_lt());
-        const bool is_c = (cand >> lane) & 1u;
-        bw = max(bw, __reduce_max_sync(FULL, is_c && crank >= FR_CW - 1 ? khi : 0u));
-        const bool listed = (lane == wl && whi != 0u) || (is_c && crank < FR_CW - 1);
-        if (listed) {
-            const float *c = scoord + (int(kj) - lo) * 3;
-            FrEntry *e = mine + (lane == wl ? 0 : 1 + crank);
-            e->hi = khi;
-            e->j = kj;
-            e->x = c[0];
-            e->y = c[1];
-            e->z = c[2];
-        }
-        const int nlisted = (whi != 0u ? 1 : 0) + min(__popc(cand), FR_CW - 1);
-        if (lane >= nlisted && lane < FR_CW) mine[lane].hi = 0u;
-        if (lane == 0) *mybound = make_uint4(bw, 0u, 0u, 0u);
         fence_proxy_async_smem();  // the list, for the bulk copies
         __syncthreads();
-        if (warp == 0) {
+        if (rw) {
             // testing hook: block 0 of the first cloud withholds round 0
             const bool withhold = (a.stall & 2) && b == 0 && rank == 0 && round == 0;
             if (lane < a.nblocks && !withhold) {
@@ -627,17 +687,45 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
                 __all_sync(FULL, mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns));
             if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&xbar[par], xbytes);
             // the list may be rewritten once this round is over
-            if (warp == 0 && lane < a.nblocks) bulk_wait_read_all();
+            if (rw && lane < a.nblocks) bulk_wait_read_all();
             if (!got && lane == 0) *s_fail = 1;
         }
-        // 5. every warp scans its share of the lists; warp 0 resolves the run
+        // 5. every warp scans its share of the lists; the resolving warp
+        // certifies the run
         const unsigned char *lists = recv + size_t(par) * a.nblocks * msg;
-        const unsigned bnd = fr_scan(lists, a.nblocks, W, msg, cidx,
-                                     wfirst + warp, s_total, s_over);
+        const unsigned bnd = fr_count(lists, a.nblocks, W, NW, msg, lcnt, wfirst + warp);
         __syncthreads();
-        if (warp == 0 && !*s_fail)
-            fr_pick(lists, W, bnd, min(FR_RMAX, a.npoint - t), cidx, wfirst, *s_total,
-                    *s_over, cen, s_nc, rank == 0 ? out + t : nullptr);
+        fr_place(lists, a.nblocks, W, NW, msg, bnd, lcnt, cidx, s_over);
+        if (threadIdx.x == 0) {  // candidates in all: the first center and the counts
+            int total = 1;
+            for (int l = 0; l < a.nblocks; ++l) total += lcnt[l];
+            *s_total = total;
+        }
+        __syncthreads();
+        if (rw) {
+            if (!*s_fail)
+                fr_pick(lists, NW, bnd, min(FR_RMAX, a.npoint - t), cidx, wfirst, *s_total,
+                        *s_over, cen, s_nc, s_pub, s_fin, rank == 0 ? out + t : nullptr);
+            else if (lane == 0)
+                *s_fin = 1;
+        } else {
+            // apply the run's centers as the resolving warp publishes them
+            // (bounded wait: the run is short, the limit is a safety net)
+            int c = 0;
+            const uint64_t w0 = global_timer_ns();
+            for (int spin = 0;; ++spin) {
+                const int fin = *s_fin;
+                __threadfence_block();
+                const int pub = *s_pub;
+                __threadfence_block();
+                for (; c < pub; ++c) apply(cen[c]);
+                if (fin) break;
+                if ((spin & 255) == 255 && global_timer_ns() - w0 > a.timeout_ns) {
+                    if (lane == 0) *s_fail = 1;
+                    break;
+                }
+            }
+        }
         __syncthreads();
         const int taken = *s_nc;
         if (*s_fail || taken <= 0) {
@@ -647,13 +735,15 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
             break;
         }
         t += taken;
-        if (threadIdx.x == 0) {  // for the next round's scan
+        if (threadIdx.x == 0) {  // for the next round
             *s_total = 1;
             *s_over = 0u;
+            *s_pub = 0;
+            *s_fin = 0;
         }
     }
     // no copy in flight and no block exits while peers may write
-    if (warp == 0 && lane < a.nblocks) bulk_wait_all();
+    if (rw && lane < a.nblocks) bulk_wait_all();
     cluster_sync_all();
 }
 
@@ -1344,19 +1434,21 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
     // lists fit; the step-by-step kernel otherwise.  (With one block per
     // cloud there is no exchange to share: one center per step is faster --
     // GB300, 96 clouds of 4096 points, 1024 samples: 0.41 ms vs 0.54.)
-    if (fps_batched() && plan.strategy == 2 && plan.threads <= fr_max_threads(plan.ppt)) {
+    unsigned threads = unsigned(plan.threads);
+    if (fps_batched() && plan.strategy == 2 && plan.threads + 32 <= fr_max_threads(plan.ppt)) {
         const size_t need = fps_rounds_smem(plan.chunk, plan.threads / 32, plan.cluster);
         const size_t rsmem = std::max(smem, need);
         const void *rfn = fps_rounds_ptr(plan.ppt);
         if (rsmem <= dev.smem_per_block_optin &&
-            (rsmem == smem || max_active_clusters(rfn, plan.cluster, plan.threads, rsmem) >= 1)) {
+            max_active_clusters(rfn, plan.cluster, plan.threads + 32, rsmem) >= 1) {
             fn = rfn;
             smem = rsmem;
+            threads = unsigned(plan.threads + 32);
         }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(B * plan.blocks_per_cloud));
-    cfg.blockDim = dim3(unsigned(plan.threads));
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];

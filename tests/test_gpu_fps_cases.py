@@ -141,3 +141,25 @@ def test_short_runs(batched, npoint):
     x = inputs.random_cloud(65, 3, 9000)
     assert_idx_equal(gpu_fps(x, npoint, 7, strategy=pc.PC_FPS_CLUSTER, cluster_size=8),
                      oracle.fps(x, npoint, 7), f"npoint={npoint}")
+
+
+@pytest.fixture(scope="module")
+def large_fps_oracle():
+    """The oracle's 4096 samples of the 100k-point cloud and of its first
+    90,000 points (computed once)."""
+    out = {}
+    for name, x in (("100k", inputs.large()), ("90k", inputs.large()[:, :90000].copy())):
+        out[name] = (x, oracle.fps(x, 4096, 0, threads=THREADS))
+    return out
+
+
+@pytest.mark.parametrize("cloud", ["100k", "90k"])
+@pytest.mark.parametrize("cs", [11, 12, 13, 14, 15, 16])
+def test_rounds_every_cluster_size_large(large_fps_oracle, cloud, cs):
+    """Every block of a cloud must certify the same run from the same lists:
+    with more candidates above the bound than a run can hold, the ones kept
+    must not depend on the warps' timing (the 100k cloud on 12 blocks and
+    the 90k cloud on 16 exceed the candidate capacity in some rounds)."""
+    x, want = large_fps_oracle[cloud]
+    got = gpu_fps(x, 4096, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=cs)
+    assert_idx_equal(got, want, f"{cloud} on {cs} blocks")
