@@ -175,3 +175,23 @@ def test_fuzz_fps_grid_two_levels(case):
         pytest.skip(f"cluster size {cs} unsupported for B={B}: {e}")
     want = oracle.fps(x, npoint, start, threads=THREADS)
     assert_idx_equal(idx, want, f"fuzz fps grid B={B} N={N} npoint={npoint} cs={cs}")
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_fps_cluster_rounds(case):
+    """The CLUSTER schedule in rounds (a run of centers certified per
+    exchange) against the oracle on random clouds of 4k-140k points:
+    lattice coordinates (exact ties), tight clusters, duplicates, every
+    cluster size the cloud admits from 2 to 16, and sample counts that end
+    runs early or exhaust the cloud."""
+    rng = np.random.default_rng(9100 + case)
+    B = int(rng.integers(1, 3))
+    N = int(rng.integers(4096, 140_000))
+    x = cloud(rng, B, N)
+    npoint = int(rng.choice([1, 2, 64, 600, 2048, 4096]))
+    start = int(rng.integers(0, N))
+    cs = int(rng.integers(max(2, -(-N // 9216)), 17))   # 9,216 points per block at most
+    got = pc.pc_fps(to_dev(x), npoint, start, strategy=pc.PC_FPS_CLUSTER,
+                    cluster_size=cs).cpu().numpy()
+    want = oracle.fps(x, npoint, start, threads=THREADS)
+    assert_idx_equal(got, want, f"fuzz fps rounds B={B} N={N} cs={cs} npoint={npoint}")
