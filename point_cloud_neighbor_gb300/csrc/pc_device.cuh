@@ -23,6 +23,15 @@ __device__ __forceinline__ float sqdist(float ax, float ay, float az,
                      __fmul_rn(dz, dz));
 }
 
+// The smallest of three floats in one instruction (three-operand min.f32,
+// sm_100 and later).  A NaN operand is ignored unless all three are NaN, as
+// with fminf; the filters use it only on values that are never NaN.
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Packed f32x2 arithmetic in PTX.  add2_rn is one round-to-nearest-even
 // addition per half.  Squares are NOT written as mul.rn.f32x2: ptxas fuses a
 // single-use packed multiply into the packed add that consumes it (an FMA,

@@ -85,7 +85,7 @@ __device__ __forceinline__ bool filter_any(const float2 (&x)[P],
         float2 v = fma2_rn(x[p], make_float2(axy.x, axy.y), w[p]);
         v = fma2_rn(y[p], make_float2(axy.z, axy.w), v);
         v = fma2_rn(z[p], make_float2(azt.x, azt.y), v);
-        m = fminf(m, fminf(v.x, v.y));
+        m = fmin3(m, v.x, v.y);
     }
     return m <= azt.z;
 }

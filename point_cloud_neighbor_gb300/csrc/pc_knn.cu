@@ -711,7 +711,7 @@ __device__ __forceinline__ void lane_pass1(const float4 *ck, int nsteps,
             const int step = s0 + ss;
             const float4 *row = ck + 8 * step;
             const int x = ss << (3 - KL_SB);  // the row's slot swizzle
-            float mu[NQ][4];  // min of t' over each pair of points
+            float mn[NQ];  // running min of t' over the step's points
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float4 A = row[(2 * u) ^ x];
@@ -722,14 +722,11 @@ __device__ __forceinline__ void lane_pass1(const float4 *ck, int nsteps,
                                           make_float2(Z.z, Z.w));
                     v = __ffma2_rn(make_float2(A.z, A.w), ay[q], v);
                     v = __ffma2_rn(make_float2(Z.x, Z.y), az[q], v);
-                    mu[q][u] = fminf(v.x, v.y);
+                    mn[q] = u == 0 ? fminf(v.x, v.y) : fmin3(mn[q], v.x, v.y);
                 }
             }
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                const float mn = fminf(fminf(mu[q][0], mu[q][1]), fminf(mu[q][2], mu[q][3]));
-                pend[q] |= (mn <= thr[q] ? 1u : 0u) << step;
-            }
+            for (int q = 0; q < NQ; ++q) pend[q] |= (mn[q] <= thr[q] ? 1u : 0u) << step;
         }
     }
 }
