@@ -96,13 +96,15 @@ int pc_version(void);
  * Schedules (chosen from B and N): one thread block per cloud, one thread
  * block cluster per cloud (distributed shared memory), or -- for clouds too
  * large for one cluster -- a cooperative grid of clusters per cloud: the
- * blocks of each cluster exchange through distributed shared memory and each
- * cluster's first block publishes the cluster's best candidate (a tagged key
- * and the point's coordinates, four 64-bit words) per step through the
- * workspace and sends the winner back to its cluster (with
- * cluster_size 1 in pc_fps_ex, one level: one 64-bit key per block and
- * step).  Only the grid schedule uses scratch; the cluster and grid
- * schedules bound their device-side waits: if a wait runs out the kernel
+ * blocks of each cluster send their lists of best points to the cluster's
+ * first block through distributed shared memory, which publishes the
+ * cluster's summary (up to 128 listed points and a bound, 4128 bytes per
+ * cluster and round parity) through the workspace, and every block
+ * certifies the same run of centers from all clusters' summaries (the
+ * rounds of pc_fps_set_batched; with rounds off, one tagged key and the
+ * point's coordinates per cluster and step; with cluster_size 1 in
+ * pc_fps_ex, one level: one 64-bit key per block and step).  Only the grid
+ * schedule uses scratch; the cluster and grid schedules bound their device-side waits: if a wait runs out the kernel
  * stops, writes -1 into the remaining out_idx slots of that cloud and raises
  * the device status word (PC_ERR_DEVICE_TIMEOUT).
  *
@@ -155,14 +157,16 @@ int pc_fps_plan(int64_t B, int64_t N, int strategy, int cluster_size,
  * or break its accounting, or a real-time loop with a fixed footprint).  The
  * mps-pointops pages have no counterpart of this entry point.
  *
- * The grid schedule's exchange scratch is a fixed array of 4096 64-bit words
- * (32 KiB) inside the library, present on every device that loads the
- * library until the process exits; the call allocates nothing.  Limit: the
- * schedule needs B * max(2 * blocks_per_cloud, 32 * clusters per cloud)
- * words (one 128-byte line per cluster and step parity with two levels; 2
- * words per block with one level, when blocks_per_cloud is not a multiple
- * of 4), at most 4096 in all, and the blocks are bounded by the SM count;
- * larger requests return PC_ERR_INVALID_ARGUMENT.  Arguments and results are
+ * The grid schedule's exchange scratch is a fixed array of 16384 64-bit
+ * words (128 KiB) inside the library, present on every device that loads
+ * the library until the process exits; the call allocates nothing.  The
+ * two-level grid runs in rounds when its summaries fit in the array (B * 2 *
+ * clusters per cloud slots of 4128 bytes), else one center per step.  Limit:
+ * the step-by-step schedule needs B * max(2 * blocks_per_cloud, 32 *
+ * clusters per cloud) words (one 128-byte line per cluster and step parity
+ * with two levels; 2 words per block with one level, when blocks_per_cloud
+ * is not a multiple of 4), at most 16384 in all, and the blocks are bounded
+ * by the SM count; larger requests return PC_ERR_INVALID_ARGUMENT.  Arguments and results are
  * those of pc_fps_ex with strategy PC_FPS_GRID and cluster_size 0
  * (blocks_per_cloud 0 = automatic).
  *
@@ -521,10 +525,12 @@ void pc_debug_set_fps_grid_stall(int enable);
 void pc_set_sm_reserve(int sms);
 
 /*
- * FPS of the CLUSTER schedule in rounds (default on): per exchange between
- * the blocks of a cloud, a run of several centers is certified from each
- * warp's listed points and the bound of its other points (project page,
- * "Farthest point sampling": the same centers as one step at a time).
+ * FPS of the CLUSTER and two-level GRID schedules in rounds (default on):
+ * per exchange between the blocks of a cloud, a run of several centers is
+ * certified from each warp's listed points and the bound of its other
+ * points (project page, "Farthest point sampling": the same centers as one
+ * step at a time); in the grid each cluster first summarizes its blocks'
+ * lists.
  * pc_fps_set_batched(0) makes every exchange take one center, 1 restores
  * the rounds; applies to launches enqueued after the call on every device.
  * Returns the previous setting.

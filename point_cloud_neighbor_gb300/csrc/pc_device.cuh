@@ -320,6 +320,16 @@ __device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t *p, uint64_t v) {
                  : "memory");
 }
 
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu_u32(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Record the first device-side error in the library's status word.
 __device__ __forceinline__ void raise_status(int *status, int code) {
     if (status) atomicCAS(status, 0, code);

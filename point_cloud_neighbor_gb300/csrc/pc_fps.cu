@@ -354,29 +354,34 @@ __host__ __device__ constexpr size_t fps_rounds_smem(int chunk, int warps, int n
 
 // Every warp of a block (nscan of them), once the round's lists are in,
 // pass 1: B, the largest bound of an unlisted point (returned); for lists
-// warp, warp + nscan, ... (W: the listing warps of a block) the number of
-// entries above B (cnt[list]) and the warp's largest entry (smallest index on
-// a tie) in *wfirst as (key, index, offset).
-__device__ __forceinline__ unsigned fr_count(const unsigned char *lists, int nl, int W,
-                                             int nscan, unsigned msg, int *cnt,
-                                             uint4 *wfirst) {
+// warp, warp + nscan, ... the number of entries above B (cnt[list]) and the
+// warp's largest entry (smallest index on a tie) in *wfirst as (key, index,
+// offset).  A list is `msg` bytes: `per` entries, then `nbnd` bounds (uint4,
+// key in .x) -- a block's list (per = W * FR_CW, nbnd = W) or a cluster's
+// summary (per = FR_SUM, nbnd = 1), of which only the first lens[l] entries
+// are read when lens is given.
+__device__ __forceinline__ unsigned fr_count(const unsigned char *lists, int nl, int per,
+                                             int nbnd, int nscan, unsigned msg, int *cnt,
+                                             uint4 *wfirst, const int *lens = nullptr) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int per = W * FR_CW;  // entries per list
+    // the bounds: lane = (list of its group, bound), 32 / nbnd lists at a time
     unsigned bnd = 0u;
-    for (int l = 0; l < nl; ++l)
-        if (lane < W)
+    const int lpi = 32 / nbnd, li = lane / nbnd, bi = lane - li * nbnd;
+    if (li < lpi)
+        for (int l = li; l < nl; l += lpi)
             bnd = max(bnd, reinterpret_cast<const uint4 *>(lists + size_t(l) * msg +
-                                                           size_t(per) * 32)[lane].x);
+                                                           size_t(per) * 32)[bi].x);
     bnd = __reduce_max_sync(FULL, bnd);
     unsigned gh = 0u, gj = FULL;
     int go = 0;
     for (int l = warp; l < nl; l += nscan) {
         int n = 0;
-        for (int k0 = 0; k0 < per; k0 += 32) {
+        const int len = lens ? lens[l] : per;
+        for (int k0 = 0; k0 < len; k0 += 32) {
             const int k = k0 + lane;
             const int off = l * int(msg) + k * 32;
             unsigned h = 0u, j = FULL;
-            if (k < per) {
+            if (k < len) {
                 const uint2 hj = *reinterpret_cast<const uint2 *>(lists + off);
                 h = hj.x;
                 j = hj.y;
@@ -397,26 +402,34 @@ __device__ __forceinline__ unsigned fr_count(const unsigned char *lists, int nl,
     return bnd;
 }
 
+// The sum of cnt[0 .. l) (l <= nl, the same in every lane of the warp).
+__device__ __forceinline__ int fr_before(const int *cnt, int l) {
+    const int lane = threadIdx.x & 31;
+    int acc = 0;
+    for (int i = lane; i < l; i += 32) acc += cnt[i];
+    return __reduce_add_sync(FULL, acc);
+}
+
 // Pass 2, after a barrier: every entry above B gets the candidate position
 // 1 + (entries above B in the lists before its own) + (those before it in its
 // list) -- the same in every block of the cloud, whatever the warps' timing
 // -- and its byte offset goes to cidx; the ones at positions past
 // 32 * FR_LIST raise *s_over to their m instead (every block then keeps the
 // same candidates and the same bound, and certifies the same run).
-__device__ __forceinline__ void fr_place(const unsigned char *lists, int nl, int W,
+__device__ __forceinline__ void fr_place(const unsigned char *lists, int nl, int per,
                                          int nscan, unsigned msg, unsigned bnd,
-                                         const int *cnt, int *cidx, unsigned *s_over) {
+                                         const int *cnt, int *cidx, unsigned *s_over,
+                                         const int *lens = nullptr) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int per = W * FR_CW;
     constexpr int CAP = 32 * FR_LIST;
     unsigned over = 0u;
     for (int l = warp; l < nl; l += nscan) {
-        int base = 1;
-        for (int i = 0; i < l; ++i) base += cnt[i];
-        for (int k0 = 0; k0 < per; k0 += 32) {
+        int base = 1 + fr_before(cnt, l);
+        const int len = lens ? lens[l] : per;
+        for (int k0 = 0; k0 < len; k0 += 32) {
             const int k = k0 + lane;
             const int off = l * int(msg) + k * 32;
-            const unsigned h = k < per ? *reinterpret_cast<const unsigned *>(lists + off) : 0u;
+            const unsigned h = k < len ? *reinterpret_cast<const unsigned *>(lists + off) : 0u;
             const bool keep = h > bnd;
             const unsigned bal = __ballot_sync(FULL, keep);
             const int pos = base + __popc(bal & lanemask_lt());
@@ -528,6 +541,55 @@ __device__ __forceinline__ void fr_pick(const unsigned char *lists, int nscan, u
     }
 }
 
+// A point warp's list for the round (every lane of the warp): its entries
+// at mine[0 .. FR_CW) (empty ones with key 0) and its bound at *mybound.
+template <int PPT>
+__device__ __forceinline__ void fr_list(const ThreadPoints<PPT> &pt, const float *scoord,
+                                        int lo, int T, FrEntry *mine, uint4 *mybound) {
+    const int lane = threadIdx.x & 31;
+    // the lane's best point (its slots are in increasing index, so a
+    // strict ">" keeps the smaller index on a tie) and its second largest m
+    float best = -1.0f, second = -1.0f;
+    int bp = 0;
+#pragma unroll
+    for (int p = 0; p < PPT; ++p) {
+        const float v = pt.m[p];
+        if (v > best) {
+            second = best;
+            best = v;
+            bp = p;
+        } else {
+            second = fmaxf(second, v);
+        }
+    }
+    const unsigned khi = best >= 0.0f ? __float_as_uint(best) + 1u : 0u;
+    const unsigned kj = khi ? unsigned(lo + bp * T + int(threadIdx.x)) : FULL;
+    const unsigned shi = second >= 0.0f ? __float_as_uint(second) + 1u : 0u;
+    // the warp's list (its best first, then lanes whose best is above
+    // the bound, in lane order) and its bound
+    unsigned whi, wj;
+    warp_argmax_hi_min_lo(khi, kj, whi, wj);
+    const int wl = __ffs(__ballot_sync(FULL, khi == whi && kj == wj)) - 1;
+    unsigned bw = __reduce_max_sync(FULL, shi);
+    const unsigned cand = __ballot_sync(FULL, khi > bw && lane != wl);
+    const int crank = __popc(cand & lanemask_lt());
+    const bool is_c = (cand >> lane) & 1u;
+    bw = max(bw, __reduce_max_sync(FULL, is_c && crank >= FR_CW - 1 ? khi : 0u));
+    const bool listed = (lane == wl && whi != 0u) || (is_c && crank < FR_CW - 1);
+    if (listed) {
+        const float *c = scoord + (int(kj) - lo) * 3;
+        FrEntry *e = mine + (lane == wl ? 0 : 1 + crank);
+        e->hi = khi;
+        e->j = kj;
+        e->x = c[0];
+        e->y = c[1];
+        e->z = c[2];
+    }
+    const int nlisted = (whi != 0u ? 1 : 0) + min(__popc(cand), FR_CW - 1);
+    if (lane >= nlisted && lane < FR_CW) mine[lane].hi = 0u;
+    if (lane == 0) *mybound = make_uint4(bw, 0u, 0u, 0u);
+}
+
 // Threads a rounds kernel with PPT points per thread may use: the point
 // threads of the schedules (at most 256 with 32 points, 384 with fewer) and
 // the resolving warp.
@@ -614,6 +676,22 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
             pt.m[2 * i + 1] = fminf(pt.m[2 * i + 1], s.y);
         }
     };
+    // lower them by two centers at once (min is exact in any order)
+    auto apply2 = [&](const float4 c0, const float4 c1) {
+        const float2 ncx = make_float2(-c0.x, -c0.x);
+        const float2 ncy = make_float2(-c0.y, -c0.y);
+        const float2 ncz = make_float2(-c0.z, -c0.z);
+        const float2 mcx = make_float2(-c1.x, -c1.x);
+        const float2 mcy = make_float2(-c1.y, -c1.y);
+        const float2 mcz = make_float2(-c1.z, -c1.z);
+#pragma unroll
+        for (int i = 0; i < PPT / 2; ++i) {
+            const float2 s = sqdist2(pt.x[i], pt.y[i], pt.z[i], ncx, ncy, ncz, nz0);
+            const float2 u = sqdist2(pt.x[i], pt.y[i], pt.z[i], mcx, mcy, mcz, nz0);
+            pt.m[2 * i] = fmin3(pt.m[2 * i], s.x, u.x);
+            pt.m[2 * i + 1] = fmin3(pt.m[2 * i + 1], s.y, u.y);
+        }
+    };
     FrEntry *mine = reinterpret_cast<FrEntry *>(sbuf) + warp * FR_CW;
     uint4 *mybound = reinterpret_cast<uint4 *>(sbuf + size_t(W) * FR_CW * 32) + warp;
     int t = 1;  // centers output so far
@@ -622,49 +700,7 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
         // 1. the start lowers the points' m (later centers were applied while
         // the resolving warp picked them)
         if (round == 0 && !rw) apply(cen[0]);
-        if (!rw) {
-            // 2. the lane's best point (its slots are in increasing index, so a
-            // strict ">" keeps the smaller index on a tie) and its second largest m
-            float best = -1.0f, second = -1.0f;
-            int bp = 0;
-    #pragma unroll
-            for (int p = 0; p < PPT; ++p) {
-                const float v = pt.m[p];
-                if (v > best) {
-                    second = best;
-                    best = v;
-                    bp = p;
-                } else {
-                    second = fmaxf(second, v);
-                }
-            }
-            const unsigned khi = best >= 0.0f ? __float_as_uint(best) + 1u : 0u;
-            const unsigned kj = khi ? unsigned(lo + bp * T + int(threadIdx.x)) : FULL;
-            const unsigned shi = second >= 0.0f ? __float_as_uint(second) + 1u : 0u;
-            // 3. the warp's list (its best first, then lanes whose best is above
-            // the bound, in lane order) and its bound
-            unsigned whi, wj;
-            warp_argmax_hi_min_lo(khi, kj, whi, wj);
-            const int wl = __ffs(__ballot_sync(FULL, khi == whi && kj == wj)) - 1;
-            unsigned bw = __reduce_max_sync(FULL, shi);
-            const unsigned cand = __ballot_sync(FULL, khi > bw && lane != wl);
-            const int crank = __popc(cand & lanemask_lt());
-            const bool is_c = (cand >> lane) & 1u;
-            bw = max(bw, __reduce_max_sync(FULL, is_c && crank >= FR_CW - 1 ? khi : 0u));
-            const bool listed = (lane == wl && whi != 0u) || (is_c && crank < FR_CW - 1);
-            if (listed) {
-                const float *c = scoord + (int(kj) - lo) * 3;
-                FrEntry *e = mine + (lane == wl ? 0 : 1 + crank);
-                e->hi = khi;
-                e->j = kj;
-                e->x = c[0];
-                e->y = c[1];
-                e->z = c[2];
-            }
-            const int nlisted = (whi != 0u ? 1 : 0) + min(__popc(cand), FR_CW - 1);
-            if (lane >= nlisted && lane < FR_CW) mine[lane].hi = 0u;
-            if (lane == 0) *mybound = make_uint4(bw, 0u, 0u, 0u);
-        }
+        if (!rw) fr_list<PPT>(pt, scoord, lo, T, mine, mybound);
         fence_proxy_async_smem();  // the list, for the bulk copies
         __syncthreads();
         if (rw) {
@@ -693,13 +729,13 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
         // 5. every warp scans its share of the lists; the resolving warp
         // certifies the run
         const unsigned char *lists = recv + size_t(par) * a.nblocks * msg;
-        const unsigned bnd = fr_count(lists, a.nblocks, W, NW, msg, lcnt, wfirst + warp);
+        const unsigned bnd =
+            fr_count(lists, a.nblocks, W * FR_CW, W, NW, msg, lcnt, wfirst + warp);
         __syncthreads();
-        fr_place(lists, a.nblocks, W, NW, msg, bnd, lcnt, cidx, s_over);
-        if (threadIdx.x == 0) {  // candidates in all: the first center and the counts
-            int total = 1;
-            for (int l = 0; l < a.nblocks; ++l) total += lcnt[l];
-            *s_total = total;
+        fr_place(lists, a.nblocks, W * FR_CW, NW, msg, bnd, lcnt, cidx, s_over);
+        if (warp == 0) {  // candidates in all: the first center and the counts
+            const int total = 1 + fr_before(lcnt, a.nblocks);
+            if (lane == 0) *s_total = total;
         }
         __syncthreads();
         if (rw) {
@@ -718,7 +754,15 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
                 __threadfence_block();
                 const int pub = *s_pub;
                 __threadfence_block();
-                for (; c < pub; ++c) apply(cen[c]);
+                while (c < pub) {  // two at a time where two are out
+                    if (c + 1 < pub) {
+                        apply2(cen[c], cen[c + 1]);
+                        c += 2;
+                    } else {
+                        apply(cen[c]);
+                        ++c;
+                    }
+                }
                 if (fin) break;
                 if ((spin & 255) == 255 && global_timer_ns() - w0 > a.timeout_ns) {
                     if (lane == 0) *s_fail = 1;
@@ -1060,6 +1104,356 @@ __global__ void __launch_bounds__(fps_max_threads(PPT), 1)
     cluster_sync_all();  // no block exits while peers may write
 }
 
+// ---------------------------------------------------------------------------
+// GRID schedule in rounds (two levels): the rounds above for a cloud spread
+// over a cooperative grid of clusters.  Per round:
+//   1. every point warp lists its points (as in a cluster) and each block
+//      sends its list to its cluster's block 0 (its leader) with one bulk
+//      copy into distributed shared memory;
+//   2. the leader summarizes its cluster: Bc, the largest bound of its lists;
+//      the cluster's largest listed point first; then, in list order, the
+//      listed points above Bc, FR_SUM in all (points past that raise Bc to
+//      their m, as a block's overflow does); it writes the summary, its
+//      length and Bc to the cluster's slot of the workspace and then the
+//      round's tag with a release store;
+//   3. every block waits for the tags of all clusters of its cloud (acquire;
+//      bounded), copies the summaries into shared memory (L2 loads) and
+//      certifies the run from them exactly as a cluster certifies it from
+//      its blocks' lists: B is the largest Bc, the first center the largest
+//      summarized point (the cloud's largest: every warp lists its best and
+//      every cluster puts its largest first), later centers the summarized
+//      points still strictly above B; every point left out of a summary or
+//      of the candidates is at most B.  Positions follow list order, so every
+//      block keeps the same candidates and certifies the same run.
+// A summary slot is double-buffered by round parity: a leader writes round
+// r + 2 only after all its blocks finished round r + 1, which needs every
+// cluster's round r + 1 summary, which each cluster publishes only after
+// all its blocks finished round r -- so no block still reads round r.
+// Every wait is bounded.
+constexpr int FR_SUM = 32 * FR_LIST;  // entries of a cluster's summary
+constexpr int FR_MAX_LISTS = 64;      // lists or summaries a block scans at most
+
+// A summary slot: FR_SUM entries (32 B), the bound (uint4, key in .x), the
+// tag (uint4: round + 1 in .x, the number of entries written in .y).
+__host__ __device__ constexpr unsigned fr_sum_bytes() { return FR_SUM * 32u + 32u; }
+
+// Threads of a grid rounds kernel: the point threads and the resolving warp,
+// at most 10 warps with 32 points a thread and 12 with 24 (three warps on
+// an SM sub-partition leave 168 registers a thread for the points), 13 with
+// fewer.
+__host__ __device__ constexpr int fgr_max_threads(int ppt) {
+    return ppt >= 32 ? 320 : ppt >= 24 ? 384 : 416;
+}
+
+// Shared memory: the points, the block's list, the leader's copies of its
+// cluster's lists, the cloud's summaries, then the run's state as in
+// fps_rounds_smem.
+__host__ __device__ constexpr size_t fps_grid_rounds_smem(int chunk, int warps, int cs,
+                                                          int ncl) {
+    return fr_align16(size_t(chunk) * 12) + fr_msg_bytes(warps) +
+           size_t(cs) * fr_msg_bytes(warps) + size_t(ncl) * fr_sum_bytes() +
+           size_t(FR_RMAX) * 16 + 32 * FR_LIST * sizeof(int) + 32 * sizeof(uint4) +
+           2 * FR_MAX_LISTS * sizeof(int) + 2 * sizeof(uint64_t) + 48;
+}
+
+// Workspace of the grid rounds: per cloud [2 parities][ncl] summary slots.
+__host__ __device__ constexpr size_t fps_grid_rounds_ws(int64_t B, int ncl) {
+    return size_t(B) * 2 * size_t(ncl) * fr_sum_bytes();
+}
+
+template <int PPT>
+__global__ void __launch_bounds__(fgr_max_threads(PPT), 1)
+    fps_grid_rounds_kernel(const FpsArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int T = int(blockDim.x) - 32;  // threads holding points
+    const int W = T >> 5;                // their warps, which list
+    const int NW = W + 1;                // and the resolving warp
+    const bool rw = warp == W;
+    const unsigned msg = fr_msg_bytes(W);
+    const unsigned smsg = fr_sum_bytes();
+    float *scoord = reinterpret_cast<float *>(smem);
+    unsigned char *sbuf = smem + fr_align16(size_t(a.chunk) * 12);
+    unsigned char *recv = sbuf + msg;                          // [cs] lists (leader)
+    unsigned char *gsum = recv + size_t(a.cs) * msg;           // [ncl] summaries
+    float4 *cen = reinterpret_cast<float4 *>(gsum + size_t(a.ncl) * smsg);
+    int *cidx = reinterpret_cast<int *>(cen + FR_RMAX);
+    uint4 *wfirst = reinterpret_cast<uint4 *>(cidx + 32 * FR_LIST);
+    int *lcnt = reinterpret_cast<int *>(wfirst + 32);  // [FR_MAX_LISTS]
+    int *glen = lcnt + FR_MAX_LISTS;  // [FR_MAX_LISTS] entries of each summary
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(glen + FR_MAX_LISTS);
+    int *s_nc = reinterpret_cast<int *>(xbar + 2);
+    int *s_fail = s_nc + 1;
+    int *s_total = s_nc + 2;
+    unsigned *s_over = reinterpret_cast<unsigned *>(s_nc + 3);
+    volatile int *s_pub = s_nc + 4;
+    volatile int *s_fin = s_nc + 5;
+    int *s_first = s_nc + 6;  // leader: the offset of its cluster's largest entry
+
+    // every distributed-shared-memory address below targets rank 0 of a
+    // cluster of a.cs blocks; a launch without that shape stops here
+    if (cluster_nctarank() != unsigned(a.cs) || a.cs > FR_MAX_LISTS ||
+        a.ncl > FR_MAX_LISTS) {
+        if (threadIdx.x == 0) raise_status(a.status, 3 /* PC_ERR_CUDA */);
+        return;
+    }
+    const unsigned rank = cluster_ctarank();
+    const int b = blockIdx.x / a.nblocks;
+    const int r = blockIdx.x % a.nblocks;  // block of the cloud
+    const int cl = r / a.cs;               // cluster of the cloud
+    const float *x = a.xyz + size_t(b) * size_t(a.N) * 3;
+    const int lo = r * a.chunk;
+    const int hi = min(a.N, lo + a.chunk);
+    const float2 nz0 = make_float2(a.negzero, a.negzero);
+    const unsigned xbytes = unsigned(a.cs) * msg;
+    // slot (parity p, cluster c) of this cloud
+    unsigned char *ws = reinterpret_cast<unsigned char *>(a.slots) +
+                        size_t(b) * 2 * size_t(a.ncl) * smsg;
+    auto slot = [&](int p, int c) { return ws + (size_t(p) * a.ncl + c) * smsg; };
+
+    ThreadPoints<PPT> pt;
+    if (!rw) {
+        fps_load_points<PPT>(x, lo, hi, T, pt, scoord);
+    } else {
+#pragma unroll
+        for (int p = 0; p < PPT; ++p) pt.m[p] = -1.0f;
+#pragma unroll
+        for (int i = 0; i < PPT / 2; ++i) pt.x[i] = pt.y[i] = pt.z[i] = make_float2(0.f, 0.f);
+    }
+    int64_t *out = a.out + size_t(b) * a.npoint;
+    if (threadIdx.x == 0) {
+        cen[0] = make_float4(x[size_t(a.start) * 3 + 0], x[size_t(a.start) * 3 + 1],
+                             x[size_t(a.start) * 3 + 2], 0.f);
+        *s_nc = 1;
+        *s_fail = 0;
+        *s_total = 1;
+        *s_over = 0u;
+        *s_pub = 0;
+        *s_fin = 0;
+        if (r == 0) out[0] = a.start;
+        // the leader's exchange mbarriers, one per round parity
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (rank == 0) {
+            mbar_arrive_expect_tx(&xbar[0], xbytes);
+            mbar_arrive_expect_tx(&xbar[1], xbytes);
+        }
+    }
+    __syncthreads();
+    cluster_sync_all();  // the leader's barriers exist before any copy
+
+    auto apply = [&](const float4 cc) {
+        const float2 ncx = make_float2(-cc.x, -cc.x);
+        const float2 ncy = make_float2(-cc.y, -cc.y);
+        const float2 ncz = make_float2(-cc.z, -cc.z);
+#pragma unroll
+        for (int i = 0; i < PPT / 2; ++i) {
+            const float2 s = sqdist2(pt.x[i], pt.y[i], pt.z[i], ncx, ncy, ncz, nz0);
+            pt.m[2 * i] = fminf(pt.m[2 * i], s.x);
+            pt.m[2 * i + 1] = fminf(pt.m[2 * i + 1], s.y);
+        }
+    };
+    // lower them by two centers at once (min is exact in any order)
+    auto apply2 = [&](const float4 c0, const float4 c1) {
+        const float2 ncx = make_float2(-c0.x, -c0.x);
+        const float2 ncy = make_float2(-c0.y, -c0.y);
+        const float2 ncz = make_float2(-c0.z, -c0.z);
+        const float2 mcx = make_float2(-c1.x, -c1.x);
+        const float2 mcy = make_float2(-c1.y, -c1.y);
+        const float2 mcz = make_float2(-c1.z, -c1.z);
+#pragma unroll
+        for (int i = 0; i < PPT / 2; ++i) {
+            const float2 s = sqdist2(pt.x[i], pt.y[i], pt.z[i], ncx, ncy, ncz, nz0);
+            const float2 u = sqdist2(pt.x[i], pt.y[i], pt.z[i], mcx, mcy, mcz, nz0);
+            pt.m[2 * i] = fmin3(pt.m[2 * i], s.x, u.x);
+            pt.m[2 * i + 1] = fmin3(pt.m[2 * i + 1], s.y, u.y);
+        }
+    };
+    FrEntry *mine = reinterpret_cast<FrEntry *>(sbuf) + warp * FR_CW;
+    uint4 *mybound = reinterpret_cast<uint4 *>(sbuf + size_t(W) * FR_CW * 32) + warp;
+    int t = 1;  // centers output so far
+    for (int round = 0; t < a.npoint; ++round) {
+        const int par = round & 1;
+        const unsigned tag = unsigned(round) + 1u;
+        if (round == 0 && !rw) apply(cen[0]);
+        if (!rw) fr_list<PPT>(pt, scoord, lo, T, mine, mybound);
+        fence_proxy_async_smem();  // the list, for the bulk copy
+        __syncthreads();
+        // 1. the block's list to its leader; the list may be rewritten once
+        // the copy has read it
+        if (rw && lane == 0) {
+            const uint32_t dst = map_shared_rank(recv + size_t(rank) * msg, 0u);
+            const uint32_t bar = map_shared_rank(&xbar[par], 0u);
+            bulk_copy_to_cluster(dst, sbuf, msg, bar);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+        // 2. the leader: its cluster's summary, then the round's tag
+        if (rank == 0) {
+            const unsigned ph = unsigned(round >> 1) & 1u;
+            const bool got =
+                __all_sync(FULL, mbar_wait_cluster_bounded(&xbar[par], ph, a.timeout_ns));
+            if (threadIdx.x == 0 && got) mbar_arrive_expect_tx(&xbar[par], xbytes);
+            if (!got && lane == 0) *s_fail = 1;
+            __syncthreads();
+            if (!*s_fail) {
+                const unsigned bc =
+                    fr_count(recv, a.cs, W * FR_CW, W, NW, msg, lcnt, wfirst + warp);
+                __syncthreads();
+                fr_place(recv, a.cs, W * FR_CW, NW, msg, bc, lcnt, cidx, s_over);
+                if (warp == 0) {  // the cluster's largest entry and the candidates' count
+                    const uint4 f = lane < NW ? wfirst[lane] : make_uint4(0u, FULL, 0u, 0u);
+                    unsigned fh, fj;
+                    warp_argmax_hi_min_lo(f.x, f.y, fh, fj);
+                    const int who = __ffs(__ballot_sync(FULL, f.x == fh && f.y == fj)) - 1;
+                    const int off = int(__shfl_sync(FULL, f.z, who));
+                    const int total = 1 + fr_before(lcnt, a.cs);
+                    if (lane == 0) {
+                        *s_first = fh != 0u ? off : -1;
+                        *s_total = total;
+                    }
+                }
+                __syncthreads();
+                unsigned char *sl = slot(par, cl);
+                const int first = *s_first;
+                const int total = *s_total;
+                const int n = min(total, FR_SUM);  // positions written
+                for (int e = int(threadIdx.x); e < n; e += int(blockDim.x)) {
+                    int off = e == 0 ? first : (e < total ? cidx[e] : -1);
+                    if (e > 0 && off == first) off = -1;  // already at position 0
+                    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+                    if (off >= 0) {
+                        v0 = reinterpret_cast<const uint4 *>(recv + off)[0];
+                        v1 = reinterpret_cast<const uint4 *>(recv + off)[1];
+                    }
+                    reinterpret_cast<uint4 *>(sl + size_t(e) * 32)[0] = v0;
+                    reinterpret_cast<uint4 *>(sl + size_t(e) * 32)[1] = v1;
+                }
+                if (threadIdx.x == 0) {
+                    *reinterpret_cast<uint4 *>(sl + FR_SUM * 32) =
+                        make_uint4(max(bc, *s_over), 0u, 0u, 0u);
+                    reinterpret_cast<unsigned *>(sl + FR_SUM * 32 + 16)[1] = unsigned(n);
+                }
+                __syncthreads();
+                // testing hook: cluster 0 of the first cloud withholds round 0
+                const bool withhold = (a.stall & 1) && b == 0 && cl == 0 && round == 0;
+                // the block's writes, ordered by the barrier, are released with
+                // the tag
+                if (threadIdx.x == 0 && !withhold)
+                    st_release_gpu_u32(reinterpret_cast<unsigned *>(sl + FR_SUM * 32 + 16),
+                                       tag);
+            }
+        }
+        // 3. every block: the round's summaries of all clusters of the cloud
+        if (rw && !*s_fail) {
+            bool ok = true;
+            for (int c = lane; c < a.ncl && ok; c += 32) {
+                const unsigned *tp =
+                    reinterpret_cast<const unsigned *>(slot(par, c) + FR_SUM * 32 + 16);
+                const uint64_t t0 = global_timer_ns();
+                for (int spin = 0;; ++spin) {
+                    if (ld_acquire_gpu_u32(tp) == tag) break;
+                    if ((spin & 63) == 63 && global_timer_ns() - t0 > a.timeout_ns) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (ok) glen[c] = min(int(__ldcg(tp + 1)), FR_SUM);
+            }
+            if (!__all_sync(FULL, ok) && lane == 0) *s_fail = 1;
+        }
+        __syncthreads();
+        if (!*s_fail) {  // each summary's entries and bound (a warp per summary)
+            for (int c = warp; c < a.ncl; c += NW) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(slot(par, c));
+                uint4 *dst = reinterpret_cast<uint4 *>(gsum + size_t(c) * smsg);
+                const int n16 = 2 * glen[c];
+                for (int v = lane; v < n16; v += 32) dst[v] = __ldcg(src + v);
+                if (lane == 0) dst[2 * FR_SUM] = __ldcg(src + 2 * FR_SUM);
+            }
+        }
+        if (threadIdx.x == 0) {  // the leader's counters, for the cloud's candidates
+            *s_total = 1;
+            *s_over = 0u;
+        }
+        __syncthreads();
+        if (!*s_fail) {
+            // 4. the cloud's candidates and the run, as in fps_rounds_kernel
+            const unsigned bnd =
+                fr_count(gsum, a.ncl, FR_SUM, 1, NW, smsg, lcnt, wfirst + warp, glen);
+            __syncthreads();
+            fr_place(gsum, a.ncl, FR_SUM, NW, smsg, bnd, lcnt, cidx, s_over, glen);
+            if (warp == 0) {
+                const int total = 1 + fr_before(lcnt, a.ncl);
+                if (lane == 0) *s_total = total;
+            }
+            __syncthreads();
+            if (rw) {
+                fr_pick(gsum, NW, bnd, min(FR_RMAX, a.npoint - t), cidx, wfirst, *s_total,
+                        *s_over, cen, s_nc, s_pub, s_fin, r == 0 ? out + t : nullptr);
+            } else {
+                int c = 0;
+                const uint64_t w0 = global_timer_ns();
+                for (int spin = 0;; ++spin) {
+                    const int fin = *s_fin;
+                    __threadfence_block();
+                    const int pub = *s_pub;
+                    __threadfence_block();
+                    while (c < pub) {  // two at a time where two are out
+                        if (c + 1 < pub) {
+                            apply2(cen[c], cen[c + 1]);
+                            c += 2;
+                        } else {
+                            apply(cen[c]);
+                            ++c;
+                        }
+                    }
+                    if (fin) break;
+                    if ((spin & 255) == 255 && global_timer_ns() - w0 > a.timeout_ns) {
+                        if (lane == 0) *s_fail = 1;
+                        break;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        const int taken = *s_nc;
+        if (*s_fail || taken <= 0) {
+            raise_status(a.status, *s_fail ? 4 /* PC_ERR_DEVICE_TIMEOUT */ : 3 /* PC_ERR_CUDA */);
+            if (r == 0)
+                for (int i = t + int(threadIdx.x); i < a.npoint; i += int(blockDim.x)) out[i] = -1;
+            break;
+        }
+        t += taken;
+        if (threadIdx.x == 0) {  // for the next round
+            *s_total = 1;
+            *s_over = 0u;
+            *s_pub = 0;
+            *s_fin = 0;
+        }
+    }
+    // no copy in flight and no block exits while peers may write
+    if (rw && lane == 0) bulk_wait_all();
+    cluster_sync_all();
+}
+
+template <int PPT>
+const void *fgr_ptr_t() {
+    return reinterpret_cast<const void *>(&fps_grid_rounds_kernel<PPT>);
+}
+
+const void *fps_grid_rounds_ptr(int ppt) {
+    switch (ppt) {
+        case 2: return fgr_ptr_t<2>();
+        case 4: return fgr_ptr_t<4>();
+        case 8: return fgr_ptr_t<8>();
+        case 16: return fgr_ptr_t<16>();
+        case 24: return fgr_ptr_t<24>();
+        default: return fgr_ptr_t<32>();
+    }
+}
+
 const void *fps_rounds_ptr(int ppt) {
     switch (ppt) {
         case 2: return reinterpret_cast<const void *>(&fps_rounds_kernel<2>);
@@ -1239,6 +1633,30 @@ FpsPlan plan_cgrid(const DeviceInfo &dev, int64_t B, int64_t N, int cs, int bpc_
                     size_t(B) * std::max<size_t>(2 * CG_SLOT_WORDS * size_t(bpc / cs),
                                                  2 * size_t(bpc));
                 p.workspace_bytes = (words * sizeof(uint64_t) + 255) & ~size_t(255);
+                p.step_workspace_bytes = p.workspace_bytes;
+                // in rounds: the same blocks with a resolving warp more, where
+                // its shared memory fits and every cluster stays resident
+                // (the step's shape, else 32 points a thread where the
+                // resolving warp would leave too few registers)
+                const int ncl = int(bpc / cs);
+                int rppt = p.ppt, rthreads = p.threads + 32;
+                if (rthreads > fgr_max_threads(rppt)) {
+                    rppt = 32;
+                    rthreads = std::max(32, round_up((p.chunk + 31) / 32, 32)) + 32;
+                }
+                const size_t rsmem =
+                    fps_grid_rounds_smem(p.chunk, rthreads / 32 - 1, cs, ncl);
+                if (rthreads <= fgr_max_threads(rppt) && ncl <= FR_MAX_LISTS &&
+                    cs <= FR_MAX_LISTS && rsmem <= dev.smem_per_block_optin &&
+                    max_active_clusters(fps_grid_rounds_ptr(rppt), cs, rthreads, rsmem) /
+                            std::max<int64_t>(B, 1) >= ncl) {
+                    p.grid_rounds = true;
+                    p.rounds_ppt = rppt;
+                    p.rounds_threads = rthreads;
+                    p.rounds_smem = rsmem;
+                    p.workspace_bytes = std::max(
+                        p.workspace_bytes, (fps_grid_rounds_ws(B, ncl) + 255) & ~size_t(255));
+                }
                 p.ok = true;
                 return p;
             }
@@ -1428,13 +1846,17 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
     a.negzero = -0.0f;
 
     const bool cgrid = plan.strategy == 3 && plan.cluster > 1;
-    const void *fn = cgrid ? fps_cgrid_ptr(plan.ppt) : fps_kernel_ptr(plan.strategy, plan.ppt);
-    size_t smem = plan.smem_bytes;
+    // two-level GRID in rounds (fps_grid_rounds_kernel) where the plan allows
+    const bool grounds = cgrid && plan.grid_rounds && fps_batched();
+    const void *fn = grounds  ? fps_grid_rounds_ptr(plan.rounds_ppt)
+                     : cgrid ? fps_cgrid_ptr(plan.ppt)
+                             : fps_kernel_ptr(plan.strategy, plan.ppt);
+    size_t smem = grounds ? plan.rounds_smem : plan.smem_bytes;
     // CLUSTER: several centers per exchange (fps_rounds_kernel) where its
     // lists fit; the step-by-step kernel otherwise.  (With one block per
     // cloud there is no exchange to share: one center per step is faster --
     // GB300, 96 clouds of 4096 points, 1024 samples: 0.41 ms vs 0.54.)
-    unsigned threads = unsigned(plan.threads);
+    unsigned threads = unsigned(grounds ? plan.rounds_threads : plan.threads);
     if (fps_batched() && plan.strategy == 2 && plan.threads + 32 <= fr_max_threads(plan.ppt)) {
         const size_t need = fps_rounds_smem(plan.chunk, plan.threads / 32, plan.cluster);
         const size_t rsmem = std::max(smem, need);
@@ -1463,8 +1885,7 @@ cudaError_t launch_fps(const DeviceInfo &dev, const FpsPlan &plan,
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             if (e != cudaSuccess) return e;
         }
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(plan.smem_bytes));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return e;
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = unsigned(plan.cluster);

@@ -23,11 +23,13 @@
 
 namespace {
 
-// 4096 exchange words (32 KiB) per device.  The grid schedule uses
-// B * max(2 * blocks per cloud, 32 * clusters per cloud) words, and the
-// blocks never exceed the SM count, so this covers any device with up to
-// 2048 SMs.
-constexpr size_t kStaticScratchWords = 4096;
+// 16384 exchange words (128 KiB) per device.  The step-by-step grid
+// schedule uses B * max(2 * blocks per cloud, 32 * clusters per cloud)
+// words, and the blocks never exceed the SM count, so this covers any device
+// with up to 8192 SMs; the rounds take B * 2 * clusters * 4128 bytes (one
+// cloud in up to 15 clusters) and fall back to the step-by-step kernel
+// beyond that.
+constexpr size_t kStaticScratchWords = 16384;
 static __device__ __align__(256) uint64_t g_fps_static_scratch[kStaticScratchWords];
 
 constexpr int kMaxDevices = 64;
@@ -92,6 +94,12 @@ extern "C" int pc_fps_grid_static(const float *xyz, int64_t B, int64_t N,
     if (!plan.ok) {
         std::snprintf(msg, sizeof(msg), "fps_grid_static: %s", plan.why);
         return pcn::api_fail(PC_ERR_UNSUPPORTED, msg);
+    }
+    // the rounds kernel's summaries where they fit, else the step-by-step
+    // kernel's slots
+    if (plan.grid_rounds && plan.workspace_bytes > sizeof(uint64_t) * kStaticScratchWords) {
+        plan.grid_rounds = false;
+        plan.workspace_bytes = plan.step_workspace_bytes;
     }
     if (plan.workspace_bytes > sizeof(uint64_t) * kStaticScratchWords) {
         std::snprintf(msg, sizeof(msg),

@@ -105,6 +105,14 @@ struct FpsPlan {
     int chunk = 0;          // points per block
     size_t smem_bytes = 0;
     size_t workspace_bytes = 0;
+    // two-level GRID: the rounds kernel fits (threads with its resolving
+    // warp, its shared memory); workspace_bytes then covers it, and
+    // step_workspace_bytes is what the step-by-step kernel alone needs
+    bool grid_rounds = false;
+    int rounds_ppt = 0;
+    int rounds_threads = 0;
+    size_t rounds_smem = 0;
+    size_t step_workspace_bytes = 0;
     bool ok = false;
     const char *why = "";
 };

@@ -163,3 +163,61 @@ def test_rounds_every_cluster_size_large(large_fps_oracle, cloud, cs):
     x, want = large_fps_oracle[cloud]
     got = gpu_fps(x, 4096, 0, strategy=pc.PC_FPS_CLUSTER, cluster_size=cs)
     assert_idx_equal(got, want, f"{cloud} on {cs} blocks")
+
+
+# ---------------------------------------------------------------------------
+# The two-level GRID schedule: in rounds, each cluster's leader summarizes
+# its blocks' lists and every block certifies the run from all clusters'
+# summaries; per step, one slot per cluster.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cs,bpc", [(2, 4), (4, 8), (4, 12), (8, 16), (8, 40), (16, 32)])
+def test_grid_two_levels_ties(batched, cs, bpc):
+    """Two clouds of 12,000 points on a 1/32 grid (exact ties between points
+    of different clusters), 900 samples from start 7."""
+    x = inputs.random_cloud(66, 2, 12_000, grid=1 / 32)
+    want = oracle.fps(x, 900, 7, threads=THREADS)
+    got = gpu_fps(x, 900, 7, strategy=pc.PC_FPS_GRID, cluster_size=cs, blocks_per_cloud=bpc)
+    assert_idx_equal(got, want, f"grid ties, {bpc // cs} clusters of {cs}")
+
+
+def test_grid_two_levels_exhausted(batched):
+    """8,192 points at 40 places on 3 clusters of 4: every minimum reaches 0,
+    then the slots repeat index 0."""
+    rng = np.random.default_rng(67)
+    places = rng.random((40, 3)).astype(np.float32)
+    x = places[rng.integers(0, 40, size=(1, 8192))]
+    want = oracle.fps(x, 120, 5, threads=THREADS)
+    got = gpu_fps(x, 120, 5, strategy=pc.PC_FPS_GRID, cluster_size=4, blocks_per_cloud=12)
+    assert_idx_equal(got, want, "grid exhausted")
+
+
+@pytest.mark.parametrize("cloud", ["100k", "90k"])
+@pytest.mark.parametrize("cs,bpc", [(16, 32), (16, 48), (8, 40), (4, 36)])
+def test_grid_rounds_large(large_fps_oracle, cloud, cs, bpc):
+    """The 100k-point cloud and its first 90,000 points, 4096 samples, on
+    two-level grids of 2 to 9 clusters: summaries that overflow their 128
+    places in some rounds must still give every block the same run."""
+    x, want = large_fps_oracle[cloud]
+    got = gpu_fps(x, 4096, 0, strategy=pc.PC_FPS_GRID, cluster_size=cs, blocks_per_cloud=bpc)
+    assert_idx_equal(got, want, f"{cloud} on {bpc // cs} clusters of {cs}")
+
+
+def test_grid_rounds_wait_timeout(batched):
+    """Cluster 0 of the first cloud withholds its first summary (rounds) or
+    its first slot (per step): every bounded wait of that cloud's blocks runs
+    out, its slots after the start are -1, the other cloud is exact, the
+    status word says so, and the next call is correct."""
+    x = inputs.random_cloud(68, 2, 9000)
+    pc.pc_set_wait_timeout_ns(2_000_000)
+    pc.pc_debug_set_stall(pc.PC_STALL_FPS_GRID)
+    try:
+        idx = gpu_fps(x, 30, 0, strategy=pc.PC_FPS_GRID, cluster_size=4, blocks_per_cloud=8)
+    finally:
+        pc.pc_debug_set_stall(0)
+        pc.pc_set_wait_timeout_ns(2_000_000_000)
+    assert pc.pc_device_status(reset=True) == 4
+    assert idx[0, 0] == 0 and (idx[0, 1:] == -1).all()
+    want = oracle.fps(x, 30, 0)
+    assert_idx_equal(idx[1], want[1], "the cloud that did not stall")
+    assert_idx_equal(gpu_fps(x, 30, 0, strategy=pc.PC_FPS_GRID, cluster_size=4,
+                             blocks_per_cloud=8), want, "after the timeout")

@@ -195,3 +195,36 @@ def test_fuzz_fps_cluster_rounds(case):
                     cluster_size=cs).cpu().numpy()
     want = oracle.fps(x, npoint, start, threads=THREADS)
     assert_idx_equal(got, want, f"fuzz fps rounds B={B} N={N} cs={cs} npoint={npoint}")
+
+
+# clusters of each size that fit on the GPU at once (GB300: 7 of 16, 15 of
+# 8); more clusters than fit raise PointCloudError (status 2) and skip
+GRID_CLUSTERS = {2: 9, 4: 9, 8: 7, 16: 3}
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_fuzz_fps_grid_rounds(case):
+    """The two-level GRID schedule in rounds (cluster summaries, one run of
+    centers certified per round) against the oracle on random clouds of
+    8k-400k points: lattice, clustered and spread coordinates with
+    duplicates, clusters of 2 to 16 blocks, 1 to 9 clusters per cloud, at
+    most 9,000 points per block, and sample counts that end runs early or
+    exhaust the cloud."""
+    rng = np.random.default_rng(9200 + case)
+    B = int(rng.integers(1, 3))
+    cs = int(rng.choice([2, 4, 8, 16]))
+    cap = max(1, GRID_CLUSTERS[cs] // B)
+    N = int(rng.integers(8192, min(400_000, cap * cs * 9000)))
+    ncl = int(rng.integers(-(-N // (9000 * cs)), cap + 1))
+    x = cloud(rng, B, N)
+    npoint = int(rng.choice([1, 2, 64, 600, 2048, 4096]))
+    start = int(rng.integers(0, N))
+    what = f"fuzz fps grid rounds B={B} N={N} {ncl}x{cs} npoint={npoint}"
+    try:
+        idx = pc.pc_fps(to_dev(x), npoint, start, strategy=pc.PC_FPS_GRID,
+                        cluster_size=cs, blocks_per_cloud=ncl * cs).cpu().numpy()
+    except pc.PointCloudError as e:       # more clusters than can be resident
+        assert e.status == 2, e
+        pytest.skip(f"{what}: {e}")
+    want = oracle.fps(x, npoint, start, threads=THREADS)
+    assert_idx_equal(idx, want, what)
