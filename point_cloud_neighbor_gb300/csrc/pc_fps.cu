@@ -1161,6 +1161,100 @@ __host__ __device__ constexpr size_t fps_grid_rounds_ws(int64_t B, int ncl) {
     return size_t(B) * 2 * size_t(ncl) * fr_sum_bytes();
 }
 
+// When more than CAP - 1 listed entries lie above bnd (*s_total, 1 + their
+// number, above CAP = FR_SUM): a bound tau > bnd with at most CAP - 1
+// entries above it, as low as two levels of a 64-bin histogram of the keys
+// above bnd find; cnt becomes the lists' counts above tau and *s_total 1 +
+// their sum.  Dropping the smallest keys keeps a run long, where dropping the
+// entries past the first CAP - 1 in list order raises the bound to whatever
+// those hold (1M points on 7 clusters: about 50 centers a round instead of
+// 13 in a CPU simulation of both rules).  Every thread of the block calls it
+// (barriers inside), after fr_count and a barrier; every block computes the
+// same bound from the same lists.  hist: 128 ints of shared memory.
+__device__ unsigned fr_cap_bound(const unsigned char *lists, int nl, int per, int nscan,
+                                 unsigned msg, unsigned bnd, const uint4 *wfirst, int *cnt,
+                                 int *hist, int *s_total, unsigned *s_tau, const int *lens) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int CAP = FR_SUM;
+    unsigned kmax = lane < nscan ? wfirst[lane].x : 0u;  // the largest key
+    kmax = __reduce_max_sync(FULL, kmax);
+    const unsigned lo = bnd + 1u;
+    const unsigned span = kmax - bnd;  // >= 1: some entry is above bnd
+    const int s1 = max(0, 32 - __clz(int(span - 1u)) - 6);  // 64 bins of 2^s1 keys
+    const int s2 = max(0, s1 - 6);                           // bin b - 1 in 64 parts
+    for (int i = int(threadIdx.x); i < 128; i += int(blockDim.x)) hist[i] = 0;
+    __syncthreads();
+    auto key_at = [&](int l, int k) {
+        return *reinterpret_cast<const unsigned *>(lists + size_t(l) * msg + size_t(k) * 32);
+    };
+    for (int l = warp; l < nl; l += nscan) {
+        const int len = lens ? lens[l] : per;
+        for (int k = lane; k < len; k += 32) {
+            const unsigned h = key_at(l, k);
+            if (h > bnd) atomicAdd(&hist[(h - lo) >> s1], 1);
+        }
+    }
+    __syncthreads();
+    // the entries at or above each bin (lane: bins 2 lane, 2 lane + 1), the
+    // first bin with at most CAP - 1 of them, and that count
+    auto first_fit = [&](const int *hg, int extra, int &b, int &cb) {
+        const int h0 = hg[2 * lane], h1 = hg[2 * lane + 1];
+        int suf = h0 + h1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_down_sync(FULL, suf, o);
+            if (lane + o < 32) suf += v;
+        }
+        const int c0 = suf + extra, c1 = suf - h0 + extra;
+        const unsigned m0 = __ballot_sync(FULL, c0 <= CAP - 1);
+        const unsigned m1 = __ballot_sync(FULL, c1 <= CAP - 1);
+        b = 64;
+        if (m0) b = 2 * (__ffs(m0) - 1);
+        if (m1) b = min(b, 2 * (__ffs(m1) - 1) + 1);
+        const int v0 = __shfl_sync(FULL, c0, (b >> 1) & 31);
+        const int v1 = __shfl_sync(FULL, c1, (b >> 1) & 31);
+        cb = b == 64 ? extra : ((b & 1) ? v1 : v0);
+    };
+    int b, cb;
+    first_fit(hist, 0, b, cb);  // b >= 1: bin 0 holds the first too many
+    const unsigned base2 = unsigned(b - 1) << s1;
+    for (int l = warp; l < nl; l += nscan) {
+        const int len = lens ? lens[l] : per;
+        for (int k = lane; k < len; k += 32) {
+            const unsigned h = key_at(l, k);
+            if (h > bnd && ((h - lo) >> s1) == unsigned(b - 1))
+                atomicAdd(&hist[64 + (((h - lo) - base2) >> s2)], 1);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int c, cc;
+        first_fit(hist + 64, cb, c, cc);
+        // every key below lo + base2 + (c << s2) is dropped
+        const unsigned long long t =
+            (unsigned long long)lo + base2 + ((unsigned long long)c << s2) - 1ull;
+        if (lane == 0) *s_tau = unsigned(min(t, (unsigned long long)kmax));
+    }
+    __syncthreads();
+    const unsigned tau = *s_tau;
+    for (int l = warp; l < nl; l += nscan) {
+        const int len = lens ? lens[l] : per;
+        int n = 0;
+        for (int k0 = 0; k0 < len; k0 += 32) {
+            const int k = k0 + lane;
+            n += __popc(__ballot_sync(FULL, k < len && key_at(l, k) > tau));
+        }
+        if (lane == 0) cnt[l] = n;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int total = 1 + fr_before(cnt, nl);
+        if (lane == 0) *s_total = total;
+    }
+    __syncthreads();
+    return tau;
+}
+
 template <int PPT>
 __global__ void __launch_bounds__(fgr_max_threads(PPT), 1)
     fps_grid_rounds_kernel(const FpsArgs a) {
@@ -1189,6 +1283,7 @@ __global__ void __launch_bounds__(fgr_max_threads(PPT), 1)
     volatile int *s_pub = s_nc + 4;
     volatile int *s_fin = s_nc + 5;
     int *s_first = s_nc + 6;  // leader: the offset of its cluster's largest entry
+    unsigned *s_tau = reinterpret_cast<unsigned *>(s_nc + 7);
 
     // every distributed-shared-memory address below targets rank 0 of a
     // cluster of a.cs blocks; a launch without that shape stops here
@@ -1298,10 +1393,9 @@ __global__ void __launch_bounds__(fgr_max_threads(PPT), 1)
             if (!got && lane == 0) *s_fail = 1;
             __syncthreads();
             if (!*s_fail) {
-                const unsigned bc =
+                unsigned bc =
                     fr_count(recv, a.cs, W * FR_CW, W, NW, msg, lcnt, wfirst + warp);
                 __syncthreads();
-                fr_place(recv, a.cs, W * FR_CW, NW, msg, bc, lcnt, cidx, s_over);
                 if (warp == 0) {  // the cluster's largest entry and the candidates' count
                     const uint4 f = lane < NW ? wfirst[lane] : make_uint4(0u, FULL, 0u, 0u);
                     unsigned fh, fj;
@@ -1314,6 +1408,12 @@ __global__ void __launch_bounds__(fgr_max_threads(PPT), 1)
                         *s_total = total;
                     }
                 }
+                __syncthreads();
+                // more candidates than a summary holds: drop the smallest
+                if (*s_total > FR_SUM)
+                    bc = fr_cap_bound(recv, a.cs, W * FR_CW, NW, msg, bc, wfirst, lcnt, cidx,
+                                      s_total, s_tau, nullptr);
+                fr_place(recv, a.cs, W * FR_CW, NW, msg, bc, lcnt, cidx, s_over);
                 __syncthreads();
                 unsigned char *sl = slot(par, cl);
                 const int first = *s_first;
@@ -1380,14 +1480,19 @@ __global__ void __launch_bounds__(fgr_max_threads(PPT), 1)
         __syncthreads();
         if (!*s_fail) {
             // 4. the cloud's candidates and the run, as in fps_rounds_kernel
-            const unsigned bnd =
+            unsigned bnd =
                 fr_count(gsum, a.ncl, FR_SUM, 1, NW, smsg, lcnt, wfirst + warp, glen);
             __syncthreads();
-            fr_place(gsum, a.ncl, FR_SUM, NW, smsg, bnd, lcnt, cidx, s_over, glen);
             if (warp == 0) {
                 const int total = 1 + fr_before(lcnt, a.ncl);
                 if (lane == 0) *s_total = total;
             }
+            __syncthreads();
+            // more candidates than the resolving warp holds: drop the smallest
+            if (*s_total > FR_SUM)
+                bnd = fr_cap_bound(gsum, a.ncl, FR_SUM, NW, smsg, bnd, wfirst, lcnt, cidx,
+                                   s_total, s_tau, glen);
+            fr_place(gsum, a.ncl, FR_SUM, NW, smsg, bnd, lcnt, cidx, s_over, glen);
             __syncthreads();
             if (rw) {
                 fr_pick(gsum, NW, bnd, min(FR_RMAX, a.npoint - t), cidx, wfirst, *s_total,
