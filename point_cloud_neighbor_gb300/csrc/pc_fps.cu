@@ -1874,17 +1874,26 @@ FpsPlan plan_fps_uncached(const DeviceInfo &dev, int64_t B, int64_t N, int strat
         // then one slot per cluster in the workspace) unless cluster_size is
         // 1: the cluster size that keeps the most blocks resident
         if (cluster_size != 1) {
-            // the largest cluster that fits: fewest slots and leaders in the
-            // global exchange (GB300, 1M points: 2.0 us per step with 7
-            // clusters of 16, 2.7 with 15 of 8, 6.9 with 36 of 4, when every
-            // block polled every slot)
-            FpsPlan best;
+            // one center per exchange: the largest cluster that fits, fewest
+            // slots and leaders in the global exchange (GB300, 1M points: 2.0
+            // us per step with 7 clusters of 16, 2.7 with 15 of 8, 6.9 with
+            // 36 of 4, when every block polled every slot).  In rounds the
+            // exchange is paid once a run and the point work per center
+            // counts more: the size whose rounds plan holds the most blocks
+            // (1M points, 16,384 samples: 9.3 ms on 15 clusters of 8, 10.5
+            // on 7 of 16)
+            FpsPlan best, first;
             const int sizes[3] = {16, 8, 4};
             for (int cs : sizes) {
                 if (cluster_size > 1 && cs != cluster_size) continue;
-                best = plan_cgrid(dev, B, N, cs, blocks_per_cloud);
-                if (best.ok) break;
+                const FpsPlan c = plan_cgrid(dev, B, N, cs, blocks_per_cloud);
+                if (!c.ok) continue;
+                if (!first.ok) first = c;
+                if (c.grid_rounds &&
+                    (!best.ok || c.blocks_per_cloud > best.blocks_per_cloud))
+                    best = c;
             }
+            if (!best.ok) best = first;
             if (cluster_size > 1 && !best.ok && cluster_size != 16 &&
                 cluster_size != 8 && cluster_size != 4)
                 best = plan_cgrid(dev, B, N, cluster_size, blocks_per_cloud);
