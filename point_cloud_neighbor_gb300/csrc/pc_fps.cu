@@ -519,11 +519,10 @@ __device__ __forceinline__ void fr_pick(const unsigned char *lists, int nscan, u
         const float cy = __shfl_sync(FULL, rab ? yb : ya, wl);
         const float cz = __shfl_sync(FULL, rab ? zb : za, wl);
         const unsigned cj = __shfl_sync(FULL, bj, wl);
-        if (lane == 0) {  // the center, then its publication
-            cen[k] = make_float4(cx, cy, cz, 0.f);
+        if (lane == 0) {  // the center (its index in .w), then its publication
+            cen[k] = make_float4(cx, cy, cz, __uint_as_float(cj));
             __threadfence_block();
             *s_pub = k + 1;
-            if (out) out[k] = int64_t(cj);
         }
         // lower the candidates' m by the new center, as the step would (a
         // NaN distance leaves m, as fminf does)
@@ -538,6 +537,12 @@ __device__ __forceinline__ void fr_pick(const unsigned char *lists, int nscan, u
         *s_nc = k;
         __threadfence_block();
         *s_fin = 1;
+    }
+    // the run's indices, after the run: a global store inside the loop would
+    // hold up the next center's fence until it completed
+    if (out) {
+        __syncwarp();
+        for (int i = lane; i < k; i += 32) out[i] = int64_t(__float_as_uint(cen[i].w));
     }
 }
 
@@ -747,24 +752,30 @@ __global__ void __launch_bounds__(fr_max_threads(PPT), 1)
         } else {
             // apply the run's centers as the resolving warp publishes them
             // (bounded wait: the run is short, the limit is a safety net)
+            // (a warp that finds nothing new sleeps briefly instead of polling:
+            // its loads and fences would slow the resolving warp's shuffles)
             int c = 0;
             const uint64_t w0 = global_timer_ns();
             for (int spin = 0;; ++spin) {
                 const int fin = *s_fin;
-                __threadfence_block();
                 const int pub = *s_pub;
-                __threadfence_block();
-                while (c < pub) {  // two at a time where two are out
-                    if (c + 1 < pub) {
-                        apply2(cen[c], cen[c + 1]);
-                        c += 2;
-                    } else {
-                        apply(cen[c]);
-                        ++c;
+                if (pub > c || fin) {
+                    __threadfence_block();  // the centers published before pub / fin
+                    const int upto = fin ? *s_pub : pub;
+                    while (c < upto) {  // two at a time where two are out
+                        if (c + 1 < upto) {
+                            apply2(cen[c], cen[c + 1]);
+                            c += 2;
+                        } else {
+                            apply(cen[c]);
+                            ++c;
+                        }
                     }
+                    if (fin) break;
+                    continue;
                 }
-                if (fin) break;
-                if ((spin & 255) == 255 && global_timer_ns() - w0 > a.timeout_ns) {
+                __nanosleep(32);
+                if ((spin & 63) == 63 && global_timer_ns() - w0 > a.timeout_ns) {
                     if (lane == 0) *s_fail = 1;
                     break;
                 }
@@ -1498,24 +1509,30 @@ __global__ void __launch_bounds__(fgr_max_threads(PPT), 1)
                 fr_pick(gsum, NW, bnd, min(FR_RMAX, a.npoint - t), cidx, wfirst, *s_total,
                         *s_over, cen, s_nc, s_pub, s_fin, r == 0 ? out + t : nullptr);
             } else {
+                // (a warp that finds nothing new sleeps briefly instead of polling:
+                // its loads and fences would slow the resolving warp's shuffles)
                 int c = 0;
                 const uint64_t w0 = global_timer_ns();
                 for (int spin = 0;; ++spin) {
                     const int fin = *s_fin;
-                    __threadfence_block();
                     const int pub = *s_pub;
-                    __threadfence_block();
-                    while (c < pub) {  // two at a time where two are out
-                        if (c + 1 < pub) {
-                            apply2(cen[c], cen[c + 1]);
-                            c += 2;
-                        } else {
-                            apply(cen[c]);
-                            ++c;
+                    if (pub > c || fin) {
+                        __threadfence_block();  // the centers published before pub / fin
+                        const int upto = fin ? *s_pub : pub;
+                        while (c < upto) {  // two at a time where two are out
+                            if (c + 1 < upto) {
+                                apply2(cen[c], cen[c + 1]);
+                                c += 2;
+                            } else {
+                                apply(cen[c]);
+                                ++c;
+                            }
                         }
+                        if (fin) break;
+                        continue;
                     }
-                    if (fin) break;
-                    if ((spin & 255) == 255 && global_timer_ns() - w0 > a.timeout_ns) {
+                    __nanosleep(32);
+                    if ((spin & 63) == 63 && global_timer_ns() - w0 > a.timeout_ns) {
                         if (lane == 0) *s_fail = 1;
                         break;
                     }
