@@ -225,6 +225,8 @@ def recorded_traffic(op: str):
         return None
     want = kernel_source_hash(op)
     for line in open(path):
+        if line.startswith("#"):  # the header: the capture command
+            continue
         kv = dict(p.split("=", 1) for p in line.split() if "=" in p)
         if kv.get("op") == op and kv.get("src_sha256") == want:
             try:
@@ -374,6 +376,12 @@ def run_gpu(args):
                 5, 3, flush, stream)
         finally:
             pc.pc_set_sm_reserve(0)
+        # and on every SM (each kernel's own fraction of the GPU)
+        per["knn_all_sms"] = _timed(
+            lambda: pc.pc_knn(x, x, k, out_dist=knn_d, out_idx=knn_i), 5, 3, flush, stream)
+        per["ball_query_all_sms"] = _timed(
+            lambda: pc.pc_ball_query(x, x, r, K, out_dist2=bq_d, out_idx=bq_i),
+            5, 3, flush, stream)
     else:
         per = {"fps": fps_ms / args.steps, "knn": knn_ms / args.steps,
                "ball_query": bq_ms / args.steps}
@@ -398,8 +406,12 @@ def run_gpu(args):
         },
     }
     if fused:
-        for op in ("knn", "ball_query"):
+        for op, pairs in (("knn", knn_pairs), ("ball_query", bq_pairs)):
             ops[op]["timed"] = "alone on the SMs FPS leaves, outside the timed step"
+            ops[op]["sms_used"] = sm_count - reserve
+            ops[op]["ms_all_sms"] = per[op + "_all_sms"]
+            ops[op]["achieved_tflops_all_sms"] = (
+                pairs * FLOPS_PER_PAIR / (per[op + "_all_sms"] / 1e3) / 1e12)
         t_fused = per["knn_ball_query"] / 1e3
         ops["knn_ball_query"] = {
             "queries_per_s": 2 * N * world / t_fused,
@@ -463,6 +475,11 @@ def run_gpu(args):
                  "frac": ops[op]["achieved_tflops"] / alu_peak}
             if "alu_frac_pairs_once" in ops[op]:
                 r["frac_pairs_once"] = ops[op]["alu_frac_pairs_once"]
+            if "sms_used" in ops[op]:
+                # against the peak of the SMs it ran on, and alone on all SMs
+                r["frac_of_sms_used"] = (ops[op]["achieved_tflops"] /
+                                         (alu_peak * ops[op]["sms_used"] / sm_count))
+                r["frac_all_sms"] = ops[op]["achieved_tflops_all_sms"] / alu_peak
         r["traffic"] = recorded_traffic(op)
         r["kernel"] = op
         r["peak_source"] = (f"FP32 CUDA cores: {sm_count} SMs x 128 x 2 flop x "
