@@ -75,3 +75,39 @@ def test_knn_d_limits():
     assert e.value.status == 2
     with pytest.raises(pc.PointCloudError):
         pc.pc_knn_d(x, x, 51)
+
+
+@pytest.mark.parametrize("offset", [1e3, 1e5])
+@pytest.mark.parametrize("D", [16, 64, 128])
+def test_knn_d_translated_features(offset, D):
+    """Features far from the origin (each squared difference rounds at a
+    larger exponent): every row the oracle's."""
+    x = (feats(40 + D, 2, 700, D).astype(np.float64) + offset).astype(np.float32)
+    q = (feats(50 + D, 2, 130, D).astype(np.float64) + offset).astype(np.float32)
+    check(q, x, 20, what=f"knn_d +{offset:g} D={D}")
+
+
+def test_knn_d_zero_dimension_changes_nothing():
+    """One more dimension that is zero in every row adds +0 to every s: the
+    same indices and bit-identical distances."""
+    x = feats(60, 2, 900, 128)
+    q = feats(61, 2, 200, 128)
+    d1, i1 = pc.pc_knn_d(to_dev(q), to_dev(x), 24)
+    pad = lambda a: np.concatenate([a, np.zeros(a.shape[:2] + (1,), np.float32)], axis=2)
+    d2, i2 = pc.pc_knn_d(to_dev(pad(q)), to_dev(pad(x)), 24)
+    assert torch.equal(i1, i2)
+    assert torch.equal(d1.view(torch.int32), d2.view(torch.int32))
+
+
+def test_knn_d_huge_and_infinite_features():
+    """Coordinates near the float range (squares up to ~1e32) and an
+    infinite one: the exact s decides as in the oracle (the contract covers
+    finite inputs; an infinite s sorts last, ties by index)."""
+    x = feats(70, 1, 600, 32)
+    q = feats(71, 1, 100, 32)
+    x[0, 17, :] = 3e15
+    x[0, 40, 0] = np.inf
+    x[0, 41, :] = -2e15
+    q[0, 9, :] = 2e15
+    q[0, 10, :5] = 1e16
+    check(q, x, 16, what="knn_d huge and infinite")
