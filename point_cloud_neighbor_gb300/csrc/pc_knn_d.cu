@@ -8,7 +8,10 @@
 // (for D = 3 this is the s32 of the point operators); the k smallest (s, j)
 // in lexicographic order, D = sqrt(s) or s (PC_KNN_SQUARED).
 //
-// Design (one launch; k <= 32, D <= 256):
+// Two kernels, one launch: D <= 64 knn_d_packed_kernel (below: the query
+// row in registers, two references per packed instruction), else this one.
+//
+// knn_d_kernel (k <= 32, D <= 256):
 //  * A block owns KD_QT = 64 queries of one cloud and has KD_PH = 4 phases of
 //    64 threads: thread (phase p, query q) examines the references whose
 //    position in each tile of KD_RT = 32 falls in [8p, 8p + 8).  Query rows
@@ -56,6 +59,7 @@ struct KnnDArgs {
     int squared;
     float *out_dist;
     int64_t *out_idx;
+    float negzero;  // -0.0f, supplied at run time (see sq2_rn)
 };
 
 __device__ __forceinline__ bool kd_after(float as, int aj, float bs, int bj) {
@@ -192,6 +196,121 @@ __global__ void __launch_bounds__(KD_THREADS) knn_d_kernel(const KnnDArgs a) {
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// knn_d_packed_kernel<DM> (D <= DM = 64): the same arithmetic, two references
+// per packed f32x2 instruction.  The thread's query row lives in registers,
+// negated (x + (-q) is -(q - x) under round-to-nearest-even and the square
+// removes the sign); the tile is stored dimension-major, so the thread's 8
+// references of a dimension are two 128-bit broadcasts; per dimension and
+// pair of references one packed add, one packed square (fma with a -0
+// addend supplied at run time, see sq2_rn) and one packed accumulation, in
+// increasing d -- each half the exact kernel's s bit for bit.  (The packed exact kernel with query rows in
+// shared memory was bound by their per-lane loads.)
+constexpr int KP_DM = 64;
+constexpr int KP_STRIDE = KD_RT + 4;  // floats between dimensions of the tile
+
+__host__ __device__ constexpr size_t kp_smem(int k) {
+    return size_t(KP_DM) * KP_STRIDE * sizeof(float) + size_t(KD_THREADS) * k * 8;
+}
+
+template <int DM>
+__global__ void __launch_bounds__(KD_THREADS) knn_d_packed_kernel(const KnnDArgs a) {
+    extern __shared__ __align__(16) float kp_smem_f[];
+    const int D = a.D, k = a.k;
+    float *xt = kp_smem_f;                   // [DM][KP_STRIDE]
+    float *hs_all = xt + DM * KP_STRIDE;     // [k][KD_THREADS]
+    int *hj_all = reinterpret_cast<int *>(hs_all + size_t(k) * KD_THREADS);
+    const int b = blockIdx.y;
+    const int q0 = blockIdx.x * KD_QT;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ql = tid % KD_QT, phase = tid / KD_QT;
+    const float inf = __int_as_float(0x7f800000);
+    const float2 nz = make_float2(a.negzero, a.negzero);
+
+    const int nq = min(KD_QT, a.Q - q0);
+    const bool qvalid = ql < nq;
+    const float *qg = a.query + (size_t(b) * a.Q + q0 + (qvalid ? ql : 0)) * D;
+    float nqr[DM];
+#pragma unroll
+    for (int d = 0; d < DM; ++d) nqr[d] = (qvalid && d < D) ? -qg[d] : 0.0f;
+    float *hs = hs_all + tid;
+    int *hj = hj_all + tid;
+    for (int e = 0; e < k; ++e) {
+        hs[e * KD_THREADS] = inf;
+        hj[e * KD_THREADS] = INT_MAX;
+    }
+    float ts = inf;
+    int tj = INT_MAX;
+    const float *xg = a.ref + size_t(b) * a.N * D;
+    const int r0 = phase * 8;  // the thread's 8 references of each tile
+
+    for (int j0 = 0; j0 < a.N; j0 += KD_RT) {
+        __syncthreads();  // the previous tile is no longer read
+        const int nr = min(KD_RT, a.N - j0);
+        // reference r, dimension d at xt[d * KP_STRIDE + r] (a warp per row)
+        for (int r = warp; r < KD_RT; r += KD_THREADS / 32)
+            for (int d = lane; d < D; d += 32)
+                xt[d * KP_STRIDE + r] = r < nr ? xg[size_t(j0 + r) * D + d] : 0.0f;
+        __syncthreads();
+        float2 s0 = make_float2(0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
+#pragma unroll
+        for (int d = 0; d < DM; ++d) {
+            if (d >= D) break;
+            const float4 xa = *reinterpret_cast<const float4 *>(xt + d * KP_STRIDE + r0);
+            const float4 xb = *reinterpret_cast<const float4 *>(xt + d * KP_STRIDE + r0 + 4);
+            const float2 nqd = make_float2(nqr[d], nqr[d]);
+            float2 t = __fadd2_rn(make_float2(xa.x, xa.y), nqd);
+            s0 = __fadd2_rn(s0, __ffma2_rn(t, t, nz));
+            t = __fadd2_rn(make_float2(xa.z, xa.w), nqd);
+            s1 = __fadd2_rn(s1, __ffma2_rn(t, t, nz));
+            t = __fadd2_rn(make_float2(xb.x, xb.y), nqd);
+            s2 = __fadd2_rn(s2, __ffma2_rn(t, t, nz));
+            t = __fadd2_rn(make_float2(xb.z, xb.w), nqd);
+            s3 = __fadd2_rn(s3, __ffma2_rn(t, t, nz));
+        }
+        const float sv[8] = {s0.x, s0.y, s1.x, s1.y, s2.x, s2.y, s3.x, s3.y};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + r0 + u;
+            if (r0 + u < nr && kd_after(ts, tj, sv[u], j)) {
+                kd_sift(hs, hj, k, KD_THREADS, 0, sv[u], j);
+                ts = hs[0];
+                tj = hj[0];
+            }
+        }
+    }
+    __syncthreads();
+    if (phase != 0 || !qvalid) return;
+    // merge the other phases' heaps of this query into this one
+    for (int p = 1; p < KD_PH; ++p) {
+        const int other = p * KD_QT + ql;
+        for (int e = 0; e < k; ++e) {
+            const float sx = hs_all[e * KD_THREADS + other];
+            const int jx = hj_all[e * KD_THREADS + other];
+            if (kd_after(ts, tj, sx, jx)) {
+                kd_sift(hs, hj, k, KD_THREADS, 0, sx, jx);
+                ts = hs[0];
+                tj = hj[0];
+            }
+        }
+    }
+    for (int n = k - 1; n > 0; --n) {  // heap sort into ascending order
+        const float sx = hs[n * KD_THREADS];
+        const int jx = hj[n * KD_THREADS];
+        hs[n * KD_THREADS] = hs[0];
+        hj[n * KD_THREADS] = hj[0];
+        kd_sift(hs, hj, n, KD_THREADS, 0, sx, jx);
+    }
+    const size_t row = size_t(b) * a.Q + q0 + ql;
+    for (int e = 0; e < k; ++e) {
+        const float sx = hs[e * KD_THREADS];
+        a.out_idx[row * k + e] = hj[e * KD_THREADS];
+        a.out_dist[row * k + e] = a.squared ? sx : __fsqrt_rn(sx);
+    }
+}
+
 }  // namespace
 }  // namespace pcn
 
@@ -235,14 +354,23 @@ extern "C" int pc_knn_d(const float *query, int64_t B, int64_t Q,
     a.squared = (flags & PC_KNN_SQUARED) != 0;
     a.out_dist = out_dist;
     a.out_idx = out_idx;
-    const size_t smem = pcn::kd_smem(int(D), int(k));
-    cudaError_t e = cudaFuncSetAttribute(pcn::knn_d_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(smem));
+    a.negzero = -0.0f;
+    // D <= 64: the packed kernel with the query row in registers
+    const bool packed = D <= pcn::KP_DM;
+    const size_t smem = packed ? pcn::kp_smem(int(k)) : pcn::kd_smem(int(D), int(k));
+    const void *fn = packed
+                         ? reinterpret_cast<const void *>(&pcn::knn_d_packed_kernel<pcn::KP_DM>)
+                         : reinterpret_cast<const void *>(&pcn::knn_d_kernel);
+    cudaError_t e =
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e == cudaSuccess) {
         const dim3 grid(unsigned((Q + pcn::KD_QT - 1) / pcn::KD_QT), unsigned(B));
-        pcn::knn_d_kernel<<<grid, pcn::KD_THREADS, smem,
-                            static_cast<cudaStream_t>(stream)>>>(a);
+        if (packed)
+            pcn::knn_d_packed_kernel<pcn::KP_DM><<<grid, pcn::KD_THREADS, smem,
+                                                  static_cast<cudaStream_t>(stream)>>>(a);
+        else
+            pcn::knn_d_kernel<<<grid, pcn::KD_THREADS, smem,
+                                static_cast<cudaStream_t>(stream)>>>(a);
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) {
