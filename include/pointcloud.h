@@ -57,7 +57,7 @@ extern "C" {
 typedef enum pc_status {
     PC_OK = 0,
     PC_ERR_INVALID_ARGUMENT = 1, /* a size, pointer or parameter is invalid  */
-    PC_ERR_UNSUPPORTED = 2,      /* valid, but beyond what this build runs   */
+    PC_ERR_UNSUPPORTED = 2,      /* valid, but beyond what the library runs  */
     PC_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed     */
     PC_ERR_DEVICE_TIMEOUT = 4,   /* a bounded device-side wait ran out       */
     PC_ERR_NO_DEVICE = 5         /* no usable sm_103 device is current       */
